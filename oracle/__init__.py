@@ -1,0 +1,219 @@
+"""fp64 CPU oracle for the Mamba2 SSD / exact-replay hot path.
+
+TEST INFRASTRUCTURE ONLY: imported by the test suite, by the package smoke
+check and by the bench's CPU-baseline leg, never by the product path.  It
+shares no code with the CUDA library (only the seeded input generator in
+``synth`` serves both).
+
+Everything here reduces to the plain token-by-token recurrence in
+``oracle.c`` (see its header):
+
+    delta_t = softplus(dt_t + dt_bias),  S_t = exp(delta_t A) S_{t-1} + delta_t x_t B_t^T,
+    y_t = S_t C_t + D x_t
+
+The protocol models below (prefill, exact-replay decode, ReplaySSM verify and
+commit) only decide WHICH tokens the recurrence runs over and from WHICH
+starting state, following the exact-replay RFC (vLLM issue 55524, section 3
+"Proposal") and the ReplaySSM reproduction notes ("Motivation and method",
+"Core equations").
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+from typing import List, Optional, Sequence, Tuple
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "oracle.c")
+_LIB_PATH = os.path.join(_HERE, "_oracle.so")
+# The mutation test points this at a deliberately broken build of oracle.c.
+_LIB_OVERRIDE = os.environ.get("ERS_ORACLE_LIB")
+_lib = None
+_lock = threading.Lock()
+
+
+def build(force: bool = False) -> str:
+    """Compile oracle.c into a shared library next to it (gcc, -O2, no fast-math)."""
+    if force or not os.path.exists(_LIB_PATH) or os.path.getmtime(_LIB_PATH) < os.path.getmtime(_SRC):
+        tmp = _LIB_PATH + f".tmp{os.getpid()}"
+        subprocess.check_call(["gcc", "-O2", "-fno-fast-math", "-ffp-contract=off", "-fPIC", "-shared",
+                               "-o", tmp, _SRC, "-lm", "-lpthread"])
+        os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            if _LIB_OVERRIDE:
+                lib = ctypes.CDLL(_LIB_OVERRIDE)
+            else:
+                build()
+                lib = ctypes.CDLL(_LIB_PATH)
+            dp = ctypes.POINTER(ctypes.c_double)
+            lib.oracle_ssm_recurrence.argtypes = [ctypes.c_int] * 5 + [ctypes.POINTER(ctypes.c_int64)] + \
+                [dp] * 9 + [ctypes.c_int]
+            lib.oracle_ssm_recurrence.restype = ctypes.c_int
+            lib.oracle_softplus.argtypes = [ctypes.c_double]
+            lib.oracle_softplus.restype = ctypes.c_double
+            _lib = lib
+    return _lib
+
+
+def default_threads() -> int:
+    try:
+        return max(1, len(os.sched_getaffinity(0)))
+    except AttributeError:  # pragma: no cover
+        return max(1, os.cpu_count() or 1)
+
+
+def _f64(a) -> np.ndarray:
+    return np.ascontiguousarray(a, dtype=np.float64)
+
+
+def _ptr(a: np.ndarray):
+    return a.ctypes.data_as(ctypes.POINTER(ctypes.c_double))
+
+
+def softplus(z: float) -> float:
+    """fp64 softplus as the oracle recurrence evaluates it."""
+    return float(_load().oracle_softplus(float(z)))
+
+
+def recurrence(x, dt, A, B, C, D, dt_bias, cu_seqlens=None, init_state=None,
+               nthreads: Optional[int] = None) -> Tuple[np.ndarray, np.ndarray]:
+    """Run the recurrence over packed sequences.
+
+    x [T,H,P], dt [T,H] (raw), A/D/dt_bias [H], B/C [T,G,N]; cu_seqlens [S+1]
+    (default: one sequence of all T tokens); init_state [S,H,P,N] or None (zero).
+    Returns (y [T,H,P], final_state [S,H,P,N]) in fp64.
+    """
+    x, dt, A, B, C, D, dt_bias = map(_f64, (x, dt, A, B, C, D, dt_bias))
+    T, H, P = x.shape
+    G, N = B.shape[1], B.shape[2]
+    if cu_seqlens is None:
+        cu_seqlens = np.array([0, T], dtype=np.int64)
+    cu = np.ascontiguousarray(cu_seqlens, dtype=np.int64)
+    S = cu.shape[0] - 1
+    if cu[0] != 0 or cu[-1] != T or np.any(np.diff(cu) < 0):
+        raise ValueError("bad cu_seqlens")
+    state = np.zeros((S, H, P, N)) if init_state is None else np.array(init_state, dtype=np.float64, copy=True)
+    if state.shape != (S, H, P, N):
+        raise ValueError("init_state shape")
+    state = np.ascontiguousarray(state)
+    y = np.zeros((T, H, P))
+    rc = _load().oracle_ssm_recurrence(
+        S, H, G, P, N, cu.ctypes.data_as(ctypes.POINTER(ctypes.c_int64)), _ptr(x), _ptr(dt), _ptr(A),
+        _ptr(B), _ptr(C), _ptr(D), _ptr(dt_bias), _ptr(state), _ptr(y),
+        int(nthreads if nthreads is not None else default_threads()))
+    if rc != 0:
+        raise RuntimeError(f"oracle_ssm_recurrence failed ({rc})")
+    return y, state
+
+
+def bf16_round(a: np.ndarray) -> np.ndarray:
+    """Round to bf16 (round-to-nearest-even), through fp32 as the GPU anchor is
+    stored in fp32.  Returned as fp64 values."""
+    f = np.ascontiguousarray(a, dtype=np.float32)
+    u = f.view(np.uint32).astype(np.uint64)
+    r = (((u + 0x7FFF + ((u >> 16) & 1)) >> 16) << 16).astype(np.uint32)
+    return r.view(np.float32).astype(np.float64)
+
+
+class _Seq:
+    __slots__ = ("x", "dt", "B", "C")
+
+    def __init__(self, x, dt, B, C):
+        self.x, self.dt, self.B, self.C = x, dt, B, C
+
+
+def _pack(parts: Sequence[Tuple[np.ndarray, np.ndarray, np.ndarray, np.ndarray]]):
+    lens = [p[0].shape[0] for p in parts]
+    cu = np.zeros(len(parts) + 1, dtype=np.int64)
+    cu[1:] = np.cumsum(lens)
+    cat = [np.concatenate([p[i] for p in parts]) for i in range(4)]
+    return cat, cu
+
+
+class ReplaySSMModel:
+    """ReplaySSM-style speculative decoding with a dual-precision anchor.
+
+    Per sequence: an fp64 recurrence anchor, a bf16 read copy cast from it,
+    and the committed input records since the last refresh (h of them).
+    ``verify`` flushes when h + T > L (refresh the committed records into the
+    anchor and recast the read copy), then returns the T draft outputs computed
+    from the READ COPY over committed records + drafts 1..s.  ``commit`` appends
+    the first ``accepted`` drafts to the committed records; rejected drafts
+    never enter the recurrence.  (ReplaySSM reproduction notes, "Motivation and
+    method" and "Core equations": outputs read the low-precision copy, refresh
+    forms S from committed raw records and casts both copies from it.)
+    """
+
+    def __init__(self, params, anchor: np.ndarray, L: int, nthreads: Optional[int] = None, read_cast=None):
+        self.A, self.D, self.dt_bias = (_f64(params.A), _f64(params.D), _f64(params.dt_bias))
+        self.anchor = np.array(anchor, dtype=np.float64, copy=True)  # [S,H,P,N]
+        self.read_cast = read_cast if read_cast is not None else bf16_round
+        self.read = self.read_cast(self.anchor)
+        self.L = L
+        self.nthreads = nthreads
+        S = anchor.shape[0]
+        self.committed: List[List[Tuple[np.ndarray, ...]]] = [[] for _ in range(S)]
+        self.flushes = 0
+
+    def h(self) -> np.ndarray:
+        return np.array([len(c) for c in self.committed], dtype=np.int32)
+
+    def _records(self, i):
+        c = self.committed[i]
+        if not c:
+            return None
+        return tuple(np.stack([r[k] for r in c]) for k in range(4))
+
+    def refresh(self, which: Sequence[int]):
+        """Fold the committed records of the listed sequences into their anchors."""
+        which = [i for i in which if self.committed[i]]
+        if not which:
+            return
+        parts = [self._records(i) for i in which]
+        (x, dt, B, C), cu = _pack(parts)
+        _, fin = recurrence(x, dt, self.A, B, C, self.D, self.dt_bias, cu, self.anchor[which], self.nthreads)
+        for k, i in enumerate(which):
+            self.anchor[i] = fin[k]
+            self.read[i] = self.read_cast(fin[k])
+            self.committed[i] = []
+        self.flushes += len(which)
+
+    def verify(self, drafts: Sequence[Tuple[np.ndarray, np.ndarray, np.ndarray, np.ndarray]]) -> np.ndarray:
+        """drafts[i] = (x [T,H,P], dt [T,H], B [T,G,N], C [T,G,N]).  Returns y [S,T,H,P]."""
+        S = len(drafts)
+        T = drafts[0][0].shape[0]
+        flush = [i for i in range(S) if len(self.committed[i]) + T > self.L]
+        self.refresh(flush)
+        parts = []
+        for i in range(S):
+            rec = self._records(i)
+            if rec is None:
+                parts.append(drafts[i])
+            else:
+                parts.append(tuple(np.concatenate([rec[k], drafts[i][k]]) for k in range(4)))
+        (x, dt, B, C), cu = _pack(parts)
+        y, _ = recurrence(x, dt, self.A, B, C, self.D, self.dt_bias, cu, self.read, self.nthreads)
+        H, P = x.shape[1], x.shape[2]
+        out = np.zeros((S, T, H, P))
+        for i in range(S):
+            out[i] = y[cu[i + 1] - T:cu[i + 1]]
+        self._pending = drafts
+        return out
+
+    def commit(self, accepted: Sequence[int]):
+        for i, a in enumerate(accepted):
+            if a < 0 or a > self._pending[i][0].shape[0]:
+                raise ValueError("accepted out of range")
+            for j in range(int(a)):
+                self.committed[i].append(tuple(self._pending[i][k][j] for k in range(4)))
+        self._pending = None

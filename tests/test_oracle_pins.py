@@ -1,0 +1,336 @@
+"""Pins for the fp64 oracle: it is checked against things other than itself.
+
+Each test uses a different route to the same numbers: a hand-worked fixture,
+closed forms (geometric series, no-decay linear attention, one token), the
+chunked SSD form and the ReplaySSM reassociated output form written out from
+their own equations, a library IIR filter, linearity, and invariants (prefix,
+packing, group mapping).  A dropped term, a wrong sign, swapped B/C, a wrong
+group index or a wrong decay would fail at least one of them.
+"""
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+
+import oracle
+import synth
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+
+
+def _rand_case(rng, T, H, G, P, N, A_scale=(1.0, 16.0)):
+    x = rng.standard_normal((T, H, P))
+    dt = rng.standard_normal((T, H))
+    B = rng.standard_normal((T, G, N))
+    C = rng.standard_normal((T, G, N))
+    A = -rng.uniform(*A_scale, size=H)
+    D = rng.standard_normal(H)
+    dt_bias = np.log(np.expm1(rng.uniform(1e-3, 1e-1, size=H)))
+    return x, dt, A, B, C, D, dt_bias
+
+
+def _delta(dt, dt_bias):
+    # softplus written as log(1 + e^z) directly; inputs here stay in |z| < 30.
+    return np.log1p(np.exp(dt + dt_bias[None, :]))
+
+
+def _relerr(a, b):
+    return float(np.max(np.abs(a - b)) / max(np.max(np.abs(b)), 1e-300))
+
+
+# -- softplus ------------------------------------------------------------------------------------
+
+def test_softplus_identities():
+    assert oracle.softplus(0.0) == pytest.approx(math.log(2.0), rel=0, abs=1e-16)
+    for z in (-30.0, -3.5, -0.25, 0.7, 4.0, 25.0):
+        # softplus(z) - softplus(-z) = z  and  softplus(z) > max(z, 0)
+        assert oracle.softplus(z) - oracle.softplus(-z) == pytest.approx(z, rel=1e-14, abs=1e-14)
+        assert oracle.softplus(z) > max(z, 0.0)
+    assert oracle.softplus(700.0) == 700.0          # no overflow for large arguments
+    assert oracle.softplus(-40.0) == pytest.approx(math.exp(-40.0), rel=1e-12)
+
+
+# -- hand-worked fixture ---------------------------------------------------------------------------
+
+def test_golden_scalar_two_token():
+    with open(os.path.join(HERE, "golden", "scalar_two_token.json")) as f:
+        g = json.load(f)
+    env = {"log": math.log, "exp": math.exp}
+    inp = g["inputs"]
+    x = np.array(inp["x"]).reshape(2, 1, 1)
+    dt = np.array(inp["dt"]).reshape(2, 1)
+    B = np.array(inp["B"]).reshape(2, 1, 1)
+    C = np.array(inp["C"]).reshape(2, 1, 1)
+    A = np.array([eval(inp["A"], env)])
+    y, fin = oracle.recurrence(x, dt, A, B, C, np.array([inp["D"]]), np.array([inp["dt_bias"]]))
+    exp_y = [eval(e, env) for e in g["expected_y"]]
+    assert y[:, 0, 0] == pytest.approx(exp_y, rel=1e-14)
+    assert fin[0, 0, 0, 0] == pytest.approx(eval(g["expected_final_state"], env), rel=1e-14)
+
+
+# -- closed forms ------------------------------------------------------------------------------------
+
+def test_single_token_closed_form():
+    rng = np.random.default_rng(1)
+    x, dt, A, B, C, D, dtb = _rand_case(rng, 1, 3, 1, 5, 7)
+    y, fin = oracle.recurrence(x, dt, A, B, C, D, dtb)
+    delta = _delta(dt, dtb)[0]
+    bc = float(B[0, 0] @ C[0, 0])
+    want = delta[:, None] * bc * x[0] + D[:, None] * x[0]
+    assert _relerr(y[0], want) < 1e-14
+    want_state = delta[:, None, None] * x[0][:, :, None] * B[0, 0][None, None, :]
+    assert _relerr(fin[0], want_state) < 1e-14
+
+
+def test_geometric_series_constant_inputs():
+    """Constant inputs: S_T = v k^T (1 - a^T) / (1 - a) with a = exp(delta A)."""
+    rng = np.random.default_rng(2)
+    T, H, P, N = 37, 2, 3, 4
+    x1 = rng.standard_normal((H, P))
+    B1 = rng.standard_normal(N)
+    C1 = rng.standard_normal(N)
+    dt1 = rng.standard_normal(H)
+    A = -rng.uniform(0.05, 2.0, size=H)
+    D = rng.standard_normal(H)
+    dtb = np.zeros(H)
+    x = np.broadcast_to(x1, (T, H, P)).copy()
+    B = np.broadcast_to(B1, (T, 1, N)).copy()
+    C = np.broadcast_to(C1, (T, 1, N)).copy()
+    dt = np.broadcast_to(dt1, (T, H)).copy()
+    y, fin = oracle.recurrence(x, dt, A, B, C, D, dtb)
+    delta = np.log1p(np.exp(dt1))
+    a = np.exp(delta * A)
+    for t in (0, 5, T - 1):
+        geo = (1 - a ** (t + 1)) / (1 - a)
+        S = (delta * geo)[:, None, None] * x1[:, :, None] * B1[None, None, :]
+        want = S @ C1 + D[:, None] * x1
+        assert _relerr(y[t], want) < 1e-13
+    S = (delta * (1 - a ** T) / (1 - a))[:, None, None] * x1[:, :, None] * B1[None, None, :]
+    assert _relerr(fin[0], S) < 1e-13
+
+
+def test_no_decay_is_causal_linear_attention():
+    """A = 0: y_t = sum_{s<=t} delta_s (B_s . C_t) x_s + D x_t (+ init C_t)."""
+    rng = np.random.default_rng(3)
+    T, H, G, P, N = 23, 4, 2, 3, 5
+    x, dt, _, B, C, D, dtb = _rand_case(rng, T, H, G, P, N)
+    A = np.zeros(H)
+    init = rng.standard_normal((1, H, P, N))
+    y, fin = oracle.recurrence(x, dt, A, B, C, D, dtb, init_state=init)
+    delta = _delta(dt, dtb)
+    for h in range(H):
+        g = h // (H // G)
+        att = np.tril(C[:, g] @ B[:, g].T) * delta[None, :, h]     # [t, s]
+        want = att @ x[:, h] + (C[:, g] @ init[0, h].T) + D[h] * x[:, h]
+        assert _relerr(y[:, h], want) < 1e-13
+        want_state = init[0, h] + np.einsum("s,sp,sn->pn", delta[:, h], x[:, h], B[:, g])
+        assert _relerr(fin[0, h], want_state) < 1e-13
+
+
+def test_scalar_case_matches_scipy_lfilter():
+    """P = N = 1 with constant delta is a first-order IIR filter."""
+    signal = pytest.importorskip("scipy.signal")
+    rng = np.random.default_rng(4)
+    T = 200
+    xs = rng.standard_normal(T)
+    Cs = rng.standard_normal(T)
+    dt = np.full((T, 1), 0.3)
+    A = np.array([-1.7])
+    D = np.array([0.25])
+    y, _ = oracle.recurrence(xs.reshape(T, 1, 1), dt, A, np.ones((T, 1, 1)), Cs.reshape(T, 1, 1), D,
+                             np.array([0.0]))
+    delta = math.log1p(math.exp(0.3))
+    a = math.exp(delta * A[0])
+    state = signal.lfilter([delta], [1.0, -a], xs)
+    assert _relerr(y[:, 0, 0], state * Cs + D[0] * xs) < 1e-13
+
+
+# -- the chunked SSD form, written from its own equations --------------------------------------------
+
+def _ssd_chunked(x, dt, A, B, C, D, dtb, Q, init):
+    T, H, P = x.shape
+    G = B.shape[1]
+    delta = _delta(dt, dtb)
+    y = np.zeros_like(x)
+    state = init.copy()
+    for c0 in range(0, T, Q):
+        c1 = min(T, c0 + Q)
+        for h in range(H):
+            g = h // (H // G)
+            dA = delta[c0:c1, h] * A[h]
+            acum = np.cumsum(dA)
+            seg = acum[:, None] - acum[None, :]                      # Acum_t - Acum_s
+            Lmask = np.where(np.tril(np.ones((c1 - c0, c1 - c0), bool)), np.exp(np.where(
+                np.tril(np.ones((c1 - c0, c1 - c0), bool)), seg, 0.0)), 0.0)
+            Gm = C[c0:c1, g] @ B[c0:c1, g].T                          # [t, s]
+            M = Gm * Lmask * delta[None, c0:c1, h]
+            y_diag = M @ x[c0:c1, h]                                 # [t, P]
+            y_off = np.exp(acum)[:, None] * (C[c0:c1, g] @ state[h].T)
+            y[c0:c1, h] = y_diag + y_off + D[h] * x[c0:c1, h]
+            w = np.exp(acum[-1] - acum) * delta[c0:c1, h]
+            state[h] = np.exp(acum[-1]) * state[h] + np.einsum("s,sp,sn->pn", w, x[c0:c1, h], B[c0:c1, g])
+    return y, state
+
+
+@pytest.mark.parametrize("Q", [1, 7, 16, 64])
+def test_chunked_ssd_form_matches(Q):
+    rng = np.random.default_rng(10 + Q)
+    T, H, G, P, N = 64, 4, 1, 16, 16
+    x, dt, A, B, C, D, dtb = _rand_case(rng, T, H, G, P, N)
+    init = rng.standard_normal((H, P, N))
+    want_y, want_s = _ssd_chunked(x, dt, A, B, C, D, dtb, Q, init)
+    y, fin = oracle.recurrence(x, dt, A, B, C, D, dtb, init_state=init[None])
+    assert _relerr(y, want_y) < 1e-12
+    assert _relerr(fin[0], want_s) < 1e-12
+
+
+# -- ReplaySSM reassociated output form (explicit gamma products) --------------------------------------
+
+def test_reassociated_output_only_form():
+    """S_h = gamma_{1:h} S_ckpt + sum_j gamma_{j+1:h} v_j k_j^T and
+    O = S_ckpt Q D + V (W . K^T Q) with W_js = 1[j <= h+s] gamma_{j+1:h+s}."""
+    rng = np.random.default_rng(5)
+    h, T = 9, 4                      # committed records, drafts
+    H, G, P, N = 2, 1, 3, 5
+    x, dt, A, B, C, D, dtb = _rand_case(rng, h + T, H, G, P, N, A_scale=(0.1, 3.0))
+    S_ckpt = rng.standard_normal((1, H, P, N))
+    y, _ = oracle.recurrence(x, dt, A, B, C, D, dtb, init_state=S_ckpt)
+    _, S_h = oracle.recurrence(x[:h], dt[:h], A, B[:h], C[:h], D, dtb, init_state=S_ckpt)
+    delta = _delta(dt, dtb)
+    for hd in range(H):
+        alpha = np.exp(delta[:, hd] * A[hd])              # alpha_i, i = 1..h+T  (0-based here)
+        gam = lambda a, b: float(np.prod(alpha[a - 1:b])) if b >= a else 1.0  # gamma_{a:b}, 1-based
+        V = delta[:, hd, None] * x[:, hd]                  # v_j  [j, P]
+        K = B[:, 0]                                        # k_j  [j, N]
+        Qm = C[:, 0]                                       # q    [j, N]
+        Sh = gam(1, h) * S_ckpt[0, hd] + sum(gam(j + 2, h) * np.outer(V[j], K[j]) for j in range(h))
+        assert _relerr(S_h[0, hd], Sh) < 1e-13
+        for s in range(1, T + 1):
+            col = h + s                                    # 1-based position of draft s
+            q = Qm[col - 1]
+            O = gam(1, col) * (S_ckpt[0, hd] @ q)
+            for j in range(1, col + 1):
+                O = O + V[j - 1] * gam(j + 1, col) * float(K[j - 1] @ q)
+            want = O + D[hd] * x[col - 1, hd]
+            assert _relerr(y[col - 1, hd], want) < 1e-13
+
+
+# -- invariants --------------------------------------------------------------------------------------
+
+def test_linearity_in_x_and_initial_state():
+    rng = np.random.default_rng(6)
+    T, H, G, P, N = 19, 2, 1, 4, 3
+    x1, dt, A, B, C, D, dtb = _rand_case(rng, T, H, G, P, N)
+    x2 = rng.standard_normal(x1.shape)
+    i1, i2 = rng.standard_normal((2, 1, H, P, N))
+    a, b = 0.75, -1.3
+    y1, s1 = oracle.recurrence(x1, dt, A, B, C, D, dtb, init_state=i1)
+    y2, s2 = oracle.recurrence(x2, dt, A, B, C, D, dtb, init_state=i2)
+    y, s = oracle.recurrence(a * x1 + b * x2, dt, A, B, C, D, dtb, init_state=a * i1 + b * i2)
+    assert _relerr(y, a * y1 + b * y2) < 1e-12
+    assert _relerr(s, a * s1 + b * s2) < 1e-12
+
+
+def test_group_mapping_contiguous_heads():
+    """Heads h use group h // (H/G): compare with G = H and B/C replicated per head."""
+    rng = np.random.default_rng(7)
+    T, H, G, P, N = 11, 6, 2, 3, 4
+    x, dt, A, B, C, D, dtb = _rand_case(rng, T, H, G, P, N)
+    y, s = oracle.recurrence(x, dt, A, B, C, D, dtb)
+    idx = np.arange(H) // (H // G)
+    y2, s2 = oracle.recurrence(x, dt, A, B[:, idx], C[:, idx], D, dtb)
+    assert np.array_equal(y, y2) and np.array_equal(s, s2)
+
+
+def test_prefix_and_packing_invariance():
+    rng = np.random.default_rng(8)
+    H, G, P, N = 4, 2, 3, 5
+    x, dt, A, B, C, D, dtb = _rand_case(rng, 30, H, G, P, N)
+    y, _ = oracle.recurrence(x, dt, A, B, C, D, dtb)
+    for t in (1, 7, 29):
+        yp, _ = oracle.recurrence(x[:t], dt[:t], A, B[:t], C[:t], D, dtb)
+        assert np.array_equal(yp, y[:t])
+    cu = np.array([0, 12, 13, 30])
+    yk, sk = oracle.recurrence(x, dt, A, B, C, D, dtb, cu_seqlens=cu)
+    for i in range(3):
+        lo, hi = cu[i], cu[i + 1]
+        ys, ss = oracle.recurrence(x[lo:hi], dt[lo:hi], A, B[lo:hi], C[lo:hi], D, dtb)
+        assert np.array_equal(yk[lo:hi], ys) and np.array_equal(sk[i], ss[0])
+
+
+def test_thread_count_does_not_change_bits():
+    rng = np.random.default_rng(9)
+    x, dt, A, B, C, D, dtb = _rand_case(rng, 40, 8, 2, 8, 8)
+    cu = np.array([0, 17, 40])
+    y1, s1 = oracle.recurrence(x, dt, A, B, C, D, dtb, cu, nthreads=1)
+    y8, s8 = oracle.recurrence(x, dt, A, B, C, D, dtb, cu, nthreads=8)
+    assert np.array_equal(y1, y8) and np.array_equal(s1, s8)
+
+
+# -- the ReplaySSM protocol model ------------------------------------------------------------------------
+
+def _protocol_case(seed, S=3, steps=9, T=4, L=16):
+    rng = np.random.default_rng(seed)
+    H, G, P, N = 2, 1, 3, 4
+    params = synth.Params(-rng.uniform(0.2, 3.0, H).astype(np.float32), rng.standard_normal(H).astype(np.float32),
+                          np.log(np.expm1(rng.uniform(1e-3, 1e-1, H))).astype(np.float32))
+    anchor = rng.standard_normal((S, H, P, N))
+    drafts = [[(rng.standard_normal((T, H, P)), rng.standard_normal((T, H)), rng.standard_normal((T, G, N)),
+                rng.standard_normal((T, G, N))) for _ in range(S)] for _ in range(steps)]
+    acc = rng.integers(0, T + 1, size=(steps, S))
+    return params, anchor, drafts, acc, L
+
+
+def test_protocol_zero_acceptance_keeps_anchor():
+    params, anchor, drafts, _, L = _protocol_case(11)
+    m = oracle.ReplaySSMModel(params, anchor, L)
+    for k in range(6):
+        m.verify(drafts[k])
+        m.commit([0] * len(drafts[k]))
+    assert np.array_equal(m.anchor, anchor) and m.flushes == 0 and np.all(m.h() == 0)
+
+
+def test_protocol_committed_stream_matches_plain_recurrence():
+    """After any accept/reject pattern, anchor + committed records reproduce the
+    plain recurrence over exactly the accepted tokens (rejected drafts never enter)."""
+    params, anchor, drafts, acc, L = _protocol_case(12, steps=12)
+    m = oracle.ReplaySSMModel(params, anchor, L)
+    accepted = [[] for _ in range(len(anchor))]
+    for k in range(len(drafts)):
+        m.verify(drafts[k])
+        m.commit(acc[k])
+        for i in range(len(anchor)):
+            for j in range(acc[k, i]):
+                accepted[i].append(tuple(drafts[k][i][q][j] for q in range(4)))
+    assert m.flushes > 0
+    m.refresh(range(len(anchor)))
+    for i in range(len(anchor)):
+        rec = [np.stack([r[q] for r in accepted[i]]) for q in range(4)]
+        _, fin = oracle.recurrence(rec[0], rec[1], params.A, rec[2], rec[3], params.D, params.dt_bias,
+                                   init_state=anchor[i:i + 1])
+        assert _relerr(m.anchor[i], fin[0]) < 1e-12
+
+
+def test_protocol_anchor_independent_of_read_precision():
+    """Read-copy rounding never feeds the anchor (dual precision)."""
+    params, anchor, drafts, acc, L = _protocol_case(13, steps=12)
+    m1 = oracle.ReplaySSMModel(params, anchor, L)
+    m2 = oracle.ReplaySSMModel(params, anchor, L, read_cast=lambda s: np.array(s, copy=True))  # unrounded
+    y1 = y2 = None
+    for k in range(len(drafts)):
+        y1 = m1.verify(drafts[k]); m1.commit(acc[k])
+        y2 = m2.verify(drafts[k]); m2.commit(acc[k])
+    assert m1.flushes > 0
+    assert np.array_equal(m1.anchor, m2.anchor)
+    assert not np.array_equal(y1, y2)        # outputs do see the read precision
+
+
+def test_bf16_round_matches_synth_rounding():
+    rng = np.random.default_rng(14)
+    v = rng.standard_normal(10000).astype(np.float32) * 7
+    assert np.array_equal(oracle.bf16_round(v).astype(np.float32), synth.round_bf16(v))
+    # ties go to even: 1 + 2^-8 lies halfway between bf16 neighbours 1 and 1 + 2^-7
+    assert oracle.bf16_round(np.array([1.0 + 2.0 ** -8], np.float32))[0] == 1.0
+    assert oracle.bf16_round(np.array([1.0 + 3 * 2.0 ** -8], np.float32))[0] == 1.0 + 2.0 ** -6
