@@ -1,0 +1,338 @@
+// C ABI of the library (declared in include/ers.h): host-side validation, workspace carving and
+// dispatch to the kernels.  A call that fails validation launches nothing.
+#include <stdint.h>
+#include <string.h>
+
+#include "ers.h"
+#include "ers_internal.h"
+
+using ers::LaunchArgs;
+
+namespace {
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+ers_status check_ptr(const void* p, bool required) {
+  if (p == nullptr) return required ? ERS_EINVAL : ERS_OK;
+  return aligned16(p) ? ERS_OK : ERS_EPTR;
+}
+
+#define ERS_TRY(expr)                  \
+  do {                                 \
+    const ers_status st_ = (expr);     \
+    if (st_ != ERS_OK) return st_;     \
+  } while (0)
+
+ers_status check_dims(const ers_dims* d) {
+  if (d == nullptr) return ERS_EINVAL;
+  if (d->io_dtype != ERS_DTYPE_F32 && d->io_dtype != ERS_DTYPE_BF16) return ERS_EDTYPE;
+  if (d->nheads <= 0 || d->ngroups <= 0 || d->nheads % d->ngroups != 0) return ERS_ESHAPE;
+  if (d->chunk < 1 || d->chunk > ers::kQMaxHost) return ERS_ESHAPE;
+  if (!ers::fma_supported(d->headdim, d->dstate)) return ERS_ESHAPE;
+  return ERS_OK;
+}
+
+ers_status check_params(const ers_params* p) {
+  if (p == nullptr) return ERS_EINVAL;
+  ERS_TRY(check_ptr(p->A, true));
+  ERS_TRY(check_ptr(p->D, true));
+  ERS_TRY(check_ptr(p->dt_bias, true));
+  return ERS_OK;
+}
+
+ers_status check_cache(const ers_cache* c, bool need_read_copy) {
+  if (c == nullptr || c->nslots < 0) return ERS_EINVAL;
+  ERS_TRY(check_ptr(c->state, true));
+  ERS_TRY(check_ptr(c->read_copy, need_read_copy));
+  ERS_TRY(check_ptr(c->buf_x, true));
+  ERS_TRY(check_ptr(c->buf_dt, true));
+  ERS_TRY(check_ptr(c->buf_B, true));
+  ERS_TRY(check_ptr(c->buf_C, true));
+  ERS_TRY(check_ptr(c->pos, true));
+  return ERS_OK;
+}
+
+LaunchArgs base_args(const ers_dims* d, const ers_params* p) {
+  LaunchArgs a;
+  memset(&a, 0, sizeof(a));
+  a.H = d->nheads;
+  a.G = d->ngroups;
+  a.P = d->headdim;
+  a.N = d->dstate;
+  a.Q = d->chunk;
+  a.io = d->io_dtype;
+  if (p != nullptr) {
+    a.A = p->A;
+    a.D = p->D;
+    a.dt_bias = p->dt_bias;
+  }
+  return a;
+}
+
+void set_cache(LaunchArgs& a, const ers_cache* c) {
+  a.state = c->state;
+  a.read_copy = c->read_copy;
+  a.bx = c->buf_x;
+  a.bdt = c->buf_dt;
+  a.bB = c->buf_B;
+  a.bC = c->buf_C;
+  a.pos = c->pos;
+  a.nslots = c->nslots;
+}
+
+struct Workspace {
+  size_t states, tot, total;
+};
+
+Workspace prefill_workspace(const ers_dims* d, int32_t nseq, int32_t max_chunks) {
+  Workspace w;
+  const size_t units = (size_t)(nseq > 0 ? nseq : 0) * (size_t)(max_chunks > 0 ? max_chunks : 0) * d->nheads;
+  w.states = ers::align256(units * d->headdim * d->dstate * sizeof(float));
+  w.tot = ers::align256(units * sizeof(float));
+  w.total = w.states + w.tot;
+  return w;
+}
+
+int32_t scan_chunks(int32_t max_seqlen, int32_t Q) { return (max_seqlen + Q - 1) / Q; }
+int32_t resume_chunks(int32_t max_seqlen, int32_t Q) { return (max_seqlen + Q - 1 + Q - 1) / Q; }
+
+ers_status finish(cudaError_t e) { return e == cudaSuccess ? ERS_OK : ERS_ECUDA; }
+
+ers_status check_tokens(const void* x, const float* dt, const void* B, const void* C, bool required) {
+  ERS_TRY(check_ptr(x, required));
+  ERS_TRY(check_ptr(dt, required));
+  ERS_TRY(check_ptr(B, required));
+  ERS_TRY(check_ptr(C, required));
+  return ERS_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* ers_status_str(ers_status s) {
+  switch (s) {
+    case ERS_OK: return "ok";
+    case ERS_EINVAL: return "invalid argument";
+    case ERS_ESHAPE: return "unsupported dimensions";
+    case ERS_EDTYPE: return "unsupported dtype";
+    case ERS_EPTR: return "pointer not 16-byte aligned";
+    case ERS_EALIGN: return "slot position outside its legal range";
+    case ERS_EOVERFLOW: return "committed pointer plus drafts exceeds the refresh period";
+    case ERS_ECOMMIT: return "accepted count outside [0, T]";
+    case ERS_ESLOT: return "slot index out of range";
+    case ERS_ETIMEOUT: return "bounded device wait gave up";
+    case ERS_EWORKSPACE: return "workspace missing or too small";
+    case ERS_ECUDA: return "CUDA launch error";
+    case ERS_EUNSUPPORTED: return "unsupported request";
+    default: return "unknown status";
+  }
+}
+
+int32_t ers_version(void) { return 100; }
+
+size_t ers_ssd_scan_fwd_workspace_size(const ers_dims* dims, int32_t nseq, int32_t max_seqlen) {
+  if (check_dims(dims) != ERS_OK || nseq < 0 || max_seqlen < 0) return 0;
+  return prefill_workspace(dims, nseq, scan_chunks(max_seqlen, dims->chunk)).total;
+}
+
+size_t ers_chunked_prefill_workspace_size(const ers_dims* dims, int32_t nseq, int32_t max_seqlen) {
+  if (check_dims(dims) != ERS_OK || nseq < 0 || max_seqlen < 0) return 0;
+  return prefill_workspace(dims, nseq, resume_chunks(max_seqlen, dims->chunk)).total;
+}
+
+ers_status ers_ssd_scan_fwd(const ers_dims* dims, const ers_params* prm, int32_t nseq, int64_t ntokens,
+                            int32_t max_seqlen, const int32_t* cu_seqlens, const void* x, const float* dt,
+                            const void* B, const void* C, const float* init_state, void* y,
+                            float* final_state, float* chunk_states, void* workspace, size_t workspace_bytes,
+                            ers_stream_t stream, int32_t* dev_status) {
+  ERS_TRY(check_dims(dims));
+  ERS_TRY(check_params(prm));
+  if (nseq < 0 || ntokens < 0 || max_seqlen < 0) return ERS_EINVAL;
+  if (nseq == 0) return ERS_OK;
+  ERS_TRY(check_ptr(cu_seqlens, true));
+  ERS_TRY(check_tokens(x, dt, B, C, ntokens > 0));
+  ERS_TRY(check_ptr(y, ntokens > 0));
+  ERS_TRY(check_ptr(final_state, true));
+  ERS_TRY(check_ptr(init_state, false));
+  ERS_TRY(check_ptr(chunk_states, false));
+  ERS_TRY(check_ptr(dev_status, false));
+  const int32_t mc = scan_chunks(max_seqlen, dims->chunk);
+  const Workspace w = prefill_workspace(dims, nseq, mc);
+  if (w.total > 0 && (workspace == nullptr || workspace_bytes < w.total)) return ERS_EWORKSPACE;
+  ERS_TRY(check_ptr(workspace, false));
+  LaunchArgs a = base_args(dims, prm);
+  a.x = x; a.dt = dt; a.B = B; a.C = C;
+  a.cu = cu_seqlens;
+  a.nseq = nseq;
+  a.max_chunks = mc;
+  a.y = y;
+  a.init_state = init_state;
+  a.final_state = final_state;
+  a.chunk_states = chunk_states;
+  a.ws_states = (float*)workspace;
+  a.ws_tot = (float*)((char*)workspace + w.states);
+  a.status = dev_status;
+  return finish(ers::fma_prefill(a, ers::Op::kScan, (cudaStream_t)stream));
+}
+
+ers_status ers_chunked_prefill(const ers_dims* dims, const ers_params* prm, const ers_cache* cache,
+                               int32_t nseq, int64_t ntokens, int32_t max_seqlen, const int32_t* cu_seqlens,
+                               const int32_t* slot, const void* x, const float* dt, const void* B,
+                               const void* C, void* y, void* workspace, size_t workspace_bytes,
+                               ers_stream_t stream, int32_t* dev_status) {
+  ERS_TRY(check_dims(dims));
+  ERS_TRY(check_params(prm));
+  ERS_TRY(check_cache(cache, false));
+  if (nseq < 0 || ntokens < 0 || max_seqlen < 0) return ERS_EINVAL;
+  if (nseq == 0) return ERS_OK;
+  if (slot == nullptr && nseq > cache->nslots) return ERS_EINVAL;
+  ERS_TRY(check_ptr(cu_seqlens, true));
+  ERS_TRY(check_ptr(slot, false));
+  ERS_TRY(check_tokens(x, dt, B, C, ntokens > 0));
+  ERS_TRY(check_ptr(y, ntokens > 0));
+  ERS_TRY(check_ptr(dev_status, false));
+  const int32_t mc = resume_chunks(max_seqlen, dims->chunk);
+  const Workspace w = prefill_workspace(dims, nseq, mc);
+  if (w.total > 0 && (workspace == nullptr || workspace_bytes < w.total)) return ERS_EWORKSPACE;
+  ERS_TRY(check_ptr(workspace, false));
+  LaunchArgs a = base_args(dims, prm);
+  set_cache(a, cache);
+  a.x = x; a.dt = dt; a.B = B; a.C = C;
+  a.cu = cu_seqlens;
+  a.slot = slot;
+  a.nseq = nseq;
+  a.max_chunks = mc;
+  a.y = y;
+  a.ws_states = (float*)workspace;
+  a.ws_tot = (float*)((char*)workspace + w.states);
+  a.status = dev_status;
+  return finish(ers::fma_prefill(a, ers::Op::kChunkedPrefill, (cudaStream_t)stream));
+}
+
+ers_status ers_replay_decode(const ers_dims* dims, const ers_params* prm, const ers_cache* cache, int32_t nseq,
+                             const int32_t* slot, const void* x, const float* dt, const void* B, const void* C,
+                             uint32_t flags, void* y, ers_stream_t stream, int32_t* dev_status) {
+  ERS_TRY(check_dims(dims));
+  ERS_TRY(check_params(prm));
+  const bool rssm = (flags & ERS_FLAG_REPLAYSSM) != 0;
+  if ((flags & ~(ERS_FLAG_FUSE_REFRESH | ERS_FLAG_REPLAYSSM)) != 0) return ERS_EINVAL;
+  if (rssm && (flags & ERS_FLAG_FUSE_REFRESH)) return ERS_EINVAL;
+  ERS_TRY(check_cache(cache, rssm));
+  if (nseq < 0) return ERS_EINVAL;
+  if (nseq == 0) return ERS_OK;
+  if (slot == nullptr && nseq > cache->nslots) return ERS_EINVAL;
+  ERS_TRY(check_ptr(slot, false));
+  ERS_TRY(check_tokens(x, dt, B, C, true));
+  ERS_TRY(check_ptr(y, true));
+  ERS_TRY(check_ptr(dev_status, false));
+  LaunchArgs a = base_args(dims, prm);
+  set_cache(a, cache);
+  a.x = x; a.dt = dt; a.B = B; a.C = C;
+  a.slot = slot;
+  a.nseq = nseq;
+  a.flags = flags;
+  a.y = y;
+  a.status = dev_status;
+  return finish(ers::fma_decode(a, (cudaStream_t)stream));
+}
+
+ers_status ers_refresh(const ers_dims* dims, const ers_params* prm, const ers_cache* cache, int32_t nseq,
+                       const int32_t* slot, uint32_t flags, int32_t drafts_T, ers_stream_t stream,
+                       int32_t* dev_status) {
+  ERS_TRY(check_dims(dims));
+  ERS_TRY(check_params(prm));
+  if ((flags & ~ERS_FLAG_REPLAYSSM) != 0) return ERS_EINVAL;
+  ERS_TRY(check_cache(cache, false));
+  if (nseq < 0 || drafts_T < 0) return ERS_EINVAL;
+  if (nseq == 0) return ERS_OK;
+  if (slot == nullptr && nseq > cache->nslots) return ERS_EINVAL;
+  ERS_TRY(check_ptr(slot, false));
+  ERS_TRY(check_ptr(dev_status, false));
+  LaunchArgs a = base_args(dims, prm);
+  set_cache(a, cache);
+  a.slot = slot;
+  a.nseq = nseq;
+  a.flags = flags;
+  a.T = drafts_T;
+  a.status = dev_status;
+  return finish(ers::fma_refresh(a, (cudaStream_t)stream));
+}
+
+ers_status ers_spec_verify(const ers_dims* dims, const ers_params* prm, const ers_cache* cache, int32_t nseq,
+                           const int32_t* slot, int32_t T, const void* x, const float* dt, const void* B,
+                           const void* C, uint32_t flags, void* y, ers_stream_t stream, int32_t* dev_status) {
+  ERS_TRY(check_dims(dims));
+  ERS_TRY(check_params(prm));
+  if ((flags & ~ERS_FLAG_AUTO_FLUSH) != 0) return ERS_EINVAL;
+  ERS_TRY(check_cache(cache, true));
+  if (nseq < 0 || T < 1 || T > dims->chunk) return ERS_EINVAL;
+  if (nseq == 0) return ERS_OK;
+  if (slot == nullptr && nseq > cache->nslots) return ERS_EINVAL;
+  ERS_TRY(check_ptr(slot, false));
+  ERS_TRY(check_tokens(x, dt, B, C, true));
+  ERS_TRY(check_ptr(y, true));
+  ERS_TRY(check_ptr(dev_status, false));
+  LaunchArgs a = base_args(dims, prm);
+  set_cache(a, cache);
+  a.x = x; a.dt = dt; a.B = B; a.C = C;
+  a.slot = slot;
+  a.nseq = nseq;
+  a.T = T;
+  a.flags = flags;
+  a.y = y;
+  a.status = dev_status;
+  return finish(ers::fma_verify(a, (cudaStream_t)stream));
+}
+
+ers_status ers_commit(const ers_dims* dims, const ers_cache* cache, int32_t nseq, const int32_t* slot,
+                      const int32_t* accepted, int32_t T, uint32_t flags, ers_stream_t stream,
+                      int32_t* dev_status) {
+  ERS_TRY(check_dims(dims));
+  if ((flags & ~ERS_FLAG_AUTO_FLUSH) != 0) return ERS_EINVAL;
+  if (cache == nullptr || cache->nslots < 0) return ERS_EINVAL;
+  ERS_TRY(check_ptr(cache->pos, true));
+  if (nseq < 0 || T < 1 || T > dims->chunk) return ERS_EINVAL;
+  if (nseq == 0) return ERS_OK;
+  if (slot == nullptr && nseq > cache->nslots) return ERS_EINVAL;
+  ERS_TRY(check_ptr(slot, false));
+  ERS_TRY(check_ptr(accepted, true));
+  ERS_TRY(check_ptr(dev_status, false));
+  LaunchArgs a = base_args(dims, nullptr);
+  a.pos = cache->pos;
+  a.nslots = cache->nslots;
+  a.slot = slot;
+  a.nseq = nseq;
+  a.accepted = accepted;
+  a.T = T;
+  a.flags = flags;
+  a.status = dev_status;
+  return finish(ers::launch_commit(a, (cudaStream_t)stream));
+}
+
+ers_status ers_ssu_update(const ers_dims* dims, const ers_params* prm, float* state, int32_t nslots,
+                          int32_t nseq, const int32_t* slot, const void* x, const float* dt, const void* B,
+                          const void* C, void* y, ers_stream_t stream, int32_t* dev_status) {
+  ERS_TRY(check_dims(dims));
+  ERS_TRY(check_params(prm));
+  if (!ers::ssu_supported(dims->headdim, dims->dstate)) return ERS_ESHAPE;
+  if (nseq < 0 || nslots < 0) return ERS_EINVAL;
+  if (nseq == 0) return ERS_OK;
+  if (slot == nullptr && nseq > nslots) return ERS_EINVAL;
+  ERS_TRY(check_ptr(state, true));
+  ERS_TRY(check_ptr(slot, false));
+  ERS_TRY(check_tokens(x, dt, B, C, true));
+  ERS_TRY(check_ptr(y, true));
+  ERS_TRY(check_ptr(dev_status, false));
+  LaunchArgs a = base_args(dims, prm);
+  a.state = state;
+  a.nslots = nslots;
+  a.slot = slot;
+  a.nseq = nseq;
+  a.x = x; a.dt = dt; a.B = B; a.C = C;
+  a.y = y;
+  a.status = dev_status;
+  return finish(ers::ssu_update(a, (cudaStream_t)stream));
+}
+
+}  // extern "C"

@@ -1,0 +1,698 @@
+// CUDA-core ("FMA") chunk engine: every path of the library built on one set of fixed-order
+// device functions.
+//
+// The chunked SSD scan (exact-replay RFC, vLLM issue 55524, section 1) computes, for a chunk of Q
+// tokens starting from boundary state H (per head, [P x N]):
+//   Acum_t      = sum_{r<=t} delta_r A                           (prefix of log-decays)
+//   y_t         = exp(Acum_t) (H C_t) + sum_{s<=t} (C_t . B_s) delta_s exp(Acum_t - Acum_s) x_s + D x_t
+//   H'          = exp(Acum_last) H + sum_s delta_s exp(Acum_last - Acum_s) x_s B_s^T
+// Exact replay (RFC section 3) recomputes the outputs of a partial chunk from its boundary state
+// and buffered inputs.  Here each output element and each chunk state is produced by the same
+// device function in every path (row_output / chunk_state below), so prefill, chunked prefill,
+// decode, refresh and verify agree bit for bit by construction.
+//
+// This engine serves fp32 io (all paths) and is the first, simple implementation for bf16 io.
+#include <stdio.h>
+
+#include "ers_common.cuh"
+#include "ers_internal.h"
+
+namespace ers {
+namespace {
+
+struct FmaSmem {
+  float hi[kQMax];     // Acum (double-float, hi part); holds dA before the scan
+  float lo[kQMax];
+  float delta[kQMax];  // softplus(dt + dt_bias)
+  float w[kQMax];      // chunk-state weights delta_s exp(Acum_last - Acum_s)
+  float M[kQMax];      // one output row's masked, decayed Gram column
+  const void* rowB[kQMax];
+  const void* rowC[kQMax];
+  float yoff[64];
+};
+// followed in dynamic shared memory by xs[Q][P] (x rows as fp32)
+
+__host__ __device__ constexpr size_t fma_smem_bytes(int Q, int P) {
+  return ((sizeof(FmaSmem) + 15) & ~size_t(15)) + (size_t)Q * P * sizeof(float);
+}
+
+// Row source of a chunk: rows [0, nbuf) come from a slot's partial-chunk buffer, rows >= nbuf from
+// packed token inputs (row r is token tok0 + r).  Row strides are the token strides H*P, H, G*N.
+template <typename T>
+struct Rows {
+  int nbuf;
+  const T* bx;
+  const float* bdt;
+  const T* bB;
+  const T* bC;
+  const T* x0;
+  const float* dt0;
+  const T* B0;
+  const T* C0;
+  long long tok0;
+  int sx, sdt, sB;
+  __device__ __forceinline__ const T* x(int r) const {
+    return r < nbuf ? bx + (long long)r * sx : x0 + (tok0 + r) * sx;
+  }
+  __device__ __forceinline__ float dt(int r) const {
+    return r < nbuf ? bdt[(long long)r * sdt] : dt0[(tok0 + r) * sdt];
+  }
+  __device__ __forceinline__ const T* B(int r) const {
+    return r < nbuf ? bB + (long long)r * sB : B0 + (tok0 + r) * sB;
+  }
+  __device__ __forceinline__ const T* C(int r) const {
+    return r < nbuf ? bC + (long long)r * sB : C0 + (tok0 + r) * sB;
+  }
+};
+
+template <typename T>
+__device__ __forceinline__ Rows<T> make_rows(const LaunchArgs& a, int slot, int h, int nbuf, long long tok0) {
+  const int g = h / (a.H / a.G);
+  Rows<T> r;
+  r.nbuf = nbuf;
+  r.sx = a.H * a.P;
+  r.sdt = a.H;
+  r.sB = a.G * a.N;
+  if (slot >= 0 && a.bx != nullptr) {
+    r.bx = (const T*)a.bx + ((size_t)slot * a.Q * a.H + h) * a.P;
+    r.bdt = a.bdt + (size_t)slot * a.Q * a.H + h;
+    r.bB = (const T*)a.bB + ((size_t)slot * a.Q * a.G + g) * a.N;
+    r.bC = (const T*)a.bC + ((size_t)slot * a.Q * a.G + g) * a.N;
+  } else {
+    r.bx = nullptr; r.bdt = nullptr; r.bB = nullptr; r.bC = nullptr;
+  }
+  r.x0 = (const T*)a.x + (size_t)h * a.P;
+  r.dt0 = a.dt + h;
+  r.B0 = (const T*)a.B + (size_t)g * a.N;
+  r.C0 = (const T*)a.C + (size_t)g * a.N;
+  r.tok0 = tok0;
+  return r;
+}
+
+// Loads rows [0, nrows) (x as fp32, delta, dA, B/C row pointers), zeroes the rest, and scans the
+// log-decays.  All kThreads threads must call it.
+template <typename T, int P>
+__device__ void load_rows(FmaSmem& sm, float* xs, int nrows, const Rows<T>& rows, float A, float bias) {
+  const int tid = threadIdx.x;
+  if (tid < kQMax) {
+    if (tid < nrows) {
+      const float d = delta_of(rows.dt(tid), bias);
+      sm.delta[tid] = d;
+      sm.hi[tid] = __fmul_rn(d, A);
+      sm.rowB[tid] = rows.B(tid);
+      sm.rowC[tid] = rows.C(tid);
+    } else {
+      sm.delta[tid] = 0.f;
+      sm.hi[tid] = 0.f;
+      sm.rowB[tid] = nullptr;
+      sm.rowC[tid] = nullptr;
+    }
+    sm.lo[tid] = 0.f;
+  }
+  for (int idx = tid; idx < nrows * P; idx += kThreads) {
+    const int r = idx / P, d = idx % P;
+    xs[idx] = to_f(rows.x(r)[d]);
+  }
+  __syncthreads();
+  chunk_scan(sm.hi, sm.lo);
+}
+
+// y for chunk row t (all kThreads threads call it).  Hd points at the [P x N] boundary state (fp32
+// checkpoint/anchor, or the bf16 read copy).  out points at the row's P outputs.
+template <typename T, int P, int N, typename HT>
+__device__ void row_output(FmaSmem& sm, const float* xs, int t, const HT* __restrict__ Hd, float Dh, T* out) {
+  using Dt = Dot<N>;
+  constexpr int NG = kThreads / Dt::W;
+  const int tid = threadIdx.x;
+  const int gid = tid / Dt::W, j = tid % Dt::W;
+  float c[Dt::K];
+  load_k<T, Dt::K>((const T*)sm.rowC[t] + j * Dt::K, c);
+  const df at = {sm.hi[t], sm.lo[t]};
+  // masked, decayed Gram column M[s] = (C_t . B_s) delta_s exp(Acum_t - Acum_s), s <= t
+  for (int s0 = 0; s0 <= t; s0 += NG) {
+    const int s = s0 + gid;
+    float b[Dt::K];
+    if (s <= t) {
+      load_k<T, Dt::K>((const T*)sm.rowB[s] + j * Dt::K, b);
+    } else {
+#pragma unroll
+      for (int k = 0; k < Dt::K; ++k) b[k] = 0.f;
+    }
+    const float g = Dt::reduce(Dt::partial(c, b));
+    if (s <= t && j == 0)
+      sm.M[s] = __fmul_rn(__fmul_rn(g, sm.delta[s]), expf(df_diff(at, df{sm.hi[s], sm.lo[s]})));
+  }
+  // off-diagonal term H C_t, one dot product per headdim row
+  for (int d0 = 0; d0 < P; d0 += NG) {
+    const int d = d0 + gid;
+    float hv[Dt::K];
+    if (d < P) {
+      load_k<HT, Dt::K>(Hd + (size_t)d * N + j * Dt::K, hv);
+    } else {
+#pragma unroll
+      for (int k = 0; k < Dt::K; ++k) hv[k] = 0.f;
+    }
+    const float v = Dt::reduce(Dt::partial(c, hv));
+    if (d < P && j == 0) sm.yoff[d] = v;
+  }
+  __syncthreads();
+  if (tid < P) {
+    float acc = 0.f;
+    for (int s = 0; s <= t; ++s) acc = __fmaf_rn(sm.M[s], xs[s * P + tid], acc);
+    out[tid] = from_f<T>(combine_out(expf(at.hi), sm.yoff[tid], acc, Dh, xs[t * P + tid]));
+  }
+  __syncthreads();
+}
+
+// Chunk-state weights w_s = delta_s exp(Acum_last - Acum_s) for s < nrows.
+__device__ __forceinline__ void state_weights(FmaSmem& sm, int nrows) {
+  const int tid = threadIdx.x;
+  if (tid < nrows) {
+    const df last = {sm.hi[nrows - 1], sm.lo[nrows - 1]};
+    sm.w[tid] = __fmul_rn(sm.delta[tid], expf(df_diff(last, df{sm.hi[tid], sm.lo[tid]})));
+  }
+  __syncthreads();
+}
+
+// S[d][n] = sum_{s < nrows} (w_s x_s[d]) B_s[n], in s order.  Thread tid owns elements
+// tid + e*kThreads (row-major [P][N]).
+template <typename T, int P, int N>
+__device__ __forceinline__ void chunk_state(const FmaSmem& sm, const float* xs, int nrows,
+                                            float (&acc)[P * N / kThreads]) {
+  constexpr int EPT = P * N / kThreads;
+  const int tid = threadIdx.x;
+#pragma unroll
+  for (int e = 0; e < EPT; ++e) acc[e] = 0.f;
+  for (int s = 0; s < nrows; ++s) {
+    const T* b = (const T*)sm.rowB[s];
+    const float ws = sm.w[s];
+#pragma unroll
+    for (int e = 0; e < EPT; ++e) {
+      const int idx = tid + e * kThreads;
+      const int d = idx / N, n = idx % N;
+      acc[e] = __fmaf_rn(__fmul_rn(ws, xs[s * P + d]), to_f(b[n]), acc[e]);
+    }
+  }
+}
+
+// H' = exp(Acum_last) H + S written over H (fp32) and, if present, the bf16 read copy cast from the
+// same fp32 value (ReplaySSM "Core equations": both copies cast independently from one state).
+template <int P, int N>
+__device__ __forceinline__ void fold_state(float* Hd, __nv_bfloat16* Rd, float decay, const float (&S)[P * N / kThreads]) {
+  constexpr int EPT = P * N / kThreads;
+  const int tid = threadIdx.x;
+#pragma unroll
+  for (int e = 0; e < EPT; ++e) {
+    const int idx = tid + e * kThreads;
+    const float v = __fmaf_rn(decay, Hd[idx], S[e]);
+    Hd[idx] = v;
+    if (Rd != nullptr) Rd[idx] = __float2bfloat16_rn(v);
+  }
+}
+
+__device__ __forceinline__ bool resolve_slot(const LaunchArgs& a, int i, int* slot) {
+  const int s = a.slot != nullptr ? a.slot[i] : i;
+  if (s < 0 || s >= a.nslots) {
+    if (threadIdx.x == 0) report(a.status, ERS_ESLOT);
+    return false;
+  }
+  *slot = s;
+  return true;
+}
+
+// Boundary-anchored chunk grid of sequence i: buffered p rows then the new tokens.
+struct SeqGrid {
+  int slot, p, len, total, nch;
+};
+
+__device__ __forceinline__ bool seq_grid(const LaunchArgs& a, bool chunked, int i, SeqGrid* g) {
+  g->slot = -1;
+  g->p = 0;
+  if (chunked) {
+    if (!resolve_slot(a, i, &g->slot)) return false;
+    g->p = a.pos[g->slot];
+    if (g->p < 0 || g->p >= a.Q) {
+      if (threadIdx.x == 0) report(a.status, ERS_EALIGN);
+      return false;
+    }
+  }
+  g->len = a.cu[i + 1] - a.cu[i];
+  g->total = g->p + g->len;
+  g->nch = (g->total + a.Q - 1) / a.Q;
+  return true;
+}
+
+extern __shared__ __align__(16) unsigned char dyn_smem[];
+
+__device__ __forceinline__ FmaSmem& smem_hdr() { return *reinterpret_cast<FmaSmem*>(dyn_smem); }
+__device__ __forceinline__ float* smem_xs() {
+  return reinterpret_cast<float*>(dyn_smem + ((sizeof(FmaSmem) + 15) & ~size_t(15)));
+}
+
+// ---- prefill: chunk states -------------------------------------------------------------------
+template <typename T, int P, int N>
+__global__ void __launch_bounds__(kThreads) k_prefill_state(LaunchArgs a, bool chunked) {
+  const int c = blockIdx.x, i = blockIdx.y, h = blockIdx.z;
+  SeqGrid sg;
+  if (!seq_grid(a, chunked, i, &sg) || c >= sg.nch) return;
+  FmaSmem& sm = smem_hdr();
+  float* xs = smem_xs();
+  const int nrows = min(a.Q, sg.total - c * a.Q);
+  const int nbuf = max(0, sg.p - c * a.Q);
+  const Rows<T> rows = make_rows<T>(a, sg.slot, h, nbuf, (long long)a.cu[i] + (long long)c * a.Q - sg.p);
+  load_rows<T, P>(sm, xs, nrows, rows, a.A[h], a.dt_bias[h]);
+  state_weights(sm, nrows);
+  float S[P * N / kThreads];
+  chunk_state<T, P, N>(sm, xs, nrows, S);
+  const size_t base = (((size_t)i * a.max_chunks + c) * a.H + h);
+  float* out = a.ws_states + base * P * N;
+#pragma unroll
+  for (int e = 0; e < P * N / kThreads; ++e) out[threadIdx.x + e * kThreads] = S[e];
+  if (threadIdx.x == 0) a.ws_tot[base] = sm.hi[nrows - 1];
+}
+
+// ---- prefill: inter-chunk state passing in fp32 (RFC Evidence 4: the state stays fp32 inside one
+// call and is rounded only on store; here it is never rounded) ----------------------------------
+template <int P, int N>
+__global__ void __launch_bounds__(kThreads) k_prefill_chain(LaunchArgs a, bool chunked) {
+  const int i = blockIdx.x, h = blockIdx.y;
+  SeqGrid sg;
+  if (!seq_grid(a, chunked, i, &sg)) return;
+  constexpr int EPT = P * N / kThreads;
+  const size_t hs = (size_t)P * N;
+  float* ckpt = chunked ? a.state + ((size_t)sg.slot * a.H + h) * hs : nullptr;
+  const float* init = chunked ? ckpt : (a.init_state ? a.init_state + ((size_t)i * a.H + h) * hs : nullptr);
+  float Hr[EPT], keep[EPT];
+#pragma unroll
+  for (int e = 0; e < EPT; ++e) {
+    Hr[e] = init ? init[threadIdx.x + e * kThreads] : 0.f;
+    keep[e] = Hr[e];
+  }
+  const bool aligned_end = (sg.total % a.Q) == 0;
+  for (int c = 0; c < sg.nch; ++c) {
+    const size_t base = ((size_t)i * a.max_chunks + c) * a.H + h;
+    float* S = a.ws_states + base * hs;
+    const float decay = expf(a.ws_tot[base]);
+    if (c == sg.nch - 1 && !aligned_end) {
+#pragma unroll
+      for (int e = 0; e < EPT; ++e) keep[e] = Hr[e];
+    }
+#pragma unroll
+    for (int e = 0; e < EPT; ++e) {
+      const int idx = threadIdx.x + e * kThreads;
+      const float s = S[idx];
+      S[idx] = Hr[e];  // the state at the start of chunk c, read by the output kernel
+      Hr[e] = __fmaf_rn(decay, Hr[e], s);
+    }
+    if (a.chunk_states != nullptr) {
+      float* cs = a.chunk_states + base * hs;
+#pragma unroll
+      for (int e = 0; e < EPT; ++e) cs[threadIdx.x + e * kThreads] = Hr[e];
+    }
+  }
+  if (!chunked) {
+    float* fin = a.final_state + ((size_t)i * a.H + h) * hs;
+#pragma unroll
+    for (int e = 0; e < EPT; ++e) fin[threadIdx.x + e * kThreads] = Hr[e];
+  } else if (sg.nch > 0) {
+#pragma unroll
+    for (int e = 0; e < EPT; ++e) ckpt[threadIdx.x + e * kThreads] = aligned_end ? Hr[e] : keep[e];
+  }
+}
+
+// ---- prefill: outputs ---------------------------------------------------------------------------
+template <typename T, int P, int N>
+__global__ void __launch_bounds__(kThreads) k_prefill_out(LaunchArgs a, bool chunked) {
+  const int c = blockIdx.x, i = blockIdx.y, h = blockIdx.z;
+  SeqGrid sg;
+  if (!seq_grid(a, chunked, i, &sg) || c >= sg.nch) return;
+  FmaSmem& sm = smem_hdr();
+  float* xs = smem_xs();
+  const int nrows = min(a.Q, sg.total - c * a.Q);
+  const int nbuf = max(0, sg.p - c * a.Q);
+  const long long tok0 = (long long)a.cu[i] + (long long)c * a.Q - sg.p;
+  const Rows<T> rows = make_rows<T>(a, sg.slot, h, nbuf, tok0);
+  load_rows<T, P>(sm, xs, nrows, rows, a.A[h], a.dt_bias[h]);
+  const float* Hc = a.ws_states + (((size_t)i * a.max_chunks + c) * a.H + h) * P * N;
+  const float Dh = a.D[h];
+  T* y = (T*)a.y;
+  for (int t = nbuf; t < nrows; ++t)
+    row_output<T, P, N, float>(sm, xs, t, Hc, Dh, y + ((tok0 + t) * a.H + h) * P);
+}
+
+// ---- replay decode --------------------------------------------------------------------------------
+template <typename T, int P, int N>
+__global__ void __launch_bounds__(kThreads) k_decode(LaunchArgs a) {
+  const int i = blockIdx.x, h = blockIdx.y;
+  int slot;
+  if (!resolve_slot(a, i, &slot)) return;
+  const bool rssm = (a.flags & ERS_FLAG_REPLAYSSM) != 0;
+  const int p = a.pos[slot];
+  if (p < 0 || p >= a.Q) {
+    if (threadIdx.x == 0) report(a.status, ERS_EALIGN);
+    return;
+  }
+  FmaSmem& sm = smem_hdr();
+  float* xs = smem_xs();
+  // rows 0..p-1 from the buffer, row p is the new token (input index i == tok0 + p)
+  const Rows<T> rows = make_rows<T>(a, slot, h, p, (long long)i - p);
+  load_rows<T, P>(sm, xs, p + 1, rows, a.A[h], a.dt_bias[h]);
+  const size_t hs = (size_t)P * N;
+  float* Hd = a.state + ((size_t)slot * a.H + h) * hs;
+  T* y = (T*)a.y + ((size_t)i * a.H + h) * P;
+  if (rssm)
+    row_output<T, P, N, __nv_bfloat16>(sm, xs, p, (const __nv_bfloat16*)a.read_copy + ((size_t)slot * a.H + h) * hs,
+                                       a.D[h], y);
+  else
+    row_output<T, P, N, float>(sm, xs, p, Hd, a.D[h], y);
+  // append the new token to the buffer (B/C once per group)
+  const int g = h / (a.H / a.G);
+  T* bx = (T*)a.bx + (((size_t)slot * a.Q + p) * a.H + h) * P;
+  const T* nx = (const T*)a.x + ((size_t)i * a.H + h) * P;
+  for (int d = threadIdx.x; d < P; d += kThreads) bx[d] = nx[d];
+  if (threadIdx.x == 0) a.bdt[((size_t)slot * a.Q + p) * a.H + h] = a.dt[(size_t)i * a.H + h];
+  if (h % (a.H / a.G) == 0) {
+    T* bB = (T*)a.bB + (((size_t)slot * a.Q + p) * a.G + g) * N;
+    T* bC = (T*)a.bC + (((size_t)slot * a.Q + p) * a.G + g) * N;
+    const T* nB = (const T*)a.B + ((size_t)i * a.G + g) * N;
+    const T* nC = (const T*)a.C + ((size_t)i * a.G + g) * N;
+    for (int n = threadIdx.x; n < N; n += kThreads) {
+      bB[n] = nB[n];
+      bC[n] = nC[n];
+    }
+  }
+  // the chunk filled: its final state becomes the new boundary state
+  if (!rssm && (a.flags & ERS_FLAG_FUSE_REFRESH) && p + 1 == a.Q) {
+    state_weights(sm, a.Q);
+    float S[P * N / kThreads];
+    chunk_state<T, P, N>(sm, xs, a.Q, S);
+    __nv_bfloat16* Rd = a.read_copy ? (__nv_bfloat16*)a.read_copy + ((size_t)slot * a.H + h) * hs : nullptr;
+    fold_state<P, N>(Hd, Rd, expf(sm.hi[a.Q - 1]), S);
+  }
+}
+
+// ---- refresh (exact: pos == Q; ReplaySSM: pos + T > L) ---------------------------------------------
+template <typename T, int P, int N>
+__global__ void __launch_bounds__(kThreads) k_refresh(LaunchArgs a) {
+  const int i = blockIdx.x, h = blockIdx.y;
+  int slot;
+  if (!resolve_slot(a, i, &slot)) return;
+  const bool rssm = (a.flags & ERS_FLAG_REPLAYSSM) != 0;
+  const int p = a.pos[slot];
+  if (p < 0 || p > a.Q) {
+    if (threadIdx.x == 0) report(a.status, ERS_EALIGN);
+    return;
+  }
+  const bool go = rssm ? (p + a.T > a.Q) : (p == a.Q);
+  if (!go) return;
+  const size_t hs = (size_t)P * N;
+  float* Hd = a.state + ((size_t)slot * a.H + h) * hs;
+  __nv_bfloat16* Rd = a.read_copy ? (__nv_bfloat16*)a.read_copy + ((size_t)slot * a.H + h) * hs : nullptr;
+  if (p == 0) {  // empty committed history: anchor unchanged, read copy recast from it
+    if (Rd != nullptr)
+      for (int idx = threadIdx.x; idx < P * N; idx += kThreads) Rd[idx] = __float2bfloat16_rn(Hd[idx]);
+    return;
+  }
+  FmaSmem& sm = smem_hdr();
+  float* xs = smem_xs();
+  const Rows<T> rows = make_rows<T>(a, slot, h, p, 0);
+  load_rows<T, P>(sm, xs, p, rows, a.A[h], a.dt_bias[h]);
+  state_weights(sm, p);
+  float S[P * N / kThreads];
+  chunk_state<T, P, N>(sm, xs, p, S);
+  fold_state<P, N>(Hd, Rd, expf(sm.hi[p - 1]), S);
+}
+
+// ---- speculative verify --------------------------------------------------------------------------
+// Launch 1: slots whose committed pointer would overflow fold their committed records first.
+template <typename T, int P, int N>
+__global__ void __launch_bounds__(kThreads) k_verify_flush(LaunchArgs a) {
+  const int i = blockIdx.x, h = blockIdx.y;
+  int slot;
+  if (!resolve_slot(a, i, &slot)) return;
+  const int hc = a.pos[slot];
+  if (hc < 0 || hc > a.Q) {
+    if (threadIdx.x == 0) report(a.status, ERS_EALIGN);
+    return;
+  }
+  if (hc + a.T <= a.Q) return;
+  if (!(a.flags & ERS_FLAG_AUTO_FLUSH)) {
+    if (threadIdx.x == 0) report(a.status, ERS_EOVERFLOW);
+    return;
+  }
+  const size_t hs = (size_t)P * N;
+  float* Hd = a.state + ((size_t)slot * a.H + h) * hs;
+  __nv_bfloat16* Rd = (__nv_bfloat16*)a.read_copy + ((size_t)slot * a.H + h) * hs;
+  FmaSmem& sm = smem_hdr();
+  float* xs = smem_xs();
+  const Rows<T> rows = make_rows<T>(a, slot, h, hc, 0);
+  load_rows<T, P>(sm, xs, hc, rows, a.A[h], a.dt_bias[h]);
+  state_weights(sm, hc);
+  float S[P * N / kThreads];
+  chunk_state<T, P, N>(sm, xs, hc, S);
+  fold_state<P, N>(Hd, Rd, expf(sm.hi[hc - 1]), S);
+}
+
+// Launch 2: drafts go to buffer rows [h', h'+T); outputs for each draft from the read copy.
+template <typename T, int P, int N>
+__global__ void __launch_bounds__(kThreads) k_verify(LaunchArgs a) {
+  const int i = blockIdx.x, h = blockIdx.y;
+  int slot;
+  if (!resolve_slot(a, i, &slot)) return;
+  const int hc = a.pos[slot];
+  if (hc < 0 || hc > a.Q) return;  // reported by the flush launch
+  int h0 = hc;
+  if (hc + a.T > a.Q) {
+    if (!(a.flags & ERS_FLAG_AUTO_FLUSH)) return;
+    h0 = 0;
+  }
+  FmaSmem& sm = smem_hdr();
+  float* xs = smem_xs();
+  // rows [0, h0) committed (buffer), rows [h0, h0+T) the drafts: input token i*T + (r - h0)
+  const Rows<T> rows = make_rows<T>(a, slot, h, h0, (long long)i * a.T - h0);
+  const int nrows = h0 + a.T;
+  load_rows<T, P>(sm, xs, nrows, rows, a.A[h], a.dt_bias[h]);
+  const size_t hs = (size_t)P * N;
+  const __nv_bfloat16* Rd = (const __nv_bfloat16*)a.read_copy + ((size_t)slot * a.H + h) * hs;
+  T* y = (T*)a.y;
+  for (int j = 0; j < a.T; ++j)
+    row_output<T, P, N, __nv_bfloat16>(sm, xs, h0 + j, Rd, a.D[h], y + (((size_t)i * a.T + j) * a.H + h) * P);
+  // write the drafts into the buffer
+  const int g = h / (a.H / a.G);
+  for (int idx = threadIdx.x; idx < a.T * P; idx += kThreads) {
+    const int j = idx / P, d = idx % P;
+    ((T*)a.bx)[(((size_t)slot * a.Q + h0 + j) * a.H + h) * P + d] =
+        ((const T*)a.x)[(((size_t)i * a.T + j) * a.H + h) * P + d];
+  }
+  for (int j = threadIdx.x; j < a.T; j += kThreads)
+    a.bdt[((size_t)slot * a.Q + h0 + j) * a.H + h] = a.dt[((size_t)i * a.T + j) * a.H + h];
+  if (h % (a.H / a.G) == 0) {
+    for (int idx = threadIdx.x; idx < a.T * N; idx += kThreads) {
+      const int j = idx / N, n = idx % N;
+      const size_t dst = (((size_t)slot * a.Q + h0 + j) * a.G + g) * N + n;
+      const size_t src = (((size_t)i * a.T + j) * a.G + g) * N + n;
+      ((T*)a.bB)[dst] = ((const T*)a.B)[src];
+      ((T*)a.bC)[dst] = ((const T*)a.C)[src];
+    }
+  }
+}
+
+// ---- pointer-only kernels ---------------------------------------------------------------------------
+// Runs after the compute launch of the same call, so every head of a slot has read the old pos.
+__global__ void k_setpos(LaunchArgs a, int kind) {
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= a.nseq) return;
+  const int slot = a.slot != nullptr ? a.slot[i] : i;
+  if (slot < 0 || slot >= a.nslots) return;
+  const int p = a.pos[slot];
+  const bool rssm = (a.flags & ERS_FLAG_REPLAYSSM) != 0;
+  if (kind == 0) {  // after a decode step
+    if (p < 0 || p >= a.Q) return;
+    a.pos[slot] = (!rssm && (a.flags & ERS_FLAG_FUSE_REFRESH) && p + 1 == a.Q) ? 0 : p + 1;
+  } else {  // after a refresh
+    if (p < 0 || p > a.Q) return;
+    const bool go = rssm ? (p + a.T > a.Q) : (p == a.Q);
+    if (go) a.pos[slot] = 0;
+  }
+}
+
+__global__ void k_commit(LaunchArgs a) {
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= a.nseq) return;
+  const int slot = a.slot != nullptr ? a.slot[i] : i;
+  if (slot < 0 || slot >= a.nslots) {
+    report(a.status, ERS_ESLOT);
+    return;
+  }
+  const int hc = a.pos[slot];
+  const int acc = a.accepted[i];
+  if (acc < 0 || acc > a.T) {
+    report(a.status, ERS_ECOMMIT);
+    return;
+  }
+  if (hc < 0 || hc > a.Q) {
+    report(a.status, ERS_EALIGN);
+    return;
+  }
+  const bool overflow = hc + a.T > a.Q;
+  if (overflow && !(a.flags & ERS_FLAG_AUTO_FLUSH)) {
+    report(a.status, ERS_EOVERFLOW);
+    return;
+  }
+  a.pos[slot] = (overflow ? 0 : hc) + acc;
+}
+
+// Chunked prefill epilogue: the trailing partial chunk's inputs go to the buffer and pos advances.
+template <typename T>
+__global__ void k_tail(LaunchArgs a) {
+  const int i = blockIdx.x;
+  SeqGrid sg;
+  if (!seq_grid(a, true, i, &sg)) return;
+  const int nfull = sg.total / a.Q;
+  const int rem = sg.total - nfull * a.Q;
+  const int HP = a.H * a.P, GN = a.G * a.N;
+  for (int r = 0; r < rem; ++r) {
+    const int rs = nfull * a.Q + r;  // stream position
+    if (rs < sg.p) continue;          // already buffered at row r (only when nfull == 0)
+    const size_t tok = (size_t)a.cu[i] + (rs - sg.p);
+    const size_t brow = (size_t)sg.slot * a.Q + r;
+    for (int k = threadIdx.x; k < HP; k += blockDim.x) ((T*)a.bx)[brow * HP + k] = ((const T*)a.x)[tok * HP + k];
+    for (int k = threadIdx.x; k < a.H; k += blockDim.x) a.bdt[brow * a.H + k] = a.dt[tok * a.H + k];
+    for (int k = threadIdx.x; k < GN; k += blockDim.x) {
+      ((T*)a.bB)[brow * GN + k] = ((const T*)a.B)[tok * GN + k];
+      ((T*)a.bC)[brow * GN + k] = ((const T*)a.C)[tok * GN + k];
+    }
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) a.pos[sg.slot] = rem;
+}
+
+// ---- host dispatch -------------------------------------------------------------------------------
+template <typename K>
+cudaError_t prep(K kernel, size_t smem) {
+  return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+}
+
+template <typename T, int P, int N>
+cudaError_t prefill_impl(const LaunchArgs& a, Op op, cudaStream_t s) {
+  const bool chunked = op == Op::kChunkedPrefill;
+  const size_t sm = fma_smem_bytes(a.Q, P);
+  cudaError_t e;
+  if ((e = prep(k_prefill_state<T, P, N>, sm)) != cudaSuccess) return e;
+  if ((e = prep(k_prefill_out<T, P, N>, sm)) != cudaSuccess) return e;
+  if (a.max_chunks > 0 && a.nseq > 0) {
+    dim3 grid(a.max_chunks, a.nseq, a.H);
+    k_prefill_state<T, P, N><<<grid, kThreads, sm, s>>>(a, chunked);
+    k_prefill_chain<P, N><<<dim3(a.nseq, a.H), kThreads, 0, s>>>(a, chunked);
+    k_prefill_out<T, P, N><<<grid, kThreads, sm, s>>>(a, chunked);
+  }
+  if (chunked && a.nseq > 0) k_tail<T><<<a.nseq, kThreads, 0, s>>>(a);
+  return cudaGetLastError();
+}
+
+template <typename T, int P, int N>
+cudaError_t decode_impl(const LaunchArgs& a, cudaStream_t s) {
+  const size_t sm = fma_smem_bytes(a.Q, P);
+  cudaError_t e = prep(k_decode<T, P, N>, sm);
+  if (e != cudaSuccess) return e;
+  k_decode<T, P, N><<<dim3(a.nseq, a.H), kThreads, sm, s>>>(a);
+  return launch_setpos(a, 0, s);
+}
+
+template <typename T, int P, int N>
+cudaError_t refresh_impl(const LaunchArgs& a, cudaStream_t s) {
+  const size_t sm = fma_smem_bytes(a.Q, P);
+  cudaError_t e = prep(k_refresh<T, P, N>, sm);
+  if (e != cudaSuccess) return e;
+  k_refresh<T, P, N><<<dim3(a.nseq, a.H), kThreads, sm, s>>>(a);
+  return launch_setpos(a, 1, s);
+}
+
+template <typename T, int P, int N>
+cudaError_t verify_impl(const LaunchArgs& a, cudaStream_t s) {
+  const size_t sm = fma_smem_bytes(a.Q, P);
+  cudaError_t e;
+  if ((e = prep(k_verify_flush<T, P, N>, sm)) != cudaSuccess) return e;
+  if ((e = prep(k_verify<T, P, N>, sm)) != cudaSuccess) return e;
+  k_verify_flush<T, P, N><<<dim3(a.nseq, a.H), kThreads, sm, s>>>(a);
+  k_verify<T, P, N><<<dim3(a.nseq, a.H), kThreads, sm, s>>>(a);
+  return cudaGetLastError();
+}
+
+// Supported (P, N) pairs of this engine.
+#define ERS_FMA_SHAPES(X) X(16, 16) X(32, 32) X(64, 64) X(64, 128)
+
+#define ERS_DISPATCH()                                                                               \
+  do {                                                                                               \
+    if (a.io == ERS_DTYPE_BF16) {                                                                    \
+      ERS_FMA_SHAPES(ERS_CASE_BF16)                                                                  \
+    } else {                                                                                         \
+      ERS_FMA_SHAPES(ERS_CASE_F32)                                                                   \
+    }                                                                                                \
+    return cudaErrorInvalidValue;                                                                    \
+  } while (0)
+
+}  // namespace
+
+bool fma_supported(int P, int N) {
+#define ERS_SUP(p_, n_) if (P == p_ && N == n_) return true;
+  ERS_FMA_SHAPES(ERS_SUP)
+#undef ERS_SUP
+  return false;
+}
+
+#define ERS_CASE_BF16(p_, n_) if (a.P == p_ && a.N == n_) return IMPL<__nv_bfloat16, p_, n_>(ERS_ARGS);
+#define ERS_CASE_F32(p_, n_) if (a.P == p_ && a.N == n_) return IMPL<float, p_, n_>(ERS_ARGS);
+
+cudaError_t fma_prefill(const LaunchArgs& a, Op op, cudaStream_t s) {
+#define IMPL prefill_impl
+#define ERS_ARGS a, op, s
+  ERS_DISPATCH();
+#undef IMPL
+#undef ERS_ARGS
+}
+
+cudaError_t fma_decode(const LaunchArgs& a, cudaStream_t s) {
+#define IMPL decode_impl
+#define ERS_ARGS a, s
+  ERS_DISPATCH();
+#undef IMPL
+#undef ERS_ARGS
+}
+
+cudaError_t fma_refresh(const LaunchArgs& a, cudaStream_t s) {
+#define IMPL refresh_impl
+#define ERS_ARGS a, s
+  ERS_DISPATCH();
+#undef IMPL
+#undef ERS_ARGS
+}
+
+cudaError_t fma_verify(const LaunchArgs& a, cudaStream_t s) {
+#define IMPL verify_impl
+#define ERS_ARGS a, s
+  ERS_DISPATCH();
+#undef IMPL
+#undef ERS_ARGS
+}
+
+cudaError_t launch_setpos(const LaunchArgs& a, int kind, cudaStream_t s) {
+  if (a.nseq > 0) k_setpos<<<(a.nseq + 255) / 256, 256, 0, s>>>(a, kind);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_commit(const LaunchArgs& a, cudaStream_t s) {
+  if (a.nseq > 0) k_commit<<<(a.nseq + 255) / 256, 256, 0, s>>>(a);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_tail(const LaunchArgs& a, cudaStream_t s) {
+  if (a.nseq <= 0) return cudaSuccess;
+  if (a.io == ERS_DTYPE_BF16)
+    k_tail<__nv_bfloat16><<<a.nseq, kThreads, 0, s>>>(a);
+  else
+    k_tail<float><<<a.nseq, kThreads, 0, s>>>(a);
+  return cudaGetLastError();
+}
+
+}  // namespace ers

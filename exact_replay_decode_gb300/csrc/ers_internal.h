@@ -1,0 +1,75 @@
+// Internal launch interface between the C-ABI layer (ers_api.cu) and the kernels.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "ers.h"
+
+namespace ers {
+
+constexpr int kQMaxHost = 256;  // largest chunk / refresh period (matches kQMax in ers_common.cuh)
+
+// Everything one launch needs; unused pointers are NULL.
+struct LaunchArgs {
+  // dims
+  int H, G, P, N, Q;
+  int io;  // ERS_DTYPE_*
+  // per-head parameters
+  const float* A;
+  const float* D;
+  const float* dt_bias;
+  // packed token inputs (prefill: [ntokens, ...]; decode: [nseq, ...]; verify: [nseq, T, ...])
+  const void* x;
+  const float* dt;
+  const void* B;
+  const void* C;
+  const int32_t* cu;  // prefill: [nseq+1]
+  int nseq;
+  int max_chunks;     // prefill grid bound
+  int T;              // verify: drafts per sequence; refresh: flush-rule T
+  uint32_t flags;
+  // cache
+  float* state;
+  void* read_copy;
+  void* bx;
+  float* bdt;
+  void* bB;
+  void* bC;
+  int32_t* pos;
+  const int32_t* slot;
+  int nslots;
+  // outputs / plain-scan state
+  void* y;
+  const float* init_state;
+  float* final_state;
+  float* chunk_states;
+  // workspace
+  float* ws_states;  // [nseq, max_chunks, H, P, N]
+  float* ws_tot;     // [nseq, max_chunks, H]
+  const int32_t* accepted;
+  int32_t* status;
+};
+
+enum class Op { kScan, kChunkedPrefill };
+
+// FMA (CUDA-core) engine, ers_fma.cu
+cudaError_t fma_prefill(const LaunchArgs& a, Op op, cudaStream_t s);
+cudaError_t fma_decode(const LaunchArgs& a, cudaStream_t s);
+cudaError_t fma_refresh(const LaunchArgs& a, cudaStream_t s);
+cudaError_t fma_verify(const LaunchArgs& a, cudaStream_t s);
+bool fma_supported(int P, int N);
+
+// pointer-only kernels, ers_fma.cu
+cudaError_t launch_setpos(const LaunchArgs& a, int kind, cudaStream_t s);  // kind: 0 decode, 1 refresh
+cudaError_t launch_commit(const LaunchArgs& a, cudaStream_t s);
+cudaError_t launch_tail(const LaunchArgs& a, cudaStream_t s);
+
+// SSU baseline, ers_ssu.cu
+cudaError_t ssu_update(const LaunchArgs& a, cudaStream_t s);
+bool ssu_supported(int P, int N);
+
+inline size_t align256(size_t v) { return (v + 255) & ~size_t(255); }
+
+}  // namespace ers

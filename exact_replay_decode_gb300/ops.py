@@ -1,0 +1,293 @@
+"""PyTorch-facing binding of the C ABI (include/ers.h).
+
+Marshalling only: every step of the hot path runs in the CUDA library.  PyTorch provides device
+memory, streams and shape/dtype checks; outputs and workspaces are allocated here with torch so
+the library itself never allocates.
+"""
+from __future__ import annotations
+
+import ctypes
+import dataclasses
+from typing import Optional, Sequence, Tuple, Union
+
+import torch
+
+from . import _abi
+
+_IO = {torch.bfloat16: _abi.DTYPE_BF16, torch.float32: _abi.DTYPE_F32}
+
+
+@dataclasses.dataclass
+class LayerParams:
+    """Per-head parameters, fp32 [H] on the device: A (< 0), D (skip) and dt_bias."""
+    A: torch.Tensor
+    D: torch.Tensor
+    dt_bias: torch.Tensor
+
+    def _c(self) -> _abi.Params:
+        for t in (self.A, self.D, self.dt_bias):
+            _need(t, torch.float32, "params")
+        return _abi.Params(self.A.data_ptr(), self.D.data_ptr(), self.dt_bias.data_ptr())
+
+
+def _need(t: torch.Tensor, dtype, name: str, shape: Optional[Sequence[int]] = None) -> None:
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name}: expected a torch.Tensor")
+    if t.device.type != "cuda":
+        raise ValueError(f"{name}: must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name}: dtype {t.dtype}, expected {dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name}: must be contiguous")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name}: shape {tuple(t.shape)}, expected {tuple(shape)}")
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    return None if t is None else t.data_ptr()
+
+
+def _stream(stream: Optional[torch.cuda.Stream]) -> int:
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return s.cuda_stream
+
+
+class Status:
+    """Device int32 status word the kernels report into; read() synchronises."""
+
+    def __init__(self, device=None):
+        self.t = torch.zeros(1, dtype=torch.int32, device=device or "cuda")
+
+    def ptr(self) -> int:
+        return self.t.data_ptr()
+
+    def reset(self) -> None:
+        self.t.zero_()
+
+    def read(self) -> int:
+        return int(self.t.item())
+
+    def raise_if_error(self, where: str) -> None:
+        code = self.read()
+        if code != 0:
+            raise _abi.ErsError(code, where)
+
+
+def _finish(code: int, where: str, status: Optional[Status], check: bool) -> None:
+    _abi.check(code, where)
+    if check and status is not None:
+        status.raise_if_error(where)
+
+
+def _dims(H: int, G: int, P: int, N: int, Q: int, io: torch.dtype) -> _abi.Dims:
+    if io not in _IO:
+        raise TypeError(f"io dtype {io} not supported (bf16 or fp32)")
+    return _abi.Dims(H, G, P, N, Q, _IO[io])
+
+
+def _io_from(x: torch.Tensor) -> torch.dtype:
+    if x.dtype not in _IO:
+        raise TypeError(f"x dtype {x.dtype} not supported (bf16 or fp32)")
+    return x.dtype
+
+
+def _max_len(cu_seqlens: torch.Tensor, max_seqlen: Optional[int]) -> int:
+    if max_seqlen is not None:
+        return int(max_seqlen)
+    lens = (cu_seqlens[1:] - cu_seqlens[:-1]).max() if cu_seqlens.numel() > 1 else torch.zeros(())
+    return int(lens.item())
+
+
+# ------------------------------------------------------------------------------------------------
+def ssd_scan_fwd(x: torch.Tensor, dt: torch.Tensor, params: LayerParams, B: torch.Tensor, C: torch.Tensor,
+                 chunk: int, cu_seqlens: Optional[torch.Tensor] = None, init_state: Optional[torch.Tensor] = None,
+                 return_chunk_states: bool = False, max_seqlen: Optional[int] = None,
+                 status: Optional[Status] = None, check: bool = True, stream=None,
+                 out: Optional[Tuple[torch.Tensor, torch.Tensor]] = None, workspace: Optional[torch.Tensor] = None):
+    """Chunked SSD prefill over packed varlen sequences (ers_ssd_scan_fwd).
+
+    x [T,H,P], dt [T,H] fp32 raw, B/C [T,G,N]; cu_seqlens int32 [S+1] (default: one sequence).
+    Returns (y [T,H,P], final_state [S,H,P,N] fp32[, chunk_states [S,ceil(max_seqlen/Q),H,P,N]]).
+    """
+    io = _io_from(x)
+    T, H, P = x.shape
+    G, N = B.shape[1], B.shape[2]
+    dev = x.device
+    if cu_seqlens is None:
+        cu_seqlens = torch.tensor([0, T], dtype=torch.int32, device=dev)
+    S = cu_seqlens.numel() - 1
+    _need(x, io, "x", (T, H, P)); _need(dt, torch.float32, "dt", (T, H))
+    _need(B, io, "B", (T, G, N)); _need(C, io, "C", (T, G, N)); _need(cu_seqlens, torch.int32, "cu_seqlens")
+    if init_state is not None:
+        _need(init_state, torch.float32, "init_state", (S, H, P, N))
+    ms = _max_len(cu_seqlens, max_seqlen)
+    dims = _dims(H, G, P, N, chunk, io)
+    if out is None:
+        y = torch.empty_like(x)
+        fin = torch.empty(S, H, P, N, dtype=torch.float32, device=dev)
+    else:
+        y, fin = out
+    cs = None
+    if return_chunk_states:
+        cs = torch.empty(S, (ms + chunk - 1) // chunk, H, P, N, dtype=torch.float32, device=dev)
+    L = _abi.lib()
+    wsz = L.ers_ssd_scan_fwd_workspace_size(ctypes.byref(dims), S, ms)
+    if workspace is None or workspace.numel() < wsz:
+        workspace = torch.empty(max(wsz, 1), dtype=torch.uint8, device=dev)
+    st = status if status is not None else (Status(dev) if check else None)
+    code = L.ers_ssd_scan_fwd(ctypes.byref(dims), ctypes.byref(params._c()), S, T, ms, cu_seqlens.data_ptr(),
+                              x.data_ptr(), dt.data_ptr(), B.data_ptr(), C.data_ptr(), _ptr(init_state),
+                              y.data_ptr(), fin.data_ptr(), _ptr(cs), workspace.data_ptr(), workspace.numel(),
+                              _stream(stream), _ptr(st.t) if st else None)
+    _finish(code, "ers_ssd_scan_fwd", st, check)
+    return (y, fin, cs) if return_chunk_states else (y, fin)
+
+
+# ------------------------------------------------------------------------------------------------
+class ReplayCache:
+    """Per-slot exact-replay / ReplaySSM state: fp32 checkpoint (anchor), optional bf16 read copy,
+    token-major partial-chunk buffers of (x, raw dt, B, C) and the per-slot position."""
+
+    def __init__(self, nslots: int, nheads: int, ngroups: int, headdim: int, dstate: int, chunk: int,
+                 io_dtype: torch.dtype = torch.bfloat16, read_copy: bool = False, device="cuda"):
+        self.nslots, self.H, self.G, self.P, self.N, self.Q = nslots, nheads, ngroups, headdim, dstate, chunk
+        self.io = io_dtype
+        z = dict(device=device)
+        self.state = torch.zeros(nslots, nheads, headdim, dstate, dtype=torch.float32, **z)
+        self.read_copy = torch.zeros(nslots, nheads, headdim, dstate, dtype=torch.bfloat16, **z) if read_copy else None
+        self.buf_x = torch.zeros(nslots, chunk, nheads, headdim, dtype=io_dtype, **z)
+        self.buf_dt = torch.zeros(nslots, chunk, nheads, dtype=torch.float32, **z)
+        self.buf_B = torch.zeros(nslots, chunk, ngroups, dstate, dtype=io_dtype, **z)
+        self.buf_C = torch.zeros(nslots, chunk, ngroups, dstate, dtype=io_dtype, **z)
+        self.pos = torch.zeros(nslots, dtype=torch.int32, **z)
+
+    @property
+    def dims(self) -> _abi.Dims:
+        return _dims(self.H, self.G, self.P, self.N, self.Q, self.io)
+
+    def _c(self) -> _abi.Cache:
+        return _abi.Cache(self.state.data_ptr(), _ptr(self.read_copy), self.buf_x.data_ptr(), self.buf_dt.data_ptr(),
+                          self.buf_B.data_ptr(), self.buf_C.data_ptr(), self.pos.data_ptr(), self.nslots)
+
+    def nbytes(self) -> int:
+        ts = [self.state, self.buf_x, self.buf_dt, self.buf_B, self.buf_C, self.pos]
+        if self.read_copy is not None:
+            ts.append(self.read_copy)
+        return sum(t.numel() * t.element_size() for t in ts)
+
+
+def _tok_checks(cache: ReplayCache, x, dt, B, C, lead: Tuple[int, ...]):
+    _need(x, cache.io, "x", lead + (cache.H, cache.P)); _need(dt, torch.float32, "dt", lead + (cache.H,))
+    _need(B, cache.io, "B", lead + (cache.G, cache.N)); _need(C, cache.io, "C", lead + (cache.G, cache.N))
+
+
+def _slot_arg(slot: Optional[torch.Tensor], nseq: int):
+    if slot is None:
+        return None
+    _need(slot, torch.int32, "slot", (nseq,))
+    return slot.data_ptr()
+
+
+def chunked_prefill(cache: ReplayCache, params: LayerParams, x, dt, B, C, cu_seqlens: Optional[torch.Tensor] = None,
+                    slot: Optional[torch.Tensor] = None, max_seqlen: Optional[int] = None,
+                    status: Optional[Status] = None, check: bool = True, stream=None,
+                    workspace: Optional[torch.Tensor] = None) -> torch.Tensor:
+    """Boundary-anchored (chunked) prefill into the cache (ers_chunked_prefill); returns y of the new tokens."""
+    T = x.shape[0]
+    if cu_seqlens is None:
+        cu_seqlens = torch.tensor([0, T], dtype=torch.int32, device=x.device)
+    S = cu_seqlens.numel() - 1
+    _tok_checks(cache, x, dt, B, C, (T,))
+    _need(cu_seqlens, torch.int32, "cu_seqlens")
+    ms = _max_len(cu_seqlens, max_seqlen)
+    y = torch.empty_like(x)
+    L = _abi.lib()
+    dims = cache.dims
+    wsz = L.ers_chunked_prefill_workspace_size(ctypes.byref(dims), S, ms)
+    if workspace is None or workspace.numel() < wsz:
+        workspace = torch.empty(max(wsz, 1), dtype=torch.uint8, device=x.device)
+    st = status if status is not None else (Status(x.device) if check else None)
+    code = L.ers_chunked_prefill(ctypes.byref(dims), ctypes.byref(params._c()), ctypes.byref(cache._c()), S, T, ms,
+                                 cu_seqlens.data_ptr(), _slot_arg(slot, S), x.data_ptr(), dt.data_ptr(),
+                                 B.data_ptr(), C.data_ptr(), y.data_ptr(), workspace.data_ptr(), workspace.numel(),
+                                 _stream(stream), _ptr(st.t) if st else None)
+    _finish(code, "ers_chunked_prefill", st, check)
+    return y
+
+
+def replay_decode(cache: ReplayCache, params: LayerParams, x, dt, B, C, slot: Optional[torch.Tensor] = None,
+                  fuse_refresh: bool = True, replayssm: bool = False, status: Optional[Status] = None,
+                  check: bool = True, stream=None, out: Optional[torch.Tensor] = None) -> torch.Tensor:
+    """One exact-replay decode step per sequence (ers_replay_decode).  x [S,H,P], dt [S,H], B/C [S,G,N]."""
+    S = x.shape[0]
+    _tok_checks(cache, x, dt, B, C, (S,))
+    y = torch.empty_like(x) if out is None else out
+    flags = (_abi.FLAG_REPLAYSSM if replayssm else (_abi.FLAG_FUSE_REFRESH if fuse_refresh else 0))
+    st = status if status is not None else (Status(x.device) if check else None)
+    code = _abi.lib().ers_replay_decode(ctypes.byref(cache.dims), ctypes.byref(params._c()), ctypes.byref(cache._c()),
+                                        S, _slot_arg(slot, S), x.data_ptr(), dt.data_ptr(), B.data_ptr(),
+                                        C.data_ptr(), flags, y.data_ptr(), _stream(stream),
+                                        _ptr(st.t) if st else None)
+    _finish(code, "ers_replay_decode", st, check)
+    return y
+
+
+def refresh(cache: ReplayCache, params: LayerParams, nseq: Optional[int] = None, slot: Optional[torch.Tensor] = None,
+            replayssm: bool = False, drafts_T: int = 0, status: Optional[Status] = None, check: bool = True,
+            stream=None) -> None:
+    """Checkpoint refresh (ers_refresh): exact mode folds full chunks; ReplaySSM mode applies h + T > L."""
+    S = cache.nslots if nseq is None else nseq
+    st = status if status is not None else (Status(cache.state.device) if check else None)
+    code = _abi.lib().ers_refresh(ctypes.byref(cache.dims), ctypes.byref(params._c()), ctypes.byref(cache._c()), S,
+                                  _slot_arg(slot, S), _abi.FLAG_REPLAYSSM if replayssm else 0, int(drafts_T),
+                                  _stream(stream), _ptr(st.t) if st else None)
+    _finish(code, "ers_refresh", st, check)
+
+
+def spec_verify(cache: ReplayCache, params: LayerParams, x, dt, B, C, slot: Optional[torch.Tensor] = None,
+                auto_flush: bool = True, status: Optional[Status] = None, check: bool = True, stream=None,
+                out: Optional[torch.Tensor] = None) -> torch.Tensor:
+    """Output-only speculative verify of T drafts per sequence (ers_spec_verify).  x [S,T,H,P] ..."""
+    S, T = x.shape[0], x.shape[1]
+    _tok_checks(cache, x, dt, B, C, (S, T))
+    y = torch.empty_like(x) if out is None else out
+    st = status if status is not None else (Status(x.device) if check else None)
+    code = _abi.lib().ers_spec_verify(ctypes.byref(cache.dims), ctypes.byref(params._c()), ctypes.byref(cache._c()),
+                                      S, _slot_arg(slot, S), T, x.data_ptr(), dt.data_ptr(), B.data_ptr(),
+                                      C.data_ptr(), _abi.FLAG_AUTO_FLUSH if auto_flush else 0, y.data_ptr(),
+                                      _stream(stream), _ptr(st.t) if st else None)
+    _finish(code, "ers_spec_verify", st, check)
+    return y
+
+
+def commit(cache: ReplayCache, accepted: torch.Tensor, T: int, slot: Optional[torch.Tensor] = None,
+           auto_flush: bool = True, status: Optional[Status] = None, check: bool = True, stream=None) -> None:
+    """Advance the committed pointer by the accepted draft count (ers_commit)."""
+    S = accepted.numel()
+    _need(accepted, torch.int32, "accepted", (S,))
+    st = status if status is not None else (Status(accepted.device) if check else None)
+    code = _abi.lib().ers_commit(ctypes.byref(cache.dims), ctypes.byref(cache._c()), S, _slot_arg(slot, S),
+                                 accepted.data_ptr(), int(T), _abi.FLAG_AUTO_FLUSH if auto_flush else 0,
+                                 _stream(stream), _ptr(st.t) if st else None)
+    _finish(code, "ers_commit", st, check)
+
+
+def ssu_update(state: torch.Tensor, params: LayerParams, x, dt, B, C, slot: Optional[torch.Tensor] = None,
+               status: Optional[Status] = None, check: bool = True, stream=None,
+               out: Optional[torch.Tensor] = None) -> torch.Tensor:
+    """Per-token state-writeback update (ers_ssu_update); state [nslots,H,P,N] fp32 updated in place."""
+    io = _io_from(x)
+    S, H, P = x.shape
+    G, N = B.shape[1], B.shape[2]
+    nslots = state.shape[0]
+    _need(state, torch.float32, "state", (nslots, H, P, N))
+    _need(x, io, "x", (S, H, P)); _need(dt, torch.float32, "dt", (S, H))
+    _need(B, io, "B", (S, G, N)); _need(C, io, "C", (S, G, N))
+    y = torch.empty_like(x) if out is None else out
+    dims = _dims(H, G, P, N, 1, io)
+    st = status if status is not None else (Status(x.device) if check else None)
+    code = _abi.lib().ers_ssu_update(ctypes.byref(dims), ctypes.byref(params._c()), state.data_ptr(), nslots, S,
+                                     _slot_arg(slot, S), x.data_ptr(), dt.data_ptr(), B.data_ptr(), C.data_ptr(),
+                                     y.data_ptr(), _stream(stream), _ptr(st.t) if st else None)
+    _finish(code, "ers_ssu_update", st, check)
+    return y

@@ -1,0 +1,244 @@
+/*
+ * ers.h — C ABI of the exact-replay SSD library (Mamba2 selective state space,
+ * hand-written CUDA for sm_103a / GB300).
+ *
+ * The operations follow two sources:
+ *  - "[RFC] Mamba2: exact-replay decode so that prefill, chunked prefill and
+ *    decode produce identical bits" (vLLM issue 55524), section 3 "Proposal":
+ *    per sequence an fp32 boundary state at the last multiple of the chunk size
+ *    plus a partial-chunk buffer of (x, raw dt, B, C); decode replays the buffer
+ *    from the boundary state; any prefill/chunked prefill starts at the boundary.
+ *  - The ReplaySSM reproduction notes (arXiv 2610.13778), "Motivation and
+ *    method" and "Core equations": periodic refresh of a checkpoint from
+ *    buffered inputs, output-only speculative verification, commit that moves
+ *    only the committed-input pointer, and a fp32 recurrence anchor with a
+ *    separately cast low-precision read copy.
+ *
+ * Per head h (group g = h / (H/G)), with delta = softplus(dt + dt_bias):
+ *     S_t = exp(delta_t A[h]) S_{t-1} + delta_t x_t B_t^T      (S is [P x N])
+ *     y_t = S_t C_t + D[h] x_t
+ *
+ * Conventions shared by every entry point
+ *  - All tensor pointers are DEVICE pointers to caller-owned, densely packed
+ *    row-major memory with the shapes given below; the library keeps no pointer
+ *    after a call returns and allocates no device or host memory.  Scratch
+ *    memory, where needed, is a caller buffer sized by the matching
+ *    *_workspace_size query.
+ *  - Dtypes: x, B, C, y and the partial-chunk buffers x/B/C use dims->io_dtype
+ *    (ERS_DTYPE_BF16 or ERS_DTYPE_F32, the same for all of them); dt, A, D,
+ *    dt_bias and every recurrence state are fp32; the read copy is bf16; index
+ *    arrays are int32.  Every pointer must be 16-byte aligned.
+ *  - Every call is asynchronous on `stream` (0 = legacy default stream).  Host
+ *    validation runs first; a call that returns an error has launched nothing.
+ *  - Errors the host cannot see (slot positions, slot indices, accepted counts,
+ *    a bounded device wait that gave up) are reported through `dev_status`, a
+ *    device int32 that the caller zeroes and reads back after synchronising; the
+ *    first error wins.  It may be NULL, in which case such errors are dropped
+ *    (the affected sequence's outputs are left unwritten).  No kernel traps.
+ *  - Within one call, distinct sequences must name distinct slots.
+ */
+#ifndef ERS_H
+#define ERS_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#if defined(__GNUC__)
+#define ERS_API __attribute__((visibility("default")))
+#else
+#define ERS_API
+#endif
+
+typedef struct CUstream_st* ers_stream_t; /* a cudaStream_t */
+
+typedef int32_t ers_status;
+#define ERS_OK 0
+#define ERS_EINVAL 1        /* NULL pointer, bad count or bad flag combination */
+#define ERS_ESHAPE 2        /* unsupported dimensions (see ers_dims) */
+#define ERS_EDTYPE 3        /* unsupported io dtype */
+#define ERS_EPTR 4          /* pointer not 16-byte aligned */
+#define ERS_EALIGN 5        /* device: a slot's buffered position is outside its legal range, i.e. the
+                               state's physical offset would differ from the offset the caller tracks */
+#define ERS_EOVERFLOW 6     /* device: h + T > L in a verify without ERS_FLAG_AUTO_FLUSH */
+#define ERS_ECOMMIT 7       /* device: accepted count outside [0, T] */
+#define ERS_ESLOT 8         /* device: slot index outside [0, nslots) */
+#define ERS_ETIMEOUT 9      /* device: a bounded wait gave up */
+#define ERS_EWORKSPACE 10   /* workspace NULL or smaller than the size query returns */
+#define ERS_ECUDA 11        /* the CUDA runtime rejected a launch */
+#define ERS_EUNSUPPORTED 12 /* a valid request this build does not implement */
+
+#define ERS_DTYPE_F32 0
+#define ERS_DTYPE_BF16 1
+
+/* Flags */
+#define ERS_FLAG_FUSE_REFRESH 1u /* replay_decode (exact mode): refresh in the same launch when a chunk fills */
+#define ERS_FLAG_REPLAYSSM 2u    /* replay_decode / refresh: ReplaySSM mode (read copy, flush rule) */
+#define ERS_FLAG_AUTO_FLUSH 4u   /* spec_verify / commit: flush when h + T > L instead of failing */
+
+/* Problem dimensions.  Supported: headdim P in {16, 32, 64}, dstate N in {16, 32, 64, 128},
+ * nheads % ngroups == 0, chunk Q in [1, 256].  In ReplaySSM mode `chunk` is the refresh
+ * period L (the buffer capacity). */
+typedef struct ers_dims {
+  int32_t nheads;   /* H */
+  int32_t ngroups;  /* G; head h reads B/C group h / (H/G) */
+  int32_t headdim;  /* P */
+  int32_t dstate;   /* N */
+  int32_t chunk;    /* Q (exact mode) or L (ReplaySSM mode) */
+  int32_t io_dtype; /* ERS_DTYPE_BF16 or ERS_DTYPE_F32 */
+} ers_dims;
+
+/* Per-head layer parameters, fp32 [H] each.  A < 0; dt_bias is added to the raw dt before softplus. */
+typedef struct ers_params {
+  const float* A;
+  const float* D;
+  const float* dt_bias;
+} ers_params;
+
+/* Per-slot replay cache (exact-replay RFC section 3; ReplaySSM "Motivation and method").
+ *   state     [nslots, H, P, N] fp32: the boundary checkpoint (exact mode) or recurrence anchor (ReplaySSM)
+ *   read_copy [nslots, H, P, N] bf16 or NULL: low-precision copy cast from the same fp32 values as `state`
+ *   buf_x     [nslots, Q, H, P] io dtype;  buf_dt [nslots, Q, H] fp32 raw dt
+ *   buf_B, buf_C [nslots, Q, G, N] io dtype: token-major partial-chunk input buffers
+ *   pos       [nslots] int32: buffered tokens p (exact mode, 0 <= p < Q between calls) or the
+ *             committed pointer h (ReplaySSM mode, 0 <= h <= L). */
+typedef struct ers_cache {
+  float* state;
+  void* read_copy;
+  void* buf_x;
+  float* buf_dt;
+  void* buf_B;
+  void* buf_C;
+  int32_t* pos;
+  int32_t nslots;
+} ers_cache;
+
+/* Human-readable name of a status code (static storage, never NULL). */
+ERS_API const char* ers_status_str(ers_status s);
+
+/* Library version as major*10000 + minor*100 + patch. */
+ERS_API int32_t ers_version(void);
+
+/* ---------------------------------------------------------------------------------------------
+ * Chunked SSD scan (prefill).  RFC section 1 (the chunked scan used for prefill), Evidence 3
+ * (prefix- and packing-invariant outputs) and Evidence 4 (fp32 inter-chunk state passing inside
+ * one call, rounded only on store).
+ *
+ * nseq sequences are packed along the token axis: sequence i owns tokens
+ * [cu_seqlens[i], cu_seqlens[i+1]) (cu_seqlens: device int32 [nseq+1], cu_seqlens[0] = 0,
+ * non-decreasing, cu_seqlens[nseq] = ntokens); max_seqlen >= every sequence length.  Each
+ * sequence's chunk grid starts at its own first token; no chunk spans two sequences.
+ *   x [ntokens, H, P], dt [ntokens, H] raw, B/C [ntokens, G, N]
+ *   init_state [nseq, H, P, N] fp32 or NULL (zero)
+ *   y [ntokens, H, P] (out), final_state [nseq, H, P, N] fp32 (out)
+ *   chunk_states [nseq, ceil(max_seqlen/Q), H, P, N] fp32 or NULL (out): the state at the end of
+ *     each chunk of each sequence ("return_intermediate_states"); entries past a sequence's last
+ *     chunk are left unwritten.
+ * Workspace: ers_ssd_scan_fwd_workspace_size(dims, nseq, max_seqlen) bytes. */
+ERS_API size_t ers_ssd_scan_fwd_workspace_size(const ers_dims* dims, int32_t nseq, int32_t max_seqlen);
+ERS_API ers_status ers_ssd_scan_fwd(const ers_dims* dims, const ers_params* prm, int32_t nseq, int64_t ntokens,
+                            int32_t max_seqlen, const int32_t* cu_seqlens, const void* x, const float* dt,
+                            const void* B, const void* C, const float* init_state, void* y,
+                            float* final_state, float* chunk_states, void* workspace, size_t workspace_bytes,
+                            ers_stream_t stream, int32_t* dev_status);
+
+/* ---------------------------------------------------------------------------------------------
+ * Boundary-anchored prefill / chunked prefill / recompute.  RFC section 3, second bullet: the
+ * call starts at each sequence's boundary, the buffered tokens are prepended and their outputs
+ * discarded, the trailing partial chunk's inputs go to the buffer, and the boundary state becomes
+ * the state at the last full chunk.
+ *
+ * Sequence i resumes slot slot[i] (slot: device int32 [nseq], or NULL for slot = i), whose pos p
+ * must satisfy 0 <= p < Q, and appends its new tokens (packed as in ers_ssd_scan_fwd; max_seqlen
+ * bounds the NEW token counts).  y receives the outputs of the new tokens only.  On return
+ * (stream order) cache->state holds the state at the last chunk boundary, the buffer holds the
+ * (p + len) mod Q trailing inputs, and pos = (p + len) mod Q.
+ * Workspace: ers_chunked_prefill_workspace_size(dims, nseq, max_seqlen) bytes. */
+ERS_API size_t ers_chunked_prefill_workspace_size(const ers_dims* dims, int32_t nseq, int32_t max_seqlen);
+ERS_API ers_status ers_chunked_prefill(const ers_dims* dims, const ers_params* prm, const ers_cache* cache,
+                               int32_t nseq, int64_t ntokens, int32_t max_seqlen, const int32_t* cu_seqlens,
+                               const int32_t* slot, const void* x, const float* dt, const void* B,
+                               const void* C, void* y, void* workspace, size_t workspace_bytes,
+                               ers_stream_t stream, int32_t* dev_status);
+
+/* ---------------------------------------------------------------------------------------------
+ * Exact-replay decode step.  RFC section 3, first bullet: each sequence's buffered partial chunk
+ * plus its new token is replayed from the boundary state; the last token's output is the layer
+ * output; the new token's inputs are appended to the buffer; when the chunk fills, the chunk's
+ * final state becomes the new boundary state and the buffer empties.
+ *
+ *   x [nseq, H, P], dt [nseq, H], B/C [nseq, G, N]: one new token per sequence; y [nseq, H, P] (out)
+ * Exact mode (flags without ERS_FLAG_REPLAYSSM): requires 0 <= pos < Q, reads cache->state (fp32).
+ *   With ERS_FLAG_FUSE_REFRESH a slot that fills its chunk is refreshed in the same call (pos -> 0);
+ *   without it pos reaches Q and ers_refresh(EXACT) must run before the next decode.  Both give
+ *   identical bits.
+ * ReplaySSM mode (ERS_FLAG_REPLAYSSM): requires 0 <= pos < L and a read copy; outputs read the read
+ *   copy; no refresh happens here (ers_refresh applies the flush rule).
+ * Device errors: ERS_EALIGN (pos out of range), ERS_ESLOT. */
+ERS_API ers_status ers_replay_decode(const ers_dims* dims, const ers_params* prm, const ers_cache* cache, int32_t nseq,
+                             const int32_t* slot, const void* x, const float* dt, const void* B, const void* C,
+                             uint32_t flags, void* y, ers_stream_t stream, int32_t* dev_status);
+
+/* ---------------------------------------------------------------------------------------------
+ * Checkpoint refresh.  RFC section 3 (the chunk's final state becomes the new boundary state) and
+ * ReplaySSM "Core equations" (refresh forms S from the committed raw records, then casts the
+ * high- and low-precision copies independently from the same unrounded state).
+ *
+ * Exact mode (flags = 0): slots with pos == Q fold their Q buffered tokens into cache->state and
+ *   get pos = 0; other slots are untouched.
+ * ReplaySSM mode (ERS_FLAG_REPLAYSSM): slots with pos + T > L (T = drafts_T, the flush rule; pass
+ *   drafts_T > L to refresh every slot) fold their pos committed records into the anchor, write the
+ *   read copy (if present) from the same fp32 values, and get pos = 0.  A slot with pos == 0 keeps
+ *   its anchor bits unchanged (its read copy is rewritten from them).
+ * Device errors: ERS_EALIGN (pos outside [0, Q] / [0, L]), ERS_ESLOT. */
+ERS_API ers_status ers_refresh(const ers_dims* dims, const ers_params* prm, const ers_cache* cache, int32_t nseq,
+                       const int32_t* slot, uint32_t flags, int32_t drafts_T, ers_stream_t stream,
+                       int32_t* dev_status);
+
+/* ---------------------------------------------------------------------------------------------
+ * Output-only speculative verification.  ReplaySSM "Motivation and method" (outputs replay the
+ * checkpoint and buffered inputs; verification uses an output-only form rather than a per-draft
+ * state) and "Core equations" (O = S_ckpt Q D + V (W . K^T Q); flush when h + T > L).
+ *
+ *   x [nseq, T, H, P], dt [nseq, T, H], B/C [nseq, T, G, N]: T draft tokens per sequence
+ *   y [nseq, T, H, P] (out): draft s's output given committed records and drafts 1..s, computed
+ *     from the bf16 read copy (required).
+ * The drafts are written to buffer rows [h', h'+T) where h' = 0 if the slot flushed, else h = pos.
+ * pos is NOT changed: ers_commit must follow before the next verify on the same slots.
+ * With ERS_FLAG_AUTO_FLUSH a slot with h + T > L first refreshes its h committed records (as
+ * ers_refresh in ReplaySSM mode); without it such a slot reports ERS_EOVERFLOW.
+ * Requires 1 <= T <= L. */
+ERS_API ers_status ers_spec_verify(const ers_dims* dims, const ers_params* prm, const ers_cache* cache, int32_t nseq,
+                           const int32_t* slot, int32_t T, const void* x, const float* dt, const void* B,
+                           const void* C, uint32_t flags, void* y, ers_stream_t stream, int32_t* dev_status);
+
+/* ---------------------------------------------------------------------------------------------
+ * Commit.  ReplaySSM "Motivation and method": the acceptance length advances only the
+ * committed-input pointer; rejected drafts never enter the recurrence and may be overwritten.
+ *
+ * accepted: device int32 [nseq] with 0 <= accepted[i] <= T.  For each sequence,
+ *   pos[slot] = (flushed ? 0 : pos[slot]) + accepted[i], flushed = (flags & AUTO_FLUSH) && pos + T > L,
+ * i.e. the same decision the preceding ers_spec_verify (same T, L and flags) took.  Nothing but
+ * pos is touched.  Device errors: ERS_ECOMMIT, ERS_ESLOT. */
+ERS_API ers_status ers_commit(const ers_dims* dims, const ers_cache* cache, int32_t nseq, const int32_t* slot,
+                      const int32_t* accepted, int32_t T, uint32_t flags, ers_stream_t stream,
+                      int32_t* dev_status);
+
+/* ---------------------------------------------------------------------------------------------
+ * Per-token state-writeback update (the recurrent "selective state update" the RFC's section 1
+ * contrasts with the chunked scan; the comparison point for replay decode).
+ *   state [nslots, H, P, N] fp32, updated in place for slot[i] (slot NULL = identity)
+ *   x [nseq, H, P], dt [nseq, H], B/C [nseq, G, N]; y [nseq, H, P] (out)
+ * Device errors: ERS_ESLOT. */
+ERS_API ers_status ers_ssu_update(const ers_dims* dims, const ers_params* prm, float* state, int32_t nslots,
+                          int32_t nseq, const int32_t* slot, const void* x, const float* dt, const void* B,
+                          const void* C, void* y, ers_stream_t stream, int32_t* dev_status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* ERS_H */

@@ -1,0 +1,116 @@
+"""C-ABI library checks that need no GPU: it builds, loads, exports every function include/ers.h
+declares, and rejects invalid calls during host validation (before any launch)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from exact_replay_decode_gb300 import build, _abi
+    build.build()
+    return _abi.lib()
+
+
+def _declared():
+    src = open(os.path.join(ROOT, "include", "ers.h")).read()
+    return sorted(set(re.findall(r"^ERS_API [^(]*?\b(ers_\w+)\(", src, flags=re.M)))
+
+
+def test_header_declares_expected_entry_points():
+    names = _declared()
+    for n in ("ers_ssd_scan_fwd", "ers_chunked_prefill", "ers_replay_decode", "ers_refresh", "ers_spec_verify",
+              "ers_commit", "ers_ssu_update"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    from exact_replay_decode_gb300 import _abi
+    for n in _declared():
+        assert hasattr(lib, n), n
+    assert set(_declared()) == set(_abi.EXPORTS)
+
+
+def test_status_strings(lib):
+    from exact_replay_decode_gb300 import _abi
+    for code in _abi.STATUS_NAMES:
+        assert _abi.status_str(code)
+    assert _abi.status_str(0) == "ok"
+    assert lib.ers_version() >= 100
+
+
+# Host-validation cases.  Each one fails a check that runs before any CUDA call, so no pointer is
+# ever dereferenced; they are skipped on machines with a GPU so that a validation regression can
+# never turn into a launch on fake pointers.
+needs_no_gpu = pytest.mark.skipif(__import__("torch").cuda.is_available(), reason="host-only validation test")
+
+FAKE = 1 << 20          # 16-byte aligned dummy address, never dereferenced
+MISALIGNED = FAKE + 4
+
+
+def _dims(**kw):
+    from exact_replay_decode_gb300 import _abi
+    d = dict(nheads=8, ngroups=2, headdim=64, dstate=128, chunk=16, io_dtype=_abi.DTYPE_BF16)
+    d.update(kw)
+    return _abi.Dims(**d)
+
+
+def _prm(a=FAKE):
+    from exact_replay_decode_gb300 import _abi
+    return _abi.Params(a, FAKE, FAKE)
+
+
+def _scan(lib, dims, prm, workspace=FAKE, wbytes=1 << 40, cu=FAKE):
+    return lib.ers_ssd_scan_fwd(ctypes.byref(dims), ctypes.byref(prm), 1, 32, 32, cu, FAKE, FAKE, FAKE, FAKE,
+                                None, FAKE, FAKE, None, workspace, wbytes, None, None)
+
+
+@needs_no_gpu
+def test_validation_rejects_bad_dims(lib):
+    from exact_replay_decode_gb300 import _abi
+    assert _scan(lib, _dims(io_dtype=7), _prm()) == 3                   # ERS_EDTYPE
+    assert _scan(lib, _dims(ngroups=3), _prm()) == 2                    # nheads % ngroups
+    assert _scan(lib, _dims(chunk=0), _prm()) == 2
+    assert _scan(lib, _dims(chunk=257), _prm()) == 2
+    assert _scan(lib, _dims(headdim=48), _prm()) == 2
+    assert _scan(lib, _dims(dstate=96), _prm()) == 2
+
+
+@needs_no_gpu
+def test_validation_rejects_bad_pointers_and_workspace(lib):
+    assert _scan(lib, _dims(), _prm(a=MISALIGNED)) == 4                 # ERS_EPTR
+    assert _scan(lib, _dims(), _prm(a=0)) == 1                          # ERS_EINVAL (NULL)
+    assert _scan(lib, _dims(), _prm(), cu=0) == 1
+    assert _scan(lib, _dims(), _prm(), workspace=0) == 10               # ERS_EWORKSPACE
+    assert _scan(lib, _dims(), _prm(), wbytes=16) == 10
+
+
+@needs_no_gpu
+def test_validation_rejects_bad_verify_and_commit_args(lib):
+    from exact_replay_decode_gb300 import _abi
+    d = _dims()
+    c = _abi.Cache(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 4)
+    p = _prm()
+    v = lambda T, flags=0: lib.ers_spec_verify(ctypes.byref(d), ctypes.byref(p), ctypes.byref(c), 4, None, T, FAKE,
+                                               FAKE, FAKE, FAKE, flags, FAKE, None, None)
+    assert v(0) == 1 and v(17) == 1 and v(4, flags=8) == 1
+    nocopy = _abi.Cache(FAKE, 0, FAKE, FAKE, FAKE, FAKE, FAKE, 4)
+    assert lib.ers_spec_verify(ctypes.byref(d), ctypes.byref(p), ctypes.byref(nocopy), 4, None, 4, FAKE, FAKE,
+                               FAKE, FAKE, 0, FAKE, None, None) == 1    # read copy required
+    assert lib.ers_commit(ctypes.byref(d), ctypes.byref(c), 4, None, FAKE, 0, 0, None, None) == 1
+    assert lib.ers_commit(ctypes.byref(d), ctypes.byref(c), 5, None, FAKE, 4, 0, None, None) == 1  # nseq > nslots
+    dec = lambda flags: lib.ers_replay_decode(ctypes.byref(d), ctypes.byref(p), ctypes.byref(c), 4, None, FAKE, FAKE,
+                                              FAKE, FAKE, flags, FAKE, None, None)
+    assert dec(_abi.FLAG_REPLAYSSM | _abi.FLAG_FUSE_REFRESH) == 1
+    assert dec(64) == 1
+
+
+@needs_no_gpu
+def test_zero_sequences_is_a_noop(lib):
+    d, p = _dims(), _prm()
+    assert lib.ers_ssd_scan_fwd(ctypes.byref(d), ctypes.byref(p), 0, 0, 0, None, None, None, None, None, None,
+                                None, None, None, None, 0, None, None) == 0

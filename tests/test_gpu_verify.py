@@ -1,0 +1,115 @@
+"""Output-only speculative verify + commit on the GPU (ReplaySSM notes, "Motivation and method",
+"Core equations"): verify outputs of accepted drafts equal non-speculative ReplaySSM-mode decode
+bit for bit over the same committed stream and refresh points; the anchor never sees the read
+copy; parity with the oracle's dual-precision protocol model."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+from synth import torch_io
+from gpu_helpers import STATE_TOL, dev, layer, out_err, same_bits, state_err
+
+pytestmark = pytest.mark.gpu
+
+
+def _ers():
+    import exact_replay_decode_gb300 as ers
+    return ers
+
+
+def _prefilled(w, S, steps, seed, history=32):
+    ers = _ers()
+    d = w.dims
+    params, hist, drafts, acc = synth.verify_inputs(w, seed=seed, batch=S, steps=steps, history=history)
+    prm = layer(params)
+    hx, hdt, hB, hC = torch_io.tokens_to(hist, dev())
+    cu = torch.arange(0, S * history + 1, history, dtype=torch.int32, device=dev())
+    _, fin = ers.ssd_scan_fwd(hx, hdt, prm, hB, hC, chunk=d.chunk, cu_seqlens=cu)
+    cache = ers.ReplayCache(S, d.nheads, d.ngroups, d.headdim, d.dstate, d.chunk, torch.bfloat16, read_copy=True)
+    cache.state.copy_(fin)
+    ers.refresh(cache, prm, replayssm=True, drafts_T=d.chunk + 1)   # h = 0 everywhere: cast the read copy
+    return params, prm, hist, drafts, acc, cache
+
+
+def test_verify_b512_matches_nonspec_decode_and_oracle():
+    ers = _ers()
+    w = synth.workload("verify_b512_t4")
+    S, K, T, L = w.batch, w.steps, w.drafts, w.dims.chunk
+    params, prm, hist, drafts, acc, cache = _prefilled(w, S, K, seed=0)
+    ref = _prefilled(w, S, K, seed=0)[-1]                     # identical starting cache for the comparator
+    assert same_bits(cache.read_copy, ref.read_copy)
+    dx, ddt, dB, dC = torch_io.tokens_to(drafts, dev(), lead=(K, S, T))
+    acc_t = torch.from_numpy(acc).to(dev())
+    samples = [0, 1, 200, 511]
+    model = oracle.ReplaySSMModel(params, _oracle_anchor(params, hist, samples, 32), L)
+    ys_all = []
+    for k in range(K):
+        y = ers.spec_verify(cache, prm, dx[k], ddt[k], dB[k], dC[k])
+        ers.commit(cache, acc_t[k], T)
+        ys_all.append(y)
+        # non-speculative comparator: same flush decisions, then one accepted token at a time
+        ers.refresh(ref, prm, replayssm=True, drafts_T=T)
+        a = acc[k]
+        for j in range(T):
+            sel = np.nonzero(a > j)[0]
+            if sel.size == 0:
+                break
+            sel_t = torch.from_numpy(sel.astype(np.int32)).to(dev())
+            sl = sel_t.long()
+            yd = ers.replay_decode(ref, prm, dx[k, sl, j], ddt[k, sl, j], dB[k, sl, j], dC[k, sl, j], slot=sel_t,
+                                   replayssm=True)
+            assert same_bits(yd, y[sl, j]), f"step {k} draft {j}"
+        # the oracle's protocol model on sampled sequences
+        dr = [tuple(np.ascontiguousarray(getattr(drafts, f).reshape(K, S, T, *getattr(drafts, f).shape[1:])[k, i])
+                    for f in ("x", "dt", "B", "C")) for i in samples]
+        y_o = model.verify(dr)
+        model.commit([int(acc[k, i]) for i in samples])
+        assert out_err(y[samples], y_o) <= 2e-3, k
+    assert torch.equal(cache.pos, ref.pos)
+    assert same_bits(cache.state, ref.state) and same_bits(cache.read_copy, ref.read_copy)
+    assert np.array_equal(cache.pos.cpu().numpy()[samples], model.h())
+    assert state_err(cache.state[samples], model.anchor) <= STATE_TOL
+    assert model.flushes > 0
+
+
+def _oracle_anchor(params, hist, samples, history):
+    rows = np.concatenate([np.arange(i * history, (i + 1) * history) for i in samples])
+    cu = np.arange(0, len(samples) * history + 1, history)
+    _, fin = oracle.recurrence(hist.x[rows], hist.dt[rows], params.A, hist.B[rows], hist.C[rows], params.D,
+                               params.dt_bias, cu)
+    return fin
+
+
+def test_zero_acceptance_keeps_anchor_bits():
+    ers = _ers()
+    w = synth.workload("verify_b512_t4")
+    S, K, T = 8, 6, w.drafts
+    params, prm, hist, drafts, acc, cache = _prefilled(w, S, K, seed=1)
+    anchor0 = cache.state.clone()
+    dx, ddt, dB, dC = torch_io.tokens_to(drafts, dev(), lead=(K, S, T))
+    zero = torch.zeros(S, dtype=torch.int32, device=dev())
+    for k in range(K):
+        ers.spec_verify(cache, prm, dx[k], ddt[k], dB[k], dC[k])
+        ers.commit(cache, zero, T)
+    assert same_bits(cache.state, anchor0) and int(cache.pos.abs().sum()) == 0
+
+
+def test_anchor_independent_of_read_copy():
+    """Corrupting the read copy changes outputs but never the anchor (dual precision)."""
+    ers = _ers()
+    w = synth.workload("verify_b512_t4")
+    S, K, T = 8, 12, w.drafts
+    params, prm, hist, drafts, acc, c1 = _prefilled(w, S, K, seed=2)
+    c2 = _prefilled(w, S, K, seed=2)[-1]
+    dx, ddt, dB, dC = torch_io.tokens_to(drafts, dev(), lead=(K, S, T))
+    acc_t = torch.from_numpy(acc).to(dev())
+    differ = False
+    for k in range(K):
+        c2.read_copy.mul_(1.0078125)          # perturb the read copy between refreshes
+        y1 = ers.spec_verify(c1, prm, dx[k], ddt[k], dB[k], dC[k]); ers.commit(c1, acc_t[k], T)
+        y2 = ers.spec_verify(c2, prm, dx[k], ddt[k], dB[k], dC[k]); ers.commit(c2, acc_t[k], T)
+        differ |= not same_bits(y1, y2)
+    assert differ
+    assert same_bits(c1.state, c2.state)
