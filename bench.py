@@ -1,0 +1,514 @@
+"""Benchmark of the exact-replay SSD hot path on GB300.
+
+Headline: replay-decode seq-steps/s per layer at B=256 (256 sequences x 64 heads / 8 groups,
+headdim 64, dstate 128, chunk = refresh period 16, each sequence starting at a uniform-random
+position in its partial chunk).  One step = one ers_replay_decode call over the batch, including
+the fused checkpoint refresh of the sequences whose chunk fills.  The same line reports SSD
+prefill tok/s (2048 tokens x 32 heads; varlen {2048, 777, 513, 1} x 64 heads), speculative
+verify + commit (512 sequences, 4 drafts, L = 16) and the per-token-writeback SSU comparison
+kernel, each against its HBM roofline.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Under torchrun every rank runs its own 256-sequence batch on its own GPU (weak scaling, no
+collective on the data path); the timed region is bracketed by a barrier and a device sync on
+both sides and the slowest rank's time is reported.  --impl reference times the fp64 CPU oracle
+on a bounded sample of the same workload on this host's cores.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import synth  # noqa: E402
+
+# Algorithmic HBM bytes per sequence-step of the decode workload (64 heads x 64 x 128):
+#   fp32 checkpoint read 2,097,152 + E[p] = 7.5 buffered rows x 10,496 (x 8,192 + dt 256 + B 2,048)
+#   + new-token read 12,544 + buffer append 12,544 + y 8,192 + refresh write 2,097,152 / 16
+DECODE_BYTES_PER_SEQ_STEP = 2_340_224
+SSU_BYTES_PER_SEQ_STEP = 4_215_040       # state read + write 4,194,304 + token in 12,544 + y 8,192
+PREFILL_BYTES = {"prefill_2048_h32": 19_136_896, "varlen_4seq_h64": 77_626_880}
+PREFILL_FLOPS = {"prefill_2048_h32": 3.29e9, "varlen_4seq_h64": 11.38e9}
+L2_FLUSH_BYTES = 256 << 20
+
+
+def _peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), float(p["bf16_tflops"]), "measured"
+    except Exception:
+        return 6800.0, 1900.0, "fallback"
+
+
+# ---------------------------------------------------------------------------------------------
+class ClockSampler:
+    """Samples nvidia-smi SM clocks and throttle reasons every 200 ms while running."""
+
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+         "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+         "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.idx = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.idx), f"--query-gpu={self.Q}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except Exception:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            f = [v.strip() for v in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx = float(f[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": mx, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------------------------
+def _dist():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def max_over_ranks(value: float, device=None) -> float:
+    """Max of a per-rank float over the default process group (identity without one)."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return value
+    t = torch.tensor([value], dtype=torch.float64, device=device if device is not None else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def sum_over_ranks(value: float, device=None) -> float:
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return value
+    t = torch.tensor([value], dtype=torch.float64, device=device if device is not None else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.SUM)
+    return float(t.item())
+
+
+def _barrier():
+    import torch.distributed as dist
+    if dist.is_available() and dist.is_initialized():
+        dist.barrier()
+
+
+# ---------------------------------------------------------------------------------------------
+class DecodeBench:
+    """The B=256 replay-decode workload, prefilled to its random starting positions."""
+
+    def __init__(self, dev, steps_total: int, seed: int, batch: int = None):
+        import torch
+        import exact_replay_decode_gb300 as ers
+        from synth import torch_io
+        self.ers, self.torch = ers, torch
+        w = synth.workload("decode_b256_h64")
+        d = w.dims
+        self.w = w
+        self.S = batch or w.batch
+        params, hist, p0, stream = synth.decode_inputs(w, seed=seed, batch=self.S, steps=steps_total)
+        self.params, self.hist, self.p0, self.stream = params, hist, p0, stream
+        A, D, dtb = torch_io.params_to(params, dev)
+        self.prm = ers.LayerParams(A, D, dtb)
+        self.cache = ers.ReplayCache(self.S, d.nheads, d.ngroups, d.headdim, d.dstate, d.chunk, torch.bfloat16)
+        ht = synth.Tokens.concat(hist)
+        cu = torch.tensor(np.concatenate([[0], np.cumsum([h.ntokens for h in hist])]), dtype=torch.int32, device=dev)
+        ers.chunked_prefill(self.cache, self.prm, *torch_io.tokens_to(ht, dev), cu)
+        self.tok = torch_io.tokens_to(stream, dev, lead=(steps_total, self.S))
+        self.y = torch.empty(self.S, d.nheads, d.headdim, dtype=torch.bfloat16, device=dev)
+        self.status = ers.Status(dev)
+        self.launches_per_step = 2   # decode kernel + position advance
+
+    def step(self, k: int):
+        x, dt, B, C = (t[k] for t in self.tok)
+        self.ers.replay_decode(self.cache, self.prm, x, dt, B, C, status=self.status, check=False, out=self.y)
+
+
+def time_decode(dev, steps: int, warmup: int, seed: int, batch=None):
+    import torch
+    b = DecodeBench(dev, steps + warmup, seed, batch)
+    for k in range(warmup):
+        b.step(k)
+    torch.cuda.synchronize()
+    _barrier()
+    torch.cuda.synchronize()
+    s = torch.cuda.current_stream()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(torch.cuda.current_device()) as clk:
+        e0.record(s)
+        for k in range(warmup, warmup + steps):
+            b.step(k)
+        e1.record(s)
+        torch.cuda.synchronize()
+    _barrier()
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1)
+    b.status.raise_if_error("bench decode")
+    return b, ms, clk.summary()
+
+
+def time_decode_e2e(dev, steps: int, warmup: int, seed: int, batch=None):
+    """Same workload through the public API with host buffers: each step copies its tokens from
+    pinned host memory and reads its outputs back; copies are inside the timed region."""
+    import torch
+    b = DecodeBench(dev, steps + warmup, seed, batch)
+    host = [t.cpu().pin_memory() for t in b.tok]
+    dev_in = [torch.empty_like(t[0]) for t in b.tok]
+    y_host = torch.empty(b.y.shape, dtype=b.y.dtype).pin_memory()
+    h2d = sum(t[0].numel() * t.element_size() for t in host)
+    d2h = y_host.numel() * y_host.element_size()
+
+    def one(k):
+        for d_, h_ in zip(dev_in, host):
+            d_.copy_(h_[k], non_blocking=True)
+        b.ers.replay_decode(b.cache, b.prm, *dev_in, status=b.status, check=False, out=b.y)
+        y_host.copy_(b.y, non_blocking=True)
+
+    for k in range(warmup):
+        one(k)
+    torch.cuda.synchronize()
+    _barrier()
+    t0 = time.perf_counter()
+    for k in range(warmup, warmup + steps):
+        one(k)
+    torch.cuda.synchronize()
+    el = time.perf_counter() - t0
+    _barrier()
+    return el * 1e3, h2d, d2h
+
+
+def _flush_buf(dev):
+    import torch
+    return torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+
+
+def time_per_iter(fn, iters: int, warmup: int, dev, flush: bool = True):
+    """Mean device time of fn() over iters, L2 flushed before each timed call (events per call)."""
+    import torch
+    fb = _flush_buf(dev) if flush else None
+    for _ in range(warmup):
+        fn()
+    s = torch.cuda.current_stream()
+    evs = []
+    for _ in range(iters):
+        if fb is not None:
+            fb.zero_()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(s)
+        fn()
+        e1.record(s)
+        evs.append((e0, e1))
+    torch.cuda.synchronize()
+    return statistics.median([a.elapsed_time(b) for a, b in evs])
+
+
+def bench_prefill(dev, name: str, iters: int, warmup: int, hbm: float, tc: float):
+    import torch
+    import exact_replay_decode_gb300 as ers
+    from synth import torch_io
+    w = synth.workload(name)
+    params, toks, cu = synth.prefill_inputs(w, seed=0)
+    A, D, dtb = torch_io.params_to(params, dev)
+    prm = ers.LayerParams(A, D, dtb)
+    x, dt, B, C = torch_io.tokens_to(toks, dev)
+    cu_t = torch.from_numpy(cu).to(dev)
+    S = len(cu) - 1
+    ms_len = int(np.diff(cu).max())
+    y = torch.empty_like(x)
+    fin = torch.empty(S, w.dims.nheads, w.dims.headdim, w.dims.dstate, dtype=torch.float32, device=dev)
+    ws = torch.empty(1 << 28, dtype=torch.uint8, device=dev)
+    st = ers.Status(dev)
+    fn = lambda: ers.ssd_scan_fwd(x, dt, prm, B, C, chunk=w.dims.chunk, cu_seqlens=cu_t, max_seqlen=ms_len,
+                                  status=st, check=False, out=(y, fin), workspace=ws)
+    ms = time_per_iter(fn, iters, warmup, dev)
+    st.raise_if_error("bench prefill")
+    T = toks.ntokens
+    ach = PREFILL_BYTES[name] / (ms * 1e-3) / 1e9
+    return {"tok_per_s": T / (ms * 1e-3), "us_per_call": ms * 1e3, "achieved_gbs": ach,
+            "hbm_frac": ach / hbm, "roofline_us": PREFILL_BYTES[name] / (hbm * 1e9) * 1e6,
+            "tflops": PREFILL_FLOPS[name] / (ms * 1e-3) / 1e12, "l2": "flushed before each call"}
+
+
+def bench_verify(dev, steps: int, hbm: float):
+    import torch
+    import exact_replay_decode_gb300 as ers
+    from synth import torch_io
+    w = synth.workload("verify_b512_t4")
+    d = w.dims
+    S, T, L = w.batch, w.drafts, d.chunk
+    params, hist, drafts, acc = synth.verify_inputs(w, seed=0, steps=steps)
+    A, D, dtb = torch_io.params_to(params, dev)
+    prm = ers.LayerParams(A, D, dtb)
+    hx, hdt, hB, hC = torch_io.tokens_to(hist, dev)
+    cu = torch.arange(0, S * 32 + 1, 32, dtype=torch.int32, device=dev)
+    _, fin = ers.ssd_scan_fwd(hx, hdt, prm, hB, hC, chunk=L, cu_seqlens=cu)
+    cache = ers.ReplayCache(S, d.nheads, d.ngroups, d.headdim, d.dstate, L, torch.bfloat16, read_copy=True)
+    cache.state.copy_(fin)
+    ers.refresh(cache, prm, replayssm=True, drafts_T=L + 1)
+    dx, ddt, dB, dC = torch_io.tokens_to(drafts, dev, lead=(steps, S, T))
+    acc_t = torch.from_numpy(acc).to(dev)
+    y = torch.empty(S, T, d.nheads, d.headdim, dtype=torch.bfloat16, device=dev)
+    st = ers.Status(dev)
+    # algorithmic bytes from the actual committed pointers and flush decisions
+    hs = np.zeros(S, dtype=np.int64)
+    total_bytes = 0
+    for k in range(steps):
+        flush = hs + T > L
+        base = np.where(flush, 0, hs)
+        total_bytes += S * (1_048_576 + 50_176 + 50_176 + 32_768) + int(base.sum()) * 10_496
+        total_bytes += int(flush.sum()) * (2_097_152 + 2_097_152 + 1_048_576 - 1_048_576) + \
+            int(hs[flush].sum()) * 10_496
+        hs = base + acc[k]
+    torch.cuda.synchronize()
+    s = torch.cuda.current_stream()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(s)
+    for k in range(steps):
+        ers.spec_verify(cache, prm, dx[k], ddt[k], dB[k], dC[k], status=st, check=False, out=y)
+        ers.commit(cache, acc_t[k], T, status=st, check=False)
+    e1.record(s)
+    torch.cuda.synchronize()
+    st.raise_if_error("bench verify")
+    ms = e0.elapsed_time(e1)
+    ach = total_bytes / (ms * 1e-3) / 1e9
+    return {"seq_verify_steps_per_s": S * steps / (ms * 1e-3), "committed_tok_per_s": float(acc.sum()) / (ms * 1e-3),
+            "us_per_step": ms * 1e3 / steps, "achieved_gbs": ach, "hbm_frac": ach / hbm,
+            "algorithmic_bytes": total_bytes, "steps": steps}
+
+
+def bench_ssu(dev, steps: int, hbm: float):
+    import torch
+    import exact_replay_decode_gb300 as ers
+    from synth import torch_io
+    w = synth.workload("decode_b256_h64")
+    d = w.dims
+    S = w.batch
+    rng = np.random.Generator(np.random.PCG64(5))
+    params = synth.make_params(rng, d.nheads)
+    toks = synth.make_tokens(rng, (steps + 3) * S, d, True)
+    A, D, dtb = torch_io.params_to(params, dev)
+    prm = ers.LayerParams(A, D, dtb)
+    x, dt, B, C = torch_io.tokens_to(toks, dev, lead=(steps + 3, S))
+    state = torch.randn(S, d.nheads, d.headdim, d.dstate, device=dev)
+    y = torch.empty(S, d.nheads, d.headdim, dtype=torch.bfloat16, device=dev)
+    st = ers.Status(dev)
+    for k in range(3):
+        ers.ssu_update(state, prm, x[k], dt[k], B[k], C[k], status=st, check=False, out=y)
+    torch.cuda.synchronize()
+    s = torch.cuda.current_stream()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(s)
+    for k in range(3, steps + 3):
+        ers.ssu_update(state, prm, x[k], dt[k], B[k], C[k], status=st, check=False, out=y)
+    e1.record(s)
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / steps
+    ach = SSU_BYTES_PER_SEQ_STEP * S / (ms * 1e-3) / 1e9
+    return {"seq_steps_per_s": S / (ms * 1e-3), "us_per_step": ms * 1e3, "achieved_gbs": ach, "hbm_frac": ach / hbm}
+
+
+# ---------------------------------------------------------------------------------------------
+def cpu_baseline(seed: int, budget_s: float = 10.0):
+    """fp64 oracle on this host's cores: decode seq-steps/s on a bounded sample of the B=256
+    workload (a subset of sequences advanced token by token from a prefilled state)."""
+    import oracle
+    w = synth.workload("decode_b256_h64")
+    d = w.dims
+    threads = oracle.default_threads()
+    rng = np.random.Generator(np.random.PCG64(seed))
+    params = synth.make_params(rng, d.nheads)
+
+    def run(S, K):
+        toks = synth.make_tokens(rng, S * K, d, True)
+        order = np.arange(S * K).reshape(K, S).T.reshape(-1)       # sequence-major stream
+        cu = np.arange(0, S * K + 1, K)
+        init = rng.standard_normal((S, d.nheads, d.headdim, d.dstate))
+        t0 = time.perf_counter()
+        oracle.recurrence(toks.x[order], toks.dt[order], params.A, toks.B[order], toks.C[order], params.D,
+                          params.dt_bias, cu, init, nthreads=threads)
+        return time.perf_counter() - t0
+
+    S = max(threads, 4)
+    t1 = run(S, 2)
+    K = int(max(2, min(64, budget_s / max(t1 / 2, 1e-6))))
+    el = run(S, K)
+    return {"value": S * K / el, "unit": "seq-steps/s", "cores": threads, "kind": "oracle",
+            "sample": f"{S} of the 256 sequences x {K} decode steps (fp64 recurrence, {d.nheads} heads, "
+                      f"headdim {d.headdim}, dstate {d.dstate}), {el:.1f} s"}
+
+
+def reference_arm(args):
+    """The fp64 oracle as the reference implementation, timed on host cores."""
+    ws, rank, _ = _dist()
+    if rank != 0:
+        return 0
+    import oracle
+    w = synth.workload("decode_b256_h64")
+    d = w.dims
+    threads = oracle.default_threads()
+    rng = np.random.Generator(np.random.PCG64(1))
+    params = synth.make_params(rng, d.nheads)
+    S, K = max(threads, 4), 4          # one "step" = 4 decode steps of a 16-sequence sample
+    state = rng.standard_normal((S, d.nheads, d.headdim, d.dstate))
+
+    def step():
+        nonlocal state
+        toks = synth.make_tokens(rng, S * K, d, True)
+        order = np.arange(S * K).reshape(K, S).T.reshape(-1)
+        cu = np.arange(0, S * K + 1, K)
+        _, state = oracle.recurrence(toks.x[order], toks.dt[order], params.A, toks.B[order], toks.C[order],
+                                     params.D, params.dt_bias, cu, state, nthreads=threads)
+
+    for _ in range(args.warmup):
+        step()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        step()
+    el = time.perf_counter() - t0
+    v = S * K * args.steps / el
+    line = {"impl": "reference", "metric": "replay-decode seq-steps/s per layer @B=256", "value": v,
+            "unit": "seq-steps/s", "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": el * 1e3 / args.steps, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "f64", "data": "synthetic",
+            "config": {"workload": "decode_b256_h64 (sampled)", "batch": 256, "sample_per_step": f"{S} seqs x {K} steps"},
+            "cpu_baseline": {"value": v, "unit": "seq-steps/s", "cores": threads, "kind": "oracle",
+                             "sample": f"{S} sequences x {K} decode steps per step, fp64 recurrence"},
+            "e2e": {"value": v, "unit": "seq-steps/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line))
+    return 0
+
+
+# ---------------------------------------------------------------------------------------------
+def main(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--decode-only", action="store_true", help="only the headline decode measurement")
+    ap.add_argument("--batch", type=int, default=None, help="decode sequences per GPU (profiling runs only)")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    if args.impl == "reference":
+        return reference_arm(args)
+
+    import torch
+    import torch.distributed as dist
+    ws, rank, local = _dist()
+    if ws > 1:
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    dev = torch.device("cuda", torch.cuda.current_device())
+    hbm, tc, peak_kind = _peaks()
+
+    b, ms, clocks = time_decode(dev, args.steps, args.warmup, seed=1000 + rank, batch=args.batch)
+    ms = max_over_ranks(ms, dev)
+    S = b.S
+    value = S * args.steps * ws / (ms * 1e-3)
+    ms_step = ms / args.steps
+    ach = DECODE_BYTES_PER_SEQ_STEP * S / (ms_step * 1e-3) / 1e9
+    e2e_ms, h2d, d2h = time_decode_e2e(dev, args.steps, args.warmup, seed=2000 + rank, batch=args.batch)
+    e2e_ms = max_over_ranks(e2e_ms, dev)
+    del b
+    torch.cuda.empty_cache()
+
+    extra = {}
+    if not args.decode_only:
+        extra["prefill"] = {n: bench_prefill(dev, n, 10, 3, hbm, tc) for n in ("prefill_2048_h32", "varlen_4seq_h64")}
+        extra["verify"] = bench_verify(dev, 32, hbm)
+        extra["ssu"] = bench_ssu(dev, 16, hbm)
+    line = {
+        "metric": "replay-decode seq-steps/s per layer @B=256",
+        "value": value,
+        "unit": "seq-steps/s",
+        "n_gpus": ws,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": ms_step,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f32",
+        "data": "synthetic",
+        "config": {"workload": "decode_b256_h64: 256 seqs x 64 heads / 8 groups, headdim 64, dstate 128, "
+                               "chunk = refresh period 16, start position ~U{0..15}, bf16 x/B/C, fp32 checkpoint",
+                   "batch_per_gpu": S, "global_batch": S * ws, "parallelism": f"replicas x{ws} (independent sequences)",
+                   "l2": "inputs larger than L2 (512 MiB fp32 checkpoints per step)"},
+        "roofline": {"bound": "hbm", "achieved": ach, "peak": hbm, "unit": "GB/s", "frac": ach / hbm,
+                     "traffic": None, "peak_kind": f"{peak_kind} copy bandwidth",
+                     "kernel": "replay decode step (decode kernel + position advance)",
+                     "algorithmic_bytes_per_launch": DECODE_BYTES_PER_SEQ_STEP * S},
+        "e2e": {"value": S * args.steps * ws / (e2e_ms * 1e-3), "unit": "seq-steps/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": b_launches(args.steps),
+        "clocks": clocks,
+    }
+    line.update(extra)
+    if rank == 0 and ws == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(seed=7)
+    if rank == 0:
+        print(json.dumps(line))
+    if ws > 1:
+        dist.barrier()
+        dist.destroy_process_group()
+    return 0
+
+
+def b_launches(steps: int) -> int:
+    return 2 * steps
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -173,6 +173,7 @@ ers_status ers_ssd_scan_fwd(const ers_dims* dims, const ers_params* prm, int32_t
   a.ws_states = (float*)workspace;
   a.ws_tot = (float*)((char*)workspace + w.states);
   a.status = dev_status;
+  if (ers::tc_supported(a.io, a.P, a.N, a.Q)) return finish(ers::tc_prefill(a, ers::Op::kScan, (cudaStream_t)stream));
   return finish(ers::fma_prefill(a, ers::Op::kScan, (cudaStream_t)stream));
 }
 
@@ -207,6 +208,8 @@ ers_status ers_chunked_prefill(const ers_dims* dims, const ers_params* prm, cons
   a.ws_states = (float*)workspace;
   a.ws_tot = (float*)((char*)workspace + w.states);
   a.status = dev_status;
+  if (ers::tc_supported(a.io, a.P, a.N, a.Q))
+    return finish(ers::tc_prefill(a, ers::Op::kChunkedPrefill, (cudaStream_t)stream));
   return finish(ers::fma_prefill(a, ers::Op::kChunkedPrefill, (cudaStream_t)stream));
 }
 
@@ -234,6 +237,7 @@ ers_status ers_replay_decode(const ers_dims* dims, const ers_params* prm, const 
   a.flags = flags;
   a.y = y;
   a.status = dev_status;
+  if (ers::tc_supported(a.io, a.P, a.N, a.Q)) return finish(ers::tc_decode(a, (cudaStream_t)stream));
   return finish(ers::fma_decode(a, (cudaStream_t)stream));
 }
 
@@ -256,6 +260,7 @@ ers_status ers_refresh(const ers_dims* dims, const ers_params* prm, const ers_ca
   a.flags = flags;
   a.T = drafts_T;
   a.status = dev_status;
+  if (ers::tc_supported(a.io, a.P, a.N, a.Q)) return finish(ers::tc_refresh(a, (cudaStream_t)stream));
   return finish(ers::fma_refresh(a, (cudaStream_t)stream));
 }
 
@@ -282,6 +287,7 @@ ers_status ers_spec_verify(const ers_dims* dims, const ers_params* prm, const er
   a.flags = flags;
   a.y = y;
   a.status = dev_status;
+  if (ers::tc_supported(a.io, a.P, a.N, a.Q)) return finish(ers::tc_verify(a, (cudaStream_t)stream));
   return finish(ers::fma_verify(a, (cudaStream_t)stream));
 }
 

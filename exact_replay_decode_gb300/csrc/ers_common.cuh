@@ -15,6 +15,7 @@
 #include <stdint.h>
 
 #include "ers.h"
+#include "ers_internal.h"
 
 namespace ers {
 
@@ -124,6 +125,91 @@ __device__ __forceinline__ void load_k(const T* __restrict__ p, float (&v)[K]) {
 // the io dtype at the end.
 __device__ __forceinline__ float combine_out(float decay_t, float yoff, float ydiag, float Dh, float xt) {
   return __fmaf_rn(Dh, xt, __fadd_rn(__fmul_rn(decay_t, yoff), ydiag));
+}
+
+// Row source of a chunk: rows [0, nbuf) come from a slot's partial-chunk buffer, rows >= nbuf from
+// packed token inputs (row r is token tok0 + r).  Row strides are the token strides H*P, H, G*N.
+template <typename T>
+struct Rows {
+  int nbuf;
+  const T* bx;
+  const float* bdt;
+  const T* bB;
+  const T* bC;
+  const T* x0;
+  const float* dt0;
+  const T* B0;
+  const T* C0;
+  long long tok0;
+  int sx, sdt, sB;
+  __device__ __forceinline__ const T* x(int r) const {
+    return r < nbuf ? bx + (long long)r * sx : x0 + (tok0 + r) * sx;
+  }
+  __device__ __forceinline__ float dt(int r) const {
+    return r < nbuf ? bdt[(long long)r * sdt] : dt0[(tok0 + r) * sdt];
+  }
+  __device__ __forceinline__ const T* B(int r) const {
+    return r < nbuf ? bB + (long long)r * sB : B0 + (tok0 + r) * sB;
+  }
+  __device__ __forceinline__ const T* C(int r) const {
+    return r < nbuf ? bC + (long long)r * sB : C0 + (tok0 + r) * sB;
+  }
+};
+
+template <typename T>
+__device__ __forceinline__ Rows<T> make_rows(const LaunchArgs& a, int slot, int h, int nbuf, long long tok0) {
+  const int g = h / (a.H / a.G);
+  Rows<T> r;
+  r.nbuf = nbuf;
+  r.sx = a.H * a.P;
+  r.sdt = a.H;
+  r.sB = a.G * a.N;
+  if (slot >= 0 && a.bx != nullptr) {
+    r.bx = (const T*)a.bx + ((size_t)slot * a.Q * a.H + h) * a.P;
+    r.bdt = a.bdt + (size_t)slot * a.Q * a.H + h;
+    r.bB = (const T*)a.bB + ((size_t)slot * a.Q * a.G + g) * a.N;
+    r.bC = (const T*)a.bC + ((size_t)slot * a.Q * a.G + g) * a.N;
+  } else {
+    r.bx = nullptr; r.bdt = nullptr; r.bB = nullptr; r.bC = nullptr;
+  }
+  r.x0 = (const T*)a.x + (size_t)h * a.P;
+  r.dt0 = a.dt + h;
+  r.B0 = (const T*)a.B + (size_t)g * a.N;
+  r.C0 = (const T*)a.C + (size_t)g * a.N;
+  r.tok0 = tok0;
+  return r;
+}
+
+__device__ __forceinline__ bool resolve_slot(const LaunchArgs& a, int i, int* slot) {
+  const int s = a.slot != nullptr ? a.slot[i] : i;
+  if (s < 0 || s >= a.nslots) {
+    if (threadIdx.x == 0) report(a.status, ERS_ESLOT);
+    return false;
+  }
+  *slot = s;
+  return true;
+}
+
+// Boundary-anchored chunk grid of sequence i: buffered p rows then the new tokens.
+struct SeqGrid {
+  int slot, p, len, total, nch;
+};
+
+__device__ __forceinline__ bool seq_grid(const LaunchArgs& a, bool chunked, int i, SeqGrid* g) {
+  g->slot = -1;
+  g->p = 0;
+  if (chunked) {
+    if (!resolve_slot(a, i, &g->slot)) return false;
+    g->p = a.pos[g->slot];
+    if (g->p < 0 || g->p >= a.Q) {
+      if (threadIdx.x == 0) report(a.status, ERS_EALIGN);
+      return false;
+    }
+  }
+  g->len = a.cu[i + 1] - a.cu[i];
+  g->total = g->p + g->len;
+  g->nch = (g->total + a.Q - 1) / a.Q;
+  return true;
 }
 
 }  // namespace ers

@@ -36,59 +36,6 @@ __host__ __device__ constexpr size_t fma_smem_bytes(int Q, int P) {
   return ((sizeof(FmaSmem) + 15) & ~size_t(15)) + (size_t)Q * P * sizeof(float);
 }
 
-// Row source of a chunk: rows [0, nbuf) come from a slot's partial-chunk buffer, rows >= nbuf from
-// packed token inputs (row r is token tok0 + r).  Row strides are the token strides H*P, H, G*N.
-template <typename T>
-struct Rows {
-  int nbuf;
-  const T* bx;
-  const float* bdt;
-  const T* bB;
-  const T* bC;
-  const T* x0;
-  const float* dt0;
-  const T* B0;
-  const T* C0;
-  long long tok0;
-  int sx, sdt, sB;
-  __device__ __forceinline__ const T* x(int r) const {
-    return r < nbuf ? bx + (long long)r * sx : x0 + (tok0 + r) * sx;
-  }
-  __device__ __forceinline__ float dt(int r) const {
-    return r < nbuf ? bdt[(long long)r * sdt] : dt0[(tok0 + r) * sdt];
-  }
-  __device__ __forceinline__ const T* B(int r) const {
-    return r < nbuf ? bB + (long long)r * sB : B0 + (tok0 + r) * sB;
-  }
-  __device__ __forceinline__ const T* C(int r) const {
-    return r < nbuf ? bC + (long long)r * sB : C0 + (tok0 + r) * sB;
-  }
-};
-
-template <typename T>
-__device__ __forceinline__ Rows<T> make_rows(const LaunchArgs& a, int slot, int h, int nbuf, long long tok0) {
-  const int g = h / (a.H / a.G);
-  Rows<T> r;
-  r.nbuf = nbuf;
-  r.sx = a.H * a.P;
-  r.sdt = a.H;
-  r.sB = a.G * a.N;
-  if (slot >= 0 && a.bx != nullptr) {
-    r.bx = (const T*)a.bx + ((size_t)slot * a.Q * a.H + h) * a.P;
-    r.bdt = a.bdt + (size_t)slot * a.Q * a.H + h;
-    r.bB = (const T*)a.bB + ((size_t)slot * a.Q * a.G + g) * a.N;
-    r.bC = (const T*)a.bC + ((size_t)slot * a.Q * a.G + g) * a.N;
-  } else {
-    r.bx = nullptr; r.bdt = nullptr; r.bB = nullptr; r.bC = nullptr;
-  }
-  r.x0 = (const T*)a.x + (size_t)h * a.P;
-  r.dt0 = a.dt + h;
-  r.B0 = (const T*)a.B + (size_t)g * a.N;
-  r.C0 = (const T*)a.C + (size_t)g * a.N;
-  r.tok0 = tok0;
-  return r;
-}
-
 // Loads rows [0, nrows) (x as fp32, delta, dA, B/C row pointers), zeroes the rest, and scans the
 // log-decays.  All kThreads threads must call it.
 template <typename T, int P>
@@ -208,38 +155,6 @@ __device__ __forceinline__ void fold_state(float* Hd, __nv_bfloat16* Rd, float d
     Hd[idx] = v;
     if (Rd != nullptr) Rd[idx] = __float2bfloat16_rn(v);
   }
-}
-
-__device__ __forceinline__ bool resolve_slot(const LaunchArgs& a, int i, int* slot) {
-  const int s = a.slot != nullptr ? a.slot[i] : i;
-  if (s < 0 || s >= a.nslots) {
-    if (threadIdx.x == 0) report(a.status, ERS_ESLOT);
-    return false;
-  }
-  *slot = s;
-  return true;
-}
-
-// Boundary-anchored chunk grid of sequence i: buffered p rows then the new tokens.
-struct SeqGrid {
-  int slot, p, len, total, nch;
-};
-
-__device__ __forceinline__ bool seq_grid(const LaunchArgs& a, bool chunked, int i, SeqGrid* g) {
-  g->slot = -1;
-  g->p = 0;
-  if (chunked) {
-    if (!resolve_slot(a, i, &g->slot)) return false;
-    g->p = a.pos[g->slot];
-    if (g->p < 0 || g->p >= a.Q) {
-      if (threadIdx.x == 0) report(a.status, ERS_EALIGN);
-      return false;
-    }
-  }
-  g->len = a.cu[i + 1] - a.cu[i];
-  g->total = g->p + g->len;
-  g->nch = (g->total + a.Q - 1) / a.Q;
-  return true;
 }
 
 extern __shared__ __align__(16) unsigned char dyn_smem[];
@@ -684,6 +599,14 @@ cudaError_t launch_setpos(const LaunchArgs& a, int kind, cudaStream_t s) {
 cudaError_t launch_commit(const LaunchArgs& a, cudaStream_t s) {
   if (a.nseq > 0) k_commit<<<(a.nseq + 255) / 256, 256, 0, s>>>(a);
   return cudaGetLastError();
+}
+
+cudaError_t launch_chain(const LaunchArgs& a, bool chunked, cudaStream_t s) {
+  if (a.nseq <= 0 || a.max_chunks <= 0) return cudaSuccess;
+#define ERS_CH(p_, n_) if (a.P == p_ && a.N == n_) { k_prefill_chain<p_, n_><<<dim3(a.nseq, a.H), kThreads, 0, s>>>(a, chunked); return cudaGetLastError(); }
+  ERS_FMA_SHAPES(ERS_CH)
+#undef ERS_CH
+  return cudaErrorInvalidValue;
 }
 
 cudaError_t launch_tail(const LaunchArgs& a, cudaStream_t s) {

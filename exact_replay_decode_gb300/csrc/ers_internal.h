@@ -65,6 +65,14 @@ bool fma_supported(int P, int N);
 cudaError_t launch_setpos(const LaunchArgs& a, int kind, cudaStream_t s);  // kind: 0 decode, 1 refresh
 cudaError_t launch_commit(const LaunchArgs& a, cudaStream_t s);
 cudaError_t launch_tail(const LaunchArgs& a, cudaStream_t s);
+cudaError_t launch_chain(const LaunchArgs& a, bool chunked, cudaStream_t s);
+
+// tensor-core engine (bf16 io, P = 64, N = 128, Q % 16 == 0), ers_tc.cu
+bool tc_supported(int io, int P, int N, int Q);
+cudaError_t tc_prefill(const LaunchArgs& a, Op op, cudaStream_t s);
+cudaError_t tc_decode(const LaunchArgs& a, cudaStream_t s);
+cudaError_t tc_refresh(const LaunchArgs& a, cudaStream_t s);
+cudaError_t tc_verify(const LaunchArgs& a, cudaStream_t s);
 
 // SSU baseline, ers_ssu.cu
 cudaError_t ssu_update(const LaunchArgs& a, cudaStream_t s);
