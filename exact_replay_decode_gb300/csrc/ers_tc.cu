@@ -77,13 +77,6 @@ __device__ __forceinline__ void teardown_tmem(uint32_t ncols) {
   if (threadIdx.x / 32 == 0) tmem_dealloc(hdr().tmem, ncols);
 }
 
-// make generic-proxy smem writes visible to the tensor core, then sync the CTA
-__device__ __forceinline__ void publish() {
-  fence_async_smem();
-  before_sync();
-  __syncthreads();
-  after_sync();
-}
 
 // delta / dA for rows [0, nrows) (zeros beyond), then the chunk scan
 __device__ __forceinline__ void load_decays(const Rows<bf16>& rows, int nrows, float A, float bias) {
@@ -148,7 +141,7 @@ __device__ bool tc_outputs(const Arena& ar, int Q, int tau, int tmax, int out_lo
     issue_yoff(tb + RG, smem_u32(ar.Hs), smem_u32(ar.C), 128, 1024, ge.TT);
     commit(&hd.bar);
   }
-  ok = mbar_wait(&hd.bar, phase, status);
+  ok = __syncthreads_and(mbar_wait(&hd.bar, phase, status));
   phase ^= 1;
   after_sync();
   const int tlim = tmax < ge.t0 + ge.TT ? tmax : ge.t0 + ge.TT;
@@ -156,8 +149,7 @@ __device__ bool tc_outputs(const Arena& ar, int Q, int tau, int tmax, int out_lo
     const int width = ge.S_ext - 128 * blk < 128 ? ge.S_ext - 128 * blk : 128;
     if (64 * half < width) {
       float g[64];
-      tmem_ld32(taddr(tb, 32 * q, 128 * blk + 64 * half), *reinterpret_cast<float(*)[32]>(&g[0]));
-      tmem_ld32(taddr(tb, 32 * q, 128 * blk + 64 * half + 32), *reinterpret_cast<float(*)[32]>(&g[32]));
+      tmem_ld64(taddr(tb, 32 * q, 128 * blk + 64 * half), g);
       m_row(g, t, tlim, blk, half, ge.S_ext, hd.delta, hd.ahi, hd.alo, ar.C, ar.Hs, 128, row);
     }
     publish();
@@ -165,7 +157,7 @@ __device__ bool tc_outputs(const Arena& ar, int Q, int tau, int tmax, int out_lo
       issue_ydiag(tb, smem_u32(ar.C), smem_u32(ar.Hs), 128, 1024, smem_u32(ar.X), blk, ge.S_ext);
       commit(&hd.bar);
     }
-    ok = mbar_wait(&hd.bar, phase, status);
+    ok = __syncthreads_and(mbar_wait(&hd.bar, phase, status));
     phase ^= 1;
     after_sync();
   }
@@ -243,7 +235,7 @@ __device__ bool tc_state(const Arena& ar, int nrows, uint8_t* u, int32_t* status
       issue_state_block(hd.tmem, smem_u32(ar.B), ar.BR, smem_u32(u0), smem_u32(u1), smem_u32(u2), s0, nr / 16);
       commit(&hd.bar);
     }
-    ok = mbar_wait(&hd.bar, *phase, status);
+    ok = __syncthreads_and(mbar_wait(&hd.bar, *phase, status));
     *phase ^= 1;
     after_sync();
   }
@@ -522,6 +514,7 @@ cudaError_t tc_prefill(const LaunchArgs& a, Op op, cudaStream_t s) {
 }
 
 cudaError_t tc_decode(const LaunchArgs& a, cudaStream_t s) {
+  if (tc_decode_persistent_supported(a.Q)) return tc_decode_persistent(a, s);
   const size_t so = out_smem(a.Q);
   cudaError_t e = set_smem(k_tc_decode, so);
   if (e != cudaSuccess) return e;

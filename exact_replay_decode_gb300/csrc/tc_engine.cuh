@@ -133,7 +133,7 @@ __device__ __forceinline__ void split8(const float (&v)[8], uint4& hi, uint4& lo
 
 // fp32 state [64][128] -> [H_hi; H_lo] tile.  Called by all kThreads threads.
 __device__ __forceinline__ void state_to_tile(const float* __restrict__ H, uint8_t* tile) {
-  for (int id = threadIdx.x; id < P * (N / 8); id += kThreads) {
+  for (int id = threadIdx.x; id < P * (N / 8); id += blockDim.x) {
     const int d = id / (N / 8), c = id % (N / 8);
     const float4 a = *reinterpret_cast<const float4*>(H + d * N + 8 * c);
     const float4 b = *reinterpret_cast<const float4*>(H + d * N + 8 * c + 4);
@@ -147,7 +147,7 @@ __device__ __forceinline__ void state_to_tile(const float* __restrict__ H, uint8
 
 // bf16 read copy [64][128] -> [R; 0] tile (a single term)
 __device__ __forceinline__ void readcopy_to_tile(const __nv_bfloat16* __restrict__ R, uint8_t* tile) {
-  for (int id = threadIdx.x; id < P * (N / 8); id += kThreads) {
+  for (int id = threadIdx.x; id < P * (N / 8); id += blockDim.x) {
     const int d = id / (N / 8), c = id % (N / 8);
     *reinterpret_cast<uint4*>(tile + sw128(128, d, 8 * c)) = *reinterpret_cast<const uint4*>(R + d * N + 8 * c);
     *reinterpret_cast<uint4*>(tile + sw128(128, P + d, 8 * c)) = make_uint4(0, 0, 0, 0);
@@ -168,7 +168,7 @@ __device__ __forceinline__ void zero_tile_chunk(uint8_t* tile, uint32_t R, uint3
 // s >= nrows are written as zeros.  All kThreads threads.
 __device__ __forceinline__ void build_u_tiles(const uint8_t* xT, const float* w, int nrows, int s0, int nr,
                                               uint8_t* u0, uint8_t* u1, uint8_t* u2) {
-  for (int id = threadIdx.x; id < nr * (P / 8); id += kThreads) {
+  for (int id = threadIdx.x; id < nr * (P / 8); id += blockDim.x) {
     const int r = id / (P / 8), c = id % (P / 8);
     const int s = s0 + r;
     uint4 h4 = make_uint4(0, 0, 0, 0), m4 = h4, l4 = h4;
