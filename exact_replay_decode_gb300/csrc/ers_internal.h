@@ -73,9 +73,9 @@ cudaError_t tc_prefill(const LaunchArgs& a, Op op, cudaStream_t s);
 cudaError_t tc_decode(const LaunchArgs& a, cudaStream_t s);
 cudaError_t tc_refresh(const LaunchArgs& a, cudaStream_t s);
 cudaError_t tc_verify(const LaunchArgs& a, cudaStream_t s);
-// persistent pipelined decode (chunk <= 128), ers_tc_decode.cu
-bool tc_decode_persistent_supported(int Q);
-cudaError_t tc_decode_persistent(const LaunchArgs& a, cudaStream_t s);
+// group-batched persistent decode (chunk <= 16), ers_tc_decode_group.cu
+bool tc_decode_group_supported(int Q);
+cudaError_t tc_decode_group(const LaunchArgs& a, cudaStream_t s);
 
 // SSU baseline, ers_ssu.cu
 cudaError_t ssu_update(const LaunchArgs& a, cudaStream_t s);

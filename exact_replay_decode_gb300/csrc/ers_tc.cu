@@ -138,13 +138,14 @@ __device__ bool tc_outputs(const Arena& ar, int Q, int tau, int tmax, int out_lo
   bool ok = true;
   if (threadIdx.x == 0) {
     issue_gram(tb, smem_u32(ar.C), 128, 1024, smem_u32(ar.B), ar.BR, ge.S_ext);
-    issue_yoff(tb + RG, smem_u32(ar.Hs), smem_u32(ar.C), 128, 1024, ge.TT);
+    issue_yoff(tb + RG, smem_u32(ar.C), 128, 1024, smem_u32(ar.Hs), 128);
     commit(&hd.bar);
   }
   ok = __syncthreads_and(mbar_wait(&hd.bar, phase, status));
   phase ^= 1;
   after_sync();
   const int tlim = tmax < ge.t0 + ge.TT ? tmax : ge.t0 + ge.TT;
+  // M tiles (hi over the C tile, lo over the H tile) once the Gram and off-diagonal MMAs are done
   for (int blk = 0; blk < ge.nblk && ok; ++blk) {
     const int width = ge.S_ext - 128 * blk < 128 ? ge.S_ext - 128 * blk : 128;
     if (64 * half < width) {
@@ -154,7 +155,8 @@ __device__ bool tc_outputs(const Arena& ar, int Q, int tau, int tmax, int out_lo
     }
     publish();
     if (threadIdx.x == 0) {
-      issue_ydiag(tb, smem_u32(ar.C), smem_u32(ar.Hs), 128, 1024, smem_u32(ar.X), blk, ge.S_ext);
+      issue_ydiag(tb, smem_u32(ar.C), 128, 1024, smem_u32(ar.X), blk, ge.S_ext);
+      issue_ydiag(tb + 64, smem_u32(ar.Hs), 128, 1024, smem_u32(ar.X), blk, ge.S_ext);
       commit(&hd.bar);
     }
     ok = __syncthreads_and(mbar_wait(&hd.bar, phase, status));
@@ -162,33 +164,12 @@ __device__ bool tc_outputs(const Arena& ar, int Q, int tau, int tmax, int out_lo
     after_sync();
   }
   if (!ok) return false;
-  // transpose the off-diagonal term into ysum[t][d] = hi + lo (fp32, rows padded to 65)
-  float* ysum = reinterpret_cast<float*>(ar.C);
-  const int nc16 = ge.TT / 16;
-  if (q >= 2) {
-    for (int c16 = half; c16 < nc16; c16 += 2) {
-      float v[16];
-      tmem_ld16(taddr(tb, 32 * q, RG + 16 * c16), v);
-#pragma unroll
-      for (int j = 0; j < 16; ++j) ysum[(16 * c16 + j) * 65 + (row - P)] = v[j];
-    }
-  }
-  __syncthreads();
-  if (q < 2) {
-    for (int c16 = half; c16 < nc16; c16 += 2) {
-      float v[16];
-      tmem_ld16(taddr(tb, 32 * q, RG + 16 * c16), v);
-#pragma unroll
-      for (int j = 0; j < 16; ++j) {
-        float* dst = &ysum[(16 * c16 + j) * 65 + row];
-        *dst = __fadd_rn(v[j], *dst);
-      }
-    }
-  }
-  __syncthreads();
   // combine: thread (row, half) writes d in [32 half, 32 half + 32)
-  float yd[32];
-  tmem_ld32(taddr(tb, 32 * q, 32 * half), yd);
+  float oh[32], ol[32], dh[32], dl[32];
+  tmem_ld32(taddr(tb, 32 * q, RG + 32 * half), oh);
+  tmem_ld32(taddr(tb, 32 * q, RG + 64 + 32 * half), ol);
+  tmem_ld32(taddr(tb, 32 * q, 32 * half), dh);
+  tmem_ld32(taddr(tb, 32 * q, 64 + 32 * half), dl);
   if (t >= out_lo && t < out_hi && row < ge.TT) {
     const float et = expf(hd.ahi[t]);
     uint32_t packed[16];
@@ -199,7 +180,7 @@ __device__ bool tc_outputs(const Arena& ar, int Q, int tau, int tmax, int out_lo
       for (int u = 0; u < 2; ++u) {
         const int d = 32 * half + j + u;
         const float xv = __bfloat162float(*reinterpret_cast<const bf16*>(ar.X + sw128(1, t, d)));
-        o[u] = combine_out(et, ysum[row * 65 + d], yd[j + u], Dh, xv);
+        o[u] = combine_out(et, __fadd_rn(oh[j + u], ol[j + u]), __fadd_rn(dh[j + u], dl[j + u]), Dh, xv);
       }
       packed[j / 2] = pack_bf16x2(o[0], o[1]);
     }
@@ -514,7 +495,7 @@ cudaError_t tc_prefill(const LaunchArgs& a, Op op, cudaStream_t s) {
 }
 
 cudaError_t tc_decode(const LaunchArgs& a, cudaStream_t s) {
-  if (tc_decode_persistent_supported(a.Q)) return tc_decode_persistent(a, s);
+  if (tc_decode_group_supported(a.Q)) return tc_decode_group(a, s);
   const size_t so = out_smem(a.Q);
   cudaError_t e = set_smem(k_tc_decode, so);
   if (e != cudaSuccess) return e;

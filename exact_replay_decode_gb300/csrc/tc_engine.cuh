@@ -5,15 +5,17 @@
 //   G^T[t,s] = C_t . B_s                                       (Gram, K = N)
 //   M^T[t,s] = G^T[t,s] delta_s exp(Acum_t - Acum_s) [s<=t]    (masked, decayed)
 //   Ydiag^T[t,d] = sum_s M^T[t,s] x_s[d]                        (K = s)
-//   Yoff[d,t] = sum_n H[d,n] C_t[n]                             (K = N)
-//   y[t,d] = fma(D, x_t[d], exp(Acum_t) Yoff[d,t] + Ydiag^T[t,d])
+//   Yoff^T[t,d] = sum_n C_t[n] H[d,n]                           (K = N)
+//   y[t,d] = fma(D, x_t[d], exp(Acum_t) Yoff^T[t,d] + Ydiag^T[t,d])
 //   S^T[n,d] = sum_s B_s[n] (delta_s exp(Acum_last - Acum_s) x_s[d]),  H' = fma(exp(Acum_last), H, S)
 //
 // Every contraction runs on the tensor cores as M = 128 MMAs with bf16 operands and fp32
-// accumulation.  Operands that are fp32 are split into bf16 terms, accumulated in a fixed order:
-// M^T as hi + lo (a single bf16 term costs ~0.05% of output accuracy), H as hi and lo stacked in the
-// 128 rows of one MMA (free: P = 64 fills only half of M = 128), the state input as hi + mid + lo
-// (the fp32 state must match the fp64 recurrence to 1e-5).
+// accumulation.  Operands that are fp32 are split into bf16 terms: M^T as hi + lo (a single bf16
+// term costs ~0.05% of output accuracy), each with its own accumulator, summed once in fp32; H as
+// hi and lo stacked along N of one MMA (columns [0, 64) hi, [64, 128) lo), summed once in fp32; the
+// state input as hi + mid + lo accumulated in that order (the fp32 state must match the fp64
+// recurrence to 1e-5).  An MMA costs about the same for any N up to 256, so the off-diagonal
+// contraction puts the tokens on M and the headdim rows (of one or two heads) on N.
 //
 // Bitwise identity.  Prefill, chunked prefill, replay decode, refresh and verify all build the
 // same operand VALUES for a token and issue the same instruction sequence (shapes, K order, split
@@ -46,11 +48,12 @@ __host__ __device__ __forceinline__ Geom geom(int Q, int tau) {
   return g;
 }
 
-// TMEM columns: [0, RG) Gram, reused for Ydiag and the chunk state; [RG, RG + TT) Yoff.
-__host__ __device__ __forceinline__ int tmem_rg(int S_ext) { return S_ext < 64 ? 64 : S_ext; }
+// TMEM columns: [0, RG) Gram, reused for the diagonal (hi [0, 64), lo [64, 128)) and the chunk
+// state; [RG, RG + 128) the off-diagonal (hi [RG, RG + 64), lo [RG + 64, RG + 128)).
+__host__ __device__ __forceinline__ int tmem_rg(int S_ext) { return S_ext < 128 ? 128 : S_ext; }
 __host__ __device__ __forceinline__ uint32_t tmem_cols(int Q) {
   const Geom g = geom(Q, (Q - 1) / 128);
-  const int need = tmem_rg(g.S_ext) + g.TT;
+  const int need = tmem_rg(g.S_ext) + 128;
   uint32_t c = 32;
   while ((int)c < need) c <<= 1;
   return c;
@@ -69,32 +72,32 @@ __device__ __forceinline__ void issue_gram(uint32_t tG, uint32_t cT, uint32_t cR
   }
 }
 
-// Off-diagonal: Yoff[d', t] into columns [tY, tY + TT), d' < 64 the hi term, d' >= 64 the lo term.
-// A = [H_hi; H_lo] tile (128 rows, atoms 128 rows apart), B = C tile (rows t).
-__device__ __forceinline__ void issue_yoff(uint32_t tY, uint32_t hT, uint32_t cT, uint32_t cR, uint32_t cS, int TT) {
-  const uint32_t id = idesc_bf16(128, TT, false, false);
+// Off-diagonal: Yoff^T[t, j] into columns [tY, tY + hR), A = C tile (rows t; atoms cR rows apart,
+// SBO cS), B = hR rows of [H_hi; H_lo] tiles (one head: hR = 128; two heads packed: 256), K = N.
+__device__ __forceinline__ void issue_yoff(uint32_t tY, uint32_t cT, uint32_t cR, uint32_t cS, uint32_t hT,
+                                           uint32_t hR) {
+  const uint32_t id = idesc_bf16(128, (int)hR, false, false);
 #pragma unroll
   for (int k = 0; k < N / 16; ++k) {
-    const uint32_t ao = (k >> 2) * 128u * 128u + (k & 3) * 32u, bo = (k >> 2) * cR * 128u + (k & 3) * 32u;
-    mma(tY, sdesc(hT + ao, 16, 1024), sdesc(cT + bo, 16, cS), id, k > 0);
+    const uint32_t ao = (k >> 2) * cR * 128u + (k & 3) * 32u, bo = (k >> 2) * hR * 128u + (k & 3) * 32u;
+    mma(tY, sdesc(cT + ao, 16, cS), sdesc(hT + bo, 16, 1024), id, k > 0);
   }
 }
 
-// Diagonal block blk (s in [128 blk, min(S_ext, 128 blk + 128))): Ydiag^T[t, d] += M_hi X + M_lo X
-// into columns [tD, tD + 64).  M tiles hold s - 128 blk as their inner index (rows t, atoms mR rows
-// apart, SBO mS); the X tile holds rows s (MN-major B, N = 64).
-__device__ __forceinline__ void issue_ydiag(uint32_t tD, uint32_t mhi, uint32_t mlo, uint32_t mR, uint32_t mS,
-                                            uint32_t xT, int blk, int S_ext) {
+// Diagonal block blk (s in [128 blk, min(S_ext, 128 blk + 128))) of ONE bf16 term: Ydiag^T[t, d] +=
+// Mterm X into columns [tD, tD + 64).  The M tile holds s - 128 blk as its inner index (rows t,
+// atoms mR rows apart, SBO mS); the X tile holds rows s (MN-major B, N = 64).  The hi and lo terms
+// run as two such chains into two accumulators (decode may hold both in one 8-row aliased tile,
+// hi at row t % 8 and lo at row (t + 4) % 8, and run a single chain).
+__device__ __forceinline__ void issue_ydiag(uint32_t tD, uint32_t mT, uint32_t mR, uint32_t mS, uint32_t xT, int blk,
+                                            int S_ext) {
   const uint32_t id = idesc_bf16(128, P, false, true);
   const int s0 = 128 * blk;
   const int nk = ((S_ext - s0 < 128 ? S_ext - s0 : 128)) / 16;
-  for (int term = 0; term < 2; ++term) {
-    const uint32_t mT = term == 0 ? mhi : mlo;
-    for (int k = 0; k < nk; ++k) {
-      const uint32_t ao = (k >> 2) * mR * 128u + (k & 3) * 32u;
-      const uint32_t bo = (uint32_t)(s0 + 16 * k) * 128u;
-      mma(tD, sdesc(mT + ao, 16, mS), sdesc(xT + bo, 1024, 1024), id, (blk > 0 || term > 0 || k > 0) ? 1u : 0u);
-    }
+  for (int k = 0; k < nk; ++k) {
+    const uint32_t ao = (k >> 2) * mR * 128u + (k & 3) * 32u;
+    const uint32_t bo = (uint32_t)(s0 + 16 * k) * 128u;
+    mma(tD, sdesc(mT + ao, 16, mS), sdesc(xT + bo, 1024, 1024), id, (blk > 0 || k > 0) ? 1u : 0u);
   }
 }
 
