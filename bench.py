@@ -18,6 +18,7 @@ on a bounded sample of the same workload on this host's cores.
 from __future__ import annotations
 
 import argparse
+import datetime
 import json
 import os
 import statistics
@@ -54,21 +55,25 @@ def _peaks():
 
 # ---------------------------------------------------------------------------------------------
 class ClockSampler:
-    """Samples nvidia-smi SM clocks and throttle reasons every 200 ms while running."""
+    """Samples nvidia-smi SM clocks and throttle reasons every 100 ms while running.
 
-    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
-         "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
-         "clocks_event_reasons.sw_power_cap")
+    Each sample carries nvidia-smi's own timestamp, so the summary can keep only the samples
+    taken inside the timed region (``mark_start``/``mark_stop`` bracket it on the host)."""
+
+    Q = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
     def __init__(self, gpu_index: int):
         self.idx = gpu_index
         self.proc = None
         self.lines = []
+        self.t_start = self.t_stop = None
 
     def __enter__(self):
         try:
             self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.idx), f"--query-gpu={self.Q}",
-                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
                                          stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self.t = threading.Thread(target=self._read, daemon=True)
             self.t.start()
@@ -80,32 +85,47 @@ class ClockSampler:
         for line in self.proc.stdout:
             self.lines.append(line.strip())
 
+    def mark_start(self):
+        self.t_start = datetime.datetime.now()
+
+    def mark_stop(self):
+        self.t_stop = datetime.datetime.now()
+
     def __exit__(self, *exc):
         if self.proc is not None:
+            time.sleep(0.25)          # let the last sample of the window arrive
             self.proc.terminate()
             try:
                 self.proc.wait(timeout=5)
             except Exception:
                 self.proc.kill()
+            self.t.join(timeout=2)
 
-    def summary(self):
-        sm, mx, reasons = [], None, set()
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+    def _parse(self):
+        out = []
         for ln in self.lines:
             f = [v.strip() for v in ln.split(",")]
-            if len(f) < 9:
+            if len(f) < 10:
                 continue
             try:
-                sm.append(float(f[1]))
-                mx = float(f[2])
+                ts = datetime.datetime.strptime(f[0], "%Y/%m/%d %H:%M:%S.%f")
+                out.append((ts, float(f[2]), float(f[3]), f[6:10]))
             except ValueError:
                 continue
-            for n, v in zip(names, f[5:9]):
-                if v.lower().startswith("active"):
-                    reasons.add(n)
-        if not sm:
-            return {"sm_mhz": None, "sm_max_mhz": mx, "reasons": [], "samples": 0}
-        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons), "samples": len(sm)}
+        return out
+
+    def summary(self):
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        rows = self._parse()
+        window = "timed region"
+        sel = [r for r in rows if self.t_start and self.t_stop and self.t_start <= r[0] <= self.t_stop]
+        if not sel:
+            sel, window = rows, "warm-up soak + timed region (no sample fell inside the timed region)"
+        if not sel:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        reasons = sorted({n for r in sel for n, v in zip(names, r[3]) if v.lower().startswith("active")})
+        return {"sm_mhz": statistics.median(r[1] for r in sel), "sm_max_mhz": max(r[2] for r in sel),
+                "reasons": reasons, "samples": len(sel), "window": window}
 
 
 # ---------------------------------------------------------------------------------------------
@@ -144,10 +164,17 @@ def _barrier():
 
 
 # ---------------------------------------------------------------------------------------------
-class DecodeBench:
-    """The B=256 replay-decode workload, prefilled to its random starting positions."""
+TOKEN_RING = 64          # distinct token sets cycled through by the decode steps
+SOAK_S = 0.5             # untimed decode steps before the timed region (clocks settle, samples exist)
 
-    def __init__(self, dev, steps_total: int, seed: int, batch: int = None):
+
+class DecodeBench:
+    """The B=256 replay-decode workload, prefilled to its random starting positions.
+
+    Step k feeds token set k mod TOKEN_RING (fresh N(0,1) bf16 x/B/C and dt for every sequence);
+    the ring keeps host-side generation bounded while every step still does the full work."""
+
+    def __init__(self, dev, seed: int, batch: int = None):
         import torch
         import exact_replay_decode_gb300 as ers
         from synth import torch_io
@@ -156,42 +183,56 @@ class DecodeBench:
         d = w.dims
         self.w = w
         self.S = batch or w.batch
-        params, hist, p0, stream = synth.decode_inputs(w, seed=seed, batch=self.S, steps=steps_total)
-        self.params, self.hist, self.p0, self.stream = params, hist, p0, stream
+        params, hist, p0, stream = synth.decode_inputs(w, seed=seed, batch=self.S, steps=TOKEN_RING)
         A, D, dtb = torch_io.params_to(params, dev)
         self.prm = ers.LayerParams(A, D, dtb)
         self.cache = ers.ReplayCache(self.S, d.nheads, d.ngroups, d.headdim, d.dstate, d.chunk, torch.bfloat16)
         ht = synth.Tokens.concat(hist)
         cu = torch.tensor(np.concatenate([[0], np.cumsum([h.ntokens for h in hist])]), dtype=torch.int32, device=dev)
         ers.chunked_prefill(self.cache, self.prm, *torch_io.tokens_to(ht, dev), cu)
-        self.tok = torch_io.tokens_to(stream, dev, lead=(steps_total, self.S))
+        self.tok = torch_io.tokens_to(stream, dev, lead=(TOKEN_RING, self.S))
         self.y = torch.empty(self.S, d.nheads, d.headdim, dtype=torch.bfloat16, device=dev)
         self.status = ers.Status(dev)
-        self.launches_per_step = 2   # decode kernel + position advance
+        self.launches_per_step = 2   # group decode kernel + position advance
 
     def step(self, k: int):
-        x, dt, B, C = (t[k] for t in self.tok)
+        x, dt, B, C = (t[k % TOKEN_RING] for t in self.tok)
         self.ers.replay_decode(self.cache, self.prm, x, dt, B, C, status=self.status, check=False, out=self.y)
+
+
+def _soak(step, seconds: float, k0: int = 0):
+    import torch
+    t0 = time.perf_counter()
+    k = k0
+    while time.perf_counter() - t0 < seconds:
+        for _ in range(32):
+            step(k)
+            k += 1
+        torch.cuda.synchronize()
+    return k
 
 
 def time_decode(dev, steps: int, warmup: int, seed: int, batch=None):
     import torch
-    b = DecodeBench(dev, steps + warmup, seed, batch)
-    for k in range(warmup):
-        b.step(k)
-    torch.cuda.synchronize()
-    _barrier()
-    torch.cuda.synchronize()
+    b = DecodeBench(dev, seed, batch)
     s = torch.cuda.current_stream()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     with ClockSampler(torch.cuda.current_device()) as clk:
-        e0.record(s)
-        for k in range(warmup, warmup + steps):
+        for k in range(warmup):
             b.step(k)
+        k = _soak(b.step, SOAK_S, warmup)
+        torch.cuda.synchronize()
+        _barrier()
+        torch.cuda.synchronize()
+        clk.mark_start()
+        e0.record(s)
+        for i in range(steps):
+            b.step(k + i)
         e1.record(s)
         torch.cuda.synchronize()
-    _barrier()
-    torch.cuda.synchronize()
+        clk.mark_stop()
+        _barrier()
+        torch.cuda.synchronize()
     ms = e0.elapsed_time(e1)
     b.status.raise_if_error("bench decode")
     return b, ms, clk.summary()
@@ -201,7 +242,7 @@ def time_decode_e2e(dev, steps: int, warmup: int, seed: int, batch=None):
     """Same workload through the public API with host buffers: each step copies its tokens from
     pinned host memory and reads its outputs back; copies are inside the timed region."""
     import torch
-    b = DecodeBench(dev, steps + warmup, seed, batch)
+    b = DecodeBench(dev, seed, batch)
     host = [t.cpu().pin_memory() for t in b.tok]
     dev_in = [torch.empty_like(t[0]) for t in b.tok]
     y_host = torch.empty(b.y.shape, dtype=b.y.dtype).pin_memory()
@@ -210,7 +251,7 @@ def time_decode_e2e(dev, steps: int, warmup: int, seed: int, batch=None):
 
     def one(k):
         for d_, h_ in zip(dev_in, host):
-            d_.copy_(h_[k], non_blocking=True)
+            d_.copy_(h_[k % TOKEN_RING], non_blocking=True)
         b.ers.replay_decode(b.cache, b.prm, *dev_in, status=b.status, check=False, out=b.y)
         y_host.copy_(b.y, non_blocking=True)
 
@@ -224,6 +265,7 @@ def time_decode_e2e(dev, steps: int, warmup: int, seed: int, batch=None):
     torch.cuda.synchronize()
     el = time.perf_counter() - t0
     _barrier()
+    b.status.raise_if_error("bench decode e2e")
     return el * 1e3, h2d, d2h
 
 
@@ -358,71 +400,78 @@ def bench_ssu(dev, steps: int, hbm: float):
 
 
 # ---------------------------------------------------------------------------------------------
+class _OracleDecode:
+    """The fp64 oracle advancing a sample of the B=256 decode workload token by token.
+
+    Tokens come from a small pre-generated ring (sequence-major, ready for the oracle's varlen
+    call) so that only the recurrence itself is timed; the state is carried from call to call."""
+
+    def __init__(self, seed: int, S: int, K: int, ring: int = 4):
+        import oracle
+        self.oracle = oracle
+        w = synth.workload("decode_b256_h64")
+        self.d = d = w.dims
+        self.threads = oracle.default_threads()
+        rng = np.random.Generator(np.random.PCG64(seed))
+        self.params = synth.make_params(rng, d.nheads)
+        self.S, self.K = S, K
+        order = np.arange(S * K).reshape(K, S).T.reshape(-1)
+        self.ring = []
+        for _ in range(ring):
+            t = synth.make_tokens(rng, S * K, d, True)
+            self.ring.append(tuple(np.ascontiguousarray(a[order]) for a in (t.x, t.dt, t.B, t.C)))
+        self.cu = np.arange(0, S * K + 1, K)
+        self.state = rng.standard_normal((S, d.nheads, d.headdim, d.dstate))
+        self.i = 0
+
+    def call(self):
+        x, dt, B, C = self.ring[self.i % len(self.ring)]
+        self.i += 1
+        p = self.params
+        _, self.state = self.oracle.recurrence(x, dt, p.A, B, C, p.D, p.dt_bias, self.cu, self.state,
+                                               nthreads=self.threads)
+        return self.S * self.K
+
+
 def cpu_baseline(seed: int, budget_s: float = 10.0):
     """fp64 oracle on this host's cores: decode seq-steps/s on a bounded sample of the B=256
-    workload (a subset of sequences advanced token by token from a prefilled state)."""
-    import oracle
-    w = synth.workload("decode_b256_h64")
-    d = w.dims
-    threads = oracle.default_threads()
-    rng = np.random.Generator(np.random.PCG64(seed))
-    params = synth.make_params(rng, d.nheads)
-
-    def run(S, K):
-        toks = synth.make_tokens(rng, S * K, d, True)
-        order = np.arange(S * K).reshape(K, S).T.reshape(-1)       # sequence-major stream
-        cu = np.arange(0, S * K + 1, K)
-        init = rng.standard_normal((S, d.nheads, d.headdim, d.dstate))
-        t0 = time.perf_counter()
-        oracle.recurrence(toks.x[order], toks.dt[order], params.A, toks.B[order], toks.C[order], params.D,
-                          params.dt_bias, cu, init, nthreads=threads)
-        return time.perf_counter() - t0
-
-    S = max(threads, 4)
-    t1 = run(S, 2)
-    K = int(max(2, min(64, budget_s / max(t1 / 2, 1e-6))))
-    el = run(S, K)
-    return {"value": S * K / el, "unit": "seq-steps/s", "cores": threads, "kind": "oracle",
-            "sample": f"{S} of the 256 sequences x {K} decode steps (fp64 recurrence, {d.nheads} heads, "
-                      f"headdim {d.headdim}, dstate {d.dstate}), {el:.1f} s"}
+    workload (32 of the sequences advanced 16 steps per call, state carried, for ~budget_s)."""
+    o = _OracleDecode(seed, S=32, K=16)
+    o.call()
+    done, t0 = 0, time.perf_counter()
+    while time.perf_counter() - t0 < budget_s:
+        done += o.call()
+    el = time.perf_counter() - t0
+    d = o.d
+    return {"value": done / el, "unit": "seq-steps/s", "cores": o.threads, "kind": "oracle",
+            "sample": f"{o.S} of the 256 sequences x {done // o.S} decode steps, state carried (fp64 recurrence, "
+                      f"{d.nheads} heads, headdim {d.headdim}, dstate {d.dstate}), {el:.1f} s"}
 
 
 def reference_arm(args):
-    """The fp64 oracle as the reference implementation, timed on host cores."""
+    """The fp64 oracle as the reference implementation, timed on host cores.  One step advances a
+    16-sequence sample of the B=256 workload by 4 tokens."""
     ws, rank, _ = _dist()
     if rank != 0:
         return 0
-    import oracle
-    w = synth.workload("decode_b256_h64")
-    d = w.dims
-    threads = oracle.default_threads()
-    rng = np.random.Generator(np.random.PCG64(1))
-    params = synth.make_params(rng, d.nheads)
-    S, K = max(threads, 4), 4          # one "step" = 4 decode steps of a 16-sequence sample
-    state = rng.standard_normal((S, d.nheads, d.headdim, d.dstate))
-
-    def step():
-        nonlocal state
-        toks = synth.make_tokens(rng, S * K, d, True)
-        order = np.arange(S * K).reshape(K, S).T.reshape(-1)
-        cu = np.arange(0, S * K + 1, K)
-        _, state = oracle.recurrence(toks.x[order], toks.dt[order], params.A, toks.B[order], toks.C[order],
-                                     params.D, params.dt_bias, cu, state, nthreads=threads)
-
+    o = _OracleDecode(1, S=16, K=4)
     for _ in range(args.warmup):
-        step()
+        o.call()
     t0 = time.perf_counter()
+    done = 0
     for _ in range(args.steps):
-        step()
+        done += o.call()
     el = time.perf_counter() - t0
-    v = S * K * args.steps / el
+    v = done / el
     line = {"impl": "reference", "metric": "replay-decode seq-steps/s per layer @B=256", "value": v,
             "unit": "seq-steps/s", "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": el * 1e3 / args.steps, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": "f64", "data": "synthetic",
-            "config": {"workload": "decode_b256_h64 (sampled)", "batch": 256, "sample_per_step": f"{S} seqs x {K} steps"},
-            "cpu_baseline": {"value": v, "unit": "seq-steps/s", "cores": threads, "kind": "oracle",
-                             "sample": f"{S} sequences x {K} decode steps per step, fp64 recurrence"},
+            "config": {"workload": "decode_b256_h64 (sampled)", "batch": 256,
+                       "sample_per_step": f"{o.S} seqs x {o.K} steps"},
+            "cpu_baseline": {"value": v, "unit": "seq-steps/s", "cores": o.threads, "kind": "oracle",
+                             "sample": f"{o.S} sequences x {o.K} decode steps per step, state carried, "
+                                       f"fp64 recurrence"},
             "e2e": {"value": v, "unit": "seq-steps/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line))
     return 0
@@ -432,7 +481,7 @@ def reference_arm(args):
 def main(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=1000)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")

@@ -306,6 +306,163 @@ __global__ void __launch_bounds__(kThreads) k_decode(LaunchArgs a) {
   }
 }
 
+// ---- replay decode for small chunks, shaped for HBM bandwidth -------------------------------------
+// Same arithmetic as k_decode (row_output, state_weights, chunk_state and fold_state, operation for
+// operation), laid out so that the boundary state streams from HBM once with 16-byte loads and is
+// reduced in registers.  One CTA per (sequence, head), 8 warps; warp w owns headdim rows
+// [RPW*w, RPW*w + RPW) and lane j holds elements [4j, 4j+4) of each, which is the lane split of
+// Dot<128>: the off-diagonal dot products reduce with the warp butterfly straight from the loaded
+// registers, and a fused refresh folds the new chunk state into the same registers.  The state
+// loads are issued before anything that depends on the slot's position, so they overlap the
+// buffer-row loads.  Rows of the chunk are scanned by one warp with shuffles: for rows < 32 the
+// strides >= 32 of chunk_scan leave every value unchanged, so the bits are those of chunk_scan.
+constexpr int kRowsWarps = kThreads / 32;
+
+template <typename HT> struct Quad;
+template <> struct Quad<float> {
+  __device__ __forceinline__ static void load(const float* p, float (&v)[4]) {
+    const float4 u = __ldcs(reinterpret_cast<const float4*>(p));
+    v[0] = u.x; v[1] = u.y; v[2] = u.z; v[3] = u.w;
+  }
+};
+template <> struct Quad<__nv_bfloat16> {
+  __device__ __forceinline__ static void load(const __nv_bfloat16* p, float (&v)[4]) {
+    const uint2 u = __ldcs(reinterpret_cast<const uint2*>(p));
+    const __nv_bfloat162 a = *reinterpret_cast<const __nv_bfloat162*>(&u.x);
+    const __nv_bfloat162 b = *reinterpret_cast<const __nv_bfloat162*>(&u.y);
+    v[0] = __low2float(a); v[1] = __high2float(a); v[2] = __low2float(b); v[3] = __high2float(b);
+  }
+};
+
+template <typename T, typename HT, int P, int N, int QM>
+__global__ void __launch_bounds__(kThreads, 4) k_decode_rows(LaunchArgs a) {
+  static_assert(N == 128 && P % kRowsWarps == 0, "lane split of Dot<128>, whole rows per warp");
+  static_assert(QM <= 32 && QM % kRowsWarps == 0, "one warp scans the chunk");
+  constexpr int RPW = P / kRowsWarps;
+  __shared__ float s_hi[32], s_lo[32], s_delta[32], s_M[QM], s_w[QM];
+  __shared__ float s_yoff[P];
+  __shared__ float s_x[QM * P];
+  __shared__ float s_B[QM * N];      // B rows, staged only when the chunk fills
+  const int i = blockIdx.x, h = blockIdx.y;
+  const int tid = threadIdx.x, w = tid >> 5, j = tid & 31;
+  int slot;
+  if (!resolve_slot(a, i, &slot)) return;
+  const bool rssm = (a.flags & ERS_FLAG_REPLAYSSM) != 0;
+  const size_t hs = (size_t)P * N;
+  const size_t soff = ((size_t)slot * a.H + h) * hs;
+  const HT* Hsrc = rssm ? (const HT*)a.read_copy + soff : (const HT*)(a.state + soff);
+  float hv[RPW][4];
+#pragma unroll
+  for (int r = 0; r < RPW; ++r) Quad<HT>::load(Hsrc + (size_t)(RPW * w + r) * N + 4 * j, hv[r]);
+  const int p = a.pos[slot];
+  if (p < 0 || p >= a.Q) {
+    if (tid == 0) report(a.status, ERS_EALIGN);
+    return;
+  }
+  const Rows<T> rows = make_rows<T>(a, slot, h, p, (long long)i - p);
+  float c[4];
+  load_k<T, 4>(rows.C(p) + 4 * j, c);
+  constexpr int SPW = QM / kRowsWarps;  // Gram rows per warp
+  float b[SPW][4];
+#pragma unroll
+  for (int k = 0; k < SPW; ++k) {
+    const int s = w + kRowsWarps * k;
+    if (s <= p) {
+      load_k<T, 4>(rows.B(s) + 4 * j, b[k]);
+    } else {
+#pragma unroll
+      for (int e = 0; e < 4; ++e) b[k][e] = 0.f;
+    }
+  }
+  for (int idx = tid; idx < (p + 1) * P; idx += kThreads) {
+    const int r = idx / P, d = idx % P;
+    s_x[idx] = to_f(rows.x(r)[d]);
+  }
+  const bool refresh = !rssm && (a.flags & ERS_FLAG_FUSE_REFRESH) && p + 1 == a.Q;
+  if (refresh)
+    for (int idx = tid; idx < (p + 1) * N; idx += kThreads) {
+      const int r = idx / N, n = idx % N;
+      s_B[idx] = to_f(rows.B(r)[n]);
+    }
+  if (w == 0) {
+    float dl = 0.f;
+    df v = {0.f, 0.f};
+    if (j <= p) {
+      dl = delta_of(rows.dt(j), a.dt_bias[h]);
+      v.hi = __fmul_rn(dl, a.A[h]);
+    }
+#pragma unroll
+    for (int st = 1; st < 32; st <<= 1) {
+      const float ph = __shfl_up_sync(kFull, v.hi, st), pl = __shfl_up_sync(kFull, v.lo, st);
+      if (j >= st) v = df_add(df{ph, pl}, v);
+    }
+    s_hi[j] = v.hi;
+    s_lo[j] = v.lo;
+    s_delta[j] = dl;
+  }
+  __syncthreads();
+  const df at = {s_hi[p], s_lo[p]};
+#pragma unroll
+  for (int k = 0; k < SPW; ++k) {
+    const int s = w + kRowsWarps * k;
+    const float g = Dot<N>::reduce(Dot<N>::partial(c, b[k]));
+    if (s <= p && j == 0)
+      s_M[s] = __fmul_rn(__fmul_rn(g, s_delta[s]), expf(df_diff(at, df{s_hi[s], s_lo[s]})));
+  }
+#pragma unroll
+  for (int r = 0; r < RPW; ++r) {
+    const float v = Dot<N>::reduce(Dot<N>::partial(c, hv[r]));
+    if (j == r) s_yoff[RPW * w + r] = v;
+  }
+  if (refresh && tid <= p)
+    s_w[tid] = __fmul_rn(s_delta[tid], expf(df_diff(at, df{s_hi[tid], s_lo[tid]})));
+  __syncthreads();
+  if (tid < P) {
+    float acc = 0.f;
+    for (int s = 0; s <= p; ++s) acc = __fmaf_rn(s_M[s], s_x[s * P + tid], acc);
+    ((T*)a.y)[((size_t)i * a.H + h) * P + tid] =
+        from_f<T>(combine_out(expf(at.hi), s_yoff[tid], acc, a.D[h], s_x[p * P + tid]));
+  } else if (tid < 2 * P) {
+    const int d = tid - P;
+    ((T*)a.bx)[(((size_t)slot * a.Q + p) * a.H + h) * P + d] = ((const T*)a.x)[((size_t)i * a.H + h) * P + d];
+    if (d == 0) a.bdt[((size_t)slot * a.Q + p) * a.H + h] = a.dt[(size_t)i * a.H + h];
+  } else if (h % (a.H / a.G) == 0) {
+    const int g = h / (a.H / a.G);
+    const size_t dst = (((size_t)slot * a.Q + p) * a.G + g) * N, src = ((size_t)i * a.G + g) * N;
+    for (int n = tid - 2 * P; n < N; n += kThreads - 2 * P) {
+      ((T*)a.bB)[dst + n] = ((const T*)a.B)[src + n];
+      ((T*)a.bC)[dst + n] = ((const T*)a.C)[src + n];
+    }
+  }
+  if (!refresh) return;
+  // the chunk filled: H' = exp(Acum_last) H + sum_s (w_s x_s) B_s^T, row by row in registers
+  const float decay = expf(s_hi[p]);
+  float* Hd = a.state + soff;
+  __nv_bfloat16* Rd = a.read_copy ? (__nv_bfloat16*)a.read_copy + soff : nullptr;
+#pragma unroll
+  for (int r = 0; r < RPW; ++r) {
+    const int d = RPW * w + r;
+    float acc[4] = {0.f, 0.f, 0.f, 0.f};
+    for (int s = 0; s <= p; ++s) {
+      const float wx = __fmul_rn(s_w[s], s_x[s * P + d]);
+#pragma unroll
+      for (int e = 0; e < 4; ++e) acc[e] = __fmaf_rn(wx, s_B[s * N + 4 * j + e], acc[e]);
+    }
+    float v[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) v[e] = __fmaf_rn(decay, hv[r][e], acc[e]);
+    const size_t o = (size_t)d * N + 4 * j;
+    *reinterpret_cast<float4*>(Hd + o) = make_float4(v[0], v[1], v[2], v[3]);
+    if (Rd != nullptr) {
+      __nv_bfloat162 lo2 = __floats2bfloat162_rn(v[0], v[1]), hi2 = __floats2bfloat162_rn(v[2], v[3]);
+      uint2 u;
+      u.x = *reinterpret_cast<uint32_t*>(&lo2);
+      u.y = *reinterpret_cast<uint32_t*>(&hi2);
+      *reinterpret_cast<uint2*>(Rd + o) = u;
+    }
+  }
+}
+
 // ---- refresh (exact: pos == Q; ReplaySSM: pos + T > L) ---------------------------------------------
 template <typename T, int P, int N>
 __global__ void __launch_bounds__(kThreads) k_refresh(LaunchArgs a) {
@@ -507,6 +664,20 @@ cudaError_t prefill_impl(const LaunchArgs& a, Op op, cudaStream_t s) {
 
 template <typename T, int P, int N>
 cudaError_t decode_impl(const LaunchArgs& a, cudaStream_t s) {
+  if constexpr (N == 128 && P % kRowsWarps == 0) {
+    const dim3 grid(a.nseq, a.H);
+    const bool rssm = (a.flags & ERS_FLAG_REPLAYSSM) != 0;
+    if (a.Q <= 16) {
+      if (rssm) k_decode_rows<T, __nv_bfloat16, P, N, 16><<<grid, kThreads, 0, s>>>(a);
+      else k_decode_rows<T, float, P, N, 16><<<grid, kThreads, 0, s>>>(a);
+      return launch_setpos(a, 0, s);
+    }
+    if (a.Q <= 32) {
+      if (rssm) k_decode_rows<T, __nv_bfloat16, P, N, 32><<<grid, kThreads, 0, s>>>(a);
+      else k_decode_rows<T, float, P, N, 32><<<grid, kThreads, 0, s>>>(a);
+      return launch_setpos(a, 0, s);
+    }
+  }
   const size_t sm = fma_smem_bytes(a.Q, P);
   cudaError_t e = prep(k_decode<T, P, N>, sm);
   if (e != cudaSuccess) return e;

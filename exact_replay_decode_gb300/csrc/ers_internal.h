@@ -67,15 +67,17 @@ cudaError_t launch_commit(const LaunchArgs& a, cudaStream_t s);
 cudaError_t launch_tail(const LaunchArgs& a, cudaStream_t s);
 cudaError_t launch_chain(const LaunchArgs& a, bool chunked, cudaStream_t s);
 
-// tensor-core engine (bf16 io, P = 64, N = 128, Q % 16 == 0), ers_tc.cu
+// tensor-core engine (bf16 io, P = 64, N = 128, Q % 16 == 0, Q >= kTcMinChunk), ers_tc.cu.  Each
+// configuration runs every path on ONE engine (bitwise identity needs identical arithmetic):
+// chunks of at least kTcMinChunk tokens make the intra-chunk products dense enough for the tensor
+// cores; below that a decode step is a bandwidth-bound matrix-vector product and the CUDA-core
+// engine defines the arithmetic.
+constexpr int kTcMinChunk = 64;
 bool tc_supported(int io, int P, int N, int Q);
 cudaError_t tc_prefill(const LaunchArgs& a, Op op, cudaStream_t s);
 cudaError_t tc_decode(const LaunchArgs& a, cudaStream_t s);
 cudaError_t tc_refresh(const LaunchArgs& a, cudaStream_t s);
 cudaError_t tc_verify(const LaunchArgs& a, cudaStream_t s);
-// group-batched persistent decode (chunk <= 16), ers_tc_decode_group.cu
-bool tc_decode_group_supported(int Q);
-cudaError_t tc_decode_group(const LaunchArgs& a, cudaStream_t s);
 
 // SSU baseline, ers_ssu.cu
 cudaError_t ssu_update(const LaunchArgs& a, cudaStream_t s);

@@ -466,7 +466,7 @@ size_t state_smem(int K) { return kHdrBytes + (size_t)K * (256 + 128) + kUBytes 
 }  // namespace
 
 bool tc_supported(int io, int P_, int N_, int Q) {
-  return io == ERS_DTYPE_BF16 && P_ == P && N_ == N && Q % 16 == 0 && Q >= 16 && Q <= kQMax;
+  return io == ERS_DTYPE_BF16 && P_ == P && N_ == N && Q % 16 == 0 && Q >= kTcMinChunk && Q <= kQMax;
 }
 
 cudaError_t tc_prefill(const LaunchArgs& a, Op op, cudaStream_t s) {
@@ -495,7 +495,6 @@ cudaError_t tc_prefill(const LaunchArgs& a, Op op, cudaStream_t s) {
 }
 
 cudaError_t tc_decode(const LaunchArgs& a, cudaStream_t s) {
-  if (tc_decode_group_supported(a.Q)) return tc_decode_group(a, s);
   const size_t so = out_smem(a.Q);
   cudaError_t e = set_smem(k_tc_decode, so);
   if (e != cudaSuccess) return e;

@@ -68,3 +68,25 @@ def test_reference_arm_other_ranks_exit_quietly():
     r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference", "--steps", "1",
                         "--warmup", "3"], capture_output=True, text=True, timeout=600, cwd=ROOT, env=env)
     assert r.returncode == 0 and r.stdout.strip() == ""
+
+
+def test_clock_summary_keeps_only_samples_inside_the_timed_region():
+    import datetime
+    sys.path.insert(0, ROOT)
+    import bench
+    c = bench.ClockSampler(0)
+    c.lines = ["2026/12/02 06:00:00.000, 0, 1000, 2070, 500.0, 0x0, Not Active, Not Active, Not Active, Not Active",
+               "2026/12/02 06:00:01.000, 0, 1900, 2070, 900.0, 0x4, Not Active, Not Active, Not Active, Active",
+               "2026/12/02 06:00:01.100, 0, 1950, 2070, 900.0, 0x0, Not Active, Not Active, Not Active, Not Active",
+               "2026/12/02 06:00:01.200, 0, 2000, 2070, 900.0, 0x0, Not Active, Not Active, Not Active, Not Active",
+               "2026/12/02 06:00:09.000, 0, 300, 2070, 90.0, 0x8, Active, Not Active, Not Active, Not Active",
+               "garbled"]
+    c.t_start = datetime.datetime(2026, 12, 2, 6, 0, 0, 500000)
+    c.t_stop = datetime.datetime(2026, 12, 2, 6, 0, 2)
+    s = c.summary()
+    assert s["samples"] == 3 and s["sm_mhz"] == 1950 and s["sm_max_mhz"] == 2070
+    assert s["reasons"] == ["sw_power_cap"] and s["window"] == "timed region"
+    c.t_start = datetime.datetime(2026, 12, 2, 7)
+    c.t_stop = datetime.datetime(2026, 12, 2, 8)
+    s = c.summary()
+    assert s["samples"] == 5 and "hw_slowdown" in s["reasons"]

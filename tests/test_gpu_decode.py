@@ -118,3 +118,29 @@ def test_decode_slot_indirection_and_subset():
     others = [i for i in range(S) if i not in (9, 2, 14)]
     assert same_bits(c2.state[others], before[others])
     assert torch.equal(c2.pos[sel.long()], c1.pos[sel.long()])
+
+
+@pytest.mark.parametrize("chunk", [32, 64, 128])
+def test_decode_bitwise_across_engines_and_chunk_sizes(chunk):
+    """Chunk 32 runs on the CUDA-core engine's bandwidth-shaped decode, chunks >= 64 on the
+    tensor-core engine: in each, decode by replay equals single-shot prefill bit for bit and
+    matches the oracle, across several refreshes."""
+    import dataclasses
+    ers = _ers()
+    base = synth.workload("decode_b256_h64")
+    w = dataclasses.replace(base, dims=synth.Dims(16, 2, 64, 128, chunk), batch=12, steps=chunk + 40,
+                            history_chunks=1)
+    S, K = w.batch, w.steps
+    params, prm, hist, p0, stream, cache, (sx, sdt, sB, sC) = _setup(w, S, K, seed=11)
+    ys = torch.stack([ers.replay_decode(cache, prm, sx[k], sdt[k], sB[k], sC[k]) for k in range(K)])
+    parts, cu, y_ss, fin = _single_shot(w, prm, hist, stream, S, K)
+    for i in range(S):
+        ref = y_ss[int(cu[i]) + hist[i].ntokens:int(cu[i + 1])]
+        assert same_bits(ys[:, i], ref), f"sequence {i} (p0={p0[i]})"
+    for i in (0, S - 1):
+        p = parts[i]
+        y_o, _ = oracle.recurrence(p.x, p.dt, params.A, p.B, p.C, params.D, params.dt_bias)
+        assert out_err(ys[:, i], y_o[hist[i].ntokens:]) <= 2e-3
+        nb = (p.ntokens // chunk) * chunk
+        _, s_o = oracle.recurrence(p.x[:nb], p.dt[:nb], params.A, p.B[:nb], p.C[:nb], params.D, params.dt_bias)
+        assert state_err(cache.state[i], s_o[0]) <= STATE_TOL

@@ -33,22 +33,18 @@ def _prefilled(w, S, steps, seed, history=32):
     return params, prm, hist, drafts, acc, cache
 
 
-def test_verify_b512_matches_nonspec_decode_and_oracle():
+def _verify_vs_nonspec(w, S, K, seed, samples):
     ers = _ers()
-    w = synth.workload("verify_b512_t4")
-    S, K, T, L = w.batch, w.steps, w.drafts, w.dims.chunk
-    params, prm, hist, drafts, acc, cache = _prefilled(w, S, K, seed=0)
-    ref = _prefilled(w, S, K, seed=0)[-1]                     # identical starting cache for the comparator
+    T, L = w.drafts, w.dims.chunk
+    params, prm, hist, drafts, acc, cache = _prefilled(w, S, K, seed=seed)
+    ref = _prefilled(w, S, K, seed=seed)[-1]                  # identical starting cache for the comparator
     assert same_bits(cache.read_copy, ref.read_copy)
     dx, ddt, dB, dC = torch_io.tokens_to(drafts, dev(), lead=(K, S, T))
     acc_t = torch.from_numpy(acc).to(dev())
-    samples = [0, 1, 200, 511]
     model = oracle.ReplaySSMModel(params, _oracle_anchor(params, hist, samples, 32), L)
-    ys_all = []
     for k in range(K):
         y = ers.spec_verify(cache, prm, dx[k], ddt[k], dB[k], dC[k])
         ers.commit(cache, acc_t[k], T)
-        ys_all.append(y)
         # non-speculative comparator: same flush decisions, then one accepted token at a time
         ers.refresh(ref, prm, replayssm=True, drafts_T=T)
         a = acc[k]
@@ -72,6 +68,19 @@ def test_verify_b512_matches_nonspec_decode_and_oracle():
     assert np.array_equal(cache.pos.cpu().numpy()[samples], model.h())
     assert state_err(cache.state[samples], model.anchor) <= STATE_TOL
     assert model.flushes > 0
+
+
+def test_verify_b512_matches_nonspec_decode_and_oracle():
+    w = synth.workload("verify_b512_t4")
+    _verify_vs_nonspec(w, w.batch, w.steps, 0, [0, 1, 200, 511])
+
+
+def test_verify_tensor_core_engine_chunk64():
+    """Chunk 64 runs verify, commit, flush and ReplaySSM decode on the tensor-core engine."""
+    import dataclasses
+    base = synth.workload("verify_b512_t4")
+    w = dataclasses.replace(base, dims=synth.Dims(16, 2, 64, 128, 64))
+    _verify_vs_nonspec(w, 12, 40, 3, [0, 5, 11])
 
 
 def _oracle_anchor(params, hist, samples, history):
