@@ -44,6 +44,25 @@ PREFILL_FLOPS = {"prefill_2048_h32": 3.29e9, "varlen_4seq_h64": 11.38e9}
 L2_FLUSH_BYTES = 256 << 20
 
 
+DECODE_PROFILE = os.path.join(ROOT, "profiles", "k_decode_heads.decode_b256_h64.md")
+DECODE_SOURCE = os.path.join(ROOT, "exact_replay_decode_gb300", "csrc", "ers_decode.cu")
+
+
+def profiled_traffic(profile: str = DECODE_PROFILE, source: str = DECODE_SOURCE):
+    """DRAM bytes per launch (dram__bytes_read.sum + dram__bytes_write.sum) from the committed ncu
+    summary, or None when the kernel source has changed since the capture (or no record exists)."""
+    import hashlib
+    import re
+    try:
+        text = open(profile).read()
+        want = re.search(r"kernel_source_sha256 = ([0-9a-f]{64})", text).group(1)
+        traffic = int(re.search(r"traffic_per_launch_bytes = (\d+)", text).group(1))
+        have = hashlib.sha256(open(source, "rb").read()).hexdigest()
+    except (OSError, AttributeError):
+        return None
+    return traffic if have == want else None
+
+
 def _peaks():
     try:
         with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
@@ -536,8 +555,8 @@ def main(argv=None):
                    "batch_per_gpu": S, "global_batch": S * ws, "parallelism": f"replicas x{ws} (independent sequences)",
                    "l2": "inputs larger than L2 (512 MiB fp32 checkpoints per step)"},
         "roofline": {"bound": "hbm", "achieved": ach, "peak": hbm, "unit": "GB/s", "frac": ach / hbm,
-                     "traffic": None, "peak_kind": f"{peak_kind} copy bandwidth",
-                     "kernel": "replay decode step (decode kernel + position advance)",
+                     "traffic": profiled_traffic(), "peak_kind": f"{peak_kind} copy bandwidth (burst)",
+                     "kernel": "k_decode_heads + k_setpos (one replay-decode step; time is the whole step)",
                      "algorithmic_bytes_per_launch": DECODE_BYTES_PER_SEQ_STEP * S},
         "e2e": {"value": S * args.steps * ws / (e2e_ms * 1e-3), "unit": "seq-steps/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},

@@ -1,0 +1,324 @@
+// Replay decode for small chunks (chunk <= 32, P a multiple of 32, N = 128): the bandwidth-shaped
+// decode kernel of the CUDA-core engine.
+//
+// A decode step at a small chunk is, per head, a matrix-vector product with the fp32 boundary
+// checkpoint plus a replay of at most 31 buffered rows (exact-replay RFC, section 3), so its cost is
+// streaming the checkpoint from HBM.  The arithmetic is the engine's, operation for operation
+// (row_output, state_weights, chunk_state, fold_state in ers_fma.cu; Dot<128> and chunk_scan in
+// ers_common.cuh), so decode equals single-shot and chunked prefill bit for bit.
+#include "ers_common.cuh"
+#include "ers_internal.h"
+#include "tc_common.cuh"
+
+namespace ers {
+namespace {
+
+template <typename K>
+cudaError_t prep(K kernel, size_t smem) {
+  return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+}
+
+// ---- replay decode for small chunks, shaped for HBM bandwidth -------------------------------------
+// Same arithmetic as k_decode (row_output, state_weights, chunk_state and fold_state, operation for
+// operation), organised so that a step costs little more than streaming the boundary state once.
+//  * One CTA per (sequence, block of up to 8 heads of one B/C group), one warp per head.  The warp
+//    streams its head's [P x N] state through registers, 8 rows at a time, two blocks in flight;
+//    lane j holds elements [4j, 4j+4) of each row, the lane split of Dot<128>.
+//  * The 32 lane partials of 32 rows are combined by a reduce-scatter whose pairings are those of
+//    Dot<128>'s butterfly (xor 16, 8, 4, 2, 1): each stage halves the rows a lane keeps, and lane j
+//    ends with row j's dot product, bit-identical to the butterfly (same tree; fp32 addition is
+//    commutative) at about one shuffle per row instead of five.
+//  * The group's Gram row C_p . B_s is computed once per CTA; buffer rows arrive by cp.async while
+//    the state streams; the log-decay scan runs per warp with shuffles (for rows < 32 the strides
+//    >= 32 of chunk_scan change nothing, so the bits are chunk_scan's).
+//  * When the step fills the chunk, the state is streamed after the chunk's weights are known and
+//    each row is folded (fold_state) and written back in the same pass.
+constexpr int kHeadsPerCta = kThreads / 32;
+
+template <typename HT> struct Quad;
+template <> struct Quad<float> {
+  using raw = float4;
+  __device__ __forceinline__ static raw ld_stream(const float* p) { return __ldcs(reinterpret_cast<const float4*>(p)); }
+  __device__ __forceinline__ static void unpack(raw u, float (&v)[4]) {
+    v[0] = u.x; v[1] = u.y; v[2] = u.z; v[3] = u.w;
+  }
+};
+template <> struct Quad<__nv_bfloat16> {
+  using raw = uint2;
+  __device__ __forceinline__ static raw ld_stream(const __nv_bfloat16* p) {
+    return __ldcs(reinterpret_cast<const uint2*>(p));
+  }
+  __device__ __forceinline__ static void unpack(raw u, float (&v)[4]) {
+    const __nv_bfloat162 a = *reinterpret_cast<const __nv_bfloat162*>(&u.x);
+    const __nv_bfloat162 b = *reinterpret_cast<const __nv_bfloat162*>(&u.y);
+    v[0] = __low2float(a); v[1] = __high2float(a); v[2] = __low2float(b); v[3] = __high2float(b);
+  }
+};
+
+// four consecutive io elements from shared memory, widened
+__device__ __forceinline__ void lds4(const float* p, float (&v)[4]) {
+  const float4 u = *reinterpret_cast<const float4*>(p);
+  v[0] = u.x; v[1] = u.y; v[2] = u.z; v[3] = u.w;
+}
+__device__ __forceinline__ void lds4(const __nv_bfloat16* p, float (&v)[4]) {
+  Quad<__nv_bfloat16>::unpack(*reinterpret_cast<const uint2*>(p), v);
+}
+
+// Reduce-scatter of 16 rows' lane partials v[0..15] with the pairings of Dot<128>'s butterfly
+// (xor 16, 8, 4, 2, then 1 on the single remaining row): lane j returns row (j >> 1)'s reduction,
+// bit-identical to Dot<128>::reduce of that row (same tree; fp32 addition is commutative).
+__device__ __forceinline__ float reduce_scatter16(float (&v)[16], int j) {
+#pragma unroll
+  for (int o = 16, n = 16; o >= 2; o >>= 1, n >>= 1) {
+    const bool up = (j & o) != 0;
+#pragma unroll
+    for (int r = 0; r < n / 2; ++r) {
+      const float keep = up ? v[r + n / 2] : v[r];
+      const float send = up ? v[r] : v[r + n / 2];
+      v[r] = __fadd_rn(keep, __shfl_xor_sync(kFull, send, o));
+    }
+  }
+  return __fadd_rn(v[0], __shfl_xor_sync(kFull, v[0], 1));
+}
+
+__device__ __forceinline__ void cp_async16(void* dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(tc::smem_u32(dst)), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() {
+  asm volatile("cp.async.commit_group;\ncp.async.wait_group 0;" ::: "memory");
+}
+
+template <typename T, int P, int N, int QM>
+constexpr size_t heads_smem_bytes() {
+  return (size_t)QM * N * sizeof(T) + (size_t)kHeadsPerCta * QM * P * sizeof(T) + QM * sizeof(float) +
+         (size_t)kHeadsPerCta * (P + QM) * sizeof(float);
+}
+
+// Streams one head's state: lane j of row d reads elements [4j, 4j+4), 8 rows per block, two
+// blocks in flight (q holds rows 0..15 on entry).  yo[d] ends with the off-diagonal term (H C_p)[d]
+// (per-warp shared memory).
+template <typename HT, int P, int N>
+__device__ __forceinline__ void stream_state(const HT* __restrict__ Hsrc, typename Quad<HT>::raw (&q)[16],
+                                             const float (&c)[4], float* yo, int j) {
+  constexpr int NBLK = P / 8;
+  float part[16];
+#pragma unroll
+  for (int blk = 0; blk < NBLK; ++blk) {
+    const int sl = (blk & 1) * 8;
+#pragma unroll
+    for (int r = 0; r < 8; ++r) {
+      const int d = blk * 8 + r;
+      float h[4];
+      Quad<HT>::unpack(q[sl + r], h);
+      part[sl + r] = Dot<N>::partial(c, h);
+      if (blk + 2 < NBLK) q[sl + r] = Quad<HT>::ld_stream(Hsrc + (size_t)(d + 16) * N + 4 * j);
+    }
+    if (blk & 1) {
+      const float v = reduce_scatter16(part, j);
+      if ((j & 1) == 0) yo[(blk - 1) * 8 + (j >> 1)] = v;
+    }
+  }
+  __syncwarp();
+}
+
+// The same stream for a step that fills the chunk: each row is also folded with the chunk state,
+// H'[d] = exp(Acum_last) H[d] + sum_s (w_s x_s[d]) B_s (chunk_state / fold_state order; weights
+// sw[s] in shared memory), and written to Hd and, if present, the bf16 copy Rd.  Rows go 8 at a
+// time so that 32 independent accumulation chains hide the FMA latency.
+template <typename T, int P, int N>
+__device__ __noinline__ void stream_state_refresh(const float* __restrict__ Hsrc, const float (&c)[4], float* yo,
+                                                  int j, int p, const float* sw, float decay, const T* sB,
+                                                  const T* sx, float* Hd, __nv_bfloat16* Rd) {
+#pragma unroll 1
+  for (int d0 = 0; d0 < P; d0 += 16) {
+    float part[16];
+#pragma unroll
+    for (int half = 0; half < 2; ++half) {
+      const int db = d0 + 8 * half;
+      float h[8][4], acc[8][4];
+#pragma unroll
+      for (int r = 0; r < 8; ++r) {
+        Quad<float>::unpack(__ldcs(reinterpret_cast<const float4*>(Hsrc + (size_t)(db + r) * N + 4 * j)), h[r]);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) acc[r][e] = 0.f;
+      }
+      for (int s = 0; s <= p; ++s) {
+        float bs[4];
+        lds4(sB + s * N + 4 * j, bs);
+        const float ws = sw[s];
+#pragma unroll
+        for (int r = 0; r < 8; ++r) {
+          const float wx = __fmul_rn(ws, to_f(sx[s * P + db + r]));
+#pragma unroll
+          for (int e = 0; e < 4; ++e) acc[r][e] = __fmaf_rn(wx, bs[e], acc[r][e]);
+        }
+      }
+#pragma unroll
+      for (int r = 0; r < 8; ++r) {
+        part[8 * half + r] = Dot<N>::partial(c, h[r]);
+        float v[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) v[e] = __fmaf_rn(decay, h[r][e], acc[r][e]);
+        const size_t o = (size_t)(db + r) * N + 4 * j;
+        *reinterpret_cast<float4*>(Hd + o) = make_float4(v[0], v[1], v[2], v[3]);
+        if (Rd != nullptr) {
+          __nv_bfloat162 lo2 = __floats2bfloat162_rn(v[0], v[1]), hi2 = __floats2bfloat162_rn(v[2], v[3]);
+          uint2 u;
+          u.x = *reinterpret_cast<uint32_t*>(&lo2);
+          u.y = *reinterpret_cast<uint32_t*>(&hi2);
+          *reinterpret_cast<uint2*>(Rd + o) = u;
+        }
+      }
+    }
+    const float v = reduce_scatter16(part, j);
+    if ((j & 1) == 0) yo[d0 + (j >> 1)] = v;
+  }
+  __syncwarp();
+}
+
+template <typename T, typename HT, int P, int N, int QM>
+__global__ void __launch_bounds__(kThreads, 2) k_decode_heads(LaunchArgs a) {
+  static_assert(N == 128 && P % 32 == 0, "lane split of Dot<128>; 32-row reduction blocks");
+  static_assert(QM <= 32, "one warp scans the chunk");
+  extern __shared__ __align__(16) unsigned char hsm[];
+  T* sB = reinterpret_cast<T*>(hsm);                                  // [QM][N] group B rows 0..p
+  T* sxa = sB + QM * N;                                               // [warp][QM][P] x rows 0..p
+  float* sg = reinterpret_cast<float*>(sxa + kHeadsPerCta * QM * P);  // [QM] Gram row
+  float* syo = sg + QM;                                               // [warp][P] off-diagonal terms
+  float* swa = syo + kHeadsPerCta * P;                                // [warp][QM] chunk-state weights
+  const int tid = threadIdx.x, w = tid >> 5, j = tid & 31;
+  const int i = blockIdx.y;
+  const int hpg = a.H / a.G, nbl = (hpg + kHeadsPerCta - 1) / kHeadsPerCta;
+  const int g = blockIdx.x / nbl, hb = blockIdx.x % nbl;
+  const int hl = hb * kHeadsPerCta + w;  // head within the group
+  const bool active = hl < hpg;
+  const int h = g * hpg + (active ? hl : 0);
+  int slot;
+  if (!resolve_slot(a, i, &slot)) return;
+  const bool rssm = (a.flags & ERS_FLAG_REPLAYSSM) != 0;
+  const size_t HP = (size_t)a.H * P, GN = (size_t)a.G * N;
+  const size_t soff = ((size_t)slot * a.H + h) * P * N;
+  const HT* Hsrc = rssm ? (const HT*)((const __nv_bfloat16*)a.read_copy + soff) : (const HT*)(a.state + soff);
+  const int p = a.pos[slot];
+  float c[4];
+  load_k<T, 4>((const T*)a.C + (size_t)i * GN + (size_t)g * N + 4 * j, c);
+  typename Quad<HT>::raw q[16];
+  if (active) {
+#pragma unroll
+    for (int r = 0; r < 16; ++r) q[r] = Quad<HT>::ld_stream(Hsrc + (size_t)r * N + 4 * j);
+  }
+  if (p < 0 || p >= a.Q) {
+    if (tid == 0) report(a.status, ERS_EALIGN);
+    return;
+  }
+  const bool refresh = !rssm && (a.flags & ERS_FLAG_FUSE_REFRESH) && p + 1 == a.Q;
+  // buffer rows 0..p-1 and the new token as row p: the group's B rows, this head's x rows
+  const T* bB = (const T*)a.bB + (size_t)slot * a.Q * GN + (size_t)g * N;
+  const T* nB = (const T*)a.B + (size_t)i * GN + (size_t)g * N;
+  constexpr int kBChunks = N * sizeof(T) / 16, kXChunks = P * sizeof(T) / 16;
+  for (int k = tid; k < (p + 1) * kBChunks; k += kThreads) {
+    const int s = k / kBChunks, e = k % kBChunks;
+    cp_async16(reinterpret_cast<char*>(sB + s * N) + 16 * e,
+               reinterpret_cast<const char*>(s < p ? bB + s * GN : nB) + 16 * e);
+  }
+  T* sx = sxa + w * QM * P;
+  const T* bx = (const T*)a.bx + (size_t)slot * a.Q * HP + (size_t)h * P;
+  const T* nx = (const T*)a.x + (size_t)i * HP + (size_t)h * P;
+  if (active)
+    for (int k = j; k < (p + 1) * kXChunks; k += 32) {
+      const int s = k / kXChunks, e = k % kXChunks;
+      cp_async16(reinterpret_cast<char*>(sx + s * P) + 16 * e,
+                 reinterpret_cast<const char*>(s < p ? bx + s * HP : nx) + 16 * e);
+    }
+  const float dt_raw = j <= p ? (j < p ? a.bdt[((size_t)slot * a.Q + j) * a.H + h] : a.dt[(size_t)i * a.H + h]) : 0.f;
+  const float Ah = a.A[h], bias = a.dt_bias[h];
+  float* yo = syo + w * P;
+  if (!refresh && active)
+    stream_state<HT, P, N>(Hsrc, q, c, yo, j);
+  float dl = 0.f;
+  df v = {0.f, 0.f};
+  if (j <= p) {
+    dl = delta_of(dt_raw, bias);
+    v.hi = __fmul_rn(dl, Ah);
+  }
+  cp_async_wait_all();
+  __syncthreads();
+  // the group's Gram row, split over the warps
+  for (int s = w; s <= p; s += kHeadsPerCta) {
+    float bs[4];
+    lds4(sB + s * N + 4 * j, bs);
+    const float gv = Dot<N>::reduce(Dot<N>::partial(c, bs));
+    if (j == 0) sg[s] = gv;
+  }
+  // this head's log-decay prefix (lane s holds row s)
+#pragma unroll
+  for (int st = 1; st < 32; st <<= 1) {
+    const float ph = __shfl_up_sync(kFull, v.hi, st), pl = __shfl_up_sync(kFull, v.lo, st);
+    if (j >= st) v = df_add(df{ph, pl}, v);
+  }
+  const df at = {__shfl_sync(kFull, v.hi, p), __shfl_sync(kFull, v.lo, p)};
+  __syncthreads();
+  if (!active) return;
+  float M = 0.f;
+  if (j <= p) M = __fmul_rn(__fmul_rn(sg[j], dl), expf(df_diff(at, v)));
+  if (refresh) {
+    float* sw = swa + w * QM;
+    if (j <= p) sw[j] = __fmul_rn(dl, expf(df_diff(at, v)));
+    __syncwarp();
+    __nv_bfloat16* Rd = a.read_copy ? (__nv_bfloat16*)a.read_copy + soff : nullptr;
+    stream_state_refresh<T, P, N>(a.state + soff, c, yo, j, p, sw, expf(at.hi), sB, sx, a.state + soff, Rd);
+  }
+  // outputs d = 32k + j
+  const float et = expf(at.hi), Dh = a.D[h];
+  T* y = (T*)a.y + (size_t)i * HP + (size_t)h * P;
+#pragma unroll
+  for (int k = 0; k < P / 32; ++k) {
+    const int d = 32 * k + j;
+    float acc = 0.f;
+    for (int s = 0; s <= p; ++s) acc = __fmaf_rn(__shfl_sync(kFull, M, s), to_f(sx[s * P + d]), acc);
+    y[d] = from_f<T>(combine_out(et, yo[d], acc, Dh, to_f(sx[p * P + d])));
+  }
+  // append the new token to the buffer (B/C once per group)
+  T* dx = (T*)a.bx + ((size_t)slot * a.Q + p) * HP + (size_t)h * P;
+  for (int d = j; d < P; d += 32) dx[d] = sx[p * P + d];
+  if (j == 0) a.bdt[((size_t)slot * a.Q + p) * a.H + h] = a.dt[(size_t)i * a.H + h];
+  if (hl == 0) {
+    const size_t dst = ((size_t)slot * a.Q + p) * GN + (size_t)g * N, src = (size_t)i * GN + (size_t)g * N;
+    for (int n = j; n < N; n += 32) {
+      ((T*)a.bB)[dst + n] = sB[p * N + n];
+      ((T*)a.bC)[dst + n] = ((const T*)a.C)[src + n];
+    }
+  }
+}
+
+template <typename T, int P, int N, int QM>
+cudaError_t launch_decode_heads(const LaunchArgs& a, cudaStream_t s) {
+  const int hpg = a.H / a.G, nbl = (hpg + kHeadsPerCta - 1) / kHeadsPerCta;
+  const dim3 grid(a.G * nbl, a.nseq);
+  constexpr size_t sm = heads_smem_bytes<T, P, N, QM>();
+  cudaError_t e;
+  if (a.flags & ERS_FLAG_REPLAYSSM) {
+    if ((e = prep(k_decode_heads<T, __nv_bfloat16, P, N, QM>, sm)) != cudaSuccess) return e;
+    k_decode_heads<T, __nv_bfloat16, P, N, QM><<<grid, kThreads, sm, s>>>(a);
+  } else {
+    if ((e = prep(k_decode_heads<T, float, P, N, QM>, sm)) != cudaSuccess) return e;
+    k_decode_heads<T, float, P, N, QM><<<grid, kThreads, sm, s>>>(a);
+  }
+  return launch_setpos(a, 0, s);
+}
+
+}  // namespace
+
+bool heads_decode_supported(int P, int N, int Q) { return N == 128 && (P == 64) && Q >= 1 && Q <= 32; }
+
+cudaError_t heads_decode(const LaunchArgs& a, cudaStream_t s) {
+  constexpr int P = 64, N = 128;
+  if (a.io == ERS_DTYPE_BF16) {
+    if (a.Q <= 16) return launch_decode_heads<__nv_bfloat16, P, N, 16>(a, s);
+    return launch_decode_heads<__nv_bfloat16, P, N, 32>(a, s);
+  }
+  if (a.Q <= 16) return launch_decode_heads<float, P, N, 16>(a, s);
+  return launch_decode_heads<float, P, N, 32>(a, s);
+}
+
+}  // namespace ers

@@ -61,6 +61,10 @@ cudaError_t fma_refresh(const LaunchArgs& a, cudaStream_t s);
 cudaError_t fma_verify(const LaunchArgs& a, cudaStream_t s);
 bool fma_supported(int P, int N);
 
+// warp-per-head replay decode of the CUDA-core engine (chunk <= 32, P = 64, N = 128), ers_decode.cu
+bool heads_decode_supported(int P, int N, int Q);
+cudaError_t heads_decode(const LaunchArgs& a, cudaStream_t s);
+
 // pointer-only kernels, ers_fma.cu
 cudaError_t launch_setpos(const LaunchArgs& a, int kind, cudaStream_t s);  // kind: 0 decode, 1 refresh
 cudaError_t launch_commit(const LaunchArgs& a, cudaStream_t s);

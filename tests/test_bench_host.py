@@ -90,3 +90,18 @@ def test_clock_summary_keeps_only_samples_inside_the_timed_region():
     c.t_stop = datetime.datetime(2026, 12, 2, 8)
     s = c.summary()
     assert s["samples"] == 5 and "hw_slowdown" in s["reasons"]
+
+
+def test_profiled_traffic_is_null_once_the_kernel_changed(tmp_path):
+    sys.path.insert(0, ROOT)
+    import hashlib
+    import bench
+    src = tmp_path / "k.cu"
+    src.write_text("kernel v1")
+    prof = tmp_path / "p.md"
+    h = hashlib.sha256(b"kernel v1").hexdigest()
+    prof.write_text(f"kernel_source_sha256 = {h}\ntraffic_per_launch_bytes = 1234\n")
+    assert bench.profiled_traffic(str(prof), str(src)) == 1234
+    src.write_text("kernel v2")
+    assert bench.profiled_traffic(str(prof), str(src)) is None
+    assert bench.profiled_traffic(str(tmp_path / "missing.md"), str(src)) is None
