@@ -7,7 +7,8 @@ absence is an error (there is no fallback path).
 """
 __version__ = "0.1.0"
 
-_OPS = ("LayerParams", "ReplayCache", "Status", "ssd_scan_fwd", "chunked_prefill", "replay_decode", "refresh",
+_OPS = ("LayerParams", "ReplayCache", "Status", "ssd_scan_fwd", "ssd_scan_fwd_static", "STATIC_SCRATCH_BYTES",
+        "chunked_prefill", "replay_decode", "refresh",
         "spec_verify", "commit", "ssu_update")
 
 

@@ -28,7 +28,7 @@ FLAG_AUTO_FLUSH = 4
 EXPORTS = (
     "ers_status_str", "ers_version", "ers_ssd_scan_fwd_workspace_size", "ers_ssd_scan_fwd",
     "ers_chunked_prefill_workspace_size", "ers_chunked_prefill", "ers_replay_decode", "ers_refresh",
-    "ers_spec_verify", "ers_commit", "ers_ssu_update",
+    "ers_spec_verify", "ers_commit", "ers_ssu_update", "ers_ssd_scan_fwd_static",
 )
 
 
@@ -71,6 +71,7 @@ _SIGS = {
     "ers_ssd_scan_fwd_workspace_size": ([_DIMS, _I32, _I32], _SZ),
     "ers_chunked_prefill_workspace_size": ([_DIMS, _I32, _I32], _SZ),
     "ers_ssd_scan_fwd": ([_DIMS, _PRM, _I32, _I64, _I32, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _SZ, _P, _P], _I32),
+    "ers_ssd_scan_fwd_static": ([_DIMS, _PRM, _I32, _I64, _I32, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P], _I32),
     "ers_chunked_prefill": ([_DIMS, _PRM, _CACHE, _I32, _I64, _I32, _P, _P, _P, _P, _P, _P, _P, _P, _SZ, _P, _P],
                             _I32),
     "ers_replay_decode": ([_DIMS, _PRM, _CACHE, _I32, _P, _P, _P, _P, _P, _U32, _P, _P, _P], _I32),

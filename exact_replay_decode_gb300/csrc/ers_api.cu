@@ -3,6 +3,8 @@
 #include <stdint.h>
 #include <string.h>
 
+#include <mutex>
+
 #include "ers.h"
 #include "ers_internal.h"
 
@@ -339,6 +341,55 @@ ers_status ers_ssu_update(const ers_dims* dims, const ers_params* prm, float* st
   a.y = y;
   a.status = dev_status;
   return finish(ers::ssu_update(a, (cudaStream_t)stream));
+}
+
+}  // extern "C"
+
+// ---- scan with library-owned scratch ------------------------------------------------------------
+// Scratch of ers_ssd_scan_fwd_static, for callers that cannot pass a workspace (see include/ers.h).
+// A file-scope device array: it exists once per device context, sized at build time, and no byte
+// of it needs an initial value.
+static __device__ __align__(256) unsigned char ers_scan_scratch[ERS_STATIC_SCRATCH_BYTES];
+
+namespace {
+constexpr int kMaxScratchDevices = 64;
+std::mutex scratch_mu;
+void* scratch_addr[kMaxScratchDevices];
+
+// Address of ers_scan_scratch on the current device, looked up once per device (with that device
+// current) and cached.
+ers_status static_scratch(void** out) {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess) {
+    cudaGetLastError();
+    return ERS_ECUDA;
+  }
+  if (dev < 0 || dev >= kMaxScratchDevices) return ERS_EUNSUPPORTED;
+  std::lock_guard<std::mutex> lock(scratch_mu);
+  if (scratch_addr[dev] == nullptr) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, ers_scan_scratch) != cudaSuccess || p == nullptr) {
+      cudaGetLastError();
+      return ERS_ECUDA;
+    }
+    scratch_addr[dev] = p;
+  }
+  *out = scratch_addr[dev];
+  return ERS_OK;
+}
+}  // namespace
+
+extern "C" {
+
+ers_status ers_ssd_scan_fwd_static(const ers_dims* dims, const ers_params* prm, int32_t nseq, int64_t ntokens,
+                                   int32_t max_seqlen, const int32_t* cu_seqlens, const void* x, const float* dt,
+                                   const void* B, const void* C, const float* init_state, void* y,
+                                   float* final_state, float* chunk_states, ers_stream_t stream,
+                                   int32_t* dev_status) {
+  void* scratch = nullptr;
+  ERS_TRY(static_scratch(&scratch));
+  return ers_ssd_scan_fwd(dims, prm, nseq, ntokens, max_seqlen, cu_seqlens, x, dt, B, C, init_state, y,
+                          final_state, chunk_states, scratch, ERS_STATIC_SCRATCH_BYTES, stream, dev_status);
 }
 
 }  // extern "C"

@@ -143,6 +143,44 @@ def ssd_scan_fwd(x: torch.Tensor, dt: torch.Tensor, params: LayerParams, B: torc
     return (y, fin, cs) if return_chunk_states else (y, fin)
 
 
+def ssd_scan_fwd_static(x: torch.Tensor, dt: torch.Tensor, params: LayerParams, B: torch.Tensor, C: torch.Tensor,
+                        chunk: int, cu_seqlens: Optional[torch.Tensor] = None,
+                        init_state: Optional[torch.Tensor] = None, max_seqlen: Optional[int] = None,
+                        status: Optional[Status] = None, check: bool = True, stream=None,
+                        out: Optional[Tuple[torch.Tensor, torch.Tensor]] = None):
+    """ssd_scan_fwd through ers_ssd_scan_fwd_static: the library's fixed device scratch
+    (STATIC_SCRATCH_BYTES per device) instead of a workspace.  Raises ErsError (ERS_EWORKSPACE) when
+    the call needs more scratch than that.  Calls that may overlap on one device race on the scratch."""
+    io = _io_from(x)
+    T, H, P = x.shape
+    G, N = B.shape[1], B.shape[2]
+    dev = x.device
+    if cu_seqlens is None:
+        cu_seqlens = torch.tensor([0, T], dtype=torch.int32, device=dev)
+    S = cu_seqlens.numel() - 1
+    _need(x, io, "x", (T, H, P)); _need(dt, torch.float32, "dt", (T, H))
+    _need(B, io, "B", (T, G, N)); _need(C, io, "C", (T, G, N)); _need(cu_seqlens, torch.int32, "cu_seqlens")
+    if init_state is not None:
+        _need(init_state, torch.float32, "init_state", (S, H, P, N))
+    ms = _max_len(cu_seqlens, max_seqlen)
+    dims = _dims(H, G, P, N, chunk, io)
+    if out is None:
+        y = torch.empty_like(x)
+        fin = torch.empty(S, H, P, N, dtype=torch.float32, device=dev)
+    else:
+        y, fin = out
+    st = status if status is not None else (Status(dev) if check else None)
+    code = _abi.lib().ers_ssd_scan_fwd_static(
+        ctypes.byref(dims), ctypes.byref(params._c()), S, T, ms, cu_seqlens.data_ptr(), x.data_ptr(),
+        dt.data_ptr(), B.data_ptr(), C.data_ptr(), _ptr(init_state), y.data_ptr(), fin.data_ptr(), None,
+        _stream(stream), _ptr(st.t) if st else None)
+    _finish(code, "ers_ssd_scan_fwd_static", st, check)
+    return y, fin
+
+
+STATIC_SCRATCH_BYTES = 16 << 20
+
+
 # ------------------------------------------------------------------------------------------------
 class ReplayCache:
     """Per-slot exact-replay / ReplaySSM state: fp32 checkpoint (anchor), optional bf16 read copy,

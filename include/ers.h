@@ -237,6 +237,29 @@ ERS_API ers_status ers_ssu_update(const ers_dims* dims, const ers_params* prm, f
                           int32_t nseq, const int32_t* slot, const void* x, const float* dt, const void* B,
                           const void* C, void* y, ers_stream_t stream, int32_t* dev_status);
 
+/* ---------------------------------------------------------------------------------------------
+ * ers_ssd_scan_fwd with library-owned scratch.  The pages have no counterpart to this call; it
+ * exists for callers that cannot hand the scan a workspace: a host program that owns no device
+ * allocator (plain C over the runtime, no tensor library), and serving loops that must not
+ * allocate per call because cudaMalloc/cudaFree synchronise the device.
+ *
+ * Same arguments, semantics and outputs as ers_ssd_scan_fwd minus the workspace.  The scratch is a
+ * fixed device array of ERS_STATIC_SCRATCH_BYTES inside this library (one per device context); a
+ * call whose ers_ssd_scan_fwd_workspace_size exceeds it returns ERS_EWORKSPACE and launches
+ * nothing (16 MiB holds, e.g., 2048 tokens x 32 heads x headdim 64 x dstate 128 at chunk 256,
+ * which needs 8.4 MB).  Nothing in the scratch needs to start at zero: a call reads only bytes it
+ * wrote earlier in the same call.  The first call on a device looks up the scratch address with
+ * that device current (cudaGetSymbolAddress) and caches it; make one call on each device before
+ * any stream capture.  Allocates nothing.  The scratch is shared: two calls on the same device
+ * that can run at the same time (different streams, or different host threads) race on it and
+ * must be serialised by the caller. */
+#define ERS_STATIC_SCRATCH_BYTES ((size_t)16 << 20)
+ERS_API ers_status ers_ssd_scan_fwd_static(const ers_dims* dims, const ers_params* prm, int32_t nseq,
+                                   int64_t ntokens, int32_t max_seqlen, const int32_t* cu_seqlens,
+                                   const void* x, const float* dt, const void* B, const void* C,
+                                   const float* init_state, void* y, float* final_state, float* chunk_states,
+                                   ers_stream_t stream, int32_t* dev_status);
+
 #ifdef __cplusplus
 }
 #endif

@@ -5,7 +5,7 @@ import torch
 import synth
 from synth import torch_io
 
-# Tolerances (BASELINE target): bf16 outputs mean|dy| <= 2e-3 mean|y|; fp32 states
+# Parity tolerances: bf16 outputs mean|dy| <= 2e-3 mean|y|; fp32 states
 # max|dS| <= 1e-5 max|S| per (sequence, head).  fp32-io outputs are held to 1e-5 as well.
 OUT_TOL_BF16 = 2e-3
 OUT_TOL_F32 = 1e-5
