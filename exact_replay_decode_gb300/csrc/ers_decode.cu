@@ -8,15 +8,12 @@
 // ers_common.cuh), so decode equals single-shot and chunked prefill bit for bit.
 #include "ers_common.cuh"
 #include "ers_internal.h"
-#include "tc_common.cuh"
+#include "warp_heads.cuh"
 
 namespace ers {
 namespace {
 
-template <typename K>
-cudaError_t prep(K kernel, size_t smem) {
-  return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-}
+using namespace wh;
 
 // ---- replay decode for small chunks, shaped for HBM bandwidth -------------------------------------
 // Same arithmetic as k_decode (row_output, state_weights, chunk_state and fold_state, operation for
@@ -24,69 +21,13 @@ cudaError_t prep(K kernel, size_t smem) {
 //  * One CTA per (sequence, block of up to 8 heads of one B/C group), one warp per head.  The warp
 //    streams its head's [P x N] state through registers, 8 rows at a time, two blocks in flight;
 //    lane j holds elements [4j, 4j+4) of each row, the lane split of Dot<128>.
-//  * The 32 lane partials of 32 rows are combined by a reduce-scatter whose pairings are those of
-//    Dot<128>'s butterfly (xor 16, 8, 4, 2, 1): each stage halves the rows a lane keeps, and lane j
-//    ends with row j's dot product, bit-identical to the butterfly (same tree; fp32 addition is
-//    commutative) at about one shuffle per row instead of five.
+//  * The lane partials of 16 rows are combined by reduce_scatter16 (warp_heads.cuh), which keeps
+//    the pairings of Dot<128>'s butterfly and so each row's bits, at about one shuffle per row.
 //  * The group's Gram row C_p . B_s is computed once per CTA; buffer rows arrive by cp.async while
 //    the state streams; the log-decay scan runs per warp with shuffles (for rows < 32 the strides
 //    >= 32 of chunk_scan change nothing, so the bits are chunk_scan's).
 //  * When the step fills the chunk, the state is streamed after the chunk's weights are known and
 //    each row is folded (fold_state) and written back in the same pass.
-constexpr int kHeadsPerCta = kThreads / 32;
-
-template <typename HT> struct Quad;
-template <> struct Quad<float> {
-  using raw = float4;
-  __device__ __forceinline__ static raw ld_stream(const float* p) { return __ldcs(reinterpret_cast<const float4*>(p)); }
-  __device__ __forceinline__ static void unpack(raw u, float (&v)[4]) {
-    v[0] = u.x; v[1] = u.y; v[2] = u.z; v[3] = u.w;
-  }
-};
-template <> struct Quad<__nv_bfloat16> {
-  using raw = uint2;
-  __device__ __forceinline__ static raw ld_stream(const __nv_bfloat16* p) {
-    return __ldcs(reinterpret_cast<const uint2*>(p));
-  }
-  __device__ __forceinline__ static void unpack(raw u, float (&v)[4]) {
-    const __nv_bfloat162 a = *reinterpret_cast<const __nv_bfloat162*>(&u.x);
-    const __nv_bfloat162 b = *reinterpret_cast<const __nv_bfloat162*>(&u.y);
-    v[0] = __low2float(a); v[1] = __high2float(a); v[2] = __low2float(b); v[3] = __high2float(b);
-  }
-};
-
-// four consecutive io elements from shared memory, widened
-__device__ __forceinline__ void lds4(const float* p, float (&v)[4]) {
-  const float4 u = *reinterpret_cast<const float4*>(p);
-  v[0] = u.x; v[1] = u.y; v[2] = u.z; v[3] = u.w;
-}
-__device__ __forceinline__ void lds4(const __nv_bfloat16* p, float (&v)[4]) {
-  Quad<__nv_bfloat16>::unpack(*reinterpret_cast<const uint2*>(p), v);
-}
-
-// Reduce-scatter of 16 rows' lane partials v[0..15] with the pairings of Dot<128>'s butterfly
-// (xor 16, 8, 4, 2, then 1 on the single remaining row): lane j returns row (j >> 1)'s reduction,
-// bit-identical to Dot<128>::reduce of that row (same tree; fp32 addition is commutative).
-__device__ __forceinline__ float reduce_scatter16(float (&v)[16], int j) {
-#pragma unroll
-  for (int o = 16, n = 16; o >= 2; o >>= 1, n >>= 1) {
-    const bool up = (j & o) != 0;
-#pragma unroll
-    for (int r = 0; r < n / 2; ++r) {
-      const float keep = up ? v[r + n / 2] : v[r];
-      const float send = up ? v[r] : v[r + n / 2];
-      v[r] = __fadd_rn(keep, __shfl_xor_sync(kFull, send, o));
-    }
-  }
-  return __fadd_rn(v[0], __shfl_xor_sync(kFull, v[0], 1));
-}
-
-__device__ __forceinline__ void cp_async16(void* dst, const void* src) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(tc::smem_u32(dst)), "l"(src) : "memory");
-}
-__device__ __forceinline__ void cp_async_wait_all() {
-  asm volatile("cp.async.commit_group;\ncp.async.wait_group 0;" ::: "memory");
-}
 
 template <typename T, int P, int N, int QM>
 constexpr size_t heads_smem_bytes() {

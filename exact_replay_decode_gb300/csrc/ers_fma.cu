@@ -527,6 +527,7 @@ cudaError_t refresh_impl(const LaunchArgs& a, cudaStream_t s) {
 
 template <typename T, int P, int N>
 cudaError_t verify_impl(const LaunchArgs& a, cudaStream_t s) {
+  if (heads_verify_supported(a.P, a.N, a.Q, a.T, a.H, a.G)) return heads_verify(a, s);
   const size_t sm = fma_smem_bytes(a.Q, P);
   cudaError_t e;
   if ((e = prep(k_verify_flush<T, P, N>, sm)) != cudaSuccess) return e;

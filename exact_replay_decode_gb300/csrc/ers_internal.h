@@ -64,6 +64,9 @@ bool fma_supported(int P, int N);
 // warp-per-head replay decode of the CUDA-core engine (chunk <= 32, P = 64, N = 128), ers_decode.cu
 bool heads_decode_supported(int P, int N, int Q);
 cudaError_t heads_decode(const LaunchArgs& a, cudaStream_t s);
+// warp-per-head speculative verify (chunk <= 16, P = 64, N = 128, T <= 4, H/G <= 8), ers_verify.cu
+bool heads_verify_supported(int P, int N, int Q, int T, int H, int G);
+cudaError_t heads_verify(const LaunchArgs& a, cudaStream_t s);
 
 // pointer-only kernels, ers_fma.cu
 cudaError_t launch_setpos(const LaunchArgs& a, int kind, cudaStream_t s);  // kind: 0 decode, 1 refresh

@@ -1,0 +1,299 @@
+// Output-only speculative verify for small chunks (chunk <= 32, P = 64, N = 128, up to 4 drafts,
+// at most 8 heads per B/C group): the bandwidth-shaped verify kernel of the CUDA-core engine.
+//
+// ReplaySSM ("Motivation and method", "Core equations"): outputs of the T draft tokens are computed
+// causally from the low-precision read copy over the committed records plus drafts 1..s; the
+// commit moves only the pointer.  A slot whose committed pointer h would overflow (h + T > L)
+// first folds its h records into the fp32 anchor and recasts the read copy from the same unrounded
+// values.  The arithmetic is the engine's, operation for operation (k_verify_flush and k_verify in
+// ers_fma.cu: load_rows, state_weights, chunk_state, fold_state, row_output), so verify equals
+// ReplaySSM-mode replay decode bit for bit.
+//
+// One CTA per (sequence, B/C group), one warp per head.  A warp streams its head's state once:
+// the bf16 read copy, or, for a flushing slot, the fp32 anchor, which it folds, writes back and
+// recasts row by row, feeding the freshly cast bf16 values (the values the read copy now holds)
+// to the drafts' dot products.  The T drafts' lane partials of 8 rows are reduce-scattered
+// together (32 values, one shuffle each).  The flush and the outputs are one launch because each
+// warp reads only its own head's state and the CTA's own group rows, which it has staged in shared
+// memory before any draft is written into the buffer.
+#include "ers_common.cuh"
+#include "ers_internal.h"
+#include "warp_heads.cuh"
+
+namespace ers {
+namespace {
+
+using namespace wh;
+
+constexpr int kDraftsMax = 4;
+constexpr int kVerifyRowsInFlight = 16;
+
+template <typename T, int P, int N, int QM>
+constexpr size_t verify_smem_bytes() {
+  constexpr int QR = QM + kDraftsMax;
+  return (size_t)QR * N * sizeof(T)                                  // B rows: committed, then drafts
+         + (size_t)kHeadsPerCta * QR * P * sizeof(T)                 // x rows, per warp
+         + (size_t)kDraftsMax * QR * sizeof(float)                   // Gram rows, per draft
+         + (size_t)kHeadsPerCta * kDraftsMax * P * sizeof(float)     // off-diagonal terms, per warp
+         + (size_t)kHeadsPerCta * QM * sizeof(float);                // flush weights, per warp
+}
+
+// Read-copy stream: yo[k * P + d] = Dot<128>(C of draft k, R[d]) for all rows d.  q holds rows
+// [0, kVerifyRowsInFlight) on entry.
+template <int P, int N>
+__device__ __forceinline__ void stream_read_copy(const __nv_bfloat16* __restrict__ R,
+                                                 Quad<__nv_bfloat16>::raw (&q)[kVerifyRowsInFlight],
+                                                 const float (&c)[kDraftsMax][4], float* yo, int j) {
+  constexpr int NBLK = P / 8, QB = kVerifyRowsInFlight / 8;
+#pragma unroll
+  for (int blk = 0; blk < NBLK; ++blk) {
+    float part[32];
+#pragma unroll
+    for (int r = 0; r < 8; ++r) {
+      const int qs = (blk % QB) * 8 + r;
+      float hv[4];
+      Quad<__nv_bfloat16>::unpack(q[qs], hv);
+#pragma unroll
+      for (int k = 0; k < kDraftsMax; ++k) part[k * 8 + r] = Dot<N>::partial(c[k], hv);
+      if (blk + QB < NBLK) q[qs] = Quad<__nv_bfloat16>::ld_stream(R + (size_t)(blk * 8 + r + kVerifyRowsInFlight) * N + 4 * j);
+    }
+    const float v = reduce_scatter32(part, j);
+    yo[(j >> 3) * P + blk * 8 + (j & 7)] = v;
+  }
+  __syncwarp();
+}
+
+// Flush stream: each anchor row is folded with the committed records (chunk_state / fold_state
+// order, weights sw[s] for s < hc), written back to the anchor, cast to bf16 into the read copy, and
+// the cast values feed the drafts' dot products (yo as above).
+template <typename T, int P, int N>
+__device__ __noinline__ void stream_anchor_flush(float* __restrict__ Hd, __nv_bfloat16* __restrict__ Rd,
+                                                 const float (&c)[kDraftsMax][4], float* yo, int j, int hc,
+                                                 const float* sw, float decay, const T* sB, const T* sx) {
+#pragma unroll 1
+  for (int d0 = 0; d0 < P; d0 += 8) {
+    float part[32];
+#pragma unroll
+    for (int half = 0; half < 2; ++half) {
+      const int db = d0 + 4 * half;
+      float h[4][4], acc[4][4];
+#pragma unroll
+      for (int r = 0; r < 4; ++r) {
+        Quad<float>::unpack(__ldcs(reinterpret_cast<const float4*>(Hd + (size_t)(db + r) * N + 4 * j)), h[r]);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) acc[r][e] = 0.f;
+      }
+      for (int s = 0; s < hc; ++s) {
+        float bs[4];
+        lds4(sB + s * N + 4 * j, bs);
+        const float ws = sw[s];
+#pragma unroll
+        for (int r = 0; r < 4; ++r) {
+          const float wx = __fmul_rn(ws, to_f(sx[s * P + db + r]));
+#pragma unroll
+          for (int e = 0; e < 4; ++e) acc[r][e] = __fmaf_rn(wx, bs[e], acc[r][e]);
+        }
+      }
+#pragma unroll
+      for (int r = 0; r < 4; ++r) {
+        float v[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) v[e] = __fmaf_rn(decay, h[r][e], acc[r][e]);
+        const size_t o = (size_t)(db + r) * N + 4 * j;
+        *reinterpret_cast<float4*>(Hd + o) = make_float4(v[0], v[1], v[2], v[3]);
+        __nv_bfloat162 lo2 = __floats2bfloat162_rn(v[0], v[1]), hi2 = __floats2bfloat162_rn(v[2], v[3]);
+        uint2 u;
+        u.x = *reinterpret_cast<uint32_t*>(&lo2);
+        u.y = *reinterpret_cast<uint32_t*>(&hi2);
+        *reinterpret_cast<uint2*>(Rd + o) = u;
+        float rv[4];
+        Quad<__nv_bfloat16>::unpack(u, rv);
+#pragma unroll
+        for (int k = 0; k < kDraftsMax; ++k) part[k * 8 + 4 * half + r] = Dot<N>::partial(c[k], rv);
+      }
+    }
+    const float v = reduce_scatter32(part, j);
+    yo[(j >> 3) * P + d0 + (j & 7)] = v;
+  }
+  __syncwarp();
+}
+
+// Inclusive double-float prefix over lanes (lane s holds row s), the warp form of chunk_scan.
+__device__ __forceinline__ df warp_scan(df v, int j) {
+#pragma unroll
+  for (int st = 1; st < 32; st <<= 1) {
+    const float ph = __shfl_up_sync(kFull, v.hi, st), pl = __shfl_up_sync(kFull, v.lo, st);
+    if (j >= st) v = df_add(df{ph, pl}, v);
+  }
+  return v;
+}
+
+template <typename T, int P, int N, int QM>
+__global__ void __launch_bounds__(kThreads, 2) k_verify_heads(LaunchArgs a) {
+  static_assert(N == 128 && P % 8 == 0 && QM <= 32 - kDraftsMax, "lane split of Dot<128>; one warp scans");
+  constexpr int QR = QM + kDraftsMax;
+  extern __shared__ __align__(16) unsigned char vsm[];
+  T* sB = reinterpret_cast<T*>(vsm);
+  T* sxa = sB + QR * N;
+  float* sg = reinterpret_cast<float*>(sxa + kHeadsPerCta * QR * P);
+  float* syo = sg + kDraftsMax * QR;
+  float* swa = syo + kHeadsPerCta * kDraftsMax * P;
+  const int tid = threadIdx.x, w = tid >> 5, j = tid & 31;
+  const int i = blockIdx.y, g = blockIdx.x;
+  const int hpg = a.H / a.G;
+  const bool active = w < hpg;
+  const int h = g * hpg + (active ? w : 0);
+  const int Td = a.T;
+  int slot;
+  if (!resolve_slot(a, i, &slot)) return;
+  const int hc = a.pos[slot];
+  if (hc < 0 || hc > a.Q) {
+    if (tid == 0) report(a.status, ERS_EALIGN);
+    return;
+  }
+  const bool flush = hc + Td > a.Q;
+  if (flush && !(a.flags & ERS_FLAG_AUTO_FLUSH)) {
+    if (tid == 0) report(a.status, ERS_EOVERFLOW);
+    return;
+  }
+  const int h0 = flush ? 0 : hc;   // committed rows that precede the drafts
+  const size_t HP = (size_t)a.H * P, GN = (size_t)a.G * N;
+  const size_t soff = ((size_t)slot * a.H + h) * P * N;
+  const __nv_bfloat16* R = (const __nv_bfloat16*)a.read_copy + soff;
+  // the drafts' C rows (lane quads); drafts >= T contribute nothing
+  float c[kDraftsMax][4];
+#pragma unroll
+  for (int k = 0; k < kDraftsMax; ++k) {
+    if (k < Td) {
+      load_k<T, 4>((const T*)a.C + ((size_t)i * Td + k) * GN + (size_t)g * N + 4 * j, c[k]);
+    } else {
+#pragma unroll
+      for (int e = 0; e < 4; ++e) c[k][e] = 0.f;
+    }
+  }
+  Quad<__nv_bfloat16>::raw q[kVerifyRowsInFlight];
+  if (!flush && active) {
+#pragma unroll
+    for (int r = 0; r < kVerifyRowsInFlight; ++r) q[r] = Quad<__nv_bfloat16>::ld_stream(R + (size_t)r * N + 4 * j);
+  }
+  // committed rows 0..hc-1 at smem rows 0..hc-1, drafts at rows QM..QM+T-1
+  const T* bB = (const T*)a.bB + (size_t)slot * a.Q * GN + (size_t)g * N;
+  constexpr int kBChunks = N * sizeof(T) / 16, kXChunks = P * sizeof(T) / 16;
+  for (int k = tid; k < (hc + Td) * kBChunks; k += kThreads) {
+    const int r = k / kBChunks, e = k % kBChunks;
+    const T* src = r < hc ? bB + r * GN : (const T*)a.B + ((size_t)i * Td + (r - hc)) * GN + (size_t)g * N;
+    cp_async16(reinterpret_cast<char*>(sB + (r < hc ? r : QM + r - hc) * N) + 16 * e,
+               reinterpret_cast<const char*>(src) + 16 * e);
+  }
+  T* sx = sxa + w * QR * P;
+  if (active) {
+    const T* bx = (const T*)a.bx + (size_t)slot * a.Q * HP + (size_t)h * P;
+    for (int k = j; k < (hc + Td) * kXChunks; k += 32) {
+      const int r = k / kXChunks, e = k % kXChunks;
+      const T* src = r < hc ? bx + r * HP : (const T*)a.x + ((size_t)i * Td + (r - hc)) * HP + (size_t)h * P;
+      cp_async16(reinterpret_cast<char*>(sx + (r < hc ? r : QM + r - hc) * P) + 16 * e,
+                 reinterpret_cast<const char*>(src) + 16 * e);
+    }
+  }
+  const float dt_c = j < hc ? a.bdt[((size_t)slot * a.Q + j) * a.H + h] : 0.f;
+  const float dt_d = j < Td ? a.dt[((size_t)i * Td + j) * a.H + h] : 0.f;
+  const float Ah = a.A[h], bias = a.dt_bias[h];
+  float* yo = syo + w * kDraftsMax * P;
+  if (!flush && active) stream_read_copy<P, N>(R, q, c, yo, j);
+  // output rows s < h0 + T: committed rows then drafts
+  const int nout = h0 + Td;
+  const float dt_o_d = __shfl_sync(kFull, dt_d, max(j - h0, 0) & 31);
+  float dl = 0.f;
+  df v = {0.f, 0.f};
+  if (j < nout) {
+    dl = delta_of(j < h0 ? dt_c : dt_o_d, bias);
+    v.hi = __fmul_rn(dl, Ah);
+  }
+  v = warp_scan(v, j);
+  cp_async_wait_all();
+  __syncthreads();
+  // Gram rows of the drafts: G[k][s] = C_{h0+k} . B_s for s <= h0 + k
+  for (int k = 0; k < Td; ++k)
+    for (int s = w; s <= h0 + k; s += kHeadsPerCta) {
+      float bs[4];
+      lds4(sB + (s < h0 ? s : QM + s - h0) * N + 4 * j, bs);
+      const float gv = Dot<N>::reduce(Dot<N>::partial(c[k], bs));
+      if (j == 0) sg[k * QR + s] = gv;
+    }
+  // a flushing slot folds its committed records (rows 0..hc-1) into the anchor
+  float* sw = swa + w * QM;
+  float decay = 0.f;
+  if (flush) {
+    float dc = 0.f;
+    df vc = {0.f, 0.f};
+    if (j < hc) {
+      dc = delta_of(dt_c, bias);
+      vc.hi = __fmul_rn(dc, Ah);
+    }
+    vc = warp_scan(vc, j);
+    const df last = {__shfl_sync(kFull, vc.hi, hc - 1), __shfl_sync(kFull, vc.lo, hc - 1)};
+    if (j < hc) sw[j] = __fmul_rn(dc, expf(df_diff(last, vc)));
+    decay = expf(last.hi);
+    __syncwarp();
+  }
+  __syncthreads();
+  if (!active) return;
+  if (flush)
+    stream_anchor_flush<T, P, N>(a.state + soff, (__nv_bfloat16*)a.read_copy + soff, c, yo, j, hc, sw, decay, sB, sx);
+  // outputs of draft k (row t = h0 + k): d = j and j + 32 for P = 64
+  const float Dh = a.D[h];
+  for (int k = 0; k < Td; ++k) {
+    const int t = h0 + k;
+    const df at = {__shfl_sync(kFull, v.hi, t), __shfl_sync(kFull, v.lo, t)};
+    float M = 0.f;
+    if (j <= t) M = __fmul_rn(__fmul_rn(sg[k * QR + j], dl), expf(df_diff(at, v)));
+    const float et = expf(at.hi);
+    T* y = (T*)a.y + ((size_t)i * Td + k) * HP + (size_t)h * P;
+    for (int d = j; d < P; d += 32) {
+      float acc = 0.f;
+      for (int s = 0; s <= t; ++s)
+        acc = __fmaf_rn(__shfl_sync(kFull, M, s), to_f(sx[(s < h0 ? s : QM + s - h0) * P + d]), acc);
+      y[d] = from_f<T>(combine_out(et, yo[k * P + d], acc, Dh, to_f(sx[(QM + k) * P + d])));
+    }
+  }
+  // the drafts go to buffer rows h0..h0+T-1 (B/C once per group)
+  for (int k = 0; k < Td; ++k) {
+    T* dx = (T*)a.bx + ((size_t)slot * a.Q + h0 + k) * HP + (size_t)h * P;
+    for (int d = j; d < P; d += 32) dx[d] = sx[(QM + k) * P + d];
+  }
+  if (j < Td) a.bdt[((size_t)slot * a.Q + h0 + j) * a.H + h] = dt_d;
+  if (w == 0) {
+    for (int k = 0; k < Td; ++k) {
+      const size_t dst = ((size_t)slot * a.Q + h0 + k) * GN + (size_t)g * N;
+      const size_t src = ((size_t)i * Td + k) * GN + (size_t)g * N;
+      for (int n = j; n < N; n += 32) {
+        ((T*)a.bB)[dst + n] = sB[(QM + k) * N + n];
+        ((T*)a.bC)[dst + n] = ((const T*)a.C)[src + n];
+      }
+    }
+  }
+}
+
+template <typename T, int QM>
+cudaError_t launch_verify_heads(const LaunchArgs& a, cudaStream_t s) {
+  constexpr int P = 64, N = 128;
+  constexpr size_t sm = verify_smem_bytes<T, P, N, QM>();
+  cudaError_t e = prep(k_verify_heads<T, P, N, QM>, sm);
+  if (e != cudaSuccess) return e;
+  k_verify_heads<T, P, N, QM><<<dim3(a.G, a.nseq), kThreads, sm, s>>>(a);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+bool heads_verify_supported(int P, int N, int Q, int T, int H, int G) {
+  return P == 64 && N == 128 && Q >= 1 && Q <= 16 && T >= 1 && T <= kDraftsMax && G > 0 && H % G == 0 &&
+         H / G <= kHeadsPerCta;
+}
+
+cudaError_t heads_verify(const LaunchArgs& a, cudaStream_t s) {
+  if (a.io == ERS_DTYPE_BF16) return launch_verify_heads<__nv_bfloat16, 16>(a, s);
+  return launch_verify_heads<float, 16>(a, s);
+}
+
+}  // namespace ers

@@ -1,0 +1,97 @@
+// Warp-per-head building blocks of the bandwidth-shaped decode and verify kernels (CUDA-core
+// engine, dstate N = 128).  A warp owns one head; lane j holds elements [4j, 4j+4) of every state
+// row, the lane split of Dot<128> (ers_common.cuh), so every row dot product is a per-lane fmaf
+// chain over 4 elements followed by the xor-16,8,4,2,1 butterfly, evaluated here as a
+// reduce-scatter that keeps each row's pairings (and therefore its bits).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+#include "ers_common.cuh"
+#include "tc_common.cuh"
+
+namespace ers {
+namespace wh {
+
+constexpr int kHeadsPerCta = kThreads / 32;
+
+template <typename HT> struct Quad;
+template <> struct Quad<float> {
+  using raw = float4;
+  __device__ __forceinline__ static raw ld_stream(const float* p) { return __ldcs(reinterpret_cast<const float4*>(p)); }
+  __device__ __forceinline__ static void unpack(raw u, float (&v)[4]) {
+    v[0] = u.x; v[1] = u.y; v[2] = u.z; v[3] = u.w;
+  }
+};
+template <> struct Quad<__nv_bfloat16> {
+  using raw = uint2;
+  __device__ __forceinline__ static raw ld_stream(const __nv_bfloat16* p) {
+    return __ldcs(reinterpret_cast<const uint2*>(p));
+  }
+  __device__ __forceinline__ static void unpack(raw u, float (&v)[4]) {
+    const __nv_bfloat162 a = *reinterpret_cast<const __nv_bfloat162*>(&u.x);
+    const __nv_bfloat162 b = *reinterpret_cast<const __nv_bfloat162*>(&u.y);
+    v[0] = __low2float(a); v[1] = __high2float(a); v[2] = __low2float(b); v[3] = __high2float(b);
+  }
+};
+
+// four consecutive io elements from shared memory, widened
+__device__ __forceinline__ void lds4(const float* p, float (&v)[4]) {
+  const float4 u = *reinterpret_cast<const float4*>(p);
+  v[0] = u.x; v[1] = u.y; v[2] = u.z; v[3] = u.w;
+}
+__device__ __forceinline__ void lds4(const __nv_bfloat16* p, float (&v)[4]) {
+  Quad<__nv_bfloat16>::unpack(*reinterpret_cast<const uint2*>(p), v);
+}
+
+// Reduce-scatter of 32 partials v[0..31] (row r of the 32 in v[r]) with the pairings of
+// Dot<128>'s butterfly: each stage keeps the half of the rows whose index bit matches the lane's,
+// so lane j returns row j's reduction, bit-identical to Dot<128>::reduce of that row (same tree;
+// fp32 addition is commutative) at one shuffle per row instead of five.
+__device__ __forceinline__ float reduce_scatter32(float (&v)[32], int j) {
+#pragma unroll
+  for (int o = 16, n = 32; o >= 1; o >>= 1, n >>= 1) {
+    const bool up = (j & o) != 0;
+#pragma unroll
+    for (int r = 0; r < n / 2; ++r) {
+      const float keep = up ? v[r + n / 2] : v[r];
+      const float send = up ? v[r] : v[r + n / 2];
+      v[r] = __fadd_rn(keep, __shfl_xor_sync(kFull, send, o));
+    }
+  }
+  return v[0];
+}
+
+// Reduce-scatter of 16 rows' lane partials v[0..15] with the pairings of Dot<128>'s butterfly
+// (xor 16, 8, 4, 2, then 1 on the single remaining row): lane j returns row (j >> 1)'s reduction,
+// bit-identical to Dot<128>::reduce of that row (same tree; fp32 addition is commutative).
+__device__ __forceinline__ float reduce_scatter16(float (&v)[16], int j) {
+#pragma unroll
+  for (int o = 16, n = 16; o >= 2; o >>= 1, n >>= 1) {
+    const bool up = (j & o) != 0;
+#pragma unroll
+    for (int r = 0; r < n / 2; ++r) {
+      const float keep = up ? v[r + n / 2] : v[r];
+      const float send = up ? v[r] : v[r + n / 2];
+      v[r] = __fadd_rn(keep, __shfl_xor_sync(kFull, send, o));
+    }
+  }
+  return __fadd_rn(v[0], __shfl_xor_sync(kFull, v[0], 1));
+}
+
+__device__ __forceinline__ void cp_async16(void* dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(tc::smem_u32(dst)), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() {
+  asm volatile("cp.async.commit_group;\ncp.async.wait_group 0;" ::: "memory");
+}
+
+
+template <typename K>
+cudaError_t prep(K kernel, size_t smem) {
+  return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+}
+
+}  // namespace wh
+}  // namespace ers
