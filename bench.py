@@ -506,6 +506,8 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--decode-only", action="store_true", help="only the headline decode measurement")
     ap.add_argument("--batch", type=int, default=None, help="decode sequences per GPU (profiling runs only)")
+    ap.add_argument("--section", choices=["prefill", "verify", "ssu"], default=None,
+                    help="run only this secondary workload and print its JSON (profiling aid, no headline)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -520,6 +522,16 @@ def main(argv=None):
         dist.init_process_group("nccl", device_id=torch.device("cuda", local))
     dev = torch.device("cuda", torch.cuda.current_device())
     hbm, tc, peak_kind = _peaks()
+    if args.section is not None:
+        if args.section == "prefill":
+            out = {n: bench_prefill(dev, n, 10, args.warmup, hbm, tc) for n in ("prefill_2048_h32", "varlen_4seq_h64")}
+        elif args.section == "verify":
+            out = bench_verify(dev, 32, hbm)
+        else:
+            out = bench_ssu(dev, 16, hbm)
+        if rank == 0:
+            print(json.dumps({args.section: out}))
+        return 0
 
     b, ms, clocks = time_decode(dev, args.steps, args.warmup, seed=1000 + rank, batch=args.batch)
     ms = max_over_ranks(ms, dev)

@@ -188,50 +188,74 @@ __global__ void __launch_bounds__(kThreads) k_prefill_state(LaunchArgs a, bool c
 
 // ---- prefill: inter-chunk state passing in fp32 (RFC Evidence 4: the state stays fp32 inside one
 // call and is rounded only on store; here it is never rounded) ----------------------------------
+// H_{c+1} = fma(exp(Acum_last,c), H_c, S_c) is elementwise, so each (sequence, head) state is split
+// over kChainSlices CTAs of kThreads threads x 4 consecutive elements (one 16-byte access each).
+// The chunk states and log-decays are inputs of the chain, not results of it, so a thread loads
+// them for kChainBatch chunks at once and only the fma chain itself runs in chunk order.
+constexpr int kChainElems = 4;
+constexpr int kChainBatch = 8;
+
+__host__ __device__ constexpr int chain_slices(int P, int N) {
+  return (P * N + kThreads * kChainElems - 1) / (kThreads * kChainElems);
+}
+
 template <int P, int N>
 __global__ void __launch_bounds__(kThreads) k_prefill_chain(LaunchArgs a, bool chunked) {
+  static_assert((P * N) % kChainElems == 0, "whole 16-byte groups");
   const int i = blockIdx.x, h = blockIdx.y;
   SeqGrid sg;
   if (!seq_grid(a, chunked, i, &sg)) return;
-  constexpr int EPT = P * N / kThreads;
+  const int idx = (blockIdx.z * kThreads + threadIdx.x) * kChainElems;
+  if (idx >= P * N) return;
   const size_t hs = (size_t)P * N;
   float* ckpt = chunked ? a.state + ((size_t)sg.slot * a.H + h) * hs : nullptr;
   const float* init = chunked ? ckpt : (a.init_state ? a.init_state + ((size_t)i * a.H + h) * hs : nullptr);
-  float Hr[EPT], keep[EPT];
+  float Hr[kChainElems], keep[kChainElems];
+  if (init != nullptr) {
+    const float4 v = *reinterpret_cast<const float4*>(init + idx);
+    Hr[0] = v.x; Hr[1] = v.y; Hr[2] = v.z; Hr[3] = v.w;
+  } else {
 #pragma unroll
-  for (int e = 0; e < EPT; ++e) {
-    Hr[e] = init ? init[threadIdx.x + e * kThreads] : 0.f;
-    keep[e] = Hr[e];
+    for (int e = 0; e < kChainElems; ++e) Hr[e] = 0.f;
   }
+#pragma unroll
+  for (int e = 0; e < kChainElems; ++e) keep[e] = Hr[e];
   const bool aligned_end = (sg.total % a.Q) == 0;
-  for (int c = 0; c < sg.nch; ++c) {
-    const size_t base = ((size_t)i * a.max_chunks + c) * a.H + h;
-    float* S = a.ws_states + base * hs;
-    const float decay = expf(a.ws_tot[base]);
-    if (c == sg.nch - 1 && !aligned_end) {
+  for (int c0 = 0; c0 < sg.nch; c0 += kChainBatch) {
+    float4 sv[kChainBatch];
+    float tot[kChainBatch];
 #pragma unroll
-      for (int e = 0; e < EPT; ++e) keep[e] = Hr[e];
+    for (int k = 0; k < kChainBatch; ++k) {
+      if (c0 + k < sg.nch) {
+        const size_t base = ((size_t)i * a.max_chunks + c0 + k) * a.H + h;
+        sv[k] = *reinterpret_cast<const float4*>(a.ws_states + base * hs + idx);
+        tot[k] = a.ws_tot[base];
+      }
     }
 #pragma unroll
-    for (int e = 0; e < EPT; ++e) {
-      const int idx = threadIdx.x + e * kThreads;
-      const float s = S[idx];
-      S[idx] = Hr[e];  // the state at the start of chunk c, read by the output kernel
-      Hr[e] = __fmaf_rn(decay, Hr[e], s);
-    }
-    if (a.chunk_states != nullptr) {
-      float* cs = a.chunk_states + base * hs;
+    for (int k = 0; k < kChainBatch; ++k) {
+      const int c = c0 + k;
+      if (c >= sg.nch) break;
+      const size_t base = ((size_t)i * a.max_chunks + c) * a.H + h;
+      const float decay = expf(tot[k]);
+      if (c == sg.nch - 1 && !aligned_end) {
 #pragma unroll
-      for (int e = 0; e < EPT; ++e) cs[threadIdx.x + e * kThreads] = Hr[e];
+        for (int e = 0; e < kChainElems; ++e) keep[e] = Hr[e];
+      }
+      const float sc[kChainElems] = {sv[k].x, sv[k].y, sv[k].z, sv[k].w};
+      // the state at the start of chunk c, read by the output kernel
+      *reinterpret_cast<float4*>(a.ws_states + base * hs + idx) = make_float4(Hr[0], Hr[1], Hr[2], Hr[3]);
+#pragma unroll
+      for (int e = 0; e < kChainElems; ++e) Hr[e] = __fmaf_rn(decay, Hr[e], sc[e]);
+      if (a.chunk_states != nullptr)
+        *reinterpret_cast<float4*>(a.chunk_states + base * hs + idx) = make_float4(Hr[0], Hr[1], Hr[2], Hr[3]);
     }
   }
   if (!chunked) {
-    float* fin = a.final_state + ((size_t)i * a.H + h) * hs;
-#pragma unroll
-    for (int e = 0; e < EPT; ++e) fin[threadIdx.x + e * kThreads] = Hr[e];
+    *reinterpret_cast<float4*>(a.final_state + ((size_t)i * a.H + h) * hs + idx) = make_float4(Hr[0], Hr[1], Hr[2], Hr[3]);
   } else if (sg.nch > 0) {
-#pragma unroll
-    for (int e = 0; e < EPT; ++e) ckpt[threadIdx.x + e * kThreads] = aligned_end ? Hr[e] : keep[e];
+    const float* v = aligned_end ? Hr : keep;
+    *reinterpret_cast<float4*>(ckpt + idx) = make_float4(v[0], v[1], v[2], v[3]);
   }
 }
 
@@ -499,7 +523,7 @@ cudaError_t prefill_impl(const LaunchArgs& a, Op op, cudaStream_t s) {
   if (a.max_chunks > 0 && a.nseq > 0) {
     dim3 grid(a.max_chunks, a.nseq, a.H);
     k_prefill_state<T, P, N><<<grid, kThreads, sm, s>>>(a, chunked);
-    k_prefill_chain<P, N><<<dim3(a.nseq, a.H), kThreads, 0, s>>>(a, chunked);
+    k_prefill_chain<P, N><<<dim3(a.nseq, a.H, chain_slices(P, N)), kThreads, 0, s>>>(a, chunked);
     k_prefill_out<T, P, N><<<grid, kThreads, sm, s>>>(a, chunked);
   }
   if (chunked && a.nseq > 0) k_tail<T><<<a.nseq, kThreads, 0, s>>>(a);
@@ -606,7 +630,11 @@ cudaError_t launch_commit(const LaunchArgs& a, cudaStream_t s) {
 
 cudaError_t launch_chain(const LaunchArgs& a, bool chunked, cudaStream_t s) {
   if (a.nseq <= 0 || a.max_chunks <= 0) return cudaSuccess;
-#define ERS_CH(p_, n_) if (a.P == p_ && a.N == n_) { k_prefill_chain<p_, n_><<<dim3(a.nseq, a.H), kThreads, 0, s>>>(a, chunked); return cudaGetLastError(); }
+#define ERS_CH(p_, n_)                                                                                  \
+  if (a.P == p_ && a.N == n_) {                                                                        \
+    k_prefill_chain<p_, n_><<<dim3(a.nseq, a.H, chain_slices(p_, n_)), kThreads, 0, s>>>(a, chunked); \
+    return cudaGetLastError();                                                                         \
+  }
   ERS_FMA_SHAPES(ERS_CH)
 #undef ERS_CH
   return cudaErrorInvalidValue;

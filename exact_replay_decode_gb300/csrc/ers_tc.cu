@@ -260,6 +260,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_prefill_state(LaunchArgs a) 
   uint8_t* u = ar.X + (size_t)K * 128;
   load_decays(rows, nrows, a.A[h], a.dt_bias[h]);
   load_xb(rows, nrows, ar);
+  cp_async_wait_all();
   __syncthreads();
   uint32_t phase = 0;
   if (tc_state(ar, nrows, u, a.status, &phase)) {
@@ -388,6 +389,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_refresh(LaunchArgs a, bool v
   ar.Hs = nullptr;
   load_decays(rows, p, a.A[h], a.dt_bias[h]);
   load_xb(rows, p, ar);
+  cp_async_wait_all();
   __syncthreads();
   uint32_t phase = 0;
   if (tc_state(ar, p, ar.X + (size_t)K * 128, a.status, &phase)) fold_from_tmem(Hd, Rd, expf(hdr().ahi[p - 1]));

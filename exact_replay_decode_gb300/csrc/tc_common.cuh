@@ -106,13 +106,24 @@ __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t by
       : "memory");
 }
 
+// 16-byte asynchronous global -> shared copy (cp.async, L2 only); complete after cp_async_wait_all
+__device__ __forceinline__ void cp_async16(void* dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst)), "l"(src) : "memory");
+}
+// waits for all of the calling thread's cp.async copies
+__device__ __forceinline__ void cp_async_wait_all() {
+  asm volatile("cp.async.commit_group;\ncp.async.wait_group 0;" ::: "memory");
+}
+
 // generic-proxy smem writes -> visible to the tensor core (async proxy)
 __device__ __forceinline__ void fence_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
 __device__ __forceinline__ void before_sync() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void after_sync() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
 
-// make generic-proxy smem writes visible to the tensor core, then sync the CTA
+// complete this thread's cp.async copies, make its smem writes visible to the tensor core, then
+// sync the CTA
 __device__ __forceinline__ void publish() {
+  cp_async_wait_all();
   fence_async_smem();
   before_sync();
   __syncthreads();

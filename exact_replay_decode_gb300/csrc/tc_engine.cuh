@@ -134,13 +134,24 @@ __device__ __forceinline__ void split8(const float (&v)[8], uint4& hi, uint4& lo
   lo = make_uint4(pack_bf16x2(l[0], l[1]), pack_bf16x2(l[2], l[3]), pack_bf16x2(l[4], l[5]), pack_bf16x2(l[6], l[7]));
 }
 
-// fp32 state [64][128] -> [H_hi; H_lo] tile.  Called by all kThreads threads.
+// fp32 state [64][128] -> [H_hi; H_lo] tile.  Called by all kThreads threads (blockDim.x ==
+// kThreads); every thread's loads are issued before any of its splits.
 __device__ __forceinline__ void state_to_tile(const float* __restrict__ H, uint8_t* tile) {
-  for (int id = threadIdx.x; id < P * (N / 8); id += blockDim.x) {
+  constexpr int IT = P * (N / 8) / kThreads;
+  static_assert(P * (N / 8) % kThreads == 0, "whole iterations");
+  float4 a[IT], b[IT];
+#pragma unroll
+  for (int k = 0; k < IT; ++k) {
+    const int id = threadIdx.x + k * kThreads;
     const int d = id / (N / 8), c = id % (N / 8);
-    const float4 a = *reinterpret_cast<const float4*>(H + d * N + 8 * c);
-    const float4 b = *reinterpret_cast<const float4*>(H + d * N + 8 * c + 4);
-    const float v[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+    a[k] = *reinterpret_cast<const float4*>(H + d * N + 8 * c);
+    b[k] = *reinterpret_cast<const float4*>(H + d * N + 8 * c + 4);
+  }
+#pragma unroll
+  for (int k = 0; k < IT; ++k) {
+    const int id = threadIdx.x + k * kThreads;
+    const int d = id / (N / 8), c = id % (N / 8);
+    const float v[8] = {a[k].x, a[k].y, a[k].z, a[k].w, b[k].x, b[k].y, b[k].z, b[k].w};
     uint4 hi, lo;
     split8(v, hi, lo);
     *reinterpret_cast<uint4*>(tile + sw128(128, d, 8 * c)) = hi;
@@ -148,19 +159,21 @@ __device__ __forceinline__ void state_to_tile(const float* __restrict__ H, uint8
   }
 }
 
-// bf16 read copy [64][128] -> [R; 0] tile (a single term)
+// bf16 read copy [64][128] -> [R; 0] tile (a single term); asynchronous (cp.async), complete after
+// cp_async_wait_all (publish() waits)
 __device__ __forceinline__ void readcopy_to_tile(const __nv_bfloat16* __restrict__ R, uint8_t* tile) {
   for (int id = threadIdx.x; id < P * (N / 8); id += blockDim.x) {
     const int d = id / (N / 8), c = id % (N / 8);
-    *reinterpret_cast<uint4*>(tile + sw128(128, d, 8 * c)) = *reinterpret_cast<const uint4*>(R + d * N + 8 * c);
+    cp_async16(tile + sw128(128, d, 8 * c), R + d * N + 8 * c);
     *reinterpret_cast<uint4*>(tile + sw128(128, P + d, 8 * c)) = make_uint4(0, 0, 0, 0);
   }
 }
 
-// 16-byte chunk copy of one token row (row length `elems` bf16) into tile row r (atoms R rows apart)
+// 16-byte chunk of one token row into tile row r (atoms R rows apart); asynchronous (cp.async),
+// complete after cp_async_wait_all (publish() waits)
 __device__ __forceinline__ void row_to_tile(const __nv_bfloat16* __restrict__ src, uint8_t* tile, uint32_t R,
                                             uint32_t r, int chunk) {
-  *reinterpret_cast<uint4*>(tile + sw128(R, r, 8 * chunk)) = *reinterpret_cast<const uint4*>(src + 8 * chunk);
+  cp_async16(tile + sw128(R, r, 8 * chunk), src + 8 * chunk);
 }
 __device__ __forceinline__ void zero_tile_chunk(uint8_t* tile, uint32_t R, uint32_t r, int chunk) {
   *reinterpret_cast<uint4*>(tile + sw128(R, r, 8 * chunk)) = make_uint4(0, 0, 0, 0);

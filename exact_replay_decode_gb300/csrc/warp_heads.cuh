@@ -80,12 +80,8 @@ __device__ __forceinline__ float reduce_scatter16(float (&v)[16], int j) {
   return __fadd_rn(v[0], __shfl_xor_sync(kFull, v[0], 1));
 }
 
-__device__ __forceinline__ void cp_async16(void* dst, const void* src) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(tc::smem_u32(dst)), "l"(src) : "memory");
-}
-__device__ __forceinline__ void cp_async_wait_all() {
-  asm volatile("cp.async.commit_group;\ncp.async.wait_group 0;" ::: "memory");
-}
+using tc::cp_async16;
+using tc::cp_async_wait_all;
 
 
 template <typename K>
