@@ -258,29 +258,55 @@ def time_decode(dev, steps: int, warmup: int, seed: int, batch=None):
 
 
 def time_decode_e2e(dev, steps: int, warmup: int, seed: int, batch=None):
-    """Same workload through the public API with host buffers: each step copies its tokens from
-    pinned host memory and reads its outputs back; copies are inside the timed region."""
+    """Same workload through the public API with host buffers.  Every step copies its tokens from
+    pinned host memory and reads its outputs back into pinned host memory, inside the timed region.
+    The copies are pipelined the way a serving loop would: step k+1's inputs upload on one copy
+    stream and step k-1's outputs download on another while step k computes (double-buffered device
+    tensors; events order every reuse)."""
     import torch
     b = DecodeBench(dev, seed, batch)
     host = [t.cpu().pin_memory() for t in b.tok]
-    dev_in = [torch.empty_like(t[0]) for t in b.tok]
-    y_host = torch.empty(b.y.shape, dtype=b.y.dtype).pin_memory()
+    dev_in = [[torch.empty_like(t[0]) for t in b.tok] for _ in range(2)]
+    y_dev = [torch.empty_like(b.y) for _ in range(2)]
+    y_host = [torch.empty(b.y.shape, dtype=b.y.dtype).pin_memory() for _ in range(2)]
     h2d = sum(t[0].numel() * t.element_size() for t in host)
-    d2h = y_host.numel() * y_host.element_size()
+    d2h = y_host[0].numel() * y_host[0].element_size()
+    comp = torch.cuda.current_stream()
+    up, down = torch.cuda.Stream(), torch.cuda.Stream()
+    ev = lambda: torch.cuda.Event()
+    in_ready, in_free, y_ready, y_free = [ev(), ev()], [ev(), ev()], [ev(), ev()], [ev(), ev()]
+    for e in in_free + y_free:
+        e.record(comp)
 
-    def one(k):
-        for d_, h_ in zip(dev_in, host):
-            d_.copy_(h_[k % TOKEN_RING], non_blocking=True)
-        b.ers.replay_decode(b.cache, b.prm, *dev_in, status=b.status, check=False, out=b.y)
-        y_host.copy_(b.y, non_blocking=True)
+    def upload(k):
+        j = k % 2
+        up.wait_event(in_free[j])
+        with torch.cuda.stream(up):
+            for d_, h_ in zip(dev_in[j], host):
+                d_.copy_(h_[k % TOKEN_RING], non_blocking=True)
+        in_ready[j].record(up)
 
-    for k in range(warmup):
-        one(k)
+    def run(k0, n):
+        upload(k0)
+        for k in range(k0, k0 + n):
+            j = k % 2
+            if k + 1 < k0 + n:
+                upload(k + 1)
+            comp.wait_event(in_ready[j])
+            comp.wait_event(y_free[j])
+            b.ers.replay_decode(b.cache, b.prm, *dev_in[j], status=b.status, check=False, out=y_dev[j])
+            in_free[j].record(comp)
+            y_ready[j].record(comp)
+            down.wait_event(y_ready[j])
+            with torch.cuda.stream(down):
+                y_host[j].copy_(y_dev[j], non_blocking=True)
+            y_free[j].record(down)
+
+    run(0, warmup)
     torch.cuda.synchronize()
     _barrier()
     t0 = time.perf_counter()
-    for k in range(warmup, warmup + steps):
-        one(k)
+    run(warmup, steps)
     torch.cuda.synchronize()
     el = time.perf_counter() - t0
     _barrier()
