@@ -16,10 +16,19 @@ namespace wh {
 
 constexpr int kHeadsPerCta = kThreads / 32;
 
+// Read-once state streams: 16 (fp32) or 8 (bf16) bytes per lane, through the read-only path
+// without L1 allocation and with a 256-byte L2 fetch (a warp's row is 512 or 256 contiguous
+// bytes).  Only for memory that no thread writes during the kernel before reading it this way.
 template <typename HT> struct Quad;
 template <> struct Quad<float> {
   using raw = float4;
-  __device__ __forceinline__ static raw ld_stream(const float* p) { return __ldcs(reinterpret_cast<const float4*>(p)); }
+  __device__ __forceinline__ static raw ld_stream(const float* p) {
+    float4 v;
+    asm volatile("ld.global.nc.L1::no_allocate.L2::256B.v4.f32 {%0,%1,%2,%3}, [%4];"
+                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+                 : "l"(p));
+    return v;
+  }
   __device__ __forceinline__ static void unpack(raw u, float (&v)[4]) {
     v[0] = u.x; v[1] = u.y; v[2] = u.z; v[3] = u.w;
   }
@@ -27,7 +36,9 @@ template <> struct Quad<float> {
 template <> struct Quad<__nv_bfloat16> {
   using raw = uint2;
   __device__ __forceinline__ static raw ld_stream(const __nv_bfloat16* p) {
-    return __ldcs(reinterpret_cast<const uint2*>(p));
+    uint2 v;
+    asm volatile("ld.global.nc.L1::no_allocate.L2::256B.v2.u32 {%0,%1}, [%2];" : "=r"(v.x), "=r"(v.y) : "l"(p));
+    return v;
   }
   __device__ __forceinline__ static void unpack(raw u, float (&v)[4]) {
     const __nv_bfloat162 a = *reinterpret_cast<const __nv_bfloat162*>(&u.x);
