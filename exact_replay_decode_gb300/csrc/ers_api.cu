@@ -83,15 +83,18 @@ void set_cache(LaunchArgs& a, const ers_cache* c) {
 }
 
 struct Workspace {
-  size_t states, tot, total;
+  size_t states, tot, decay, total;
 };
 
+// Prefill scratch: per (sequence, chunk, head) the chunk state (later the state at the chunk's
+// start), the chunk's total log-decay, and its rows' delta and log-decay prefix.
 Workspace prefill_workspace(const ers_dims* d, int32_t nseq, int32_t max_chunks) {
   Workspace w;
   const size_t units = (size_t)(nseq > 0 ? nseq : 0) * (size_t)(max_chunks > 0 ? max_chunks : 0) * d->nheads;
   w.states = ers::align256(units * d->headdim * d->dstate * sizeof(float));
   w.tot = ers::align256(units * sizeof(float));
-  w.total = w.states + w.tot;
+  w.decay = ers::align256(units * 3 * (size_t)d->chunk * sizeof(float));
+  w.total = w.states + w.tot + w.decay;
   return w;
 }
 
@@ -174,6 +177,7 @@ ers_status ers_ssd_scan_fwd(const ers_dims* dims, const ers_params* prm, int32_t
   a.chunk_states = chunk_states;
   a.ws_states = (float*)workspace;
   a.ws_tot = (float*)((char*)workspace + w.states);
+  a.ws_decay = (float*)((char*)workspace + w.states + w.tot);
   a.status = dev_status;
   if (ers::tc_supported(a.io, a.P, a.N, a.Q)) return finish(ers::tc_prefill(a, ers::Op::kScan, (cudaStream_t)stream));
   return finish(ers::fma_prefill(a, ers::Op::kScan, (cudaStream_t)stream));
@@ -209,6 +213,7 @@ ers_status ers_chunked_prefill(const ers_dims* dims, const ers_params* prm, cons
   a.y = y;
   a.ws_states = (float*)workspace;
   a.ws_tot = (float*)((char*)workspace + w.states);
+  a.ws_decay = (float*)((char*)workspace + w.states + w.tot);
   a.status = dev_status;
   if (ers::tc_supported(a.io, a.P, a.N, a.Q))
     return finish(ers::tc_prefill(a, ers::Op::kChunkedPrefill, (cudaStream_t)stream));

@@ -48,6 +48,8 @@ struct LaunchArgs {
   // workspace
   float* ws_states;  // [nseq, max_chunks, H, P, N]
   float* ws_tot;     // [nseq, max_chunks, H]
+  float* ws_decay;   // [nseq, max_chunks, H, 3, Q]: delta, Acum (hi), Acum (lo) of each chunk row
+  int ws_split;      // chain output: 0 = fp32 start states, 1 = [H_hi; H_lo] bf16 operand tiles
   const int32_t* accepted;
   int32_t* status;
 };

@@ -98,7 +98,7 @@ __device__ __forceinline__ void load_decays(const Rows<bf16>& rows, int nrows, f
 
 // X and B tile rows [0, BR): valid rows [0, nrows) from `rows`, zeros beyond
 __device__ __forceinline__ void load_xb(const Rows<bf16>& rows, int nrows, const Arena& ar) {
-  for (int id = threadIdx.x; id < (int)ar.BR * 24; id += kThreads) {
+  for (int id = threadIdx.x; id < (int)ar.BR * 24; id += blockDim.x) {
     const int r = id / 24, c = id % 24;
     if (c < 8) {
       if (r < nrows) row_to_tile(rows.x(r), ar.X, 1, r, c);
@@ -112,7 +112,7 @@ __device__ __forceinline__ void load_xb(const Rows<bf16>& rows, int nrows, const
 
 // C tile (128 rows): tile row j holds chunk row t0 + j for j in [lo - t0, hi - t0), zeros elsewhere
 __device__ __forceinline__ void load_c(const Rows<bf16>& rows, int t0, int lo, int hi, const Arena& ar) {
-  for (int id = threadIdx.x; id < 128 * 16; id += kThreads) {
+  for (int id = threadIdx.x; id < 128 * 16; id += blockDim.x) {
     const int j = id / 16, c = id % 16;
     const int t = t0 + j;
     if (t >= lo && t < hi) row_to_tile(rows.C(t), ar.C, 128, j, c);
@@ -121,17 +121,24 @@ __device__ __forceinline__ void load_c(const Rows<bf16>& rows, int t0, int lo, i
 }
 
 // ---------------------------------------------------------------------------------------------
-// Outputs of chunk rows [out_lo, out_hi) inside t-tile tau (all kThreads threads).  Tiles (C, H, B,
+// Outputs of chunk rows [out_lo, out_hi) inside t-tile tau, by all NW warps of the CTA (NW = 8 or
+// 16; warp w reads TMEM lane quarter w % 4 and a 1/(NW/4) slice of the columns).  Tiles (C, H, B,
 // X) and the scanned decays must be in place.  Rows >= tmax are invalid (their M^T rows are zero).
-// Row t's output goes to ybase + (t - out_lo) * yrs.  Returns false if a wait timed out.
+// Row t's output goes to ybase + (t - out_lo) * yrs.  Returns false if a wait timed out.  The MMA
+// sequence and every value are independent of NW.
+template <int NW>
 __device__ bool tc_outputs(const Arena& ar, int Q, int tau, int tmax, int out_lo, int out_hi, float Dh,
                            bf16* ybase, long long yrs, int32_t* status) {
+  static_assert(NW == 8 || NW == 16, "4 TMEM lane quarters x 2 or 4 column slices");
+  constexpr int NS = NW / 4;          // column slices
+  constexpr int MC = 128 / NS;        // M columns per warp and block
+  constexpr int OC = 64 / NS;         // output columns per warp
   TcHdr& hd = hdr();
   const Geom ge = geom(Q, tau);
   const uint32_t tb = hd.tmem;
   const int RG = tmem_rg(ge.S_ext);
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-  const int q = warp & 3, half = warp >> 2;
+  const int q = warp & 3, sl = warp >> 2;
   const int row = 32 * q + lane;
   const int t = ge.t0 + row;
   uint32_t phase = 0;
@@ -148,10 +155,11 @@ __device__ bool tc_outputs(const Arena& ar, int Q, int tau, int tmax, int out_lo
   // M tiles (hi over the C tile, lo over the H tile) once the Gram and off-diagonal MMAs are done
   for (int blk = 0; blk < ge.nblk && ok; ++blk) {
     const int width = ge.S_ext - 128 * blk < 128 ? ge.S_ext - 128 * blk : 128;
-    if (64 * half < width) {
-      float g[64];
-      tmem_ld64(taddr(tb, 32 * q, 128 * blk + 64 * half), g);
-      m_row(g, t, tlim, blk, half, ge.S_ext, hd.delta, hd.ahi, hd.alo, ar.C, ar.Hs, 128, row);
+    if (MC * sl < width) {
+      float g[MC];
+      if constexpr (MC == 64) tmem_ld64(taddr(tb, 32 * q, 128 * blk + MC * sl), g);
+      else tmem_ld32(taddr(tb, 32 * q, 128 * blk + MC * sl), g);
+      m_row<MC>(g, t, tlim, blk, MC * sl, ge.S_ext, hd.delta, hd.ahi, hd.alo, ar.C, ar.Hs, 128, row);
     }
     publish();
     if (threadIdx.x == 0) {
@@ -164,29 +172,36 @@ __device__ bool tc_outputs(const Arena& ar, int Q, int tau, int tmax, int out_lo
     after_sync();
   }
   if (!ok) return false;
-  // combine: thread (row, half) writes d in [32 half, 32 half + 32)
-  float oh[32], ol[32], dh[32], dl[32];
-  tmem_ld32(taddr(tb, 32 * q, RG + 32 * half), oh);
-  tmem_ld32(taddr(tb, 32 * q, RG + 64 + 32 * half), ol);
-  tmem_ld32(taddr(tb, 32 * q, 32 * half), dh);
-  tmem_ld32(taddr(tb, 32 * q, 64 + 32 * half), dl);
+  // combine: thread (row, slice) writes d in [OC sl, OC sl + OC)
+  float oh[OC], ol[OC], dh[OC], dl[OC];
+  if constexpr (OC == 32) {
+    tmem_ld32(taddr(tb, 32 * q, RG + OC * sl), oh);
+    tmem_ld32(taddr(tb, 32 * q, RG + 64 + OC * sl), ol);
+    tmem_ld32(taddr(tb, 32 * q, OC * sl), dh);
+    tmem_ld32(taddr(tb, 32 * q, 64 + OC * sl), dl);
+  } else {
+    tmem_ld16(taddr(tb, 32 * q, RG + OC * sl), oh);
+    tmem_ld16(taddr(tb, 32 * q, RG + 64 + OC * sl), ol);
+    tmem_ld16(taddr(tb, 32 * q, OC * sl), dh);
+    tmem_ld16(taddr(tb, 32 * q, 64 + OC * sl), dl);
+  }
   if (t >= out_lo && t < out_hi && row < ge.TT) {
     const float et = expf(hd.ahi[t]);
-    uint32_t packed[16];
+    uint32_t packed[OC / 2];
 #pragma unroll
-    for (int j = 0; j < 32; j += 2) {
+    for (int j = 0; j < OC; j += 2) {
       float o[2];
 #pragma unroll
       for (int u = 0; u < 2; ++u) {
-        const int d = 32 * half + j + u;
+        const int d = OC * sl + j + u;
         const float xv = __bfloat162float(*reinterpret_cast<const bf16*>(ar.X + sw128(1, t, d)));
         o[u] = combine_out(et, __fadd_rn(oh[j + u], ol[j + u]), __fadd_rn(dh[j + u], dl[j + u]), Dh, xv);
       }
       packed[j / 2] = pack_bf16x2(o[0], o[1]);
     }
-    uint4* dst = reinterpret_cast<uint4*>(ybase + (long long)(t - out_lo) * yrs + 32 * half);
+    uint4* dst = reinterpret_cast<uint4*>(ybase + (long long)(t - out_lo) * yrs + OC * sl);
 #pragma unroll
-    for (int k = 0; k < 4; ++k) dst[k] = make_uint4(packed[4 * k], packed[4 * k + 1], packed[4 * k + 2], packed[4 * k + 3]);
+    for (int k = 0; k < OC / 8; ++k) dst[k] = make_uint4(packed[4 * k], packed[4 * k + 1], packed[4 * k + 2], packed[4 * k + 3]);
   }
   return true;
 }
@@ -260,6 +275,15 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_prefill_state(LaunchArgs a) 
   uint8_t* u = ar.X + (size_t)K * 128;
   load_decays(rows, nrows, a.A[h], a.dt_bias[h]);
   load_xb(rows, nrows, ar);
+  {  // the chunk's decays, for the output kernel
+    TcHdr& hd = hdr();
+    float* wd = a.ws_decay + (((size_t)i * a.max_chunks + c) * a.H + h) * 3 * a.Q;
+    for (int t = threadIdx.x; t < a.Q; t += kThreads) {
+      wd[t] = hd.delta[t];
+      wd[a.Q + t] = hd.ahi[t];
+      wd[2 * a.Q + t] = hd.alo[t];
+    }
+  }
   cp_async_wait_all();
   __syncthreads();
   uint32_t phase = 0;
@@ -268,20 +292,23 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_prefill_state(LaunchArgs a) 
     const int q = warp & 3, half = warp >> 2;
     const int n = 32 * q + lane;
     const size_t base = ((size_t)i * a.max_chunks + c) * a.H + h;
-    float* out = a.ws_states + base * P * N;
+    uint8_t* out = reinterpret_cast<uint8_t*>(a.ws_states + base * P * N);   // tile-aligned layout
     float s[32];
     tmem_ld32(taddr(hdr().tmem, 32 * q, 32 * half), s);
 #pragma unroll 4
-    for (int j = 0; j < 32; ++j) out[(32 * half + j) * N + n] = s[j];
+    for (int j = 0; j < 32; ++j) *reinterpret_cast<float*>(out + tile_aligned_f32(32 * half + j, n)) = s[j];
     if (threadIdx.x == 0) a.ws_tot[base] = hdr().ahi[nrows - 1];
   }
   teardown_tmem(64);
 }
 
 // ---- prefill: outputs, one CTA per (chunk, t-tile, sequence, head) ---------------------------------
+constexpr int kOutWarps = 16;   // the output kernel's M tiles and epilogue are latency-bound: 16 warps
+
 template <bool CHUNKED>
-__global__ void __launch_bounds__(kThreads, 1) k_tc_prefill_out(LaunchArgs a, int ntiles, uint32_t tcols) {
-  const int c = blockIdx.x / ntiles, tau = blockIdx.x % ntiles, i = blockIdx.y, h = blockIdx.z;
+__global__ void __launch_bounds__(kOutWarps * 32, 1) k_tc_prefill_out(LaunchArgs a, int ntiles, uint32_t tcols) {
+  // the later (longer) t-tiles of every chunk are scheduled first: z = (ntiles - 1 - tau) * H + h
+  const int c = blockIdx.x, i = blockIdx.y, tau = ntiles - 1 - (int)blockIdx.z / a.H, h = blockIdx.z % a.H;
   SeqGrid sg;
   if (!seq_grid(a, CHUNKED, i, &sg) || c >= sg.nch) return;
   const Geom ge = geom(a.Q, tau);
@@ -293,13 +320,25 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_prefill_out(LaunchArgs a, in
   const Rows<bf16> rows = make_rows<bf16>(a, sg.slot, h, nbuf, tok0);
   setup_tmem(tcols);
   const Arena ar = arena(ge.S_ext);
-  load_decays(rows, nrows, a.A[h], a.dt_bias[h]);
+  {  // the chunk's decays (written by the chunk-state kernel) and its start state, already split
+     // into the [H_hi; H_lo] operand tile by the inter-chunk chain
+    TcHdr& hd = hdr();
+    const size_t unit = ((size_t)i * a.max_chunks + c) * a.H + h;
+    const float* wd = a.ws_decay + unit * 3 * a.Q;
+    const int q4 = a.Q / 4;
+    for (int k = threadIdx.x; k < 3 * q4; k += blockDim.x) {
+      const int part = k / q4, e = k % q4;
+      float* dst = part == 0 ? hd.delta : (part == 1 ? hd.ahi : hd.alo);
+      cp_async16(dst + 4 * e, wd + part * a.Q + 4 * e);
+    }
+    const uint8_t* tile = reinterpret_cast<const uint8_t*>(a.ws_states + unit * P * N);
+    for (int k = threadIdx.x; k < (int)(kHTile / 16); k += blockDim.x) cp_async16(ar.Hs + 16 * k, tile + 16 * k);
+  }
   load_xb(rows, min(nrows, ge.S_ext), ar);
   load_c(rows, ge.t0, ge.t0, min(nrows, ge.t0 + ge.TT), ar);
-  state_to_tile(a.ws_states + (((size_t)i * a.max_chunks + c) * a.H + h) * P * N, ar.Hs);
   publish();
   bf16* ybase = (bf16*)a.y + ((tok0 + out_lo) * a.H + h) * P;
-  tc_outputs(ar, a.Q, tau, nrows, out_lo, out_hi, a.D[h], ybase, (long long)a.H * P, a.status);
+  tc_outputs<kOutWarps>(ar, a.Q, tau, nrows, out_lo, out_hi, a.D[h], ybase, (long long)a.H * P, a.status);
   teardown_tmem(tcols);
 }
 
@@ -329,7 +368,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_decode(LaunchArgs a, uint32_
   if (rssm) readcopy_to_tile(Rd, ar.Hs);
   else state_to_tile(Hd, ar.Hs);
   publish();
-  bool ok = tc_outputs(ar, a.Q, tau, p + 1, p, p + 1, a.D[h], (bf16*)a.y + ((size_t)i * a.H + h) * P, 0, a.status);
+  bool ok = tc_outputs<8>(ar, a.Q, tau, p + 1, p, p + 1, a.D[h], (bf16*)a.y + ((size_t)i * a.H + h) * P, 0, a.status);
   // append the new token to the buffer (B/C once per group)
   const int g = h / (a.H / a.G);
   const bf16* nx = (const bf16*)a.x + ((size_t)i * a.H + h) * P;
@@ -426,7 +465,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_verify(LaunchArgs a, uint32_
     publish();
     bf16* ybase = (bf16*)a.y + (((size_t)i * a.T + (lo - h0)) * a.H + h) * P;
     // a fresh barrier phase sequence per tile: re-initialise between tiles
-    ok = tc_outputs(ar, a.Q, tau, nrows, lo, hi, a.D[h], ybase, (long long)a.H * P, a.status);
+    ok = tc_outputs<8>(ar, a.Q, tau, nrows, lo, hi, a.D[h], ybase, (long long)a.H * P, a.status);
     if (tau < (nrows - 1) / 128) {
       __syncthreads();
       if (threadIdx.x == 0) {
@@ -474,6 +513,8 @@ bool tc_supported(int io, int P_, int N_, int Q) {
 cudaError_t tc_prefill(const LaunchArgs& a, Op op, cudaStream_t s) {
   const bool chunked = op == Op::kChunkedPrefill;
   cudaError_t e;
+  LaunchArgs b = a;
+  b.ws_split = 1;   // the chain hands the output kernel ready [H_hi; H_lo] tiles
   if (a.max_chunks > 0 && a.nseq > 0) {
     const int ntiles = (a.Q + 127) / 128;
     const size_t ss = state_smem(a.Q), so = out_smem(a.Q);
@@ -482,14 +523,14 @@ cudaError_t tc_prefill(const LaunchArgs& a, Op op, cudaStream_t s) {
       if ((e = set_smem(k_tc_prefill_state<true>, ss)) != cudaSuccess) return e;
       if ((e = set_smem(k_tc_prefill_out<true>, so)) != cudaSuccess) return e;
       k_tc_prefill_state<true><<<dim3(a.max_chunks, a.nseq, a.H), kThreads, ss, s>>>(a);
-      if ((e = launch_chain(a, true, s)) != cudaSuccess) return e;
-      k_tc_prefill_out<true><<<dim3(a.max_chunks * ntiles, a.nseq, a.H), kThreads, so, s>>>(a, ntiles, tcols);
+      if ((e = launch_chain(b, true, s)) != cudaSuccess) return e;
+      k_tc_prefill_out<true><<<dim3(a.max_chunks, a.nseq, a.H * ntiles), kOutWarps * 32, so, s>>>(a, ntiles, tcols);
     } else {
       if ((e = set_smem(k_tc_prefill_state<false>, ss)) != cudaSuccess) return e;
       if ((e = set_smem(k_tc_prefill_out<false>, so)) != cudaSuccess) return e;
       k_tc_prefill_state<false><<<dim3(a.max_chunks, a.nseq, a.H), kThreads, ss, s>>>(a);
-      if ((e = launch_chain(a, false, s)) != cudaSuccess) return e;
-      k_tc_prefill_out<false><<<dim3(a.max_chunks * ntiles, a.nseq, a.H), kThreads, so, s>>>(a, ntiles, tcols);
+      if ((e = launch_chain(b, false, s)) != cudaSuccess) return e;
+      k_tc_prefill_out<false><<<dim3(a.max_chunks, a.nseq, a.H * ntiles), kOutWarps * 32, so, s>>>(a, ntiles, tcols);
     }
   }
   if (chunked) return launch_tail(a, s);

@@ -134,6 +134,28 @@ __device__ __forceinline__ void split8(const float (&v)[8], uint4& hi, uint4& lo
   lo = make_uint4(pack_bf16x2(l[0], l[1]), pack_bf16x2(l[2], l[3]), pack_bf16x2(l[4], l[5]), pack_bf16x2(l[6], l[7]));
 }
 
+// Byte offset, inside a [H_hi; H_lo] tile slot (32 KB), of fp32 state element (d, n) in the
+// "tile-aligned" layout the prefill workspace uses: elements n4 = n & ~3 .. n4 + 1 of row d sit in
+// the 8 bytes that will hold their hi halves (tile row d), elements n4 + 2, n4 + 3 in the 8 bytes
+// of their lo halves (tile row P + d).  A thread that owns (d, n4 .. n4 + 3) reads exactly the 16
+// bytes it later overwrites with the split values.
+__host__ __device__ __forceinline__ uint32_t tile_aligned_f32(uint32_t d, uint32_t n) {
+  const uint32_t n4 = n & ~3u, e = n & 3u;
+  return e < 2 ? sw128(128, d, n4) + 4 * e : sw128(128, P + d, n4) + 4 * (e - 2);
+}
+
+// 4 fp32 values -> hi and lo bf16 (8 bytes each), the same operations as split8
+__device__ __forceinline__ void split4(const float (&v)[4], uint2& hi, uint2& lo) {
+  float h[4], l[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    h[i] = __bfloat162float(__float2bfloat16_rn(v[i]));
+    l[i] = __fsub_rn(v[i], h[i]);
+  }
+  hi = make_uint2(pack_bf16x2(h[0], h[1]), pack_bf16x2(h[2], h[3]));
+  lo = make_uint2(pack_bf16x2(l[0], l[1]), pack_bf16x2(l[2], l[3]));
+}
+
 // fp32 state [64][128] -> [H_hi; H_lo] tile.  Called by all kThreads threads (blockDim.x ==
 // kThreads); every thread's loads are issued before any of its splits.
 __device__ __forceinline__ void state_to_tile(const float* __restrict__ H, uint8_t* tile) {
@@ -216,28 +238,33 @@ __device__ __forceinline__ void build_u_tiles(const uint8_t* xT, const float* w,
 }
 
 // Row `row` (chunk row t = t0 + row) of the masked decayed Gram for block blk, 64 columns
-// [64*half, 64*half + 64) of the block, from 64 Gram values g[] (TMEM columns of the same range).
+// [col0, col0 + NC) of the block, from NC Gram values g[] (TMEM columns of the same range).
+// The segment decay uses the hardware exponential (__expf): its relative error (a few 1e-7 for the
+// O(1) segment sums that matter, growing with |Acum_t - Acum_s| only where the decay is already
+// negligible) is far below the 2^-16 resolution of the hi + lo bf16 split it feeds.
 // Writes hi and lo bf16 to the M tiles at tile row `trow` (atoms mR rows apart).  Entries with
 // s > t, s >= S_ext or t >= tmax are zero.
-__device__ __forceinline__ void m_row(const float (&g)[64], int t, int tmax, int blk, int half, int S_ext,
+template <int NC>
+__device__ __forceinline__ void m_row(const float (&g)[NC], int t, int tmax, int blk, int col0, int S_ext,
                                       const float* delta, const float* ahi, const float* alo, uint8_t* mhi,
                                       uint8_t* mlo, uint32_t mR, uint32_t trow) {
+  static_assert(NC % 8 == 0, "whole 16-byte chunks");
   const df at = {ahi[t], alo[t]};
 #pragma unroll
-  for (int c = 0; c < 8; ++c) {
+  for (int c = 0; c < NC / 8; ++c) {
     float v[8];
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
-      const int sl = 64 * half + 8 * c + i;  // s within the block
+      const int sl = col0 + 8 * c + i;  // s within the block
       const int s = 128 * blk + sl;
       float m = 0.f;
       if (s <= t && s < S_ext && t < tmax)
-        m = __fmul_rn(__fmul_rn(g[8 * c + i], delta[s]), expf(df_diff(at, df{ahi[s], alo[s]})));
+        m = __fmul_rn(__fmul_rn(g[8 * c + i], delta[s]), __expf(df_diff(at, df{ahi[s], alo[s]})));
       v[i] = m;
     }
     uint4 hi, lo;
     split8(v, hi, lo);
-    const uint32_t off = sw128(mR, trow, 64 * half + 8 * c);
+    const uint32_t off = sw128(mR, trow, col0 + 8 * c);
     *reinterpret_cast<uint4*>(mhi + off) = hi;
     *reinterpret_cast<uint4*>(mlo + off) = lo;
   }
