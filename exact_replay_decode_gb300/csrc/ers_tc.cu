@@ -255,8 +255,10 @@ __device__ __forceinline__ void fold_from_tmem(float* Hd, bf16* Rd, float decay)
 }
 
 // ---- prefill: chunk states ------------------------------------------------------------------------
+constexpr int kStateWarps = 16;   // U-tile build and loads are latency-bound: 16 warps
+
 template <bool CHUNKED>
-__global__ void __launch_bounds__(kThreads, 1) k_tc_prefill_state(LaunchArgs a) {
+__global__ void __launch_bounds__(kStateWarps * 32, 1) k_tc_prefill_state(LaunchArgs a) {
   const int c = blockIdx.x, i = blockIdx.y, h = blockIdx.z;
   SeqGrid sg;
   if (!seq_grid(a, CHUNKED, i, &sg) || c >= sg.nch) return;
@@ -273,12 +275,12 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_prefill_state(LaunchArgs a) 
   ar.C = nullptr;
   ar.Hs = nullptr;
   uint8_t* u = ar.X + (size_t)K * 128;
+  load_xb(rows, nrows, ar);   // asynchronous: lands while the decays are scanned
   load_decays(rows, nrows, a.A[h], a.dt_bias[h]);
-  load_xb(rows, nrows, ar);
   {  // the chunk's decays, for the output kernel
     TcHdr& hd = hdr();
     float* wd = a.ws_decay + (((size_t)i * a.max_chunks + c) * a.H + h) * 3 * a.Q;
-    for (int t = threadIdx.x; t < a.Q; t += kThreads) {
+    for (int t = threadIdx.x; t < a.Q; t += blockDim.x) {
       wd[t] = hd.delta[t];
       wd[a.Q + t] = hd.ahi[t];
       wd[2 * a.Q + t] = hd.alo[t];
@@ -289,14 +291,15 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_prefill_state(LaunchArgs a) 
   uint32_t phase = 0;
   if (tc_state(ar, nrows, u, a.status, &phase)) {
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-    const int q = warp & 3, half = warp >> 2;
+    constexpr int DC = P / (kStateWarps / 4);   // state columns (d) per warp
+    const int q = warp & 3, sl = warp >> 2;
     const int n = 32 * q + lane;
     const size_t base = ((size_t)i * a.max_chunks + c) * a.H + h;
     uint8_t* out = reinterpret_cast<uint8_t*>(a.ws_states + base * P * N);   // tile-aligned layout
-    float s[32];
-    tmem_ld32(taddr(hdr().tmem, 32 * q, 32 * half), s);
-#pragma unroll 4
-    for (int j = 0; j < 32; ++j) *reinterpret_cast<float*>(out + tile_aligned_f32(32 * half + j, n)) = s[j];
+    float s[DC];
+    tmem_ld16(taddr(hdr().tmem, 32 * q, DC * sl), s);
+#pragma unroll
+    for (int j = 0; j < DC; ++j) *reinterpret_cast<float*>(out + tile_aligned_f32(DC * sl + j, n)) = s[j];
     if (threadIdx.x == 0) a.ws_tot[base] = hdr().ahi[nrows - 1];
   }
   teardown_tmem(64);
@@ -522,13 +525,13 @@ cudaError_t tc_prefill(const LaunchArgs& a, Op op, cudaStream_t s) {
     if (chunked) {
       if ((e = set_smem(k_tc_prefill_state<true>, ss)) != cudaSuccess) return e;
       if ((e = set_smem(k_tc_prefill_out<true>, so)) != cudaSuccess) return e;
-      k_tc_prefill_state<true><<<dim3(a.max_chunks, a.nseq, a.H), kThreads, ss, s>>>(a);
+      k_tc_prefill_state<true><<<dim3(a.max_chunks, a.nseq, a.H), kStateWarps * 32, ss, s>>>(a);
       if ((e = launch_chain(b, true, s)) != cudaSuccess) return e;
       k_tc_prefill_out<true><<<dim3(a.max_chunks, a.nseq, a.H * ntiles), kOutWarps * 32, so, s>>>(a, ntiles, tcols);
     } else {
       if ((e = set_smem(k_tc_prefill_state<false>, ss)) != cudaSuccess) return e;
       if ((e = set_smem(k_tc_prefill_out<false>, so)) != cudaSuccess) return e;
-      k_tc_prefill_state<false><<<dim3(a.max_chunks, a.nseq, a.H), kThreads, ss, s>>>(a);
+      k_tc_prefill_state<false><<<dim3(a.max_chunks, a.nseq, a.H), kStateWarps * 32, ss, s>>>(a);
       if ((e = launch_chain(b, false, s)) != cudaSuccess) return e;
       k_tc_prefill_out<false><<<dim3(a.max_chunks, a.nseq, a.H * ntiles), kOutWarps * 32, so, s>>>(a, ntiles, tcols);
     }
