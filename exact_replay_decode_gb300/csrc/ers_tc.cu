@@ -254,11 +254,57 @@ __device__ __forceinline__ void fold_from_tmem(float* Hd, bf16* Rd, float decay)
   }
 }
 
+// X and B rows [s0, s0 + 128) into 128-row block tiles (zeros from row nrows on); asynchronous.
+__device__ __forceinline__ void load_xb_block(const Rows<bf16>& rows, int nrows, int s0, uint8_t* Bt, uint8_t* Xt) {
+  for (int id = threadIdx.x; id < 128 * 24; id += blockDim.x) {
+    const int r = id / 24, c = id % 24, s = s0 + r;
+    if (c < 8) {
+      if (s < nrows) row_to_tile(rows.x(s), Xt, 1, r, c);
+      else zero_tile_chunk(Xt, 1, r, c);
+    } else {
+      if (s < nrows) row_to_tile(rows.B(s), Bt, 128, r, c - 8);
+      else zero_tile_chunk(Bt, 128, r, c - 8);
+    }
+  }
+}
+
+// tc_state with the B and X rows loaded one 128-row K block at a time (block 0 already issued by
+// the caller).  Same weights, U tiles and MMA sequence, so the same chunk state.
+__device__ bool tc_state_blocked(const Rows<bf16>& rows, int nrows, int K, uint8_t* Bt, uint8_t* Xt, uint8_t* u,
+                                 int32_t* status, uint32_t* phase) {
+  TcHdr& hd = hdr();
+  if (threadIdx.x < nrows) {
+    const df last = {hd.ahi[nrows - 1], hd.alo[nrows - 1]};
+    hd.w[threadIdx.x] =
+        __fmul_rn(hd.delta[threadIdx.x], expf(df_diff(last, df{hd.ahi[threadIdx.x], hd.alo[threadIdx.x]})));
+  }
+  uint8_t* u0 = u;
+  uint8_t* u1 = u + 128 * 128;
+  uint8_t* u2 = u + 2 * 128 * 128;
+  bool ok = true;
+  for (int s0 = 0; s0 < K && ok; s0 += 128) {
+    const int nr = K - s0 < 128 ? K - s0 : 128;
+    if (s0 > 0) load_xb_block(rows, nrows, s0, Bt, Xt);
+    cp_async_wait_all();
+    __syncthreads();
+    build_u_tiles(Xt - (size_t)s0 * 128, hd.w, nrows, s0, nr, u0, u1, u2);   // X rows addressed by s
+    publish();
+    if (threadIdx.x == 0) {
+      issue_state_block_rel(hd.tmem, smem_u32(Bt), smem_u32(u0), smem_u32(u1), smem_u32(u2), nr / 16, s0 > 0);
+      commit(&hd.bar);
+    }
+    ok = __syncthreads_and(mbar_wait(&hd.bar, *phase, status));
+    *phase ^= 1;
+    after_sync();
+  }
+  return ok;
+}
+
 // ---- prefill: chunk states ------------------------------------------------------------------------
 constexpr int kStateWarps = 16;   // U-tile build and loads are latency-bound: 16 warps
 
 template <bool CHUNKED>
-__global__ void __launch_bounds__(kStateWarps * 32, 1) k_tc_prefill_state(LaunchArgs a) {
+__global__ void __launch_bounds__(kStateWarps * 32, 2) k_tc_prefill_state(LaunchArgs a) {
   const int c = blockIdx.x, i = blockIdx.y, h = blockIdx.z;
   SeqGrid sg;
   if (!seq_grid(a, CHUNKED, i, &sg) || c >= sg.nch) return;
@@ -267,15 +313,12 @@ __global__ void __launch_bounds__(kStateWarps * 32, 1) k_tc_prefill_state(Launch
   const Rows<bf16> rows = make_rows<bf16>(a, sg.slot, h, nbuf, (long long)a.cu[i] + (long long)c * a.Q - sg.p);
   const int K = round16(nrows);
   setup_tmem(64);
-  // arena: B (K x 256) | X (K x 128) | U (3 x K x 128)
-  Arena ar;
-  ar.BR = K;
-  ar.B = tiles();
-  ar.X = ar.B + (size_t)K * 256;
-  ar.C = nullptr;
-  ar.Hs = nullptr;
-  uint8_t* u = ar.X + (size_t)K * 128;
-  load_xb(rows, nrows, ar);   // asynchronous: lands while the decays are scanned
+  // arena: B block (128 x 256) | X block (128 x 128) | U (3 x 128 x 128): one 128-row K block at a
+  // time, so that two CTAs fit on an SM
+  uint8_t* Bt = tiles();
+  uint8_t* Xt = Bt + 128 * 256;
+  uint8_t* u = Xt + 128 * 128;
+  load_xb_block(rows, nrows, 0, Bt, Xt);   // asynchronous: lands while the decays are scanned
   load_decays(rows, nrows, a.A[h], a.dt_bias[h]);
   {  // the chunk's decays, for the output kernel
     TcHdr& hd = hdr();
@@ -286,10 +329,8 @@ __global__ void __launch_bounds__(kStateWarps * 32, 1) k_tc_prefill_state(Launch
       wd[2 * a.Q + t] = hd.alo[t];
     }
   }
-  cp_async_wait_all();
-  __syncthreads();
   uint32_t phase = 0;
-  if (tc_state(ar, nrows, u, a.status, &phase)) {
+  if (tc_state_blocked(rows, nrows, K, Bt, Xt, u, a.status, &phase)) {
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
     constexpr int DC = P / (kStateWarps / 4);   // state columns (d) per warp
     const int q = warp & 3, sl = warp >> 2;
@@ -506,6 +547,7 @@ cudaError_t set_smem(K kernel, size_t bytes) {
 
 size_t out_smem(int BR) { return kHdrBytes + arena_bytes(BR) + 1024; }
 size_t state_smem(int K) { return kHdrBytes + (size_t)K * (256 + 128) + kUBytes + 1024; }
+size_t state_blocked_smem() { return kHdrBytes + 128 * (256 + 128) + kUBytes + 1024; }
 
 }  // namespace
 
@@ -520,7 +562,7 @@ cudaError_t tc_prefill(const LaunchArgs& a, Op op, cudaStream_t s) {
   b.ws_split = 1;   // the chain hands the output kernel ready [H_hi; H_lo] tiles
   if (a.max_chunks > 0 && a.nseq > 0) {
     const int ntiles = (a.Q + 127) / 128;
-    const size_t ss = state_smem(a.Q), so = out_smem(a.Q);
+    const size_t ss = state_blocked_smem(), so = out_smem(a.Q);
     const uint32_t tcols = tmem_cols(a.Q);
     if (chunked) {
       if ((e = set_smem(k_tc_prefill_state<true>, ss)) != cudaSuccess) return e;

@@ -116,6 +116,19 @@ __device__ __forceinline__ void issue_state_block(uint32_t tS, uint32_t bT, uint
   }
 }
 
+// The same MMAs for one 128-row K block held in its own tile (rows relative to the block):
+// accumulate = acc_in || term > 0 || k > 0 reproduces the sequence above for s0 = 128 * blk.
+__device__ __forceinline__ void issue_state_block_rel(uint32_t tS, uint32_t bT, uint32_t u0, uint32_t u1,
+                                                      uint32_t u2, int nk, bool acc_in) {
+  const uint32_t id = idesc_bf16(128, P, true, true);
+  for (int term = 0; term < 3; ++term) {
+    const uint32_t uT = term == 0 ? u0 : (term == 1 ? u1 : u2);
+    for (int k = 0; k < nk; ++k)
+      mma(tS, sdesc(bT + (uint32_t)(16 * k) * 128u, 128u * 128u, 1024), sdesc(uT + (uint32_t)k * 2048u, 1024, 1024),
+          id, (acc_in || term > 0 || k > 0) ? 1u : 0u);
+  }
+}
+
 // ---- operand builders (generic proxy writes; the caller fences before issuing) ---------------------
 __device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
   const __nv_bfloat162 v = __floats2bfloat162_rn(a, b);
