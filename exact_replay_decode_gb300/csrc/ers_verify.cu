@@ -35,7 +35,7 @@ constexpr size_t verify_smem_bytes() {
          + (size_t)kHeadsPerCta * QR * P * sizeof(T)                 // x rows, per warp
          + (size_t)kDraftsMax * QR * sizeof(float)                   // Gram rows, per draft
          + (size_t)kHeadsPerCta * kDraftsMax * P * sizeof(float)     // off-diagonal terms, per warp
-         + (size_t)kHeadsPerCta * QM * sizeof(float);                // flush weights, per warp
+         + (size_t)kHeadsPerCta * QM * P * sizeof(float);            // flush w_s x_s[d], per warp
 }
 
 // Read-copy stream: yo[k * P + d] = Dot<128>(C of draft k, R[d]) for all rows d.  q holds rows
@@ -64,53 +64,50 @@ __device__ __forceinline__ void stream_read_copy(const __nv_bfloat16* __restrict
 }
 
 // Flush stream: each anchor row is folded with the committed records (chunk_state / fold_state
-// order, weights sw[s] for s < hc), written back to the anchor, cast to bf16 into the read copy, and
-// the cast values feed the drafts' dot products (yo as above).
+// order: acc = fma(w_s x_s[d], B_s[n], acc) over s < hc, then fma(decay, H, acc)), written back to
+// the anchor, cast to bf16 into the read copy, and the cast values feed the drafts' dot products
+// (yo as above).  wx[s * P + d] = w_s x_s[d] is precomputed per warp; 8 rows per pass.
 template <typename T, int P, int N>
 __device__ __noinline__ void stream_anchor_flush(float* __restrict__ Hd, __nv_bfloat16* __restrict__ Rd,
                                                  const float (&c)[kDraftsMax][4], float* yo, int j, int hc,
-                                                 const float* sw, float decay, const T* sB, const T* sx) {
+                                                 const float* wx, float decay, const T* sB) {
 #pragma unroll 1
   for (int d0 = 0; d0 < P; d0 += 8) {
+    float h[8][4], acc[8][4];
+#pragma unroll
+    for (int r = 0; r < 8; ++r) {
+      Quad<float>::unpack(__ldcs(reinterpret_cast<const float4*>(Hd + (size_t)(d0 + r) * N + 4 * j)), h[r]);
+#pragma unroll
+      for (int e = 0; e < 4; ++e) acc[r][e] = 0.f;
+    }
+    for (int s = 0; s < hc; ++s) {
+      float bs[4];
+      lds4(sB + s * N + 4 * j, bs);
+      const float4 w0 = *reinterpret_cast<const float4*>(wx + s * P + d0);
+      const float4 w1 = *reinterpret_cast<const float4*>(wx + s * P + d0 + 4);
+      const float wr[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
+#pragma unroll
+      for (int r = 0; r < 8; ++r)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) acc[r][e] = __fmaf_rn(wr[r], bs[e], acc[r][e]);
+    }
     float part[32];
 #pragma unroll
-    for (int half = 0; half < 2; ++half) {
-      const int db = d0 + 4 * half;
-      float h[4][4], acc[4][4];
+    for (int r = 0; r < 8; ++r) {
+      float v[4];
 #pragma unroll
-      for (int r = 0; r < 4; ++r) {
-        Quad<float>::unpack(__ldcs(reinterpret_cast<const float4*>(Hd + (size_t)(db + r) * N + 4 * j)), h[r]);
+      for (int e = 0; e < 4; ++e) v[e] = __fmaf_rn(decay, h[r][e], acc[r][e]);
+      const size_t o = (size_t)(d0 + r) * N + 4 * j;
+      *reinterpret_cast<float4*>(Hd + o) = make_float4(v[0], v[1], v[2], v[3]);
+      __nv_bfloat162 lo2 = __floats2bfloat162_rn(v[0], v[1]), hi2 = __floats2bfloat162_rn(v[2], v[3]);
+      uint2 u;
+      u.x = *reinterpret_cast<uint32_t*>(&lo2);
+      u.y = *reinterpret_cast<uint32_t*>(&hi2);
+      *reinterpret_cast<uint2*>(Rd + o) = u;
+      float rv[4];
+      Quad<__nv_bfloat16>::unpack(u, rv);
 #pragma unroll
-        for (int e = 0; e < 4; ++e) acc[r][e] = 0.f;
-      }
-      for (int s = 0; s < hc; ++s) {
-        float bs[4];
-        lds4(sB + s * N + 4 * j, bs);
-        const float ws = sw[s];
-#pragma unroll
-        for (int r = 0; r < 4; ++r) {
-          const float wx = __fmul_rn(ws, to_f(sx[s * P + db + r]));
-#pragma unroll
-          for (int e = 0; e < 4; ++e) acc[r][e] = __fmaf_rn(wx, bs[e], acc[r][e]);
-        }
-      }
-#pragma unroll
-      for (int r = 0; r < 4; ++r) {
-        float v[4];
-#pragma unroll
-        for (int e = 0; e < 4; ++e) v[e] = __fmaf_rn(decay, h[r][e], acc[r][e]);
-        const size_t o = (size_t)(db + r) * N + 4 * j;
-        *reinterpret_cast<float4*>(Hd + o) = make_float4(v[0], v[1], v[2], v[3]);
-        __nv_bfloat162 lo2 = __floats2bfloat162_rn(v[0], v[1]), hi2 = __floats2bfloat162_rn(v[2], v[3]);
-        uint2 u;
-        u.x = *reinterpret_cast<uint32_t*>(&lo2);
-        u.y = *reinterpret_cast<uint32_t*>(&hi2);
-        *reinterpret_cast<uint2*>(Rd + o) = u;
-        float rv[4];
-        Quad<__nv_bfloat16>::unpack(u, rv);
-#pragma unroll
-        for (int k = 0; k < kDraftsMax; ++k) part[k * 8 + 4 * half + r] = Dot<N>::partial(c[k], rv);
-      }
+      for (int k = 0; k < kDraftsMax; ++k) part[k * 8 + r] = Dot<N>::partial(c[k], rv);
     }
     const float v = reduce_scatter32(part, j);
     yo[(j >> 3) * P + d0 + (j & 7)] = v;
@@ -221,7 +218,7 @@ __global__ void __launch_bounds__(kThreads, 2) k_verify_heads(LaunchArgs a) {
       if (j == 0) sg[k * QR + s] = gv;
     }
   // a flushing slot folds its committed records (rows 0..hc-1) into the anchor
-  float* sw = swa + w * QM;
+  float* sw = swa + w * QM * P;
   float decay = 0.f;
   if (flush) {
     float dc = 0.f;
@@ -232,28 +229,63 @@ __global__ void __launch_bounds__(kThreads, 2) k_verify_heads(LaunchArgs a) {
     }
     vc = warp_scan(vc, j);
     const df last = {__shfl_sync(kFull, vc.hi, hc - 1), __shfl_sync(kFull, vc.lo, hc - 1)};
-    if (j < hc) sw[j] = __fmul_rn(dc, expf(df_diff(last, vc)));
+    const float wl = j < hc ? __fmul_rn(dc, expf(df_diff(last, vc))) : 0.f;   // state_weights
     decay = expf(last.hi);
+    for (int s = 0; s < hc; ++s) {   // chunk_state's w_s x_s[d], once per (s, d)
+      const float ws = __shfl_sync(kFull, wl, s);
+#pragma unroll
+      for (int m = 0; m < P / 32; ++m) sw[s * P + 32 * m + j] = __fmul_rn(ws, to_f(sx[s * P + 32 * m + j]));
+    }
     __syncwarp();
   }
   __syncthreads();
   if (!active) return;
   if (flush)
-    stream_anchor_flush<T, P, N>(a.state + soff, (__nv_bfloat16*)a.read_copy + soff, c, yo, j, hc, sw, decay, sB, sx);
-  // outputs of draft k (row t = h0 + k): d = j and j + 32 for P = 64
+    stream_anchor_flush<T, P, N>(a.state + soff, (__nv_bfloat16*)a.read_copy + soff, c, yo, j, hc, sw, decay, sB);
+  // outputs of draft k (row t_k = h0 + k), d = j + 32 m: one pass over the rows s serves every draft
+  // (each draft's sum still runs over s = 0..t_k in order)
   const float Dh = a.D[h];
-  for (int k = 0; k < Td; ++k) {
-    const int t = h0 + k;
-    const df at = {__shfl_sync(kFull, v.hi, t), __shfl_sync(kFull, v.lo, t)};
-    float M = 0.f;
-    if (j <= t) M = __fmul_rn(__fmul_rn(sg[k * QR + j], dl), expf(df_diff(at, v)));
-    const float et = expf(at.hi);
+  float Mk[kDraftsMax], et[kDraftsMax];
+#pragma unroll
+  for (int k = 0; k < kDraftsMax; ++k) {
+    Mk[k] = 0.f;
+    et[k] = 0.f;
+    if (k < Td) {
+      const int t = h0 + k;
+      const df at = {__shfl_sync(kFull, v.hi, t), __shfl_sync(kFull, v.lo, t)};
+      if (j <= t) Mk[k] = __fmul_rn(__fmul_rn(sg[k * QR + j], dl), expf(df_diff(at, v)));
+      et[k] = expf(at.hi);
+    }
+  }
+  constexpr int DPL = P / 32;   // outputs per lane and draft
+  float acc[kDraftsMax][DPL];
+#pragma unroll
+  for (int k = 0; k < kDraftsMax; ++k)
+#pragma unroll
+    for (int m = 0; m < DPL; ++m) acc[k][m] = 0.f;
+  const int tlast = h0 + Td - 1;
+  for (int s = 0; s <= tlast; ++s) {
+    float xs[DPL];
+    const T* xr = sx + (s < h0 ? s : QM + s - h0) * P;
+#pragma unroll
+    for (int m = 0; m < DPL; ++m) xs[m] = to_f(xr[32 * m + j]);
+#pragma unroll
+    for (int k = 0; k < kDraftsMax; ++k) {
+      const float Ms = __shfl_sync(kFull, Mk[k], s);
+      if (k < Td && s <= h0 + k) {
+#pragma unroll
+        for (int m = 0; m < DPL; ++m) acc[k][m] = __fmaf_rn(Ms, xs[m], acc[k][m]);
+      }
+    }
+  }
+#pragma unroll
+  for (int k = 0; k < kDraftsMax; ++k) {
+    if (k >= Td) break;
     T* y = (T*)a.y + ((size_t)i * Td + k) * HP + (size_t)h * P;
-    for (int d = j; d < P; d += 32) {
-      float acc = 0.f;
-      for (int s = 0; s <= t; ++s)
-        acc = __fmaf_rn(__shfl_sync(kFull, M, s), to_f(sx[(s < h0 ? s : QM + s - h0) * P + d]), acc);
-      y[d] = from_f<T>(combine_out(et, yo[k * P + d], acc, Dh, to_f(sx[(QM + k) * P + d])));
+#pragma unroll
+    for (int m = 0; m < DPL; ++m) {
+      const int d = 32 * m + j;
+      y[d] = from_f<T>(combine_out(et[k], yo[k * P + d], acc[k][m], Dh, to_f(sx[(QM + k) * P + d])));
     }
   }
   // the drafts go to buffer rows h0..h0+T-1 (B/C once per group)
