@@ -45,22 +45,27 @@ L2_FLUSH_BYTES = 256 << 20
 
 
 DECODE_PROFILE = os.path.join(ROOT, "profiles", "k_decode_heads.decode_b256_h64.md")
-DECODE_SOURCE = os.path.join(ROOT, "exact_replay_decode_gb300", "csrc", "ers_decode.cu")
+DECODE_SOURCES = [os.path.join(ROOT, "exact_replay_decode_gb300", "csrc", f)
+                  for f in ("ers_decode.cu", "warp_heads.cuh", "ers_common.cuh")]
 
 
-def profiled_traffic(profile: str = DECODE_PROFILE, source: str = DECODE_SOURCE):
+def profiled_traffic(profile: str = DECODE_PROFILE, sources=None):
     """DRAM bytes per launch (dram__bytes_read.sum + dram__bytes_write.sum) from the committed ncu
-    summary, or None when the kernel source has changed since the capture (or no record exists)."""
+    summary, or None when the kernel's sources have changed since the capture (sha256 over the
+    concatenated files) or no record exists."""
     import hashlib
     import re
+    sources = DECODE_SOURCES if sources is None else sources
     try:
         text = open(profile).read()
         want = re.search(r"kernel_source_sha256 = ([0-9a-f]{64})", text).group(1)
         traffic = int(re.search(r"traffic_per_launch_bytes = (\d+)", text).group(1))
-        have = hashlib.sha256(open(source, "rb").read()).hexdigest()
+        hsh = hashlib.sha256()
+        for f in sources:
+            hsh.update(open(f, "rb").read())
     except (OSError, AttributeError):
         return None
-    return traffic if have == want else None
+    return traffic if hsh.hexdigest() == want else None
 
 
 def _peaks():
