@@ -40,7 +40,7 @@ def _single_shot(w, prm, hist, stream, batch, steps):
     for i in range(batch):
         rows = [k * batch + i for k in range(steps)]
         parts.append(synth.Tokens.concat([hist[i], synth.Tokens(stream.x[rows], stream.dt[rows], stream.B[rows],
-                                                                 stream.C[rows], True)]))
+                                                                 stream.C[rows], stream.bf16)]))
     allt = synth.Tokens.concat(parts)
     lens = [p.ntokens for p in parts]
     cu = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
@@ -144,3 +144,35 @@ def test_decode_bitwise_across_engines_and_chunk_sizes(chunk):
         nb = (p.ntokens // chunk) * chunk
         _, s_o = oracle.recurrence(p.x[:nb], p.dt[:nb], params.A, p.B[:nb], p.C[:nb], params.D, params.dt_bias)
         assert state_err(cache.state[i], s_o[0]) <= STATE_TOL
+
+
+@pytest.mark.parametrize("heads,groups,bf16", [(32, 2, True), (16, 2, False), (20, 2, True)])
+def test_decode_head_blocks_and_fp32_io(heads, groups, bf16):
+    """The warp-per-head decode with 16 heads per group (two head blocks per group), with fp32 io,
+    and with 10 heads per group (a partly idle second head block): bitwise equal to single-shot
+    prefill, and within tolerance of the oracle."""
+    import dataclasses
+    ers = _ers()
+    base = synth.workload("decode_b256_h64")
+    w = dataclasses.replace(base, dims=synth.Dims(heads, groups, 64, 128, 16), batch=6, steps=40, bf16=bf16,
+                            history_chunks=1)
+    S, K = w.batch, w.steps
+    d = w.dims
+    params, hist, p0, stream = synth.decode_inputs(w, seed=21, batch=S, steps=K)
+    prm = layer(params)
+    io = torch.bfloat16 if bf16 else torch.float32
+    cache = ers.ReplayCache(S, d.nheads, d.ngroups, d.headdim, d.dstate, d.chunk, io)
+    htoks = synth.Tokens.concat(hist)
+    cu = torch.tensor(np.concatenate([[0], np.cumsum([h.ntokens for h in hist])]), dtype=torch.int32, device=dev())
+    ers.chunked_prefill(cache, prm, *torch_io.tokens_to(htoks, dev()), cu)
+    sx, sdt, sB, sC = torch_io.tokens_to(stream, dev(), lead=(K, S))
+    ys = torch.stack([ers.replay_decode(cache, prm, sx[k], sdt[k], sB[k], sC[k]) for k in range(K)])
+    parts, cu_ss, y_ss, _ = _single_shot(w, prm, hist, stream, S, K)
+    for i in range(S):
+        ref = y_ss[int(cu_ss[i]) + hist[i].ntokens:int(cu_ss[i + 1])]
+        assert same_bits(ys[:, i], ref), f"sequence {i} (p0={p0[i]})"
+    tol = 2e-3 if bf16 else 1e-5
+    for i in (0, S - 1):
+        p = parts[i]
+        y_o, _ = oracle.recurrence(p.x, p.dt, params.A, p.B, p.C, params.D, params.dt_bias)
+        assert out_err(ys[:, i], y_o[hist[i].ntokens:]) <= tol

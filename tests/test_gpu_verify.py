@@ -27,7 +27,8 @@ def _prefilled(w, S, steps, seed, history=32):
     hx, hdt, hB, hC = torch_io.tokens_to(hist, dev())
     cu = torch.arange(0, S * history + 1, history, dtype=torch.int32, device=dev())
     _, fin = ers.ssd_scan_fwd(hx, hdt, prm, hB, hC, chunk=d.chunk, cu_seqlens=cu)
-    cache = ers.ReplayCache(S, d.nheads, d.ngroups, d.headdim, d.dstate, d.chunk, torch.bfloat16, read_copy=True)
+    io = torch.bfloat16 if w.bf16 else torch.float32
+    cache = ers.ReplayCache(S, d.nheads, d.ngroups, d.headdim, d.dstate, d.chunk, io, read_copy=True)
     cache.state.copy_(fin)
     ers.refresh(cache, prm, replayssm=True, drafts_T=d.chunk + 1)   # h = 0 everywhere: cast the read copy
     return params, prm, hist, drafts, acc, cache
@@ -122,3 +123,13 @@ def test_anchor_independent_of_read_copy():
         differ |= not same_bits(y1, y2)
     assert differ
     assert same_bits(c1.state, c2.state)
+
+
+@pytest.mark.parametrize("heads,groups,bf16,drafts", [(16, 2, False, 4), (32, 2, True, 4), (16, 2, True, 6)])
+def test_verify_fp32_io_wide_groups_and_long_drafts(heads, groups, bf16, drafts):
+    """Verify with fp32 io on the warp-per-head kernel, and on the per-(sequence, head) kernels it
+    hands over to when a group has more than 8 heads or there are more than 4 drafts."""
+    import dataclasses
+    base = synth.workload("verify_b512_t4")
+    w = dataclasses.replace(base, dims=synth.Dims(heads, groups, 64, 128, 16), bf16=bf16, drafts=drafts)
+    _verify_vs_nonspec(w, 8, 24, 4, [0, 7])
