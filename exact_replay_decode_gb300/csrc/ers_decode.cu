@@ -32,7 +32,7 @@ using namespace wh;
 template <typename T, int P, int N, int QM>
 constexpr size_t heads_smem_bytes() {
   return (size_t)QM * N * sizeof(T) + (size_t)kHeadsPerCta * QM * P * sizeof(T) + QM * sizeof(float) +
-         (size_t)kHeadsPerCta * (P + QM) * sizeof(float);
+         (size_t)kHeadsPerCta * (P + QM * P) * sizeof(float);
 }
 
 // Streams one head's state: lane j of row d reads elements [4j, 4j+4), 8 rows per block, two
@@ -62,45 +62,57 @@ __device__ __forceinline__ void stream_state(const HT* __restrict__ Hsrc, typena
   __syncwarp();
 }
 
-// The same stream for a step that fills the chunk: each row is also folded with the chunk state,
-// H'[d] = exp(Acum_last) H[d] + sum_s (w_s x_s[d]) B_s (chunk_state / fold_state order; weights
-// sw[s] in shared memory), and written to Hd and, if present, the bf16 copy Rd.  Rows go 8 at a
-// time so that 32 independent accumulation chains hide the FMA latency.
+// The same stream for a step that fills the chunk: each row is also folded with the chunk state and
+// written back, in chunk_state / fold_state order,
+//   H'[d][n] = fma(decay, H[d][n], acc),  acc = fma(wx[s][d], B_s[n], acc) over s = 0..p,
+// where wx[s][d] = w_s x_s[d] is a per-warp shared-memory table.  Rows are read (coherently: this
+// loop writes the rows it has consumed) 8 at a time with the next 8 in flight, and each 4 rows'
+// fold accumulates over the chunk with 16 independent chains.
 template <typename T, int P, int N>
-__device__ __noinline__ void stream_state_refresh(const float* __restrict__ Hsrc, const float (&c)[4], float* yo,
-                                                  int j, int p, const float* sw, float decay, const T* sB,
-                                                  const T* sx, float* Hd, __nv_bfloat16* Rd) {
+__device__ __noinline__ void stream_state_refresh(float* __restrict__ Hd, __nv_bfloat16* __restrict__ Rd, float c0,
+                                                  float c1, float c2, float c3, float* yo, int j, int p,
+                                                  const float* wx, float decay, const T* sB) {
+  constexpr int NBLK = P / 8;
+  const float c[4] = {c0, c1, c2, c3};
+  float4 cur[8], nxt[8];
+#pragma unroll
+  for (int r = 0; r < 8; ++r) cur[r] = __ldcs(reinterpret_cast<const float4*>(Hd + (size_t)r * N + 4 * j));
+  float part[16];
 #pragma unroll 1
-  for (int d0 = 0; d0 < P; d0 += 16) {
-    float part[16];
+  for (int blk = 0; blk < NBLK; ++blk) {
+    if (blk + 1 < NBLK) {
 #pragma unroll
-    for (int half = 0; half < 2; ++half) {
-      const int db = d0 + 8 * half;
-      float h[8][4], acc[8][4];
+      for (int r = 0; r < 8; ++r)
+        nxt[r] = __ldcs(reinterpret_cast<const float4*>(Hd + (size_t)((blk + 1) * 8 + r) * N + 4 * j));
+    }
+    float pb[8];
 #pragma unroll
-      for (int r = 0; r < 8; ++r) {
-        Quad<float>::unpack(__ldcs(reinterpret_cast<const float4*>(Hsrc + (size_t)(db + r) * N + 4 * j)), h[r]);
+    for (int hf = 0; hf < 2; ++hf) {
+      float acc[4][4];
+#pragma unroll
+      for (int r = 0; r < 4; ++r)
 #pragma unroll
         for (int e = 0; e < 4; ++e) acc[r][e] = 0.f;
-      }
       for (int s = 0; s <= p; ++s) {
         float bs[4];
         lds4(sB + s * N + 4 * j, bs);
-        const float ws = sw[s];
+        const float4 wv = *reinterpret_cast<const float4*>(wx + s * P + blk * 8 + 4 * hf);
+        const float wr[4] = {wv.x, wv.y, wv.z, wv.w};
 #pragma unroll
-        for (int r = 0; r < 8; ++r) {
-          const float wx = __fmul_rn(ws, to_f(sx[s * P + db + r]));
+        for (int r = 0; r < 4; ++r)
 #pragma unroll
-          for (int e = 0; e < 4; ++e) acc[r][e] = __fmaf_rn(wx, bs[e], acc[r][e]);
-        }
+          for (int e = 0; e < 4; ++e) acc[r][e] = __fmaf_rn(wr[r], bs[e], acc[r][e]);
       }
 #pragma unroll
-      for (int r = 0; r < 8; ++r) {
-        part[8 * half + r] = Dot<N>::partial(c, h[r]);
+      for (int r4 = 0; r4 < 4; ++r4) {
+        const int r = 4 * hf + r4;
+        float h[4];
+        Quad<float>::unpack(cur[r], h);
+        pb[r] = Dot<N>::partial(c, h);
         float v[4];
 #pragma unroll
-        for (int e = 0; e < 4; ++e) v[e] = __fmaf_rn(decay, h[r][e], acc[r][e]);
-        const size_t o = (size_t)(db + r) * N + 4 * j;
+        for (int e = 0; e < 4; ++e) v[e] = __fmaf_rn(decay, h[e], acc[r4][e]);
+        const size_t o = (size_t)(blk * 8 + r) * N + 4 * j;
         *reinterpret_cast<float4*>(Hd + o) = make_float4(v[0], v[1], v[2], v[3]);
         if (Rd != nullptr) {
           __nv_bfloat162 lo2 = __floats2bfloat162_rn(v[0], v[1]), hi2 = __floats2bfloat162_rn(v[2], v[3]);
@@ -111,8 +123,17 @@ __device__ __noinline__ void stream_state_refresh(const float* __restrict__ Hsrc
         }
       }
     }
-    const float v = reduce_scatter16(part, j);
-    if ((j & 1) == 0) yo[d0 + (j >> 1)] = v;
+    if ((blk & 1) == 0) {
+#pragma unroll
+      for (int r = 0; r < 8; ++r) part[r] = pb[r];
+    } else {
+#pragma unroll
+      for (int r = 0; r < 8; ++r) part[8 + r] = pb[r];
+      const float v = reduce_scatter16(part, j);
+      if ((j & 1) == 0) yo[(blk - 1) * 8 + (j >> 1)] = v;
+    }
+#pragma unroll
+    for (int r = 0; r < 8; ++r) cur[r] = nxt[r];
   }
   __syncwarp();
 }
@@ -126,7 +147,7 @@ __global__ void __launch_bounds__(kThreads, 2) k_decode_heads(LaunchArgs a) {
   T* sxa = sB + QM * N;                                               // [warp][QM][P] x rows 0..p
   float* sg = reinterpret_cast<float*>(sxa + kHeadsPerCta * QM * P);  // [QM] Gram row
   float* syo = sg + QM;                                               // [warp][P] off-diagonal terms
-  float* swa = syo + kHeadsPerCta * P;                                // [warp][QM] chunk-state weights
+  float* swa = syo + kHeadsPerCta * P;                                // [warp][QM][P] w_s x_s[d] (refresh)
   const int tid = threadIdx.x, w = tid >> 5, j = tid & 31;
   const int i = blockIdx.y;
   const int hpg = a.H / a.G, nbl = (hpg + kHeadsPerCta - 1) / kHeadsPerCta;
@@ -172,42 +193,42 @@ __global__ void __launch_bounds__(kThreads, 2) k_decode_heads(LaunchArgs a) {
                  reinterpret_cast<const char*>(s < p ? bx + s * HP : nx) + 16 * e);
     }
   const float dt_raw = j <= p ? (j < p ? a.bdt[((size_t)slot * a.Q + j) * a.H + h] : a.dt[(size_t)i * a.H + h]) : 0.f;
-  const float Ah = a.A[h], bias = a.dt_bias[h];
-  float* yo = syo + w * P;
-  if (!refresh && active)
-    stream_state<HT, P, N>(Hsrc, q, c, yo, j);
   float dl = 0.f;
   df v = {0.f, 0.f};
   if (j <= p) {
-    dl = delta_of(dt_raw, bias);
-    v.hi = __fmul_rn(dl, Ah);
+    dl = delta_of(dt_raw, a.dt_bias[h]);
+    v.hi = __fmul_rn(dl, a.A[h]);
   }
+  // this head's log-decay prefix (lane s holds row s) and the group's Gram row, while the first
+  // state rows are in flight
+  v = warp_scan_df(v, j);
+  const df at = {__shfl_sync(kFull, v.hi, p), __shfl_sync(kFull, v.lo, p)};
   cp_async_wait_all();
   __syncthreads();
-  // the group's Gram row, split over the warps
   for (int s = w; s <= p; s += kHeadsPerCta) {
     float bs[4];
     lds4(sB + s * N + 4 * j, bs);
     const float gv = Dot<N>::reduce(Dot<N>::partial(c, bs));
     if (j == 0) sg[s] = gv;
   }
-  // this head's log-decay prefix (lane s holds row s)
-#pragma unroll
-  for (int st = 1; st < 32; st <<= 1) {
-    const float ph = __shfl_up_sync(kFull, v.hi, st), pl = __shfl_up_sync(kFull, v.lo, st);
-    if (j >= st) v = df_add(df{ph, pl}, v);
-  }
-  const df at = {__shfl_sync(kFull, v.hi, p), __shfl_sync(kFull, v.lo, p)};
   __syncthreads();
   if (!active) return;
   float M = 0.f;
   if (j <= p) M = __fmul_rn(__fmul_rn(sg[j], dl), expf(df_diff(at, v)));
+  float* yo = syo + w * P;
   if (refresh) {
-    float* sw = swa + w * QM;
-    if (j <= p) sw[j] = __fmul_rn(dl, expf(df_diff(at, v)));
+    float* wx = swa + w * QM * P;
+    const float wl = j <= p ? __fmul_rn(dl, expf(df_diff(at, v))) : 0.f;   // state_weights
+    for (int s = 0; s <= p; ++s) {                                          // chunk_state's w_s x_s[d]
+      const float ws = __shfl_sync(kFull, wl, s);
+#pragma unroll
+      for (int m = 0; m < P / 32; ++m) wx[s * P + 32 * m + j] = __fmul_rn(ws, to_f(sx[s * P + 32 * m + j]));
+    }
     __syncwarp();
     __nv_bfloat16* Rd = a.read_copy ? (__nv_bfloat16*)a.read_copy + soff : nullptr;
-    stream_state_refresh<T, P, N>(a.state + soff, c, yo, j, p, sw, expf(at.hi), sB, sx, a.state + soff, Rd);
+    stream_state_refresh<T, P, N>(a.state + soff, Rd, c[0], c[1], c[2], c[3], yo, j, p, wx, expf(at.hi), sB);
+  } else {
+    stream_state<HT, P, N>(Hsrc, q, c, yo, j);
   }
   // outputs d = 32k + j
   const float et = expf(at.hi), Dh = a.D[h];

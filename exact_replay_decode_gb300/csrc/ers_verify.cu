@@ -115,16 +115,6 @@ __device__ __noinline__ void stream_anchor_flush(float* __restrict__ Hd, __nv_bf
   __syncwarp();
 }
 
-// Inclusive double-float prefix over lanes (lane s holds row s), the warp form of chunk_scan.
-__device__ __forceinline__ df warp_scan(df v, int j) {
-#pragma unroll
-  for (int st = 1; st < 32; st <<= 1) {
-    const float ph = __shfl_up_sync(kFull, v.hi, st), pl = __shfl_up_sync(kFull, v.lo, st);
-    if (j >= st) v = df_add(df{ph, pl}, v);
-  }
-  return v;
-}
-
 template <typename T, int P, int N, int QM>
 __global__ void __launch_bounds__(kThreads, 2) k_verify_heads(LaunchArgs a) {
   static_assert(N == 128 && P % 8 == 0 && QM <= 32 - kDraftsMax, "lane split of Dot<128>; one warp scans");
@@ -206,7 +196,7 @@ __global__ void __launch_bounds__(kThreads, 2) k_verify_heads(LaunchArgs a) {
     dl = delta_of(j < h0 ? dt_c : dt_o_d, bias);
     v.hi = __fmul_rn(dl, Ah);
   }
-  v = warp_scan(v, j);
+  v = warp_scan_df(v, j);
   cp_async_wait_all();
   __syncthreads();
   // Gram rows of the drafts: G[k][s] = C_{h0+k} . B_s for s <= h0 + k
@@ -227,7 +217,7 @@ __global__ void __launch_bounds__(kThreads, 2) k_verify_heads(LaunchArgs a) {
       dc = delta_of(dt_c, bias);
       vc.hi = __fmul_rn(dc, Ah);
     }
-    vc = warp_scan(vc, j);
+    vc = warp_scan_df(vc, j);
     const df last = {__shfl_sync(kFull, vc.hi, hc - 1), __shfl_sync(kFull, vc.lo, hc - 1)};
     const float wl = j < hc ? __fmul_rn(dc, expf(df_diff(last, vc))) : 0.f;   // state_weights
     decay = expf(last.hi);

@@ -95,6 +95,18 @@ using tc::cp_async16;
 using tc::cp_async_wait_all;
 
 
+// Inclusive double-float prefix over the lanes (lane s holds row s): the warp form of chunk_scan.
+// For rows < 32 the strides >= 32 of chunk_scan leave every value unchanged, so the bits are
+// chunk_scan's.
+__device__ __forceinline__ df warp_scan_df(df v, int j) {
+#pragma unroll
+  for (int st = 1; st < 32; st <<= 1) {
+    const float ph = __shfl_up_sync(kFull, v.hi, st), pl = __shfl_up_sync(kFull, v.lo, st);
+    if (j >= st) v = df_add(df{ph, pl}, v);
+  }
+  return v;
+}
+
 template <typename K>
 cudaError_t prep(K kernel, size_t smem) {
   return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
