@@ -217,7 +217,7 @@ class DecodeBench:
         self.tok = torch_io.tokens_to(stream, dev, lead=(TOKEN_RING, self.S))
         self.y = torch.empty(self.S, d.nheads, d.headdim, dtype=torch.bfloat16, device=dev)
         self.status = ers.Status(dev)
-        self.launches_per_step = 2   # group decode kernel + position advance
+        self.launches_per_step = 1   # k_decode_heads (advances the positions itself)
 
     def step(self, k: int):
         x, dt, B, C = (t[k % TOKEN_RING] for t in self.tok)
@@ -572,6 +572,7 @@ def main(argv=None):
     ach = DECODE_BYTES_PER_SEQ_STEP * S / (ms_step * 1e-3) / 1e9
     e2e_ms, h2d, d2h = time_decode_e2e(dev, args.steps, args.warmup, seed=2000 + rank, batch=args.batch)
     e2e_ms = max_over_ranks(e2e_ms, dev)
+    launches_per_step = b.launches_per_step
     del b
     torch.cuda.empty_cache()
 
@@ -599,11 +600,11 @@ def main(argv=None):
                    "l2": "inputs larger than L2 (512 MiB fp32 checkpoints per step)"},
         "roofline": {"bound": "hbm", "achieved": ach, "peak": hbm, "unit": "GB/s", "frac": ach / hbm,
                      "traffic": profiled_traffic(), "peak_kind": f"{peak_kind} copy bandwidth (burst)",
-                     "kernel": "k_decode_heads + k_setpos (one replay-decode step; time is the whole step)",
+                     "kernel": "k_decode_heads (one replay-decode step; time is the whole step)",
                      "algorithmic_bytes_per_launch": DECODE_BYTES_PER_SEQ_STEP * S},
         "e2e": {"value": S * args.steps * ws / (e2e_ms * 1e-3), "unit": "seq-steps/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
-        "gpu_launches": b_launches(args.steps),
+        "gpu_launches": launches_per_step * args.steps,
         "clocks": clocks,
     }
     line.update(extra)
@@ -616,9 +617,6 @@ def main(argv=None):
         dist.destroy_process_group()
     return 0
 
-
-def b_launches(steps: int) -> int:
-    return 2 * steps
 
 
 if __name__ == "__main__":

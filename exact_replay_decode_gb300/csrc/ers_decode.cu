@@ -138,6 +138,20 @@ __device__ __noinline__ void stream_state_refresh(float* __restrict__ Hd, __nv_b
   __syncwarp();
 }
 
+// Position advance inside the decode launch.  Every CTA of a slot adds 1 << 16 to pos[slot] once
+// all of its threads have read the position (the low 16 bits); the CTA that completes the count
+// (ncta CTAs per slot) stores the new position, which also clears the count.  No CTA of the slot can
+// read pos after that store, and pos holds a plain position again when the launch ends.  A position
+// outside [0, Q) reads as out of range in every CTA of the slot, so none counts and it is left as
+// it was (reported as ERS_EALIGN).
+constexpr int kPosBits = 16;
+constexpr int32_t kPosMask = (1 << kPosBits) - 1;
+
+__device__ __forceinline__ void advance_pos(int32_t* pos, int ncta, int32_t newp) {
+  const int32_t old = atomicAdd(pos, 1 << kPosBits);
+  if ((old >> kPosBits) == ncta - 1) atomicExch(pos, newp);
+}
+
 template <typename T, typename HT, int P, int N, int QM>
 __global__ void __launch_bounds__(kThreads, 2) k_decode_heads(LaunchArgs a) {
   static_assert(N == 128 && P % 32 == 0, "lane split of Dot<128>; 32-row reduction blocks");
@@ -161,7 +175,8 @@ __global__ void __launch_bounds__(kThreads, 2) k_decode_heads(LaunchArgs a) {
   const size_t HP = (size_t)a.H * P, GN = (size_t)a.G * N;
   const size_t soff = ((size_t)slot * a.H + h) * P * N;
   const HT* Hsrc = rssm ? (const HT*)((const __nv_bfloat16*)a.read_copy + soff) : (const HT*)(a.state + soff);
-  const int p = a.pos[slot];
+  const int p = a.pos[slot] & kPosMask;
+  const int ncta = a.G * nbl;   // CTAs that read this slot's position
   float c[4];
   load_k<T, 4>((const T*)a.C + (size_t)i * GN + (size_t)g * N + 4 * j, c);
   typename Quad<HT>::raw q[16];
@@ -169,7 +184,7 @@ __global__ void __launch_bounds__(kThreads, 2) k_decode_heads(LaunchArgs a) {
 #pragma unroll
     for (int r = 0; r < 16; ++r) q[r] = Quad<HT>::ld_stream(Hsrc + (size_t)r * N + 4 * j);
   }
-  if (p < 0 || p >= a.Q) {
+  if (p >= a.Q) {   // the same for every CTA of the slot: none of them counts, pos stays as it is
     if (tid == 0) report(a.status, ERS_EALIGN);
     return;
   }
@@ -205,6 +220,7 @@ __global__ void __launch_bounds__(kThreads, 2) k_decode_heads(LaunchArgs a) {
   const df at = {__shfl_sync(kFull, v.hi, p), __shfl_sync(kFull, v.lo, p)};
   cp_async_wait_all();
   __syncthreads();
+  if (tid == 0) advance_pos(&a.pos[slot], ncta, refresh ? 0 : p + 1);
   for (int s = w; s <= p; s += kHeadsPerCta) {
     float bs[4];
     lds4(sB + s * N + 4 * j, bs);
@@ -266,7 +282,7 @@ cudaError_t launch_decode_heads(const LaunchArgs& a, cudaStream_t s) {
     if ((e = prep(k_decode_heads<T, float, P, N, QM>, sm)) != cudaSuccess) return e;
     k_decode_heads<T, float, P, N, QM><<<grid, kThreads, sm, s>>>(a);
   }
-  return launch_setpos(a, 0, s);
+  return cudaGetLastError();   // the kernel advances the positions itself
 }
 
 }  // namespace
