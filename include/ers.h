@@ -177,6 +177,9 @@ ERS_API ers_status ers_chunked_prefill(const ers_dims* dims, const ers_params* p
  *   identical bits.
  * ReplaySSM mode (ERS_FLAG_REPLAYSSM): requires 0 <= pos < L and a read copy; outputs read the read
  *   copy; no refresh happens here (ers_refresh applies the flush rule).
+ * pos advances by one per call (or returns to 0 on a fused refresh); while the call runs, the
+ * upper 16 bits of a slot's pos entry may hold a count of the kernel's own, cleared before it ends,
+ * so no other work may read or write pos concurrently with the call.
  * Device errors: ERS_EALIGN (pos out of range), ERS_ESLOT. */
 ERS_API ers_status ers_replay_decode(const ers_dims* dims, const ers_params* prm, const ers_cache* cache, int32_t nseq,
                              const int32_t* slot, const void* x, const float* dt, const void* B, const void* C,
