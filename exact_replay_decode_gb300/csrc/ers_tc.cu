@@ -346,28 +346,30 @@ __global__ void __launch_bounds__(kStateWarps * 32, 2) k_tc_prefill_state(Launch
   teardown_tmem(64);
 }
 
-// ---- prefill: outputs, one CTA per (chunk, t-tile, sequence, head) ---------------------------------
+// ---- prefill: outputs, one CTA per (chunk, sequence, head), all t-tiles of the chunk ----------------
 constexpr int kOutWarps = 16;   // the output kernel's M tiles and epilogue are latency-bound: 16 warps
 
+// The token X and B tiles (all rows the chunk's last t-tile needs) and the decays are loaded once;
+// each t-tile then loads its query tile C and the start-state tile (its M tiles overwrite both) and
+// runs tc_outputs.  The B operand of every tile is read from the same full-height B tile, which
+// gives the MMAs the same operand values as a tile-sized one.
 template <bool CHUNKED>
 __global__ void __launch_bounds__(kOutWarps * 32, 1) k_tc_prefill_out(LaunchArgs a, int ntiles, uint32_t tcols) {
-  // the later (longer) t-tiles of every chunk are scheduled first: z = (ntiles - 1 - tau) * H + h
-  const int c = blockIdx.x, i = blockIdx.y, tau = ntiles - 1 - (int)blockIdx.z / a.H, h = blockIdx.z % a.H;
+  const int c = blockIdx.x, i = blockIdx.y, h = blockIdx.z;
   SeqGrid sg;
   if (!seq_grid(a, CHUNKED, i, &sg) || c >= sg.nch) return;
-  const Geom ge = geom(a.Q, tau);
   const int nrows = min(a.Q, sg.total - c * a.Q);
   const int nbuf = max(0, sg.p - c * a.Q);
-  const int out_lo = max(nbuf, ge.t0), out_hi = min(nrows, ge.t0 + ge.TT);
-  if (out_lo >= out_hi) return;
+  if (nbuf >= nrows) return;   // no new token in this chunk
   const long long tok0 = (long long)a.cu[i] + (long long)c * a.Q - sg.p;
   const Rows<bf16> rows = make_rows<bf16>(a, sg.slot, h, nbuf, tok0);
   setup_tmem(tcols);
-  const Arena ar = arena(ge.S_ext);
-  {  // the chunk's decays (written by the chunk-state kernel) and its start state, already split
-     // into the [H_hi; H_lo] operand tile by the inter-chunk chain
+  const int S_max = geom(a.Q, ntiles - 1).S_ext;
+  const Arena ar = arena(S_max);
+  const size_t unit = ((size_t)i * a.max_chunks + c) * a.H + h;
+  const uint8_t* htile = reinterpret_cast<const uint8_t*>(a.ws_states + unit * P * N);
+  {  // the chunk's decays, written by the chunk-state kernel
     TcHdr& hd = hdr();
-    const size_t unit = ((size_t)i * a.max_chunks + c) * a.H + h;
     const float* wd = a.ws_decay + unit * 3 * a.Q;
     const int q4 = a.Q / 4;
     for (int k = threadIdx.x; k < 3 * q4; k += blockDim.x) {
@@ -375,14 +377,29 @@ __global__ void __launch_bounds__(kOutWarps * 32, 1) k_tc_prefill_out(LaunchArgs
       float* dst = part == 0 ? hd.delta : (part == 1 ? hd.ahi : hd.alo);
       cp_async16(dst + 4 * e, wd + part * a.Q + 4 * e);
     }
-    const uint8_t* tile = reinterpret_cast<const uint8_t*>(a.ws_states + unit * P * N);
-    for (int k = threadIdx.x; k < (int)(kHTile / 16); k += blockDim.x) cp_async16(ar.Hs + 16 * k, tile + 16 * k);
   }
-  load_xb(rows, min(nrows, ge.S_ext), ar);
-  load_c(rows, ge.t0, ge.t0, min(nrows, ge.t0 + ge.TT), ar);
-  publish();
-  bf16* ybase = (bf16*)a.y + ((tok0 + out_lo) * a.H + h) * P;
-  tc_outputs<kOutWarps>(ar, a.Q, tau, nrows, out_lo, out_hi, a.D[h], ybase, (long long)a.H * P, a.status);
+  load_xb(rows, min(nrows, S_max), ar);
+  bool first = true;
+  for (int tau = 0; tau < ntiles; ++tau) {
+    const Geom ge = geom(a.Q, tau);
+    const int out_lo = max(nbuf, ge.t0), out_hi = min(nrows, ge.t0 + ge.TT);
+    if (out_lo >= out_hi) continue;
+    if (!first) {   // fresh barrier phases for this tile's MMAs
+      __syncthreads();
+      if (threadIdx.x == 0) {
+        mbar_init(&hdr().bar, 1);
+        fence_mbar_init();
+      }
+    }
+    first = false;
+    // the start state, already split into the [H_hi; H_lo] operand tile by the inter-chunk chain
+    for (int k = threadIdx.x; k < (int)(kHTile / 16); k += blockDim.x) cp_async16(ar.Hs + 16 * k, htile + 16 * k);
+    load_c(rows, ge.t0, ge.t0, min(nrows, ge.t0 + ge.TT), ar);
+    publish();
+    bf16* ybase = (bf16*)a.y + ((tok0 + out_lo) * a.H + h) * P;
+    if (!tc_outputs<kOutWarps>(ar, a.Q, tau, nrows, out_lo, out_hi, a.D[h], ybase, (long long)a.H * P, a.status))
+      break;
+  }
   teardown_tmem(tcols);
 }
 
@@ -569,13 +586,13 @@ cudaError_t tc_prefill(const LaunchArgs& a, Op op, cudaStream_t s) {
       if ((e = set_smem(k_tc_prefill_out<true>, so)) != cudaSuccess) return e;
       k_tc_prefill_state<true><<<dim3(a.max_chunks, a.nseq, a.H), kStateWarps * 32, ss, s>>>(a);
       if ((e = launch_chain(b, true, s)) != cudaSuccess) return e;
-      k_tc_prefill_out<true><<<dim3(a.max_chunks, a.nseq, a.H * ntiles), kOutWarps * 32, so, s>>>(a, ntiles, tcols);
+      k_tc_prefill_out<true><<<dim3(a.max_chunks, a.nseq, a.H), kOutWarps * 32, so, s>>>(a, ntiles, tcols);
     } else {
       if ((e = set_smem(k_tc_prefill_state<false>, ss)) != cudaSuccess) return e;
       if ((e = set_smem(k_tc_prefill_out<false>, so)) != cudaSuccess) return e;
       k_tc_prefill_state<false><<<dim3(a.max_chunks, a.nseq, a.H), kStateWarps * 32, ss, s>>>(a);
       if ((e = launch_chain(b, false, s)) != cudaSuccess) return e;
-      k_tc_prefill_out<false><<<dim3(a.max_chunks, a.nseq, a.H * ntiles), kOutWarps * 32, so, s>>>(a, ntiles, tcols);
+      k_tc_prefill_out<false><<<dim3(a.max_chunks, a.nseq, a.H), kOutWarps * 32, so, s>>>(a, ntiles, tcols);
     }
   }
   if (chunked) return launch_tail(a, s);
