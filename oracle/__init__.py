@@ -125,6 +125,38 @@ def bf16_round(a: np.ndarray) -> np.ndarray:
     return r.view(np.float32).astype(np.float64)
 
 
+E4M3_MAX = 448.0
+
+
+def e4m3_round(a: np.ndarray) -> np.ndarray:
+    """Round fp32 values to the nearest FP8 e4m3 value (1 sign, 4 exponent bits with bias 7, 3
+    mantissa bits, subnormals below 2^-6, no infinities), ties to even, magnitudes beyond 448
+    saturated to 448.  Returned as fp32 values."""
+    f = np.asarray(a, dtype=np.float32).astype(np.float64)
+    mag = np.abs(f)
+    _, e = np.frexp(mag)                          # mag = m * 2**e, m in [0.5, 1): floor(log2 mag) = e - 1
+    ex = np.maximum(e - 1, -6)                    # subnormals share the quantum of the smallest binade
+    quantum = np.ldexp(1.0, ex - 3)
+    r = np.round(mag / quantum) * quantum         # numpy rounds halves to even
+    r = np.minimum(r, E4M3_MAX)
+    r = np.where(mag == 0, 0.0, r)
+    return (np.sign(f) * r).astype(np.float32)
+
+
+def fp8_rows_round(a: np.ndarray) -> np.ndarray:
+    """FP8 read copy of an fp32 state with one scale per row (the last axis is dstate):
+    scale = amax(|row|) / 448, q = e4m3(v / scale), read back as q * scale, all fp32 operations
+    (a zero row reads as zeros).  Input values are taken through fp32 as the GPU anchor is stored
+    in fp32; returned as fp64."""
+    f = np.ascontiguousarray(a, dtype=np.float32)
+    amax = np.max(np.abs(f), axis=-1, keepdims=True)
+    scale = (amax / np.float32(E4M3_MAX)).astype(np.float32)
+    with np.errstate(divide="ignore", invalid="ignore"):
+        y = np.where(scale > 0, f / np.where(scale > 0, scale, np.float32(1)), np.float32(0)).astype(np.float32)
+    q = e4m3_round(y)
+    return (q * scale).astype(np.float32).astype(np.float64)
+
+
 class _Seq:
     __slots__ = ("x", "dt", "B", "C")
 

@@ -334,3 +334,68 @@ def test_bf16_round_matches_synth_rounding():
     # ties go to even: 1 + 2^-8 lies halfway between bf16 neighbours 1 and 1 + 2^-7
     assert oracle.bf16_round(np.array([1.0 + 2.0 ** -8], np.float32))[0] == 1.0
     assert oracle.bf16_round(np.array([1.0 + 3 * 2.0 ** -8], np.float32))[0] == 1.0 + 2.0 ** -6
+
+
+def _e4m3_table():
+    """Every finite e4m3 value, decoded from the bit fields by the format's definition."""
+    vals = []
+    for code in range(256):
+        sgn, ex, man = code >> 7, (code >> 3) & 0xF, code & 7
+        if ex == 0xF and man == 7:
+            continue                                   # the NaN codes
+        v = (man / 8.0) * 2.0 ** -6 if ex == 0 else (1 + man / 8.0) * 2.0 ** (ex - 7)
+        vals.append((-v if sgn else v, code))
+    return vals
+
+
+def test_e4m3_round_fixes_every_code_and_saturates():
+    table = _e4m3_table()
+    v = np.array([t[0] for t in table], dtype=np.float32)
+    assert np.array_equal(oracle.e4m3_round(v), v)
+    assert max(abs(t[0]) for t in table) == 448.0 and min(abs(t[0]) for t in table if t[0] != 0) == 2.0 ** -9
+    assert np.array_equal(oracle.e4m3_round(np.array([1e6, -500.0, 449.0], np.float32)), np.array([448, -448, 448], np.float32))
+
+
+def test_e4m3_round_matches_brute_force_nearest_even():
+    table = [t for t in _e4m3_table() if t[0] >= 0]
+    vals = np.array([t[0] for t in table])
+    codes = np.array([t[1] for t in table])
+    rng = np.random.Generator(np.random.PCG64(8))
+    x = np.concatenate([rng.uniform(0, 448, 3000), 2.0 ** rng.uniform(-12, 9, 3000),
+                        (vals[:-1] + vals[1:]) / 2])          # exact midpoints exercise the ties
+    x = x.astype(np.float32).astype(np.float64)
+    got = oracle.e4m3_round(x.astype(np.float32)).astype(np.float64)
+    for xi, gi in zip(x, got):
+        d = np.abs(vals - xi)
+        best = np.nonzero(d == d.min())[0]
+        want = vals[best[np.argmin(codes[best] & 1)]] if len(best) > 1 else vals[best[0]]   # tie: even code
+        assert gi == want, (xi, gi, want)
+    assert np.array_equal(oracle.e4m3_round(-x.astype(np.float32)), -oracle.e4m3_round(x.astype(np.float32)))
+
+
+def test_fp8_rows_round_scales_each_row_to_its_max():
+    rng = np.random.Generator(np.random.PCG64(9))
+    a = rng.standard_normal((3, 4, 16, 128)) * np.exp(rng.uniform(-8, 8, (3, 4, 16, 1)))
+    a[0, 0, 0] = 0.0                                          # an all-zero row reads as zeros
+    r = oracle.fp8_rows_round(a)
+    f = a.astype(np.float32).astype(np.float64)
+    amax = np.abs(f).max(axis=-1, keepdims=True)
+    assert np.all(r[0, 0, 0] == 0)
+    # e4m3 keeps 3 mantissa bits: error <= half a quantum of the row's scaled value, plus fp32 rounding
+    rel = np.abs(r - f) / np.where(amax > 0, amax, 1)
+    assert rel.max() <= 2.0 ** -4 * 1.001
+    # the row maximum is read back to within fp32 rounding of its value
+    i = np.argmax(np.abs(f), axis=-1)[..., None]
+    assert np.allclose(np.take_along_axis(r, i, -1), np.take_along_axis(f, i, -1), rtol=1e-6)
+
+
+def test_protocol_anchor_independent_of_fp8_read_copy():
+    """The fp32 anchor is the same whether outputs read a bf16 or an FP8 copy."""
+    params, anchor, drafts, acc, L = _protocol_case(17, steps=12)
+    m1 = oracle.ReplaySSMModel(params, anchor, L)
+    m2 = oracle.ReplaySSMModel(params, anchor, L, read_cast=oracle.fp8_rows_round)
+    for k in range(len(drafts)):
+        y1 = m1.verify(drafts[k]); m1.commit(acc[k])
+        y2 = m2.verify(drafts[k]); m2.commit(acc[k])
+    assert m1.flushes > 0 and np.array_equal(m1.anchor, m2.anchor)
+    assert not np.array_equal(y1, y2)
