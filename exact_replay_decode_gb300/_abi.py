@@ -24,6 +24,9 @@ FLAG_FUSE_REFRESH = 1
 FLAG_REPLAYSSM = 2
 FLAG_AUTO_FLUSH = 4
 
+READ_BF16 = 0
+READ_FP8_E4M3 = 1
+
 # Every function include/ers.h declares.
 EXPORTS = (
     "ers_status_str", "ers_version", "ers_ssd_scan_fwd_workspace_size", "ers_ssd_scan_fwd",
@@ -50,7 +53,8 @@ class Params(ctypes.Structure):
 class Cache(ctypes.Structure):
     _fields_ = [("state", ctypes.c_void_p), ("read_copy", ctypes.c_void_p), ("buf_x", ctypes.c_void_p),
                 ("buf_dt", ctypes.c_void_p), ("buf_B", ctypes.c_void_p), ("buf_C", ctypes.c_void_p),
-                ("pos", ctypes.c_void_p), ("nslots", ctypes.c_int32)]
+                ("pos", ctypes.c_void_p), ("nslots", ctypes.c_int32), ("read_dtype", ctypes.c_int32),
+                ("read_scale", ctypes.c_void_p)]
 
 
 _lib = None

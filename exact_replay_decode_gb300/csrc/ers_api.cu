@@ -42,10 +42,20 @@ ers_status check_params(const ers_params* p) {
   return ERS_OK;
 }
 
+ers_status check_state_ptrs(const ers_cache* c) { return check_ptr(c->state, true); }
+
+// FP8 read copies are implemented by the CUDA-core warp-per-head kernels only.
+bool fp8_read_shape(const ers_dims* d) {
+  return d->headdim == 64 && d->dstate == 128 && d->chunk >= 1 && d->chunk <= 16;
+}
+bool has_fp8_copy(const ers_cache* c) { return c->read_copy != nullptr && c->read_dtype == ERS_READ_FP8_E4M3; }
+
 ers_status check_cache(const ers_cache* c, bool need_read_copy) {
   if (c == nullptr || c->nslots < 0) return ERS_EINVAL;
-  ERS_TRY(check_ptr(c->state, true));
+  if (c->read_dtype != ERS_READ_BF16 && c->read_dtype != ERS_READ_FP8_E4M3) return ERS_EDTYPE;
+  ERS_TRY(check_state_ptrs(c));
   ERS_TRY(check_ptr(c->read_copy, need_read_copy));
+  if (c->read_dtype == ERS_READ_FP8_E4M3 && c->read_copy != nullptr) ERS_TRY(check_ptr(c->read_scale, true));
   ERS_TRY(check_ptr(c->buf_x, true));
   ERS_TRY(check_ptr(c->buf_dt, true));
   ERS_TRY(check_ptr(c->buf_B, true));
@@ -74,6 +84,8 @@ LaunchArgs base_args(const ers_dims* d, const ers_params* p) {
 void set_cache(LaunchArgs& a, const ers_cache* c) {
   a.state = c->state;
   a.read_copy = c->read_copy;
+  a.read_fp8 = c->read_copy != nullptr && c->read_dtype == ERS_READ_FP8_E4M3;
+  a.read_scale = c->read_scale;
   a.bx = c->buf_x;
   a.bdt = c->buf_dt;
   a.bB = c->buf_B;
@@ -236,6 +248,7 @@ ers_status ers_replay_decode(const ers_dims* dims, const ers_params* prm, const 
   ERS_TRY(check_tokens(x, dt, B, C, true));
   ERS_TRY(check_ptr(y, true));
   ERS_TRY(check_ptr(dev_status, false));
+  if (has_fp8_copy(cache) && !fp8_read_shape(dims)) return ERS_EUNSUPPORTED;
   LaunchArgs a = base_args(dims, prm);
   set_cache(a, cache);
   a.x = x; a.dt = dt; a.B = B; a.C = C;
@@ -260,6 +273,7 @@ ers_status ers_refresh(const ers_dims* dims, const ers_params* prm, const ers_ca
   if (slot == nullptr && nseq > cache->nslots) return ERS_EINVAL;
   ERS_TRY(check_ptr(slot, false));
   ERS_TRY(check_ptr(dev_status, false));
+  if (has_fp8_copy(cache) && !fp8_read_shape(dims)) return ERS_EUNSUPPORTED;
   LaunchArgs a = base_args(dims, prm);
   set_cache(a, cache);
   a.slot = slot;
@@ -285,6 +299,10 @@ ers_status ers_spec_verify(const ers_dims* dims, const ers_params* prm, const er
   ERS_TRY(check_tokens(x, dt, B, C, true));
   ERS_TRY(check_ptr(y, true));
   ERS_TRY(check_ptr(dev_status, false));
+  if (has_fp8_copy(cache) && !(fp8_read_shape(dims) && ers::heads_verify_supported(dims->headdim, dims->dstate,
+                                                                                       dims->chunk, T, dims->nheads,
+                                                                                       dims->ngroups)))
+    return ERS_EUNSUPPORTED;
   LaunchArgs a = base_args(dims, prm);
   set_cache(a, cache);
   a.x = x; a.dt = dt; a.B = B; a.C = C;

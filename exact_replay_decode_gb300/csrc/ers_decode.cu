@@ -6,6 +6,8 @@
 // streaming the checkpoint from HBM.  The arithmetic is the engine's, operation for operation
 // (row_output, state_weights, chunk_state, fold_state in ers_fma.cu; Dot<128> and chunk_scan in
 // ers_common.cuh), so decode equals single-shot and chunked prefill bit for bit.
+#include <type_traits>
+
 #include "ers_common.cuh"
 #include "ers_internal.h"
 #include "warp_heads.cuh"
@@ -38,9 +40,18 @@ constexpr size_t heads_smem_bytes() {
 // Streams one head's state: lane j of row d reads elements [4j, 4j+4), 8 rows per block, two
 // blocks in flight (q holds rows 0..15 on entry).  yo[d] ends with the off-diagonal term (H C_p)[d]
 // (per-warp shared memory).
+template <typename HT>
+__device__ __forceinline__ void unpack_row(typename Quad<HT>::raw r, const float (&sc)[2], int d, float (&h)[4]) {
+  if constexpr (std::is_same<HT, uint8_t>::value) {
+    fp8_dequant(r, __shfl_sync(kFull, sc[d >> 5], d & 31), h);   // row scale held by lane d % 32
+  } else {
+    Quad<HT>::unpack(r, h);
+  }
+}
+
 template <typename HT, int P, int N>
 __device__ __forceinline__ void stream_state(const HT* __restrict__ Hsrc, typename Quad<HT>::raw (&q)[16],
-                                             const float (&c)[4], float* yo, int j) {
+                                             const float (&c)[4], float* yo, int j, const float (&sc)[2]) {
   constexpr int NBLK = P / 8;
   float part[16];
 #pragma unroll
@@ -50,7 +61,7 @@ __device__ __forceinline__ void stream_state(const HT* __restrict__ Hsrc, typena
     for (int r = 0; r < 8; ++r) {
       const int d = blk * 8 + r;
       float h[4];
-      Quad<HT>::unpack(q[sl + r], h);
+      unpack_row<HT>(q[sl + r], sc, d, h);
       part[sl + r] = Dot<N>::partial(c, h);
       if (blk + 2 < NBLK) q[sl + r] = Quad<HT>::ld_stream(Hsrc + (size_t)(d + 16) * N + 4 * j);
     }
@@ -69,7 +80,8 @@ __device__ __forceinline__ void stream_state(const HT* __restrict__ Hsrc, typena
 // loop writes the rows it has consumed) 8 at a time with the next 8 in flight, and each 4 rows'
 // fold accumulates over the chunk with 16 independent chains.
 template <typename T, int P, int N>
-__device__ __noinline__ void stream_state_refresh(float* __restrict__ Hd, __nv_bfloat16* __restrict__ Rd, float c0,
+__device__ __noinline__ void stream_state_refresh(float* __restrict__ Hd, __nv_bfloat16* __restrict__ Rd,
+                                                  uint8_t* __restrict__ R8, float* __restrict__ Rs, float c0,
                                                   float c1, float c2, float c3, float* yo, int j, int p,
                                                   const float* wx, float decay, const T* sB) {
   constexpr int NBLK = P / 8;
@@ -121,6 +133,7 @@ __device__ __noinline__ void stream_state_refresh(float* __restrict__ Hd, __nv_b
           u.y = *reinterpret_cast<uint32_t*>(&hi2);
           *reinterpret_cast<uint2*>(Rd + o) = u;
         }
+        if (R8 != nullptr) fp8_store_row<N>(v, R8, Rs, blk * 8 + r, j);   // warp-uniform branch
       }
     }
     if ((blk & 1) == 0) {
@@ -152,7 +165,9 @@ __device__ __forceinline__ void advance_pos(int32_t* pos, int ncta, int32_t newp
   if ((old >> kPosBits) == ncta - 1) atomicExch(pos, newp);
 }
 
-template <typename T, typename HT, int P, int N, int QM>
+// HT: what the output stream reads (fp32 checkpoint, bf16 or FP8 read copy); W8: the read copy a
+// fused refresh writes is FP8 (else bf16, or none when read_copy is null).
+template <typename T, typename HT, bool W8, int P, int N, int QM>
 __global__ void __launch_bounds__(kThreads, 2) k_decode_heads(LaunchArgs a) {
   static_assert(N == 128 && P % 32 == 0, "lane split of Dot<128>; 32-row reduction blocks");
   static_assert(QM <= 32, "one warp scans the chunk");
@@ -174,7 +189,13 @@ __global__ void __launch_bounds__(kThreads, 2) k_decode_heads(LaunchArgs a) {
   const bool rssm = (a.flags & ERS_FLAG_REPLAYSSM) != 0;
   const size_t HP = (size_t)a.H * P, GN = (size_t)a.G * N;
   const size_t soff = ((size_t)slot * a.H + h) * P * N;
-  const HT* Hsrc = rssm ? (const HT*)((const __nv_bfloat16*)a.read_copy + soff) : (const HT*)(a.state + soff);
+  const HT* Hsrc = rssm ? (const HT*)a.read_copy + soff : (const HT*)(a.state + soff);
+  float sc[2] = {0.f, 0.f};   // FP8 read copy: scales of rows j and 32 + j
+  if constexpr (std::is_same<HT, uint8_t>::value) {
+    const float* Rs = a.read_scale + ((size_t)slot * a.H + h) * P;
+    sc[0] = Rs[j];
+    sc[1] = Rs[32 + j];
+  }
   const int p = a.pos[slot] & kPosMask;
   const int ncta = a.G * nbl;   // CTAs that read this slot's position
   float c[4];
@@ -241,10 +262,17 @@ __global__ void __launch_bounds__(kThreads, 2) k_decode_heads(LaunchArgs a) {
       for (int m = 0; m < P / 32; ++m) wx[s * P + 32 * m + j] = __fmul_rn(ws, to_f(sx[s * P + 32 * m + j]));
     }
     __syncwarp();
-    __nv_bfloat16* Rd = a.read_copy ? (__nv_bfloat16*)a.read_copy + soff : nullptr;
-    stream_state_refresh<T, P, N>(a.state + soff, Rd, c[0], c[1], c[2], c[3], yo, j, p, wx, expf(at.hi), sB);
+    if constexpr (W8) {   // the copy pointers are compile-time nulls in the other variants (fewer live registers)
+      stream_state_refresh<T, P, N>(a.state + soff, nullptr, (uint8_t*)a.read_copy + soff,
+                                    a.read_scale + ((size_t)slot * a.H + h) * P, c[0], c[1], c[2], c[3], yo, j, p,
+                                    wx, expf(at.hi), sB);
+    } else {
+      __nv_bfloat16* Rd = a.read_copy ? (__nv_bfloat16*)a.read_copy + soff : nullptr;
+      stream_state_refresh<T, P, N>(a.state + soff, Rd, nullptr, nullptr, c[0], c[1], c[2], c[3], yo, j, p, wx,
+                                    expf(at.hi), sB);
+    }
   } else {
-    stream_state<HT, P, N>(Hsrc, q, c, yo, j);
+    stream_state<HT, P, N>(Hsrc, q, c, yo, j, sc);
   }
   // outputs d = 32k + j
   const float et = expf(at.hi), Dh = a.D[h];
@@ -274,15 +302,47 @@ cudaError_t launch_decode_heads(const LaunchArgs& a, cudaStream_t s) {
   const int hpg = a.H / a.G, nbl = (hpg + kHeadsPerCta - 1) / kHeadsPerCta;
   const dim3 grid(a.G * nbl, a.nseq);
   constexpr size_t sm = heads_smem_bytes<T, P, N, QM>();
-  cudaError_t e;
-  if (a.flags & ERS_FLAG_REPLAYSSM) {
-    if ((e = prep(k_decode_heads<T, __nv_bfloat16, P, N, QM>, sm)) != cudaSuccess) return e;
-    k_decode_heads<T, __nv_bfloat16, P, N, QM><<<grid, kThreads, sm, s>>>(a);
-  } else {
-    if ((e = prep(k_decode_heads<T, float, P, N, QM>, sm)) != cudaSuccess) return e;
-    k_decode_heads<T, float, P, N, QM><<<grid, kThreads, sm, s>>>(a);
+  const bool rssm = (a.flags & ERS_FLAG_REPLAYSSM) != 0;
+  auto run = [&](auto kernel) {
+    cudaError_t e = prep(kernel, sm);
+    if (e != cudaSuccess) return e;
+    kernel<<<grid, kThreads, sm, s>>>(a);
+    return cudaGetLastError();   // the kernel advances the positions itself
+  };
+  if constexpr (QM <= 16) {   // FP8 read copies: chunk <= 16 only (checked by the API)
+    if (a.read_fp8)
+      return rssm ? run(k_decode_heads<T, uint8_t, true, P, N, QM>) : run(k_decode_heads<T, float, true, P, N, QM>);
   }
-  return cudaGetLastError();   // the kernel advances the positions itself
+  if (a.read_fp8) return cudaErrorNotSupported;
+  return rssm ? run(k_decode_heads<T, __nv_bfloat16, false, P, N, QM>) : run(k_decode_heads<T, float, false, P, N, QM>);
+}
+
+// ---- FP8 read-copy recast for ers_refresh -------------------------------------------------------------
+// After the refresh kernel has folded a slot's anchor (or left it unchanged for an empty history),
+// the slot's FP8 read copy is cast from the fp32 anchor as stored, i.e. from the same unrounded
+// values ("Core equations": both copies are cast independently from one state).  Same slot
+// predicate as the refresh kernel; runs before the position is reset.  Warp w casts rows
+// [8w, 8w + 8) of head blockIdx.y, one row per pass.
+template <int P, int N>
+__global__ void __launch_bounds__(kThreads) k_recast_fp8(LaunchArgs a) {
+  const int i = blockIdx.x, h = blockIdx.y;
+  const int slot = a.slot != nullptr ? a.slot[i] : i;
+  if (slot < 0 || slot >= a.nslots) return;   // reported by the refresh kernel
+  const int p = a.pos[slot];
+  if (p < 0 || p > a.Q) return;
+  const bool rssm = (a.flags & ERS_FLAG_REPLAYSSM) != 0;
+  if (!(rssm ? (p + a.T > a.Q) : (p == a.Q))) return;
+  const int w = threadIdx.x >> 5, j = threadIdx.x & 31;
+  const size_t soff = ((size_t)slot * a.H + h) * P * N;
+  uint8_t* R8 = (uint8_t*)a.read_copy + soff;
+  float* Rs = a.read_scale + ((size_t)slot * a.H + h) * P;
+#pragma unroll
+  for (int r = 0; r < P / kHeadsPerCta; ++r) {
+    const int d = (P / kHeadsPerCta) * w + r;
+    const float4 u = *reinterpret_cast<const float4*>(a.state + soff + (size_t)d * N + 4 * j);
+    const float v[4] = {u.x, u.y, u.z, u.w};
+    fp8_store_row<N>(v, R8, Rs, d, j);
+  }
 }
 
 }  // namespace
@@ -299,4 +359,12 @@ cudaError_t heads_decode(const LaunchArgs& a, cudaStream_t s) {
   return launch_decode_heads<float, P, N, 32>(a, s);
 }
 
+}  // namespace ers
+
+namespace ers {
+cudaError_t heads_recast_fp8(const LaunchArgs& a, cudaStream_t s) {
+  if (a.nseq <= 0) return cudaSuccess;
+  k_recast_fp8<64, 128><<<dim3(a.nseq, a.H), kThreads, 0, s>>>(a);
+  return cudaGetLastError();
+}
 }  // namespace ers

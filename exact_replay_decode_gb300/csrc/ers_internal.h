@@ -33,6 +33,8 @@ struct LaunchArgs {
   // cache
   float* state;
   void* read_copy;
+  int read_fp8;        // read copy is FP8 e4m3 with per-row scales (read_scale [nslots, H, P])
+  float* read_scale;
   void* bx;
   float* bdt;
   void* bB;
@@ -66,6 +68,8 @@ bool fma_supported(int P, int N);
 // warp-per-head replay decode of the CUDA-core engine (chunk <= 32, P = 64, N = 128), ers_decode.cu
 bool heads_decode_supported(int P, int N, int Q);
 cudaError_t heads_decode(const LaunchArgs& a, cudaStream_t s);
+// FP8 read-copy recast after a refresh (P = 64, N = 128), ers_decode.cu
+cudaError_t heads_recast_fp8(const LaunchArgs& a, cudaStream_t s);
 // warp-per-head speculative verify (chunk <= 16, P = 64, N = 128, T <= 4, H/G <= 8), ers_verify.cu
 bool heads_verify_supported(int P, int N, int Q, int T, int H, int G);
 cudaError_t heads_verify(const LaunchArgs& a, cudaStream_t s);

@@ -16,6 +16,8 @@
 // together (32 values, one shuffle each).  The flush and the outputs are one launch because each
 // warp reads only its own head's state and the CTA's own group rows, which it has staged in shared
 // memory before any draft is written into the buffer.
+#include <type_traits>
+
 #include "ers_common.cuh"
 #include "ers_internal.h"
 #include "warp_heads.cuh"
@@ -40,10 +42,11 @@ constexpr size_t verify_smem_bytes() {
 
 // Read-copy stream: yo[k * P + d] = Dot<128>(C of draft k, R[d]) for all rows d.  q holds rows
 // [0, kVerifyRowsInFlight) on entry.
-template <int P, int N>
-__device__ __forceinline__ void stream_read_copy(const __nv_bfloat16* __restrict__ R,
-                                                 Quad<__nv_bfloat16>::raw (&q)[kVerifyRowsInFlight],
-                                                 const float (&c)[kDraftsMax][4], float* yo, int j) {
+template <typename HT, int P, int N>
+__device__ __forceinline__ void stream_read_copy(const HT* __restrict__ R,
+                                                 typename Quad<HT>::raw (&q)[kVerifyRowsInFlight],
+                                                 const float (&c)[kDraftsMax][4], float* yo, int j,
+                                                 const float (&sc)[2]) {
   constexpr int NBLK = P / 8, QB = kVerifyRowsInFlight / 8;
 #pragma unroll
   for (int blk = 0; blk < NBLK; ++blk) {
@@ -52,10 +55,15 @@ __device__ __forceinline__ void stream_read_copy(const __nv_bfloat16* __restrict
     for (int r = 0; r < 8; ++r) {
       const int qs = (blk % QB) * 8 + r;
       float hv[4];
-      Quad<__nv_bfloat16>::unpack(q[qs], hv);
+      if constexpr (std::is_same<HT, uint8_t>::value) {
+        const int d = blk * 8 + r;
+        fp8_dequant(q[qs], __shfl_sync(kFull, sc[d >> 5], d & 31), hv);
+      } else {
+        Quad<HT>::unpack(q[qs], hv);
+      }
 #pragma unroll
       for (int k = 0; k < kDraftsMax; ++k) part[k * 8 + r] = Dot<N>::partial(c[k], hv);
-      if (blk + QB < NBLK) q[qs] = Quad<__nv_bfloat16>::ld_stream(R + (size_t)(blk * 8 + r + kVerifyRowsInFlight) * N + 4 * j);
+      if (blk + QB < NBLK) q[qs] = Quad<HT>::ld_stream(R + (size_t)(blk * 8 + r + kVerifyRowsInFlight) * N + 4 * j);
     }
     const float v = reduce_scatter32(part, j);
     yo[(j >> 3) * P + blk * 8 + (j & 7)] = v;
@@ -69,6 +77,7 @@ __device__ __forceinline__ void stream_read_copy(const __nv_bfloat16* __restrict
 // (yo as above).  wx[s * P + d] = w_s x_s[d] is precomputed per warp; 8 rows per pass.
 template <typename T, int P, int N>
 __device__ __noinline__ void stream_anchor_flush(float* __restrict__ Hd, __nv_bfloat16* __restrict__ Rd,
+                                                 uint8_t* __restrict__ R8, float* __restrict__ Rs,
                                                  const float (&c)[kDraftsMax][4], float* yo, int j, int hc,
                                                  const float* wx, float decay, const T* sB) {
 #pragma unroll 1
@@ -99,13 +108,21 @@ __device__ __noinline__ void stream_anchor_flush(float* __restrict__ Hd, __nv_bf
       for (int e = 0; e < 4; ++e) v[e] = __fmaf_rn(decay, h[r][e], acc[r][e]);
       const size_t o = (size_t)(d0 + r) * N + 4 * j;
       *reinterpret_cast<float4*>(Hd + o) = make_float4(v[0], v[1], v[2], v[3]);
-      __nv_bfloat162 lo2 = __floats2bfloat162_rn(v[0], v[1]), hi2 = __floats2bfloat162_rn(v[2], v[3]);
-      uint2 u;
-      u.x = *reinterpret_cast<uint32_t*>(&lo2);
-      u.y = *reinterpret_cast<uint32_t*>(&hi2);
-      *reinterpret_cast<uint2*>(Rd + o) = u;
-      float rv[4];
-      Quad<__nv_bfloat16>::unpack(u, rv);
+      float rv[4];   // the values the read copy now holds
+      if (R8 != nullptr) {
+        float s;
+        const uint32_t wq = fp8_quant_row(v, &s);
+        *reinterpret_cast<uint32_t*>(R8 + o) = wq;
+        if (j == 0) Rs[d0 + r] = s;
+        fp8_dequant(wq, s, rv);
+      } else {
+        __nv_bfloat162 lo2 = __floats2bfloat162_rn(v[0], v[1]), hi2 = __floats2bfloat162_rn(v[2], v[3]);
+        uint2 u;
+        u.x = *reinterpret_cast<uint32_t*>(&lo2);
+        u.y = *reinterpret_cast<uint32_t*>(&hi2);
+        *reinterpret_cast<uint2*>(Rd + o) = u;
+        Quad<__nv_bfloat16>::unpack(u, rv);
+      }
 #pragma unroll
       for (int k = 0; k < kDraftsMax; ++k) part[k * 8 + r] = Dot<N>::partial(c[k], rv);
     }
@@ -115,7 +132,7 @@ __device__ __noinline__ void stream_anchor_flush(float* __restrict__ Hd, __nv_bf
   __syncwarp();
 }
 
-template <typename T, int P, int N, int QM>
+template <typename T, typename HT, int P, int N, int QM>
 __global__ void __launch_bounds__(kThreads, 2) k_verify_heads(LaunchArgs a) {
   static_assert(N == 128 && P % 8 == 0 && QM <= 32 - kDraftsMax, "lane split of Dot<128>; one warp scans");
   constexpr int QR = QM + kDraftsMax;
@@ -146,7 +163,15 @@ __global__ void __launch_bounds__(kThreads, 2) k_verify_heads(LaunchArgs a) {
   const int h0 = flush ? 0 : hc;   // committed rows that precede the drafts
   const size_t HP = (size_t)a.H * P, GN = (size_t)a.G * N;
   const size_t soff = ((size_t)slot * a.H + h) * P * N;
-  const __nv_bfloat16* R = (const __nv_bfloat16*)a.read_copy + soff;
+  const HT* R = (const HT*)a.read_copy + soff;   // bf16 values or FP8 codes
+  float sc[2] = {0.f, 0.f};                      // FP8: scales of rows j and 32 + j
+  if constexpr (std::is_same<HT, uint8_t>::value) {
+    if (!flush && active) {
+      const float* Rs = a.read_scale + ((size_t)slot * a.H + h) * P;
+      sc[0] = Rs[j];
+      sc[1] = Rs[32 + j];
+    }
+  }
   // the drafts' C rows (lane quads); drafts >= T contribute nothing
   float c[kDraftsMax][4];
 #pragma unroll
@@ -158,10 +183,10 @@ __global__ void __launch_bounds__(kThreads, 2) k_verify_heads(LaunchArgs a) {
       for (int e = 0; e < 4; ++e) c[k][e] = 0.f;
     }
   }
-  Quad<__nv_bfloat16>::raw q[kVerifyRowsInFlight];
+  typename Quad<HT>::raw q[kVerifyRowsInFlight];
   if (!flush && active) {
 #pragma unroll
-    for (int r = 0; r < kVerifyRowsInFlight; ++r) q[r] = Quad<__nv_bfloat16>::ld_stream(R + (size_t)r * N + 4 * j);
+    for (int r = 0; r < kVerifyRowsInFlight; ++r) q[r] = Quad<HT>::ld_stream(R + (size_t)r * N + 4 * j);
   }
   // committed rows 0..hc-1 at smem rows 0..hc-1, drafts at rows QM..QM+T-1
   const T* bB = (const T*)a.bB + (size_t)slot * a.Q * GN + (size_t)g * N;
@@ -186,7 +211,7 @@ __global__ void __launch_bounds__(kThreads, 2) k_verify_heads(LaunchArgs a) {
   const float dt_d = j < Td ? a.dt[((size_t)i * Td + j) * a.H + h] : 0.f;
   const float Ah = a.A[h], bias = a.dt_bias[h];
   float* yo = syo + w * kDraftsMax * P;
-  if (!flush && active) stream_read_copy<P, N>(R, q, c, yo, j);
+  if (!flush && active) stream_read_copy<HT, P, N>(R, q, c, yo, j, sc);
   // output rows s < h0 + T: committed rows then drafts
   const int nout = h0 + Td;
   const float dt_o_d = __shfl_sync(kFull, dt_d, max(j - h0, 0) & 31);
@@ -231,7 +256,10 @@ __global__ void __launch_bounds__(kThreads, 2) k_verify_heads(LaunchArgs a) {
   __syncthreads();
   if (!active) return;
   if (flush)
-    stream_anchor_flush<T, P, N>(a.state + soff, (__nv_bfloat16*)a.read_copy + soff, c, yo, j, hc, sw, decay, sB);
+    stream_anchor_flush<T, P, N>(a.state + soff, a.read_fp8 ? nullptr : (__nv_bfloat16*)a.read_copy + soff,
+                                 a.read_fp8 ? (uint8_t*)a.read_copy + soff : nullptr,
+                                 a.read_fp8 ? a.read_scale + ((size_t)slot * a.H + h) * P : nullptr, c, yo, j, hc,
+                                 sw, decay, sB);
   // outputs of draft k (row t_k = h0 + k), d = j + 32 m: one pass over the rows s serves every draft
   // (each draft's sum still runs over s = 0..t_k in order)
   const float Dh = a.D[h];
@@ -296,13 +324,13 @@ __global__ void __launch_bounds__(kThreads, 2) k_verify_heads(LaunchArgs a) {
   }
 }
 
-template <typename T, int QM>
+template <typename T, typename HT, int QM>
 cudaError_t launch_verify_heads(const LaunchArgs& a, cudaStream_t s) {
   constexpr int P = 64, N = 128;
   constexpr size_t sm = verify_smem_bytes<T, P, N, QM>();
-  cudaError_t e = prep(k_verify_heads<T, P, N, QM>, sm);
+  cudaError_t e = prep(k_verify_heads<T, HT, P, N, QM>, sm);
   if (e != cudaSuccess) return e;
-  k_verify_heads<T, P, N, QM><<<dim3(a.G, a.nseq), kThreads, sm, s>>>(a);
+  k_verify_heads<T, HT, P, N, QM><<<dim3(a.G, a.nseq), kThreads, sm, s>>>(a);
   return cudaGetLastError();
 }
 
@@ -314,8 +342,12 @@ bool heads_verify_supported(int P, int N, int Q, int T, int H, int G) {
 }
 
 cudaError_t heads_verify(const LaunchArgs& a, cudaStream_t s) {
-  if (a.io == ERS_DTYPE_BF16) return launch_verify_heads<__nv_bfloat16, 16>(a, s);
-  return launch_verify_heads<float, 16>(a, s);
+  if (a.read_fp8) {
+    if (a.io == ERS_DTYPE_BF16) return launch_verify_heads<__nv_bfloat16, uint8_t, 16>(a, s);
+    return launch_verify_heads<float, uint8_t, 16>(a, s);
+  }
+  if (a.io == ERS_DTYPE_BF16) return launch_verify_heads<__nv_bfloat16, __nv_bfloat16, 16>(a, s);
+  return launch_verify_heads<float, __nv_bfloat16, 16>(a, s);
 }
 
 }  // namespace ers

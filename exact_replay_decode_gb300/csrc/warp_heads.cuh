@@ -6,6 +6,7 @@
 #pragma once
 
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <stdint.h>
 
 #include "ers_common.cuh"
@@ -31,6 +32,14 @@ template <> struct Quad<float> {
   }
   __device__ __forceinline__ static void unpack(raw u, float (&v)[4]) {
     v[0] = u.x; v[1] = u.y; v[2] = u.z; v[3] = u.w;
+  }
+};
+template <> struct Quad<uint8_t> {   // FP8 e4m3 read copy: a lane's 4 codes (dequantised with the row scale)
+  using raw = uint32_t;
+  __device__ __forceinline__ static raw ld_stream(const uint8_t* p) {
+    uint32_t v;
+    asm volatile("ld.global.nc.L1::no_allocate.L2::256B.u32 %0, [%1];" : "=r"(v) : "l"(p));
+    return v;
   }
 };
 template <> struct Quad<__nv_bfloat16> {
@@ -105,6 +114,52 @@ __device__ __forceinline__ df warp_scan_df(df v, int j) {
     if (j >= st) v = df_add(df{ph, pl}, v);
   }
   return v;
+}
+
+// ---- FP8 e4m3 read copy with one fp32 scale per state row ----------------------------------------
+// Row d of a head is held by the warp, lane j owning elements [4j, 4j+4).  Quantisation:
+// s = amax_n |S[d][n]| / 448 (IEEE division), q[n] = RNE_satfinite(S[d][n] / s), all-zero rows give
+// s = 0 and zero bytes; lane j's 4 codes form one 32-bit word, element 4j in the low byte.
+constexpr float kE4M3Max = 448.f;
+
+__device__ __forceinline__ uint32_t e4m3x2(float lo, float hi) {   // two codes, lo in the low byte
+  uint16_t r;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+// Quantises the warp's row (lane quad v); returns lane j's 4 codes, the row scale in *scale.
+__device__ __forceinline__ uint32_t fp8_quant_row(const float (&v)[4], float* scale) {
+  float m = fmaxf(fmaxf(fabsf(v[0]), fabsf(v[1])), fmaxf(fabsf(v[2]), fabsf(v[3])));
+#pragma unroll
+  for (int o = 16; o >= 1; o >>= 1) m = fmaxf(m, __shfl_xor_sync(kFull, m, o));
+  const float s = __fdiv_rn(m, kE4M3Max);
+  *scale = s;
+  if (s == 0.f) return 0u;
+  const float y0 = __fdiv_rn(v[0], s), y1 = __fdiv_rn(v[1], s), y2 = __fdiv_rn(v[2], s), y3 = __fdiv_rn(v[3], s);
+  return e4m3x2(y0, y1) | (e4m3x2(y2, y3) << 16);
+}
+
+// Lane quad of an FP8 row: the 4 codes of word w read back as q * s.
+__device__ __forceinline__ void fp8_dequant(uint32_t w, float s, float (&v)[4]) {
+  uint32_t h01, h23;
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h01) : "h"((uint16_t)(w & 0xFFFFu)));
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h23) : "h"((uint16_t)(w >> 16)));
+  const __half2 a = *reinterpret_cast<const __half2*>(&h01);
+  const __half2 b = *reinterpret_cast<const __half2*>(&h23);
+  v[0] = __fmul_rn(__low2float(a), s);
+  v[1] = __fmul_rn(__high2float(a), s);
+  v[2] = __fmul_rn(__low2float(b), s);
+  v[3] = __fmul_rn(__high2float(b), s);
+}
+
+// Writes row d (lane quad v) of an FP8 copy: codes to R8 + d*N + 4j, scale to Rs[d].
+template <int N>
+__device__ __forceinline__ void fp8_store_row(const float (&v)[4], uint8_t* R8, float* Rs, int d, int j) {
+  float s;
+  const uint32_t w = fp8_quant_row(v, &s);
+  *reinterpret_cast<uint32_t*>(R8 + (size_t)d * N + 4 * j) = w;
+  if (j == 0) Rs[d] = s;
 }
 
 template <typename K>

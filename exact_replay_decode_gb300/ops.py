@@ -183,16 +183,30 @@ STATIC_SCRATCH_BYTES = 16 << 20
 
 # ------------------------------------------------------------------------------------------------
 class ReplayCache:
-    """Per-slot exact-replay / ReplaySSM state: fp32 checkpoint (anchor), optional bf16 read copy,
-    token-major partial-chunk buffers of (x, raw dt, B, C) and the per-slot position."""
+    """Per-slot exact-replay / ReplaySSM state: fp32 checkpoint (anchor), optional read copy,
+    token-major partial-chunk buffers of (x, raw dt, B, C) and the per-slot position.
+
+    read_dtype "bf16": read_copy [S,H,P,N] bf16.  read_dtype "fp8": read_copy [S,H,P,N] uint8 holding
+    e4m3 codes and read_scale [S,H,P] fp32, one scale per state row (value = code * scale)."""
 
     def __init__(self, nslots: int, nheads: int, ngroups: int, headdim: int, dstate: int, chunk: int,
-                 io_dtype: torch.dtype = torch.bfloat16, read_copy: bool = False, device="cuda"):
+                 io_dtype: torch.dtype = torch.bfloat16, read_copy: bool = False, device="cuda",
+                 read_dtype: str = "bf16"):
+        if read_dtype not in ("bf16", "fp8"):
+            raise ValueError(f"read_dtype must be 'bf16' or 'fp8', got {read_dtype!r}")
         self.nslots, self.H, self.G, self.P, self.N, self.Q = nslots, nheads, ngroups, headdim, dstate, chunk
         self.io = io_dtype
+        self.read_dtype = read_dtype
         z = dict(device=device)
-        self.state = torch.zeros(nslots, nheads, headdim, dstate, dtype=torch.float32, **z)
-        self.read_copy = torch.zeros(nslots, nheads, headdim, dstate, dtype=torch.bfloat16, **z) if read_copy else None
+        shp = (nslots, nheads, headdim, dstate)
+        self.state = torch.zeros(*shp, dtype=torch.float32, **z)
+        self.read_copy = None
+        self.read_scale = None
+        if read_copy:
+            fp8 = read_dtype == "fp8"
+            self.read_copy = torch.zeros(*shp, dtype=torch.uint8 if fp8 else torch.bfloat16, **z)
+            if fp8:
+                self.read_scale = torch.zeros(nslots, nheads, headdim, dtype=torch.float32, **z)
         self.buf_x = torch.zeros(nslots, chunk, nheads, headdim, dtype=io_dtype, **z)
         self.buf_dt = torch.zeros(nslots, chunk, nheads, dtype=torch.float32, **z)
         self.buf_B = torch.zeros(nslots, chunk, ngroups, dstate, dtype=io_dtype, **z)
@@ -204,13 +218,22 @@ class ReplayCache:
         return _dims(self.H, self.G, self.P, self.N, self.Q, self.io)
 
     def _c(self) -> _abi.Cache:
+        rd = _abi.READ_FP8_E4M3 if self.read_dtype == "fp8" else _abi.READ_BF16
         return _abi.Cache(self.state.data_ptr(), _ptr(self.read_copy), self.buf_x.data_ptr(), self.buf_dt.data_ptr(),
-                          self.buf_B.data_ptr(), self.buf_C.data_ptr(), self.pos.data_ptr(), self.nslots)
+                          self.buf_B.data_ptr(), self.buf_C.data_ptr(), self.pos.data_ptr(), self.nslots, rd,
+                          _ptr(self.read_scale))
+
+    def read_values(self) -> Optional[torch.Tensor]:
+        """The read copy's values as fp32 (FP8: code * row scale), or None without a read copy."""
+        if self.read_copy is None:
+            return None
+        if self.read_scale is None:
+            return self.read_copy.float()
+        return self.read_copy.view(torch.float8_e4m3fn).float() * self.read_scale.unsqueeze(-1)
 
     def nbytes(self) -> int:
         ts = [self.state, self.buf_x, self.buf_dt, self.buf_B, self.buf_C, self.pos]
-        if self.read_copy is not None:
-            ts.append(self.read_copy)
+        ts += [t for t in (self.read_copy, self.read_scale) if t is not None]
         return sum(t.numel() * t.element_size() for t in ts)
 
 

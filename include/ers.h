@@ -59,7 +59,7 @@ typedef int32_t ers_status;
 #define ERS_OK 0
 #define ERS_EINVAL 1        /* NULL pointer, bad count or bad flag combination */
 #define ERS_ESHAPE 2        /* unsupported dimensions (see ers_dims) */
-#define ERS_EDTYPE 3        /* unsupported io dtype */
+#define ERS_EDTYPE 3        /* unsupported io dtype or read-copy dtype */
 #define ERS_EPTR 4          /* pointer not 16-byte aligned */
 #define ERS_EALIGN 5        /* device: a slot's buffered position is outside its legal range, i.e. the
                                state's physical offset would differ from the offset the caller tracks */
@@ -100,11 +100,25 @@ typedef struct ers_params {
 
 /* Per-slot replay cache (exact-replay RFC section 3; ReplaySSM "Motivation and method").
  *   state     [nslots, H, P, N] fp32: the boundary checkpoint (exact mode) or recurrence anchor (ReplaySSM)
- *   read_copy [nslots, H, P, N] bf16 or NULL: low-precision copy cast from the same fp32 values as `state`
+ *   read_copy [nslots, H, P, N] or NULL: low-precision copy cast from the same fp32 values as `state`,
+ *             bf16 (read_dtype ERS_READ_BF16) or FP8 e4m3 bytes (ERS_READ_FP8_E4M3)
  *   buf_x     [nslots, Q, H, P] io dtype;  buf_dt [nslots, Q, H] fp32 raw dt
  *   buf_B, buf_C [nslots, Q, G, N] io dtype: token-major partial-chunk input buffers
  *   pos       [nslots] int32: buffered tokens p (exact mode, 0 <= p < Q between calls) or the
- *             committed pointer h (ReplaySSM mode, 0 <= h <= L). */
+ *             committed pointer h (ReplaySSM mode, 0 <= h <= L).
+ *   read_dtype ERS_READ_BF16 (0) or ERS_READ_FP8_E4M3 (1).
+ *   read_scale [nslots, H, P] fp32, FP8 read copy only (else NULL): one scale per state row.
+ *
+ * FP8 read copy (ReplaySSM "Paper-reported results", the FP8-read / FP32-recurrence mode; the page
+ * names the mode without its quantisation, so this library defines it): each state row (one d of
+ * one head) is stored as e4m3 bytes q[n] = RNE_satfinite(S[d][n] / s) with the row scale
+ * s = amax_n |S[d][n]| / 448 (IEEE fp32 division; an all-zero row stores s = 0 and zero bytes) and
+ * read as q[n] * s (fp32).  Supported where the CUDA-core warp-per-head kernels run (headdim 64,
+ * dstate 128, chunk <= 16; verify with at most 4 drafts and 8 heads per group); elsewhere calls
+ * that read or write the copy return ERS_EUNSUPPORTED. */
+#define ERS_READ_BF16 0
+#define ERS_READ_FP8_E4M3 1
+
 typedef struct ers_cache {
   float* state;
   void* read_copy;
@@ -114,6 +128,8 @@ typedef struct ers_cache {
   void* buf_C;
   int32_t* pos;
   int32_t nslots;
+  int32_t read_dtype;
+  float* read_scale;
 } ers_cache;
 
 /* Human-readable name of a status code (static storage, never NULL). */

@@ -19,7 +19,7 @@ aarch64 hosts.
 from __future__ import annotations
 
 import dataclasses
-from typing import Optional, Sequence
+from typing import Optional, Sequence, Tuple
 
 import numpy as np
 
@@ -190,3 +190,26 @@ def verify_inputs(w: Workload, seed: int = 0, batch: Optional[int] = None, steps
     drafts = make_tokens(rng, K * S * T, w.dims, w.bf16)
     accepted = rng.integers(0, T + 1, size=(K, S)).astype(np.int32)
     return params, hist, drafts, accepted
+
+
+def quant_probe_state(seed: int, shape: Tuple[int, ...]) -> np.ndarray:
+    """fp32 states for read-copy quantisation checks: Gaussian rows with per-row magnitudes from
+    2^-30 to 2^30, plus rows that stress the edge cases of a per-row scale: an all-zero row, a row
+    with one large entry and the rest 2^-14 below it (codes in the subnormal range), a constant row,
+    a row of alternating signs and a row with a single nonzero entry.  The last axis is dstate; the
+    special rows sit in the first (sequence, head) and need at least 6 rows there."""
+    rng = np.random.Generator(np.random.PCG64(seed))
+    s = rng.standard_normal(shape).astype(np.float32)
+    mag = np.exp2(rng.integers(-30, 31, size=shape[:-1] + (1,))).astype(np.float32)
+    s *= mag
+    first = s.reshape(-1, shape[-2], shape[-1])[0]
+    N = shape[-1]
+    first[0] = 0.0
+    first[1] = rng.standard_normal(N).astype(np.float32) * np.float32(2.0 ** -14)
+    first[1, 5] = 3.0
+    first[2] = np.float32(0.7)
+    first[3] = np.where(np.arange(N) % 2 == 0, 1.0, -1.0).astype(np.float32) * np.float32(1e-3)
+    first[4] = 0.0
+    first[4, N - 1] = -5e-20
+    first[5] = rng.uniform(-448.0, 448.0, N).astype(np.float32)
+    return s

@@ -114,3 +114,35 @@ def test_zero_sequences_is_a_noop(lib):
     d, p = _dims(), _prm()
     assert lib.ers_ssd_scan_fwd(ctypes.byref(d), ctypes.byref(p), 0, 0, 0, None, None, None, None, None, None,
                                 None, None, None, None, 0, None, None) == 0
+
+
+@needs_no_gpu
+def test_validation_of_fp8_read_copies(lib):
+    """FP8 read copies: the dtype code is checked, the row scales are required and aligned, and
+    shapes the warp-per-head kernels do not cover return ERS_EUNSUPPORTED before any launch."""
+    from exact_replay_decode_gb300 import _abi
+    p = _prm()
+
+    def cache(read_dtype=_abi.READ_FP8_E4M3, scale=FAKE):
+        return _abi.Cache(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 4, read_dtype, scale)
+
+    def dec(d, c, flags=_abi.FLAG_REPLAYSSM):
+        return lib.ers_replay_decode(ctypes.byref(d), ctypes.byref(p), ctypes.byref(c), 4, None, FAKE, FAKE, FAKE,
+                                     FAKE, flags, FAKE, None, None)
+
+    def ver(d, c):
+        return lib.ers_spec_verify(ctypes.byref(d), ctypes.byref(p), ctypes.byref(c), 4, None, 4, FAKE, FAKE, FAKE,
+                                   FAKE, 0, FAKE, None, None)
+
+    def ref(d, c):
+        return lib.ers_refresh(ctypes.byref(d), ctypes.byref(p), ctypes.byref(c), 4, None, _abi.FLAG_REPLAYSSM, 1,
+                               None, None)
+
+    assert dec(_dims(), cache(read_dtype=2)) == 3                            # ERS_EDTYPE
+    assert dec(_dims(), cache(scale=0)) == 1                                 # scales required
+    assert dec(_dims(), cache(scale=MISALIGNED)) == 4
+    for d in (_dims(chunk=32), _dims(headdim=32, dstate=32), _dims(dstate=64)):
+        assert dec(d, cache()) == 12                                         # ERS_EUNSUPPORTED
+        assert ref(d, cache()) == 12
+    assert ver(_dims(nheads=32, ngroups=2), cache()) == 12                   # 16 heads per group
+    assert ver(_dims(chunk=32), cache()) == 12
