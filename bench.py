@@ -371,7 +371,7 @@ def bench_prefill(dev, name: str, iters: int, warmup: int, hbm: float, tc: float
             "tflops": PREFILL_FLOPS[name] / (ms * 1e-3) / 1e12, "l2": "flushed before each call"}
 
 
-def bench_verify(dev, steps: int, hbm: float):
+def bench_verify(dev, steps: int, hbm: float, read_dtype: str = "bf16"):
     import torch
     import exact_replay_decode_gb300 as ers
     from synth import torch_io
@@ -384,9 +384,13 @@ def bench_verify(dev, steps: int, hbm: float):
     hx, hdt, hB, hC = torch_io.tokens_to(hist, dev)
     cu = torch.arange(0, S * 32 + 1, 32, dtype=torch.int32, device=dev)
     _, fin = ers.ssd_scan_fwd(hx, hdt, prm, hB, hC, chunk=L, cu_seqlens=cu)
-    cache = ers.ReplayCache(S, d.nheads, d.ngroups, d.headdim, d.dstate, L, torch.bfloat16, read_copy=True)
+    cache = ers.ReplayCache(S, d.nheads, d.ngroups, d.headdim, d.dstate, L, torch.bfloat16, read_copy=True,
+                            read_dtype=read_dtype)
     cache.state.copy_(fin)
     ers.refresh(cache, prm, replayssm=True, drafts_T=L + 1)
+    # read copy per sequence: bf16 values, or FP8 codes + one fp32 scale per state row
+    copy_bytes = d.nheads * d.headdim * d.dstate * 2 if read_dtype == "bf16" else \
+        d.nheads * d.headdim * (d.dstate + 4)
     dx, ddt, dB, dC = torch_io.tokens_to(drafts, dev, lead=(steps, S, T))
     acc_t = torch.from_numpy(acc).to(dev)
     y = torch.empty(S, T, d.nheads, d.headdim, dtype=torch.bfloat16, device=dev)
@@ -397,8 +401,9 @@ def bench_verify(dev, steps: int, hbm: float):
     for k in range(steps):
         flush = hs + T > L
         base = np.where(flush, 0, hs)
-        total_bytes += S * (1_048_576 + 50_176 + 50_176 + 32_768) + int(base.sum()) * 10_496
-        total_bytes += int(flush.sum()) * (2_097_152 + 2_097_152 + 1_048_576 - 1_048_576) + \
+        total_bytes += S * (copy_bytes + 50_176 + 50_176 + 32_768) + int(base.sum()) * 10_496
+        # a flushing slot reads and writes its fp32 anchor and writes its copy instead of reading it
+        total_bytes += int(flush.sum()) * (2_097_152 + 2_097_152 + copy_bytes - copy_bytes) + \
             int(hs[flush].sum()) * 10_496
         hs = base + acc[k]
     torch.cuda.synchronize()
@@ -413,9 +418,89 @@ def bench_verify(dev, steps: int, hbm: float):
     st.raise_if_error("bench verify")
     ms = e0.elapsed_time(e1)
     ach = total_bytes / (ms * 1e-3) / 1e9
-    return {"seq_verify_steps_per_s": S * steps / (ms * 1e-3), "committed_tok_per_s": float(acc.sum()) / (ms * 1e-3),
-            "us_per_step": ms * 1e3 / steps, "achieved_gbs": ach, "hbm_frac": ach / hbm,
-            "algorithmic_bytes": total_bytes, "steps": steps}
+    return {"read_copy": read_dtype, "seq_verify_steps_per_s": S * steps / (ms * 1e-3),
+            "committed_tok_per_s": float(acc.sum()) / (ms * 1e-3), "us_per_step": ms * 1e3 / steps,
+            "achieved_gbs": ach, "hbm_frac": ach / hbm, "algorithmic_bytes": total_bytes, "steps": steps}
+
+
+def bench_rssm_decode(dev, cycles: int, hbm: float, read_dtype: str):
+    """Non-speculative ReplaySSM decode of the B=256 decode workload: each step applies the flush
+    rule for one token (ers_refresh, h + 1 > L: fold the anchor, recast the read copy) and then
+    decodes from the read copy.  One ring cycle of steps (TOKEN_RING) is captured as a CUDA graph
+    and replayed, so the host's per-call overhead does not pace the GPU.  Start positions h0 ~
+    U{0..L-1} per sequence (untimed decodes of slot subsets)."""
+    import torch
+    import exact_replay_decode_gb300 as ers
+    from synth import torch_io
+    w = synth.workload("decode_b256_h64")
+    d = w.dims
+    S, L = w.batch, d.chunk
+    params, hist, h0, stream = synth.decode_inputs(w, seed=3, batch=S, steps=TOKEN_RING)
+    A, D, dtb = torch_io.params_to(params, dev)
+    prm = ers.LayerParams(A, D, dtb)
+    ht = synth.Tokens.concat(hist)
+    cu = torch.tensor(np.concatenate([[0], np.cumsum([h.ntokens for h in hist])]), dtype=torch.int32, device=dev)
+    hx, hdt, hB, hC = torch_io.tokens_to(ht, dev)
+    _, fin = ers.ssd_scan_fwd(hx, hdt, prm, hB, hC, chunk=L, cu_seqlens=cu)
+    del hx, hdt, hB, hC
+    cache = ers.ReplayCache(S, d.nheads, d.ngroups, d.headdim, d.dstate, L, torch.bfloat16, read_copy=True,
+                            read_dtype=read_dtype)
+    cache.state.copy_(fin)
+    ers.refresh(cache, prm, replayssm=True, drafts_T=L + 1)           # h = 0: cast the read copy
+    tok = torch_io.tokens_to(stream, dev, lead=(TOKEN_RING, S))
+    y = torch.empty(S, d.nheads, d.headdim, dtype=torch.bfloat16, device=dev)
+    st = ers.Status(dev)
+    for r in range(L - 1):                                              # advance slot i to h0[i]
+        sel = torch.from_numpy(np.nonzero(h0 > r)[0].astype(np.int32)).to(dev)
+        if sel.numel():
+            sl = sel.long()
+            ers.replay_decode(cache, prm, *(t[TOKEN_RING - 1][sl] for t in tok), slot=sel, replayssm=True)
+
+    def step(k):
+        ers.refresh(cache, prm, replayssm=True, drafts_T=1, status=st, check=False)
+        ers.replay_decode(cache, prm, *(t[k] for t in tok), replayssm=True, status=st, check=False, out=y)
+
+    # algorithmic bytes from the run's own pointers: a flush reads and writes the anchor, reads the
+    # h buffered rows and writes the copy; a decode reads the copy, h rows and the new token, writes
+    # the token to the buffer and y
+    copy_bytes = d.nheads * d.headdim * d.dstate * 2 if read_dtype == "bf16" else d.nheads * d.headdim * (d.dstate + 4)
+    hs = h0.astype(np.int64)
+
+    def cycle_bytes():
+        nonlocal hs
+        b = 0
+        for _ in range(TOKEN_RING):
+            fl = hs + 1 > L
+            b += int(fl.sum()) * (2 * 2_097_152 + copy_bytes) + int(hs[fl].sum()) * 10_496
+            hs = np.where(fl, 0, hs)
+            b += S * (copy_bytes + 12_544 + 12_544 + 8_192) + int(hs.sum()) * 10_496
+            hs = hs + 1
+        return b
+
+    g = torch.cuda.CUDAGraph()
+    torch.cuda.synchronize()
+    with torch.cuda.graph(g, capture_error_mode="relaxed"):            # captured, not run
+        for k in range(TOKEN_RING):
+            step(k)
+    g.replay()                                                          # untimed cycle
+    cycle_bytes()
+    total = sum(cycle_bytes() for _ in range(cycles))
+    torch.cuda.synchronize()
+    s = torch.cuda.current_stream()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(s)
+    for _ in range(cycles):
+        g.replay()
+    e1.record(s)
+    torch.cuda.synchronize()
+    st.raise_if_error("bench replayssm decode")
+    if not np.array_equal(cache.pos.cpu().numpy(), hs.astype(np.int32)):
+        raise AssertionError("ReplaySSM decode bench: positions differ from the byte model")
+    nsteps = cycles * TOKEN_RING
+    ms = e0.elapsed_time(e1) / nsteps
+    ach = total / nsteps / (ms * 1e-3) / 1e9
+    return {"read_copy": read_dtype, "seq_steps_per_s": S / (ms * 1e-3), "us_per_step": ms * 1e3,
+            "achieved_gbs": ach, "hbm_frac": ach / hbm, "bytes_per_step": total / nsteps, "steps": nsteps}
 
 
 def bench_ssu(dev, steps: int, hbm: float):
@@ -537,7 +622,7 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--decode-only", action="store_true", help="only the headline decode measurement")
     ap.add_argument("--batch", type=int, default=None, help="decode sequences per GPU (profiling runs only)")
-    ap.add_argument("--section", choices=["prefill", "verify", "ssu"], default=None,
+    ap.add_argument("--section", choices=["prefill", "verify", "rssm", "ssu"], default=None,
                     help="run only this secondary workload and print its JSON (profiling aid, no headline)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
@@ -556,8 +641,13 @@ def main(argv=None):
     if args.section is not None:
         if args.section == "prefill":
             out = {n: bench_prefill(dev, n, 10, args.warmup, hbm, tc) for n in ("prefill_2048_h32", "varlen_4seq_h64")}
+        elif args.section == "rssm":
+            out = {r: bench_rssm_decode(dev, 4, hbm, r) for r in ("bf16", "fp8")}
         elif args.section == "verify":
             out = bench_verify(dev, 32, hbm)
+            fp8 = bench_verify(dev, 32, hbm, "fp8")
+            if rank == 0:
+                print(json.dumps({"verify_fp8": fp8}))
         else:
             out = bench_ssu(dev, 16, hbm)
         if rank == 0:
@@ -580,6 +670,8 @@ def main(argv=None):
     if not args.decode_only:
         extra["prefill"] = {n: bench_prefill(dev, n, 10, 3, hbm, tc) for n in ("prefill_2048_h32", "varlen_4seq_h64")}
         extra["verify"] = bench_verify(dev, 32, hbm)
+        extra["verify_fp8"] = bench_verify(dev, 32, hbm, "fp8")
+        extra["replayssm_decode"] = {r: bench_rssm_decode(dev, 4, hbm, r) for r in ("bf16", "fp8")}
         extra["ssu"] = bench_ssu(dev, 16, hbm)
     line = {
         "metric": "replay-decode seq-steps/s per layer @B=256",

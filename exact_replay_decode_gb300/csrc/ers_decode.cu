@@ -39,11 +39,12 @@ constexpr size_t heads_smem_bytes() {
 
 // Streams one head's state: lane j of row d reads elements [4j, 4j+4), 8 rows per block, two
 // blocks in flight (q holds rows 0..15 on entry).  yo[d] ends with the off-diagonal term (H C_p)[d]
-// (per-warp shared memory).
+// (per-warp shared memory).  An FP8 copy is read as codes; each row's dot product is then scaled by
+// the row scale, which lane d % 32 holds in sc[d / 32].
 template <typename HT>
-__device__ __forceinline__ void unpack_row(typename Quad<HT>::raw r, const float (&sc)[2], int d, float (&h)[4]) {
+__device__ __forceinline__ void unpack_row(typename Quad<HT>::raw r, float (&h)[4]) {
   if constexpr (std::is_same<HT, uint8_t>::value) {
-    fp8_dequant(r, __shfl_sync(kFull, sc[d >> 5], d & 31), h);   // row scale held by lane d % 32
+    fp8_codes(r, h);
   } else {
     Quad<HT>::unpack(r, h);
   }
@@ -61,12 +62,14 @@ __device__ __forceinline__ void stream_state(const HT* __restrict__ Hsrc, typena
     for (int r = 0; r < 8; ++r) {
       const int d = blk * 8 + r;
       float h[4];
-      unpack_row<HT>(q[sl + r], sc, d, h);
+      unpack_row<HT>(q[sl + r], h);
       part[sl + r] = Dot<N>::partial(c, h);
       if (blk + 2 < NBLK) q[sl + r] = Quad<HT>::ld_stream(Hsrc + (size_t)(d + 16) * N + 4 * j);
     }
     if (blk & 1) {
-      const float v = reduce_scatter16(part, j);
+      float v = reduce_scatter16(part, j);   // row (blk - 1) * 8 + j / 2 on even lanes
+      if constexpr (std::is_same<HT, uint8_t>::value)
+        v = __fmul_rn(v, __shfl_sync(kFull, sc[((blk - 1) * 8) >> 5], ((blk - 1) * 8 + (j >> 1)) & 31));
       if ((j & 1) == 0) yo[(blk - 1) * 8 + (j >> 1)] = v;
     }
   }
@@ -209,7 +212,8 @@ __global__ void __launch_bounds__(kThreads, 2) k_decode_heads(LaunchArgs a) {
     if (tid == 0) report(a.status, ERS_EALIGN);
     return;
   }
-  const bool refresh = !rssm && (a.flags & ERS_FLAG_FUSE_REFRESH) && p + 1 == a.Q;
+  // only exact mode (which streams the fp32 checkpoint) refreshes inside decode
+  const bool refresh = std::is_same<HT, float>::value && !rssm && (a.flags & ERS_FLAG_FUSE_REFRESH) && p + 1 == a.Q;
   // buffer rows 0..p-1 and the new token as row p: the group's B rows, this head's x rows
   const T* bB = (const T*)a.bB + (size_t)slot * a.Q * GN + (size_t)g * N;
   const T* nB = (const T*)a.B + (size_t)i * GN + (size_t)g * N;

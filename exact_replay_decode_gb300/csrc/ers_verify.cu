@@ -41,7 +41,8 @@ constexpr size_t verify_smem_bytes() {
 }
 
 // Read-copy stream: yo[k * P + d] = Dot<128>(C of draft k, R[d]) for all rows d.  q holds rows
-// [0, kVerifyRowsInFlight) on entry.
+// [0, kVerifyRowsInFlight) on entry.  An FP8 copy is read as codes and each row's dot products are
+// scaled by the row scale (lane d % 32 holds it in sc[d / 32]), as in the decode stream.
 template <typename HT, int P, int N>
 __device__ __forceinline__ void stream_read_copy(const HT* __restrict__ R,
                                                  typename Quad<HT>::raw (&q)[kVerifyRowsInFlight],
@@ -56,8 +57,7 @@ __device__ __forceinline__ void stream_read_copy(const HT* __restrict__ R,
       const int qs = (blk % QB) * 8 + r;
       float hv[4];
       if constexpr (std::is_same<HT, uint8_t>::value) {
-        const int d = blk * 8 + r;
-        fp8_dequant(q[qs], __shfl_sync(kFull, sc[d >> 5], d & 31), hv);
+        fp8_codes(q[qs], hv);
       } else {
         Quad<HT>::unpack(q[qs], hv);
       }
@@ -65,7 +65,9 @@ __device__ __forceinline__ void stream_read_copy(const HT* __restrict__ R,
       for (int k = 0; k < kDraftsMax; ++k) part[k * 8 + r] = Dot<N>::partial(c[k], hv);
       if (blk + QB < NBLK) q[qs] = Quad<HT>::ld_stream(R + (size_t)(blk * 8 + r + kVerifyRowsInFlight) * N + 4 * j);
     }
-    const float v = reduce_scatter32(part, j);
+    float v = reduce_scatter32(part, j);   // draft j / 8, row blk * 8 + j % 8
+    if constexpr (std::is_same<HT, uint8_t>::value)
+      v = __fmul_rn(v, __shfl_sync(kFull, sc[(blk * 8) >> 5], (blk * 8 + (j & 7)) & 31));
     yo[(j >> 3) * P + blk * 8 + (j & 7)] = v;
   }
   __syncwarp();
@@ -101,6 +103,7 @@ __device__ __noinline__ void stream_anchor_flush(float* __restrict__ Hd, __nv_bf
         for (int e = 0; e < 4; ++e) acc[r][e] = __fmaf_rn(wr[r], bs[e], acc[r][e]);
     }
     float part[32];
+    float srow = 0.f;   // FP8: scale of row d0 + j % 8
 #pragma unroll
     for (int r = 0; r < 8; ++r) {
       float v[4];
@@ -108,13 +111,14 @@ __device__ __noinline__ void stream_anchor_flush(float* __restrict__ Hd, __nv_bf
       for (int e = 0; e < 4; ++e) v[e] = __fmaf_rn(decay, h[r][e], acc[r][e]);
       const size_t o = (size_t)(d0 + r) * N + 4 * j;
       *reinterpret_cast<float4*>(Hd + o) = make_float4(v[0], v[1], v[2], v[3]);
-      float rv[4];   // the values the read copy now holds
+      float rv[4];   // what the read copy now holds (FP8: the codes, scaled after the reduction)
       if (R8 != nullptr) {
         float s;
         const uint32_t wq = fp8_quant_row(v, &s);
         *reinterpret_cast<uint32_t*>(R8 + o) = wq;
         if (j == 0) Rs[d0 + r] = s;
-        fp8_dequant(wq, s, rv);
+        if ((j & 7) == r) srow = s;
+        fp8_codes(wq, rv);
       } else {
         __nv_bfloat162 lo2 = __floats2bfloat162_rn(v[0], v[1]), hi2 = __floats2bfloat162_rn(v[2], v[3]);
         uint2 u;
@@ -126,7 +130,8 @@ __device__ __noinline__ void stream_anchor_flush(float* __restrict__ Hd, __nv_bf
 #pragma unroll
       for (int k = 0; k < kDraftsMax; ++k) part[k * 8 + r] = Dot<N>::partial(c[k], rv);
     }
-    const float v = reduce_scatter32(part, j);
+    float v = reduce_scatter32(part, j);
+    if (R8 != nullptr) v = __fmul_rn(v, srow);
     yo[(j >> 3) * P + d0 + (j & 7)] = v;
   }
   __syncwarp();

@@ -140,17 +140,18 @@ __device__ __forceinline__ uint32_t fp8_quant_row(const float (&v)[4], float* sc
   return e4m3x2(y0, y1) | (e4m3x2(y2, y3) << 16);
 }
 
-// Lane quad of an FP8 row: the 4 codes of word w read back as q * s.
-__device__ __forceinline__ void fp8_dequant(uint32_t w, float s, float (&v)[4]) {
+// Lane quad of an FP8 row as code values q (exact in fp32).  Output streams apply the row scale to
+// the row's dot product instead of to each element: (sum_n q[n] C[n]) * s.
+__device__ __forceinline__ void fp8_codes(uint32_t w, float (&v)[4]) {
   uint32_t h01, h23;
   asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h01) : "h"((uint16_t)(w & 0xFFFFu)));
   asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h23) : "h"((uint16_t)(w >> 16)));
   const __half2 a = *reinterpret_cast<const __half2*>(&h01);
   const __half2 b = *reinterpret_cast<const __half2*>(&h23);
-  v[0] = __fmul_rn(__low2float(a), s);
-  v[1] = __fmul_rn(__high2float(a), s);
-  v[2] = __fmul_rn(__low2float(b), s);
-  v[3] = __fmul_rn(__high2float(b), s);
+  v[0] = __low2float(a);
+  v[1] = __high2float(a);
+  v[2] = __low2float(b);
+  v[3] = __high2float(b);
 }
 
 // Writes row d (lane quad v) of an FP8 copy: codes to R8 + d*N + 4j, scale to Rs[d].
