@@ -143,18 +143,28 @@ def e4m3_round(a: np.ndarray) -> np.ndarray:
     return (np.sign(f) * r).astype(np.float32)
 
 
+def fp8_row_scale_exponent(amax: np.ndarray) -> np.ndarray:
+    """k of an FP8 row scale s = 2**k: the smallest integer with amax <= 448 * 2**k (no code of the
+    row saturates), at least -127 (so 1/s stays a finite fp32 power of two; all-zero and
+    subnormal-max rows take -127).  With amax = m * 2**e, m in [0.5, 1) and 448 = 0.875 * 2**9,
+    the condition reads m * 2**e <= 0.875 * 2**(9 + k)."""
+    a = np.asarray(amax, dtype=np.float64)
+    m, e = np.frexp(a)
+    k = e.astype(np.int64) - 9 + (m > 0.875)
+    tiny = a < 2.0 ** -126
+    return np.where(tiny, -127, np.maximum(k, -127))
+
+
 def fp8_rows_round(a: np.ndarray) -> np.ndarray:
-    """FP8 read copy of an fp32 state with one scale per row (the last axis is dstate):
-    scale = amax(|row|) / 448, q = e4m3(v / scale), read back as q * scale, all fp32 operations
-    (a zero row reads as zeros).  Input values are taken through fp32 as the GPU anchor is stored
-    in fp32; returned as fp64."""
-    f = np.ascontiguousarray(a, dtype=np.float32)
-    amax = np.max(np.abs(f), axis=-1, keepdims=True)
-    scale = (amax / np.float32(E4M3_MAX)).astype(np.float32)
-    with np.errstate(divide="ignore", invalid="ignore"):
-        y = np.where(scale > 0, f / np.where(scale > 0, scale, np.float32(1)), np.float32(0)).astype(np.float32)
-    q = e4m3_round(y)
-    return (q * scale).astype(np.float32).astype(np.float64)
+    """FP8 read copy of an fp32 state with one power-of-two scale per row (the last axis is dstate):
+    s = 2**fp8_row_scale_exponent(amax(|row|)), q = e4m3(v / s) (an exact scaling), read back as
+    q * s (exact).  Input values are taken through fp32 as the GPU anchor is stored in fp32;
+    returned as fp64."""
+    f = np.ascontiguousarray(a, dtype=np.float32).astype(np.float64)
+    k = fp8_row_scale_exponent(np.max(np.abs(f), axis=-1, keepdims=True))
+    s = np.ldexp(1.0, k)
+    q = e4m3_round(f / s).astype(np.float64)
+    return q * s
 
 
 class _Seq:

@@ -373,20 +373,43 @@ def test_e4m3_round_matches_brute_force_nearest_even():
     assert np.array_equal(oracle.e4m3_round(-x.astype(np.float32)), -oracle.e4m3_round(x.astype(np.float32)))
 
 
-def test_fp8_rows_round_scales_each_row_to_its_max():
+def test_fp8_row_scale_is_the_smallest_power_of_two_without_saturation():
+    # hand-worked rows: amax = 448 -> s = 1; the next fp32 above 448 -> s = 2; 1.0 -> 2^-8
+    # (256 <= 448 < 512); 0.21875 = 448 * 2^-11 exactly -> 2^-11; zero and tiny rows -> 2^-127
+    above = float(np.nextafter(np.float32(448), np.float32(1e9)))
+    got = oracle.fp8_row_scale_exponent(np.array([448.0, above, 1.0, 0.21875, 0.0, 2.0 ** -140]))
+    assert list(got) == [0, 1, -8, -11, -127, -127]
+    # brute force over random magnitudes: 448 * 2^(k-1) < amax <= 448 * 2^k
+    rng = np.random.Generator(np.random.PCG64(3))
+    amax = (rng.uniform(0.5, 1.0, 2000) * np.exp2(rng.integers(-100, 100, 2000))).astype(np.float32).astype(np.float64)
+    k = oracle.fp8_row_scale_exponent(amax)
+    assert np.all(amax <= 448.0 * np.exp2(k.astype(np.float64)))
+    assert np.all(amax > 448.0 * np.exp2(k.astype(np.float64) - 1))
+
+
+def test_fp8_rows_round_hand_worked_values():
+    # row max 1.0 -> s = 2^-8: 0.3 * 256 = 76.8 lies in [64, 128) where e4m3 steps by 8 -> 80 -> 0.3125;
+    # -0.5 * 256 = -128 is a code; 0.001 * 256 = 0.256 lies in [0.25, 0.5) (step 1/32) -> 0.25 -> 2^-10
+    r = oracle.fp8_rows_round(np.array([[1.0, 0.3, -0.5, 0.001, 0.0]]))
+    assert list(r[0]) == [1.0, 0.3125, -0.5, 2.0 ** -10, 0.0]
+    # the next fp32 above 448 reads back as 448 (s = 2: 224.00002 rounds to the code 224)
+    above = float(np.nextafter(np.float32(448), np.float32(1e9)))
+    assert oracle.fp8_rows_round(np.array([[above, 1.0]]))[0, 0] == 448.0
+    assert np.all(oracle.fp8_rows_round(np.zeros((2, 8))) == 0)
+
+
+def test_fp8_rows_round_error_bound_and_exact_codes():
     rng = np.random.Generator(np.random.PCG64(9))
     a = rng.standard_normal((3, 4, 16, 128)) * np.exp(rng.uniform(-8, 8, (3, 4, 16, 1)))
-    a[0, 0, 0] = 0.0                                          # an all-zero row reads as zeros
+    a[0, 0, 0] = 0.0
     r = oracle.fp8_rows_round(a)
     f = a.astype(np.float32).astype(np.float64)
-    amax = np.abs(f).max(axis=-1, keepdims=True)
+    s = np.exp2(oracle.fp8_row_scale_exponent(np.abs(f).max(axis=-1, keepdims=True)).astype(np.float64))
     assert np.all(r[0, 0, 0] == 0)
-    # e4m3 keeps 3 mantissa bits: error <= half a quantum of the row's scaled value, plus fp32 rounding
-    rel = np.abs(r - f) / np.where(amax > 0, amax, 1)
-    assert rel.max() <= 2.0 ** -4 * 1.001
-    # the row maximum is read back to within fp32 rounding of its value
-    i = np.argmax(np.abs(f), axis=-1)[..., None]
-    assert np.allclose(np.take_along_axis(r, i, -1), np.take_along_axis(f, i, -1), rtol=1e-6)
+    # e4m3 keeps 3 mantissa bits (half a quantum: 2^-4 relative) down to its subnormal step 2^-9
+    assert np.all(np.abs(r - f) <= 2.0 ** -4 * np.abs(f) + 2.0 ** -10 * s)
+    # every read value is a code times the row scale
+    assert np.array_equal(oracle.e4m3_round((r / s).astype(np.float32)).astype(np.float64), r / s)
 
 
 def test_protocol_anchor_independent_of_fp8_read_copy():
