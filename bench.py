@@ -424,11 +424,11 @@ def bench_verify(dev, steps: int, hbm: float, read_dtype: str = "bf16"):
 
 
 def bench_rssm_decode(dev, cycles: int, hbm: float, read_dtype: str):
-    """Non-speculative ReplaySSM decode of the B=256 decode workload: each step applies the flush
-    rule for one token (ers_refresh, h + 1 > L: fold the anchor, recast the read copy) and then
-    decodes from the read copy.  One ring cycle of steps (TOKEN_RING) is captured as a CUDA graph
-    and replayed, so the host's per-call overhead does not pace the GPU.  Start positions h0 ~
-    U{0..L-1} per sequence (untimed decodes of slot subsets)."""
+    """Non-speculative ReplaySSM decode of the B=256 decode workload: each step is one fused decode
+    call, which applies the flush rule for one token (h + 1 > L: fold the anchor, recast the read
+    copy) and decodes from the read copy.  One ring cycle of steps (TOKEN_RING) is captured as a
+    CUDA graph and replayed, so the host's per-call overhead does not pace the GPU.  Start positions
+    h0 ~ U{0..L-1} per sequence (untimed decodes of slot subsets)."""
     import torch
     import exact_replay_decode_gb300 as ers
     from synth import torch_io
@@ -454,11 +454,12 @@ def bench_rssm_decode(dev, cycles: int, hbm: float, read_dtype: str):
         sel = torch.from_numpy(np.nonzero(h0 > r)[0].astype(np.int32)).to(dev)
         if sel.numel():
             sl = sel.long()
-            ers.replay_decode(cache, prm, *(t[TOKEN_RING - 1][sl] for t in tok), slot=sel, replayssm=True)
+            ers.replay_decode(cache, prm, *(t[TOKEN_RING - 1][sl] for t in tok), slot=sel, replayssm=True,
+                              fuse_refresh=False)
 
     def step(k):
-        ers.refresh(cache, prm, replayssm=True, drafts_T=1, status=st, check=False)
-        ers.replay_decode(cache, prm, *(t[k] for t in tok), replayssm=True, status=st, check=False, out=y)
+        ers.replay_decode(cache, prm, *(t[k] for t in tok), replayssm=True, fuse_refresh=True, status=st,
+                          check=False, out=y)
 
     # algorithmic bytes from the run's own pointers: a flush reads and writes the anchor, reads the
     # h buffered rows and writes the copy; a decode reads the copy, h rows and the new token, writes
@@ -500,7 +501,8 @@ def bench_rssm_decode(dev, cycles: int, hbm: float, read_dtype: str):
     ms = e0.elapsed_time(e1) / nsteps
     ach = total / nsteps / (ms * 1e-3) / 1e9
     return {"read_copy": read_dtype, "seq_steps_per_s": S / (ms * 1e-3), "us_per_step": ms * 1e3,
-            "achieved_gbs": ach, "hbm_frac": ach / hbm, "bytes_per_step": total / nsteps, "steps": nsteps}
+            "achieved_gbs": ach, "hbm_frac": ach / hbm, "bytes_per_step": total / nsteps, "steps": nsteps,
+            "launches_per_step": 1}
 
 
 def bench_ssu(dev, steps: int, hbm: float):

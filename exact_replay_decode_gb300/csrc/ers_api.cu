@@ -239,7 +239,6 @@ ers_status ers_replay_decode(const ers_dims* dims, const ers_params* prm, const 
   ERS_TRY(check_params(prm));
   const bool rssm = (flags & ERS_FLAG_REPLAYSSM) != 0;
   if ((flags & ~(ERS_FLAG_FUSE_REFRESH | ERS_FLAG_REPLAYSSM)) != 0) return ERS_EINVAL;
-  if (rssm && (flags & ERS_FLAG_FUSE_REFRESH)) return ERS_EINVAL;
   ERS_TRY(check_cache(cache, rssm));
   if (nseq < 0) return ERS_EINVAL;
   if (nseq == 0) return ERS_OK;
@@ -257,7 +256,18 @@ ers_status ers_replay_decode(const ers_dims* dims, const ers_params* prm, const 
   a.flags = flags;
   a.y = y;
   a.status = dev_status;
-  if (ers::tc_supported(a.io, a.P, a.N, a.Q)) return finish(ers::tc_decode(a, (cudaStream_t)stream));
+  const bool tc = ers::tc_supported(a.io, a.P, a.N, a.Q);
+  if (rssm && (flags & ERS_FLAG_FUSE_REFRESH) && (tc || !ers::heads_decode_supported(a.P, a.N, a.Q))) {
+    // engines without the fused flush: the flush rule for one token (ers_refresh with T = 1), then
+    // the plain ReplaySSM decode; the warp-per-head kernel does both in one launch, same bits
+    LaunchArgs r = a;
+    r.flags = ERS_FLAG_REPLAYSSM;
+    r.T = 1;
+    const cudaError_t e = tc ? ers::tc_refresh(r, (cudaStream_t)stream) : ers::fma_refresh(r, (cudaStream_t)stream);
+    if (e != cudaSuccess) return finish(e);
+    a.flags = ERS_FLAG_REPLAYSSM;
+  }
+  if (tc) return finish(ers::tc_decode(a, (cudaStream_t)stream));
   return finish(ers::fma_decode(a, (cudaStream_t)stream));
 }
 

@@ -31,10 +31,15 @@ using namespace wh;
 //  * When the step fills the chunk, the state is streamed after the chunk's weights are known and
 //    each row is folded (fold_state) and written back in the same pass.
 
+// B and x rows: up to QM buffered rows plus the new token (a ReplaySSM flush holds L = Q committed
+// rows and the new token).
+template <int QM>
+constexpr int heads_rows() { return QM + 1; }
+
 template <typename T, int P, int N, int QM>
 constexpr size_t heads_smem_bytes() {
-  return (size_t)QM * N * sizeof(T) + (size_t)kHeadsPerCta * QM * P * sizeof(T) + QM * sizeof(float) +
-         (size_t)kHeadsPerCta * (P + QM * P) * sizeof(float);
+  return (size_t)heads_rows<QM>() * N * sizeof(T) + (size_t)kHeadsPerCta * heads_rows<QM>() * P * sizeof(T) +
+         QM * sizeof(float) + (size_t)kHeadsPerCta * (P + QM * P) * sizeof(float);
 }
 
 // Streams one head's state: lane j of row d reads elements [4j, 4j+4), 8 rows per block, two
@@ -50,10 +55,17 @@ __device__ __forceinline__ void unpack_row(typename Quad<HT>::raw r, float (&h)[
   }
 }
 
+// Rows of the stream in flight per warp: 16 fp32 rows, 32 rows of a bf16 or FP8 read copy (measured:
+// more FP8 rows than 32 spill registers and run slower).
+template <typename HT>
+constexpr int rows_in_flight() { return sizeof(typename Quad<HT>::raw) == 16 ? 16 : 32; }
+
 template <typename HT, int P, int N>
-__device__ __forceinline__ void stream_state(const HT* __restrict__ Hsrc, typename Quad<HT>::raw (&q)[16],
+__device__ __forceinline__ void stream_state(const HT* __restrict__ Hsrc,
+                                             typename Quad<HT>::raw (&q)[rows_in_flight<HT>()],
                                              const float (&c)[4], float* yo, int j, const float (&sc)[2]) {
-  constexpr int NBLK = P / 8;
+  constexpr int NBLK = P / 8, RIF = rows_in_flight<HT>();
+  static_assert(RIF % 16 == 0 && RIF <= P, "whole 16-row reduction groups in flight");
   float part[16];
 #pragma unroll
   for (int blk = 0; blk < NBLK; ++blk) {
@@ -62,9 +74,9 @@ __device__ __forceinline__ void stream_state(const HT* __restrict__ Hsrc, typena
     for (int r = 0; r < 8; ++r) {
       const int d = blk * 8 + r;
       float h[4];
-      unpack_row<HT>(q[sl + r], h);
+      unpack_row<HT>(q[d % RIF], h);
       part[sl + r] = Dot<N>::partial(c, h);
-      if (blk + 2 < NBLK) q[sl + r] = Quad<HT>::ld_stream(Hsrc + (size_t)(d + 16) * N + 4 * j);
+      if (d + RIF < P) q[d % RIF] = Quad<HT>::ld_stream(Hsrc + (size_t)(d + RIF) * N + 4 * j);
     }
     if (blk & 1) {
       float v = reduce_scatter16(part, j);   // row (blk - 1) * 8 + j / 2 on even lanes
@@ -154,6 +166,91 @@ __device__ __noinline__ void stream_state_refresh(float* __restrict__ Hd, __nv_b
   __syncwarp();
 }
 
+// ReplaySSM flush inside decode: each anchor row is folded with the h committed records in the same
+// order as stream_state_refresh (and the refresh kernels), written back, and cast into the read
+// copy (bf16, or FP8 codes with the row scale); the new token's dot product reads the cast values,
+// exactly as a decode after a separate refresh reads them from the copy.  An FP8 row's dot product
+// is scaled after the reduction (srow: lane j keeps the scale of the 16-row group's row j / 2).
+template <typename T, typename HT, int P, int N>
+__device__ __noinline__ void stream_flush_copy(float* __restrict__ Hd, HT* __restrict__ R, float* __restrict__ Rs,
+                                               float c0, float c1, float c2, float c3, float* yo, int j, int hc,
+                                               const float* wx, float decay, const T* sB) {
+  constexpr int NBLK = P / 8;
+  constexpr bool kF8 = std::is_same<HT, uint8_t>::value;
+  const float c[4] = {c0, c1, c2, c3};
+  float4 cur[8], nxt[8];
+#pragma unroll
+  for (int r = 0; r < 8; ++r) cur[r] = __ldcs(reinterpret_cast<const float4*>(Hd + (size_t)r * N + 4 * j));
+  float part[16];
+  float srow = 0.f;
+#pragma unroll 1
+  for (int blk = 0; blk < NBLK; ++blk) {
+    if (blk + 1 < NBLK) {
+#pragma unroll
+      for (int r = 0; r < 8; ++r)
+        nxt[r] = __ldcs(reinterpret_cast<const float4*>(Hd + (size_t)((blk + 1) * 8 + r) * N + 4 * j));
+    }
+    float pb[8];
+#pragma unroll
+    for (int hf = 0; hf < 2; ++hf) {
+      float acc[4][4];
+#pragma unroll
+      for (int r = 0; r < 4; ++r)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) acc[r][e] = 0.f;
+      for (int s = 0; s < hc; ++s) {
+        float bs[4];
+        lds4(sB + s * N + 4 * j, bs);
+        const float4 wv = *reinterpret_cast<const float4*>(wx + s * P + blk * 8 + 4 * hf);
+        const float wr[4] = {wv.x, wv.y, wv.z, wv.w};
+#pragma unroll
+        for (int r = 0; r < 4; ++r)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) acc[r][e] = __fmaf_rn(wr[r], bs[e], acc[r][e]);
+      }
+#pragma unroll
+      for (int r4 = 0; r4 < 4; ++r4) {
+        const int r = 4 * hf + r4;
+        float h[4], v[4], rv[4];
+        Quad<float>::unpack(cur[r], h);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) v[e] = __fmaf_rn(decay, h[e], acc[r4][e]);
+        const size_t o = (size_t)(blk * 8 + r) * N + 4 * j;
+        *reinterpret_cast<float4*>(Hd + o) = make_float4(v[0], v[1], v[2], v[3]);
+        if constexpr (kF8) {
+          float sr;
+          const uint32_t wq = fp8_quant_row(v, &sr);
+          *reinterpret_cast<uint32_t*>(R + o) = wq;
+          if (j == 0) Rs[blk * 8 + r] = sr;
+          if ((j >> 1) == (blk & 1) * 8 + r) srow = sr;
+          fp8_codes(wq, rv);
+        } else {
+          __nv_bfloat162 lo2 = __floats2bfloat162_rn(v[0], v[1]), hi2 = __floats2bfloat162_rn(v[2], v[3]);
+          uint2 u;
+          u.x = *reinterpret_cast<uint32_t*>(&lo2);
+          u.y = *reinterpret_cast<uint32_t*>(&hi2);
+          *reinterpret_cast<uint2*>(R + o) = u;
+          Quad<__nv_bfloat16>::unpack(u, rv);
+        }
+        pb[r] = Dot<N>::partial(c, rv);
+      }
+    }
+    if ((blk & 1) == 0) {
+#pragma unroll
+      for (int r = 0; r < 8; ++r) part[r] = pb[r];
+    } else {
+#pragma unroll
+      for (int r = 0; r < 8; ++r) part[8 + r] = pb[r];
+      float v = reduce_scatter16(part, j);
+      if constexpr (kF8) v = __fmul_rn(v, srow);
+      if ((j & 1) == 0) yo[(blk - 1) * 8 + (j >> 1)] = v;
+    }
+#pragma unroll
+    for (int r = 0; r < 8; ++r) cur[r] = nxt[r];
+  }
+  __syncwarp();
+}
+
 // Position advance inside the decode launch.  Every CTA of a slot adds 1 << 16 to pos[slot] once
 // all of its threads have read the position (the low 16 bits); the CTA that completes the count
 // (ncta CTAs per slot) stores the new position, which also clears the count.  No CTA of the slot can
@@ -175,9 +272,10 @@ __global__ void __launch_bounds__(kThreads, 2) k_decode_heads(LaunchArgs a) {
   static_assert(N == 128 && P % 32 == 0, "lane split of Dot<128>; 32-row reduction blocks");
   static_assert(QM <= 32, "one warp scans the chunk");
   extern __shared__ __align__(16) unsigned char hsm[];
-  T* sB = reinterpret_cast<T*>(hsm);                                  // [QM][N] group B rows 0..p
-  T* sxa = sB + QM * N;                                               // [warp][QM][P] x rows 0..p
-  float* sg = reinterpret_cast<float*>(sxa + kHeadsPerCta * QM * P);  // [QM] Gram row
+  constexpr int QR = heads_rows<QM>();
+  T* sB = reinterpret_cast<T*>(hsm);                                  // [QR][N] group B rows 0..p
+  T* sxa = sB + QR * N;                                               // [warp][QR][P] x rows 0..p
+  float* sg = reinterpret_cast<float*>(sxa + kHeadsPerCta * QR * P);  // [QM] Gram row
   float* syo = sg + QM;                                               // [warp][P] off-diagonal terms
   float* swa = syo + kHeadsPerCta * P;                                // [warp][QM][P] w_s x_s[d] (refresh)
   const int tid = threadIdx.x, w = tid >> 5, j = tid & 31;
@@ -203,17 +301,22 @@ __global__ void __launch_bounds__(kThreads, 2) k_decode_heads(LaunchArgs a) {
   const int ncta = a.G * nbl;   // CTAs that read this slot's position
   float c[4];
   load_k<T, 4>((const T*)a.C + (size_t)i * GN + (size_t)g * N + 4 * j, c);
-  typename Quad<HT>::raw q[16];
+  typename Quad<HT>::raw q[rows_in_flight<HT>()];
   if (active) {
 #pragma unroll
-    for (int r = 0; r < 16; ++r) q[r] = Quad<HT>::ld_stream(Hsrc + (size_t)r * N + 4 * j);
+    for (int r = 0; r < rows_in_flight<HT>(); ++r) q[r] = Quad<HT>::ld_stream(Hsrc + (size_t)r * N + 4 * j);
   }
-  if (p >= a.Q) {   // the same for every CTA of the slot: none of them counts, pos stays as it is
+  const bool fuse = (a.flags & ERS_FLAG_FUSE_REFRESH) != 0;
+  // ReplaySSM with a fused flush: a slot holding h = L committed records (h + 1 > L) first folds
+  // them into the anchor and recasts its read copy, then decodes the new token as record 0
+  const bool flush = !std::is_same<HT, float>::value && rssm && fuse && p == a.Q;
+  if (p > a.Q || (p == a.Q && !flush)) {   // the same for every CTA of the slot: none counts, pos stays
     if (tid == 0) report(a.status, ERS_EALIGN);
     return;
   }
-  // only exact mode (which streams the fp32 checkpoint) refreshes inside decode
-  const bool refresh = std::is_same<HT, float>::value && !rssm && (a.flags & ERS_FLAG_FUSE_REFRESH) && p + 1 == a.Q;
+  // exact mode (which streams the fp32 checkpoint) refreshes when the new token fills the chunk
+  const bool refresh = std::is_same<HT, float>::value && !rssm && fuse && p + 1 == a.Q;
+  const int o0 = flush ? p : 0, pn = p - o0;   // output rows s = 0..pn are smem rows o0 + s
   // buffer rows 0..p-1 and the new token as row p: the group's B rows, this head's x rows
   const T* bB = (const T*)a.bB + (size_t)slot * a.Q * GN + (size_t)g * N;
   const T* nB = (const T*)a.B + (size_t)i * GN + (size_t)g * N;
@@ -223,7 +326,7 @@ __global__ void __launch_bounds__(kThreads, 2) k_decode_heads(LaunchArgs a) {
     cp_async16(reinterpret_cast<char*>(sB + s * N) + 16 * e,
                reinterpret_cast<const char*>(s < p ? bB + s * GN : nB) + 16 * e);
   }
-  T* sx = sxa + w * QM * P;
+  T* sx = sxa + w * QR * P;
   const T* bx = (const T*)a.bx + (size_t)slot * a.Q * HP + (size_t)h * P;
   const T* nx = (const T*)a.x + (size_t)i * HP + (size_t)h * P;
   if (active)
@@ -232,30 +335,31 @@ __global__ void __launch_bounds__(kThreads, 2) k_decode_heads(LaunchArgs a) {
       cp_async16(reinterpret_cast<char*>(sx + s * P) + 16 * e,
                  reinterpret_cast<const char*>(s < p ? bx + s * HP : nx) + 16 * e);
     }
-  const float dt_raw = j <= p ? (j < p ? a.bdt[((size_t)slot * a.Q + j) * a.H + h] : a.dt[(size_t)i * a.H + h]) : 0.f;
+  const float dt_buf = j < p ? a.bdt[((size_t)slot * a.Q + j) * a.H + h] : 0.f;
+  const float dt_raw = j <= pn ? (o0 + j < p ? dt_buf : a.dt[(size_t)i * a.H + h]) : 0.f;
   float dl = 0.f;
   df v = {0.f, 0.f};
-  if (j <= p) {
+  if (j <= pn) {
     dl = delta_of(dt_raw, a.dt_bias[h]);
     v.hi = __fmul_rn(dl, a.A[h]);
   }
   // this head's log-decay prefix (lane s holds row s) and the group's Gram row, while the first
   // state rows are in flight
   v = warp_scan_df(v, j);
-  const df at = {__shfl_sync(kFull, v.hi, p), __shfl_sync(kFull, v.lo, p)};
+  const df at = {__shfl_sync(kFull, v.hi, pn), __shfl_sync(kFull, v.lo, pn)};
   cp_async_wait_all();
   __syncthreads();
-  if (tid == 0) advance_pos(&a.pos[slot], ncta, refresh ? 0 : p + 1);
-  for (int s = w; s <= p; s += kHeadsPerCta) {
+  if (tid == 0) advance_pos(&a.pos[slot], ncta, refresh ? 0 : pn + 1);
+  for (int s = w; s <= pn; s += kHeadsPerCta) {
     float bs[4];
-    lds4(sB + s * N + 4 * j, bs);
+    lds4(sB + (o0 + s) * N + 4 * j, bs);
     const float gv = Dot<N>::reduce(Dot<N>::partial(c, bs));
     if (j == 0) sg[s] = gv;
   }
   __syncthreads();
   if (!active) return;
   float M = 0.f;
-  if (j <= p) M = __fmul_rn(__fmul_rn(sg[j], dl), expf(df_diff(at, v)));
+  if (j <= pn) M = __fmul_rn(__fmul_rn(sg[j], dl), expf(df_diff(at, v)));
   float* yo = syo + w * P;
   if (refresh) {
     float* wx = swa + w * QM * P;
@@ -275,6 +379,28 @@ __global__ void __launch_bounds__(kThreads, 2) k_decode_heads(LaunchArgs a) {
       stream_state_refresh<T, P, N>(a.state + soff, Rd, nullptr, nullptr, c[0], c[1], c[2], c[3], yo, j, p, wx,
                                     expf(at.hi), sB);
     }
+  } else if (flush) {
+    // the committed records' weights (chunk_state's state_weights over rows 0..p-1) and decay
+    float* wx = swa + w * QM * P;
+    float dc = 0.f;
+    df vc = {0.f, 0.f};
+    if (j < p) {
+      dc = delta_of(dt_buf, a.dt_bias[h]);
+      vc.hi = __fmul_rn(dc, a.A[h]);
+    }
+    vc = warp_scan_df(vc, j);
+    const df last = {__shfl_sync(kFull, vc.hi, p - 1), __shfl_sync(kFull, vc.lo, p - 1)};
+    const float wl = j < p ? __fmul_rn(dc, expf(df_diff(last, vc))) : 0.f;
+    for (int s = 0; s < p; ++s) {
+      const float ws = __shfl_sync(kFull, wl, s);
+#pragma unroll
+      for (int m = 0; m < P / 32; ++m) wx[s * P + 32 * m + j] = __fmul_rn(ws, to_f(sx[s * P + 32 * m + j]));
+    }
+    __syncwarp();
+    if constexpr (!std::is_same<HT, float>::value)
+      stream_flush_copy<T, HT, P, N>(a.state + soff, (HT*)a.read_copy + soff,
+                                     a.read_scale + ((size_t)slot * a.H + h) * P, c[0], c[1], c[2], c[3], yo, j, p,
+                                     wx, expf(last.hi), sB);
   } else {
     stream_state<HT, P, N>(Hsrc, q, c, yo, j, sc);
   }
@@ -285,15 +411,15 @@ __global__ void __launch_bounds__(kThreads, 2) k_decode_heads(LaunchArgs a) {
   for (int k = 0; k < P / 32; ++k) {
     const int d = 32 * k + j;
     float acc = 0.f;
-    for (int s = 0; s <= p; ++s) acc = __fmaf_rn(__shfl_sync(kFull, M, s), to_f(sx[s * P + d]), acc);
+    for (int s = 0; s <= pn; ++s) acc = __fmaf_rn(__shfl_sync(kFull, M, s), to_f(sx[(o0 + s) * P + d]), acc);
     y[d] = from_f<T>(combine_out(et, yo[d], acc, Dh, to_f(sx[p * P + d])));
   }
   // append the new token to the buffer (B/C once per group)
-  T* dx = (T*)a.bx + ((size_t)slot * a.Q + p) * HP + (size_t)h * P;
+  T* dx = (T*)a.bx + ((size_t)slot * a.Q + pn) * HP + (size_t)h * P;
   for (int d = j; d < P; d += 32) dx[d] = sx[p * P + d];
-  if (j == 0) a.bdt[((size_t)slot * a.Q + p) * a.H + h] = a.dt[(size_t)i * a.H + h];
+  if (j == 0) a.bdt[((size_t)slot * a.Q + pn) * a.H + h] = a.dt[(size_t)i * a.H + h];
   if (hl == 0) {
-    const size_t dst = ((size_t)slot * a.Q + p) * GN + (size_t)g * N, src = (size_t)i * GN + (size_t)g * N;
+    const size_t dst = ((size_t)slot * a.Q + pn) * GN + (size_t)g * N, src = (size_t)i * GN + (size_t)g * N;
     for (int n = j; n < N; n += 32) {
       ((T*)a.bB)[dst + n] = sB[p * N + n];
       ((T*)a.bC)[dst + n] = ((const T*)a.C)[src + n];

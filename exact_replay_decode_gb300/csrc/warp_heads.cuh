@@ -116,12 +116,11 @@ __device__ __forceinline__ df warp_scan_df(df v, int j) {
   return v;
 }
 
-// ---- FP8 e4m3 read copy with one fp32 scale per state row ----------------------------------------
-// Row d of a head is held by the warp, lane j owning elements [4j, 4j+4).  Quantisation:
-// s = amax_n |S[d][n]| / 448 (IEEE division), q[n] = RNE_satfinite(S[d][n] / s), all-zero rows give
-// s = 0 and zero bytes; lane j's 4 codes form one 32-bit word, element 4j in the low byte.
-constexpr float kE4M3Max = 448.f;
-
+// ---- FP8 e4m3 read copy with one power-of-two scale per state row --------------------------------
+// Row d of a head is held by the warp, lane j owning elements [4j, 4j+4).  The row scale is s = 2^k,
+// k the smallest integer with amax_n |S[d][n]| <= 448 * 2^k (no code saturates), at least -127;
+// q[n] = RNE(S[d][n] / s) in e4m3 (an exact scaling, then one rounding); the value is q[n] * s.
+// Lane j's 4 codes form one 32-bit word, element 4j in the low byte.
 __device__ __forceinline__ uint32_t e4m3x2(float lo, float hi) {   // two codes, lo in the low byte
   uint16_t r;
   asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
@@ -133,11 +132,15 @@ __device__ __forceinline__ uint32_t fp8_quant_row(const float (&v)[4], float* sc
   float m = fmaxf(fmaxf(fabsf(v[0]), fabsf(v[1])), fmaxf(fabsf(v[2]), fabsf(v[3])));
 #pragma unroll
   for (int o = 16; o >= 1; o >>= 1) m = fmaxf(m, __shfl_xor_sync(kFull, m, o));
-  const float s = __fdiv_rn(m, kE4M3Max);
-  *scale = s;
-  if (s == 0.f) return 0u;
-  const float y0 = __fdiv_rn(v[0], s), y1 = __fdiv_rn(v[1], s), y2 = __fdiv_rn(v[2], s), y3 = __fdiv_rn(v[3], s);
-  return e4m3x2(y0, y1) | (e4m3x2(y2, y3) << 16);
+  // m = (1 + f) 2^(E - 127) for a normal m; 448 = 1.75 * 2^8, so k = E - 135 + (f > 0.75), i.e. the
+  // mantissa field above 0x600000; zero and subnormal maxima take k = -127
+  const uint32_t b = __float_as_uint(m);
+  const int E = (int)(b >> 23);
+  const int k = E == 0 ? -127 : max(E - 135 + ((b & 0x7FFFFFu) > 0x600000u ? 1 : 0), -127);
+  *scale = k == -127 ? __uint_as_float(0x00400000u) : __uint_as_float((uint32_t)(k + 127) << 23);
+  const float inv = __uint_as_float((uint32_t)(127 - k) << 23);   // 2^-k, a normal float for k >= -127
+  return e4m3x2(__fmul_rn(v[0], inv), __fmul_rn(v[1], inv)) |
+         (e4m3x2(__fmul_rn(v[2], inv), __fmul_rn(v[3], inv)) << 16);
 }
 
 // Lane quad of an FP8 row as code values q (exact in fp32).  Output streams apply the row scale to

@@ -279,11 +279,14 @@ def chunked_prefill(cache: ReplayCache, params: LayerParams, x, dt, B, C, cu_seq
 def replay_decode(cache: ReplayCache, params: LayerParams, x, dt, B, C, slot: Optional[torch.Tensor] = None,
                   fuse_refresh: bool = True, replayssm: bool = False, status: Optional[Status] = None,
                   check: bool = True, stream=None, out: Optional[torch.Tensor] = None) -> torch.Tensor:
-    """One exact-replay decode step per sequence (ers_replay_decode).  x [S,H,P], dt [S,H], B/C [S,G,N]."""
+    """One exact-replay decode step per sequence (ers_replay_decode).  x [S,H,P], dt [S,H], B/C [S,G,N].
+
+    fuse_refresh: exact mode refreshes a slot whose chunk fills in the same call; ReplaySSM mode
+    applies the one-token flush rule first (a slot at h = L is flushed, then decodes as record 0)."""
     S = x.shape[0]
     _tok_checks(cache, x, dt, B, C, (S,))
     y = torch.empty_like(x) if out is None else out
-    flags = (_abi.FLAG_REPLAYSSM if replayssm else (_abi.FLAG_FUSE_REFRESH if fuse_refresh else 0))
+    flags = (_abi.FLAG_REPLAYSSM if replayssm else 0) | (_abi.FLAG_FUSE_REFRESH if fuse_refresh else 0)
     st = status if status is not None else (Status(x.device) if check else None)
     code = _abi.lib().ers_replay_decode(ctypes.byref(cache.dims), ctypes.byref(params._c()), ctypes.byref(cache._c()),
                                         S, _slot_arg(slot, S), x.data_ptr(), dt.data_ptr(), B.data_ptr(),

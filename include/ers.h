@@ -111,9 +111,10 @@ typedef struct ers_params {
  *
  * FP8 read copy (ReplaySSM "Paper-reported results", the FP8-read / FP32-recurrence mode; the page
  * names the mode without its quantisation, so this library defines it): each state row (one d of
- * one head) is stored as e4m3 bytes q[n] = RNE_satfinite(S[d][n] / s) with the row scale
- * s = amax_n |S[d][n]| / 448 (IEEE fp32 division; an all-zero row stores s = 0 and zero bytes) and
- * read as q[n] * s (fp32).  Supported where the CUDA-core warp-per-head kernels run (headdim 64,
+ * one head) has a power-of-two scale s = 2^k, k the smallest integer with amax_n |S[d][n]| <= 448 * 2^k
+ * (no code saturates) and at least -127 (all-zero rows read as zeros); the row is stored as e4m3
+ * bytes q[n] = RNE(S[d][n] / s) and read as q[n] * s, both scalings exact.  Outputs apply s to the
+ * row's dot product with C.  Supported where the CUDA-core warp-per-head kernels run (headdim 64,
  * dstate 128, chunk <= 16; verify with at most 4 drafts and 8 heads per group); elsewhere calls
  * that read or write the copy return ERS_EUNSUPPORTED. */
 #define ERS_READ_BF16 0
@@ -191,9 +192,13 @@ ERS_API ers_status ers_chunked_prefill(const ers_dims* dims, const ers_params* p
  *   With ERS_FLAG_FUSE_REFRESH a slot that fills its chunk is refreshed in the same call (pos -> 0);
  *   without it pos reaches Q and ers_refresh(EXACT) must run before the next decode.  Both give
  *   identical bits.
- * ReplaySSM mode (ERS_FLAG_REPLAYSSM): requires 0 <= pos < L and a read copy; outputs read the read
- *   copy; no refresh happens here (ers_refresh applies the flush rule).
- * pos advances by one per call (or returns to 0 on a fused refresh); while the call runs, the
+ * ReplaySSM mode (ERS_FLAG_REPLAYSSM): requires a read copy; outputs read the read copy.  Without
+ *   ERS_FLAG_FUSE_REFRESH it requires 0 <= pos < L and never refreshes (ers_refresh applies the flush
+ *   rule).  With ERS_FLAG_FUSE_REFRESH it accepts 0 <= pos <= L and applies the flush rule for one
+ *   token first (pos + 1 > L: fold the L committed records into the anchor, recast the read copy,
+ *   pos = 0), so the new token always fits; identical bits to ers_refresh(ERS_FLAG_REPLAYSSM,
+ *   drafts_T = 1) followed by the decode without the flag.
+ * pos advances by one per call (or returns to 0, or 1 after a ReplaySSM flush); while the call runs, the
  * upper 16 bits of a slot's pos entry may hold a count of the kernel's own, cleared before it ends,
  * so no other work may read or write pos concurrently with the call.
  * Device errors: ERS_EALIGN (pos out of range), ERS_ESLOT. */

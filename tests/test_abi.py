@@ -105,7 +105,6 @@ def test_validation_rejects_bad_verify_and_commit_args(lib):
     assert lib.ers_commit(ctypes.byref(d), ctypes.byref(c), 5, None, FAKE, 4, 0, None, None) == 1  # nseq > nslots
     dec = lambda flags: lib.ers_replay_decode(ctypes.byref(d), ctypes.byref(p), ctypes.byref(c), 4, None, FAKE, FAKE,
                                               FAKE, FAKE, flags, FAKE, None, None)
-    assert dec(_abi.FLAG_REPLAYSSM | _abi.FLAG_FUSE_REFRESH) == 1
     assert dec(64) == 1
 
 
