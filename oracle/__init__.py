@@ -167,6 +167,63 @@ def fp8_rows_round(a: np.ndarray) -> np.ndarray:
     return q * s
 
 
+E2M1_MAX = 6.0
+
+
+def e2m1_round(a: np.ndarray) -> np.ndarray:
+    """Round fp32 values to the nearest FP4 e2m1 value (1 sign, 2 exponent bits with bias 1, 1
+    mantissa bit: magnitudes 0, 0.5, 1, 1.5, 2, 3, 4, 6), ties to the even mantissa, magnitudes
+    beyond 6 saturated to 6.  Returned as fp32 values."""
+    f = np.asarray(a, dtype=np.float32).astype(np.float64)
+    mag = np.abs(f)
+    _, e = np.frexp(mag)                          # floor(log2 mag) = e - 1
+    ex = np.maximum(e - 1, 0)                     # the subnormal 0.5 shares the quantum of [1, 2)
+    quantum = np.ldexp(1.0, ex - 1)
+    r = np.round(mag / quantum) * quantum         # halves to even: even multiples have mantissa 0
+    r = np.minimum(r, E2M1_MAX)
+    r = np.where(mag == 0, 0.0, r)
+    return (np.sign(f) * r).astype(np.float32)
+
+
+NVFP4_BLOCK = 16
+
+
+def nvfp4_row_scale_exponent(amax: np.ndarray) -> np.ndarray:
+    """k of an NVFP4 row scale s = 2**k: the smallest integer with amax <= 448 * 6 * 2**k (so no
+    block scale saturates), at least -127.  448 * 6 = 2688 = 0.65625 * 2**12."""
+    a = np.asarray(amax, dtype=np.float64)
+    m, e = np.frexp(a)
+    k = e.astype(np.int64) - 12 + (m > 0.65625)
+    return np.where(a < 2.0 ** -126, -127, np.maximum(k, -127))
+
+
+def nvfp4_rows_round(a: np.ndarray, parts: bool = False):
+    """NVFP4 read copy of an fp32 state (the last axis is dstate, a multiple of 16): FP4 e2m1 codes
+    in blocks of 16 consecutive values, each block with an e4m3 scale beta, each row with a
+    power-of-two scale s = 2**k (k from nvfp4_row_scale_exponent):
+        beta = e4m3(t / 6) with t = amax(|block|) / s (exact) and an fp32 division,
+        q    = e2m1((v / s) * rho), rho = 1 / beta (fp32 reciprocal, fp32 product); q = 0 if beta = 0,
+        value = q * beta * s (exact).
+    Input values are taken through fp32 as the GPU anchor is stored in fp32; returns fp64 values
+    (and, with parts=True, also q, beta and k)."""
+    f = np.ascontiguousarray(a, dtype=np.float32).astype(np.float64)
+    N = f.shape[-1]
+    k = nvfp4_row_scale_exponent(np.max(np.abs(f), axis=-1, keepdims=True))
+    s = np.ldexp(1.0, k)
+    fb = (f / s).reshape(f.shape[:-1] + (N // NVFP4_BLOCK, NVFP4_BLOCK))    # v / s, exact in fp64
+    fb32 = fb.astype(np.float32)                                              # rounds only below fp32 normal range
+    t = np.max(np.abs(fb32), axis=-1, keepdims=True).astype(np.float32)
+    beta = e4m3_round(t / np.float32(6.0))
+    with np.errstate(divide="ignore"):
+        rho = np.where(beta > 0, np.float32(1.0) / np.where(beta > 0, beta, np.float32(1.0)), np.float32(0.0))
+    y = (fb32 * rho.astype(np.float32)).astype(np.float32)
+    q = np.where(beta > 0, e2m1_round(y), np.float32(0.0))
+    val = (q.astype(np.float64) * beta.astype(np.float64)).reshape(f.shape) * s
+    if parts:
+        return val, q.reshape(f.shape), beta[..., 0], k[..., 0]
+    return val
+
+
 class _Seq:
     __slots__ = ("x", "dt", "B", "C")
 

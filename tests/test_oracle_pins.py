@@ -271,9 +271,9 @@ def test_thread_count_does_not_change_bits():
 
 # -- the ReplaySSM protocol model ------------------------------------------------------------------------
 
-def _protocol_case(seed, S=3, steps=9, T=4, L=16):
+def _protocol_case(seed, S=3, steps=9, T=4, L=16, N=4):
     rng = np.random.default_rng(seed)
-    H, G, P, N = 2, 1, 3, 4
+    H, G, P = 2, 1, 3
     params = synth.Params(-rng.uniform(0.2, 3.0, H).astype(np.float32), rng.standard_normal(H).astype(np.float32),
                           np.log(np.expm1(rng.uniform(1e-3, 1e-1, H))).astype(np.float32))
     anchor = rng.standard_normal((S, H, P, N))
@@ -412,13 +412,83 @@ def test_fp8_rows_round_error_bound_and_exact_codes():
     assert np.array_equal(oracle.e4m3_round((r / s).astype(np.float32)).astype(np.float64), r / s)
 
 
+def _e2m1_table():
+    """Every finite e2m1 value, decoded from the bit fields by the format's definition (bias 1;
+    exponent field 0 is subnormal: 0.5 * mantissa)."""
+    out = []
+    for code in range(16):
+        sgn = -1.0 if code & 8 else 1.0
+        e, m = (code >> 1) & 3, code & 1
+        v = 0.5 * m if e == 0 else (1 + 0.5 * m) * 2.0 ** (e - 1)
+        out.append((sgn * v, code))
+    return out
+
+
+def test_e2m1_round_fixes_every_code_and_matches_brute_force():
+    table = _e2m1_table()
+    vals = np.array([t[0] for t in table], np.float32)
+    assert sorted(set(np.abs(vals).tolist())) == [0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0]
+    assert np.array_equal(oracle.e2m1_round(vals), vals)
+    pos = [t for t in table if t[0] >= 0 and not (t[0] == 0 and t[1] == 8)]
+    pv = np.array([t[0] for t in pos])
+    pc = np.array([t[1] for t in pos])
+    x = np.concatenate([np.linspace(0, 7.9, 4001), (pv[:-1] + pv[1:]) / 2])      # a grid plus every tie
+    got = oracle.e2m1_round(x.astype(np.float32)).astype(np.float64)
+    for xi, gi in zip(x, got):
+        d = np.abs(pv - xi)
+        best = np.nonzero(d == d.min())[0]
+        want = min(6.0, pv[best[np.argmin(pc[best] & 1)]] if len(best) > 1 else pv[best[0]])  # tie: even mantissa
+        if xi > 6.0:
+            want = 6.0                                                                   # saturation
+        assert gi == want, (xi, gi, want)
+    assert np.array_equal(oracle.e2m1_round(-x.astype(np.float32)), -oracle.e2m1_round(x.astype(np.float32)))
+
+
+def test_nvfp4_scales_and_hand_worked_values():
+    # row scale: amax = 2688 -> k = 0; 6 -> -8 (2688 * 2^-9 = 5.25 < 6 <= 10.5); 1.0 -> -11; zero -> -127
+    got = oracle.nvfp4_row_scale_exponent(np.array([2688.0, 6.0, 1.0, 0.0, float(np.nextafter(np.float32(2688), np.float32(1e9)))]))
+    assert list(got) == [0, -8, -11, -127, 1]
+    # block [1.0, 0.3, 0...] (row max 1.0): s = 2^-11; t = 2048; beta = e4m3(341.33) = 352 (step 32);
+    # 1.0 -> 2048/352 = 5.82 -> e2m1 6 -> 6 * 352 / 2048 = 1.03125; 0.3 -> 1.745 -> 1.5 -> 0.2578125
+    r, q, beta, k = oracle.nvfp4_rows_round(np.array([[1.0, 0.3] + [0.0] * 14]), parts=True)
+    assert list(r[0, :3]) == [1.03125, 0.2578125, 0.0] and beta[0, 0] == 352 and k[0] == -11
+    # a row whose values are e2m1 values with maximum 6 reads back exactly (s = 2^-8, beta = 256)
+    e2 = np.array([6, -4, 3, 1.5, 0.5, 0, -6, 2, 1, -3, 4, 0.5, -1.5, 2, 6, -0.5] * 8, np.float64)[None]
+    assert np.array_equal(oracle.nvfp4_rows_round(e2), e2)
+    # a block far below its row's maximum: its beta underflows to 0 and it reads as zeros
+    row = np.zeros((1, 32)); row[0, 0] = 1000.0; row[0, 16:] = 1e-6
+    assert np.all(oracle.nvfp4_rows_round(row)[0, 16:] == 0)
+    assert np.all(oracle.nvfp4_rows_round(np.zeros((2, 32))) == 0)
+
+
+def test_nvfp4_values_are_codes_times_scales_within_bound():
+    rng = np.random.Generator(np.random.PCG64(12))
+    a = rng.standard_normal((3, 4, 16, 128)) * np.exp(rng.uniform(-8, 8, (3, 4, 16, 1)))
+    r, q, beta, k = oracle.nvfp4_rows_round(a, parts=True)
+    f = a.astype(np.float32).astype(np.float64)
+    s = np.exp2(k.astype(np.float64))[..., None]
+    qb = q.reshape(q.shape[:-1] + (8, 16)).astype(np.float64)
+    assert np.array_equal(oracle.e2m1_round(q), q)                                   # codes are e2m1 values
+    assert np.array_equal(oracle.e4m3_round(beta), beta)                             # block scales are e4m3
+    assert np.array_equal((qb * beta[..., None]).reshape(f.shape) * s, r)
+    # error: e2m1 rounding (half a step: 1/4 relative, 1/4 of beta*s absolute in the subnormal step)
+    # plus the block-scale rounding that can push a block's maximum into saturation (2^-4 relative)
+    fb = f.reshape(f.shape[:-1] + (8, 16))
+    amax_b = np.abs(fb).max(axis=-1, keepdims=True)
+    bs = (beta[..., None] * s[..., None])
+    err = np.abs(r.reshape(fb.shape) - fb)
+    assert np.all(err <= 0.25 * np.abs(fb) + 0.25 * bs + 2.0 ** -4 * amax_b * 1.01)
+
+
 def test_protocol_anchor_independent_of_fp8_read_copy():
-    """The fp32 anchor is the same whether outputs read a bf16 or an FP8 copy."""
-    params, anchor, drafts, acc, L = _protocol_case(17, steps=12)
+    """The fp32 anchor is the same whether outputs read a bf16, an FP8 or an NVFP4 copy."""
+    params, anchor, drafts, acc, L = _protocol_case(17, steps=12, N=32)   # two 16-value blocks per row
     m1 = oracle.ReplaySSMModel(params, anchor, L)
     m2 = oracle.ReplaySSMModel(params, anchor, L, read_cast=oracle.fp8_rows_round)
+    m3 = oracle.ReplaySSMModel(params, anchor, L, read_cast=oracle.nvfp4_rows_round)
     for k in range(len(drafts)):
         y1 = m1.verify(drafts[k]); m1.commit(acc[k])
         y2 = m2.verify(drafts[k]); m2.commit(acc[k])
-    assert m1.flushes > 0 and np.array_equal(m1.anchor, m2.anchor)
-    assert not np.array_equal(y1, y2)
+        y3 = m3.verify(drafts[k]); m3.commit(acc[k])
+    assert m1.flushes > 0 and np.array_equal(m1.anchor, m2.anchor) and np.array_equal(m1.anchor, m3.anchor)
+    assert not np.array_equal(y1, y2) and not np.array_equal(y2, y3)
