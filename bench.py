@@ -371,6 +371,17 @@ def bench_prefill(dev, name: str, iters: int, warmup: int, hbm: float, tc: float
             "tflops": PREFILL_FLOPS[name] / (ms * 1e-3) / 1e12, "l2": "flushed before each call"}
 
 
+def _copy_bytes(d, read_dtype: str) -> int:
+    """Bytes of one sequence's read copy: bf16 values; FP8 codes + an fp32 scale per row; NVFP4
+    codes (half a byte per value) + an e4m3 scale per 16 values + an fp32 scale per row."""
+    rows = d.nheads * d.headdim
+    if read_dtype == "bf16":
+        return rows * d.dstate * 2
+    if read_dtype == "fp8":
+        return rows * (d.dstate + 4)
+    return rows * (d.dstate // 2 + d.dstate // 16 + 4)
+
+
 def bench_verify(dev, steps: int, hbm: float, read_dtype: str = "bf16"):
     import torch
     import exact_replay_decode_gb300 as ers
@@ -389,8 +400,7 @@ def bench_verify(dev, steps: int, hbm: float, read_dtype: str = "bf16"):
     cache.state.copy_(fin)
     ers.refresh(cache, prm, replayssm=True, drafts_T=L + 1)
     # read copy per sequence: bf16 values, or FP8 codes + one fp32 scale per state row
-    copy_bytes = d.nheads * d.headdim * d.dstate * 2 if read_dtype == "bf16" else \
-        d.nheads * d.headdim * (d.dstate + 4)
+    copy_bytes = _copy_bytes(d, read_dtype)
     dx, ddt, dB, dC = torch_io.tokens_to(drafts, dev, lead=(steps, S, T))
     acc_t = torch.from_numpy(acc).to(dev)
     y = torch.empty(S, T, d.nheads, d.headdim, dtype=torch.bfloat16, device=dev)
@@ -464,7 +474,7 @@ def bench_rssm_decode(dev, cycles: int, hbm: float, read_dtype: str):
     # algorithmic bytes from the run's own pointers: a flush reads and writes the anchor, reads the
     # h buffered rows and writes the copy; a decode reads the copy, h rows and the new token, writes
     # the token to the buffer and y
-    copy_bytes = d.nheads * d.headdim * d.dstate * 2 if read_dtype == "bf16" else d.nheads * d.headdim * (d.dstate + 4)
+    copy_bytes = _copy_bytes(d, read_dtype)
     hs = h0.astype(np.int64)
 
     def cycle_bytes():
@@ -644,12 +654,13 @@ def main(argv=None):
         if args.section == "prefill":
             out = {n: bench_prefill(dev, n, 10, args.warmup, hbm, tc) for n in ("prefill_2048_h32", "varlen_4seq_h64")}
         elif args.section == "rssm":
-            out = {r: bench_rssm_decode(dev, 4, hbm, r) for r in ("bf16", "fp8")}
+            out = {r: bench_rssm_decode(dev, 4, hbm, r) for r in ("bf16", "fp8", "nvfp4")}
         elif args.section == "verify":
             out = bench_verify(dev, 32, hbm)
             fp8 = bench_verify(dev, 32, hbm, "fp8")
+            nv4 = bench_verify(dev, 32, hbm, "nvfp4")
             if rank == 0:
-                print(json.dumps({"verify_fp8": fp8}))
+                print(json.dumps({"verify_fp8": fp8, "verify_nvfp4": nv4}))
         else:
             out = bench_ssu(dev, 16, hbm)
         if rank == 0:
@@ -673,7 +684,8 @@ def main(argv=None):
         extra["prefill"] = {n: bench_prefill(dev, n, 10, 3, hbm, tc) for n in ("prefill_2048_h32", "varlen_4seq_h64")}
         extra["verify"] = bench_verify(dev, 32, hbm)
         extra["verify_fp8"] = bench_verify(dev, 32, hbm, "fp8")
-        extra["replayssm_decode"] = {r: bench_rssm_decode(dev, 4, hbm, r) for r in ("bf16", "fp8")}
+        extra["verify_nvfp4"] = bench_verify(dev, 32, hbm, "nvfp4")
+        extra["replayssm_decode"] = {r: bench_rssm_decode(dev, 4, hbm, r) for r in ("bf16", "fp8", "nvfp4")}
         extra["ssu"] = bench_ssu(dev, 16, hbm)
     line = {
         "metric": "replay-decode seq-steps/s per layer @B=256",

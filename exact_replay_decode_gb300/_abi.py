@@ -26,6 +26,7 @@ FLAG_AUTO_FLUSH = 4
 
 READ_BF16 = 0
 READ_FP8_E4M3 = 1
+READ_NVFP4 = 2
 
 # Every function include/ers.h declares.
 EXPORTS = (
@@ -54,7 +55,7 @@ class Cache(ctypes.Structure):
     _fields_ = [("state", ctypes.c_void_p), ("read_copy", ctypes.c_void_p), ("buf_x", ctypes.c_void_p),
                 ("buf_dt", ctypes.c_void_p), ("buf_B", ctypes.c_void_p), ("buf_C", ctypes.c_void_p),
                 ("pos", ctypes.c_void_p), ("nslots", ctypes.c_int32), ("read_dtype", ctypes.c_int32),
-                ("read_scale", ctypes.c_void_p)]
+                ("read_scale", ctypes.c_void_p), ("read_block_scale", ctypes.c_void_p)]
 
 
 _lib = None

@@ -44,18 +44,21 @@ ers_status check_params(const ers_params* p) {
 
 ers_status check_state_ptrs(const ers_cache* c) { return check_ptr(c->state, true); }
 
-// FP8 read copies are implemented by the CUDA-core warp-per-head kernels only.
-bool fp8_read_shape(const ers_dims* d) {
+// FP8 and NVFP4 read copies are implemented by the CUDA-core warp-per-head kernels only.
+bool narrow_read_shape(const ers_dims* d) {
   return d->headdim == 64 && d->dstate == 128 && d->chunk >= 1 && d->chunk <= 16;
 }
-bool has_fp8_copy(const ers_cache* c) { return c->read_copy != nullptr && c->read_dtype == ERS_READ_FP8_E4M3; }
+bool has_narrow_copy(const ers_cache* c) { return c->read_copy != nullptr && c->read_dtype != ERS_READ_BF16; }
+bool has_nvfp4_copy(const ers_cache* c) { return c->read_copy != nullptr && c->read_dtype == ERS_READ_NVFP4; }
 
 ers_status check_cache(const ers_cache* c, bool need_read_copy) {
   if (c == nullptr || c->nslots < 0) return ERS_EINVAL;
-  if (c->read_dtype != ERS_READ_BF16 && c->read_dtype != ERS_READ_FP8_E4M3) return ERS_EDTYPE;
+  if (c->read_dtype != ERS_READ_BF16 && c->read_dtype != ERS_READ_FP8_E4M3 && c->read_dtype != ERS_READ_NVFP4)
+    return ERS_EDTYPE;
   ERS_TRY(check_state_ptrs(c));
   ERS_TRY(check_ptr(c->read_copy, need_read_copy));
-  if (c->read_dtype == ERS_READ_FP8_E4M3 && c->read_copy != nullptr) ERS_TRY(check_ptr(c->read_scale, true));
+  if (c->read_dtype != ERS_READ_BF16 && c->read_copy != nullptr) ERS_TRY(check_ptr(c->read_scale, true));
+  if (c->read_dtype == ERS_READ_NVFP4 && c->read_copy != nullptr) ERS_TRY(check_ptr(c->read_block_scale, true));
   ERS_TRY(check_ptr(c->buf_x, true));
   ERS_TRY(check_ptr(c->buf_dt, true));
   ERS_TRY(check_ptr(c->buf_B, true));
@@ -85,7 +88,9 @@ void set_cache(LaunchArgs& a, const ers_cache* c) {
   a.state = c->state;
   a.read_copy = c->read_copy;
   a.read_fp8 = c->read_copy != nullptr && c->read_dtype == ERS_READ_FP8_E4M3;
+  a.read_nvfp4 = c->read_copy != nullptr && c->read_dtype == ERS_READ_NVFP4;
   a.read_scale = c->read_scale;
+  a.read_bscale = c->read_block_scale;
   a.bx = c->buf_x;
   a.bdt = c->buf_dt;
   a.bB = c->buf_B;
@@ -247,7 +252,8 @@ ers_status ers_replay_decode(const ers_dims* dims, const ers_params* prm, const 
   ERS_TRY(check_tokens(x, dt, B, C, true));
   ERS_TRY(check_ptr(y, true));
   ERS_TRY(check_ptr(dev_status, false));
-  if (has_fp8_copy(cache) && !fp8_read_shape(dims)) return ERS_EUNSUPPORTED;
+  if (has_narrow_copy(cache) && !narrow_read_shape(dims)) return ERS_EUNSUPPORTED;
+  if (has_nvfp4_copy(cache) && !rssm) return ERS_EUNSUPPORTED;   // NVFP4 copies: ReplaySSM mode only
   LaunchArgs a = base_args(dims, prm);
   set_cache(a, cache);
   a.x = x; a.dt = dt; a.B = B; a.C = C;
@@ -283,7 +289,8 @@ ers_status ers_refresh(const ers_dims* dims, const ers_params* prm, const ers_ca
   if (slot == nullptr && nseq > cache->nslots) return ERS_EINVAL;
   ERS_TRY(check_ptr(slot, false));
   ERS_TRY(check_ptr(dev_status, false));
-  if (has_fp8_copy(cache) && !fp8_read_shape(dims)) return ERS_EUNSUPPORTED;
+  if (has_narrow_copy(cache) && !narrow_read_shape(dims)) return ERS_EUNSUPPORTED;
+  if (has_nvfp4_copy(cache) && !(flags & ERS_FLAG_REPLAYSSM)) return ERS_EUNSUPPORTED;
   LaunchArgs a = base_args(dims, prm);
   set_cache(a, cache);
   a.slot = slot;
@@ -309,7 +316,7 @@ ers_status ers_spec_verify(const ers_dims* dims, const ers_params* prm, const er
   ERS_TRY(check_tokens(x, dt, B, C, true));
   ERS_TRY(check_ptr(y, true));
   ERS_TRY(check_ptr(dev_status, false));
-  if (has_fp8_copy(cache) && !(fp8_read_shape(dims) && ers::heads_verify_supported(dims->headdim, dims->dstate,
+  if (has_narrow_copy(cache) && !(narrow_read_shape(dims) && ers::heads_verify_supported(dims->headdim, dims->dstate,
                                                                                        dims->chunk, T, dims->nheads,
                                                                                        dims->ngroups)))
     return ERS_EUNSUPPORTED;

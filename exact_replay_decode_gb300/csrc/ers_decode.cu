@@ -42,27 +42,20 @@ constexpr size_t heads_smem_bytes() {
          QM * sizeof(float) + (size_t)kHeadsPerCta * (P + QM * P) * sizeof(float);
 }
 
-// Streams one head's state: lane j of row d reads elements [4j, 4j+4), 8 rows per block, two
-// blocks in flight (q holds rows 0..15 on entry).  yo[d] ends with the off-diagonal term (H C_p)[d]
-// (per-warp shared memory).  An FP8 copy is read as codes; each row's dot product is then scaled by
-// the row scale, which lane d % 32 holds in sc[d / 32].
-template <typename HT>
-__device__ __forceinline__ void unpack_row(typename Quad<HT>::raw r, float (&h)[4]) {
-  if constexpr (std::is_same<HT, uint8_t>::value) {
-    fp8_codes(r, h);
-  } else {
-    Quad<HT>::unpack(r, h);
-  }
-}
+// Streams one head's state: lane j of row d reads elements [4j, 4j+4), 8 rows per block, with
+// rows_in_flight rows in flight (q holds the first of them on entry).  yo[d] ends with the
+// off-diagonal term (H C_p)[d] (per-warp shared memory).  FP8 and NVFP4 copies are read as codes:
+// an NVFP4 lane partial is scaled by its block scale, and each row's dot product by the row scale,
+// which lane d % 32 holds in sc[d / 32].
 
-// Rows of the stream in flight per warp: 16 fp32 rows, 32 rows of a bf16 or FP8 read copy (measured:
-// more FP8 rows than 32 spill registers and run slower).
+// Rows of the stream in flight per warp: 16 fp32 rows, 32 rows of a read copy (measured: more FP8
+// rows than 32 spill registers and run slower).
 template <typename HT>
-constexpr int rows_in_flight() { return sizeof(typename Quad<HT>::raw) == 16 ? 16 : 32; }
+constexpr int rows_in_flight() { return sizeof(typename RawOf<HT>::type) == 16 ? 16 : 32; }
 
 template <typename HT, int P, int N>
-__device__ __forceinline__ void stream_state(const HT* __restrict__ Hsrc,
-                                             typename Quad<HT>::raw (&q)[rows_in_flight<HT>()],
+__device__ __forceinline__ void stream_state(const RowSrc<HT, N>& src,
+                                             typename RawOf<HT>::type (&q)[rows_in_flight<HT>()],
                                              const float (&c)[4], float* yo, int j, const float (&sc)[2]) {
   constexpr int NBLK = P / 8, RIF = rows_in_flight<HT>();
   static_assert(RIF % 16 == 0 && RIF <= P, "whole 16-row reduction groups in flight");
@@ -73,14 +66,16 @@ __device__ __forceinline__ void stream_state(const HT* __restrict__ Hsrc,
 #pragma unroll
     for (int r = 0; r < 8; ++r) {
       const int d = blk * 8 + r;
-      float h[4];
-      unpack_row<HT>(q[d % RIF], h);
-      part[sl + r] = Dot<N>::partial(c, h);
-      if (d + RIF < P) q[d % RIF] = Quad<HT>::ld_stream(Hsrc + (size_t)(d + RIF) * N + 4 * j);
+      float h[4], ls;
+      row_values<HT>(q[d % RIF], h, &ls);
+      float pp = Dot<N>::partial(c, h);
+      if constexpr (kLaneScale<HT>) pp = __fmul_rn(pp, ls);
+      part[sl + r] = pp;
+      if (d + RIF < P) q[d % RIF] = src.ld(d + RIF, j);
     }
     if (blk & 1) {
       float v = reduce_scatter16(part, j);   // row (blk - 1) * 8 + j / 2 on even lanes
-      if constexpr (std::is_same<HT, uint8_t>::value)
+      if constexpr (kRowScale<HT>)
         v = __fmul_rn(v, __shfl_sync(kFull, sc[((blk - 1) * 8) >> 5], ((blk - 1) * 8 + (j >> 1)) & 31));
       if ((j & 1) == 0) yo[(blk - 1) * 8 + (j >> 1)] = v;
     }
@@ -168,15 +163,17 @@ __device__ __noinline__ void stream_state_refresh(float* __restrict__ Hd, __nv_b
 
 // ReplaySSM flush inside decode: each anchor row is folded with the h committed records in the same
 // order as stream_state_refresh (and the refresh kernels), written back, and cast into the read
-// copy (bf16, or FP8 codes with the row scale); the new token's dot product reads the cast values,
-// exactly as a decode after a separate refresh reads them from the copy.  An FP8 row's dot product
-// is scaled after the reduction (srow: lane j keeps the scale of the 16-row group's row j / 2).
+// copy (bf16, FP8 or NVFP4); the new token's dot product reads the cast values, exactly as a decode
+// after a separate refresh reads them from the copy.  FP8 / NVFP4 rows' dot products are scaled
+// after the reduction (srow: lane j keeps the scale of the 16-row group's row j / 2).
 template <typename T, typename HT, int P, int N>
-__device__ __noinline__ void stream_flush_copy(float* __restrict__ Hd, HT* __restrict__ R, float* __restrict__ Rs,
-                                               float c0, float c1, float c2, float c3, float* yo, int j, int hc,
-                                               const float* wx, float decay, const T* sB) {
+__device__ __noinline__ void stream_flush_copy(float* __restrict__ Hd, void* __restrict__ R, uint8_t* __restrict__ Rb,
+                                               float* __restrict__ Rs, float c0, float c1, float c2, float c3,
+                                               float* yo, int j, int hc, const float* wx, float decay,
+                                               const T* sB) {
   constexpr int NBLK = P / 8;
   constexpr bool kF8 = std::is_same<HT, uint8_t>::value;
+  constexpr bool kNv = std::is_same<HT, Nvfp4>::value;
   const float c[4] = {c0, c1, c2, c3};
   float4 cur[8], nxt[8];
 #pragma unroll
@@ -217,10 +214,15 @@ __device__ __noinline__ void stream_flush_copy(float* __restrict__ Hd, HT* __res
         for (int e = 0; e < 4; ++e) v[e] = __fmaf_rn(decay, h[e], acc[r4][e]);
         const size_t o = (size_t)(blk * 8 + r) * N + 4 * j;
         *reinterpret_cast<float4*>(Hd + o) = make_float4(v[0], v[1], v[2], v[3]);
-        if constexpr (kF8) {
+        float ls = 1.f;
+        if constexpr (kNv) {
+          float sr;
+          nvfp4_store_row<N>(v, (uint8_t*)R, Rb, Rs, blk * 8 + r, j, rv, &ls, &sr);
+          if ((j >> 1) == (blk & 1) * 8 + r) srow = sr;
+        } else if constexpr (kF8) {
           float sr;
           const uint32_t wq = fp8_quant_row(v, &sr);
-          *reinterpret_cast<uint32_t*>(R + o) = wq;
+          *reinterpret_cast<uint32_t*>((uint8_t*)R + o) = wq;
           if (j == 0) Rs[blk * 8 + r] = sr;
           if ((j >> 1) == (blk & 1) * 8 + r) srow = sr;
           fp8_codes(wq, rv);
@@ -229,10 +231,11 @@ __device__ __noinline__ void stream_flush_copy(float* __restrict__ Hd, HT* __res
           uint2 u;
           u.x = *reinterpret_cast<uint32_t*>(&lo2);
           u.y = *reinterpret_cast<uint32_t*>(&hi2);
-          *reinterpret_cast<uint2*>(R + o) = u;
+          *reinterpret_cast<uint2*>((__nv_bfloat16*)R + o) = u;
           Quad<__nv_bfloat16>::unpack(u, rv);
         }
         pb[r] = Dot<N>::partial(c, rv);
+        if constexpr (kNv) pb[r] = __fmul_rn(pb[r], ls);
       }
     }
     if ((blk & 1) == 0) {
@@ -242,7 +245,7 @@ __device__ __noinline__ void stream_flush_copy(float* __restrict__ Hd, HT* __res
 #pragma unroll
       for (int r = 0; r < 8; ++r) part[8 + r] = pb[r];
       float v = reduce_scatter16(part, j);
-      if constexpr (kF8) v = __fmul_rn(v, srow);
+      if constexpr (kF8 || kNv) v = __fmul_rn(v, srow);
       if ((j & 1) == 0) yo[(blk - 1) * 8 + (j >> 1)] = v;
     }
 #pragma unroll
@@ -290,9 +293,15 @@ __global__ void __launch_bounds__(kThreads, 2) k_decode_heads(LaunchArgs a) {
   const bool rssm = (a.flags & ERS_FLAG_REPLAYSSM) != 0;
   const size_t HP = (size_t)a.H * P, GN = (size_t)a.G * N;
   const size_t soff = ((size_t)slot * a.H + h) * P * N;
-  const HT* Hsrc = rssm ? (const HT*)a.read_copy + soff : (const HT*)(a.state + soff);
-  float sc[2] = {0.f, 0.f};   // FP8 read copy: scales of rows j and 32 + j
-  if constexpr (std::is_same<HT, uint8_t>::value) {
+  RowSrc<HT, N> src;
+  if constexpr (std::is_same<HT, Nvfp4>::value) {
+    src.c4 = (const uint8_t*)a.read_copy + soff / 2;
+    src.bs = a.read_bscale + soff / 16;
+  } else {
+    src.p = rssm ? (const HT*)a.read_copy + soff : (const HT*)(a.state + soff);
+  }
+  float sc[2] = {0.f, 0.f};   // FP8 / NVFP4 read copy: scales of rows j and 32 + j
+  if constexpr (kRowScale<HT>) {
     const float* Rs = a.read_scale + ((size_t)slot * a.H + h) * P;
     sc[0] = Rs[j];
     sc[1] = Rs[32 + j];
@@ -301,10 +310,10 @@ __global__ void __launch_bounds__(kThreads, 2) k_decode_heads(LaunchArgs a) {
   const int ncta = a.G * nbl;   // CTAs that read this slot's position
   float c[4];
   load_k<T, 4>((const T*)a.C + (size_t)i * GN + (size_t)g * N + 4 * j, c);
-  typename Quad<HT>::raw q[rows_in_flight<HT>()];
+  typename RawOf<HT>::type q[rows_in_flight<HT>()];
   if (active) {
 #pragma unroll
-    for (int r = 0; r < rows_in_flight<HT>(); ++r) q[r] = Quad<HT>::ld_stream(Hsrc + (size_t)r * N + 4 * j);
+    for (int r = 0; r < rows_in_flight<HT>(); ++r) q[r] = src.ld(r, j);
   }
   const bool fuse = (a.flags & ERS_FLAG_FUSE_REFRESH) != 0;
   // ReplaySSM with a fused flush: a slot holding h = L committed records (h + 1 > L) first folds
@@ -398,11 +407,13 @@ __global__ void __launch_bounds__(kThreads, 2) k_decode_heads(LaunchArgs a) {
     }
     __syncwarp();
     if constexpr (!std::is_same<HT, float>::value)
-      stream_flush_copy<T, HT, P, N>(a.state + soff, (HT*)a.read_copy + soff,
-                                     a.read_scale + ((size_t)slot * a.H + h) * P, c[0], c[1], c[2], c[3], yo, j, p,
-                                     wx, expf(last.hi), sB);
+      stream_flush_copy<T, HT, P, N>(a.state + soff,
+                                     std::is_same<HT, Nvfp4>::value ? (void*)((uint8_t*)a.read_copy + soff / 2)
+                                                                    : (void*)((HT*)a.read_copy + soff),
+                                     a.read_bscale + soff / 16, a.read_scale + ((size_t)slot * a.H + h) * P, c[0],
+                                     c[1], c[2], c[3], yo, j, p, wx, expf(last.hi), sB);
   } else {
-    stream_state<HT, P, N>(Hsrc, q, c, yo, j, sc);
+    stream_state<HT, P, N>(src, q, c, yo, j, sc);
   }
   // outputs d = 32k + j
   const float et = expf(at.hi), Dh = a.D[h];
@@ -443,18 +454,21 @@ cudaError_t launch_decode_heads(const LaunchArgs& a, cudaStream_t s) {
     if (a.read_fp8)
       return rssm ? run(k_decode_heads<T, uint8_t, true, P, N, QM>) : run(k_decode_heads<T, float, true, P, N, QM>);
   }
-  if (a.read_fp8) return cudaErrorNotSupported;
+  if constexpr (QM <= 16) {   // NVFP4 read copies: ReplaySSM mode, chunk <= 16 (checked by the API)
+    if (a.read_nvfp4 && rssm) return run(k_decode_heads<T, Nvfp4, false, P, N, QM>);
+  }
+  if (a.read_fp8 || a.read_nvfp4) return cudaErrorNotSupported;
   return rssm ? run(k_decode_heads<T, __nv_bfloat16, false, P, N, QM>) : run(k_decode_heads<T, float, false, P, N, QM>);
 }
 
-// ---- FP8 read-copy recast for ers_refresh -------------------------------------------------------------
+// ---- FP8 / NVFP4 read-copy recast for ers_refresh ------------------------------------------------------
 // After the refresh kernel has folded a slot's anchor (or left it unchanged for an empty history),
-// the slot's FP8 read copy is cast from the fp32 anchor as stored, i.e. from the same unrounded
-// values ("Core equations": both copies are cast independently from one state).  Same slot
-// predicate as the refresh kernel; runs before the position is reset.  Warp w casts rows
+// the slot's FP8 or NVFP4 read copy is cast from the fp32 anchor as stored, i.e. from the same
+// unrounded values ("Core equations": both copies are cast independently from one state).  Same
+// slot predicate as the refresh kernel; runs before the position is reset.  Warp w casts rows
 // [8w, 8w + 8) of head blockIdx.y, one row per pass.
-template <int P, int N>
-__global__ void __launch_bounds__(kThreads) k_recast_fp8(LaunchArgs a) {
+template <typename HT, int P, int N>
+__global__ void __launch_bounds__(kThreads) k_recast(LaunchArgs a) {
   const int i = blockIdx.x, h = blockIdx.y;
   const int slot = a.slot != nullptr ? a.slot[i] : i;
   if (slot < 0 || slot >= a.nslots) return;   // reported by the refresh kernel
@@ -464,14 +478,18 @@ __global__ void __launch_bounds__(kThreads) k_recast_fp8(LaunchArgs a) {
   if (!(rssm ? (p + a.T > a.Q) : (p == a.Q))) return;
   const int w = threadIdx.x >> 5, j = threadIdx.x & 31;
   const size_t soff = ((size_t)slot * a.H + h) * P * N;
-  uint8_t* R8 = (uint8_t*)a.read_copy + soff;
   float* Rs = a.read_scale + ((size_t)slot * a.H + h) * P;
 #pragma unroll
   for (int r = 0; r < P / kHeadsPerCta; ++r) {
     const int d = (P / kHeadsPerCta) * w + r;
     const float4 u = *reinterpret_cast<const float4*>(a.state + soff + (size_t)d * N + 4 * j);
     const float v[4] = {u.x, u.y, u.z, u.w};
-    fp8_store_row<N>(v, R8, Rs, d, j);
+    if constexpr (std::is_same<HT, Nvfp4>::value) {
+      float rv[4], beta, sr;
+      nvfp4_store_row<N>(v, (uint8_t*)a.read_copy + soff / 2, a.read_bscale + soff / 16, Rs, d, j, rv, &beta, &sr);
+    } else {
+      fp8_store_row<N>(v, (uint8_t*)a.read_copy + soff, Rs, d, j);
+    }
   }
 }
 
@@ -492,9 +510,12 @@ cudaError_t heads_decode(const LaunchArgs& a, cudaStream_t s) {
 }  // namespace ers
 
 namespace ers {
-cudaError_t heads_recast_fp8(const LaunchArgs& a, cudaStream_t s) {
+cudaError_t heads_recast(const LaunchArgs& a, cudaStream_t s) {
   if (a.nseq <= 0) return cudaSuccess;
-  k_recast_fp8<64, 128><<<dim3(a.nseq, a.H), kThreads, 0, s>>>(a);
+  if (a.read_nvfp4)
+    k_recast<Nvfp4, 64, 128><<<dim3(a.nseq, a.H), kThreads, 0, s>>>(a);
+  else
+    k_recast<uint8_t, 64, 128><<<dim3(a.nseq, a.H), kThreads, 0, s>>>(a);
   return cudaGetLastError();
 }
 }  // namespace ers

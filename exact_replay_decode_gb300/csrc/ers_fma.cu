@@ -569,11 +569,11 @@ cudaError_t refresh_impl(const LaunchArgs& a, cudaStream_t s) {
   const size_t sm = fma_smem_bytes(a.Q, P);
   cudaError_t e = prep(k_refresh<T, P, N>, sm);
   if (e != cudaSuccess) return e;
-  if (a.read_fp8) {   // fold the anchors, then cast the FP8 copies from them
+  if (a.read_fp8 || a.read_nvfp4) {   // fold the anchors, then cast the FP8 / NVFP4 copies from them
     LaunchArgs b = a;
     b.read_copy = nullptr;
     k_refresh<T, P, N><<<dim3(a.nseq, a.H), kThreads, sm, s>>>(b);
-    if ((e = heads_recast_fp8(a, s)) != cudaSuccess) return e;
+    if ((e = heads_recast(a, s)) != cudaSuccess) return e;
   } else {
     k_refresh<T, P, N><<<dim3(a.nseq, a.H), kThreads, sm, s>>>(a);
   }

@@ -34,7 +34,9 @@ struct LaunchArgs {
   float* state;
   void* read_copy;
   int read_fp8;        // read copy is FP8 e4m3 with per-row scales (read_scale [nslots, H, P])
+  int read_nvfp4;      // read copy is NVFP4: e2m1 codes, e4m3 block scales (read_bscale), row scales
   float* read_scale;
+  uint8_t* read_bscale;   // NVFP4 block scales [nslots, H, P, N / 16]
   void* bx;
   float* bdt;
   void* bB;
@@ -69,7 +71,8 @@ bool fma_supported(int P, int N);
 bool heads_decode_supported(int P, int N, int Q);
 cudaError_t heads_decode(const LaunchArgs& a, cudaStream_t s);
 // FP8 read-copy recast after a refresh (P = 64, N = 128), ers_decode.cu
-cudaError_t heads_recast_fp8(const LaunchArgs& a, cudaStream_t s);
+// casts the FP8 or NVFP4 read copy of the slots an ReplaySSM / exact refresh just folded
+cudaError_t heads_recast(const LaunchArgs& a, cudaStream_t s);
 // warp-per-head speculative verify (chunk <= 16, P = 64, N = 128, T <= 4, H/G <= 8), ers_verify.cu
 bool heads_verify_supported(int P, int N, int Q, int T, int H, int G);
 cudaError_t heads_verify(const LaunchArgs& a, cudaStream_t s);

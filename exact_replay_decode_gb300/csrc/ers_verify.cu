@@ -41,11 +41,12 @@ constexpr size_t verify_smem_bytes() {
 }
 
 // Read-copy stream: yo[k * P + d] = Dot<128>(C of draft k, R[d]) for all rows d.  q holds rows
-// [0, kVerifyRowsInFlight) on entry.  An FP8 copy is read as codes and each row's dot products are
-// scaled by the row scale (lane d % 32 holds it in sc[d / 32]), as in the decode stream.
+// [0, kVerifyRowsInFlight) on entry.  FP8 and NVFP4 copies are read as codes: NVFP4 lane partials
+// are scaled by their block scale and each row's dot products by the row scale (lane d % 32 holds
+// it in sc[d / 32]), as in the decode stream.
 template <typename HT, int P, int N>
-__device__ __forceinline__ void stream_read_copy(const HT* __restrict__ R,
-                                                 typename Quad<HT>::raw (&q)[kVerifyRowsInFlight],
+__device__ __forceinline__ void stream_read_copy(const RowSrc<HT, N>& src,
+                                                 typename RawOf<HT>::type (&q)[kVerifyRowsInFlight],
                                                  const float (&c)[kDraftsMax][4], float* yo, int j,
                                                  const float (&sc)[2]) {
   constexpr int NBLK = P / 8, QB = kVerifyRowsInFlight / 8;
@@ -55,18 +56,17 @@ __device__ __forceinline__ void stream_read_copy(const HT* __restrict__ R,
 #pragma unroll
     for (int r = 0; r < 8; ++r) {
       const int qs = (blk % QB) * 8 + r;
-      float hv[4];
-      if constexpr (std::is_same<HT, uint8_t>::value) {
-        fp8_codes(q[qs], hv);
-      } else {
-        Quad<HT>::unpack(q[qs], hv);
-      }
+      float hv[4], ls;
+      row_values<HT>(q[qs], hv, &ls);
 #pragma unroll
-      for (int k = 0; k < kDraftsMax; ++k) part[k * 8 + r] = Dot<N>::partial(c[k], hv);
-      if (blk + QB < NBLK) q[qs] = Quad<HT>::ld_stream(R + (size_t)(blk * 8 + r + kVerifyRowsInFlight) * N + 4 * j);
+      for (int k = 0; k < kDraftsMax; ++k) {
+        part[k * 8 + r] = Dot<N>::partial(c[k], hv);
+        if constexpr (kLaneScale<HT>) part[k * 8 + r] = __fmul_rn(part[k * 8 + r], ls);
+      }
+      if (blk + QB < NBLK) q[qs] = src.ld(blk * 8 + r + kVerifyRowsInFlight, j);
     }
     float v = reduce_scatter32(part, j);   // draft j / 8, row blk * 8 + j % 8
-    if constexpr (std::is_same<HT, uint8_t>::value)
+    if constexpr (kRowScale<HT>)
       v = __fmul_rn(v, __shfl_sync(kFull, sc[(blk * 8) >> 5], (blk * 8 + (j & 7)) & 31));
     yo[(j >> 3) * P + blk * 8 + (j & 7)] = v;
   }
@@ -75,13 +75,15 @@ __device__ __forceinline__ void stream_read_copy(const HT* __restrict__ R,
 
 // Flush stream: each anchor row is folded with the committed records (chunk_state / fold_state
 // order: acc = fma(w_s x_s[d], B_s[n], acc) over s < hc, then fma(decay, H, acc)), written back to
-// the anchor, cast to bf16 into the read copy, and the cast values feed the drafts' dot products
-// (yo as above).  wx[s * P + d] = w_s x_s[d] is precomputed per warp; 8 rows per pass.
-template <typename T, int P, int N>
-__device__ __noinline__ void stream_anchor_flush(float* __restrict__ Hd, __nv_bfloat16* __restrict__ Rd,
-                                                 uint8_t* __restrict__ R8, float* __restrict__ Rs,
+// the anchor, cast into the read copy (CT: bf16, FP8 or NVFP4), and the cast values feed the
+// drafts' dot products (yo as above).  wx[s * P + d] = w_s x_s[d] is precomputed per warp; 8 rows
+// per pass.
+template <typename T, typename CT, int P, int N>
+__device__ __noinline__ void stream_anchor_flush(float* __restrict__ Hd, void* __restrict__ R,
+                                                 uint8_t* __restrict__ Rb, float* __restrict__ Rs,
                                                  const float (&c)[kDraftsMax][4], float* yo, int j, int hc,
                                                  const float* wx, float decay, const T* sB) {
+  constexpr bool kF8 = std::is_same<CT, uint8_t>::value, kNv = std::is_same<CT, Nvfp4>::value;
 #pragma unroll 1
   for (int d0 = 0; d0 < P; d0 += 8) {
     float h[8][4], acc[8][4];
@@ -111,11 +113,16 @@ __device__ __noinline__ void stream_anchor_flush(float* __restrict__ Hd, __nv_bf
       for (int e = 0; e < 4; ++e) v[e] = __fmaf_rn(decay, h[r][e], acc[r][e]);
       const size_t o = (size_t)(d0 + r) * N + 4 * j;
       *reinterpret_cast<float4*>(Hd + o) = make_float4(v[0], v[1], v[2], v[3]);
-      float rv[4];   // what the read copy now holds (FP8: the codes, scaled after the reduction)
-      if (R8 != nullptr) {
+      float rv[4];   // what the read copy now holds (FP8 / NVFP4: the codes, scaled as they are read)
+      float ls = 1.f;
+      if constexpr (kNv) {
+        float s;
+        nvfp4_store_row<N>(v, (uint8_t*)R, Rb, Rs, d0 + r, j, rv, &ls, &s);
+        if ((j & 7) == r) srow = s;
+      } else if constexpr (kF8) {
         float s;
         const uint32_t wq = fp8_quant_row(v, &s);
-        *reinterpret_cast<uint32_t*>(R8 + o) = wq;
+        *reinterpret_cast<uint32_t*>((uint8_t*)R + o) = wq;
         if (j == 0) Rs[d0 + r] = s;
         if ((j & 7) == r) srow = s;
         fp8_codes(wq, rv);
@@ -124,14 +131,17 @@ __device__ __noinline__ void stream_anchor_flush(float* __restrict__ Hd, __nv_bf
         uint2 u;
         u.x = *reinterpret_cast<uint32_t*>(&lo2);
         u.y = *reinterpret_cast<uint32_t*>(&hi2);
-        *reinterpret_cast<uint2*>(Rd + o) = u;
+        *reinterpret_cast<uint2*>((__nv_bfloat16*)R + o) = u;
         Quad<__nv_bfloat16>::unpack(u, rv);
       }
 #pragma unroll
-      for (int k = 0; k < kDraftsMax; ++k) part[k * 8 + r] = Dot<N>::partial(c[k], rv);
+      for (int k = 0; k < kDraftsMax; ++k) {
+        part[k * 8 + r] = Dot<N>::partial(c[k], rv);
+        if constexpr (kNv) part[k * 8 + r] = __fmul_rn(part[k * 8 + r], ls);
+      }
     }
     float v = reduce_scatter32(part, j);
-    if (R8 != nullptr) v = __fmul_rn(v, srow);
+    if constexpr (kF8 || kNv) v = __fmul_rn(v, srow);
     yo[(j >> 3) * P + d0 + (j & 7)] = v;
   }
   __syncwarp();
@@ -168,9 +178,15 @@ __global__ void __launch_bounds__(kThreads, 2) k_verify_heads(LaunchArgs a) {
   const int h0 = flush ? 0 : hc;   // committed rows that precede the drafts
   const size_t HP = (size_t)a.H * P, GN = (size_t)a.G * N;
   const size_t soff = ((size_t)slot * a.H + h) * P * N;
-  const HT* R = (const HT*)a.read_copy + soff;   // bf16 values or FP8 codes
-  float sc[2] = {0.f, 0.f};                      // FP8: scales of rows j and 32 + j
-  if constexpr (std::is_same<HT, uint8_t>::value) {
+  RowSrc<HT, N> src;   // bf16 values, FP8 codes or NVFP4 codes + block scales
+  if constexpr (std::is_same<HT, Nvfp4>::value) {
+    src.c4 = (const uint8_t*)a.read_copy + soff / 2;
+    src.bs = a.read_bscale + soff / 16;
+  } else {
+    src.p = (const HT*)a.read_copy + soff;
+  }
+  float sc[2] = {0.f, 0.f};   // FP8 / NVFP4: scales of rows j and 32 + j
+  if constexpr (kRowScale<HT>) {
     if (!flush && active) {
       const float* Rs = a.read_scale + ((size_t)slot * a.H + h) * P;
       sc[0] = Rs[j];
@@ -188,10 +204,10 @@ __global__ void __launch_bounds__(kThreads, 2) k_verify_heads(LaunchArgs a) {
       for (int e = 0; e < 4; ++e) c[k][e] = 0.f;
     }
   }
-  typename Quad<HT>::raw q[kVerifyRowsInFlight];
+  typename RawOf<HT>::type q[kVerifyRowsInFlight];
   if (!flush && active) {
 #pragma unroll
-    for (int r = 0; r < kVerifyRowsInFlight; ++r) q[r] = Quad<HT>::ld_stream(R + (size_t)r * N + 4 * j);
+    for (int r = 0; r < kVerifyRowsInFlight; ++r) q[r] = src.ld(r, j);
   }
   // committed rows 0..hc-1 at smem rows 0..hc-1, drafts at rows QM..QM+T-1
   const T* bB = (const T*)a.bB + (size_t)slot * a.Q * GN + (size_t)g * N;
@@ -216,7 +232,7 @@ __global__ void __launch_bounds__(kThreads, 2) k_verify_heads(LaunchArgs a) {
   const float dt_d = j < Td ? a.dt[((size_t)i * Td + j) * a.H + h] : 0.f;
   const float Ah = a.A[h], bias = a.dt_bias[h];
   float* yo = syo + w * kDraftsMax * P;
-  if (!flush && active) stream_read_copy<HT, P, N>(R, q, c, yo, j, sc);
+  if (!flush && active) stream_read_copy<HT, P, N>(src, q, c, yo, j, sc);
   // output rows s < h0 + T: committed rows then drafts
   const int nout = h0 + Td;
   const float dt_o_d = __shfl_sync(kFull, dt_d, max(j - h0, 0) & 31);
@@ -261,10 +277,11 @@ __global__ void __launch_bounds__(kThreads, 2) k_verify_heads(LaunchArgs a) {
   __syncthreads();
   if (!active) return;
   if (flush)
-    stream_anchor_flush<T, P, N>(a.state + soff, a.read_fp8 ? nullptr : (__nv_bfloat16*)a.read_copy + soff,
-                                 a.read_fp8 ? (uint8_t*)a.read_copy + soff : nullptr,
-                                 a.read_fp8 ? a.read_scale + ((size_t)slot * a.H + h) * P : nullptr, c, yo, j, hc,
-                                 sw, decay, sB);
+    stream_anchor_flush<T, HT, P, N>(a.state + soff,
+                                     std::is_same<HT, Nvfp4>::value ? (void*)((uint8_t*)a.read_copy + soff / 2)
+                                                                    : (void*)((HT*)a.read_copy + soff),
+                                     a.read_bscale + soff / 16, a.read_scale + ((size_t)slot * a.H + h) * P, c, yo,
+                                     j, hc, sw, decay, sB);
   // outputs of draft k (row t_k = h0 + k), d = j + 32 m: one pass over the rows s serves every draft
   // (each draft's sum still runs over s = 0..t_k in order)
   const float Dh = a.D[h];
@@ -350,6 +367,10 @@ cudaError_t heads_verify(const LaunchArgs& a, cudaStream_t s) {
   if (a.read_fp8) {
     if (a.io == ERS_DTYPE_BF16) return launch_verify_heads<__nv_bfloat16, uint8_t, 16>(a, s);
     return launch_verify_heads<float, uint8_t, 16>(a, s);
+  }
+  if (a.read_nvfp4) {
+    if (a.io == ERS_DTYPE_BF16) return launch_verify_heads<__nv_bfloat16, Nvfp4, 16>(a, s);
+    return launch_verify_heads<float, Nvfp4, 16>(a, s);
   }
   if (a.io == ERS_DTYPE_BF16) return launch_verify_heads<__nv_bfloat16, __nv_bfloat16, 16>(a, s);
   return launch_verify_heads<float, __nv_bfloat16, 16>(a, s);

@@ -9,6 +9,8 @@
 #include <cuda_fp16.h>
 #include <stdint.h>
 
+#include <type_traits>
+
 #include "ers_common.cuh"
 #include "tc_common.cuh"
 
@@ -164,6 +166,125 @@ __device__ __forceinline__ void fp8_store_row(const float (&v)[4], uint8_t* R8, 
   const uint32_t w = fp8_quant_row(v, &s);
   *reinterpret_cast<uint32_t*>(R8 + (size_t)d * N + 4 * j) = w;
   if (j == 0) Rs[d] = s;
+}
+
+// ---- NVFP4 read copy: e2m1 codes, an e4m3 scale per 16 values, a power-of-two scale per row -------
+// Row d of a head: codes at C4 + d*N/2 (lane j's 4 codes in the 16 bits at byte 2j, element 4j+e in
+// bits 4e..4e+3), block scales at Bs + d*N/16 (block b = values [16b, 16b+16), lanes 4b..4b+3),
+// row scale Rs[d] = 2^k, k the smallest integer with amax <= 2688 * 2^k (448 * 6: no block scale
+// saturates), at least -127.  With u = v / 2^k (exact): beta = e4m3(amax_b(|u|) / 6) (fp32 division),
+// q = e2m1(u * rcp(beta)) (fp32 reciprocal and product; q = 0 where beta = 0); value q * beta * 2^k.
+struct Nvfp4 {};   // tag type of the NVFP4 read copy
+
+// A lane's view of one NVFP4 row: its 16 code bits and its block's scale byte in bits 16..23.
+__device__ __forceinline__ uint32_t nvfp4_ld(const uint8_t* C4row, const uint8_t* Bsrow, int j) {
+  uint16_t c;
+  uint16_t b;
+  asm volatile("ld.global.nc.L1::no_allocate.u16 %0, [%1];" : "=h"(c) : "l"(C4row + 2 * j));
+  asm volatile("ld.global.nc.u8 %0, [%1];" : "=h"(b) : "l"(Bsrow + (j >> 2)));
+  return (uint32_t)c | ((uint32_t)(b & 0xFFu) << 16);
+}
+
+// e2m1 values of the 4 codes of w (exact in fp32) and the block scale beta.
+__device__ __forceinline__ void nvfp4_codes(uint32_t w, float (&v)[4], float* beta) {
+  uint32_t h01, h23, hb;
+  asm("{ .reg .b8 t; cvt.u8.u32 t, %1; cvt.rn.f16x2.e2m1x2 %0, t; }" : "=r"(h01) : "r"(w & 0xFFu));
+  asm("{ .reg .b8 t; cvt.u8.u32 t, %1; cvt.rn.f16x2.e2m1x2 %0, t; }" : "=r"(h23) : "r"((w >> 8) & 0xFFu));
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(hb) : "h"((uint16_t)((w >> 16) & 0xFFu)));
+  const __half2 a = *reinterpret_cast<const __half2*>(&h01);
+  const __half2 b = *reinterpret_cast<const __half2*>(&h23);
+  v[0] = __low2float(a);
+  v[1] = __high2float(a);
+  v[2] = __low2float(b);
+  v[3] = __high2float(b);
+  *beta = __low2float(*reinterpret_cast<const __half2*>(&hb));
+}
+
+__device__ __forceinline__ uint32_t e2m1x2(float lo, float hi) {   // two codes, lo in the low nibble
+  uint32_t r;
+  asm("{ .reg .b8 t; cvt.rn.satfinite.e2m1x2.f32 t, %1, %2; cvt.u32.u8 %0, t; }" : "=r"(r) : "f"(hi), "f"(lo));
+  return r & 0xFFu;
+}
+
+// Quantises the warp's row (lane quad v): returns lane j's 16 code bits; the block scale byte, its
+// value and the row scale in *bs, *beta, *scale.
+__device__ __forceinline__ uint32_t nvfp4_quant_row(const float (&v)[4], int j, uint32_t* bs, float* beta,
+                                                    float* scale) {
+  float m = fmaxf(fmaxf(fabsf(v[0]), fabsf(v[1])), fmaxf(fabsf(v[2]), fabsf(v[3])));
+  float mb = m;
+#pragma unroll
+  for (int o = 16; o >= 1; o >>= 1) m = fmaxf(m, __shfl_xor_sync(kFull, m, o));
+  // 2688 = 1.3125 * 2^11: k = E - 138 + (mantissa field > 0x280000) for a normal maximum
+  const uint32_t b = __float_as_uint(m);
+  const int E = (int)(b >> 23);
+  const int k = E == 0 ? -127 : max(E - 138 + ((b & 0x7FFFFFu) > 0x280000u ? 1 : 0), -127);
+  *scale = k == -127 ? __uint_as_float(0x00400000u) : __uint_as_float((uint32_t)(k + 127) << 23);
+  const float inv = __uint_as_float((uint32_t)(127 - k) << 23);
+  float u[4];
+#pragma unroll
+  for (int e = 0; e < 4; ++e) u[e] = __fmul_rn(v[e], inv);
+  mb = __fmul_rn(mb, inv);   // |u| max of the lane (a power-of-two scaling commutes with max)
+  mb = fmaxf(mb, __shfl_xor_sync(kFull, mb, 1));
+  mb = fmaxf(mb, __shfl_xor_sync(kFull, mb, 2));
+  const uint32_t bcode = e4m3x2(__fdiv_rn(mb, 6.f), 0.f) & 0xFFu;
+  uint32_t hb;
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(hb) : "h"((uint16_t)bcode));
+  const float bv = __low2float(*reinterpret_cast<const __half2*>(&hb));
+  *bs = bcode;
+  *beta = bv;
+  if (bv == 0.f) return 0u;
+  const float rho = __frcp_rn(bv);
+  return e2m1x2(__fmul_rn(u[0], rho), __fmul_rn(u[1], rho)) | (e2m1x2(__fmul_rn(u[2], rho), __fmul_rn(u[3], rho)) << 8);
+}
+
+// Writes row d (lane quad v) of an NVFP4 copy; returns the code values (rv) and the block scale
+// (*beta) that a dot product reads, and the row scale in *scale.
+template <int N>
+__device__ __forceinline__ void nvfp4_store_row(const float (&v)[4], uint8_t* C4, uint8_t* Bs, float* Rs, int d,
+                                                int j, float (&rv)[4], float* beta, float* scale) {
+  uint32_t bs;
+  const uint32_t c = nvfp4_quant_row(v, j, &bs, beta, scale);
+  *reinterpret_cast<uint16_t*>(C4 + (size_t)d * (N / 2) + 2 * j) = (uint16_t)c;
+  if ((j & 3) == 0) Bs[(size_t)d * (N / 16) + (j >> 2)] = (uint8_t)bs;
+  if (j == 0) Rs[d] = *scale;
+  float bb;
+  nvfp4_codes(c | (bs << 16), rv, &bb);
+}
+
+// ---- how the output streams read one row of their source -------------------------------------------
+// fp32 checkpoint, bf16 or FP8 read copy (lane j: elements [4j, 4j+4) of row d), or NVFP4 read copy.
+template <typename HT> struct RawOf { using type = typename Quad<HT>::raw; };
+template <> struct RawOf<Nvfp4> { using type = uint32_t; };
+
+template <typename HT> constexpr bool kRowScale = std::is_same<HT, uint8_t>::value || std::is_same<HT, Nvfp4>::value;
+template <typename HT> constexpr bool kLaneScale = std::is_same<HT, Nvfp4>::value;
+
+template <typename HT, int N> struct RowSrc {
+  const HT* p;
+  __device__ __forceinline__ typename RawOf<HT>::type ld(int d, int j) const {
+    return Quad<HT>::ld_stream(p + (size_t)d * N + 4 * j);
+  }
+};
+template <int N> struct RowSrc<Nvfp4, N> {
+  const uint8_t* c4;
+  const uint8_t* bs;
+  __device__ __forceinline__ uint32_t ld(int d, int j) const {
+    return nvfp4_ld(c4 + (size_t)d * (N / 2), bs + (size_t)d * (N / 16), j);
+  }
+};
+
+// The 4 values a lane multiplies with C (fp32 or bf16 values, FP8 or e2m1 codes) and, for NVFP4,
+// the factor of the lane's partial dot product (its block scale).  Row scales apply after the
+// row's reduction.
+template <typename HT>
+__device__ __forceinline__ void row_values(typename RawOf<HT>::type r, float (&h)[4], float* lane_scale) {
+  if constexpr (std::is_same<HT, Nvfp4>::value) {
+    nvfp4_codes(r, h, lane_scale);
+  } else if constexpr (std::is_same<HT, uint8_t>::value) {
+    fp8_codes(r, h);
+  } else {
+    Quad<HT>::unpack(r, h);
+  }
 }
 
 template <typename K>

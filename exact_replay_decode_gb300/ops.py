@@ -187,13 +187,16 @@ class ReplayCache:
     token-major partial-chunk buffers of (x, raw dt, B, C) and the per-slot position.
 
     read_dtype "bf16": read_copy [S,H,P,N] bf16.  read_dtype "fp8": read_copy [S,H,P,N] uint8 holding
-    e4m3 codes and read_scale [S,H,P] fp32, one scale per state row (value = code * scale)."""
+    e4m3 codes and read_scale [S,H,P] fp32, one scale per state row (value = code * scale).
+    read_dtype "nvfp4": read_copy [S,H,P,N/2] uint8 holding two e2m1 codes per byte (value n in the
+    low nibble of byte n/2 when n is even), read_block_scale [S,H,P,N/16] e4m3 bytes (one per 16
+    values) and read_scale [S,H,P] fp32 (value = code * block scale * row scale)."""
 
     def __init__(self, nslots: int, nheads: int, ngroups: int, headdim: int, dstate: int, chunk: int,
                  io_dtype: torch.dtype = torch.bfloat16, read_copy: bool = False, device="cuda",
                  read_dtype: str = "bf16"):
-        if read_dtype not in ("bf16", "fp8"):
-            raise ValueError(f"read_dtype must be 'bf16' or 'fp8', got {read_dtype!r}")
+        if read_dtype not in ("bf16", "fp8", "nvfp4"):
+            raise ValueError(f"read_dtype must be 'bf16', 'fp8' or 'nvfp4', got {read_dtype!r}")
         self.nslots, self.H, self.G, self.P, self.N, self.Q = nslots, nheads, ngroups, headdim, dstate, chunk
         self.io = io_dtype
         self.read_dtype = read_dtype
@@ -202,10 +205,18 @@ class ReplayCache:
         self.state = torch.zeros(*shp, dtype=torch.float32, **z)
         self.read_copy = None
         self.read_scale = None
+        self.read_block_scale = None
         if read_copy:
-            fp8 = read_dtype == "fp8"
-            self.read_copy = torch.zeros(*shp, dtype=torch.uint8 if fp8 else torch.bfloat16, **z)
-            if fp8:
+            if read_dtype == "bf16":
+                self.read_copy = torch.zeros(*shp, dtype=torch.bfloat16, **z)
+            elif read_dtype == "fp8":
+                self.read_copy = torch.zeros(*shp, dtype=torch.uint8, **z)
+            else:
+                if dstate % 16:
+                    raise ValueError("an NVFP4 read copy needs dstate divisible by 16")
+                self.read_copy = torch.zeros(nslots, nheads, headdim, dstate // 2, dtype=torch.uint8, **z)
+                self.read_block_scale = torch.zeros(nslots, nheads, headdim, dstate // 16, dtype=torch.uint8, **z)
+            if read_dtype != "bf16":
                 self.read_scale = torch.zeros(nslots, nheads, headdim, dtype=torch.float32, **z)
         self.buf_x = torch.zeros(nslots, chunk, nheads, headdim, dtype=io_dtype, **z)
         self.buf_dt = torch.zeros(nslots, chunk, nheads, dtype=torch.float32, **z)
@@ -218,10 +229,10 @@ class ReplayCache:
         return _dims(self.H, self.G, self.P, self.N, self.Q, self.io)
 
     def _c(self) -> _abi.Cache:
-        rd = _abi.READ_FP8_E4M3 if self.read_dtype == "fp8" else _abi.READ_BF16
+        rd = {"bf16": _abi.READ_BF16, "fp8": _abi.READ_FP8_E4M3, "nvfp4": _abi.READ_NVFP4}[self.read_dtype]
         return _abi.Cache(self.state.data_ptr(), _ptr(self.read_copy), self.buf_x.data_ptr(), self.buf_dt.data_ptr(),
                           self.buf_B.data_ptr(), self.buf_C.data_ptr(), self.pos.data_ptr(), self.nslots, rd,
-                          _ptr(self.read_scale))
+                          _ptr(self.read_scale), _ptr(self.read_block_scale))
 
     def read_values(self) -> Optional[torch.Tensor]:
         """The read copy's values as fp32 (FP8: code * row scale), or None without a read copy."""
@@ -229,11 +240,18 @@ class ReplayCache:
             return None
         if self.read_scale is None:
             return self.read_copy.float()
-        return self.read_copy.view(torch.float8_e4m3fn).float() * self.read_scale.unsqueeze(-1)
+        if self.read_block_scale is None:
+            return self.read_copy.view(torch.float8_e4m3fn).float() * self.read_scale.unsqueeze(-1)
+        e2m1 = torch.tensor([0, 0.5, 1, 1.5, 2, 3, 4, 6, -0.0, -0.5, -1, -1.5, -2, -3, -4, -6],
+                            dtype=torch.float32, device=self.read_copy.device)
+        c = self.read_copy.long()
+        q = torch.stack([e2m1[c & 15], e2m1[c >> 4]], dim=-1).flatten(-2)
+        beta = self.read_block_scale.view(torch.float8_e4m3fn).float().repeat_interleave(16, dim=-1)
+        return q * beta * self.read_scale.unsqueeze(-1)
 
     def nbytes(self) -> int:
         ts = [self.state, self.buf_x, self.buf_dt, self.buf_B, self.buf_C, self.pos]
-        ts += [t for t in (self.read_copy, self.read_scale) if t is not None]
+        ts += [t for t in (self.read_copy, self.read_scale, self.read_block_scale) if t is not None]
         return sum(t.numel() * t.element_size() for t in ts)
 
 

@@ -106,19 +106,31 @@ typedef struct ers_params {
  *   buf_B, buf_C [nslots, Q, G, N] io dtype: token-major partial-chunk input buffers
  *   pos       [nslots] int32: buffered tokens p (exact mode, 0 <= p < Q between calls) or the
  *             committed pointer h (ReplaySSM mode, 0 <= h <= L).
- *   read_dtype ERS_READ_BF16 (0) or ERS_READ_FP8_E4M3 (1).
- *   read_scale [nslots, H, P] fp32, FP8 read copy only (else NULL): one scale per state row.
+ *   read_dtype ERS_READ_BF16 (0), ERS_READ_FP8_E4M3 (1) or ERS_READ_NVFP4 (2).
+ *   read_scale [nslots, H, P] fp32, FP8 and NVFP4 read copies only (else NULL): one power-of-two
+ *             scale per state row.
+ *   read_block_scale [nslots, H, P, N / 16] e4m3 bytes, NVFP4 only (else NULL).
  *
  * FP8 read copy (ReplaySSM "Paper-reported results", the FP8-read / FP32-recurrence mode; the page
  * names the mode without its quantisation, so this library defines it): each state row (one d of
  * one head) has a power-of-two scale s = 2^k, k the smallest integer with amax_n |S[d][n]| <= 448 * 2^k
  * (no code saturates) and at least -127 (all-zero rows read as zeros); the row is stored as e4m3
  * bytes q[n] = RNE(S[d][n] / s) and read as q[n] * s, both scalings exact.  Outputs apply s to the
- * row's dot product with C.  Supported where the CUDA-core warp-per-head kernels run (headdim 64,
- * dstate 128, chunk <= 16; verify with at most 4 drafts and 8 heads per group); elsewhere calls
- * that read or write the copy return ERS_EUNSUPPORTED. */
+ * row's dot product with C.  read_copy is [nslots, H, P, N] bytes.
+ * NVFP4 read copy ("Paper-reported results": FP32 recurrence + NVFP4 read; the format's per-tensor
+ * fp32 scale is taken per state row): s = 2^k, k the smallest integer with amax <= 2688 * 2^k and at
+ * least -127; with u = S / s (exact), each block of 16 consecutive values n has the e4m3 scale
+ * beta = RNE_e4m3(amax_block |u| / 6) (fp32 division) and codes q = RNE_e2m1_satfinite(u * (1 / beta))
+ * (fp32 reciprocal, fp32 product; q = 0 where beta = 0); the value is q * beta * s (exact).  read_copy
+ * is [nslots, H, P, N / 2] bytes, value n of a row in bits 4 (n % 2)..4 (n % 2) + 3 of byte n / 2.
+ * Outputs apply beta to each lane's 4-value partial dot product and s to the row's.  NVFP4 copies
+ * are kept in ReplaySSM mode only.
+ * Both are supported where the CUDA-core warp-per-head kernels run (headdim 64, dstate 128,
+ * chunk <= 16; verify with at most 4 drafts and 8 heads per group); elsewhere calls that read or
+ * write the copy return ERS_EUNSUPPORTED. */
 #define ERS_READ_BF16 0
 #define ERS_READ_FP8_E4M3 1
+#define ERS_READ_NVFP4 2
 
 typedef struct ers_cache {
   float* state;
@@ -131,6 +143,7 @@ typedef struct ers_cache {
   int32_t nslots;
   int32_t read_dtype;
   float* read_scale;
+  uint8_t* read_block_scale;
 } ers_cache;
 
 /* Human-readable name of a status code (static storage, never NULL). */

@@ -117,13 +117,14 @@ def test_zero_sequences_is_a_noop(lib):
 
 @needs_no_gpu
 def test_validation_of_fp8_read_copies(lib):
-    """FP8 read copies: the dtype code is checked, the row scales are required and aligned, and
-    shapes the warp-per-head kernels do not cover return ERS_EUNSUPPORTED before any launch."""
+    """FP8 / NVFP4 read copies: the dtype code is checked, the scales are required and aligned, and
+    shapes the warp-per-head kernels do not cover (and NVFP4 outside ReplaySSM mode) return
+    ERS_EUNSUPPORTED before any launch."""
     from exact_replay_decode_gb300 import _abi
     p = _prm()
 
-    def cache(read_dtype=_abi.READ_FP8_E4M3, scale=FAKE):
-        return _abi.Cache(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 4, read_dtype, scale)
+    def cache(read_dtype=_abi.READ_FP8_E4M3, scale=FAKE, bscale=FAKE):
+        return _abi.Cache(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 4, read_dtype, scale, bscale)
 
     def dec(d, c, flags=_abi.FLAG_REPLAYSSM):
         return lib.ers_replay_decode(ctypes.byref(d), ctypes.byref(p), ctypes.byref(c), 4, None, FAKE, FAKE, FAKE,
@@ -133,11 +134,13 @@ def test_validation_of_fp8_read_copies(lib):
         return lib.ers_spec_verify(ctypes.byref(d), ctypes.byref(p), ctypes.byref(c), 4, None, 4, FAKE, FAKE, FAKE,
                                    FAKE, 0, FAKE, None, None)
 
-    def ref(d, c):
-        return lib.ers_refresh(ctypes.byref(d), ctypes.byref(p), ctypes.byref(c), 4, None, _abi.FLAG_REPLAYSSM, 1,
-                               None, None)
+    def ref(d, c, flags=_abi.FLAG_REPLAYSSM):
+        return lib.ers_refresh(ctypes.byref(d), ctypes.byref(p), ctypes.byref(c), 4, None, flags, 1, None, None)
 
-    assert dec(_dims(), cache(read_dtype=2)) == 3                            # ERS_EDTYPE
+    assert dec(_dims(), cache(read_dtype=3)) == 3                            # ERS_EDTYPE
+    assert dec(_dims(), cache(read_dtype=_abi.READ_NVFP4, bscale=0)) == 1   # NVFP4 needs block scales
+    assert dec(_dims(), cache(read_dtype=_abi.READ_NVFP4), flags=0) == 12   # NVFP4: ReplaySSM mode only
+    assert ref(_dims(), cache(read_dtype=_abi.READ_NVFP4), flags=0) == 12
     assert dec(_dims(), cache(scale=0)) == 1                                 # scales required
     assert dec(_dims(), cache(scale=MISALIGNED)) == 4
     for d in (_dims(chunk=32), _dims(headdim=32, dstate=32), _dims(dstate=64)):

@@ -1,6 +1,7 @@
-"""FP8 e4m3 read copies on the GPU (ReplaySSM notes, "Paper-reported results": the FP8-read /
-FP32-recurrence mode; the page gives no quantiser, so the library defines one: a scale per state
-row, amax / 448, codes rounded to nearest even with saturation, read as code x scale).
+"""FP8 e4m3 and NVFP4 read copies on the GPU (ReplaySSM notes, "Paper-reported results": FP8 or
+NVFP4 reads over an FP32 recurrence; the page gives no quantiser, so the library defines them:
+FP8 with a power-of-two scale per state row; NVFP4 with e2m1 codes, an e4m3 scale per 16 values
+and a power-of-two scale per row).
 
 The copies the kernels cast equal the oracle's FP8 rounding of the same fp32 state bit for bit
 (refresh, fused refresh in decode, verify flush); verify outputs equal non-speculative FP8 decode
@@ -27,18 +28,23 @@ def _params(H, seed=0):
     return synth.make_params(np.random.Generator(np.random.PCG64(seed)), H)
 
 
-def test_fp8_refresh_cast_matches_oracle():
-    """ReplaySSM refresh of an empty history only recasts: the copy is the oracle's FP8 rounding of
-    the fp32 anchor as stored (edge rows: zero, subnormal codes, constant, single entry)."""
+_CAST = {"fp8": oracle.fp8_rows_round, "nvfp4": oracle.nvfp4_rows_round}
+
+
+@pytest.mark.parametrize("read_dtype", ["fp8", "nvfp4"])
+def test_refresh_cast_matches_oracle(read_dtype):
+    """ReplaySSM refresh of an empty history only recasts: the copy is the oracle's FP8 / NVFP4
+    rounding of the fp32 anchor as stored (edge rows: zero, subnormal codes, constant, single entry,
+    rows spanning 60 binades)."""
     ers = _ers()
     S, H, G, P, N, L = 6, 16, 2, 64, 128, 16
     st = synth.quant_probe_state(11, (S, H, P, N))
-    cache = ers.ReplayCache(S, H, G, P, N, L, torch.bfloat16, read_copy=True, read_dtype="fp8")
+    cache = ers.ReplayCache(S, H, G, P, N, L, torch.bfloat16, read_copy=True, read_dtype=read_dtype)
     cache.state.copy_(torch.from_numpy(st))
     prm = layer(_params(H))
     ers.refresh(cache, prm, replayssm=True, drafts_T=L + 1)   # h = 0 + T > L everywhere
     got = cache.read_values().cpu().numpy()
-    want = oracle.fp8_rows_round(st).astype(np.float32)
+    want = _CAST[read_dtype](st).astype(np.float32)
     assert np.array_equal(got.view(np.uint32), want.view(np.uint32))
     assert same_bits(cache.state, torch.from_numpy(st).to(dev()))     # the anchor is untouched
     assert int(cache.pos.abs().sum()) == 0
@@ -118,28 +124,29 @@ def _verify_run(w, S, K, seed, read_dtype):
     return params, prm, hist, drafts, acc, fresh
 
 
-def test_fp8_verify_equals_nonspec_decode_and_oracle():
-    """Verify + commit with an FP8 copy: accepted drafts equal non-speculative ReplaySSM decode over
-    the same committed stream bit for bit, flushes recast the copy exactly as the oracle rounds the
-    anchor, and outputs match the oracle's protocol model run with the FP8 read cast."""
+@pytest.mark.parametrize("read_dtype", ["fp8", "nvfp4"])
+def test_verify_equals_nonspec_decode_and_oracle(read_dtype):
+    """Verify + commit with an FP8 / NVFP4 copy: accepted drafts equal non-speculative ReplaySSM
+    decode over the same committed stream bit for bit, flushes recast the copy exactly as the oracle
+    rounds the anchor, and outputs match the oracle's protocol model run with the same read cast."""
     ers = _ers()
     w = synth.workload("verify_b512_t4")
     S, K, T, L = 64, 24, w.drafts, w.dims.chunk
     samples = [0, 13, 63]
-    params, prm, hist, drafts, acc, fresh = _verify_run(w, S, K, 7, "fp8")
+    params, prm, hist, drafts, acc, fresh = _verify_run(w, S, K, 7, read_dtype)
     cache, ref = fresh(), fresh()
     dx, ddt, dB, dC = torch_io.tokens_to(drafts, dev(), lead=(K, S, T))
     acc_t = torch.from_numpy(acc).to(dev())
     rows = np.concatenate([np.arange(i * 32, (i + 1) * 32) for i in samples])
     _, anchor = oracle.recurrence(hist.x[rows], hist.dt[rows], params.A, hist.B[rows], hist.C[rows], params.D,
                                   params.dt_bias, np.arange(0, len(samples) * 32 + 1, 32))
-    model = oracle.ReplaySSMModel(params, anchor, L, read_cast=oracle.fp8_rows_round)
+    model = oracle.ReplaySSMModel(params, anchor, L, read_cast=_CAST[read_dtype])
     flushes = 0
     for k in range(K):
         flushing = ((cache.pos + T) > L).nonzero().flatten().tolist()
         y = ers.spec_verify(cache, prm, dx[k], ddt[k], dB[k], dC[k])
         if flushing:
-            want = oracle.fp8_rows_round(cache.state[flushing].cpu().numpy()).astype(np.float32)
+            want = _CAST[read_dtype](cache.state[flushing].cpu().numpy()).astype(np.float32)
             got = cache.read_values()[flushing].cpu().numpy()
             assert np.array_equal(got.view(np.uint32), want.view(np.uint32)), k
             flushes += len(flushing)
@@ -153,7 +160,7 @@ def test_fp8_verify_equals_nonspec_decode_and_oracle():
             sel_t = torch.from_numpy(sel.astype(np.int32)).to(dev())
             sl = sel_t.long()
             yd = ers.replay_decode(ref, prm, dx[k, sl, j], ddt[k, sl, j], dB[k, sl, j], dC[k, sl, j], slot=sel_t,
-                                   replayssm=True)
+                                   replayssm=True, fuse_refresh=False)
             assert same_bits(yd, y[sl, j]), f"step {k} draft {j}"
         dr = [tuple(np.ascontiguousarray(getattr(drafts, f).reshape(K, S, T, *getattr(drafts, f).shape[1:])[k, i])
                     for f in ("x", "dt", "B", "C")) for i in samples]
@@ -165,26 +172,29 @@ def test_fp8_verify_equals_nonspec_decode_and_oracle():
     assert torch.equal(cache.pos, ref.pos)
     assert same_bits(cache.state, ref.state)
     assert torch.equal(cache.read_copy, ref.read_copy) and same_bits(cache.read_scale, ref.read_scale)
+    if read_dtype == "nvfp4":
+        assert torch.equal(cache.read_block_scale, ref.read_block_scale)
 
 
 def test_anchor_independent_of_read_precision():
-    """The same verify/commit run with a bf16 and with an FP8 copy: outputs differ, the anchors and
-    committed pointers are bit-identical (refresh folds the fp32 anchor, never the copy)."""
+    """The same verify/commit run with a bf16, an FP8 and an NVFP4 copy: outputs differ, the anchors
+    and committed pointers are bit-identical (refresh folds the fp32 anchor, never the copy)."""
     ers = _ers()
     w = synth.workload("verify_b512_t4")
     S, K, T = 32, 20, w.drafts
     _, prm, _, drafts, acc, fresh16 = _verify_run(w, S, K, 9, "bf16")
-    _, _, _, _, _, fresh8 = _verify_run(w, S, K, 9, "fp8")
-    c16, c8 = fresh16(), fresh8()
+    c16, c8, c4 = fresh16(), _verify_run(w, S, K, 9, "fp8")[-1](), _verify_run(w, S, K, 9, "nvfp4")[-1]()
     dx, ddt, dB, dC = torch_io.tokens_to(drafts, dev(), lead=(K, S, T))
     acc_t = torch.from_numpy(acc).to(dev())
     differ = False
     for k in range(K):
         y16 = ers.spec_verify(c16, prm, dx[k], ddt[k], dB[k], dC[k]); ers.commit(c16, acc_t[k], T)
         y8 = ers.spec_verify(c8, prm, dx[k], ddt[k], dB[k], dC[k]); ers.commit(c8, acc_t[k], T)
-        differ |= not same_bits(y16, y8)
+        y4 = ers.spec_verify(c4, prm, dx[k], ddt[k], dB[k], dC[k]); ers.commit(c4, acc_t[k], T)
+        differ |= not same_bits(y16, y8) and not same_bits(y8, y4)
     assert differ
     assert same_bits(c16.state, c8.state) and torch.equal(c16.pos, c8.pos)
+    assert same_bits(c16.state, c4.state) and torch.equal(c16.pos, c4.pos)
 
 
 def test_fp8_unsupported_shapes_raise():
@@ -198,3 +208,7 @@ def test_fp8_unsupported_shapes_raise():
     with pytest.raises(ers.ErsError) as e:
         ers.replay_decode(cache, prm, x, dt, B, B.clone(), replayssm=True)
     assert e.value.code == 12                                           # ERS_EUNSUPPORTED
+    c4 = ers.ReplayCache(2, H, G, P, N, 16, torch.bfloat16, read_copy=True, read_dtype="nvfp4")
+    with pytest.raises(ers.ErsError) as e:
+        ers.replay_decode(c4, prm, x, dt, B, B.clone())                # exact mode keeps no NVFP4 copy
+    assert e.value.code == 12

@@ -2,7 +2,7 @@
 "Motivation and method" and "Core equations": a refresh folds the committed records into the anchor
 and recasts the read copy; outputs read the copy).  The fused call equals ers_refresh with T = 1
 followed by the plain decode bit for bit (outputs, anchors, read copies, buffers, positions), on
-the warp-per-head kernel (bf16 and FP8 copies) and on the engines that run the two steps as two
+the warp-per-head kernel (bf16, FP8 and NVFP4 copies) and on the engines that run the two steps as two
 launches; outputs match the oracle's protocol model (verify of one draft, commit one)."""
 import dataclasses
 
@@ -51,7 +51,7 @@ def _run(dims, read_dtype, S, K, seed, samples):
     cat = [np.concatenate([p[f] for p in parts]) for f in range(4)]
     _, anchor = oracle.recurrence(*cat[:2], params.A, *cat[2:], params.D, params.dt_bias,
                                   np.concatenate([[0], np.cumsum([len(p[0]) for p in parts])]))
-    cast = oracle.fp8_rows_round if read_dtype == "fp8" else None
+    cast = {"fp8": oracle.fp8_rows_round, "nvfp4": oracle.nvfp4_rows_round}.get(read_dtype)
     model = oracle.ReplaySSMModel(params, anchor, L, read_cast=cast)
     flushes = 0
     for k in range(K):
@@ -69,15 +69,17 @@ def _run(dims, read_dtype, S, K, seed, samples):
     assert flushes > 0
     assert torch.equal(c1.pos, c2.pos) and same_bits(c1.state, c2.state)
     assert torch.equal(c1.read_copy.view(torch.uint8), c2.read_copy.view(torch.uint8))
-    if read_dtype == "fp8":
+    if read_dtype != "bf16":
         assert same_bits(c1.read_scale, c2.read_scale)
+    if read_dtype == "nvfp4":
+        assert torch.equal(c1.read_block_scale, c2.read_block_scale)
     for f in ("buf_x", "buf_dt", "buf_B", "buf_C"):
         assert same_bits(getattr(c1, f), getattr(c2, f)), f
     assert np.array_equal(c1.pos.cpu().numpy()[samples], model.h())
     assert state_err(c1.state[samples], model.anchor) <= STATE_TOL
 
 
-@pytest.mark.parametrize("read_dtype", ["bf16", "fp8"])
+@pytest.mark.parametrize("read_dtype", ["bf16", "fp8", "nvfp4"])
 def test_fused_flush_warp_per_head(read_dtype):
     _run(synth.Dims(64, 8, 64, 128, 16), read_dtype, 48, 40, 21, [0, 17, 47])
 
