@@ -166,7 +166,16 @@ __device__ __noinline__ void stream_state_refresh(float* __restrict__ Hd, __nv_b
 // copy (bf16, FP8 or NVFP4); the new token's dot product reads the cast values, exactly as a decode
 // after a separate refresh reads them from the copy.  FP8 / NVFP4 rows' dot products are scaled
 // after the reduction (srow: lane j keeps the scale of the 16-row group's row j / 2).
-template <typename T, typename HT, int P, int N>
+// kOut = false (the standalone refresh): no output, and HT = NoCopy when the cache keeps no copy; an
+// empty history (hc = 0) leaves the anchor's bits as they are and only recasts the copy.
+struct NoCopy {};
+
+template <typename HT>
+__host__ __device__ constexpr size_t sizeof_copy() {   // bytes per value of a bf16 / FP8 copy
+  return std::is_same<HT, __nv_bfloat16>::value ? 2 : 1;
+}
+
+template <typename T, typename HT, int P, int N, bool kOut = true>
 __device__ __noinline__ void stream_flush_copy(float* __restrict__ Hd, void* __restrict__ R, uint8_t* __restrict__ Rb,
                                                float* __restrict__ Rs, float c0, float c1, float c2, float c3,
                                                float* yo, int j, int hc, const float* wx, float decay,
@@ -174,6 +183,7 @@ __device__ __noinline__ void stream_flush_copy(float* __restrict__ Hd, void* __r
   constexpr int NBLK = P / 8;
   constexpr bool kF8 = std::is_same<HT, uint8_t>::value;
   constexpr bool kNv = std::is_same<HT, Nvfp4>::value;
+  constexpr bool kBf = std::is_same<HT, __nv_bfloat16>::value;
   const float c[4] = {c0, c1, c2, c3};
   float4 cur[8], nxt[8];
 #pragma unroll
@@ -211,9 +221,9 @@ __device__ __noinline__ void stream_flush_copy(float* __restrict__ Hd, void* __r
         float h[4], v[4], rv[4];
         Quad<float>::unpack(cur[r], h);
 #pragma unroll
-        for (int e = 0; e < 4; ++e) v[e] = __fmaf_rn(decay, h[e], acc[r4][e]);
+        for (int e = 0; e < 4; ++e) v[e] = hc > 0 ? __fmaf_rn(decay, h[e], acc[r4][e]) : h[e];
         const size_t o = (size_t)(blk * 8 + r) * N + 4 * j;
-        *reinterpret_cast<float4*>(Hd + o) = make_float4(v[0], v[1], v[2], v[3]);
+        if (hc > 0) *reinterpret_cast<float4*>(Hd + o) = make_float4(v[0], v[1], v[2], v[3]);
         float ls = 1.f;
         if constexpr (kNv) {
           float sr;
@@ -226,7 +236,7 @@ __device__ __noinline__ void stream_flush_copy(float* __restrict__ Hd, void* __r
           if (j == 0) Rs[blk * 8 + r] = sr;
           if ((j >> 1) == (blk & 1) * 8 + r) srow = sr;
           fp8_codes(wq, rv);
-        } else {
+        } else if constexpr (kBf) {
           __nv_bfloat162 lo2 = __floats2bfloat162_rn(v[0], v[1]), hi2 = __floats2bfloat162_rn(v[2], v[3]);
           uint2 u;
           u.x = *reinterpret_cast<uint32_t*>(&lo2);
@@ -234,19 +244,23 @@ __device__ __noinline__ void stream_flush_copy(float* __restrict__ Hd, void* __r
           *reinterpret_cast<uint2*>((__nv_bfloat16*)R + o) = u;
           Quad<__nv_bfloat16>::unpack(u, rv);
         }
-        pb[r] = Dot<N>::partial(c, rv);
-        if constexpr (kNv) pb[r] = __fmul_rn(pb[r], ls);
+        if constexpr (kOut) {
+          pb[r] = Dot<N>::partial(c, rv);
+          if constexpr (kNv) pb[r] = __fmul_rn(pb[r], ls);
+        }
       }
     }
-    if ((blk & 1) == 0) {
+    if constexpr (kOut) {
+      if ((blk & 1) == 0) {
 #pragma unroll
-      for (int r = 0; r < 8; ++r) part[r] = pb[r];
-    } else {
+        for (int r = 0; r < 8; ++r) part[r] = pb[r];
+      } else {
 #pragma unroll
-      for (int r = 0; r < 8; ++r) part[8 + r] = pb[r];
-      float v = reduce_scatter16(part, j);
-      if constexpr (kF8 || kNv) v = __fmul_rn(v, srow);
-      if ((j & 1) == 0) yo[(blk - 1) * 8 + (j >> 1)] = v;
+        for (int r = 0; r < 8; ++r) part[8 + r] = pb[r];
+        float v = reduce_scatter16(part, j);
+        if constexpr (kF8 || kNv) v = __fmul_rn(v, srow);
+        if ((j & 1) == 0) yo[(blk - 1) * 8 + (j >> 1)] = v;
+      }
     }
 #pragma unroll
     for (int r = 0; r < 8; ++r) cur[r] = nxt[r];
@@ -461,41 +475,119 @@ cudaError_t launch_decode_heads(const LaunchArgs& a, cudaStream_t s) {
   return rssm ? run(k_decode_heads<T, __nv_bfloat16, false, P, N, QM>) : run(k_decode_heads<T, float, false, P, N, QM>);
 }
 
-// ---- FP8 / NVFP4 read-copy recast for ers_refresh ------------------------------------------------------
-// After the refresh kernel has folded a slot's anchor (or left it unchanged for an empty history),
-// the slot's FP8 or NVFP4 read copy is cast from the fp32 anchor as stored, i.e. from the same
-// unrounded values ("Core equations": both copies are cast independently from one state).  Same
-// slot predicate as the refresh kernel; runs before the position is reset.  Warp w casts rows
-// [8w, 8w + 8) of head blockIdx.y, one row per pass.
-template <typename HT, int P, int N>
-__global__ void __launch_bounds__(kThreads) k_recast(LaunchArgs a) {
-  const int i = blockIdx.x, h = blockIdx.y;
-  const int slot = a.slot != nullptr ? a.slot[i] : i;
-  if (slot < 0 || slot >= a.nslots) return;   // reported by the refresh kernel
+// ---- standalone refresh (ers_refresh) on the warp-per-head layout ---------------------------------------
+// Exact mode: slots with pos == Q fold their Q buffered rows; ReplaySSM: slots with pos + T > L fold
+// their pos committed records (pos = 0: the anchor keeps its bits, the copy is recast).  The same
+// arithmetic as k_refresh and the fused flushes (state_weights, chunk_state, fold_state order), one
+// CTA per (sequence, 8 heads of a group), so a launch has 8x fewer CTAs than one per (sequence,
+// head), and the read copy (bf16, FP8 or NVFP4) is cast in the same pass from the fp32 values.
+// Positions are reset by k_setpos afterwards.
+template <typename T, typename HT, int P, int N, int QM>
+__global__ void __launch_bounds__(kThreads, 2) k_refresh_heads(LaunchArgs a) {
+  extern __shared__ __align__(16) unsigned char rsm[];
+  T* sB = reinterpret_cast<T*>(rsm);                          // [QM][N] group B rows
+  T* sxa = sB + QM * N;                                       // [warp][QM][P] x rows
+  float* swa = reinterpret_cast<float*>(sxa + kHeadsPerCta * QM * P);   // [warp][QM][P] w_s x_s[d]
+  const int tid = threadIdx.x, w = tid >> 5, j = tid & 31;
+  const int i = blockIdx.y;
+  const int hpg = a.H / a.G, nbl = (hpg + kHeadsPerCta - 1) / kHeadsPerCta;
+  const int g = blockIdx.x / nbl, hb = blockIdx.x % nbl;
+  const int hl = hb * kHeadsPerCta + w;
+  const bool active = hl < hpg;
+  const int h = g * hpg + (active ? hl : 0);
+  int slot;
+  if (!resolve_slot(a, i, &slot)) return;
   const int p = a.pos[slot];
-  if (p < 0 || p > a.Q) return;
+  if (p < 0 || p > a.Q) {
+    if (tid == 0) report(a.status, ERS_EALIGN);
+    return;
+  }
   const bool rssm = (a.flags & ERS_FLAG_REPLAYSSM) != 0;
   if (!(rssm ? (p + a.T > a.Q) : (p == a.Q))) return;
-  const int w = threadIdx.x >> 5, j = threadIdx.x & 31;
-  const size_t soff = ((size_t)slot * a.H + h) * P * N;
-  float* Rs = a.read_scale + ((size_t)slot * a.H + h) * P;
-#pragma unroll
-  for (int r = 0; r < P / kHeadsPerCta; ++r) {
-    const int d = (P / kHeadsPerCta) * w + r;
-    const float4 u = *reinterpret_cast<const float4*>(a.state + soff + (size_t)d * N + 4 * j);
-    const float v[4] = {u.x, u.y, u.z, u.w};
-    if constexpr (std::is_same<HT, Nvfp4>::value) {
-      float rv[4], beta, sr;
-      nvfp4_store_row<N>(v, (uint8_t*)a.read_copy + soff / 2, a.read_bscale + soff / 16, Rs, d, j, rv, &beta, &sr);
-    } else {
-      fp8_store_row<N>(v, (uint8_t*)a.read_copy + soff, Rs, d, j);
-    }
+  const size_t HP = (size_t)a.H * P, GN = (size_t)a.G * N;
+  const T* bB = (const T*)a.bB + (size_t)slot * a.Q * GN + (size_t)g * N;
+  constexpr int kBChunks = N * sizeof(T) / 16, kXChunks = P * sizeof(T) / 16;
+  for (int k = tid; k < p * kBChunks; k += kThreads) {
+    const int s = k / kBChunks, e = k % kBChunks;
+    cp_async16(reinterpret_cast<char*>(sB + s * N) + 16 * e, reinterpret_cast<const char*>(bB + s * GN) + 16 * e);
   }
+  T* sx = sxa + w * QM * P;
+  const T* bx = (const T*)a.bx + (size_t)slot * a.Q * HP + (size_t)h * P;
+  if (active)
+    for (int k = j; k < p * kXChunks; k += 32) {
+      const int s = k / kXChunks, e = k % kXChunks;
+      cp_async16(reinterpret_cast<char*>(sx + s * P) + 16 * e, reinterpret_cast<const char*>(bx + s * HP) + 16 * e);
+    }
+  float dc = 0.f;
+  df vc = {0.f, 0.f};
+  if (j < p) {
+    dc = delta_of(a.bdt[((size_t)slot * a.Q + j) * a.H + h], a.dt_bias[h]);
+    vc.hi = __fmul_rn(dc, a.A[h]);
+  }
+  vc = warp_scan_df(vc, j);
+  cp_async_wait_all();
+  __syncthreads();
+  if (!active) return;
+  float* wx = swa + w * QM * P;
+  float decay = 1.f;
+  if (p > 0) {
+    const df last = {__shfl_sync(kFull, vc.hi, p - 1), __shfl_sync(kFull, vc.lo, p - 1)};
+    const float wl = j < p ? __fmul_rn(dc, expf(df_diff(last, vc))) : 0.f;   // state_weights
+    for (int s = 0; s < p; ++s) {
+      const float ws = __shfl_sync(kFull, wl, s);
+#pragma unroll
+      for (int m = 0; m < P / 32; ++m) wx[s * P + 32 * m + j] = __fmul_rn(ws, to_f(sx[s * P + 32 * m + j]));
+    }
+    __syncwarp();
+    decay = expf(last.hi);
+  }
+  const size_t soff = ((size_t)slot * a.H + h) * P * N;
+  void* R = std::is_same<HT, Nvfp4>::value ? (void*)((uint8_t*)a.read_copy + soff / 2)
+                                           : (void*)((uint8_t*)a.read_copy + soff * sizeof_copy<HT>());
+  stream_flush_copy<T, HT, P, N, false>(a.state + soff, R, a.read_bscale + soff / 16,
+                                        a.read_scale + ((size_t)slot * a.H + h) * P, 0.f, 0.f, 0.f, 0.f, nullptr, j,
+                                        p, wx, decay, sB);
+}
+
+template <typename T, int P, int N, int QM>
+constexpr size_t refresh_heads_smem_bytes() {
+  return (size_t)QM * N * sizeof(T) + (size_t)kHeadsPerCta * QM * P * sizeof(T) +
+         (size_t)kHeadsPerCta * QM * P * sizeof(float);
+}
+
+template <typename T, int P, int N, int QM>
+cudaError_t launch_refresh_heads(const LaunchArgs& a, cudaStream_t s) {
+  const int hpg = a.H / a.G, nbl = (hpg + kHeadsPerCta - 1) / kHeadsPerCta;
+  const dim3 grid(a.G * nbl, a.nseq);
+  constexpr size_t sm = refresh_heads_smem_bytes<T, P, N, QM>();
+  auto run = [&](auto kernel) {
+    cudaError_t e = prep(kernel, sm);
+    if (e != cudaSuccess) return e;
+    kernel<<<grid, kThreads, sm, s>>>(a);
+    return cudaGetLastError();
+  };
+  if (a.read_copy == nullptr) return run(k_refresh_heads<T, NoCopy, P, N, QM>);
+  if constexpr (QM <= 16) {
+    if (a.read_nvfp4) return run(k_refresh_heads<T, Nvfp4, P, N, QM>);
+    if (a.read_fp8) return run(k_refresh_heads<T, uint8_t, P, N, QM>);
+  }
+  if (a.read_fp8 || a.read_nvfp4) return cudaErrorNotSupported;
+  return run(k_refresh_heads<T, __nv_bfloat16, P, N, QM>);
 }
 
 }  // namespace
 
 bool heads_decode_supported(int P, int N, int Q) { return N == 128 && (P == 64) && Q >= 1 && Q <= 32; }
+
+cudaError_t heads_refresh(const LaunchArgs& a, cudaStream_t s) {
+  constexpr int P = 64, N = 128;
+  if (a.io == ERS_DTYPE_BF16) {
+    if (a.Q <= 16) return launch_refresh_heads<__nv_bfloat16, P, N, 16>(a, s);
+    return launch_refresh_heads<__nv_bfloat16, P, N, 32>(a, s);
+  }
+  if (a.Q <= 16) return launch_refresh_heads<float, P, N, 16>(a, s);
+  return launch_refresh_heads<float, P, N, 32>(a, s);
+}
 
 cudaError_t heads_decode(const LaunchArgs& a, cudaStream_t s) {
   constexpr int P = 64, N = 128;
@@ -509,13 +601,3 @@ cudaError_t heads_decode(const LaunchArgs& a, cudaStream_t s) {
 
 }  // namespace ers
 
-namespace ers {
-cudaError_t heads_recast(const LaunchArgs& a, cudaStream_t s) {
-  if (a.nseq <= 0) return cudaSuccess;
-  if (a.read_nvfp4)
-    k_recast<Nvfp4, 64, 128><<<dim3(a.nseq, a.H), kThreads, 0, s>>>(a);
-  else
-    k_recast<uint8_t, 64, 128><<<dim3(a.nseq, a.H), kThreads, 0, s>>>(a);
-  return cudaGetLastError();
-}
-}  // namespace ers

@@ -566,17 +566,14 @@ cudaError_t decode_impl(const LaunchArgs& a, cudaStream_t s) {
 
 template <typename T, int P, int N>
 cudaError_t refresh_impl(const LaunchArgs& a, cudaStream_t s) {
-  const size_t sm = fma_smem_bytes(a.Q, P);
-  cudaError_t e = prep(k_refresh<T, P, N>, sm);
-  if (e != cudaSuccess) return e;
-  if (a.read_fp8 || a.read_nvfp4) {   // fold the anchors, then cast the FP8 / NVFP4 copies from them
-    LaunchArgs b = a;
-    b.read_copy = nullptr;
-    k_refresh<T, P, N><<<dim3(a.nseq, a.H), kThreads, sm, s>>>(b);
-    if ((e = heads_recast(a, s)) != cudaSuccess) return e;
-  } else {
-    k_refresh<T, P, N><<<dim3(a.nseq, a.H), kThreads, sm, s>>>(a);
+  cudaError_t e;
+  if (heads_decode_supported(a.P, a.N, a.Q)) {   // warp-per-head kernel (bf16 / FP8 / NVFP4 copies)
+    if ((e = heads_refresh(a, s)) != cudaSuccess) return e;
+    return launch_setpos(a, 1, s);
   }
+  const size_t sm = fma_smem_bytes(a.Q, P);
+  if ((e = prep(k_refresh<T, P, N>, sm)) != cudaSuccess) return e;
+  k_refresh<T, P, N><<<dim3(a.nseq, a.H), kThreads, sm, s>>>(a);
   return launch_setpos(a, 1, s);
 }
 

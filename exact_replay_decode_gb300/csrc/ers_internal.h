@@ -71,8 +71,8 @@ bool fma_supported(int P, int N);
 bool heads_decode_supported(int P, int N, int Q);
 cudaError_t heads_decode(const LaunchArgs& a, cudaStream_t s);
 // FP8 read-copy recast after a refresh (P = 64, N = 128), ers_decode.cu
-// casts the FP8 or NVFP4 read copy of the slots an ReplaySSM / exact refresh just folded
-cudaError_t heads_recast(const LaunchArgs& a, cudaStream_t s);
+// standalone refresh on the warp-per-head layout (P = 64, N = 128, chunk <= 32), ers_decode.cu
+cudaError_t heads_refresh(const LaunchArgs& a, cudaStream_t s);
 // warp-per-head speculative verify (chunk <= 16, P = 64, N = 128, T <= 4, H/G <= 8), ers_verify.cu
 bool heads_verify_supported(int P, int N, int Q, int T, int H, int G);
 cudaError_t heads_verify(const LaunchArgs& a, cudaStream_t s);
