@@ -224,6 +224,71 @@ def nvfp4_rows_round(a: np.ndarray, parts: bool = False):
     return val
 
 
+# ---- counter-based random numbers and stochastic rounding of an fp16 anchor ---------------------------
+# Philox4x32-10 (Salmon, Moraes, Dror and Shaw, "Parallel random numbers: as easy as 1, 2, 3",
+# SC 2011): a 4 x 32-bit counter and a 2 x 32-bit key; each of 10 rounds multiplies counter words 0
+# and 2 by two constants (64-bit products), mixes the high halves with the other two words and the
+# key, and the key advances by two Weyl constants between rounds.
+PHILOX_M0, PHILOX_M1 = 0xD2511F53, 0xCD9E8D57
+PHILOX_W0, PHILOX_W1 = 0x9E3779B9, 0xBB67AE85
+
+
+def philox4x32_10(ctr: np.ndarray, key: Tuple[int, int]) -> np.ndarray:
+    """ctr [..., 4] uint32 -> [..., 4] uint32 random words."""
+    c = np.asarray(ctr, dtype=np.uint64) & 0xFFFFFFFF
+    k0, k1 = np.uint64(key[0] & 0xFFFFFFFF), np.uint64(key[1] & 0xFFFFFFFF)
+    m32 = np.uint64(0xFFFFFFFF)
+    c0, c1, c2, c3 = c[..., 0], c[..., 1], c[..., 2], c[..., 3]
+    for rnd in range(10):
+        if rnd:
+            k0 = (k0 + np.uint64(PHILOX_W0)) & m32
+            k1 = (k1 + np.uint64(PHILOX_W1)) & m32
+        p0 = c0 * np.uint64(PHILOX_M0)
+        p1 = c2 * np.uint64(PHILOX_M1)
+        hi0, lo0 = p0 >> np.uint64(32), p0 & m32
+        hi1, lo1 = p1 >> np.uint64(32), p1 & m32
+        c0, c1, c2, c3 = hi1 ^ c1 ^ k0, lo1, hi0 ^ c3 ^ k1, lo0
+    return np.stack([c0, c1, c2, c3], axis=-1).astype(np.uint32)
+
+
+FP16_MAX = 65504.0
+
+
+def sr_fp16(v: np.ndarray, r: np.ndarray) -> np.ndarray:
+    """Stochastic rounding of fp32 values to IEEE binary16 with one random 32-bit word r per value:
+    with lo the fp16 value of |v| rounded toward zero and ulp the fp16 spacing there (2^-24 below
+    2^-14), |v| rounds up to lo + ulp iff r < 2^32 (|v| - lo) / ulp, else down to lo; the sign is
+    kept; magnitudes at or above 65504 give 65504.  Returned as fp64 values (all on the fp16 grid)."""
+    f = np.asarray(v, dtype=np.float32).astype(np.float64)
+    a = np.abs(f)
+    _, e = np.frexp(a)                                        # a in [2^(e-1), 2^e)
+    ue = np.maximum(e - 1, -14) - 10                          # log2 of the fp16 spacing at a
+    t = np.ldexp(a, -ue)                                      # exact
+    fl = np.floor(t)
+    frac = t - fl                                             # exact, in [0, 1)
+    up = np.asarray(r, dtype=np.float64) < np.ldexp(frac, 32)
+    out = np.ldexp(fl + up, ue)
+    out = np.where(a >= FP16_MAX, FP16_MAX, out)
+    out = np.where(a == 0, 0.0, out)
+    return np.copysign(out, f)
+
+
+def sr_words(key: Tuple[int, int], nonce: int, slot: int, H: int, P: int, N: int) -> np.ndarray:
+    """The random words of one slot's anchor write: element (h, d, n) takes word n % 4 of
+    philox4x32_10(counter = (nonce, slot, h * P + d, n // 4), key).  Returns [H, P, N] uint32."""
+    hd = np.arange(H * P, dtype=np.uint64)[:, None]
+    jj = np.arange(N // 4, dtype=np.uint64)[None, :]
+    ctr = np.stack(np.broadcast_arrays(np.uint64(nonce & 0xFFFFFFFF), np.uint64(slot & 0xFFFFFFFF), hd, jj), axis=-1)
+    return philox4x32_10(ctr, key).reshape(H, P, N)
+
+
+def sr_fp16_anchor(fin: np.ndarray, key: Tuple[int, int], nonce: int, slot: int) -> np.ndarray:
+    """An fp16 anchor written by stochastic rounding of the refreshed state fin [H, P, N] (taken
+    through fp32, as the GPU folds in fp32) with the slot's random words for this nonce."""
+    H, P, N = fin.shape
+    return sr_fp16(np.asarray(fin, dtype=np.float64).astype(np.float32), sr_words(key, nonce, slot, H, P, N))
+
+
 class _Seq:
     __slots__ = ("x", "dt", "B", "C")
 
@@ -253,10 +318,13 @@ class ReplaySSMModel:
     forms S from committed raw records and casts both copies from it.)
     """
 
-    def __init__(self, params, anchor: np.ndarray, L: int, nthreads: Optional[int] = None, read_cast=None):
+    def __init__(self, params, anchor: np.ndarray, L: int, nthreads: Optional[int] = None, read_cast=None,
+                 anchor_round=None):
         self.A, self.D, self.dt_bias = (_f64(params.A), _f64(params.D), _f64(params.dt_bias))
         self.anchor = np.array(anchor, dtype=np.float64, copy=True)  # [S,H,P,N]
         self.read_cast = read_cast if read_cast is not None else bf16_round
+        # anchor_round(i, fin) -> the stored anchor of sequence i after a refresh (default: fin itself)
+        self.anchor_round = anchor_round
         self.read = self.read_cast(self.anchor)
         self.L = L
         self.nthreads = nthreads
@@ -282,7 +350,7 @@ class ReplaySSMModel:
         (x, dt, B, C), cu = _pack(parts)
         _, fin = recurrence(x, dt, self.A, B, C, self.D, self.dt_bias, cu, self.anchor[which], self.nthreads)
         for k, i in enumerate(which):
-            self.anchor[i] = fin[k]
+            self.anchor[i] = fin[k] if self.anchor_round is None else self.anchor_round(i, fin[k])
             self.read[i] = self.read_cast(fin[k])
             self.committed[i] = []
         self.flushes += len(which)

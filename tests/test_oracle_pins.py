@@ -480,6 +480,62 @@ def test_nvfp4_values_are_codes_times_scales_within_bound():
     assert np.all(err <= 0.25 * np.abs(fb) + 0.25 * bs + 2.0 ** -4 * amax_b * 1.01)
 
 
+def test_philox4x32_10_known_answers():
+    # the generator's published known-answer vectors (counter, key -> output)
+    kat = [((0, 0, 0, 0), (0, 0), (0x6627E8D5, 0xE169C58D, 0xBC57AC4C, 0x9B00DBD8)),
+           ((0xFFFFFFFF,) * 4, (0xFFFFFFFF, 0xFFFFFFFF), (0x408F276D, 0x41C83B0E, 0xA20BC7C6, 0x6D5451FD)),
+           ((0x243F6A88, 0x85A308D3, 0x13198A2E, 0x03707344), (0xA4093822, 0x299F31D0),
+            (0xD16CFE09, 0x94FDCCEB, 0x5001E420, 0x24126EA1))]
+    for ctr, key, want in kat:
+        assert tuple(int(x) for x in oracle.philox4x32_10(np.array(ctr, np.uint64), key)) == want
+    # vectorised over leading axes
+    c = np.array([k[0] for k in kat[:1]] * 3, np.uint64)
+    assert np.array_equal(oracle.philox4x32_10(c, (0, 0)), np.array([kat[0][2]] * 3, np.uint32))
+
+
+def test_sr_fp16_decisions():
+    u = 2.0 ** -10
+    # 1 + ulp/4 rounds up iff r < 2^30; on-grid values never move; the sign is kept
+    assert oracle.sr_fp16(np.float32(1 + u / 4), np.uint32(2 ** 30 - 1)) == 1 + u
+    assert oracle.sr_fp16(np.float32(1 + u / 4), np.uint32(2 ** 30)) == 1.0
+    assert oracle.sr_fp16(np.float32(-(1 + u / 4)), np.uint32(0)) == -(1 + u)
+    # in the subnormal range the spacing is 2^-24: 1.5 * 2^-24 rounds up iff r < 2^31
+    assert oracle.sr_fp16(np.float32(1.5 * 2.0 ** -24), np.uint32(2 ** 31 - 1)) == 2.0 ** -23
+    assert oracle.sr_fp16(np.float32(1.5 * 2.0 ** -24), np.uint32(2 ** 31)) == 2.0 ** -24
+    # saturation at the fp16 maximum, zero stays zero
+    assert oracle.sr_fp16(np.float32(70000.0), np.uint32(0)) == 65504.0
+    assert oracle.sr_fp16(np.float32(0.0), np.uint32(0)) == 0.0
+    rng = np.random.Generator(np.random.PCG64(5))
+    v = (rng.standard_normal(20000) * np.exp2(rng.integers(-30, 15, 20000))).astype(np.float32)
+    grid = v.astype(np.float16).astype(np.float32)
+    for r in (0, 2 ** 31, 2 ** 32 - 1):
+        assert np.array_equal(oracle.sr_fp16(grid, np.full(v.shape, r, np.uint32)), grid.astype(np.float64))
+    # with r = 2^31 - 1 the rule rounds half-way cases up and everything else to nearest: it agrees
+    # with numpy's fp16 conversion (nearest even) except at exact ties
+    out = oracle.sr_fp16(v, np.full(v.shape, 2 ** 31 - 1, np.uint32))
+    lo = oracle.sr_fp16(v, np.full(v.shape, 2 ** 32 - 1, np.uint32))
+    hi = oracle.sr_fp16(v, np.zeros(v.shape, np.uint32))
+    tie = np.abs(np.abs(v.astype(np.float64)) - np.abs(lo)) == np.abs(np.abs(hi) - np.abs(v.astype(np.float64)))
+    ok = np.abs(v) < 65504
+    assert np.array_equal(out[ok & ~tie], v.astype(np.float16).astype(np.float64)[ok & ~tie])
+
+
+def test_sr_words_counter_layout():
+    # element (h, d, n) of a slot takes word n % 4 of the generator at counter (nonce, slot, h*P + d, n // 4)
+    w = oracle.sr_words((7, 9), 3, 5, 2, 4, 8)
+    one = oracle.philox4x32_10(np.array([3, 5, 1 * 4 + 2, 1], np.uint64), (7, 9))
+    assert np.array_equal(w[1, 2, 4:8], one)
+    assert not np.array_equal(oracle.sr_words((7, 9), 4, 5, 2, 4, 8), w)   # a new nonce, new words
+
+
+def test_sr_fp16_is_unbiased():
+    # averaged over an even grid of r, the rounded value equals the input to within the grid step
+    v = np.float32(1 + 0.3 * 2.0 ** -10)
+    rs = (np.arange(4096, dtype=np.uint64) * (2 ** 32 // 4096)).astype(np.uint32)
+    mean = oracle.sr_fp16(np.full(4096, v, np.float32), rs).mean()
+    assert abs(mean - float(v)) <= 2.0 ** -10 / 4096
+
+
 def test_protocol_anchor_independent_of_fp8_read_copy():
     """The fp32 anchor is the same whether outputs read a bf16, an FP8 or an NVFP4 copy."""
     params, anchor, drafts, acc, L = _protocol_case(17, steps=12, N=32)   # two 16-value blocks per row
