@@ -382,7 +382,7 @@ def _copy_bytes(d, read_dtype: str) -> int:
     return rows * (d.dstate // 2 + d.dstate // 16 + 4)
 
 
-def bench_verify(dev, steps: int, hbm: float, read_dtype: str = "bf16"):
+def bench_verify(dev, steps: int, hbm: float, read_dtype: str = "bf16", anchor: str = "fp32"):
     import torch
     import exact_replay_decode_gb300 as ers
     from synth import torch_io
@@ -396,9 +396,10 @@ def bench_verify(dev, steps: int, hbm: float, read_dtype: str = "bf16"):
     cu = torch.arange(0, S * 32 + 1, 32, dtype=torch.int32, device=dev)
     _, fin = ers.ssd_scan_fwd(hx, hdt, prm, hB, hC, chunk=L, cu_seqlens=cu)
     cache = ers.ReplayCache(S, d.nheads, d.ngroups, d.headdim, d.dstate, L, torch.bfloat16, read_copy=True,
-                            read_dtype=read_dtype)
+                            read_dtype=read_dtype, anchor=anchor, sr_key=(0x5EED, 0xF00D))
     cache.state.copy_(fin)
     ers.refresh(cache, prm, replayssm=True, drafts_T=L + 1)
+    anchor_bytes = d.nheads * d.headdim * d.dstate * (2 if anchor == "fp16_sr" else 4)
     # read copy per sequence: bf16 values, or FP8 codes + one fp32 scale per state row
     copy_bytes = _copy_bytes(d, read_dtype)
     dx, ddt, dB, dC = torch_io.tokens_to(drafts, dev, lead=(steps, S, T))
@@ -413,7 +414,7 @@ def bench_verify(dev, steps: int, hbm: float, read_dtype: str = "bf16"):
         base = np.where(flush, 0, hs)
         total_bytes += S * (copy_bytes + 50_176 + 50_176 + 32_768) + int(base.sum()) * 10_496
         # a flushing slot reads and writes its fp32 anchor and writes its copy instead of reading it
-        total_bytes += int(flush.sum()) * (2_097_152 + 2_097_152 + copy_bytes - copy_bytes) + \
+        total_bytes += int(flush.sum()) * (2 * anchor_bytes + copy_bytes - copy_bytes) + \
             int(hs[flush].sum()) * 10_496
         hs = base + acc[k]
     torch.cuda.synchronize()
@@ -421,6 +422,7 @@ def bench_verify(dev, steps: int, hbm: float, read_dtype: str = "bf16"):
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(s)
     for k in range(steps):
+        cache.sr_nonce = k + 1
         ers.spec_verify(cache, prm, dx[k], ddt[k], dB[k], dC[k], status=st, check=False, out=y)
         ers.commit(cache, acc_t[k], T, status=st, check=False)
     e1.record(s)
@@ -428,17 +430,18 @@ def bench_verify(dev, steps: int, hbm: float, read_dtype: str = "bf16"):
     st.raise_if_error("bench verify")
     ms = e0.elapsed_time(e1)
     ach = total_bytes / (ms * 1e-3) / 1e9
-    return {"read_copy": read_dtype, "seq_verify_steps_per_s": S * steps / (ms * 1e-3),
+    return {"read_copy": read_dtype, "anchor": anchor, "seq_verify_steps_per_s": S * steps / (ms * 1e-3),
             "committed_tok_per_s": float(acc.sum()) / (ms * 1e-3), "us_per_step": ms * 1e3 / steps,
             "achieved_gbs": ach, "hbm_frac": ach / hbm, "algorithmic_bytes": total_bytes, "steps": steps}
 
 
-def bench_rssm_decode(dev, cycles: int, hbm: float, read_dtype: str):
+def bench_rssm_decode(dev, cycles: int, hbm: float, read_dtype: str, anchor: str = "fp32"):
     """Non-speculative ReplaySSM decode of the B=256 decode workload: each step is one fused decode
     call, which applies the flush rule for one token (h + 1 > L: fold the anchor, recast the read
     copy) and decodes from the read copy.  One ring cycle of steps (TOKEN_RING) is captured as a
     CUDA graph and replayed, so the host's per-call overhead does not pace the GPU.  Start positions
-    h0 ~ U{0..L-1} per sequence (untimed decodes of slot subsets)."""
+    h0 ~ U{0..L-1} per sequence (untimed decodes of slot subsets).  anchor "fp16_sr": fp16 anchors
+    written by stochastic rounding (nonce = the ring step; the graph replays the same nonces)."""
     import torch
     import exact_replay_decode_gb300 as ers
     from synth import torch_io
@@ -454,7 +457,7 @@ def bench_rssm_decode(dev, cycles: int, hbm: float, read_dtype: str):
     _, fin = ers.ssd_scan_fwd(hx, hdt, prm, hB, hC, chunk=L, cu_seqlens=cu)
     del hx, hdt, hB, hC
     cache = ers.ReplayCache(S, d.nheads, d.ngroups, d.headdim, d.dstate, L, torch.bfloat16, read_copy=True,
-                            read_dtype=read_dtype)
+                            read_dtype=read_dtype, anchor=anchor, sr_key=(0x5EED, 0xF00D))
     cache.state.copy_(fin)
     ers.refresh(cache, prm, replayssm=True, drafts_T=L + 1)           # h = 0: cast the read copy
     tok = torch_io.tokens_to(stream, dev, lead=(TOKEN_RING, S))
@@ -468,6 +471,7 @@ def bench_rssm_decode(dev, cycles: int, hbm: float, read_dtype: str):
                               fuse_refresh=False)
 
     def step(k):
+        cache.sr_nonce = k
         ers.replay_decode(cache, prm, *(t[k] for t in tok), replayssm=True, fuse_refresh=True, status=st,
                           check=False, out=y)
 
@@ -475,6 +479,7 @@ def bench_rssm_decode(dev, cycles: int, hbm: float, read_dtype: str):
     # h buffered rows and writes the copy; a decode reads the copy, h rows and the new token, writes
     # the token to the buffer and y
     copy_bytes = _copy_bytes(d, read_dtype)
+    anchor_bytes = d.nheads * d.headdim * d.dstate * (2 if anchor == "fp16_sr" else 4)
     hs = h0.astype(np.int64)
 
     def cycle_bytes():
@@ -482,7 +487,7 @@ def bench_rssm_decode(dev, cycles: int, hbm: float, read_dtype: str):
         b = 0
         for _ in range(TOKEN_RING):
             fl = hs + 1 > L
-            b += int(fl.sum()) * (2 * 2_097_152 + copy_bytes) + int(hs[fl].sum()) * 10_496
+            b += int(fl.sum()) * (2 * anchor_bytes + copy_bytes) + int(hs[fl].sum()) * 10_496
             hs = np.where(fl, 0, hs)
             b += S * (copy_bytes + 12_544 + 12_544 + 8_192) + int(hs.sum()) * 10_496
             hs = hs + 1
@@ -510,7 +515,7 @@ def bench_rssm_decode(dev, cycles: int, hbm: float, read_dtype: str):
     nsteps = cycles * TOKEN_RING
     ms = e0.elapsed_time(e1) / nsteps
     ach = total / nsteps / (ms * 1e-3) / 1e9
-    return {"read_copy": read_dtype, "seq_steps_per_s": S / (ms * 1e-3), "us_per_step": ms * 1e3,
+    return {"read_copy": read_dtype, "anchor": anchor, "seq_steps_per_s": S / (ms * 1e-3), "us_per_step": ms * 1e3,
             "achieved_gbs": ach, "hbm_frac": ach / hbm, "bytes_per_step": total / nsteps, "steps": nsteps,
             "launches_per_step": 1}
 
@@ -655,12 +660,14 @@ def main(argv=None):
             out = {n: bench_prefill(dev, n, 10, args.warmup, hbm, tc) for n in ("prefill_2048_h32", "varlen_4seq_h64")}
         elif args.section == "rssm":
             out = {r: bench_rssm_decode(dev, 4, hbm, r) for r in ("bf16", "fp8", "nvfp4")}
+            out["nvfp4_fp16sr"] = bench_rssm_decode(dev, 4, hbm, "nvfp4", "fp16_sr")
         elif args.section == "verify":
             out = bench_verify(dev, 32, hbm)
             fp8 = bench_verify(dev, 32, hbm, "fp8")
             nv4 = bench_verify(dev, 32, hbm, "nvfp4")
+            nv4sr = bench_verify(dev, 32, hbm, "nvfp4", "fp16_sr")
             if rank == 0:
-                print(json.dumps({"verify_fp8": fp8, "verify_nvfp4": nv4}))
+                print(json.dumps({"verify_fp8": fp8, "verify_nvfp4": nv4, "verify_nvfp4_fp16sr": nv4sr}))
         else:
             out = bench_ssu(dev, 16, hbm)
         if rank == 0:
@@ -685,7 +692,9 @@ def main(argv=None):
         extra["verify"] = bench_verify(dev, 32, hbm)
         extra["verify_fp8"] = bench_verify(dev, 32, hbm, "fp8")
         extra["verify_nvfp4"] = bench_verify(dev, 32, hbm, "nvfp4")
+        extra["verify_nvfp4_fp16sr"] = bench_verify(dev, 32, hbm, "nvfp4", "fp16_sr")
         extra["replayssm_decode"] = {r: bench_rssm_decode(dev, 4, hbm, r) for r in ("bf16", "fp8", "nvfp4")}
+        extra["replayssm_decode"]["nvfp4_fp16sr"] = bench_rssm_decode(dev, 4, hbm, "nvfp4", "fp16_sr")
         extra["ssu"] = bench_ssu(dev, 16, hbm)
     line = {
         "metric": "replay-decode seq-steps/s per layer @B=256",

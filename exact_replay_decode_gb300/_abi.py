@@ -28,6 +28,9 @@ READ_BF16 = 0
 READ_FP8_E4M3 = 1
 READ_NVFP4 = 2
 
+ANCHOR_F32 = 0
+ANCHOR_F16_SR = 1
+
 # Every function include/ers.h declares.
 EXPORTS = (
     "ers_status_str", "ers_version", "ers_ssd_scan_fwd_workspace_size", "ers_ssd_scan_fwd",
@@ -55,7 +58,8 @@ class Cache(ctypes.Structure):
     _fields_ = [("state", ctypes.c_void_p), ("read_copy", ctypes.c_void_p), ("buf_x", ctypes.c_void_p),
                 ("buf_dt", ctypes.c_void_p), ("buf_B", ctypes.c_void_p), ("buf_C", ctypes.c_void_p),
                 ("pos", ctypes.c_void_p), ("nslots", ctypes.c_int32), ("read_dtype", ctypes.c_int32),
-                ("read_scale", ctypes.c_void_p), ("read_block_scale", ctypes.c_void_p)]
+                ("read_scale", ctypes.c_void_p), ("read_block_scale", ctypes.c_void_p),
+                ("anchor_dtype", ctypes.c_int32), ("sr_key", ctypes.c_uint32 * 2), ("sr_nonce", ctypes.c_uint32)]
 
 
 _lib = None

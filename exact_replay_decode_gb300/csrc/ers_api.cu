@@ -50,11 +50,21 @@ bool narrow_read_shape(const ers_dims* d) {
 }
 bool has_narrow_copy(const ers_cache* c) { return c->read_copy != nullptr && c->read_dtype != ERS_READ_BF16; }
 bool has_nvfp4_copy(const ers_cache* c) { return c->read_copy != nullptr && c->read_dtype == ERS_READ_NVFP4; }
+bool f16_anchor(const ers_cache* c) { return c->anchor_dtype == ERS_ANCHOR_F16_SR; }
+
+// fp16 anchors: ReplaySSM calls only, bf16 io, a read copy, the warp-per-head shapes.
+ers_status check_f16_anchor(const ers_dims* d, const ers_cache* c, bool rssm) {
+  if (!f16_anchor(c)) return ERS_OK;
+  if (!rssm || d->io_dtype != ERS_DTYPE_BF16 || c->read_copy == nullptr || !narrow_read_shape(d))
+    return ERS_EUNSUPPORTED;
+  return ERS_OK;
+}
 
 ers_status check_cache(const ers_cache* c, bool need_read_copy) {
   if (c == nullptr || c->nslots < 0) return ERS_EINVAL;
   if (c->read_dtype != ERS_READ_BF16 && c->read_dtype != ERS_READ_FP8_E4M3 && c->read_dtype != ERS_READ_NVFP4)
     return ERS_EDTYPE;
+  if (c->anchor_dtype != ERS_ANCHOR_F32 && c->anchor_dtype != ERS_ANCHOR_F16_SR) return ERS_EDTYPE;
   ERS_TRY(check_state_ptrs(c));
   ERS_TRY(check_ptr(c->read_copy, need_read_copy));
   if (c->read_dtype != ERS_READ_BF16 && c->read_copy != nullptr) ERS_TRY(check_ptr(c->read_scale, true));
@@ -85,12 +95,16 @@ LaunchArgs base_args(const ers_dims* d, const ers_params* p) {
 }
 
 void set_cache(LaunchArgs& a, const ers_cache* c) {
-  a.state = c->state;
+  a.state = (float*)c->state;   // fp16 data when anchor_f16
   a.read_copy = c->read_copy;
   a.read_fp8 = c->read_copy != nullptr && c->read_dtype == ERS_READ_FP8_E4M3;
   a.read_nvfp4 = c->read_copy != nullptr && c->read_dtype == ERS_READ_NVFP4;
   a.read_scale = c->read_scale;
   a.read_bscale = c->read_block_scale;
+  a.anchor_f16 = c->anchor_dtype == ERS_ANCHOR_F16_SR;
+  a.sr_key0 = c->sr_key[0];
+  a.sr_key1 = c->sr_key[1];
+  a.sr_nonce = c->sr_nonce;
   a.bx = c->buf_x;
   a.bdt = c->buf_dt;
   a.bB = c->buf_B;
@@ -208,6 +222,7 @@ ers_status ers_chunked_prefill(const ers_dims* dims, const ers_params* prm, cons
   ERS_TRY(check_dims(dims));
   ERS_TRY(check_params(prm));
   ERS_TRY(check_cache(cache, false));
+  if (f16_anchor(cache)) return ERS_EUNSUPPORTED;   // chunked prefill writes fp32 checkpoints
   if (nseq < 0 || ntokens < 0 || max_seqlen < 0) return ERS_EINVAL;
   if (nseq == 0) return ERS_OK;
   if (slot == nullptr && nseq > cache->nslots) return ERS_EINVAL;
@@ -254,6 +269,7 @@ ers_status ers_replay_decode(const ers_dims* dims, const ers_params* prm, const 
   ERS_TRY(check_ptr(dev_status, false));
   if (has_narrow_copy(cache) && !narrow_read_shape(dims)) return ERS_EUNSUPPORTED;
   if (has_nvfp4_copy(cache) && !rssm) return ERS_EUNSUPPORTED;   // NVFP4 copies: ReplaySSM mode only
+  ERS_TRY(check_f16_anchor(dims, cache, rssm));
   LaunchArgs a = base_args(dims, prm);
   set_cache(a, cache);
   a.x = x; a.dt = dt; a.B = B; a.C = C;
@@ -291,6 +307,7 @@ ers_status ers_refresh(const ers_dims* dims, const ers_params* prm, const ers_ca
   ERS_TRY(check_ptr(dev_status, false));
   if (has_narrow_copy(cache) && !narrow_read_shape(dims)) return ERS_EUNSUPPORTED;
   if (has_nvfp4_copy(cache) && !(flags & ERS_FLAG_REPLAYSSM)) return ERS_EUNSUPPORTED;
+  ERS_TRY(check_f16_anchor(dims, cache, (flags & ERS_FLAG_REPLAYSSM) != 0));
   LaunchArgs a = base_args(dims, prm);
   set_cache(a, cache);
   a.slot = slot;
@@ -316,10 +333,11 @@ ers_status ers_spec_verify(const ers_dims* dims, const ers_params* prm, const er
   ERS_TRY(check_tokens(x, dt, B, C, true));
   ERS_TRY(check_ptr(y, true));
   ERS_TRY(check_ptr(dev_status, false));
-  if (has_narrow_copy(cache) && !(narrow_read_shape(dims) && ers::heads_verify_supported(dims->headdim, dims->dstate,
-                                                                                       dims->chunk, T, dims->nheads,
-                                                                                       dims->ngroups)))
+  if ((has_narrow_copy(cache) || f16_anchor(cache)) &&
+      !(narrow_read_shape(dims) && ers::heads_verify_supported(dims->headdim, dims->dstate, dims->chunk, T,
+                                                               dims->nheads, dims->ngroups)))
     return ERS_EUNSUPPORTED;
+  ERS_TRY(check_f16_anchor(dims, cache, true));
   LaunchArgs a = base_args(dims, prm);
   set_cache(a, cache);
   a.x = x; a.dt = dt; a.B = B; a.C = C;

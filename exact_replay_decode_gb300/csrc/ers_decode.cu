@@ -175,11 +175,11 @@ __host__ __device__ constexpr size_t sizeof_copy() {   // bytes per value of a b
   return std::is_same<HT, __nv_bfloat16>::value ? 2 : 1;
 }
 
-template <typename T, typename HT, int P, int N, bool kOut = true>
-__device__ __noinline__ void stream_flush_copy(float* __restrict__ Hd, void* __restrict__ R, uint8_t* __restrict__ Rb,
+template <typename T, typename HT, int P, int N, bool kOut = true, typename AT = float>
+__device__ __noinline__ void stream_flush_copy(AT* __restrict__ Hd, void* __restrict__ R, uint8_t* __restrict__ Rb,
                                                float* __restrict__ Rs, float c0, float c1, float c2, float c3,
                                                float* yo, int j, int hc, const float* wx, float decay,
-                                               const T* sB) {
+                                               const T* sB, SrCtr sr, uint32_t row0) {
   constexpr int NBLK = P / 8;
   constexpr bool kF8 = std::is_same<HT, uint8_t>::value;
   constexpr bool kNv = std::is_same<HT, Nvfp4>::value;
@@ -187,7 +187,7 @@ __device__ __noinline__ void stream_flush_copy(float* __restrict__ Hd, void* __r
   const float c[4] = {c0, c1, c2, c3};
   float4 cur[8], nxt[8];
 #pragma unroll
-  for (int r = 0; r < 8; ++r) cur[r] = __ldcs(reinterpret_cast<const float4*>(Hd + (size_t)r * N + 4 * j));
+  for (int r = 0; r < 8; ++r) cur[r] = anchor_ld<AT>(Hd, (size_t)r * N + 4 * j);
   float part[16];
   float srow = 0.f;
 #pragma unroll 1
@@ -195,7 +195,7 @@ __device__ __noinline__ void stream_flush_copy(float* __restrict__ Hd, void* __r
     if (blk + 1 < NBLK) {
 #pragma unroll
       for (int r = 0; r < 8; ++r)
-        nxt[r] = __ldcs(reinterpret_cast<const float4*>(Hd + (size_t)((blk + 1) * 8 + r) * N + 4 * j));
+        nxt[r] = anchor_ld<AT>(Hd, (size_t)((blk + 1) * 8 + r) * N + 4 * j);
     }
     float pb[8];
 #pragma unroll
@@ -223,7 +223,7 @@ __device__ __noinline__ void stream_flush_copy(float* __restrict__ Hd, void* __r
 #pragma unroll
         for (int e = 0; e < 4; ++e) v[e] = hc > 0 ? __fmaf_rn(decay, h[e], acc[r4][e]) : h[e];
         const size_t o = (size_t)(blk * 8 + r) * N + 4 * j;
-        if (hc > 0) *reinterpret_cast<float4*>(Hd + o) = make_float4(v[0], v[1], v[2], v[3]);
+        if (hc > 0) anchor_st<AT>(Hd, o, v, sr, row0 + blk * 8 + r, j);
         float ls = 1.f;
         if constexpr (kNv) {
           float sr;
@@ -284,7 +284,8 @@ __device__ __forceinline__ void advance_pos(int32_t* pos, int ncta, int32_t newp
 
 // HT: what the output stream reads (fp32 checkpoint, bf16 or FP8 read copy); W8: the read copy a
 // fused refresh writes is FP8 (else bf16, or none when read_copy is null).
-template <typename T, typename HT, bool W8, int P, int N, int QM>
+// AT: the ReplaySSM anchor's type (fp32, or fp16 written by stochastic rounding).
+template <typename T, typename HT, bool W8, int P, int N, int QM, typename AT = float>
 __global__ void __launch_bounds__(kThreads, 2) k_decode_heads(LaunchArgs a) {
   static_assert(N == 128 && P % 32 == 0, "lane split of Dot<128>; 32-row reduction blocks");
   static_assert(QM <= 32, "one warp scans the chunk");
@@ -421,11 +422,12 @@ __global__ void __launch_bounds__(kThreads, 2) k_decode_heads(LaunchArgs a) {
     }
     __syncwarp();
     if constexpr (!std::is_same<HT, float>::value)
-      stream_flush_copy<T, HT, P, N>(a.state + soff,
+      stream_flush_copy<T, HT, P, N, true, AT>((AT*)a.state + soff,
                                      std::is_same<HT, Nvfp4>::value ? (void*)((uint8_t*)a.read_copy + soff / 2)
                                                                     : (void*)((HT*)a.read_copy + soff),
                                      a.read_bscale + soff / 16, a.read_scale + ((size_t)slot * a.H + h) * P, c[0],
-                                     c[1], c[2], c[3], yo, j, p, wx, expf(last.hi), sB);
+                                     c[1], c[2], c[3], yo, j, p, wx, expf(last.hi), sB,
+                                     SrCtr{a.sr_key0, a.sr_key1, a.sr_nonce, (uint32_t)slot}, (uint32_t)(h * P));
   } else {
     stream_state<HT, P, N>(src, q, c, yo, j, sc);
   }
@@ -464,6 +466,14 @@ cudaError_t launch_decode_heads(const LaunchArgs& a, cudaStream_t s) {
     kernel<<<grid, kThreads, sm, s>>>(a);
     return cudaGetLastError();   // the kernel advances the positions itself
   };
+  if constexpr (QM <= 16 && std::is_same<T, __nv_bfloat16>::value) {   // fp16 anchors: ReplaySSM only
+    if (a.anchor_f16 && rssm) {
+      if (a.read_nvfp4) return run(k_decode_heads<T, Nvfp4, false, P, N, QM, __half>);
+      if (a.read_fp8) return run(k_decode_heads<T, uint8_t, true, P, N, QM, __half>);
+      return run(k_decode_heads<T, __nv_bfloat16, false, P, N, QM, __half>);
+    }
+  }
+  if (a.anchor_f16) return cudaErrorNotSupported;
   if constexpr (QM <= 16) {   // FP8 read copies: chunk <= 16 only (checked by the API)
     if (a.read_fp8)
       return rssm ? run(k_decode_heads<T, uint8_t, true, P, N, QM>) : run(k_decode_heads<T, float, true, P, N, QM>);
@@ -482,7 +492,7 @@ cudaError_t launch_decode_heads(const LaunchArgs& a, cudaStream_t s) {
 // CTA per (sequence, 8 heads of a group), so a launch has 8x fewer CTAs than one per (sequence,
 // head), and the read copy (bf16, FP8 or NVFP4) is cast in the same pass from the fp32 values.
 // Positions are reset by k_setpos afterwards.
-template <typename T, typename HT, int P, int N, int QM>
+template <typename T, typename HT, int P, int N, int QM, typename AT = float>
 __global__ void __launch_bounds__(kThreads, 2) k_refresh_heads(LaunchArgs a) {
   extern __shared__ __align__(16) unsigned char rsm[];
   T* sB = reinterpret_cast<T*>(rsm);                          // [QM][N] group B rows
@@ -544,9 +554,11 @@ __global__ void __launch_bounds__(kThreads, 2) k_refresh_heads(LaunchArgs a) {
   const size_t soff = ((size_t)slot * a.H + h) * P * N;
   void* R = std::is_same<HT, Nvfp4>::value ? (void*)((uint8_t*)a.read_copy + soff / 2)
                                            : (void*)((uint8_t*)a.read_copy + soff * sizeof_copy<HT>());
-  stream_flush_copy<T, HT, P, N, false>(a.state + soff, R, a.read_bscale + soff / 16,
-                                        a.read_scale + ((size_t)slot * a.H + h) * P, 0.f, 0.f, 0.f, 0.f, nullptr, j,
-                                        p, wx, decay, sB);
+  stream_flush_copy<T, HT, P, N, false, AT>((AT*)a.state + soff, R, a.read_bscale + soff / 16,
+                                            a.read_scale + ((size_t)slot * a.H + h) * P, 0.f, 0.f, 0.f, 0.f, nullptr,
+                                            j, p, wx, decay, sB,
+                                            SrCtr{a.sr_key0, a.sr_key1, a.sr_nonce, (uint32_t)slot},
+                                            (uint32_t)(h * P));
 }
 
 template <typename T, int P, int N, int QM>
@@ -566,6 +578,14 @@ cudaError_t launch_refresh_heads(const LaunchArgs& a, cudaStream_t s) {
     kernel<<<grid, kThreads, sm, s>>>(a);
     return cudaGetLastError();
   };
+  if constexpr (QM <= 16 && std::is_same<T, __nv_bfloat16>::value) {   // fp16 anchors (checked by the API)
+    if (a.anchor_f16) {
+      if (a.read_nvfp4) return run(k_refresh_heads<T, Nvfp4, P, N, QM, __half>);
+      if (a.read_fp8) return run(k_refresh_heads<T, uint8_t, P, N, QM, __half>);
+      return run(k_refresh_heads<T, __nv_bfloat16, P, N, QM, __half>);
+    }
+  }
+  if (a.anchor_f16) return cudaErrorNotSupported;
   if (a.read_copy == nullptr) return run(k_refresh_heads<T, NoCopy, P, N, QM>);
   if constexpr (QM <= 16) {
     if (a.read_nvfp4) return run(k_refresh_heads<T, Nvfp4, P, N, QM>);

@@ -37,6 +37,8 @@ struct LaunchArgs {
   int read_nvfp4;      // read copy is NVFP4: e2m1 codes, e4m3 block scales (read_bscale), row scales
   float* read_scale;
   uint8_t* read_bscale;   // NVFP4 block scales [nslots, H, P, N / 16]
+  int anchor_f16;         // ReplaySSM anchor stored as fp16 (state points to __half), written by SR
+  uint32_t sr_key0, sr_key1, sr_nonce;   // counter-based random words for the SR writes
   void* bx;
   float* bdt;
   void* bB;

@@ -78,18 +78,18 @@ __device__ __forceinline__ void stream_read_copy(const RowSrc<HT, N>& src,
 // the anchor, cast into the read copy (CT: bf16, FP8 or NVFP4), and the cast values feed the
 // drafts' dot products (yo as above).  wx[s * P + d] = w_s x_s[d] is precomputed per warp; 8 rows
 // per pass.
-template <typename T, typename CT, int P, int N>
-__device__ __noinline__ void stream_anchor_flush(float* __restrict__ Hd, void* __restrict__ R,
+template <typename T, typename CT, int P, int N, typename AT>
+__device__ __noinline__ void stream_anchor_flush(AT* __restrict__ Hd, void* __restrict__ R,
                                                  uint8_t* __restrict__ Rb, float* __restrict__ Rs,
                                                  const float (&c)[kDraftsMax][4], float* yo, int j, int hc,
-                                                 const float* wx, float decay, const T* sB) {
+                                                 const float* wx, float decay, const T* sB, SrCtr sr, uint32_t row0) {
   constexpr bool kF8 = std::is_same<CT, uint8_t>::value, kNv = std::is_same<CT, Nvfp4>::value;
 #pragma unroll 1
   for (int d0 = 0; d0 < P; d0 += 8) {
     float h[8][4], acc[8][4];
 #pragma unroll
     for (int r = 0; r < 8; ++r) {
-      Quad<float>::unpack(__ldcs(reinterpret_cast<const float4*>(Hd + (size_t)(d0 + r) * N + 4 * j)), h[r]);
+      Quad<float>::unpack(anchor_ld<AT>(Hd, (size_t)(d0 + r) * N + 4 * j), h[r]);
 #pragma unroll
       for (int e = 0; e < 4; ++e) acc[r][e] = 0.f;
     }
@@ -112,7 +112,7 @@ __device__ __noinline__ void stream_anchor_flush(float* __restrict__ Hd, void* _
 #pragma unroll
       for (int e = 0; e < 4; ++e) v[e] = __fmaf_rn(decay, h[r][e], acc[r][e]);
       const size_t o = (size_t)(d0 + r) * N + 4 * j;
-      *reinterpret_cast<float4*>(Hd + o) = make_float4(v[0], v[1], v[2], v[3]);
+      anchor_st<AT>(Hd, o, v, sr, row0 + d0 + r, j);
       float rv[4];   // what the read copy now holds (FP8 / NVFP4: the codes, scaled as they are read)
       float ls = 1.f;
       if constexpr (kNv) {
@@ -147,7 +147,7 @@ __device__ __noinline__ void stream_anchor_flush(float* __restrict__ Hd, void* _
   __syncwarp();
 }
 
-template <typename T, typename HT, int P, int N, int QM>
+template <typename T, typename HT, int P, int N, int QM, typename AT = float>
 __global__ void __launch_bounds__(kThreads, 2) k_verify_heads(LaunchArgs a) {
   static_assert(N == 128 && P % 8 == 0 && QM <= 32 - kDraftsMax, "lane split of Dot<128>; one warp scans");
   constexpr int QR = QM + kDraftsMax;
@@ -277,11 +277,12 @@ __global__ void __launch_bounds__(kThreads, 2) k_verify_heads(LaunchArgs a) {
   __syncthreads();
   if (!active) return;
   if (flush)
-    stream_anchor_flush<T, HT, P, N>(a.state + soff,
+    stream_anchor_flush<T, HT, P, N, AT>((AT*)a.state + soff,
                                      std::is_same<HT, Nvfp4>::value ? (void*)((uint8_t*)a.read_copy + soff / 2)
                                                                     : (void*)((HT*)a.read_copy + soff),
                                      a.read_bscale + soff / 16, a.read_scale + ((size_t)slot * a.H + h) * P, c, yo,
-                                     j, hc, sw, decay, sB);
+                                     j, hc, sw, decay, sB, SrCtr{a.sr_key0, a.sr_key1, a.sr_nonce, (uint32_t)slot},
+                                         (uint32_t)(h * P));
   // outputs of draft k (row t_k = h0 + k), d = j + 32 m: one pass over the rows s serves every draft
   // (each draft's sum still runs over s = 0..t_k in order)
   const float Dh = a.D[h];
@@ -346,13 +347,13 @@ __global__ void __launch_bounds__(kThreads, 2) k_verify_heads(LaunchArgs a) {
   }
 }
 
-template <typename T, typename HT, int QM>
+template <typename T, typename HT, int QM, typename AT = float>
 cudaError_t launch_verify_heads(const LaunchArgs& a, cudaStream_t s) {
   constexpr int P = 64, N = 128;
   constexpr size_t sm = verify_smem_bytes<T, P, N, QM>();
-  cudaError_t e = prep(k_verify_heads<T, HT, P, N, QM>, sm);
+  cudaError_t e = prep(k_verify_heads<T, HT, P, N, QM, AT>, sm);
   if (e != cudaSuccess) return e;
-  k_verify_heads<T, HT, P, N, QM><<<dim3(a.G, a.nseq), kThreads, sm, s>>>(a);
+  k_verify_heads<T, HT, P, N, QM, AT><<<dim3(a.G, a.nseq), kThreads, sm, s>>>(a);
   return cudaGetLastError();
 }
 
@@ -364,6 +365,12 @@ bool heads_verify_supported(int P, int N, int Q, int T, int H, int G) {
 }
 
 cudaError_t heads_verify(const LaunchArgs& a, cudaStream_t s) {
+  if (a.anchor_f16) {   // fp16 anchors: bf16 io only (checked by the API)
+    if (a.io != ERS_DTYPE_BF16) return cudaErrorNotSupported;
+    if (a.read_nvfp4) return launch_verify_heads<__nv_bfloat16, Nvfp4, 16, __half>(a, s);
+    if (a.read_fp8) return launch_verify_heads<__nv_bfloat16, uint8_t, 16, __half>(a, s);
+    return launch_verify_heads<__nv_bfloat16, __nv_bfloat16, 16, __half>(a, s);
+  }
   if (a.read_fp8) {
     if (a.io == ERS_DTYPE_BF16) return launch_verify_heads<__nv_bfloat16, uint8_t, 16>(a, s);
     return launch_verify_heads<float, uint8_t, 16>(a, s);

@@ -251,6 +251,72 @@ __device__ __forceinline__ void nvfp4_store_row(const float (&v)[4], uint8_t* C4
   nvfp4_codes(c | (bs << 16), rv, &bb);
 }
 
+// ---- fp16 anchors written by stochastic rounding (ReplaySSM "FP16+SR" recurrence) --------------------
+// Random words: Philox4x32-10 (Salmon et al., "Parallel random numbers: as easy as 1, 2, 3", SC 2011)
+// at counter (nonce, slot, h * P + d, j) with the caller's 64-bit key; word e serves value 4j + e of
+// row d.  Rounding: |v| goes up to the next fp16 value iff r < 2^32 (|v| - lo) / ulp, lo = |v|
+// rounded toward zero on the fp16 grid, ulp its spacing (2^-24 below 2^-14); the sign is kept;
+// magnitudes >= 65504 give 65504.
+struct SrCtr {
+  uint32_t k0, k1, nonce, slot;
+};
+
+__device__ __forceinline__ uint4 philox4x32_10(uint4 c, uint32_t k0, uint32_t k1) {
+#pragma unroll
+  for (int rnd = 0; rnd < 10; ++rnd) {
+    if (rnd) {
+      k0 += 0x9E3779B9u;
+      k1 += 0xBB67AE85u;
+    }
+    const uint32_t hi0 = __umulhi(0xD2511F53u, c.x), lo0 = 0xD2511F53u * c.x;
+    const uint32_t hi1 = __umulhi(0xCD9E8D57u, c.z), lo1 = 0xCD9E8D57u * c.z;
+    c = make_uint4(hi1 ^ c.y ^ k0, lo1, hi0 ^ c.w ^ k1, lo0);
+  }
+  return c;
+}
+
+__device__ __forceinline__ uint16_t sr_fp16_bits(float v, uint32_t r) {
+  const uint32_t b = __float_as_uint(v);
+  const uint16_t sign = (uint16_t)((b >> 16) & 0x8000u);
+  const float a = __uint_as_float(b & 0x7FFFFFFFu);
+  if (!(a < 65504.f)) return sign | 0x7BFFu;   // saturate (65504)
+  if (a == 0.f) return sign;
+  const int e = (int)((b >> 23) & 0xFFu) - 127;   // floor(log2 a) for a normal a; fp32-subnormal a: -127
+  const int ue = max(e, -14) - 10;                // log2 of the fp16 spacing at a
+  const float t = __fmul_rn(a, __uint_as_float((uint32_t)(127 - ue) << 23));   // a / 2^ue, exact
+  const float fl = floorf(t);
+  const float x = __fmul_rn(__fsub_rn(t, fl), 4294967296.f);                   // frac * 2^32, exact
+  const bool up = (unsigned long long)r < (unsigned long long)ceilf(x);
+  const float q = __fmul_rn(__fadd_rn(fl, up ? 1.f : 0.f), __uint_as_float((uint32_t)(127 + ue) << 23));
+  return sign | __half_as_ushort(__float2half_rn(q));   // q is on the fp16 grid: the conversion is exact
+}
+
+// One lane's 4 anchor values of row d (offset o = d * N + 4j): fp32, or fp16 read exactly.
+template <typename AT>
+__device__ __forceinline__ float4 anchor_ld(const AT* H, size_t o) {
+  if constexpr (std::is_same<AT, __half>::value) {
+    const uint2 u = __ldcs(reinterpret_cast<const uint2*>(H + o));
+    const __half2 a = *reinterpret_cast<const __half2*>(&u.x), b = *reinterpret_cast<const __half2*>(&u.y);
+    return make_float4(__low2float(a), __high2float(a), __low2float(b), __high2float(b));
+  } else {
+    return __ldcs(reinterpret_cast<const float4*>(H + o));
+  }
+}
+
+// Stores them: fp32 as is, fp16 by stochastic rounding with the words of counter (row, j).
+template <typename AT>
+__device__ __forceinline__ void anchor_st(AT* H, size_t o, const float (&v)[4], const SrCtr& sr, uint32_t row, int j) {
+  if constexpr (std::is_same<AT, __half>::value) {
+    const uint4 r = philox4x32_10(make_uint4(sr.nonce, sr.slot, row, (uint32_t)j), sr.k0, sr.k1);
+    uint2 u;
+    u.x = (uint32_t)sr_fp16_bits(v[0], r.x) | ((uint32_t)sr_fp16_bits(v[1], r.y) << 16);
+    u.y = (uint32_t)sr_fp16_bits(v[2], r.z) | ((uint32_t)sr_fp16_bits(v[3], r.w) << 16);
+    *reinterpret_cast<uint2*>(H + o) = u;
+  } else {
+    *reinterpret_cast<float4*>(H + o) = make_float4(v[0], v[1], v[2], v[3]);
+  }
+}
+
 // ---- how the output streams read one row of their source -------------------------------------------
 // fp32 checkpoint, bf16 or FP8 read copy (lane j: elements [4j, 4j+4) of row d), or NVFP4 read copy.
 template <typename HT> struct RawOf { using type = typename Quad<HT>::raw; };

@@ -190,19 +190,28 @@ class ReplayCache:
     e4m3 codes and read_scale [S,H,P] fp32, one scale per state row (value = code * scale).
     read_dtype "nvfp4": read_copy [S,H,P,N/2] uint8 holding two e2m1 codes per byte (value n in the
     low nibble of byte n/2 when n is even), read_block_scale [S,H,P,N/16] e4m3 bytes (one per 16
-    values) and read_scale [S,H,P] fp32 (value = code * block scale * row scale)."""
+    values) and read_scale [S,H,P] fp32 (value = code * block scale * row scale).
+
+    anchor "fp32": state [S,H,P,N] fp32.  anchor "fp16_sr" (ReplaySSM only): state [S,H,P,N] fp16,
+    written by stochastic rounding with random words keyed by sr_key and the attribute sr_nonce,
+    which the caller sets to a fresh value before every call that may refresh anchors."""
 
     def __init__(self, nslots: int, nheads: int, ngroups: int, headdim: int, dstate: int, chunk: int,
                  io_dtype: torch.dtype = torch.bfloat16, read_copy: bool = False, device="cuda",
-                 read_dtype: str = "bf16"):
+                 read_dtype: str = "bf16", anchor: str = "fp32", sr_key: Tuple[int, int] = (0, 0)):
         if read_dtype not in ("bf16", "fp8", "nvfp4"):
             raise ValueError(f"read_dtype must be 'bf16', 'fp8' or 'nvfp4', got {read_dtype!r}")
         self.nslots, self.H, self.G, self.P, self.N, self.Q = nslots, nheads, ngroups, headdim, dstate, chunk
+        if anchor not in ("fp32", "fp16_sr"):
+            raise ValueError(f"anchor must be 'fp32' or 'fp16_sr', got {anchor!r}")
         self.io = io_dtype
         self.read_dtype = read_dtype
+        self.anchor = anchor
+        self.sr_key = (int(sr_key[0]) & 0xFFFFFFFF, int(sr_key[1]) & 0xFFFFFFFF)
+        self.sr_nonce = 0
         z = dict(device=device)
         shp = (nslots, nheads, headdim, dstate)
-        self.state = torch.zeros(*shp, dtype=torch.float32, **z)
+        self.state = torch.zeros(*shp, dtype=torch.float16 if anchor == "fp16_sr" else torch.float32, **z)
         self.read_copy = None
         self.read_scale = None
         self.read_block_scale = None
@@ -232,7 +241,9 @@ class ReplayCache:
         rd = {"bf16": _abi.READ_BF16, "fp8": _abi.READ_FP8_E4M3, "nvfp4": _abi.READ_NVFP4}[self.read_dtype]
         return _abi.Cache(self.state.data_ptr(), _ptr(self.read_copy), self.buf_x.data_ptr(), self.buf_dt.data_ptr(),
                           self.buf_B.data_ptr(), self.buf_C.data_ptr(), self.pos.data_ptr(), self.nslots, rd,
-                          _ptr(self.read_scale), _ptr(self.read_block_scale))
+                          _ptr(self.read_scale), _ptr(self.read_block_scale),
+                          _abi.ANCHOR_F16_SR if self.anchor == "fp16_sr" else _abi.ANCHOR_F32,
+                          (ctypes.c_uint32 * 2)(*self.sr_key), int(self.sr_nonce) & 0xFFFFFFFF)
 
     def read_values(self) -> Optional[torch.Tensor]:
         """The read copy's values as fp32 (FP8: code * row scale), or None without a read copy."""

@@ -99,7 +99,8 @@ typedef struct ers_params {
 } ers_params;
 
 /* Per-slot replay cache (exact-replay RFC section 3; ReplaySSM "Motivation and method").
- *   state     [nslots, H, P, N] fp32: the boundary checkpoint (exact mode) or recurrence anchor (ReplaySSM)
+ *   state     [nslots, H, P, N] fp32 (or fp16, see anchor_dtype): the boundary checkpoint (exact
+ *             mode) or recurrence anchor (ReplaySSM)
  *   read_copy [nslots, H, P, N] or NULL: low-precision copy cast from the same fp32 values as `state`,
  *             bf16 (read_dtype ERS_READ_BF16) or FP8 e4m3 bytes (ERS_READ_FP8_E4M3)
  *   buf_x     [nslots, Q, H, P] io dtype;  buf_dt [nslots, Q, H] fp32 raw dt
@@ -132,8 +133,20 @@ typedef struct ers_params {
 #define ERS_READ_FP8_E4M3 1
 #define ERS_READ_NVFP4 2
 
+/* Anchor (state) storage.  ERS_ANCHOR_F32: state is fp32 (every mode).  ERS_ANCHOR_F16_SR (ReplaySSM
+ * "Paper-reported results", the NVFP4-read / FP16+SR-recurrence mode; the rounding is this library's
+ * reading): state is IEEE fp16 [nslots, H, P, N]; a refresh folds in fp32 from the fp16 values, casts
+ * the read copy from the fp32 result and stores the anchor by stochastic rounding: value n of row d
+ * of head h in slot s goes up to the next fp16 value iff r < 2^32 (|v| - lo) / ulp (lo = |v| rounded
+ * toward zero on the fp16 grid, ulp its spacing, 2^-24 below 2^-14; sign kept; >= 65504 gives 65504),
+ * r = word n % 4 of Philox4x32-10(counter = (sr_nonce, s, h * P + d, n / 4), key = sr_key).  The
+ * caller gives every call that may write anchors a fresh sr_nonce.  ReplaySSM mode only, bf16 io,
+ * with a read copy, where the warp-per-head kernels run (headdim 64, dstate 128, chunk <= 16). */
+#define ERS_ANCHOR_F32 0
+#define ERS_ANCHOR_F16_SR 1
+
 typedef struct ers_cache {
-  float* state;
+  void* state;
   void* read_copy;
   void* buf_x;
   float* buf_dt;
@@ -144,6 +157,9 @@ typedef struct ers_cache {
   int32_t read_dtype;
   float* read_scale;
   uint8_t* read_block_scale;
+  int32_t anchor_dtype;
+  uint32_t sr_key[2];
+  uint32_t sr_nonce;
 } ers_cache;
 
 /* Human-readable name of a status code (static storage, never NULL). */

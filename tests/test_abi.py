@@ -148,3 +148,27 @@ def test_validation_of_fp8_read_copies(lib):
         assert ref(d, cache()) == 12
     assert ver(_dims(nheads=32, ngroups=2), cache()) == 12                   # 16 heads per group
     assert ver(_dims(chunk=32), cache()) == 12
+
+
+@needs_no_gpu
+def test_validation_of_fp16_sr_anchors(lib):
+    """fp16 stochastic-rounding anchors: the dtype code is checked; exact-mode calls, fp32 io, a
+    missing read copy and chunked prefill return ERS_EUNSUPPORTED before any launch."""
+    from exact_replay_decode_gb300 import _abi
+    p = _prm()
+
+    def cache(anchor=_abi.ANCHOR_F16_SR, copy=FAKE):
+        return _abi.Cache(FAKE, copy, FAKE, FAKE, FAKE, FAKE, FAKE, 4, _abi.READ_BF16, None, None, anchor)
+
+    def dec(d, c, flags=_abi.FLAG_REPLAYSSM):
+        return lib.ers_replay_decode(ctypes.byref(d), ctypes.byref(p), ctypes.byref(c), 4, None, FAKE, FAKE, FAKE,
+                                     FAKE, flags, FAKE, None, None)
+
+    assert dec(_dims(), cache(anchor=2)) == 3                                  # ERS_EDTYPE
+    assert dec(_dims(), cache(), flags=0) == 12                                # exact mode
+    assert dec(_dims(io_dtype=_abi.DTYPE_F32), cache()) == 12                  # fp32 io
+    assert dec(_dims(chunk=32), cache()) == 12                                 # outside the warp-per-head shapes
+    assert lib.ers_refresh(ctypes.byref(_dims()), ctypes.byref(p), ctypes.byref(cache(copy=0)), 4, None,
+                           _abi.FLAG_REPLAYSSM, 1, None, None) == 12            # no read copy
+    assert lib.ers_chunked_prefill(ctypes.byref(_dims()), ctypes.byref(p), ctypes.byref(cache()), 1, 16, 16, FAKE,
+                                   None, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 1 << 40, None, None) == 12

@@ -1,0 +1,178 @@
+"""fp16 ReplaySSM anchors written by stochastic rounding (ReplaySSM notes, "Paper-reported results":
+"NVFP4 read / FP16+SR recurrence"; the rounding rule and the random words are this library's
+reading: Philox4x32-10 at counter (nonce, slot, h * P + d, n / 4)).
+
+* An anchor write equals the oracle's stochastic rounding of the fp32 refresh result, bit for bit:
+  the same refresh on an fp32-anchor cache holding the same (fp16) values yields that fp32 result,
+  and both caches cast the same read copy from it.
+* Fused flush in decode == ers_refresh + decode, verify == non-speculative decode, bit for bit, with
+  fp16 anchors and an NVFP4 copy (the paper's tp4_hi16_sr configuration).
+* Parity with the oracle's protocol model run with the same rounding (anchors within a few fp16
+  steps, outputs within the bf16 output tolerance)."""
+import dataclasses
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+from synth import torch_io
+from gpu_helpers import OUT_TOL_BF16, dev, layer, out_err, same_bits
+
+pytestmark = pytest.mark.gpu
+
+KEY = (0x1234ABCD, 0x0BADF00D)
+# fp16 anchors: the GPU's fp32 refresh result and the oracle's differ in their last fp32 bits, which
+# flips an occasional stochastic-rounding decision by one fp16 step (2^-10 relative); a few refreshes
+# accumulate a few such steps.
+ANCHOR_TOL_F16 = 4 * 2.0 ** -10
+
+
+def _ers():
+    import exact_replay_decode_gb300 as ers
+    return ers
+
+
+def _anchor_err(got: torch.Tensor, ref: np.ndarray) -> float:
+    g = got.float().cpu().numpy().astype(np.float64)
+    P, N = ref.shape[-2], ref.shape[-1]
+    d = np.abs(g - ref).reshape(-1, P * N).max(axis=1)
+    r = np.abs(ref).reshape(-1, P * N).max(axis=1)
+    return float((d / np.maximum(r, 1e-30)).max())
+
+
+def _setup(S, K, seed, read_dtype, anchor, dims=synth.Dims(64, 8, 64, 128, 16)):
+    ers = _ers()
+    w = dataclasses.replace(synth.workload("decode_b256_h64"), dims=dims)
+    d, L = w.dims, w.dims.chunk
+    params, hist, h0, stream = synth.decode_inputs(w, seed=seed, batch=S, steps=K)
+    prm = layer(params)
+    ht = synth.Tokens.concat(hist)
+    lens = [h.ntokens for h in hist]
+    cu = torch.tensor(np.concatenate([[0], np.cumsum(lens)]), dtype=torch.int32, device=dev())
+    _, fin = ers.ssd_scan_fwd(*torch_io.tokens_to(ht, dev())[:2], prm, *torch_io.tokens_to(ht, dev())[2:], chunk=L,
+                              cu_seqlens=cu)
+    fin16 = fin.half()                                          # the anchor starts on the fp16 grid
+
+    def fresh(anc=anchor):
+        c = ers.ReplayCache(S, d.nheads, d.ngroups, d.headdim, d.dstate, L, torch.bfloat16, read_copy=True,
+                            read_dtype=read_dtype, anchor=anc, sr_key=KEY)
+        c.state.copy_(fin16 if anc == "fp16_sr" else fin16.float())
+        ers.refresh(c, prm, replayssm=True, drafts_T=L + 1)    # h = 0: the anchor keeps its bits
+        return c
+    starts = np.concatenate([[0], np.cumsum(lens)])
+    return params, prm, ht, starts, stream, torch_io.tokens_to(stream, dev(), lead=(K, S)), fin16, fresh
+
+
+@pytest.mark.parametrize("read_dtype", ["bf16", "nvfp4"])
+def test_sr_anchor_write_matches_oracle(read_dtype):
+    ers = _ers()
+    S, K = 12, 9
+    params, prm, _, _, _, tok, fin16, fresh = _setup(S, K, 31, read_dtype, "fp16_sr")
+    c16, c32 = fresh("fp16_sr"), fresh("fp32")
+    assert same_bits(c16.state, fin16)
+    assert torch.equal(c16.read_copy.view(torch.uint8), c32.read_copy.view(torch.uint8))
+    for k in range(K):                                          # K < L committed records, no flush
+        y16 = ers.replay_decode(c16, prm, *(t[k] for t in tok), replayssm=True, fuse_refresh=False)
+        y32 = ers.replay_decode(c32, prm, *(t[k] for t in tok), replayssm=True, fuse_refresh=False)
+        assert same_bits(y16, y32)
+    for c in (c16, c32):
+        c.sr_nonce = 77
+        ers.refresh(c, prm, replayssm=True, drafts_T=16)        # K + 16 > L: every slot flushes
+    want = np.stack([oracle.sr_fp16_anchor(c32.state[i].cpu().numpy(), KEY, 77, i) for i in range(S)])
+    got = c16.state.float().cpu().numpy().astype(np.float64)
+    assert np.array_equal(got, want)
+    assert torch.equal(c16.read_copy.view(torch.uint8), c32.read_copy.view(torch.uint8))
+    moved = np.abs(got - c32.state.cpu().numpy().astype(np.float64)) > 0
+    assert moved.mean() > 0.5                                   # rounding did happen
+
+
+def test_fused_flush_and_verify_with_sr_anchors():
+    """tp4_hi16_sr: NVFP4 copy, fp16 SR anchor.  Fused flush == refresh + decode; verify == the
+    non-speculative decode; anchors and outputs match the oracle's protocol model."""
+    ers = _ers()
+    S, K, L = 32, 40, 16
+    samples = [0, 9, 31]
+    params, prm, ht, starts, stream, tok, fin16, fresh = _setup(S, K, 32, "nvfp4", "fp16_sr")
+    c1, c2 = fresh(), fresh()
+    anchor0 = fin16.float().cpu().numpy().astype(np.float64)[samples]
+    nonce = {"v": 0}
+    model = oracle.ReplaySSMModel(params, anchor0, L, read_cast=oracle.nvfp4_rows_round,
+                                  anchor_round=lambda i, fin: oracle.sr_fp16_anchor(fin, KEY, nonce["v"],
+                                                                                    samples[i]))
+    flushes = 0
+    for k in range(K):
+        nonce["v"] = 1000 + k
+        c1.sr_nonce = c2.sr_nonce = 1000 + k
+        flushes += int((c1.pos == L).sum())
+        y1 = ers.replay_decode(c1, prm, *(t[k] for t in tok), replayssm=True, fuse_refresh=True)
+        ers.refresh(c2, prm, replayssm=True, drafts_T=1)
+        y2 = ers.replay_decode(c2, prm, *(t[k] for t in tok), replayssm=True, fuse_refresh=False)
+        assert same_bits(y1, y2), k
+        rows = [k * S + i for i in samples]
+        y_o = model.verify([(stream.x[r:r + 1], stream.dt[r:r + 1], stream.B[r:r + 1], stream.C[r:r + 1])
+                            for r in rows])
+        model.commit([1] * len(samples))
+        assert out_err(y1[samples], y_o[:, 0]) <= OUT_TOL_BF16, k
+    assert flushes > 0
+    assert same_bits(c1.state, c2.state) and torch.equal(c1.pos, c2.pos)
+    assert torch.equal(c1.read_copy, c2.read_copy) and torch.equal(c1.read_block_scale, c2.read_block_scale)
+    assert _anchor_err(c1.state[samples], model.anchor) <= ANCHOR_TOL_F16
+
+
+def test_verify_equals_nonspec_decode_with_sr_anchors():
+    ers = _ers()
+    w = synth.workload("verify_b512_t4")
+    d = w.dims
+    S, K, T, L = 48, 20, w.drafts, d.chunk
+    params, hist, drafts, acc = synth.verify_inputs(w, seed=33, batch=S, steps=K)
+    prm = layer(params)
+    hx, hdt, hB, hC = torch_io.tokens_to(hist, dev())
+    cu = torch.arange(0, S * 32 + 1, 32, dtype=torch.int32, device=dev())
+    _, fin = ers.ssd_scan_fwd(hx, hdt, prm, hB, hC, chunk=L, cu_seqlens=cu)
+
+    def fresh():
+        c = ers.ReplayCache(S, d.nheads, d.ngroups, d.headdim, d.dstate, L, torch.bfloat16, read_copy=True,
+                            read_dtype="nvfp4", anchor="fp16_sr", sr_key=KEY)
+        c.state.copy_(fin.half())
+        ers.refresh(c, prm, replayssm=True, drafts_T=L + 1)
+        return c
+    cache, ref = fresh(), fresh()
+    dx, ddt, dB, dC = torch_io.tokens_to(drafts, dev(), lead=(K, S, T))
+    acc_t = torch.from_numpy(acc).to(dev())
+    for k in range(K):
+        cache.sr_nonce = ref.sr_nonce = 5000 + k
+        y = ers.spec_verify(cache, prm, dx[k], ddt[k], dB[k], dC[k])
+        ers.commit(cache, acc_t[k], T)
+        ers.refresh(ref, prm, replayssm=True, drafts_T=T)
+        ref.sr_nonce = 0                                        # decodes write no anchors
+        a = acc[k]
+        for j in range(T):
+            sel = np.nonzero(a > j)[0]
+            if sel.size == 0:
+                break
+            sel_t = torch.from_numpy(sel.astype(np.int32)).to(dev())
+            sl = sel_t.long()
+            yd = ers.replay_decode(ref, prm, dx[k, sl, j], ddt[k, sl, j], dB[k, sl, j], dC[k, sl, j], slot=sel_t,
+                                   replayssm=True, fuse_refresh=False)
+            assert same_bits(yd, y[sl, j]), f"step {k} draft {j}"
+    assert torch.equal(cache.pos, ref.pos) and same_bits(cache.state, ref.state)
+    assert torch.equal(cache.read_copy, ref.read_copy)
+
+
+def test_sr_anchor_unsupported_calls_raise():
+    ers = _ers()
+    H, G, P, N = 8, 2, 64, 128
+    prm = layer(synth.make_params(np.random.Generator(np.random.PCG64(0)), H))
+    x = torch.zeros(2, H, P, dtype=torch.bfloat16, device=dev())
+    dt = torch.zeros(2, H, dtype=torch.float32, device=dev())
+    B = torch.zeros(2, G, N, dtype=torch.bfloat16, device=dev())
+    c = ers.ReplayCache(2, H, G, P, N, 16, torch.bfloat16, read_copy=True, anchor="fp16_sr")
+    with pytest.raises(ers.ErsError) as e:
+        ers.replay_decode(c, prm, x, dt, B, B.clone())                 # exact mode
+    assert e.value.code == 12
+    c32 = ers.ReplayCache(2, H, G, P, N, 16, torch.float32, read_copy=True, anchor="fp16_sr")
+    with pytest.raises(ers.ErsError) as e:
+        ers.replay_decode(c32, prm, x.float(), dt, B.float(), B.float(), replayssm=True)   # fp32 io
+    assert e.value.code == 12
