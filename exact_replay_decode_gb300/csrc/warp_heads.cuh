@@ -278,7 +278,14 @@ __device__ __forceinline__ uint4 philox4x32_10(uint4 c, uint32_t k0, uint32_t k1
 __device__ __forceinline__ uint16_t sr_fp16_bits(float v, uint32_t r) {
   const uint32_t b = __float_as_uint(v);
   const uint16_t sign = (uint16_t)((b >> 16) & 0x8000u);
-  const float a = __uint_as_float(b & 0x7FFFFFFFu);
+  const uint32_t m = b & 0x7FFFFFFFu;
+  if (m >= 0x38800000u && m < 0x477FE000u) {
+    // fp16 normal range [2^-14, 65504): the step is 2^13 fp32 mantissa units, so frac * 2^32 =
+    // (m & 0x1FFF) * 2^19 and r < frac * 2^32 iff (r >> 19) < (m & 0x1FFF); the result is exact in fp16
+    const uint32_t q = (m & ~0x1FFFu) + ((r >> 19) < (m & 0x1FFFu) ? 0x2000u : 0u);
+    return sign | __half_as_ushort(__float2half_rn(__uint_as_float(q)));
+  }
+  const float a = __uint_as_float(m);
   if (!(a < 65504.f)) return sign | 0x7BFFu;   // saturate (65504)
   if (a == 0.f) return sign;
   const int e = (int)((b >> 23) & 0xFFu) - 127;   // floor(log2 a) for a normal a; fp32-subnormal a: -127

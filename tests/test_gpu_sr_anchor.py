@@ -176,3 +176,40 @@ def test_sr_anchor_unsupported_calls_raise():
     with pytest.raises(ers.ErsError) as e:
         ers.replay_decode(c32, prm, x.float(), dt, B.float(), B.float(), replayssm=True)   # fp32 io
     assert e.value.code == 12
+
+
+def test_sr_anchor_write_edge_values():
+    """Anchors spanning the fp16 range (subnormals, the smallest normals, values near 65504): with
+    x = 0 the refresh result is decay * S, so the rounding sees values across every range; the fp16
+    write equals the oracle's rounding of the fp32-anchor cache's result bit for bit."""
+    ers = _ers()
+    S, K, L, H, G, P, N = 6, 5, 16, 64, 8, 64, 128
+    w = synth.workload("decode_b256_h64")
+    params, _, _, stream = synth.decode_inputs(w, seed=34, batch=S, steps=K)
+    prm = layer(params)
+    stream.x[:] = 0
+    tok = torch_io.tokens_to(stream, dev(), lead=(K, S))
+    st = synth.quant_probe_state(35, (S, H, P, N))
+    st = np.clip(st, -60000.0, 60000.0)
+    st[0, 1] = np.float32(2.0 ** -20) * np.sign(st[0, 1])                 # a head of fp16 subnormals
+    st[0, 2] = np.float32(2.0 ** -14) * (1 + (np.arange(N) % 7) / 8.0)     # the smallest normals
+    st16 = torch.from_numpy(st).half()
+
+    def fresh(anc):
+        c = ers.ReplayCache(S, H, G, P, N, L, torch.bfloat16, read_copy=True, read_dtype="nvfp4", anchor=anc,
+                            sr_key=KEY)
+        c.state.copy_(st16 if anc == "fp16_sr" else st16.float())
+        ers.refresh(c, prm, replayssm=True, drafts_T=L + 1)
+        return c
+    c16, c32 = fresh("fp16_sr"), fresh("fp32")
+    for k in range(K):
+        ers.replay_decode(c16, prm, *(t[k] for t in tok), replayssm=True, fuse_refresh=False)
+        ers.replay_decode(c32, prm, *(t[k] for t in tok), replayssm=True, fuse_refresh=False)
+    for c in (c16, c32):
+        c.sr_nonce = 91
+        ers.refresh(c, prm, replayssm=True, drafts_T=16)
+    want = np.stack([oracle.sr_fp16_anchor(c32.state[i].cpu().numpy(), KEY, 91, i) for i in range(S)])
+    got = c16.state.float().cpu().numpy().astype(np.float64)
+    assert np.array_equal(got, want)
+    sub = np.abs(got[0, 1]) < 2.0 ** -14
+    assert sub.mean() > 0.9 and np.any(got[0, 1] != 0)                   # the subnormal path ran
