@@ -26,8 +26,9 @@
  *    *_workspace_size query.
  *  - Dtypes: x, B, C, y and the partial-chunk buffers x/B/C use dims->io_dtype
  *    (ERS_DTYPE_BF16 or ERS_DTYPE_F32, the same for all of them); dt, A, D,
- *    dt_bias and every recurrence state are fp32; the read copy is bf16; index
- *    arrays are int32.  Every pointer must be 16-byte aligned.
+ *    dt_bias and every recurrence state are fp32 (a ReplaySSM anchor may be
+ *    fp16, see ers_cache); the read copy is bf16, FP8 or NVFP4; index arrays are
+ *    int32.  Every pointer must be 16-byte aligned.
  *  - Every call is asynchronous on `stream` (0 = legacy default stream).  Host
  *    validation runs first; a call that returns an error has launched nothing.
  *  - Errors the host cannot see (slot positions, slot indices, accepted counts,

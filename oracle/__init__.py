@@ -289,6 +289,42 @@ def sr_fp16_anchor(fin: np.ndarray, key: Tuple[int, int], nonce: int, slot: int)
     return sr_fp16(np.asarray(fin, dtype=np.float64).astype(np.float32), sr_words(key, nonce, slot, H, P, N))
 
 
+# ---- causal depthwise conv1d with a conv state (exact-replay RFC, Evidence item 6) -------------------
+def silu(a: np.ndarray) -> np.ndarray:
+    """x * sigmoid(x) in fp64."""
+    a = np.asarray(a, dtype=np.float64)
+    return a / (1.0 + np.exp(-a))
+
+
+def causal_conv1d(x: np.ndarray, weight: np.ndarray, bias: Optional[np.ndarray], cu_seqlens=None,
+                  init_state: Optional[np.ndarray] = None, activation: bool = True):
+    """Depthwise causal convolution over time, per packed sequence, in fp64:
+        y[t, c] = act(bias[c] + sum_{k < W} weight[c, k] * u[t - W + 1 + k, c]),
+    where u is the sequence's inputs preceded by its W - 1 earlier inputs (init_state[i], [W-1, C],
+    oldest first; zeros when absent) and act is SiLU or the identity.  Returns (y [T, C], the final
+    states [S, W-1, C]: the last W - 1 entries of u)."""
+    x = _f64(x)
+    w = _f64(weight)
+    C, W = w.shape
+    T = x.shape[0]
+    cu = np.array([0, T] if cu_seqlens is None else cu_seqlens, dtype=np.int64)
+    S = len(cu) - 1
+    b = np.zeros(C) if bias is None else _f64(bias)
+    y = np.zeros((T, C))
+    fin = np.zeros((S, W - 1, C))
+    for i in range(S):
+        pre = np.zeros((W - 1, C)) if init_state is None else _f64(init_state[i])
+        u = np.concatenate([pre, x[cu[i]:cu[i + 1]]])
+        n = cu[i + 1] - cu[i]
+        for t in range(n):
+            acc = b.copy()
+            for k in range(W):
+                acc = acc + w[:, k] * u[t + k]
+            y[cu[i] + t] = silu(acc) if activation else acc
+        fin[i] = u[len(u) - (W - 1):]
+    return y, fin
+
+
 class _Seq:
     __slots__ = ("x", "dt", "B", "C")
 

@@ -548,3 +548,52 @@ def test_protocol_anchor_independent_of_fp8_read_copy():
         y3 = m3.verify(drafts[k]); m3.commit(acc[k])
     assert m1.flushes > 0 and np.array_equal(m1.anchor, m2.anchor) and np.array_equal(m1.anchor, m3.anchor)
     assert not np.array_equal(y1, y2) and not np.array_equal(y2, y3)
+
+
+# ---- causal conv1d (exact-replay RFC, Evidence item 6: the conv's prefill and update paths) ----------
+def test_silu_identities():
+    z = np.linspace(-30, 30, 601)
+    assert oracle.silu(np.array(0.0)) == 0.0
+    assert np.allclose(oracle.silu(z) - oracle.silu(-z), z, rtol=0, atol=1e-12)     # sigmoid(z) + sigmoid(-z) = 1
+    assert abs(oracle.silu(np.array(40.0)) - 40.0) < 1e-12
+    assert abs(oracle.silu(np.array(1.0)) - 1.0 / (1.0 + np.exp(-1.0))) < 1e-15
+
+
+def test_conv1d_matches_numpy_convolve():
+    rng = np.random.Generator(np.random.PCG64(41))
+    for W in (2, 3, 4):
+        T, C = 37, 5
+        x = rng.standard_normal((T, C))
+        w = rng.standard_normal((C, W))
+        b = rng.standard_normal(C)
+        init = rng.standard_normal((1, W - 1, C))
+        y, fin = oracle.causal_conv1d(x, w, b, init_state=init, activation=False)
+        u = np.concatenate([init[0], x])
+        for c in range(C):
+            want = np.convolve(u[:, c], w[c, ::-1], mode="valid") + b[c]
+            assert np.allclose(y[:, c], want, rtol=1e-13, atol=1e-13)
+        assert np.array_equal(fin[0], u[-(W - 1):])
+        ya, _ = oracle.causal_conv1d(x, w, b, init_state=init, activation=True)
+        assert np.allclose(ya, oracle.silu(y), rtol=1e-14, atol=1e-14)
+
+
+def test_conv1d_identity_kernel_short_sequences_and_splits():
+    rng = np.random.Generator(np.random.PCG64(42))
+    W, C = 4, 3
+    x = rng.standard_normal((9, C))
+    eye = np.zeros((C, W)); eye[:, -1] = 1.0
+    y, fin = oracle.causal_conv1d(x, eye, None, activation=False)
+    assert np.array_equal(y, x) and np.array_equal(fin[0], x[-3:])
+    # a sequence shorter than W - 1 keeps part of its initial state in the final state
+    init = rng.standard_normal((1, W - 1, C))
+    _, f1 = oracle.causal_conv1d(x[:1], eye, None, init_state=init)
+    assert np.array_equal(f1[0], np.concatenate([init[0, 1:], x[:1]]))
+    # splitting a sequence and carrying the state gives the single-shot result; packing is invariant
+    w = rng.standard_normal((C, W)); b = rng.standard_normal(C)
+    y0, f0 = oracle.causal_conv1d(x, w, b)
+    ya, fa = oracle.causal_conv1d(x[:4], w, b)
+    yb, fb = oracle.causal_conv1d(x[4:], w, b, init_state=fa)
+    assert np.allclose(np.concatenate([ya, yb]), y0, rtol=1e-15, atol=1e-15) and np.array_equal(fb, f0)
+    yp, fp = oracle.causal_conv1d(np.concatenate([x, x[:5]]), w, b, cu_seqlens=[0, 9, 14])
+    assert np.array_equal(yp[:9], y0) and np.array_equal(yp[9:], oracle.causal_conv1d(x[:5], w, b)[0])
+    assert np.array_equal(fp[0], f0[0])
