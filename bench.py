@@ -321,7 +321,14 @@ def time_decode_e2e(dev, steps: int, warmup: int, seed: int, batch=None):
 
 def _flush_buf(dev):
     import torch
-    return torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    return torch.zeros(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+
+
+def _l2_flush(fb):
+    """Evict L2 by READING a buffer larger than it: the lines it leaves are clean, so the timed
+    kernel's misses cost no write-backs of the flush itself (a write-based flush would leave ~129 MB
+    of dirty lines for the timed kernel to write back)."""
+    fb.sum()
 
 
 def time_per_iter(fn, iters: int, warmup: int, dev, flush: bool = True):
@@ -334,7 +341,7 @@ def time_per_iter(fn, iters: int, warmup: int, dev, flush: bool = True):
     evs = []
     for _ in range(iters):
         if fb is not None:
-            fb.zero_()
+            _l2_flush(fb)
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record(s)
         fn()
@@ -520,6 +527,54 @@ def bench_rssm_decode(dev, cycles: int, hbm: float, read_dtype: str, anchor: str
             "launches_per_step": 1}
 
 
+def bench_conv(dev, hbm: float, reps: int = 50):
+    """The causal conv1d upstream of the SSM on the decode workload's channels (x, B and C: 64 x 64 +
+    2 x 8 x 128 = 6144), width 4, bf16: one update step for 256 sequences (bytes: state read and
+    write 2 x 3 rows, x and y rows, per sequence) and a 2048-token prefill (x read, y written).  L2 is
+    flushed (a 256 MB read) before each timed call."""
+    import torch
+    import exact_replay_decode_gb300 as ers
+    rng = np.random.Generator(np.random.PCG64(12))
+    C, W, S, T = 6144, 4, 256, 2048
+    cast = lambda a: torch.from_numpy(a.astype(np.float32)).to(dev).to(torch.bfloat16)
+    w = cast(rng.standard_normal((C, W)) * 0.5)
+    b = cast(rng.standard_normal(C) * 0.1)
+    xs = cast(rng.standard_normal((S, C)))
+    xp = cast(rng.standard_normal((T, C)))
+    state = cast(rng.standard_normal((S, W - 1, C)))
+    y = torch.empty_like(xs)
+    yp = torch.empty_like(xp)
+    cu = torch.tensor([0, T], dtype=torch.int32, device=dev)
+    flush = _flush_buf(dev)
+    st = ers.Status(dev)
+
+    def timed(fn):
+        s = torch.cuda.current_stream()
+        ts = []
+        for _ in range(reps):
+            _l2_flush(flush)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(s)
+            fn()
+            e1.record(s)
+            torch.cuda.synchronize()
+            ts.append(e0.elapsed_time(e1))
+        return float(np.median(ts))
+    upd = lambda: ers.conv1d_update(xs, w, b, state, status=st, check=False, out=y)
+    pre = lambda: ers.conv1d_fwd(xp, w, b, cu, max_seqlen=T, status=st, check=False, out=yp)
+    for _ in range(3):
+        upd(); pre()
+    ms_u, ms_p = timed(upd), timed(pre)
+    st.raise_if_error("bench conv")
+    bytes_u = S * C * 2 * (2 * (W - 1) + 2) + C * W * 2 + C * 2
+    bytes_p = 2 * T * C * 2 + C * W * 2 + C * 2
+    return {"update_b256": {"us": ms_u * 1e3, "seq_steps_per_s": S / (ms_u * 1e-3), "bytes": bytes_u,
+                            "hbm_frac": bytes_u / (ms_u * 1e-3) / 1e9 / hbm},
+            "prefill_2048": {"us": ms_p * 1e3, "tok_per_s": T / (ms_p * 1e-3), "bytes": bytes_p,
+                             "hbm_frac": bytes_p / (ms_p * 1e-3) / 1e9 / hbm},
+            "l2": "flushed before each call"}
+
+
 def bench_ssu(dev, steps: int, hbm: float):
     import torch
     import exact_replay_decode_gb300 as ers
@@ -639,7 +694,7 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--decode-only", action="store_true", help="only the headline decode measurement")
     ap.add_argument("--batch", type=int, default=None, help="decode sequences per GPU (profiling runs only)")
-    ap.add_argument("--section", choices=["prefill", "verify", "rssm", "ssu"], default=None,
+    ap.add_argument("--section", choices=["prefill", "verify", "rssm", "ssu", "conv"], default=None,
                     help="run only this secondary workload and print its JSON (profiling aid, no headline)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
@@ -658,6 +713,8 @@ def main(argv=None):
     if args.section is not None:
         if args.section == "prefill":
             out = {n: bench_prefill(dev, n, 10, args.warmup, hbm, tc) for n in ("prefill_2048_h32", "varlen_4seq_h64")}
+        elif args.section == "conv":
+            out = bench_conv(dev, hbm)
         elif args.section == "rssm":
             out = {r: bench_rssm_decode(dev, 4, hbm, r) for r in ("bf16", "fp8", "nvfp4")}
             out["nvfp4_fp16sr"] = bench_rssm_decode(dev, 4, hbm, "nvfp4", "fp16_sr")
@@ -696,6 +753,7 @@ def main(argv=None):
         extra["replayssm_decode"] = {r: bench_rssm_decode(dev, 4, hbm, r) for r in ("bf16", "fp8", "nvfp4")}
         extra["replayssm_decode"]["nvfp4_fp16sr"] = bench_rssm_decode(dev, 4, hbm, "nvfp4", "fp16_sr")
         extra["ssu"] = bench_ssu(dev, 16, hbm)
+        extra["conv1d"] = bench_conv(dev, hbm)
     line = {
         "metric": "replay-decode seq-steps/s per layer @B=256",
         "value": value,

@@ -1,5 +1,6 @@
 """Exact-replay SSD for GB300: chunked Mamba2 SSD prefill, exact-replay decode, checkpoint refresh,
-output-only speculative verify and commit, and a per-token-writeback SSU comparison kernel, as a
+output-only speculative verify and commit, the causal conv1d upstream of the SSM, and a
+per-token-writeback SSU comparison kernel, as a
 C-ABI CUDA library (libers.so, include/ers.h) with a thin PyTorch binding.
 
 Importing the package is cheap; the CUDA library is loaded on first use of an operation and its
@@ -9,7 +10,7 @@ __version__ = "0.1.0"
 
 _OPS = ("LayerParams", "ReplayCache", "Status", "ssd_scan_fwd", "ssd_scan_fwd_static", "STATIC_SCRATCH_BYTES",
         "chunked_prefill", "replay_decode", "refresh",
-        "spec_verify", "commit", "ssu_update")
+        "spec_verify", "commit", "ssu_update", "conv1d_fwd", "conv1d_update")
 
 
 def __getattr__(name):

@@ -35,7 +35,8 @@ ANCHOR_F16_SR = 1
 EXPORTS = (
     "ers_status_str", "ers_version", "ers_ssd_scan_fwd_workspace_size", "ers_ssd_scan_fwd",
     "ers_chunked_prefill_workspace_size", "ers_chunked_prefill", "ers_replay_decode", "ers_refresh",
-    "ers_spec_verify", "ers_commit", "ers_ssu_update", "ers_ssd_scan_fwd_static",
+    "ers_spec_verify", "ers_commit", "ers_ssu_update", "ers_ssd_scan_fwd_static", "ers_conv1d_fwd",
+    "ers_conv1d_update",
 )
 
 
@@ -48,6 +49,14 @@ class ErsError(RuntimeError):
 class Dims(ctypes.Structure):
     _fields_ = [("nheads", ctypes.c_int32), ("ngroups", ctypes.c_int32), ("headdim", ctypes.c_int32),
                 ("dstate", ctypes.c_int32), ("chunk", ctypes.c_int32), ("io_dtype", ctypes.c_int32)]
+
+
+class ConvDims(ctypes.Structure):
+    _fields_ = [("channels", ctypes.c_int32), ("width", ctypes.c_int32), ("io_dtype", ctypes.c_int32),
+                ("flags", ctypes.c_uint32)]
+
+
+CONV_SILU = 1
 
 
 class Params(ctypes.Structure):
@@ -88,6 +97,9 @@ _SIGS = {
     "ers_spec_verify": ([_DIMS, _PRM, _CACHE, _I32, _P, _I32, _P, _P, _P, _P, _U32, _P, _P, _P], _I32),
     "ers_commit": ([_DIMS, _CACHE, _I32, _P, _P, _I32, _U32, _P, _P], _I32),
     "ers_ssu_update": ([_DIMS, _PRM, _P, _I32, _I32, _P, _P, _P, _P, _P, _P, _P, _P], _I32),
+    "ers_conv1d_fwd": ([ctypes.POINTER(ConvDims), _I32, _I64, _I32, _P, _P, _P, _P, _P, _I32, _P, _I32, _P, _P, _P],
+                       _I32),
+    "ers_conv1d_update": ([ctypes.POINTER(ConvDims), _I32, _P, _P, _P, _P, _I32, _P, _P, _P, _P], _I32),
 }
 
 

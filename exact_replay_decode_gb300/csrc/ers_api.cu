@@ -401,6 +401,87 @@ ers_status ers_ssu_update(const ers_dims* dims, const ers_params* prm, float* st
   return finish(ers::ssu_update(a, (cudaStream_t)stream));
 }
 
+namespace {
+ers_status check_conv(const ers_conv_dims* d) {
+  if (d == nullptr) return ERS_EINVAL;
+  if (d->io_dtype != ERS_DTYPE_F32 && d->io_dtype != ERS_DTYPE_BF16) return ERS_EDTYPE;
+  if (d->channels <= 0 || d->channels % 8 != 0 || d->width < 2 || d->width > 4) return ERS_ESHAPE;
+  if ((d->flags & ~ERS_CONV_SILU) != 0) return ERS_EINVAL;
+  return ERS_OK;
+}
+
+ers::ConvLaunch conv_launch(const ers_conv_dims* d) {
+  ers::ConvLaunch l;
+  memset(&l, 0, sizeof(l));
+  l.C = d->channels;
+  l.W = d->width;
+  l.io = d->io_dtype;
+  l.silu = (d->flags & ERS_CONV_SILU) != 0;
+  return l;
+}
+}  // namespace
+
+ers_status ers_conv1d_fwd(const ers_conv_dims* dims, int32_t nseq, int64_t ntokens, int32_t max_seqlen,
+                          const int32_t* cu_seqlens, const void* x, const void* weight, const void* bias,
+                          void* conv_state, int32_t nslots, const int32_t* slot, int32_t read_state, void* y,
+                          ers_stream_t stream, int32_t* dev_status) {
+  ERS_TRY(check_conv(dims));
+  if (nseq < 0 || ntokens < 0 || max_seqlen < 0 || nslots < 0) return ERS_EINVAL;
+  if (nseq == 0) return ERS_OK;
+  ERS_TRY(check_ptr(cu_seqlens, true));
+  ERS_TRY(check_ptr(x, ntokens > 0));
+  ERS_TRY(check_ptr(y, ntokens > 0));
+  ERS_TRY(check_ptr(weight, true));
+  ERS_TRY(check_ptr(bias, false));
+  ERS_TRY(check_ptr(conv_state, read_state != 0));
+  ERS_TRY(check_ptr(slot, false));
+  ERS_TRY(check_ptr(dev_status, false));
+  if (conv_state != nullptr && slot == nullptr && nseq > nslots) return ERS_EINVAL;
+  ers::ConvLaunch l = conv_launch(dims);
+  l.nseq = nseq;
+  l.nslots = conv_state != nullptr ? nslots : 0;
+  l.read_state = read_state != 0;
+  l.update = 0;
+  l.max_seqlen = max_seqlen;
+  l.cu = cu_seqlens;
+  l.slot = slot;
+  l.x = x;
+  l.w = weight;
+  l.bias = bias;
+  l.state = conv_state;
+  l.y = y;
+  l.status = dev_status;
+  return finish(ers::conv1d(l, (cudaStream_t)stream));
+}
+
+ers_status ers_conv1d_update(const ers_conv_dims* dims, int32_t nseq, const void* x, const void* weight,
+                             const void* bias, void* conv_state, int32_t nslots, const int32_t* slot, void* y,
+                             ers_stream_t stream, int32_t* dev_status) {
+  ERS_TRY(check_conv(dims));
+  if (nseq < 0 || nslots < 0) return ERS_EINVAL;
+  if (nseq == 0) return ERS_OK;
+  ERS_TRY(check_ptr(x, true));
+  ERS_TRY(check_ptr(y, true));
+  ERS_TRY(check_ptr(weight, true));
+  ERS_TRY(check_ptr(bias, false));
+  ERS_TRY(check_ptr(conv_state, true));
+  ERS_TRY(check_ptr(slot, false));
+  ERS_TRY(check_ptr(dev_status, false));
+  if (slot == nullptr && nseq > nslots) return ERS_EINVAL;
+  ers::ConvLaunch l = conv_launch(dims);
+  l.nseq = nseq;
+  l.nslots = nslots;
+  l.update = 1;
+  l.slot = slot;
+  l.x = x;
+  l.w = weight;
+  l.bias = bias;
+  l.state = conv_state;
+  l.y = y;
+  l.status = dev_status;
+  return finish(ers::conv1d(l, (cudaStream_t)stream));
+}
+
 }  // extern "C"
 
 // ---- scan with library-owned scratch ------------------------------------------------------------

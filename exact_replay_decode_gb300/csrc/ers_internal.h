@@ -103,4 +103,18 @@ bool ssu_supported(int P, int N);
 
 inline size_t align256(size_t v) { return (v + 255) & ~size_t(255); }
 
+// causal depthwise conv1d with a conv state, ers_conv.cu
+struct ConvLaunch {
+  int C, W, io, silu, nseq, nslots, read_state, update, max_seqlen;
+  const int32_t* cu;
+  const int32_t* slot;
+  const void* x;
+  const void* w;
+  const void* bias;
+  void* state;
+  void* y;
+  int32_t* status;
+};
+cudaError_t conv1d(const ConvLaunch& l, cudaStream_t s);
+
 }  // namespace ers

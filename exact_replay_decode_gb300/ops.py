@@ -384,3 +384,69 @@ def ssu_update(state: torch.Tensor, params: LayerParams, x, dt, B, C, slot: Opti
                                      y.data_ptr(), _stream(stream), _ptr(st.t) if st else None)
     _finish(code, "ers_ssu_update", st, check)
     return y
+
+
+# ------------------------------------------------------------------------------------------------
+def _conv_dims(C: int, W: int, io: torch.dtype, activation: bool) -> _abi.ConvDims:
+    if io not in _IO:
+        raise TypeError(f"io dtype {io} not supported (bf16 or fp32)")
+    return _abi.ConvDims(C, W, _IO[io], _abi.CONV_SILU if activation else 0)
+
+
+def _conv_params(weight: torch.Tensor, bias: Optional[torch.Tensor], io: torch.dtype):
+    C, W = weight.shape
+    _need(weight, io, "weight", (C, W))
+    if bias is not None:
+        _need(bias, io, "bias", (C,))
+    return C, W
+
+
+def conv1d_fwd(x: torch.Tensor, weight: torch.Tensor, bias: Optional[torch.Tensor] = None,
+               cu_seqlens: Optional[torch.Tensor] = None, conv_state: Optional[torch.Tensor] = None,
+               slot: Optional[torch.Tensor] = None, read_state: bool = False, activation: bool = True,
+               max_seqlen: Optional[int] = None, status: Optional[Status] = None, check: bool = True,
+               stream=None, out: Optional[torch.Tensor] = None) -> torch.Tensor:
+    """Causal depthwise conv1d over packed sequences (ers_conv1d_fwd).  x [T, C], weight [C, W],
+    bias [C]; conv_state [nslots, W-1, C] (oldest input first) is read when read_state and, when
+    given, receives each sequence's final state."""
+    io = _io_from(x)
+    T = x.shape[0]
+    C, W = _conv_params(weight, bias, io)
+    _need(x, io, "x", (T, C))
+    if cu_seqlens is None:
+        cu_seqlens = torch.tensor([0, T], dtype=torch.int32, device=x.device)
+    _need(cu_seqlens, torch.int32, "cu_seqlens")
+    S = cu_seqlens.numel() - 1
+    nslots = 0
+    if conv_state is not None:
+        nslots = conv_state.shape[0]
+        _need(conv_state, io, "conv_state", (nslots, W - 1, C))
+    y = torch.empty_like(x) if out is None else out
+    st = status if status is not None else (Status(x.device) if check else None)
+    code = _abi.lib().ers_conv1d_fwd(ctypes.byref(_conv_dims(C, W, io, activation)), S, T,
+                                     _max_len(cu_seqlens, max_seqlen), cu_seqlens.data_ptr(), x.data_ptr(),
+                                     weight.data_ptr(), _ptr(bias), _ptr(conv_state), nslots, _slot_arg(slot, S),
+                                     int(bool(read_state)), y.data_ptr(), _stream(stream), _ptr(st.t) if st else None)
+    _finish(code, "ers_conv1d_fwd", st, check)
+    return y
+
+
+def conv1d_update(x: torch.Tensor, weight: torch.Tensor, bias: Optional[torch.Tensor], conv_state: torch.Tensor,
+                  slot: Optional[torch.Tensor] = None, activation: bool = True, status: Optional[Status] = None,
+                  check: bool = True, stream=None, out: Optional[torch.Tensor] = None) -> torch.Tensor:
+    """One conv1d step per sequence (ers_conv1d_update): x [S, C]; conv_state [nslots, W-1, C] is
+    shifted by one and receives x."""
+    io = _io_from(x)
+    S = x.shape[0]
+    C, W = _conv_params(weight, bias, io)
+    _need(x, io, "x", (S, C))
+    nslots = conv_state.shape[0]
+    _need(conv_state, io, "conv_state", (nslots, W - 1, C))
+    y = torch.empty_like(x) if out is None else out
+    st = status if status is not None else (Status(x.device) if check else None)
+    code = _abi.lib().ers_conv1d_update(ctypes.byref(_conv_dims(C, W, io, activation)), S, x.data_ptr(),
+                                        weight.data_ptr(), _ptr(bias), conv_state.data_ptr(), nslots,
+                                        _slot_arg(slot, S), y.data_ptr(), _stream(stream),
+                                        _ptr(st.t) if st else None)
+    _finish(code, "ers_conv1d_update", st, check)
+    return y

@@ -292,6 +292,41 @@ ERS_API ers_status ers_ssu_update(const ers_dims* dims, const ers_params* prm, f
                           const void* C, void* y, ers_stream_t stream, int32_t* dev_status);
 
 /* ---------------------------------------------------------------------------------------------
+ * Causal depthwise conv1d with a conv state: the step upstream of the SSM, whose prefill and
+ * decode-update paths must give identical bits (exact-replay RFC, section 2 Evidence item 6; bf16
+ * operands promoted to fp32 before accumulation).  Per channel c, with u the inputs preceded by
+ * the W - 1 earlier inputs held in the conv state (oldest first; zeros when not read):
+ *     acc = bias[c];  acc = fmaf(w[c][k], u[t + k], acc) for k = 0 .. W-1;  y[t][c] = act(acc)
+ * with act(a) = a / (1 + exp(-a)) (SiLU, IEEE division) when ERS_CONV_SILU is set, else a.
+ *
+ *   dims->channels C (a multiple of 8), dims->width W in {2, 3, 4}, dims->io_dtype for x, weight, bias, y and
+ *   the state; x, y [T, C] (prefill, packed by cu_seqlens [nseq+1]) or [nseq, C] (update); weight
+ *   [C, W]; bias [C] or NULL; conv_state [nslots, W-1, C], row 0 the oldest input; slot [nseq] or
+ *   NULL (sequence i uses slot i).
+ * ers_conv1d_fwd: reads the initial state when read_state != 0 (else zeros) and writes the final
+ *   state (the last W - 1 entries of u) when conv_state is not NULL.  max_seqlen bounds the longest
+ *   sequence.
+ * ers_conv1d_update: one token per sequence; shifts the state by one and stores the new input.
+ * Device errors: ERS_ESLOT. */
+#define ERS_CONV_SILU 1u
+
+typedef struct ers_conv_dims {
+  int32_t channels;
+  int32_t width;
+  int32_t io_dtype;
+  uint32_t flags;
+} ers_conv_dims;
+
+ERS_API ers_status ers_conv1d_fwd(const ers_conv_dims* dims, int32_t nseq, int64_t ntokens, int32_t max_seqlen,
+                                  const int32_t* cu_seqlens, const void* x, const void* weight, const void* bias,
+                                  void* conv_state, int32_t nslots, const int32_t* slot, int32_t read_state,
+                                  void* y, ers_stream_t stream, int32_t* dev_status);
+
+ERS_API ers_status ers_conv1d_update(const ers_conv_dims* dims, int32_t nseq, const void* x, const void* weight,
+                                     const void* bias, void* conv_state, int32_t nslots, const int32_t* slot,
+                                     void* y, ers_stream_t stream, int32_t* dev_status);
+
+/* ---------------------------------------------------------------------------------------------
  * ers_ssd_scan_fwd with library-owned scratch.  The pages have no counterpart to this call; it
  * exists for callers that cannot hand the scan a workspace: a host program that owns no device
  * allocator (plain C over the runtime, no tensor library), and serving loops that must not

@@ -172,3 +172,22 @@ def test_validation_of_fp16_sr_anchors(lib):
                            _abi.FLAG_REPLAYSSM, 1, None, None) == 12            # no read copy
     assert lib.ers_chunked_prefill(ctypes.byref(_dims()), ctypes.byref(p), ctypes.byref(cache()), 1, 16, 16, FAKE,
                                    None, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 1 << 40, None, None) == 12
+
+
+@needs_no_gpu
+def test_validation_of_conv1d(lib):
+    from exact_replay_decode_gb300 import _abi
+
+    def fwd(C=64, W=4, io=_abi.DTYPE_BF16, flags=1, state=FAKE, read_state=1, nslots=4):
+        d = _abi.ConvDims(C, W, io, flags)
+        return lib.ers_conv1d_fwd(ctypes.byref(d), 2, 8, 4, FAKE, FAKE, FAKE, None, state, nslots, None, read_state,
+                                  FAKE, None, None)
+
+    assert fwd(C=63) == 2 and fwd(C=66) == 2 and fwd(W=5) == 2 and fwd(W=1) == 2   # ERS_ESHAPE
+    assert fwd(io=9) == 3 and fwd(flags=2) == 1
+    assert fwd(state=0) == 1                                        # reading a state needs one
+    assert fwd(nslots=1) == 1                                       # 2 sequences, 1 slot, no indirection
+    d = _abi.ConvDims(64, 4, _abi.DTYPE_BF16, 1)
+    assert lib.ers_conv1d_update(ctypes.byref(d), 2, FAKE, FAKE, None, 0, 4, None, FAKE, None, None) == 1
+    assert lib.ers_conv1d_update(ctypes.byref(d), 2, FAKE, MISALIGNED, None, FAKE, 4, None, FAKE, None, None) == 4
+    assert lib.ers_conv1d_update(ctypes.byref(d), 0, None, None, None, None, 0, None, None, None, None) == 0
