@@ -68,7 +68,8 @@ class Cache(ctypes.Structure):
                 ("buf_dt", ctypes.c_void_p), ("buf_B", ctypes.c_void_p), ("buf_C", ctypes.c_void_p),
                 ("pos", ctypes.c_void_p), ("nslots", ctypes.c_int32), ("read_dtype", ctypes.c_int32),
                 ("read_scale", ctypes.c_void_p), ("read_block_scale", ctypes.c_void_p),
-                ("anchor_dtype", ctypes.c_int32), ("sr_key", ctypes.c_uint32 * 2), ("sr_nonce", ctypes.c_uint32)]
+                ("anchor_dtype", ctypes.c_int32), ("sr_key", ctypes.c_uint32 * 2), ("sr_nonce", ctypes.c_uint32),
+                ("buf_pages", ctypes.c_void_p), ("page_rows", ctypes.c_int32), ("npages", ctypes.c_int32)]
 
 
 _lib = None

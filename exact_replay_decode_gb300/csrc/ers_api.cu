@@ -60,11 +60,18 @@ ers_status check_f16_anchor(const ers_dims* d, const ers_cache* c, bool rssm) {
   return ERS_OK;
 }
 
+ers_status check_pages(const ers_dims* d, const ers_cache* c) {
+  if (c->buf_pages != nullptr && d->chunk % c->page_rows != 0) return ERS_ESHAPE;
+  return ERS_OK;
+}
+
 ers_status check_cache(const ers_cache* c, bool need_read_copy) {
   if (c == nullptr || c->nslots < 0) return ERS_EINVAL;
   if (c->read_dtype != ERS_READ_BF16 && c->read_dtype != ERS_READ_FP8_E4M3 && c->read_dtype != ERS_READ_NVFP4)
     return ERS_EDTYPE;
   if (c->anchor_dtype != ERS_ANCHOR_F32 && c->anchor_dtype != ERS_ANCHOR_F16_SR) return ERS_EDTYPE;
+  ERS_TRY(check_ptr(c->buf_pages, false));
+  if (c->buf_pages != nullptr && (c->page_rows < 1 || c->npages < 1)) return ERS_EINVAL;
   ERS_TRY(check_state_ptrs(c));
   ERS_TRY(check_ptr(c->read_copy, need_read_copy));
   if (c->read_dtype != ERS_READ_BF16 && c->read_copy != nullptr) ERS_TRY(check_ptr(c->read_scale, true));
@@ -101,6 +108,9 @@ void set_cache(LaunchArgs& a, const ers_cache* c) {
   a.read_nvfp4 = c->read_copy != nullptr && c->read_dtype == ERS_READ_NVFP4;
   a.read_scale = c->read_scale;
   a.read_bscale = c->read_block_scale;
+  a.buf_pages = c->buf_pages;
+  a.page_rows = c->buf_pages != nullptr ? c->page_rows : 1;
+  a.npages = c->npages;
   a.anchor_f16 = c->anchor_dtype == ERS_ANCHOR_F16_SR;
   a.sr_key0 = c->sr_key[0];
   a.sr_key1 = c->sr_key[1];
@@ -222,6 +232,7 @@ ers_status ers_chunked_prefill(const ers_dims* dims, const ers_params* prm, cons
   ERS_TRY(check_dims(dims));
   ERS_TRY(check_params(prm));
   ERS_TRY(check_cache(cache, false));
+  ERS_TRY(check_pages(dims, cache));
   if (f16_anchor(cache)) return ERS_EUNSUPPORTED;   // chunked prefill writes fp32 checkpoints
   if (nseq < 0 || ntokens < 0 || max_seqlen < 0) return ERS_EINVAL;
   if (nseq == 0) return ERS_OK;
@@ -260,6 +271,7 @@ ers_status ers_replay_decode(const ers_dims* dims, const ers_params* prm, const 
   const bool rssm = (flags & ERS_FLAG_REPLAYSSM) != 0;
   if ((flags & ~(ERS_FLAG_FUSE_REFRESH | ERS_FLAG_REPLAYSSM)) != 0) return ERS_EINVAL;
   ERS_TRY(check_cache(cache, rssm));
+  ERS_TRY(check_pages(dims, cache));
   if (nseq < 0) return ERS_EINVAL;
   if (nseq == 0) return ERS_OK;
   if (slot == nullptr && nseq > cache->nslots) return ERS_EINVAL;
@@ -300,6 +312,7 @@ ers_status ers_refresh(const ers_dims* dims, const ers_params* prm, const ers_ca
   ERS_TRY(check_params(prm));
   if ((flags & ~ERS_FLAG_REPLAYSSM) != 0) return ERS_EINVAL;
   ERS_TRY(check_cache(cache, false));
+  ERS_TRY(check_pages(dims, cache));
   if (nseq < 0 || drafts_T < 0) return ERS_EINVAL;
   if (nseq == 0) return ERS_OK;
   if (slot == nullptr && nseq > cache->nslots) return ERS_EINVAL;
@@ -326,6 +339,7 @@ ers_status ers_spec_verify(const ers_dims* dims, const ers_params* prm, const er
   ERS_TRY(check_params(prm));
   if ((flags & ~ERS_FLAG_AUTO_FLUSH) != 0) return ERS_EINVAL;
   ERS_TRY(check_cache(cache, true));
+  ERS_TRY(check_pages(dims, cache));
   if (nseq < 0 || T < 1 || T > dims->chunk) return ERS_EINVAL;
   if (nseq == 0) return ERS_OK;
   if (slot == nullptr && nseq > cache->nslots) return ERS_EINVAL;

@@ -127,11 +127,36 @@ __device__ __forceinline__ float combine_out(float decay_t, float yoff, float yd
   return __fmaf_rn(Dh, xt, __fadd_rn(__fmul_rn(decay_t, yoff), ydiag));
 }
 
+// Buffer row of row r (0 <= r < Q) of a slot's partial-chunk buffer: slot * Q + r when the buffers are
+// contiguous, else the page table's page for r.  A page index outside [0, npages) is reported
+// (ERS_ESLOT) and clamped, so a bad table cannot address outside the buffers.
+struct BufMap {
+  const int32_t* pages;
+  int Q, pr, npages;
+  int32_t* status;
+  __device__ __forceinline__ long long row(int slot, int r) const {
+    if (pages == nullptr) return (long long)slot * Q + r;
+    int pg = pages[(long long)slot * (Q / pr) + r / pr];
+    if (pg < 0 || pg >= npages) {
+      report(status, ERS_ESLOT);
+      pg = pg < 0 ? 0 : npages - 1;
+    }
+    return (long long)pg * pr + r % pr;
+  }
+};
+
+__device__ __forceinline__ BufMap buf_map(const LaunchArgs& a) {
+  return BufMap{a.buf_pages, a.Q, a.page_rows, a.npages, a.status};
+}
+
+__device__ __forceinline__ long long buf_row(const LaunchArgs& a, int slot, int r) { return buf_map(a).row(slot, r); }
+
 // Row source of a chunk: rows [0, nbuf) come from a slot's partial-chunk buffer, rows >= nbuf from
 // packed token inputs (row r is token tok0 + r).  Row strides are the token strides H*P, H, G*N.
 template <typename T>
 struct Rows {
-  int nbuf;
+  int nbuf, slot;
+  BufMap map;
   const T* bx;
   const float* bdt;
   const T* bB;
@@ -143,16 +168,16 @@ struct Rows {
   long long tok0;
   int sx, sdt, sB;
   __device__ __forceinline__ const T* x(int r) const {
-    return r < nbuf ? bx + (long long)r * sx : x0 + (tok0 + r) * sx;
+    return r < nbuf ? bx + map.row(slot, r) * sx : x0 + (tok0 + r) * sx;
   }
   __device__ __forceinline__ float dt(int r) const {
-    return r < nbuf ? bdt[(long long)r * sdt] : dt0[(tok0 + r) * sdt];
+    return r < nbuf ? bdt[map.row(slot, r) * sdt] : dt0[(tok0 + r) * sdt];
   }
   __device__ __forceinline__ const T* B(int r) const {
-    return r < nbuf ? bB + (long long)r * sB : B0 + (tok0 + r) * sB;
+    return r < nbuf ? bB + map.row(slot, r) * sB : B0 + (tok0 + r) * sB;
   }
   __device__ __forceinline__ const T* C(int r) const {
-    return r < nbuf ? bC + (long long)r * sB : C0 + (tok0 + r) * sB;
+    return r < nbuf ? bC + map.row(slot, r) * sB : C0 + (tok0 + r) * sB;
   }
 };
 
@@ -161,14 +186,16 @@ __device__ __forceinline__ Rows<T> make_rows(const LaunchArgs& a, int slot, int 
   const int g = h / (a.H / a.G);
   Rows<T> r;
   r.nbuf = nbuf;
+  r.slot = slot;
+  r.map = buf_map(a);
   r.sx = a.H * a.P;
   r.sdt = a.H;
   r.sB = a.G * a.N;
   if (slot >= 0 && a.bx != nullptr) {
-    r.bx = (const T*)a.bx + ((size_t)slot * a.Q * a.H + h) * a.P;
-    r.bdt = a.bdt + (size_t)slot * a.Q * a.H + h;
-    r.bB = (const T*)a.bB + ((size_t)slot * a.Q * a.G + g) * a.N;
-    r.bC = (const T*)a.bC + ((size_t)slot * a.Q * a.G + g) * a.N;
+    r.bx = (const T*)a.bx + (size_t)h * a.P;
+    r.bdt = a.bdt + h;
+    r.bB = (const T*)a.bB + (size_t)g * a.N;
+    r.bC = (const T*)a.bC + (size_t)g * a.N;
   } else {
     r.bx = nullptr; r.bdt = nullptr; r.bB = nullptr; r.bC = nullptr;
   }

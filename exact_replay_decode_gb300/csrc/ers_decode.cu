@@ -342,24 +342,24 @@ __global__ void __launch_bounds__(kThreads, 2) k_decode_heads(LaunchArgs a) {
   const bool refresh = std::is_same<HT, float>::value && !rssm && fuse && p + 1 == a.Q;
   const int o0 = flush ? p : 0, pn = p - o0;   // output rows s = 0..pn are smem rows o0 + s
   // buffer rows 0..p-1 and the new token as row p: the group's B rows, this head's x rows
-  const T* bB = (const T*)a.bB + (size_t)slot * a.Q * GN + (size_t)g * N;
+  const T* bB = (const T*)a.bB + (size_t)g * N;   // buffer row r at buf_row(a, slot, r)
   const T* nB = (const T*)a.B + (size_t)i * GN + (size_t)g * N;
   constexpr int kBChunks = N * sizeof(T) / 16, kXChunks = P * sizeof(T) / 16;
   for (int k = tid; k < (p + 1) * kBChunks; k += kThreads) {
     const int s = k / kBChunks, e = k % kBChunks;
     cp_async16(reinterpret_cast<char*>(sB + s * N) + 16 * e,
-               reinterpret_cast<const char*>(s < p ? bB + s * GN : nB) + 16 * e);
+               reinterpret_cast<const char*>(s < p ? bB + buf_row(a, slot, s) * GN : nB) + 16 * e);
   }
   T* sx = sxa + w * QR * P;
-  const T* bx = (const T*)a.bx + (size_t)slot * a.Q * HP + (size_t)h * P;
+  const T* bx = (const T*)a.bx + (size_t)h * P;
   const T* nx = (const T*)a.x + (size_t)i * HP + (size_t)h * P;
   if (active)
     for (int k = j; k < (p + 1) * kXChunks; k += 32) {
       const int s = k / kXChunks, e = k % kXChunks;
       cp_async16(reinterpret_cast<char*>(sx + s * P) + 16 * e,
-                 reinterpret_cast<const char*>(s < p ? bx + s * HP : nx) + 16 * e);
+                 reinterpret_cast<const char*>(s < p ? bx + buf_row(a, slot, s) * HP : nx) + 16 * e);
     }
-  const float dt_buf = j < p ? a.bdt[((size_t)slot * a.Q + j) * a.H + h] : 0.f;
+  const float dt_buf = j < p ? a.bdt[buf_row(a, slot, j) * a.H + h] : 0.f;
   const float dt_raw = j <= pn ? (o0 + j < p ? dt_buf : a.dt[(size_t)i * a.H + h]) : 0.f;
   float dl = 0.f;
   df v = {0.f, 0.f};
@@ -442,11 +442,12 @@ __global__ void __launch_bounds__(kThreads, 2) k_decode_heads(LaunchArgs a) {
     y[d] = from_f<T>(combine_out(et, yo[d], acc, Dh, to_f(sx[p * P + d])));
   }
   // append the new token to the buffer (B/C once per group)
-  T* dx = (T*)a.bx + ((size_t)slot * a.Q + pn) * HP + (size_t)h * P;
+  const long long brow = buf_row(a, slot, pn);
+  T* dx = (T*)a.bx + brow * HP + (size_t)h * P;
   for (int d = j; d < P; d += 32) dx[d] = sx[p * P + d];
-  if (j == 0) a.bdt[((size_t)slot * a.Q + pn) * a.H + h] = a.dt[(size_t)i * a.H + h];
+  if (j == 0) a.bdt[brow * a.H + h] = a.dt[(size_t)i * a.H + h];
   if (hl == 0) {
-    const size_t dst = ((size_t)slot * a.Q + pn) * GN + (size_t)g * N, src = (size_t)i * GN + (size_t)g * N;
+    const size_t dst = brow * GN + (size_t)g * N, src = (size_t)i * GN + (size_t)g * N;
     for (int n = j; n < N; n += 32) {
       ((T*)a.bB)[dst + n] = sB[p * N + n];
       ((T*)a.bC)[dst + n] = ((const T*)a.C)[src + n];
@@ -515,23 +516,25 @@ __global__ void __launch_bounds__(kThreads, 2) k_refresh_heads(LaunchArgs a) {
   const bool rssm = (a.flags & ERS_FLAG_REPLAYSSM) != 0;
   if (!(rssm ? (p + a.T > a.Q) : (p == a.Q))) return;
   const size_t HP = (size_t)a.H * P, GN = (size_t)a.G * N;
-  const T* bB = (const T*)a.bB + (size_t)slot * a.Q * GN + (size_t)g * N;
+  const T* bB = (const T*)a.bB + (size_t)g * N;
   constexpr int kBChunks = N * sizeof(T) / 16, kXChunks = P * sizeof(T) / 16;
   for (int k = tid; k < p * kBChunks; k += kThreads) {
     const int s = k / kBChunks, e = k % kBChunks;
-    cp_async16(reinterpret_cast<char*>(sB + s * N) + 16 * e, reinterpret_cast<const char*>(bB + s * GN) + 16 * e);
+    cp_async16(reinterpret_cast<char*>(sB + s * N) + 16 * e,
+               reinterpret_cast<const char*>(bB + buf_row(a, slot, s) * GN) + 16 * e);
   }
   T* sx = sxa + w * QM * P;
-  const T* bx = (const T*)a.bx + (size_t)slot * a.Q * HP + (size_t)h * P;
+  const T* bx = (const T*)a.bx + (size_t)h * P;
   if (active)
     for (int k = j; k < p * kXChunks; k += 32) {
       const int s = k / kXChunks, e = k % kXChunks;
-      cp_async16(reinterpret_cast<char*>(sx + s * P) + 16 * e, reinterpret_cast<const char*>(bx + s * HP) + 16 * e);
+      cp_async16(reinterpret_cast<char*>(sx + s * P) + 16 * e,
+                 reinterpret_cast<const char*>(bx + buf_row(a, slot, s) * HP) + 16 * e);
     }
   float dc = 0.f;
   df vc = {0.f, 0.f};
   if (j < p) {
-    dc = delta_of(a.bdt[((size_t)slot * a.Q + j) * a.H + h], a.dt_bias[h]);
+    dc = delta_of(a.bdt[buf_row(a, slot, j) * a.H + h], a.dt_bias[h]);
     vc.hi = __fmul_rn(dc, a.A[h]);
   }
   vc = warp_scan_df(vc, j);

@@ -330,13 +330,13 @@ __global__ void __launch_bounds__(kThreads) k_decode(LaunchArgs a) {
     row_output<T, P, N, float>(sm, xs, p, Hd, a.D[h], y);
   // append the new token to the buffer (B/C once per group)
   const int g = h / (a.H / a.G);
-  T* bx = (T*)a.bx + (((size_t)slot * a.Q + p) * a.H + h) * P;
+  T* bx = (T*)a.bx + (buf_row(a, slot, p) * a.H + h) * P;
   const T* nx = (const T*)a.x + ((size_t)i * a.H + h) * P;
   for (int d = threadIdx.x; d < P; d += kThreads) bx[d] = nx[d];
-  if (threadIdx.x == 0) a.bdt[((size_t)slot * a.Q + p) * a.H + h] = a.dt[(size_t)i * a.H + h];
+  if (threadIdx.x == 0) a.bdt[buf_row(a, slot, p) * a.H + h] = a.dt[(size_t)i * a.H + h];
   if (h % (a.H / a.G) == 0) {
-    T* bB = (T*)a.bB + (((size_t)slot * a.Q + p) * a.G + g) * N;
-    T* bC = (T*)a.bC + (((size_t)slot * a.Q + p) * a.G + g) * N;
+    T* bB = (T*)a.bB + (buf_row(a, slot, p) * a.G + g) * N;
+    T* bC = (T*)a.bC + (buf_row(a, slot, p) * a.G + g) * N;
     const T* nB = (const T*)a.B + ((size_t)i * a.G + g) * N;
     const T* nC = (const T*)a.C + ((size_t)i * a.G + g) * N;
     for (int n = threadIdx.x; n < N; n += kThreads) {
@@ -449,15 +449,15 @@ __global__ void __launch_bounds__(kThreads) k_verify(LaunchArgs a) {
   const int g = h / (a.H / a.G);
   for (int idx = threadIdx.x; idx < a.T * P; idx += kThreads) {
     const int j = idx / P, d = idx % P;
-    ((T*)a.bx)[(((size_t)slot * a.Q + h0 + j) * a.H + h) * P + d] =
+    ((T*)a.bx)[(buf_row(a, slot, h0 + j) * a.H + h) * P + d] =
         ((const T*)a.x)[(((size_t)i * a.T + j) * a.H + h) * P + d];
   }
   for (int j = threadIdx.x; j < a.T; j += kThreads)
-    a.bdt[((size_t)slot * a.Q + h0 + j) * a.H + h] = a.dt[((size_t)i * a.T + j) * a.H + h];
+    a.bdt[buf_row(a, slot, h0 + j) * a.H + h] = a.dt[((size_t)i * a.T + j) * a.H + h];
   if (h % (a.H / a.G) == 0) {
     for (int idx = threadIdx.x; idx < a.T * N; idx += kThreads) {
       const int j = idx / N, n = idx % N;
-      const size_t dst = (((size_t)slot * a.Q + h0 + j) * a.G + g) * N + n;
+      const size_t dst = (buf_row(a, slot, h0 + j) * a.G + g) * N + n;
       const size_t src = (((size_t)i * a.T + j) * a.G + g) * N + n;
       ((T*)a.bB)[dst] = ((const T*)a.B)[src];
       ((T*)a.bC)[dst] = ((const T*)a.C)[src];
@@ -523,7 +523,7 @@ __global__ void k_tail(LaunchArgs a) {
     const int rs = nfull * a.Q + r;  // stream position
     if (rs < sg.p) continue;          // already buffered at row r (only when nfull == 0)
     const size_t tok = (size_t)a.cu[i] + (rs - sg.p);
-    const size_t brow = (size_t)sg.slot * a.Q + r;
+    const size_t brow = buf_row(a, sg.slot, r);
     for (int k = threadIdx.x; k < HP; k += blockDim.x) ((T*)a.bx)[brow * HP + k] = ((const T*)a.x)[tok * HP + k];
     for (int k = threadIdx.x; k < a.H; k += blockDim.x) a.bdt[brow * a.H + k] = a.dt[tok * a.H + k];
     for (int k = threadIdx.x; k < GN; k += blockDim.x) {

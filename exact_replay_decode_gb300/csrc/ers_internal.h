@@ -46,6 +46,10 @@ struct LaunchArgs {
   int32_t* pos;
   const int32_t* slot;
   int nslots;
+  // paged partial-chunk buffers: row r of slot s is buffer row buf_pages[s][r / page_rows] *
+  // page_rows + r % page_rows (buffers hold npages * page_rows rows); contiguous when null
+  const int32_t* buf_pages;
+  int page_rows, npages;
   // outputs / plain-scan state
   void* y;
   const float* init_state;

@@ -433,11 +433,11 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_decode(LaunchArgs a, uint32_
   // append the new token to the buffer (B/C once per group)
   const int g = h / (a.H / a.G);
   const bf16* nx = (const bf16*)a.x + ((size_t)i * a.H + h) * P;
-  bf16* bx = (bf16*)a.bx + (((size_t)slot * a.Q + p) * a.H + h) * P;
+  bf16* bx = (bf16*)a.bx + (buf_row(a, slot, p) * a.H + h) * P;
   for (int d = threadIdx.x; d < P; d += kThreads) bx[d] = nx[d];
-  if (threadIdx.x == 0) a.bdt[((size_t)slot * a.Q + p) * a.H + h] = a.dt[(size_t)i * a.H + h];
+  if (threadIdx.x == 0) a.bdt[buf_row(a, slot, p) * a.H + h] = a.dt[(size_t)i * a.H + h];
   if (h % (a.H / a.G) == 0) {
-    const size_t dst = (((size_t)slot * a.Q + p) * a.G + g) * N, src = ((size_t)i * a.G + g) * N;
+    const size_t dst = (buf_row(a, slot, p) * a.G + g) * N, src = ((size_t)i * a.G + g) * N;
     for (int n = threadIdx.x; n < N; n += kThreads) {
       ((bf16*)a.bB)[dst + n] = ((const bf16*)a.B)[src + n];
       ((bf16*)a.bC)[dst + n] = ((const bf16*)a.C)[src + n];
@@ -540,15 +540,15 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_verify(LaunchArgs a, uint32_
   const int g = h / (a.H / a.G);
   for (int idx = threadIdx.x; idx < a.T * P; idx += kThreads) {
     const int j = idx / P, d = idx % P;
-    ((bf16*)a.bx)[(((size_t)slot * a.Q + h0 + j) * a.H + h) * P + d] =
+    ((bf16*)a.bx)[(buf_row(a, slot, h0 + j) * a.H + h) * P + d] =
         ((const bf16*)a.x)[(((size_t)i * a.T + j) * a.H + h) * P + d];
   }
   for (int j = threadIdx.x; j < a.T; j += kThreads)
-    a.bdt[((size_t)slot * a.Q + h0 + j) * a.H + h] = a.dt[((size_t)i * a.T + j) * a.H + h];
+    a.bdt[buf_row(a, slot, h0 + j) * a.H + h] = a.dt[((size_t)i * a.T + j) * a.H + h];
   if (h % (a.H / a.G) == 0) {
     for (int idx = threadIdx.x; idx < a.T * N; idx += kThreads) {
       const int j = idx / N, n = idx % N;
-      const size_t dst = (((size_t)slot * a.Q + h0 + j) * a.G + g) * N + n;
+      const size_t dst = (buf_row(a, slot, h0 + j) * a.G + g) * N + n;
       const size_t src = (((size_t)i * a.T + j) * a.G + g) * N + n;
       ((bf16*)a.bB)[dst] = ((const bf16*)a.B)[src];
       ((bf16*)a.bC)[dst] = ((const bf16*)a.C)[src];

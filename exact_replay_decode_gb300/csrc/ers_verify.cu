@@ -210,25 +210,25 @@ __global__ void __launch_bounds__(kThreads, 2) k_verify_heads(LaunchArgs a) {
     for (int r = 0; r < kVerifyRowsInFlight; ++r) q[r] = src.ld(r, j);
   }
   // committed rows 0..hc-1 at smem rows 0..hc-1, drafts at rows QM..QM+T-1
-  const T* bB = (const T*)a.bB + (size_t)slot * a.Q * GN + (size_t)g * N;
+  const T* bB = (const T*)a.bB + (size_t)g * N;   // buffer row r at buf_row(a, slot, r)
   constexpr int kBChunks = N * sizeof(T) / 16, kXChunks = P * sizeof(T) / 16;
   for (int k = tid; k < (hc + Td) * kBChunks; k += kThreads) {
     const int r = k / kBChunks, e = k % kBChunks;
-    const T* src = r < hc ? bB + r * GN : (const T*)a.B + ((size_t)i * Td + (r - hc)) * GN + (size_t)g * N;
+    const T* src = r < hc ? bB + buf_row(a, slot, r) * GN : (const T*)a.B + ((size_t)i * Td + (r - hc)) * GN + (size_t)g * N;
     cp_async16(reinterpret_cast<char*>(sB + (r < hc ? r : QM + r - hc) * N) + 16 * e,
                reinterpret_cast<const char*>(src) + 16 * e);
   }
   T* sx = sxa + w * QR * P;
   if (active) {
-    const T* bx = (const T*)a.bx + (size_t)slot * a.Q * HP + (size_t)h * P;
+    const T* bx = (const T*)a.bx + (size_t)h * P;
     for (int k = j; k < (hc + Td) * kXChunks; k += 32) {
       const int r = k / kXChunks, e = k % kXChunks;
-      const T* src = r < hc ? bx + r * HP : (const T*)a.x + ((size_t)i * Td + (r - hc)) * HP + (size_t)h * P;
+      const T* src = r < hc ? bx + buf_row(a, slot, r) * HP : (const T*)a.x + ((size_t)i * Td + (r - hc)) * HP + (size_t)h * P;
       cp_async16(reinterpret_cast<char*>(sx + (r < hc ? r : QM + r - hc) * P) + 16 * e,
                  reinterpret_cast<const char*>(src) + 16 * e);
     }
   }
-  const float dt_c = j < hc ? a.bdt[((size_t)slot * a.Q + j) * a.H + h] : 0.f;
+  const float dt_c = j < hc ? a.bdt[buf_row(a, slot, j) * a.H + h] : 0.f;
   const float dt_d = j < Td ? a.dt[((size_t)i * Td + j) * a.H + h] : 0.f;
   const float Ah = a.A[h], bias = a.dt_bias[h];
   float* yo = syo + w * kDraftsMax * P;
@@ -331,13 +331,13 @@ __global__ void __launch_bounds__(kThreads, 2) k_verify_heads(LaunchArgs a) {
   }
   // the drafts go to buffer rows h0..h0+T-1 (B/C once per group)
   for (int k = 0; k < Td; ++k) {
-    T* dx = (T*)a.bx + ((size_t)slot * a.Q + h0 + k) * HP + (size_t)h * P;
+    T* dx = (T*)a.bx + buf_row(a, slot, h0 + k) * HP + (size_t)h * P;
     for (int d = j; d < P; d += 32) dx[d] = sx[(QM + k) * P + d];
   }
-  if (j < Td) a.bdt[((size_t)slot * a.Q + h0 + j) * a.H + h] = dt_d;
+  if (j < Td) a.bdt[buf_row(a, slot, h0 + j) * a.H + h] = dt_d;
   if (w == 0) {
     for (int k = 0; k < Td; ++k) {
-      const size_t dst = ((size_t)slot * a.Q + h0 + k) * GN + (size_t)g * N;
+      const size_t dst = buf_row(a, slot, h0 + k) * GN + (size_t)g * N;
       const size_t src = ((size_t)i * Td + k) * GN + (size_t)g * N;
       for (int n = j; n < N; n += 32) {
         ((T*)a.bB)[dst + n] = sB[(QM + k) * N + n];

@@ -194,11 +194,16 @@ class ReplayCache:
 
     anchor "fp32": state [S,H,P,N] fp32.  anchor "fp16_sr" (ReplaySSM only): state [S,H,P,N] fp16,
     written by stochastic rounding with random words keyed by sr_key and the attribute sr_nonce,
-    which the caller sets to a fresh value before every call that may refresh anchors."""
+    which the caller sets to a fresh value before every call that may refresh anchors.
+
+    paged=(page_rows, npages): the partial-chunk buffers are [npages, page_rows, ...] and
+    buf_pages [S, chunk / page_rows] int32 maps each slot's logical pages to physical ones
+    (initially slot s owns pages s * chunk / page_rows onward when npages allows, else page 0)."""
 
     def __init__(self, nslots: int, nheads: int, ngroups: int, headdim: int, dstate: int, chunk: int,
                  io_dtype: torch.dtype = torch.bfloat16, read_copy: bool = False, device="cuda",
-                 read_dtype: str = "bf16", anchor: str = "fp32", sr_key: Tuple[int, int] = (0, 0)):
+                 read_dtype: str = "bf16", anchor: str = "fp32", sr_key: Tuple[int, int] = (0, 0),
+                 paged: Optional[Tuple[int, int]] = None):
         if read_dtype not in ("bf16", "fp8", "nvfp4"):
             raise ValueError(f"read_dtype must be 'bf16', 'fp8' or 'nvfp4', got {read_dtype!r}")
         self.nslots, self.H, self.G, self.P, self.N, self.Q = nslots, nheads, ngroups, headdim, dstate, chunk
@@ -227,10 +232,23 @@ class ReplayCache:
                 self.read_block_scale = torch.zeros(nslots, nheads, headdim, dstate // 16, dtype=torch.uint8, **z)
             if read_dtype != "bf16":
                 self.read_scale = torch.zeros(nslots, nheads, headdim, dtype=torch.float32, **z)
-        self.buf_x = torch.zeros(nslots, chunk, nheads, headdim, dtype=io_dtype, **z)
-        self.buf_dt = torch.zeros(nslots, chunk, nheads, dtype=torch.float32, **z)
-        self.buf_B = torch.zeros(nslots, chunk, ngroups, dstate, dtype=io_dtype, **z)
-        self.buf_C = torch.zeros(nslots, chunk, ngroups, dstate, dtype=io_dtype, **z)
+        self.buf_pages = None
+        self.page_rows = 0
+        self.npages = 0
+        lead = (nslots, chunk)
+        if paged is not None:
+            pr, npg = int(paged[0]), int(paged[1])
+            if pr < 1 or chunk % pr or npg < 1:
+                raise ValueError("paged=(page_rows, npages) needs page_rows dividing chunk and npages >= 1")
+            self.page_rows, self.npages = pr, npg
+            ppl = chunk // pr
+            ids = torch.arange(nslots * ppl, dtype=torch.int32)
+            self.buf_pages = torch.where(ids < npg, ids, torch.zeros_like(ids)).view(nslots, ppl).to(device)
+            lead = (npg, pr)
+        self.buf_x = torch.zeros(*lead, nheads, headdim, dtype=io_dtype, **z)
+        self.buf_dt = torch.zeros(*lead, nheads, dtype=torch.float32, **z)
+        self.buf_B = torch.zeros(*lead, ngroups, dstate, dtype=io_dtype, **z)
+        self.buf_C = torch.zeros(*lead, ngroups, dstate, dtype=io_dtype, **z)
         self.pos = torch.zeros(nslots, dtype=torch.int32, **z)
 
     @property
@@ -243,7 +261,8 @@ class ReplayCache:
                           self.buf_B.data_ptr(), self.buf_C.data_ptr(), self.pos.data_ptr(), self.nslots, rd,
                           _ptr(self.read_scale), _ptr(self.read_block_scale),
                           _abi.ANCHOR_F16_SR if self.anchor == "fp16_sr" else _abi.ANCHOR_F32,
-                          (ctypes.c_uint32 * 2)(*self.sr_key), int(self.sr_nonce) & 0xFFFFFFFF)
+                          (ctypes.c_uint32 * 2)(*self.sr_key), int(self.sr_nonce) & 0xFFFFFFFF,
+                          _ptr(self.buf_pages), self.page_rows, self.npages)
 
     def read_values(self) -> Optional[torch.Tensor]:
         """The read copy's values as fp32 (FP8: code * row scale), or None without a read copy."""
@@ -262,7 +281,7 @@ class ReplayCache:
 
     def nbytes(self) -> int:
         ts = [self.state, self.buf_x, self.buf_dt, self.buf_B, self.buf_C, self.pos]
-        ts += [t for t in (self.read_copy, self.read_scale, self.read_block_scale) if t is not None]
+        ts += [t for t in (self.read_copy, self.read_scale, self.read_block_scale, self.buf_pages) if t is not None]
         return sum(t.numel() * t.element_size() for t in ts)
 
 

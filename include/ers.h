@@ -112,6 +112,12 @@ typedef struct ers_params {
  *   read_scale [nslots, H, P] fp32, FP8 and NVFP4 read copies only (else NULL): one power-of-two
  *             scale per state row.
  *   read_block_scale [nslots, H, P, N / 16] e4m3 bytes, NVFP4 only (else NULL).
+ *   buf_pages [nslots, Q / page_rows] int32 or NULL: paged partial-chunk buffers (RFC section 6,
+ *             "contiguous and paged buffer layouts": slot and position indexed separately).  With a
+ *             table, buf_x / buf_dt / buf_B / buf_C hold npages * page_rows rows ([npages,
+ *             page_rows, H, P] and so on) and row r of slot s is row buf_pages[s][r / page_rows] *
+ *             page_rows + r % page_rows; page_rows divides Q.  A page index outside [0, npages) is
+ *             reported as ERS_ESLOT and clamped.  NULL: the contiguous [nslots, Q, ...] layout.
  *
  * FP8 read copy (ReplaySSM "Paper-reported results", the FP8-read / FP32-recurrence mode; the page
  * names the mode without its quantisation, so this library defines it): each state row (one d of
@@ -161,6 +167,9 @@ typedef struct ers_cache {
   int32_t anchor_dtype;
   uint32_t sr_key[2];
   uint32_t sr_nonce;
+  const int32_t* buf_pages;
+  int32_t page_rows;
+  int32_t npages;
 } ers_cache;
 
 /* Human-readable name of a status code (static storage, never NULL). */

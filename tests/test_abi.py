@@ -191,3 +191,20 @@ def test_validation_of_conv1d(lib):
     assert lib.ers_conv1d_update(ctypes.byref(d), 2, FAKE, FAKE, None, 0, 4, None, FAKE, None, None) == 1
     assert lib.ers_conv1d_update(ctypes.byref(d), 2, FAKE, MISALIGNED, None, FAKE, 4, None, FAKE, None, None) == 4
     assert lib.ers_conv1d_update(ctypes.byref(d), 0, None, None, None, None, 0, None, None, None, None) == 0
+
+
+@needs_no_gpu
+def test_validation_of_paged_buffers(lib):
+    from exact_replay_decode_gb300 import _abi
+    p = _prm()
+
+    def dec(page_rows, npages, pages=FAKE, chunk=16):
+        d = _dims(chunk=chunk)
+        c = _abi.Cache(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 4, _abi.READ_BF16, None, None, 0, (0, 0), 0, pages,
+                       page_rows, npages)
+        return lib.ers_replay_decode(ctypes.byref(d), ctypes.byref(p), ctypes.byref(c), 4, None, FAKE, FAKE, FAKE,
+                                     FAKE, _abi.FLAG_FUSE_REFRESH, FAKE, None, None)
+
+    assert dec(0, 8) == 1 and dec(4, 0) == 1                       # page geometry
+    assert dec(5, 8) == 2                                          # page_rows must divide the chunk
+    assert dec(4, 8, pages=MISALIGNED) == 4
