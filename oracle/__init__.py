@@ -325,6 +325,78 @@ def causal_conv1d(x: np.ndarray, weight: np.ndarray, bias: Optional[np.ndarray],
     return y, fin
 
 
+# ---- gated delta rule (GDN), the second layer family of the ReplaySSM notes ---------------------------
+def gdn_recurrence(q, k, v, g, beta, state: np.ndarray):
+    """Gated delta rule, token by token in fp64, for one sequence:
+        a_t = exp(g_t),  u_t = beta_t (v_t - a_t S_{t-1} k_t),  S_t = a_t S_{t-1} + u_t k_t^T,
+        o_t = S_t q_t,
+    per value head h with key/query group h // (H / G).  q, k [T, G, dk]; v [T, H, dv]; g, beta
+    [T, H]; state [H, dv, dk] (S maps keys to values).  Returns (o [T, H, dv], final state)."""
+    S = np.array(state, dtype=np.float64, copy=True)
+    q, k, v, g, beta = (_f64(a) for a in (q, k, v, g, beta))
+    T, H = g.shape
+    G = q.shape[1]
+    hg = np.arange(H) // (H // G)
+    out = np.zeros((T, H, S.shape[1]))
+    for t in range(T):
+        kt, qt = k[t][hg], q[t][hg]                       # [H, dk]
+        a = np.exp(g[t])[:, None]
+        Sk = np.einsum("hdn,hn->hd", S, kt)
+        u = beta[t][:, None] * (v[t] - a * Sk)
+        S = a[:, :, None] * S + u[:, :, None] * kt[:, None, :]
+        out[t] = np.einsum("hdn,hn->hd", S, qt)
+    return out, S
+
+
+class GdnReplayModel:
+    """ReplaySSM-style speculative decoding for a GDN layer (ReplaySSM notes, "Core equations" and
+    "Data protocol"): per sequence an fp64 anchor, a read copy cast from it, and the committed
+    records since the last refresh.  verify() flushes when h + T > L (folds the committed records
+    into the anchor with the recurrence, recasts the read copy), then runs the recurrence from the
+    READ COPY over committed records + drafts and returns the drafts' outputs; commit() appends the
+    accepted drafts.  An empty history leaves the anchor unchanged."""
+
+    def __init__(self, anchor: np.ndarray, L: int, read_cast=None):
+        self.anchor = np.array(anchor, dtype=np.float64, copy=True)   # [S, H, dv, dk]
+        self.read_cast = read_cast if read_cast is not None else bf16_round
+        self.read = self.read_cast(self.anchor)
+        self.L = L
+        self.committed: List[list] = [[] for _ in range(self.anchor.shape[0])]
+        self.flushes = 0
+
+    def h(self) -> np.ndarray:
+        return np.array([len(c) for c in self.committed], dtype=np.int32)
+
+    @staticmethod
+    def _stack(recs):
+        return tuple(np.stack([r[f] for r in recs]) for f in range(5))
+
+    def verify(self, drafts):
+        """drafts[i] = (q [T,G,dk], k [T,G,dk], v [T,H,dv], g [T,H], beta [T,H]); returns [S, T, H, dv]."""
+        T = drafts[0][0].shape[0]
+        outs = []
+        for i, dr in enumerate(drafts):
+            if len(self.committed[i]) + T > self.L and self.committed[i]:   # flush (never an empty one)
+                rec = self._stack(self.committed[i])
+                _, fin = gdn_recurrence(*rec, self.anchor[i])
+                self.anchor[i] = fin
+                self.read[i] = self.read_cast(fin)
+                self.committed[i] = []
+                self.flushes += 1
+            recs = self.committed[i]
+            seq = tuple(np.concatenate([self._stack(recs)[f], dr[f]]) if recs else dr[f] for f in range(5))
+            o, _ = gdn_recurrence(*seq, self.read[i])
+            outs.append(o[len(recs):])
+        self._pending = drafts
+        return np.stack(outs)
+
+    def commit(self, accepted):
+        for i, a in enumerate(accepted):
+            for j in range(int(a)):
+                self.committed[i].append(tuple(self._pending[i][f][j] for f in range(5)))
+        self._pending = None
+
+
 class _Seq:
     __slots__ = ("x", "dt", "B", "C")
 

@@ -213,3 +213,55 @@ def quant_probe_state(seed: int, shape: Tuple[int, ...]) -> np.ndarray:
     first[4, N - 1] = -5e-20
     first[5] = rng.uniform(-448.0, 448.0, N).astype(np.float32)
     return s
+
+
+# ---- gated delta rule (GDN) verify workload ---------------------------------------------------------
+@dataclasses.dataclass(frozen=True)
+class GdnDims:
+    nheads: int      # value heads H
+    ngroups: int     # key/query heads G (head h uses group h // (H / G))
+    dk: int
+    dv: int
+    window: int      # refresh window L
+
+
+@dataclasses.dataclass
+class GdnTokens:
+    """q, k [T, G, dk] (unit L2 norm per group), v [T, H, dv], g [T, H] log-gates (< 0),
+    beta [T, H] in (0, 1).  q, k, v are bf16-representable when bf16."""
+    q: np.ndarray
+    k: np.ndarray
+    v: np.ndarray
+    g: np.ndarray
+    beta: np.ndarray
+
+
+GDN_VERIFY = dict(dims=GdnDims(32, 16, 128, 128, 16), batch=512, drafts=4, steps=32)
+
+
+def make_gdn_tokens(rng: np.random.Generator, T: int, d: GdnDims, bf16: bool = True) -> GdnTokens:
+    """Gated-delta-rule token inputs: q, k ~ N(0, 1) normalised to unit length per (token, group),
+    v ~ N(0, 1), log-gate g = -softplus(N(0, 1)) * 0.1 (decay per token in ~[0.87, 1)), beta =
+    sigmoid(N(0, 1)); q, k, v rounded to bf16 (RNE) when bf16."""
+    q = rng.standard_normal((T, d.ngroups, d.dk))
+    k = rng.standard_normal((T, d.ngroups, d.dk))
+    q /= np.linalg.norm(q, axis=-1, keepdims=True)
+    k /= np.linalg.norm(k, axis=-1, keepdims=True)
+    v = rng.standard_normal((T, d.nheads, d.dv))
+    g = -np.log1p(np.exp(rng.standard_normal((T, d.nheads)))) * 0.1
+    beta = 1.0 / (1.0 + np.exp(-rng.standard_normal((T, d.nheads))))
+    f32 = lambda a: a.astype(np.float32)
+    if bf16:
+        q, k, v = round_bf16(f32(q)), round_bf16(f32(k)), round_bf16(f32(v))
+    return GdnTokens(f32(q), f32(k), f32(v), f32(g), f32(beta))
+
+
+def gdn_verify_inputs(seed: int, batch: int, steps: int, dims: Optional[GdnDims] = None, drafts: int = 4):
+    """(anchor [batch, H, dv, dk] fp32 ~ N(0, 0.1), drafts GdnTokens with steps*batch*T rows (row
+    (k*batch + i)*T + j is draft j of sequence i at step k), accepted [steps, batch] ~ U{0..T})."""
+    d = dims if dims is not None else GDN_VERIFY["dims"]
+    rng = np.random.Generator(np.random.PCG64(seed))
+    anchor = (rng.standard_normal((batch, d.nheads, d.dv, d.dk)) * 0.1).astype(np.float32)
+    toks = make_gdn_tokens(rng, steps * batch * drafts, d)
+    accepted = rng.integers(0, drafts + 1, size=(steps, batch)).astype(np.int32)
+    return anchor, toks, accepted

@@ -597,3 +597,95 @@ def test_conv1d_identity_kernel_short_sequences_and_splits():
     yp, fp = oracle.causal_conv1d(np.concatenate([x, x[:5]]), w, b, cu_seqlens=[0, 9, 14])
     assert np.array_equal(yp[:9], y0) and np.array_equal(yp[9:], oracle.causal_conv1d(x[:5], w, b)[0])
     assert np.array_equal(fp[0], f0[0])
+
+
+# ---- gated delta rule (ReplaySSM notes, "Core equations": GDN residuals) ------------------------------
+def _gdn_case(seed, T=7, d=None, bf16=False):
+    d = d or synth.GdnDims(4, 2, 8, 6, 16)
+    rng = np.random.Generator(np.random.PCG64(seed))
+    toks = synth.make_gdn_tokens(rng, T, d, bf16)
+    S0 = rng.standard_normal((d.nheads, d.dv, d.dk))
+    return d, toks, S0
+
+
+def test_gdn_beta_zero_is_pure_decay():
+    d, t, S0 = _gdn_case(61)
+    o, S = oracle.gdn_recurrence(t.q, t.k, t.v, t.g, np.zeros_like(t.beta), S0)
+    hg = np.arange(d.nheads) // (d.nheads // d.ngroups)
+    gam = np.exp(np.cumsum(t.g.astype(np.float64), axis=0))              # [T, H]
+    for s in range(t.g.shape[0]):
+        want = gam[s][:, None] * np.einsum("hdn,hn->hd", S0, t.q[s][hg].astype(np.float64))
+        assert np.allclose(o[s], want, rtol=1e-12, atol=1e-12)
+    assert np.allclose(S, gam[-1][:, None, None] * S0, rtol=1e-12, atol=1e-12)
+
+
+def test_gdn_delta_rule_writes_the_value_at_its_key():
+    # no decay, beta = 1, unit keys: after token t the state maps k_t to v_t exactly
+    d, t, S0 = _gdn_case(62)
+    k = t.k.astype(np.float64)
+    k /= np.linalg.norm(k, axis=-1, keepdims=True)
+    hg = np.arange(d.nheads) // (d.nheads // d.ngroups)
+    for n in range(1, t.g.shape[0] + 1):
+        _, S = oracle.gdn_recurrence(t.q[:n], k[:n], t.v[:n], np.zeros_like(t.g[:n]), np.ones_like(t.beta[:n]), S0)
+        assert np.allclose(np.einsum("hdn,hn->hd", S, k[n - 1][hg]), t.v[n - 1], rtol=1e-12, atol=1e-12)
+
+
+def test_gdn_triangular_solve_form():
+    """The page's reassociation: with u from the triangular system
+    u_j + sum_{i<j} beta_j gamma_{i+1:j} (k_i . k_j) u_i = beta_j (v_j - gamma_j S_ckpt k_j),
+    S_h = gamma_h S_ckpt + sum_j gamma_{j+1:h} u_j k_j^T and o_s = S_s q_s in the same terms."""
+    d, t, S0 = _gdn_case(63, T=9)
+    o, Sfin = oracle.gdn_recurrence(t.q, t.k, t.v, t.g, t.beta, S0)
+    T = t.g.shape[0]
+    hg = np.arange(d.nheads) // (d.nheads // d.ngroups)
+    for h in range(d.nheads):
+        k = t.k[:, hg[h]].astype(np.float64); q = t.q[:, hg[h]].astype(np.float64)
+        v = t.v[:, h].astype(np.float64); beta = t.beta[:, h].astype(np.float64)
+        G = np.cumsum(t.g[:, h].astype(np.float64))
+        gam = lambda a, b: np.exp(G[b] - (G[a - 1] if a > 0 else 0.0))   # prod_{i=a}^{b} alpha_i
+        u = np.zeros((T, d.dv))
+        for j in range(T):
+            rhs = beta[j] * (v[j] - gam(0, j) * S0[h] @ k[j])
+            for i in range(j):
+                rhs -= beta[j] * gam(i + 1, j) * (k[i] @ k[j]) * u[i]
+            u[j] = rhs
+        S = gam(0, T - 1) * S0[h] + sum(gam(j + 1, T - 1) * np.outer(u[j], k[j]) if j + 1 <= T - 1
+                                       else np.outer(u[j], k[j]) for j in range(T))
+        assert np.allclose(S, Sfin[h], rtol=1e-11, atol=1e-11)
+        for s in range(T):
+            os_ = gam(0, s) * S0[h] @ q[s] + sum((gam(j + 1, s) if j < s else 1.0) * (k[j] @ q[s]) * u[j]
+                                                 for j in range(s + 1))
+            assert np.allclose(os_, o[s, h], rtol=1e-11, atol=1e-11)
+
+
+def test_gdn_protocol_pins():
+    """Zero acceptance keeps the anchor; the committed stream equals the plain recurrence from the
+    anchor; the anchor does not depend on the read precision."""
+    d = synth.GdnDims(4, 2, 8, 6, 5)
+    rng = np.random.Generator(np.random.PCG64(64))
+    S, T, K = 3, 3, 8
+    anchor = rng.standard_normal((S, d.nheads, d.dv, d.dk))
+    drafts = [[tuple(getattr(synth.make_gdn_tokens(rng, T, d, False), f) for f in ("q", "k", "v", "g", "beta"))
+               for _ in range(S)] for _ in range(K)]
+    acc = rng.integers(0, T + 1, size=(K, S))
+    m0 = oracle.GdnReplayModel(anchor, d.window)
+    for k in range(K):
+        m0.verify(drafts[k]); m0.commit([0] * S)
+    assert np.array_equal(m0.anchor, anchor) and m0.flushes == 0
+    m1 = oracle.GdnReplayModel(anchor, d.window)
+    m2 = oracle.GdnReplayModel(anchor, d.window, read_cast=lambda a: np.asarray(a, dtype=np.float64))
+    stream = [[] for _ in range(S)]
+    for k in range(K):
+        y1 = m1.verify(drafts[k]); m1.commit(acc[k])
+        y2 = m2.verify(drafts[k]); m2.commit(acc[k])
+        for i in range(S):
+            stream[i] += [tuple(f[j] for f in drafts[k][i]) for j in range(acc[k, i])]
+    assert m1.flushes > 0 and np.array_equal(m1.anchor, m2.anchor) and not np.array_equal(y1, y2)
+    for i in range(S):
+        recs = tuple(np.stack([r[f] for r in stream[i]]) for f in range(5))
+        _, want = oracle.gdn_recurrence(*recs, anchor[i])
+        got = m2.anchor[i]
+        rest = m2.committed[i]
+        if rest:
+            _, got = oracle.gdn_recurrence(*(np.stack([r[f] for r in rest]) for f in range(5)), got)
+        assert np.allclose(got, want, rtol=1e-12, atol=1e-12)
