@@ -36,7 +36,7 @@ EXPORTS = (
     "ers_status_str", "ers_version", "ers_ssd_scan_fwd_workspace_size", "ers_ssd_scan_fwd",
     "ers_chunked_prefill_workspace_size", "ers_chunked_prefill", "ers_replay_decode", "ers_refresh",
     "ers_spec_verify", "ers_commit", "ers_ssu_update", "ers_ssd_scan_fwd_static", "ers_conv1d_fwd",
-    "ers_conv1d_update",
+    "ers_conv1d_update", "ers_gdn_verify", "ers_gdn_commit", "ers_gdn_refresh",
 )
 
 
@@ -49,6 +49,17 @@ class ErsError(RuntimeError):
 class Dims(ctypes.Structure):
     _fields_ = [("nheads", ctypes.c_int32), ("ngroups", ctypes.c_int32), ("headdim", ctypes.c_int32),
                 ("dstate", ctypes.c_int32), ("chunk", ctypes.c_int32), ("io_dtype", ctypes.c_int32)]
+
+
+class GdnDims(ctypes.Structure):
+    _fields_ = [("nheads", ctypes.c_int32), ("ngroups", ctypes.c_int32), ("dk", ctypes.c_int32),
+                ("dv", ctypes.c_int32), ("window", ctypes.c_int32), ("io_dtype", ctypes.c_int32)]
+
+
+class GdnCache(ctypes.Structure):
+    _fields_ = [("anchor", ctypes.c_void_p), ("read_copy", ctypes.c_void_p), ("buf_k", ctypes.c_void_p),
+                ("buf_v", ctypes.c_void_p), ("buf_g", ctypes.c_void_p), ("buf_beta", ctypes.c_void_p),
+                ("buf_u", ctypes.c_void_p), ("pos", ctypes.c_void_p), ("nslots", ctypes.c_int32)]
 
 
 class ConvDims(ctypes.Structure):
@@ -101,6 +112,10 @@ _SIGS = {
     "ers_conv1d_fwd": ([ctypes.POINTER(ConvDims), _I32, _I64, _I32, _P, _P, _P, _P, _P, _I32, _P, _I32, _P, _P, _P],
                        _I32),
     "ers_conv1d_update": ([ctypes.POINTER(ConvDims), _I32, _P, _P, _P, _P, _I32, _P, _P, _P, _P], _I32),
+    "ers_gdn_verify": ([ctypes.POINTER(GdnDims), ctypes.POINTER(GdnCache), _I32, _P, _I32, _P, _P, _P, _P, _P,
+                        _U32, _P, _P, _P], _I32),
+    "ers_gdn_commit": ([ctypes.POINTER(GdnDims), ctypes.POINTER(GdnCache), _I32, _P, _P, _I32, _U32, _P, _P], _I32),
+    "ers_gdn_refresh": ([ctypes.POINTER(GdnDims), ctypes.POINTER(GdnCache), _I32, _P, _I32, _P, _P], _I32),
 }
 
 

@@ -416,6 +416,50 @@ ers_status ers_ssu_update(const ers_dims* dims, const ers_params* prm, float* st
 }
 
 namespace {
+ers_status check_gdn(const ers_gdn_dims* d, const ers_gdn_cache* c, int32_t nseq, const int32_t* slot, int32_t T) {
+  if (d == nullptr || c == nullptr) return ERS_EINVAL;
+  if (d->io_dtype != ERS_DTYPE_F32 && d->io_dtype != ERS_DTYPE_BF16) return ERS_EDTYPE;
+  if (d->nheads <= 0 || d->ngroups <= 0 || d->nheads % d->ngroups != 0) return ERS_ESHAPE;
+  if (!ers::gdn_supported(d->dk, d->dv, d->window, T)) return ERS_ESHAPE;
+  if (nseq < 0 || c->nslots < 0) return ERS_EINVAL;
+  if (slot == nullptr && nseq > c->nslots) return ERS_EINVAL;
+  ERS_TRY(check_ptr(c->anchor, true));
+  ERS_TRY(check_ptr(c->read_copy, true));
+  ERS_TRY(check_ptr(c->buf_k, true));
+  ERS_TRY(check_ptr(c->buf_v, true));
+  ERS_TRY(check_ptr(c->buf_g, true));
+  ERS_TRY(check_ptr(c->buf_beta, true));
+  ERS_TRY(check_ptr(c->buf_u, true));
+  ERS_TRY(check_ptr(c->pos, true));
+  ERS_TRY(check_ptr(slot, false));
+  return ERS_OK;
+}
+
+ers::GdnArgs gdn_args(const ers_gdn_dims* d, const ers_gdn_cache* c, int32_t nseq, const int32_t* slot, int32_t T,
+                      uint32_t flags, int32_t* st) {
+  ers::GdnArgs a;
+  memset(&a, 0, sizeof(a));
+  a.H = d->nheads;
+  a.G = d->ngroups;
+  a.L = d->window;
+  a.io = d->io_dtype;
+  a.T = T;
+  a.nseq = nseq;
+  a.nslots = c->nslots;
+  a.flags = flags;
+  a.slot = slot;
+  a.anchor = c->anchor;
+  a.copy = c->read_copy;
+  a.bk = c->buf_k;
+  a.bv = c->buf_v;
+  a.bg = c->buf_g;
+  a.bbeta = c->buf_beta;
+  a.bu = c->buf_u;
+  a.pos = c->pos;
+  a.status = st;
+  return a;
+}
+
 ers_status check_conv(const ers_conv_dims* d) {
   if (d == nullptr) return ERS_EINVAL;
   if (d->io_dtype != ERS_DTYPE_F32 && d->io_dtype != ERS_DTYPE_BF16) return ERS_EDTYPE;
@@ -434,6 +478,50 @@ ers::ConvLaunch conv_launch(const ers_conv_dims* d) {
   return l;
 }
 }  // namespace
+
+ers_status ers_gdn_verify(const ers_gdn_dims* dims, const ers_gdn_cache* cache, int32_t nseq, const int32_t* slot,
+                          int32_t T, const void* q, const void* k, const void* v, const float* g, const float* beta,
+                          uint32_t flags, void* o, ers_stream_t stream, int32_t* dev_status) {
+  if (T < 1) return ERS_EINVAL;
+  ERS_TRY(check_gdn(dims, cache, nseq, slot, T));
+  if (T > dims->window) return ERS_EINVAL;   // the drafts must fit the buffer after a flush
+  if ((flags & ~ERS_FLAG_AUTO_FLUSH) != 0) return ERS_EINVAL;
+  if (nseq == 0) return ERS_OK;
+  ERS_TRY(check_ptr(q, true));
+  ERS_TRY(check_ptr(k, true));
+  ERS_TRY(check_ptr(v, true));
+  ERS_TRY(check_ptr(g, true));
+  ERS_TRY(check_ptr(beta, true));
+  ERS_TRY(check_ptr(o, true));
+  ERS_TRY(check_ptr(dev_status, false));
+  ers::GdnArgs a = gdn_args(dims, cache, nseq, slot, T, flags, dev_status);
+  a.q = q; a.k = k; a.v = v; a.g = g; a.beta = beta; a.o = o;
+  return finish(ers::gdn_launch(a, 0, nullptr, (cudaStream_t)stream));
+}
+
+ers_status ers_gdn_commit(const ers_gdn_dims* dims, const ers_gdn_cache* cache, int32_t nseq, const int32_t* slot,
+                          const int32_t* accepted, int32_t T, uint32_t flags, ers_stream_t stream,
+                          int32_t* dev_status) {
+  if (T < 1) return ERS_EINVAL;
+  ERS_TRY(check_gdn(dims, cache, nseq, slot, T));
+  if (T > dims->window) return ERS_EINVAL;
+  if ((flags & ~ERS_FLAG_AUTO_FLUSH) != 0) return ERS_EINVAL;
+  if (nseq == 0) return ERS_OK;
+  ERS_TRY(check_ptr(accepted, true));
+  ERS_TRY(check_ptr(dev_status, false));
+  ers::GdnArgs a = gdn_args(dims, cache, nseq, slot, T, flags, dev_status);
+  return finish(ers::gdn_launch(a, 2, accepted, (cudaStream_t)stream));
+}
+
+ers_status ers_gdn_refresh(const ers_gdn_dims* dims, const ers_gdn_cache* cache, int32_t nseq, const int32_t* slot,
+                           int32_t drafts_T, ers_stream_t stream, int32_t* dev_status) {
+  if (drafts_T < 0) return ERS_EINVAL;
+  ERS_TRY(check_gdn(dims, cache, nseq, slot, 0));
+  if (nseq == 0) return ERS_OK;
+  ERS_TRY(check_ptr(dev_status, false));
+  ers::GdnArgs a = gdn_args(dims, cache, nseq, slot, drafts_T, 0, dev_status);
+  return finish(ers::gdn_launch(a, 1, nullptr, (cudaStream_t)stream));
+}
 
 ers_status ers_conv1d_fwd(const ers_conv_dims* dims, int32_t nseq, int64_t ntokens, int32_t max_seqlen,
                           const int32_t* cu_seqlens, const void* x, const void* weight, const void* bias,

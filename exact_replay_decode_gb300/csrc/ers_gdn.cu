@@ -1,0 +1,396 @@
+// Output-only speculative verify, refresh and commit for a gated-delta-rule (GDN) layer (ReplaySSM
+// notes, "Core equations": the GDN residuals u_j solve the triangular system
+//     u_j + sum_{i<j} beta_j gamma_{i+1:j} (k_i . k_j) u_i = beta_j (v_j - gamma_j S_ckpt k_j),
+// the state after h committed records is S_h = gamma_h S_ckpt + sum_j gamma_{j+1:h} u_j k_j^T, and a
+// draft's output is o_s = S_{h+s} q_s written in the same terms; "Data protocol": an empty
+// committed history leaves the anchor unchanged and never runs an empty solve).
+//
+// Per (sequence, value head) the cache keeps an fp32 anchor S [dv, dk], a bf16 read copy cast from
+// it, and the committed records since the last refresh: k (per key group), v, the log-gate g and
+// beta, and the residual u_j that the verify that first saw the record computed from the read copy.
+// With those cached, a verify streams the read copy once, computing for each of its T drafts
+// S_read k_s and S_read q_s; the residuals and outputs then need only scalars per row.  A flush
+// (h + T > L) folds the committed records into the anchor: one pass over the anchor rows computes
+// S k_i, solves the residuals and folds them, row by row, and casts the read copy from the same
+// fp32 values.  Fixed orders everywhere: gates are summed from the checkpoint in row order
+// (Gc[t] = g_0 + ... + g_t), gamma_{a..b} = exp(Gc[b] - Gc[a-1]), dot products are Dot<128>, the
+// residual and output sums run in row order.  The same rows give the same bits whether they are
+// drafts of one verify or tokens of T = 1 verifies, and a refresh gives the bits of the flush that
+// a verify would run.
+#include <stdint.h>
+
+#include "ers_common.cuh"
+#include "ers_internal.h"
+#include "warp_heads.cuh"
+
+namespace ers {
+namespace {
+
+using namespace wh;
+
+constexpr int kGD = 128;                       // dk = dv
+constexpr int kGWarps = kThreads / 32;         // 8
+constexpr int kGRows = kGD / kGWarps;          // state rows per warp
+constexpr int kGL = 32;                        // max window L
+constexpr int kGT = 8;                         // max drafts T
+
+struct GdnSmem {
+  float k[kGL + kGT][kGD];   // committed rows 0..hc-1, drafts at kGL + s
+  float q[kGT][kGD];
+  float v[kGT][kGD];         // drafts' v
+  float vc[kGL][kGD];        // committed v (flush)
+  float u[kGL + kGT][kGD];   // residuals: committed (cached), drafts at kGL + s
+  float y[kGT][kGD];         // S_read k_s
+  float z[kGT][kGD];         // S_read q_s
+  float gc[kGL + kGT];       // cumulative log-gates of the output rows
+  float bt[kGL + kGT];       // beta of the output rows
+  float gf[kGL];             // cumulative log-gates of the committed rows (flush)
+  float bf[kGL];
+  float kkf[kGL][kGL];       // k_i . k_r, committed rows (flush)
+  float kk[kGL + kGT][kGT];  // k_row . k_draft
+  float kq[kGL + kGT][kGT];  // k_row . q_draft
+};
+
+template <typename T>
+__device__ __forceinline__ void load_vec(const T* __restrict__ p, float* dst) {
+  for (int e = threadIdx.x & 31; e < kGD; e += 32) dst[e] = to_f(p[e]);
+}
+
+// Warp-per-dot products of two smem vectors (Dot<128> order); lane 0 stores.
+__device__ __forceinline__ float sdot(const float* a, const float* b, int j) {
+  float qa[4], qb[4];
+  lds4(a + 4 * j, qa);
+  lds4(b + 4 * j, qb);
+  return Dot<kGD>::reduce(Dot<kGD>::partial(qa, qb));
+}
+
+// One pass over the anchor rows of warp w: for each row d, S_anchor k_i for the hc committed
+// records, their residuals (every lane computes the same scalars), the fold
+//     S'[d][n] = gamma_{1..hc} S[d][n] + sum_i gamma_{i+1..hc} u_i[d] k_i[n]   (fma chain in row order)
+// stored to the anchor and cast to the bf16 read copy; with drafts, their S' k_s and S' q_s from
+// the cast values go to y and z.
+__device__ __forceinline__ void gdn_fold_rows(GdnSmem& sm, float* __restrict__ S, __nv_bfloat16* __restrict__ R,
+                                              int hc, int ndraft, int w, int j) {
+  const float gall = expf(sm.gf[hc - 1]);
+  for (int rr = 0; rr < kGRows; ++rr) {
+    const int d = w * kGRows + rr;
+    float hq[4];
+    Quad<float>::unpack(*reinterpret_cast<const float4*>(S + (size_t)d * kGD + 4 * j), hq);
+    float u[kGL];
+#pragma unroll 1
+    for (int r = 0; r < hc; ++r) {
+      float kq4[4];
+      lds4(sm.k[r] + 4 * j, kq4);
+      const float y = Dot<kGD>::reduce(Dot<kGD>::partial(kq4, hq));
+      float acc = __fmul_rn(sm.bf[r], __fmaf_rn(-expf(sm.gf[r]), y, sm.vc[r][d]));
+      for (int i = 0; i < r; ++i) {
+        const float c = __fmul_rn(__fmul_rn(sm.bf[r], expf(__fsub_rn(sm.gf[r], sm.gf[i]))), sm.kkf[i][r]);
+        acc = __fmaf_rn(-c, u[i], acc);
+      }
+      u[r] = acc;
+    }
+    float nv[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) nv[e] = __fmul_rn(gall, hq[e]);
+#pragma unroll 1
+    for (int r = 0; r < hc; ++r) {
+      float kq4[4];
+      lds4(sm.k[r] + 4 * j, kq4);
+      const float wu = __fmul_rn(expf(__fsub_rn(sm.gf[hc - 1], sm.gf[r])), u[r]);
+#pragma unroll
+      for (int e = 0; e < 4; ++e) nv[e] = __fmaf_rn(wu, kq4[e], nv[e]);
+    }
+    *reinterpret_cast<float4*>(S + (size_t)d * kGD + 4 * j) = make_float4(nv[0], nv[1], nv[2], nv[3]);
+    const __nv_bfloat162 lo2 = __floats2bfloat162_rn(nv[0], nv[1]), hi2 = __floats2bfloat162_rn(nv[2], nv[3]);
+    uint2 pk;
+    pk.x = *reinterpret_cast<const uint32_t*>(&lo2);
+    pk.y = *reinterpret_cast<const uint32_t*>(&hi2);
+    *reinterpret_cast<uint2*>(R + (size_t)d * kGD + 4 * j) = pk;
+    float rv[4];
+    Quad<__nv_bfloat16>::unpack(pk, rv);
+    for (int s = 0; s < ndraft; ++s) {
+      float a[4], b[4];
+      lds4(sm.k[kGL + s] + 4 * j, a);
+      lds4(sm.q[s] + 4 * j, b);
+      const float ys = Dot<kGD>::reduce(Dot<kGD>::partial(a, rv));
+      const float zs = Dot<kGD>::reduce(Dot<kGD>::partial(b, rv));
+      if (j == 0) {
+        sm.y[s][d] = ys;
+        sm.z[s][d] = zs;
+      }
+    }
+  }
+}
+
+// Committed records' key rows (the group's; shared by its heads) and per-head rows.
+template <typename T>
+__device__ __forceinline__ void load_committed_k(GdnSmem& sm, const GdnArgs& a, int slot, int g, int hc) {
+  const int w = threadIdx.x >> 5;
+  for (int r = w; r < hc; r += kGWarps)
+    load_vec<T>((const T*)a.bk + (((size_t)slot * a.L + r) * a.G + g) * kGD, sm.k[r]);
+}
+
+template <typename T>
+__device__ __forceinline__ void load_committed_head(GdnSmem& sm, const GdnArgs& a, int slot, int h, int hc, bool flush) {
+  const int w = threadIdx.x >> 5;
+  for (int r = w; r < hc; r += kGWarps) {
+    const size_t row = (size_t)slot * a.L + r;
+    if (flush)
+      load_vec<T>((const T*)a.bv + (row * a.H + h) * kGD, sm.vc[r]);
+    else
+      load_vec<float>(a.bu + (row * a.H + h) * kGD, sm.u[r]);
+  }
+}
+
+// Gates of the committed records summed in row order, and their betas (thread 0).
+__device__ __forceinline__ void flush_scalars(GdnSmem& sm, const GdnArgs& a, int slot, int h, int hc) {
+  if (threadIdx.x == 0) {
+    float acc = 0.f;
+    for (int r = 0; r < hc; ++r) {
+      const size_t row = (size_t)slot * a.L + r;
+      acc = __fadd_rn(acc, a.bg[row * a.H + h]);
+      sm.gf[r] = acc;
+      sm.bf[r] = a.bbeta[row * a.H + h];
+    }
+  }
+}
+
+__device__ __forceinline__ void flush_gram(GdnSmem& sm, int hc) {
+  const int w = threadIdx.x >> 5, j = threadIdx.x & 31;
+  for (int p = w; p < hc * hc; p += kGWarps) {
+    const int i = p / hc, r = p % hc;
+    if (i < r) {
+      const float v = sdot(sm.k[i], sm.k[r], j);
+      if (j == 0) sm.kkf[i][r] = v;
+    }
+  }
+}
+
+__device__ __forceinline__ bool gdn_slot(const GdnArgs& a, int i, int* slot) {
+  const int s = a.slot != nullptr ? a.slot[i] : i;
+  if (s < 0 || s >= a.nslots) {
+    if (threadIdx.x == 0) report(a.status, ERS_ESLOT);
+    return false;
+  }
+  *slot = s;
+  return true;
+}
+
+// One CTA per (sequence, key group); its value heads run one after another, so the group's key rows
+// are read once and the drafts' key rows are written after every head of the group has read the
+// committed ones (a flush reuses buffer rows from 0).
+template <typename T>
+__global__ void __launch_bounds__(kThreads, 1) k_gdn_verify(GdnArgs a) {
+  extern __shared__ __align__(16) unsigned char gsm_raw[];
+  GdnSmem& sm = *reinterpret_cast<GdnSmem*>(gsm_raw);
+  const int g = blockIdx.x, i = blockIdx.y, tid = threadIdx.x, w = tid >> 5, j = tid & 31;
+  const int hpg = a.H / a.G;
+  const int Td = a.T;
+  int slot;
+  if (!gdn_slot(a, i, &slot)) return;
+  const int hc = a.pos[slot];
+  if (hc < 0 || hc > a.L) {
+    if (tid == 0) report(a.status, ERS_EALIGN);
+    return;
+  }
+  const bool flush = hc + Td > a.L;
+  if (flush && !(a.flags & ERS_FLAG_AUTO_FLUSH)) {
+    if (tid == 0) report(a.status, ERS_EOVERFLOW);
+    return;
+  }
+  const int h0 = flush ? 0 : hc;   // committed rows that precede the drafts
+  load_committed_k<T>(sm, a, slot, g, hc);
+  for (int s = w; s < Td; s += kGWarps) {
+    const size_t tok = (size_t)i * Td + s;
+    load_vec<T>((const T*)a.k + (tok * a.G + g) * kGD, sm.k[kGL + s]);
+    load_vec<T>((const T*)a.q + (tok * a.G + g) * kGD, sm.q[s]);
+  }
+  __syncthreads();
+  if (flush && hc > 0) flush_gram(sm, hc);
+  // k_row . k_s (rows before draft s) and k_row . q_s (rows up to draft s), row r of the output rows
+  for (int p = w; p < (h0 + Td) * Td; p += kGWarps) {
+    const int r = p / Td, s = p % Td;
+    const float* kr = r < h0 ? sm.k[r] : sm.k[kGL + r - h0];
+    if (r <= h0 + s) {
+      const float vq = sdot(kr, sm.q[s], j);
+      const float vk = r < h0 + s ? sdot(kr, sm.k[kGL + s], j) : 0.f;
+      if (j == 0) {
+        sm.kq[r][s] = vq;
+        sm.kk[r][s] = vk;
+      }
+    }
+  }
+  for (int hh = 0; hh < hpg; ++hh) {
+    const int h = g * hpg + hh;
+    const size_t soff = ((size_t)slot * a.H + h) * kGD * kGD;
+    load_committed_head<T>(sm, a, slot, h, hc, flush);
+    for (int s = w; s < Td; s += kGWarps)
+      load_vec<T>((const T*)a.v + (((size_t)i * Td + s) * a.H + h) * kGD, sm.v[s]);
+    if (flush && hc > 0) flush_scalars(sm, a, slot, h, hc);
+    if (tid == 32) {   // output rows: committed rows 0..h0-1, then the drafts; gates in row order
+      float acc = 0.f;
+      for (int r = 0; r < h0 + Td; ++r) {
+        const size_t br = ((size_t)slot * a.L + r) * a.H + h, tr = ((size_t)i * Td + (r - h0)) * a.H + h;
+        acc = __fadd_rn(acc, r < h0 ? a.bg[br] : a.g[tr]);
+        sm.gc[r] = acc;
+        sm.bt[r] = r < h0 ? a.bbeta[br] : a.beta[tr];
+      }
+    }
+    __syncthreads();
+    if (flush && hc > 0) {
+      gdn_fold_rows(sm, a.anchor + soff, (__nv_bfloat16*)a.copy + soff, hc, Td, w, j);
+    } else {
+      // stream the read copy: S_read k_s and S_read q_s for every draft
+      const __nv_bfloat16* R = (const __nv_bfloat16*)a.copy + soff;
+      for (int rr = 0; rr < kGRows; ++rr) {
+        const int d = w * kGRows + rr;
+        float rv[4];
+        Quad<__nv_bfloat16>::unpack(Quad<__nv_bfloat16>::ld_stream(R + (size_t)d * kGD + 4 * j), rv);
+        for (int s = 0; s < Td; ++s) {
+          float ka[4], qb[4];
+          lds4(sm.k[kGL + s] + 4 * j, ka);
+          lds4(sm.q[s] + 4 * j, qb);
+          const float ys = Dot<kGD>::reduce(Dot<kGD>::partial(ka, rv));
+          const float zs = Dot<kGD>::reduce(Dot<kGD>::partial(qb, rv));
+          if (j == 0) {
+            sm.y[s][d] = ys;
+            sm.z[s][d] = zs;
+          }
+        }
+      }
+    }
+    __syncthreads();
+    // residuals and outputs, one state row d per thread, drafts in order
+    if (tid < kGD) {
+      const int d = tid;
+      for (int s = 0; s < Td; ++s) {
+        const int t = h0 + s;
+        const float gam = expf(sm.gc[t]);
+        float acc = __fmul_rn(sm.bt[t], __fmaf_rn(-gam, sm.y[s][d], sm.v[s][d]));
+        for (int r = 0; r < t; ++r) {
+          const float ur = r < h0 ? sm.u[r][d] : sm.u[kGL + r - h0][d];
+          const float c = __fmul_rn(__fmul_rn(sm.bt[t], expf(__fsub_rn(sm.gc[t], sm.gc[r]))), sm.kk[r][s]);
+          acc = __fmaf_rn(-c, ur, acc);
+        }
+        sm.u[kGL + s][d] = acc;
+        float out = __fmul_rn(gam, sm.z[s][d]);
+        for (int r = 0; r <= t; ++r) {
+          const float ur = r < h0 ? sm.u[r][d] : sm.u[kGL + r - h0][d];
+          const float wq = __fmul_rn(expf(__fsub_rn(sm.gc[t], sm.gc[r])), sm.kq[r][s]);
+          out = __fmaf_rn(wq, ur, out);
+        }
+        ((T*)a.o)[(((size_t)i * Td + s) * a.H + h) * kGD + d] = from_f<T>(out);
+      }
+    }
+    __syncthreads();
+    // this head's draft rows (v, residual, gate, beta) go to buffer rows h0..h0+T-1
+    for (int s = w; s < Td; s += kGWarps) {
+      const size_t row = (size_t)slot * a.L + h0 + s, tok = (size_t)i * Td + s;
+      for (int e = j; e < kGD; e += 32) {
+        ((T*)a.bv)[(row * a.H + h) * kGD + e] = ((const T*)a.v)[(tok * a.H + h) * kGD + e];
+        a.bu[(row * a.H + h) * kGD + e] = sm.u[kGL + s][e];
+      }
+      if (j == 0) {
+        a.bg[row * a.H + h] = a.g[tok * a.H + h];
+        a.bbeta[row * a.H + h] = a.beta[tok * a.H + h];
+      }
+    }
+    __syncthreads();
+  }
+  // the group's draft key rows, after every head has read the committed ones
+  for (int s = w; s < Td; s += kGWarps) {
+    const size_t row = (size_t)slot * a.L + h0 + s, tok = (size_t)i * Td + s;
+    for (int e = j; e < kGD; e += 32) ((T*)a.bk)[(row * a.G + g) * kGD + e] = ((const T*)a.k)[(tok * a.G + g) * kGD + e];
+  }
+}
+
+// Standalone refresh: slots with h + T > L (T = drafts_T) and h > 0 fold their records exactly as a
+// verify's flush does.  Positions are reset by k_gdn_setpos afterwards.
+template <typename T>
+__global__ void __launch_bounds__(kThreads, 1) k_gdn_refresh(GdnArgs a) {
+  extern __shared__ __align__(16) unsigned char gsm_raw[];
+  GdnSmem& sm = *reinterpret_cast<GdnSmem*>(gsm_raw);
+  const int g = blockIdx.x, i = blockIdx.y, w = threadIdx.x >> 5, j = threadIdx.x & 31;
+  const int hpg = a.H / a.G;
+  int slot;
+  if (!gdn_slot(a, i, &slot)) return;
+  const int hc = a.pos[slot];
+  if (hc < 0 || hc > a.L) {
+    if (threadIdx.x == 0) report(a.status, ERS_EALIGN);
+    return;
+  }
+  if (!(hc + a.T > a.L) || hc == 0) return;
+  load_committed_k<T>(sm, a, slot, g, hc);
+  __syncthreads();
+  flush_gram(sm, hc);
+  for (int hh = 0; hh < hpg; ++hh) {
+    const int h = g * hpg + hh;
+    load_committed_head<T>(sm, a, slot, h, hc, true);
+    flush_scalars(sm, a, slot, h, hc);
+    __syncthreads();
+    const size_t soff = ((size_t)slot * a.H + h) * kGD * kGD;
+    gdn_fold_rows(sm, a.anchor + soff, (__nv_bfloat16*)a.copy + soff, hc, 0, w, j);
+    __syncthreads();
+  }
+}
+
+__global__ void k_gdn_setpos(GdnArgs a) {
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= a.nseq) return;
+  const int s = a.slot != nullptr ? a.slot[i] : i;
+  if (s < 0 || s >= a.nslots) return;
+  const int hc = a.pos[s];
+  if (hc >= 0 && hc <= a.L && hc + a.T > a.L) a.pos[s] = 0;
+}
+
+// Commit: h = (flushed ? 0 : h) + accepted, flushed = AUTO_FLUSH && h + T > L.
+__global__ void k_gdn_commit(GdnArgs a, const int32_t* accepted) {
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= a.nseq) return;
+  const int s = a.slot != nullptr ? a.slot[i] : i;
+  if (s < 0 || s >= a.nslots) {
+    report(a.status, ERS_ESLOT);
+    return;
+  }
+  const int acc = accepted[i];
+  if (acc < 0 || acc > a.T) {
+    report(a.status, ERS_ECOMMIT);
+    return;
+  }
+  const int hc = a.pos[s];
+  const bool flushed = (a.flags & ERS_FLAG_AUTO_FLUSH) && hc + a.T > a.L;
+  a.pos[s] = (flushed ? 0 : hc) + acc;
+}
+
+}  // namespace
+
+bool gdn_supported(int dk, int dv, int L, int T) {
+  return dk == kGD && dv == kGD && L >= 1 && L <= kGL && T >= 0 && T <= kGT;
+}
+
+cudaError_t gdn_launch(const GdnArgs& a, int kind, const int32_t* accepted, cudaStream_t s) {
+  const size_t sm = sizeof(GdnSmem);
+  cudaError_t e;
+  if (kind == 2) {
+    k_gdn_commit<<<(a.nseq + 255) / 256, 256, 0, s>>>(a, accepted);
+    return cudaGetLastError();
+  }
+  const dim3 grid(a.G, a.nseq);
+  if (a.io == ERS_DTYPE_BF16) {
+    auto kv = kind == 0 ? k_gdn_verify<__nv_bfloat16> : k_gdn_refresh<__nv_bfloat16>;
+    if ((e = prep(kv, sm)) != cudaSuccess) return e;
+    kv<<<grid, kThreads, sm, s>>>(a);
+  } else {
+    auto kv = kind == 0 ? k_gdn_verify<float> : k_gdn_refresh<float>;
+    if ((e = prep(kv, sm)) != cudaSuccess) return e;
+    kv<<<grid, kThreads, sm, s>>>(a);
+  }
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  if (kind == 1) {
+    k_gdn_setpos<<<(a.nseq + 255) / 256, 256, 0, s>>>(a);
+    return cudaGetLastError();
+  }
+  return cudaSuccess;
+}
+
+}  // namespace ers

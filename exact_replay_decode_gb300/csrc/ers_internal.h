@@ -107,6 +107,30 @@ bool ssu_supported(int P, int N);
 
 inline size_t align256(size_t v) { return (v + 255) & ~size_t(255); }
 
+// gated delta rule (GDN) verify / refresh / commit, ers_gdn.cu
+struct GdnArgs {
+  int H, G, L, io, T, nseq, nslots;
+  uint32_t flags;
+  const int32_t* slot;
+  float* anchor;   // [nslots, H, dv, dk]
+  void* copy;      // bf16, same shape
+  void* bk;        // [nslots, L, G, dk] io
+  void* bv;        // [nslots, L, H, dv] io
+  float* bg;       // [nslots, L, H]
+  float* bbeta;    // [nslots, L, H]
+  float* bu;       // [nslots, L, H, dv] fp32 residuals
+  int32_t* pos;
+  const void* q;
+  const void* k;
+  const void* v;
+  const float* g;
+  const float* beta;
+  void* o;
+  int32_t* status;
+};
+bool gdn_supported(int dk, int dv, int L, int T);
+cudaError_t gdn_launch(const GdnArgs& a, int kind, const int32_t* accepted, cudaStream_t s);   // 0 verify, 1 refresh, 2 commit
+
 // causal depthwise conv1d with a conv state, ers_conv.cu
 struct ConvLaunch {
   int C, W, io, silu, nseq, nslots, read_state, update, max_seqlen;

@@ -469,3 +469,76 @@ def conv1d_update(x: torch.Tensor, weight: torch.Tensor, bias: Optional[torch.Te
                                         _ptr(st.t) if st else None)
     _finish(code, "ers_conv1d_update", st, check)
     return y
+
+
+# ------------------------------------------------------------------------------------------------
+class GdnCache:
+    """Per-slot ReplaySSM state of a gated-delta-rule layer: fp32 anchor [S,H,dv,dk], bf16 read copy,
+    the committed records since the last refresh (k [S,L,G,dk], v [S,L,H,dv] in the io dtype; g, beta
+    [S,L,H] and residuals u [S,L,H,dv] in fp32) and the committed count pos [S]."""
+
+    def __init__(self, nslots: int, nheads: int, ngroups: int, dk: int = 128, dv: int = 128, window: int = 16,
+                 io_dtype: torch.dtype = torch.bfloat16, device="cuda"):
+        self.nslots, self.H, self.G, self.dk, self.dv, self.L = nslots, nheads, ngroups, dk, dv, window
+        self.io = io_dtype
+        z = dict(device=device)
+        self.anchor = torch.zeros(nslots, nheads, dv, dk, dtype=torch.float32, **z)
+        self.read_copy = torch.zeros(nslots, nheads, dv, dk, dtype=torch.bfloat16, **z)
+        self.buf_k = torch.zeros(nslots, window, ngroups, dk, dtype=io_dtype, **z)
+        self.buf_v = torch.zeros(nslots, window, nheads, dv, dtype=io_dtype, **z)
+        self.buf_g = torch.zeros(nslots, window, nheads, dtype=torch.float32, **z)
+        self.buf_beta = torch.zeros(nslots, window, nheads, dtype=torch.float32, **z)
+        self.buf_u = torch.zeros(nslots, window, nheads, dv, dtype=torch.float32, **z)
+        self.pos = torch.zeros(nslots, dtype=torch.int32, **z)
+
+    @property
+    def dims(self) -> _abi.GdnDims:
+        if self.io not in _IO:
+            raise TypeError(f"io dtype {self.io} not supported (bf16 or fp32)")
+        return _abi.GdnDims(self.H, self.G, self.dk, self.dv, self.L, _IO[self.io])
+
+    def _c(self) -> _abi.GdnCache:
+        return _abi.GdnCache(self.anchor.data_ptr(), self.read_copy.data_ptr(), self.buf_k.data_ptr(),
+                             self.buf_v.data_ptr(), self.buf_g.data_ptr(), self.buf_beta.data_ptr(),
+                             self.buf_u.data_ptr(), self.pos.data_ptr(), self.nslots)
+
+
+def gdn_verify(cache: GdnCache, q, k, v, g, beta, slot: Optional[torch.Tensor] = None, auto_flush: bool = True,
+               status: Optional[Status] = None, check: bool = True, stream=None,
+               out: Optional[torch.Tensor] = None) -> torch.Tensor:
+    """Output-only verify of T drafts per sequence for a GDN layer (ers_gdn_verify).  q, k [S,T,G,dk],
+    v [S,T,H,dv], g, beta [S,T,H]; returns o [S,T,H,dv]."""
+    S, T = q.shape[0], q.shape[1]
+    _need(q, cache.io, "q", (S, T, cache.G, cache.dk)); _need(k, cache.io, "k", (S, T, cache.G, cache.dk))
+    _need(v, cache.io, "v", (S, T, cache.H, cache.dv))
+    _need(g, torch.float32, "g", (S, T, cache.H)); _need(beta, torch.float32, "beta", (S, T, cache.H))
+    o = torch.empty_like(v) if out is None else out
+    st = status if status is not None else (Status(q.device) if check else None)
+    code = _abi.lib().ers_gdn_verify(ctypes.byref(cache.dims), ctypes.byref(cache._c()), S, _slot_arg(slot, S), T,
+                                     q.data_ptr(), k.data_ptr(), v.data_ptr(), g.data_ptr(), beta.data_ptr(),
+                                     _abi.FLAG_AUTO_FLUSH if auto_flush else 0, o.data_ptr(), _stream(stream),
+                                     _ptr(st.t) if st else None)
+    _finish(code, "ers_gdn_verify", st, check)
+    return o
+
+
+def gdn_commit(cache: GdnCache, accepted: torch.Tensor, T: int, slot: Optional[torch.Tensor] = None,
+               auto_flush: bool = True, status: Optional[Status] = None, check: bool = True, stream=None) -> None:
+    """Advance the committed count by the accepted drafts (ers_gdn_commit)."""
+    S = accepted.numel()
+    _need(accepted, torch.int32, "accepted", (S,))
+    st = status if status is not None else (Status(accepted.device) if check else None)
+    code = _abi.lib().ers_gdn_commit(ctypes.byref(cache.dims), ctypes.byref(cache._c()), S, _slot_arg(slot, S),
+                                     accepted.data_ptr(), int(T), _abi.FLAG_AUTO_FLUSH if auto_flush else 0,
+                                     _stream(stream), _ptr(st.t) if st else None)
+    _finish(code, "ers_gdn_commit", st, check)
+
+
+def gdn_refresh(cache: GdnCache, drafts_T: int, nseq: Optional[int] = None, slot: Optional[torch.Tensor] = None,
+                status: Optional[Status] = None, check: bool = True, stream=None) -> None:
+    """Fold the committed records of slots with h + drafts_T > L into their anchors (ers_gdn_refresh)."""
+    S = cache.nslots if nseq is None else nseq
+    st = status if status is not None else (Status(cache.anchor.device) if check else None)
+    code = _abi.lib().ers_gdn_refresh(ctypes.byref(cache.dims), ctypes.byref(cache._c()), S, _slot_arg(slot, S),
+                                      int(drafts_T), _stream(stream), _ptr(st.t) if st else None)
+    _finish(code, "ers_gdn_refresh", st, check)

@@ -301,6 +301,62 @@ ERS_API ers_status ers_ssu_update(const ers_dims* dims, const ers_params* prm, f
                           const void* C, void* y, ers_stream_t stream, int32_t* dev_status);
 
 /* ---------------------------------------------------------------------------------------------
+ * Gated delta rule (GDN) layer: output-only speculative verify, refresh and commit (ReplaySSM notes,
+ * "Core equations": GDN residuals solve u_j + sum_{i<j} beta_j gamma_{i+1:j} (k_i . k_j) u_i =
+ * beta_j (v_j - gamma_j S_ckpt k_j); "Data protocol": an empty history leaves the anchor unchanged).
+ * Per value head h (key group h / (H/G)), token t: a_t = exp(g_t), u_t = beta_t (v_t - a_t S k_t),
+ * S <- a_t S + u_t k_t^T, o_t = S q_t; S is [dv, dk] (maps keys to values).
+ *
+ *   dims: H, G (G divides H), dk = dv = 128, window L in [1, 32], io_dtype for q, k, v, o and the
+ *         k / v buffers.
+ *   cache: anchor [nslots, H, dv, dk] fp32; read_copy [nslots, H, dv, dk] bf16 (cast from the same
+ *         fp32 values at every refresh); buf_k [nslots, L, G, dk], buf_v [nslots, L, H, dv] (io);
+ *         buf_g, buf_beta [nslots, L, H] fp32; buf_u [nslots, L, H, dv] fp32 (each committed record's
+ *         residual as computed from the read copy by the verify that produced it); pos [nslots] =
+ *         committed records h (0 <= h <= L).
+ * ers_gdn_verify: T drafts per sequence (1 <= T <= min(8, L)): q, k [nseq, T, G, dk], v [nseq, T, H, dv] (io),
+ *   g, beta [nseq, T, H] fp32 (g = log of the gate, beta in (0, 1)); o [nseq, T, H, dv] (out).  With
+ *   ERS_FLAG_AUTO_FLUSH a slot with h + T > L first folds its h records into the anchor (h > 0) and
+ *   recasts the read copy; without it such a slot reports ERS_EOVERFLOW.  Outputs read the read copy;
+ *   drafts are written to buffer rows h.. (0.. after a flush); pos is not moved.
+ * ers_gdn_commit: h = (flushed ? 0 : h) + accepted[i], flushed = AUTO_FLUSH && h + T > L.
+ * ers_gdn_refresh: slots with h + T > L (T = drafts_T) fold their records (h > 0) and get h = 0.
+ * The same committed stream and refresh points give the same bits whether tokens arrive as drafts
+ * of one verify or as T = 1 verifies.  Device errors: ERS_EALIGN, ERS_EOVERFLOW, ERS_ECOMMIT, ERS_ESLOT. */
+typedef struct ers_gdn_dims {
+  int32_t nheads;
+  int32_t ngroups;
+  int32_t dk;
+  int32_t dv;
+  int32_t window;
+  int32_t io_dtype;
+} ers_gdn_dims;
+
+typedef struct ers_gdn_cache {
+  float* anchor;
+  void* read_copy;
+  void* buf_k;
+  void* buf_v;
+  float* buf_g;
+  float* buf_beta;
+  float* buf_u;
+  int32_t* pos;
+  int32_t nslots;
+} ers_gdn_cache;
+
+ERS_API ers_status ers_gdn_verify(const ers_gdn_dims* dims, const ers_gdn_cache* cache, int32_t nseq,
+                                  const int32_t* slot, int32_t T, const void* q, const void* k, const void* v,
+                                  const float* g, const float* beta, uint32_t flags, void* o, ers_stream_t stream,
+                                  int32_t* dev_status);
+
+ERS_API ers_status ers_gdn_commit(const ers_gdn_dims* dims, const ers_gdn_cache* cache, int32_t nseq,
+                                  const int32_t* slot, const int32_t* accepted, int32_t T, uint32_t flags,
+                                  ers_stream_t stream, int32_t* dev_status);
+
+ERS_API ers_status ers_gdn_refresh(const ers_gdn_dims* dims, const ers_gdn_cache* cache, int32_t nseq,
+                                   const int32_t* slot, int32_t drafts_T, ers_stream_t stream, int32_t* dev_status);
+
+/* ---------------------------------------------------------------------------------------------
  * Causal depthwise conv1d with a conv state: the step upstream of the SSM, whose prefill and
  * decode-update paths must give identical bits (exact-replay RFC, section 2 Evidence item 6; bf16
  * operands promoted to fp32 before accumulation).  Per channel c, with u the inputs preceded by

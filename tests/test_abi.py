@@ -208,3 +208,17 @@ def test_validation_of_paged_buffers(lib):
     assert dec(0, 8) == 1 and dec(4, 0) == 1                       # page geometry
     assert dec(5, 8) == 2                                          # page_rows must divide the chunk
     assert dec(4, 8, pages=MISALIGNED) == 4
+
+
+@needs_no_gpu
+def test_validation_of_gdn_calls(lib):
+    from exact_replay_decode_gb300 import _abi
+
+    def ver(dk=128, L=16, T=4, io=_abi.DTYPE_BF16, H=8, G=4, flags=4):
+        d = _abi.GdnDims(H, G, dk, 128, L, io)
+        c = _abi.GdnCache(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 4)
+        return lib.ers_gdn_verify(ctypes.byref(d), ctypes.byref(c), 4, None, T, FAKE, FAKE, FAKE, FAKE, FAKE, flags,
+                                  FAKE, None, None)
+
+    assert ver(dk=64) == 2 and ver(L=33) == 2 and ver(T=9) == 2 and ver(H=6, G=4) == 2   # ERS_ESHAPE
+    assert ver(io=5) == 3 and ver(T=0) == 1 and ver(L=2, T=3) == 1 and ver(flags=1) == 1
