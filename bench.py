@@ -585,6 +585,60 @@ def bench_conv(dev, hbm: float, reps: int = 50):
             "l2": "flushed before each call"}
 
 
+def bench_gdn_verify(dev, steps: int, hbm: float):
+    """Output-only verify of a gated-delta-rule layer: 512 sequences x 4 drafts, 32 value heads / 16
+    key groups, dk = dv = 128, window 16, bf16 io, 32 verify + commit steps.  Bytes from the run's own
+    pointers and flushes: per sequence-step the read copy (32 x 128 x 128 bf16), the drafts' q, k, v,
+    g, beta in and o out, the committed records' k and cached residuals (and g, beta) read, and the
+    drafts' k, v, residuals, g, beta written to the buffer; per flush the anchor read and written, the
+    copy written instead of read, and the records' k and v read."""
+    import torch
+    import exact_replay_decode_gb300 as ers
+    d = synth.GDN_VERIFY["dims"]
+    S, T = synth.GDN_VERIFY["batch"], synth.GDN_VERIFY["drafts"]
+    anchor, toks, acc = synth.gdn_verify_inputs(0, S, steps, d, T)
+    cache = ers.GdnCache(S, d.nheads, d.ngroups, d.dk, d.dv, d.window, torch.bfloat16)
+    cache.anchor.copy_(torch.from_numpy(anchor))
+    cache.read_copy.copy_(cache.anchor)
+    to = lambda a, dt: torch.from_numpy(a).to(dev).to(dt)
+    q = to(toks.q, torch.bfloat16).view(steps, S, T, d.ngroups, d.dk)
+    k = to(toks.k, torch.bfloat16).view(steps, S, T, d.ngroups, d.dk)
+    v = to(toks.v, torch.bfloat16).view(steps, S, T, d.nheads, d.dv)
+    g = to(toks.g, torch.float32).view(steps, S, T, d.nheads)
+    beta = to(toks.beta, torch.float32).view(steps, S, T, d.nheads)
+    acc_t = torch.from_numpy(acc).to(dev)
+    o = torch.empty(S, T, d.nheads, d.dv, dtype=torch.bfloat16, device=dev)
+    st = ers.Status(dev)
+    H, G, D = d.nheads, d.ngroups, d.dk
+    copy = H * D * D * 2
+    row_read = G * D * 2 + H * D * 4 + H * 8                 # committed k, residual u, g and beta
+    row_write = G * D * 2 + H * D * 2 + H * D * 4 + H * 8    # a draft's k, v, u, g, beta
+    io = T * (2 * G * D * 2 + H * D * 2 + H * 8) + T * H * D * 2
+    hs = np.zeros(S, dtype=np.int64)
+    total = 0
+    for kk in range(steps):
+        fl = hs + T > d.window
+        base = np.where(fl, 0, hs)
+        total += S * (copy + io + T * row_write) + int(base.sum()) * row_read
+        total += int(fl.sum()) * (2 * H * D * D * 4) + int(hs[fl].sum()) * (G * D * 2 + H * D * 2 + H * 8)
+        hs = base + acc[kk]
+    torch.cuda.synchronize()
+    s = torch.cuda.current_stream()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(s)
+    for kk in range(steps):
+        ers.gdn_verify(cache, q[kk], k[kk], v[kk], g[kk], beta[kk], status=st, check=False, out=o)
+        ers.gdn_commit(cache, acc_t[kk], T, status=st, check=False)
+    e1.record(s)
+    torch.cuda.synchronize()
+    st.raise_if_error("bench gdn verify")
+    ms = e0.elapsed_time(e1)
+    ach = total / (ms * 1e-3) / 1e9
+    return {"seq_verify_steps_per_s": S * steps / (ms * 1e-3), "committed_tok_per_s": float(acc.sum()) / (ms * 1e-3),
+            "us_per_step": ms * 1e3 / steps, "achieved_gbs": ach, "hbm_frac": ach / hbm, "algorithmic_bytes": total,
+            "steps": steps}
+
+
 def bench_ssu(dev, steps: int, hbm: float):
     import torch
     import exact_replay_decode_gb300 as ers
@@ -704,7 +758,7 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--decode-only", action="store_true", help="only the headline decode measurement")
     ap.add_argument("--batch", type=int, default=None, help="decode sequences per GPU (profiling runs only)")
-    ap.add_argument("--section", choices=["prefill", "verify", "rssm", "ssu", "conv"], default=None,
+    ap.add_argument("--section", choices=["prefill", "verify", "rssm", "ssu", "conv", "gdn"], default=None,
                     help="run only this secondary workload and print its JSON (profiling aid, no headline)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
@@ -725,6 +779,8 @@ def main(argv=None):
             out = {n: bench_prefill(dev, n, 10, args.warmup, hbm, tc) for n in ("prefill_2048_h32", "varlen_4seq_h64")}
         elif args.section == "conv":
             out = bench_conv(dev, hbm)
+        elif args.section == "gdn":
+            out = bench_gdn_verify(dev, 32, hbm)
         elif args.section == "rssm":
             out = {r: bench_rssm_decode(dev, 4, hbm, r) for r in ("bf16", "fp8", "nvfp4")}
             out["nvfp4_fp16sr"] = bench_rssm_decode(dev, 4, hbm, "nvfp4", "fp16_sr")
@@ -764,6 +820,7 @@ def main(argv=None):
         extra["replayssm_decode"]["nvfp4_fp16sr"] = bench_rssm_decode(dev, 4, hbm, "nvfp4", "fp16_sr")
         extra["ssu"] = bench_ssu(dev, 16, hbm)
         extra["conv1d"] = bench_conv(dev, hbm)
+        extra["gdn_verify"] = bench_gdn_verify(dev, 32, hbm)
     line = {
         "metric": "replay-decode seq-steps/s per layer @B=256",
         "value": value,

@@ -49,6 +49,14 @@ struct GdnSmem {
   float kkf[kGL][kGL];       // k_i . k_r, committed rows (flush)
   float kk[kGL + kGT][kGT];  // k_row . k_draft
   float kq[kGL + kGT][kGT];  // k_row . q_draft
+  // per-head coefficients, computed once per head (same expressions, so the same bits, as inline)
+  float cf[kGL][kGL];        // flush: beta_r gamma_{i+1..r} (k_i . k_r), i < r
+  float gamf[kGL];           // flush: gamma_{1..r}
+  float wf[kGL];             // flush: gamma_{r+1..hc}
+  float cc[kGL + kGT][kGT];  // drafts: beta_t gamma_{r+1..t} (k_r . k_s), r < t = h0 + s
+  float wq[kGL + kGT][kGT];  // drafts: gamma_{r+1..t} (k_r . q_s), r <= t
+  float gam[kGT];            // drafts: gamma_{1..t}
+  float yu[kGWarps][kGRows][kGL + 1];   // flush: per warp and row, S k_i then the residual u_i (padded)
 };
 
 template <typename T>
@@ -64,39 +72,79 @@ __device__ __forceinline__ float sdot(const float* a, const float* b, int j) {
   return Dot<kGD>::reduce(Dot<kGD>::partial(qa, qb));
 }
 
-// One pass over the anchor rows of warp w: for each row d, S_anchor k_i for the hc committed
-// records, their residuals (every lane computes the same scalars), the fold
-//     S'[d][n] = gamma_{1..hc} S[d][n] + sum_i gamma_{i+1..hc} u_i[d] k_i[n]   (fma chain in row order)
-// stored to the anchor and cast to the bf16 read copy; with drafts, their S' k_s and S' q_s from
-// the cast values go to y and z.
+// S_src k_s and S_src q_s for the drafts (at most TM of them), RPG = 32 / (2 TM) rows per
+// reduce-scatter: lane l gets the sum of partial l = 2 TM * (row of the group) + (s for k, TM + s
+// for q); the pairings are Dot<128>'s, so each value has the bits of a Dot<128> reduction.
+template <int TM>
+__device__ __forceinline__ void draft_dots(GdnSmem& sm, const float (&rv)[32 / (2 * TM)][4], int d0, int Td, int j) {
+  constexpr int RPG = 32 / (2 * TM);
+  float part[32];
+#pragma unroll
+  for (int s = 0; s < TM; ++s) {
+    float ka[4], qb[4];
+    lds4(sm.k[kGL + s] + 4 * j, ka);
+    lds4(sm.q[s] + 4 * j, qb);
+#pragma unroll
+    for (int g = 0; g < RPG; ++g) {
+      part[2 * TM * g + s] = Dot<kGD>::partial(ka, rv[g]);
+      part[2 * TM * g + TM + s] = Dot<kGD>::partial(qb, rv[g]);
+    }
+  }
+  const float v = reduce_scatter32(part, j);
+  const int d = d0 + j / (2 * TM), idx = j % (2 * TM);
+  if (idx < TM) {
+    if (idx < Td) sm.y[idx][d] = v;
+  } else if (idx - TM < Td) {
+    sm.z[idx - TM][d] = v;
+  }
+}
+
+// The flush of warp w's anchor rows, in three passes:
+//  A. S k_i for the hc committed records, one reduce-scatter per row (lane i gets row d's S k_i);
+//  B. the triangular solve, one row per lane (lanes 0..15), in row order, in place of S k_i;
+//  C. the fold S'[d][n] = gamma_{1..hc} S[d][n] + sum_i gamma_{i+1..hc} u_i[d] k_i[n] (fma chain in
+//     row order), stored to the anchor and cast to the bf16 read copy; with drafts, S' k_s and S' q_s
+//     from the cast values (draft_dots).
+template <int TM>
 __device__ __forceinline__ void gdn_fold_rows(GdnSmem& sm, float* __restrict__ S, __nv_bfloat16* __restrict__ R,
                                               int hc, int ndraft, int w, int j) {
-  const float gall = expf(sm.gf[hc - 1]);
+  constexpr int RPG = 32 / (2 * TM);
+  float (*YU)[kGL + 1] = sm.yu[w];   // [row of the warp][record]: S k_i, then u_i
   for (int rr = 0; rr < kGRows; ++rr) {
     const int d = w * kGRows + rr;
     float hq[4];
     Quad<float>::unpack(*reinterpret_cast<const float4*>(S + (size_t)d * kGD + 4 * j), hq);
-    float u[kGL];
-#pragma unroll 1
-    for (int r = 0; r < hc; ++r) {
+    float part[32];
+#pragma unroll
+    for (int r = 0; r < kGL; ++r) {
       float kq4[4];
       lds4(sm.k[r] + 4 * j, kq4);
-      const float y = Dot<kGD>::reduce(Dot<kGD>::partial(kq4, hq));
-      float acc = __fmul_rn(sm.bf[r], __fmaf_rn(-expf(sm.gf[r]), y, sm.vc[r][d]));
-      for (int i = 0; i < r; ++i) {
-        const float c = __fmul_rn(__fmul_rn(sm.bf[r], expf(__fsub_rn(sm.gf[r], sm.gf[i]))), sm.kkf[i][r]);
-        acc = __fmaf_rn(-c, u[i], acc);
-      }
-      u[r] = acc;
+      part[r] = r < hc ? Dot<kGD>::partial(kq4, hq) : 0.f;
     }
-    float nv[4];
+    YU[rr][j] = reduce_scatter32(part, j);
+  }
+  __syncwarp();
+  if (j < kGRows) {
+    const int d = w * kGRows + j;
+    for (int r = 0; r < hc; ++r) {
+      float acc = __fmul_rn(sm.bf[r], __fmaf_rn(-sm.gamf[r], YU[j][r], sm.vc[r][d]));
+      for (int i = 0; i < r; ++i) acc = __fmaf_rn(-sm.cf[i][r], YU[j][i], acc);
+      YU[j][r] = acc;
+    }
+  }
+  __syncwarp();
+  const float gall = sm.gamf[hc - 1];
+  float rvg[RPG][4];
+  for (int rr = 0; rr < kGRows; ++rr) {
+    const int d = w * kGRows + rr;
+    float hq[4], nv[4];
+    Quad<float>::unpack(*reinterpret_cast<const float4*>(S + (size_t)d * kGD + 4 * j), hq);
 #pragma unroll
     for (int e = 0; e < 4; ++e) nv[e] = __fmul_rn(gall, hq[e]);
-#pragma unroll 1
     for (int r = 0; r < hc; ++r) {
       float kq4[4];
       lds4(sm.k[r] + 4 * j, kq4);
-      const float wu = __fmul_rn(expf(__fsub_rn(sm.gf[hc - 1], sm.gf[r])), u[r]);
+      const float wu = __fmul_rn(sm.wf[r], YU[rr][r]);
 #pragma unroll
       for (int e = 0; e < 4; ++e) nv[e] = __fmaf_rn(wu, kq4[e], nv[e]);
     }
@@ -108,16 +156,13 @@ __device__ __forceinline__ void gdn_fold_rows(GdnSmem& sm, float* __restrict__ S
     *reinterpret_cast<uint2*>(R + (size_t)d * kGD + 4 * j) = pk;
     float rv[4];
     Quad<__nv_bfloat16>::unpack(pk, rv);
-    for (int s = 0; s < ndraft; ++s) {
-      float a[4], b[4];
-      lds4(sm.k[kGL + s] + 4 * j, a);
-      lds4(sm.q[s] + 4 * j, b);
-      const float ys = Dot<kGD>::reduce(Dot<kGD>::partial(a, rv));
-      const float zs = Dot<kGD>::reduce(Dot<kGD>::partial(b, rv));
-      if (j == 0) {
-        sm.y[s][d] = ys;
-        sm.z[s][d] = zs;
-      }
+    if (ndraft > 0) {
+#pragma unroll
+      for (int g = 0; g < RPG; ++g)
+        if (rr % RPG == g)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) rvg[g][e] = rv[e];
+      if (rr % RPG == RPG - 1) draft_dots<TM>(sm, rvg, d - (RPG - 1), ndraft, j);
     }
   }
 }
@@ -143,14 +188,22 @@ __device__ __forceinline__ void load_committed_head(GdnSmem& sm, const GdnArgs& 
 }
 
 // Gates of the committed records summed in row order, and their betas (thread 0).
+// (Warp 0: the lanes load one row each, then lane 0 sums in row order.)
 __device__ __forceinline__ void flush_scalars(GdnSmem& sm, const GdnArgs& a, int slot, int h, int hc) {
-  if (threadIdx.x == 0) {
-    float acc = 0.f;
-    for (int r = 0; r < hc; ++r) {
+  if (threadIdx.x < 32) {
+    const int r = threadIdx.x;
+    if (r < hc) {
       const size_t row = (size_t)slot * a.L + r;
-      acc = __fadd_rn(acc, a.bg[row * a.H + h]);
-      sm.gf[r] = acc;
+      sm.gf[r] = a.bg[row * a.H + h];
       sm.bf[r] = a.bbeta[row * a.H + h];
+    }
+    __syncwarp();
+    if (r == 0) {
+      float acc = 0.f;
+      for (int q = 0; q < hc; ++q) {
+        acc = __fadd_rn(acc, sm.gf[q]);
+        sm.gf[q] = acc;
+      }
     }
   }
 }
@@ -166,6 +219,31 @@ __device__ __forceinline__ void flush_gram(GdnSmem& sm, int hc) {
   }
 }
 
+// Per-head flush coefficients from gf, bf and kkf (all threads; call after both are in smem).
+__device__ __forceinline__ void flush_coeffs(GdnSmem& sm, int hc) {
+  for (int p = threadIdx.x; p < hc * hc; p += kThreads) {
+    const int i = p / hc, r = p % hc;
+    if (i < r) sm.cf[i][r] = __fmul_rn(__fmul_rn(sm.bf[r], expf(__fsub_rn(sm.gf[r], sm.gf[i]))), sm.kkf[i][r]);
+  }
+  for (int r = threadIdx.x; r < hc; r += kThreads) {
+    sm.gamf[r] = expf(sm.gf[r]);
+    sm.wf[r] = expf(__fsub_rn(sm.gf[hc - 1], sm.gf[r]));
+  }
+}
+
+// Per-head draft coefficients from gc, bt, kk and kq.
+__device__ __forceinline__ void draft_coeffs(GdnSmem& sm, int h0, int Td) {
+  for (int p = threadIdx.x; p < (h0 + Td) * Td; p += kThreads) {
+    const int r = p / Td, s = p % Td, t = h0 + s;
+    if (r <= t) {
+      const float e = expf(__fsub_rn(sm.gc[t], sm.gc[r]));
+      sm.wq[r][s] = __fmul_rn(e, sm.kq[r][s]);
+      if (r < t) sm.cc[r][s] = __fmul_rn(__fmul_rn(sm.bt[t], e), sm.kk[r][s]);
+    }
+  }
+  for (int s = threadIdx.x; s < Td; s += kThreads) sm.gam[s] = expf(sm.gc[h0 + s]);
+}
+
 __device__ __forceinline__ bool gdn_slot(const GdnArgs& a, int i, int* slot) {
   const int s = a.slot != nullptr ? a.slot[i] : i;
   if (s < 0 || s >= a.nslots) {
@@ -179,8 +257,9 @@ __device__ __forceinline__ bool gdn_slot(const GdnArgs& a, int i, int* slot) {
 // One CTA per (sequence, key group); its value heads run one after another, so the group's key rows
 // are read once and the drafts' key rows are written after every head of the group has read the
 // committed ones (a flush reuses buffer rows from 0).
-template <typename T>
+template <typename T, int TM>
 __global__ void __launch_bounds__(kThreads, 1) k_gdn_verify(GdnArgs a) {
+  constexpr int RPG = 32 / (2 * TM);
   extern __shared__ __align__(16) unsigned char gsm_raw[];
   GdnSmem& sm = *reinterpret_cast<GdnSmem*>(gsm_raw);
   const int g = blockIdx.x, i = blockIdx.y, tid = threadIdx.x, w = tid >> 5, j = tid & 31;
@@ -227,36 +306,40 @@ __global__ void __launch_bounds__(kThreads, 1) k_gdn_verify(GdnArgs a) {
     for (int s = w; s < Td; s += kGWarps)
       load_vec<T>((const T*)a.v + (((size_t)i * Td + s) * a.H + h) * kGD, sm.v[s]);
     if (flush && hc > 0) flush_scalars(sm, a, slot, h, hc);
-    if (tid == 32) {   // output rows: committed rows 0..h0-1, then the drafts; gates in row order
-      float acc = 0.f;
-      for (int r = 0; r < h0 + Td; ++r) {
+    if (w == 1) {   // output rows: committed rows 0..h0-1, then the drafts; gates summed in row order
+      for (int r = j; r < h0 + Td; r += 32) {
         const size_t br = ((size_t)slot * a.L + r) * a.H + h, tr = ((size_t)i * Td + (r - h0)) * a.H + h;
-        acc = __fadd_rn(acc, r < h0 ? a.bg[br] : a.g[tr]);
-        sm.gc[r] = acc;
+        sm.gc[r] = r < h0 ? a.bg[br] : a.g[tr];
         sm.bt[r] = r < h0 ? a.bbeta[br] : a.beta[tr];
+      }
+      __syncwarp();
+      if (j == 0) {
+        float acc = 0.f;
+        for (int r = 0; r < h0 + Td; ++r) {
+          acc = __fadd_rn(acc, sm.gc[r]);
+          sm.gc[r] = acc;
+        }
       }
     }
     __syncthreads();
+    if (flush && hc > 0) flush_coeffs(sm, hc);
+    draft_coeffs(sm, h0, Td);
+    __syncthreads();
     if (flush && hc > 0) {
-      gdn_fold_rows(sm, a.anchor + soff, (__nv_bfloat16*)a.copy + soff, hc, Td, w, j);
+      gdn_fold_rows<TM>(sm, a.anchor + soff, (__nv_bfloat16*)a.copy + soff, hc, Td, w, j);
     } else {
       // stream the read copy: S_read k_s and S_read q_s for every draft
       const __nv_bfloat16* R = (const __nv_bfloat16*)a.copy + soff;
-      for (int rr = 0; rr < kGRows; ++rr) {
-        const int d = w * kGRows + rr;
-        float rv[4];
-        Quad<__nv_bfloat16>::unpack(Quad<__nv_bfloat16>::ld_stream(R + (size_t)d * kGD + 4 * j), rv);
-        for (int s = 0; s < Td; ++s) {
-          float ka[4], qb[4];
-          lds4(sm.k[kGL + s] + 4 * j, ka);
-          lds4(sm.q[s] + 4 * j, qb);
-          const float ys = Dot<kGD>::reduce(Dot<kGD>::partial(ka, rv));
-          const float zs = Dot<kGD>::reduce(Dot<kGD>::partial(qb, rv));
-          if (j == 0) {
-            sm.y[s][d] = ys;
-            sm.z[s][d] = zs;
-          }
-        }
+      uint2 raw[kGRows];   // the warp's rows, all in flight before the math
+#pragma unroll
+      for (int rr = 0; rr < kGRows; ++rr)
+        raw[rr] = Quad<__nv_bfloat16>::ld_stream(R + (size_t)(w * kGRows + rr) * kGD + 4 * j);
+#pragma unroll
+      for (int rr = 0; rr < kGRows; rr += RPG) {
+        float rvg[RPG][4];
+#pragma unroll
+        for (int g = 0; g < RPG; ++g) Quad<__nv_bfloat16>::unpack(raw[rr + g], rvg[g]);
+        draft_dots<TM>(sm, rvg, w * kGRows + rr, Td, j);
       }
     }
     __syncthreads();
@@ -265,19 +348,17 @@ __global__ void __launch_bounds__(kThreads, 1) k_gdn_verify(GdnArgs a) {
       const int d = tid;
       for (int s = 0; s < Td; ++s) {
         const int t = h0 + s;
-        const float gam = expf(sm.gc[t]);
+        const float gam = sm.gam[s];
         float acc = __fmul_rn(sm.bt[t], __fmaf_rn(-gam, sm.y[s][d], sm.v[s][d]));
         for (int r = 0; r < t; ++r) {
           const float ur = r < h0 ? sm.u[r][d] : sm.u[kGL + r - h0][d];
-          const float c = __fmul_rn(__fmul_rn(sm.bt[t], expf(__fsub_rn(sm.gc[t], sm.gc[r]))), sm.kk[r][s]);
-          acc = __fmaf_rn(-c, ur, acc);
+          acc = __fmaf_rn(-sm.cc[r][s], ur, acc);
         }
         sm.u[kGL + s][d] = acc;
         float out = __fmul_rn(gam, sm.z[s][d]);
         for (int r = 0; r <= t; ++r) {
           const float ur = r < h0 ? sm.u[r][d] : sm.u[kGL + r - h0][d];
-          const float wq = __fmul_rn(expf(__fsub_rn(sm.gc[t], sm.gc[r])), sm.kq[r][s]);
-          out = __fmaf_rn(wq, ur, out);
+          out = __fmaf_rn(sm.wq[r][s], ur, out);
         }
         ((T*)a.o)[(((size_t)i * Td + s) * a.H + h) * kGD + d] = from_f<T>(out);
       }
@@ -328,8 +409,10 @@ __global__ void __launch_bounds__(kThreads, 1) k_gdn_refresh(GdnArgs a) {
     load_committed_head<T>(sm, a, slot, h, hc, true);
     flush_scalars(sm, a, slot, h, hc);
     __syncthreads();
+    flush_coeffs(sm, hc);
+    __syncthreads();
     const size_t soff = ((size_t)slot * a.H + h) * kGD * kGD;
-    gdn_fold_rows(sm, a.anchor + soff, (__nv_bfloat16*)a.copy + soff, hc, 0, w, j);
+    gdn_fold_rows<4>(sm, a.anchor + soff, (__nv_bfloat16*)a.copy + soff, hc, 0, w, j);
     __syncthreads();
   }
 }
@@ -376,16 +459,20 @@ cudaError_t gdn_launch(const GdnArgs& a, int kind, const int32_t* accepted, cuda
     return cudaGetLastError();
   }
   const dim3 grid(a.G, a.nseq);
+  auto run = [&](auto kernel) {
+    cudaError_t err = prep(kernel, sm);
+    if (err != cudaSuccess) return err;
+    kernel<<<grid, kThreads, sm, s>>>(a);
+    return cudaGetLastError();
+  };
+  const bool small = a.T <= 4;   // drafts' dot products 4 wide (4 rows per reduce-scatter), else 8
   if (a.io == ERS_DTYPE_BF16) {
-    auto kv = kind == 0 ? k_gdn_verify<__nv_bfloat16> : k_gdn_refresh<__nv_bfloat16>;
-    if ((e = prep(kv, sm)) != cudaSuccess) return e;
-    kv<<<grid, kThreads, sm, s>>>(a);
+    e = kind == 1 ? run(k_gdn_refresh<__nv_bfloat16>)
+                  : (small ? run(k_gdn_verify<__nv_bfloat16, 4>) : run(k_gdn_verify<__nv_bfloat16, 8>));
   } else {
-    auto kv = kind == 0 ? k_gdn_verify<float> : k_gdn_refresh<float>;
-    if ((e = prep(kv, sm)) != cudaSuccess) return e;
-    kv<<<grid, kThreads, sm, s>>>(a);
+    e = kind == 1 ? run(k_gdn_refresh<float>) : (small ? run(k_gdn_verify<float, 4>) : run(k_gdn_verify<float, 8>));
   }
-  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  if (e != cudaSuccess) return e;
   if (kind == 1) {
     k_gdn_setpos<<<(a.nseq + 255) / 256, 256, 0, s>>>(a);
     return cudaGetLastError();
