@@ -257,8 +257,10 @@ __device__ __forceinline__ bool gdn_slot(const GdnArgs& a, int i, int* slot) {
 // One CTA per (sequence, key group); its value heads run one after another, so the group's key rows
 // are read once and the drafts' key rows are written after every head of the group has read the
 // committed ones (a flush reuses buffer rows from 0).
+// Two CTAs per SM (~102 KB of shared memory each) when the drafts' dots are 4 wide; the 8-wide
+// variant needs more registers than two CTAs leave.
 template <typename T, int TM>
-__global__ void __launch_bounds__(kThreads, 1) k_gdn_verify(GdnArgs a) {
+__global__ void __launch_bounds__(kThreads, TM == 4 ? 2 : 1) k_gdn_verify(GdnArgs a) {
   constexpr int RPG = 32 / (2 * TM);
   extern __shared__ __align__(16) unsigned char gsm_raw[];
   GdnSmem& sm = *reinterpret_cast<GdnSmem*>(gsm_raw);
@@ -388,7 +390,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_gdn_verify(GdnArgs a) {
 // Standalone refresh: slots with h + T > L (T = drafts_T) and h > 0 fold their records exactly as a
 // verify's flush does.  Positions are reset by k_gdn_setpos afterwards.
 template <typename T>
-__global__ void __launch_bounds__(kThreads, 1) k_gdn_refresh(GdnArgs a) {
+__global__ void __launch_bounds__(kThreads, 2) k_gdn_refresh(GdnArgs a) {
   extern __shared__ __align__(16) unsigned char gsm_raw[];
   GdnSmem& sm = *reinterpret_cast<GdnSmem*>(gsm_raw);
   const int g = blockIdx.x, i = blockIdx.y, w = threadIdx.x >> 5, j = threadIdx.x & 31;
