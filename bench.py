@@ -587,7 +587,8 @@ def bench_conv(dev, hbm: float, reps: int = 50):
 
 def bench_gdn_verify(dev, steps: int, hbm: float):
     """Output-only verify of a gated-delta-rule layer: 512 sequences x 4 drafts, 32 value heads / 16
-    key groups, dk = dv = 128, window 16, bf16 io, 32 verify + commit steps.  Bytes from the run's own
+    key groups, dk = dv = 128, window 16, bf16 io, 3 warm-up steps (then the cache goes back to its
+    start), 32 timed verify + commit steps; the 512 MiB read copy exceeds L2.  Bytes from the run's own
     pointers and flushes: per sequence-step the read copy (32 x 128 x 128 bf16), the drafts' q, k, v,
     g, beta in and o out, the committed records' k and cached residuals (and g, beta) read, and the
     drafts' k, v, residuals, g, beta written to the buffer; per flush the anchor read and written, the
@@ -614,6 +615,12 @@ def bench_gdn_verify(dev, steps: int, hbm: float):
     row_read = G * D * 2 + H * D * 4 + H * 8                 # committed k, residual u, g and beta
     row_write = G * D * 2 + H * D * 2 + H * D * 4 + H * 8    # a draft's k, v, u, g, beta
     io = T * (2 * G * D * 2 + H * D * 2 + H * 8) + T * H * D * 2
+    for kk in range(min(3, steps)):                              # warm-up, then back to the start
+        ers.gdn_verify(cache, q[kk], k[kk], v[kk], g[kk], beta[kk], status=st, check=False, out=o)
+        ers.gdn_commit(cache, acc_t[kk], T, status=st, check=False)
+    cache.anchor.copy_(torch.from_numpy(anchor))
+    cache.read_copy.copy_(cache.anchor)
+    cache.pos.zero_()
     hs = np.zeros(S, dtype=np.int64)
     total = 0
     for kk in range(steps):
