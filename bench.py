@@ -414,9 +414,8 @@ def bench_verify(dev, steps: int, hbm: float, read_dtype: str = "bf16", anchor: 
     _, fin = ers.ssd_scan_fwd(hx, hdt, prm, hB, hC, chunk=L, cu_seqlens=cu)
     cache = ers.ReplayCache(S, d.nheads, d.ngroups, d.headdim, d.dstate, L, torch.bfloat16, read_copy=True,
                             read_dtype=read_dtype, anchor=anchor, sr_key=(0x5EED, 0xF00D))
-    cache.state.copy_(fin)
-    ers.refresh(cache, prm, replayssm=True, drafts_T=L + 1)
-    anchor_bytes = d.nheads * d.headdim * d.dstate * (2 if anchor == "fp16_sr" else 4)
+    _seed_cache(ers, cache, prm, fin, L)
+    anchor_bytes = _anchor_bytes(d, anchor)
     # read copy per sequence: bf16 values, or FP8 codes + one fp32 scale per state row
     copy_bytes = _copy_bytes(d, read_dtype)
     dx, ddt, dB, dC = torch_io.tokens_to(drafts, dev, lead=(steps, S, T))
@@ -430,9 +429,10 @@ def bench_verify(dev, steps: int, hbm: float, read_dtype: str = "bf16", anchor: 
         flush = hs + T > L
         base = np.where(flush, 0, hs)
         total_bytes += S * (copy_bytes + 50_176 + 50_176 + 32_768) + int(base.sum()) * 10_496
-        # a flushing slot reads and writes its fp32 anchor and writes its copy instead of reading it
-        total_bytes += int(flush.sum()) * (2 * anchor_bytes + copy_bytes - copy_bytes) + \
-            int(hs[flush].sum()) * 10_496
+        # a flushing slot reads and writes its anchor and writes its copy instead of reading it (a
+        # shared NVFP4 state: reads the copy as the anchor and writes it)
+        flush_extra = copy_bytes if anchor == "nvfp4_sr_shared" else 2 * anchor_bytes
+        total_bytes += int(flush.sum()) * flush_extra + int(hs[flush].sum()) * 10_496
         hs = base + acc[k]
     torch.cuda.synchronize()
     s = torch.cuda.current_stream()
@@ -450,6 +450,23 @@ def bench_verify(dev, steps: int, hbm: float, read_dtype: str = "bf16", anchor: 
     return {"read_copy": read_dtype, "anchor": anchor, "seq_verify_steps_per_s": S * steps / (ms * 1e-3),
             "committed_tok_per_s": float(acc.sum()) / (ms * 1e-3), "us_per_step": ms * 1e3 / steps,
             "achieved_gbs": ach, "hbm_frac": ach / hbm, "algorithmic_bytes": total_bytes, "steps": steps}
+
+
+def _anchor_bytes(d, anchor: str) -> int:
+    """Bytes of one sequence's separate anchor: fp32 or fp16 (none for the shared NVFP4 state)."""
+    if anchor == "nvfp4_sr_shared":
+        return 0
+    return d.nheads * d.headdim * d.dstate * (2 if anchor == "fp16_sr" else 4)
+
+
+def _seed_cache(ers, cache, prm, fin, L: int) -> None:
+    """Put the fp32 state fin into the cache with every position 0: anchor copied and read copy cast,
+    or (shared NVFP4 state) the round-to-nearest cast."""
+    if cache.anchor == "nvfp4_sr_shared":
+        cache.seed(fin, prm)
+        return
+    cache.state.copy_(fin)
+    ers.refresh(cache, prm, replayssm=True, drafts_T=L + 1)
 
 
 def bench_rssm_decode(dev, cycles: int, hbm: float, read_dtype: str, anchor: str = "fp32"):
@@ -475,8 +492,7 @@ def bench_rssm_decode(dev, cycles: int, hbm: float, read_dtype: str, anchor: str
     del hx, hdt, hB, hC
     cache = ers.ReplayCache(S, d.nheads, d.ngroups, d.headdim, d.dstate, L, torch.bfloat16, read_copy=True,
                             read_dtype=read_dtype, anchor=anchor, sr_key=(0x5EED, 0xF00D))
-    cache.state.copy_(fin)
-    ers.refresh(cache, prm, replayssm=True, drafts_T=L + 1)           # h = 0: cast the read copy
+    _seed_cache(ers, cache, prm, fin, L)                                # h = 0: cast the read copy
     tok = torch_io.tokens_to(stream, dev, lead=(TOKEN_RING, S))
     y = torch.empty(S, d.nheads, d.headdim, dtype=torch.bfloat16, device=dev)
     st = ers.Status(dev)
@@ -492,11 +508,13 @@ def bench_rssm_decode(dev, cycles: int, hbm: float, read_dtype: str, anchor: str
         ers.replay_decode(cache, prm, *(t[k] for t in tok), replayssm=True, fuse_refresh=True, status=st,
                           check=False, out=y)
 
-    # algorithmic bytes from the run's own pointers: a flush reads and writes the anchor, reads the
-    # h buffered rows and writes the copy; a decode reads the copy, h rows and the new token, writes
-    # the token to the buffer and y
+    # algorithmic bytes from the run's own pointers: a flush reads and writes the anchor (a shared
+    # NVFP4 state: reads and writes the copy), reads the h buffered rows and writes the copy, and its
+    # output comes from the new values; a decode without a flush reads the copy; every step reads
+    # its h rows and the new token and writes the token to the buffer and y
     copy_bytes = _copy_bytes(d, read_dtype)
-    anchor_bytes = d.nheads * d.headdim * d.dstate * (2 if anchor == "fp16_sr" else 4)
+    anchor_bytes = _anchor_bytes(d, anchor)
+    shared = anchor == "nvfp4_sr_shared"
     hs = h0.astype(np.int64)
 
     def cycle_bytes():
@@ -504,9 +522,10 @@ def bench_rssm_decode(dev, cycles: int, hbm: float, read_dtype: str, anchor: str
         b = 0
         for _ in range(TOKEN_RING):
             fl = hs + 1 > L
-            b += int(fl.sum()) * (2 * anchor_bytes + copy_bytes) + int(hs[fl].sum()) * 10_496
+            nfl = int(fl.sum())
+            b += nfl * (2 * anchor_bytes + copy_bytes + (copy_bytes if shared else 0)) + int(hs[fl].sum()) * 10_496
             hs = np.where(fl, 0, hs)
-            b += S * (copy_bytes + 12_544 + 12_544 + 8_192) + int(hs.sum()) * 10_496
+            b += (S - nfl) * copy_bytes + S * (12_544 + 12_544 + 8_192) + int(hs.sum()) * 10_496
             hs = hs + 1
         return b
 
@@ -791,13 +810,16 @@ def main(argv=None):
         elif args.section == "rssm":
             out = {r: bench_rssm_decode(dev, 4, hbm, r) for r in ("bf16", "fp8", "nvfp4")}
             out["nvfp4_fp16sr"] = bench_rssm_decode(dev, 4, hbm, "nvfp4", "fp16_sr")
+            out["nvfp4_shared_sr"] = bench_rssm_decode(dev, 4, hbm, "nvfp4", "nvfp4_sr_shared")
         elif args.section == "verify":
             out = bench_verify(dev, 32, hbm)
             fp8 = bench_verify(dev, 32, hbm, "fp8")
             nv4 = bench_verify(dev, 32, hbm, "nvfp4")
             nv4sr = bench_verify(dev, 32, hbm, "nvfp4", "fp16_sr")
+            nv4sh = bench_verify(dev, 32, hbm, "nvfp4", "nvfp4_sr_shared")
             if rank == 0:
-                print(json.dumps({"verify_fp8": fp8, "verify_nvfp4": nv4, "verify_nvfp4_fp16sr": nv4sr}))
+                print(json.dumps({"verify_fp8": fp8, "verify_nvfp4": nv4, "verify_nvfp4_fp16sr": nv4sr,
+                                  "verify_nvfp4_shared_sr": nv4sh}))
         else:
             out = bench_ssu(dev, 16, hbm)
         if rank == 0:
@@ -823,8 +845,10 @@ def main(argv=None):
         extra["verify_fp8"] = bench_verify(dev, 32, hbm, "fp8")
         extra["verify_nvfp4"] = bench_verify(dev, 32, hbm, "nvfp4")
         extra["verify_nvfp4_fp16sr"] = bench_verify(dev, 32, hbm, "nvfp4", "fp16_sr")
+        extra["verify_nvfp4_shared_sr"] = bench_verify(dev, 32, hbm, "nvfp4", "nvfp4_sr_shared")
         extra["replayssm_decode"] = {r: bench_rssm_decode(dev, 4, hbm, r) for r in ("bf16", "fp8", "nvfp4")}
         extra["replayssm_decode"]["nvfp4_fp16sr"] = bench_rssm_decode(dev, 4, hbm, "nvfp4", "fp16_sr")
+        extra["replayssm_decode"]["nvfp4_shared_sr"] = bench_rssm_decode(dev, 4, hbm, "nvfp4", "nvfp4_sr_shared")
         extra["ssu"] = bench_ssu(dev, 16, hbm)
         extra["conv1d"] = bench_conv(dev, hbm)
         extra["gdn_verify"] = bench_gdn_verify(dev, 32, hbm)

@@ -30,6 +30,7 @@ READ_NVFP4 = 2
 
 ANCHOR_F32 = 0
 ANCHOR_F16_SR = 1
+ANCHOR_NVFP4_SHARED_SR = 2
 
 # Every function include/ers.h declares.
 EXPORTS = (

@@ -42,7 +42,10 @@ ers_status check_params(const ers_params* p) {
   return ERS_OK;
 }
 
-ers_status check_state_ptrs(const ers_cache* c) { return check_ptr(c->state, true); }
+// The shared NVFP4 state keeps no separate anchor: state is unused (may be NULL).
+ers_status check_state_ptrs(const ers_cache* c) {
+  return check_ptr(c->state, c->anchor_dtype != ERS_ANCHOR_NVFP4_SHARED_SR);
+}
 
 // FP8 and NVFP4 read copies are implemented by the CUDA-core warp-per-head kernels only.
 bool narrow_read_shape(const ers_dims* d) {
@@ -50,13 +53,17 @@ bool narrow_read_shape(const ers_dims* d) {
 }
 bool has_narrow_copy(const ers_cache* c) { return c->read_copy != nullptr && c->read_dtype != ERS_READ_BF16; }
 bool has_nvfp4_copy(const ers_cache* c) { return c->read_copy != nullptr && c->read_dtype == ERS_READ_NVFP4; }
-bool f16_anchor(const ers_cache* c) { return c->anchor_dtype == ERS_ANCHOR_F16_SR; }
+bool f16_anchor(const ers_cache* c) {   // an anchor other than fp32: fp16 SR or the shared NVFP4 state
+  return c->anchor_dtype == ERS_ANCHOR_F16_SR || c->anchor_dtype == ERS_ANCHOR_NVFP4_SHARED_SR;
+}
 
-// fp16 anchors: ReplaySSM calls only, bf16 io, a read copy, the warp-per-head shapes.
+// fp16 anchors and the shared NVFP4 state: ReplaySSM calls only, bf16 io, a read copy (NVFP4 for the
+// shared state), the warp-per-head shapes.
 ers_status check_f16_anchor(const ers_dims* d, const ers_cache* c, bool rssm) {
   if (!f16_anchor(c)) return ERS_OK;
   if (!rssm || d->io_dtype != ERS_DTYPE_BF16 || c->read_copy == nullptr || !narrow_read_shape(d))
     return ERS_EUNSUPPORTED;
+  if (c->anchor_dtype == ERS_ANCHOR_NVFP4_SHARED_SR && c->read_dtype != ERS_READ_NVFP4) return ERS_EUNSUPPORTED;
   return ERS_OK;
 }
 
@@ -69,7 +76,9 @@ ers_status check_cache(const ers_cache* c, bool need_read_copy) {
   if (c == nullptr || c->nslots < 0) return ERS_EINVAL;
   if (c->read_dtype != ERS_READ_BF16 && c->read_dtype != ERS_READ_FP8_E4M3 && c->read_dtype != ERS_READ_NVFP4)
     return ERS_EDTYPE;
-  if (c->anchor_dtype != ERS_ANCHOR_F32 && c->anchor_dtype != ERS_ANCHOR_F16_SR) return ERS_EDTYPE;
+  if (c->anchor_dtype != ERS_ANCHOR_F32 && c->anchor_dtype != ERS_ANCHOR_F16_SR &&
+      c->anchor_dtype != ERS_ANCHOR_NVFP4_SHARED_SR)
+    return ERS_EDTYPE;
   ERS_TRY(check_ptr(c->buf_pages, false));
   if (c->buf_pages != nullptr && (c->page_rows < 1 || c->npages < 1)) return ERS_EINVAL;
   ERS_TRY(check_state_ptrs(c));
@@ -112,6 +121,7 @@ void set_cache(LaunchArgs& a, const ers_cache* c) {
   a.page_rows = c->buf_pages != nullptr ? c->page_rows : 1;
   a.npages = c->npages;
   a.anchor_f16 = c->anchor_dtype == ERS_ANCHOR_F16_SR;
+  a.anchor_shared = c->anchor_dtype == ERS_ANCHOR_NVFP4_SHARED_SR;
   a.sr_key0 = c->sr_key[0];
   a.sr_key1 = c->sr_key[1];
   a.sr_nonce = c->sr_nonce;

@@ -184,10 +184,12 @@ __device__ __noinline__ void stream_flush_copy(AT* __restrict__ Hd, void* __rest
   constexpr bool kF8 = std::is_same<HT, uint8_t>::value;
   constexpr bool kNv = std::is_same<HT, Nvfp4>::value;
   constexpr bool kBf = std::is_same<HT, __nv_bfloat16>::value;
+  constexpr bool kSh = std::is_same<AT, Nvfp4Shared>::value;   // the NVFP4 copy is the state
+  static_assert(!kSh || kNv, "a shared state is an NVFP4 copy");
   const float c[4] = {c0, c1, c2, c3};
   float4 cur[8], nxt[8];
 #pragma unroll
-  for (int r = 0; r < 8; ++r) cur[r] = anchor_ld<AT>(Hd, (size_t)r * N + 4 * j);
+  for (int r = 0; r < 8; ++r) cur[r] = anchor_row<AT, N>(Hd, R, Rb, Rs, r, j);
   float part[16];
   float srow = 0.f;
 #pragma unroll 1
@@ -195,7 +197,7 @@ __device__ __noinline__ void stream_flush_copy(AT* __restrict__ Hd, void* __rest
     if (blk + 1 < NBLK) {
 #pragma unroll
       for (int r = 0; r < 8; ++r)
-        nxt[r] = anchor_ld<AT>(Hd, (size_t)((blk + 1) * 8 + r) * N + 4 * j);
+        nxt[r] = anchor_row<AT, N>(Hd, R, Rb, Rs, (blk + 1) * 8 + r, j);
     }
     float pb[8];
 #pragma unroll
@@ -226,9 +228,10 @@ __device__ __noinline__ void stream_flush_copy(AT* __restrict__ Hd, void* __rest
         if (hc > 0) anchor_st<AT>(Hd, o, v, sr, row0 + blk * 8 + r, j);
         float ls = 1.f;
         if constexpr (kNv) {
-          float sr;
-          nvfp4_store_row<N>(v, (uint8_t*)R, Rb, Rs, blk * 8 + r, j, rv, &ls, &sr);
-          if ((j >> 1) == (blk & 1) * 8 + r) srow = sr;
+          float rsc;
+          nvfp4_store_row<N, kSh>(v, (uint8_t*)R, Rb, Rs, blk * 8 + r, j, rv, &ls, &rsc,
+                                  copy_words<AT>(sr, row0 + blk * 8 + r, j));
+          if ((j >> 1) == (blk & 1) * 8 + r) srow = rsc;
         } else if constexpr (kF8) {
           float sr;
           const uint32_t wq = fp8_quant_row(v, &sr);
@@ -422,7 +425,7 @@ __global__ void __launch_bounds__(kThreads, 2) k_decode_heads(LaunchArgs a) {
     }
     __syncwarp();
     if constexpr (!std::is_same<HT, float>::value)
-      stream_flush_copy<T, HT, P, N, true, AT>((AT*)a.state + soff,
+      stream_flush_copy<T, HT, P, N, true, AT>(anchor_ptr<AT>(a, soff),
                                      std::is_same<HT, Nvfp4>::value ? (void*)((uint8_t*)a.read_copy + soff / 2)
                                                                     : (void*)((HT*)a.read_copy + soff),
                                      a.read_bscale + soff / 16, a.read_scale + ((size_t)slot * a.H + h) * P, c[0],
@@ -468,13 +471,14 @@ cudaError_t launch_decode_heads(const LaunchArgs& a, cudaStream_t s) {
     return cudaGetLastError();   // the kernel advances the positions itself
   };
   if constexpr (QM <= 16 && std::is_same<T, __nv_bfloat16>::value) {   // fp16 anchors: ReplaySSM only
+    if (a.anchor_shared && rssm && a.read_nvfp4) return run(k_decode_heads<T, Nvfp4, false, P, N, QM, Nvfp4Shared>);
     if (a.anchor_f16 && rssm) {
       if (a.read_nvfp4) return run(k_decode_heads<T, Nvfp4, false, P, N, QM, __half>);
       if (a.read_fp8) return run(k_decode_heads<T, uint8_t, true, P, N, QM, __half>);
       return run(k_decode_heads<T, __nv_bfloat16, false, P, N, QM, __half>);
     }
   }
-  if (a.anchor_f16) return cudaErrorNotSupported;
+  if (a.anchor_f16 || a.anchor_shared) return cudaErrorNotSupported;
   if constexpr (QM <= 16) {   // FP8 read copies: chunk <= 16 only (checked by the API)
     if (a.read_fp8)
       return rssm ? run(k_decode_heads<T, uint8_t, true, P, N, QM>) : run(k_decode_heads<T, float, true, P, N, QM>);
@@ -515,6 +519,7 @@ __global__ void __launch_bounds__(kThreads, 2) k_refresh_heads(LaunchArgs a) {
   }
   const bool rssm = (a.flags & ERS_FLAG_REPLAYSSM) != 0;
   if (!(rssm ? (p + a.T > a.Q) : (p == a.Q))) return;
+  if (std::is_same<AT, Nvfp4Shared>::value && p == 0) return;   // an empty history leaves the state as it is
   const size_t HP = (size_t)a.H * P, GN = (size_t)a.G * N;
   const T* bB = (const T*)a.bB + (size_t)g * N;
   constexpr int kBChunks = N * sizeof(T) / 16, kXChunks = P * sizeof(T) / 16;
@@ -557,7 +562,7 @@ __global__ void __launch_bounds__(kThreads, 2) k_refresh_heads(LaunchArgs a) {
   const size_t soff = ((size_t)slot * a.H + h) * P * N;
   void* R = std::is_same<HT, Nvfp4>::value ? (void*)((uint8_t*)a.read_copy + soff / 2)
                                            : (void*)((uint8_t*)a.read_copy + soff * sizeof_copy<HT>());
-  stream_flush_copy<T, HT, P, N, false, AT>((AT*)a.state + soff, R, a.read_bscale + soff / 16,
+  stream_flush_copy<T, HT, P, N, false, AT>(anchor_ptr<AT>(a, soff), R, a.read_bscale + soff / 16,
                                             a.read_scale + ((size_t)slot * a.H + h) * P, 0.f, 0.f, 0.f, 0.f, nullptr,
                                             j, p, wx, decay, sB,
                                             SrCtr{a.sr_key0, a.sr_key1, a.sr_nonce, (uint32_t)slot},
@@ -582,13 +587,14 @@ cudaError_t launch_refresh_heads(const LaunchArgs& a, cudaStream_t s) {
     return cudaGetLastError();
   };
   if constexpr (QM <= 16 && std::is_same<T, __nv_bfloat16>::value) {   // fp16 anchors (checked by the API)
+    if (a.anchor_shared && a.read_nvfp4) return run(k_refresh_heads<T, Nvfp4, P, N, QM, Nvfp4Shared>);
     if (a.anchor_f16) {
       if (a.read_nvfp4) return run(k_refresh_heads<T, Nvfp4, P, N, QM, __half>);
       if (a.read_fp8) return run(k_refresh_heads<T, uint8_t, P, N, QM, __half>);
       return run(k_refresh_heads<T, __nv_bfloat16, P, N, QM, __half>);
     }
   }
-  if (a.anchor_f16) return cudaErrorNotSupported;
+  if (a.anchor_f16 || a.anchor_shared) return cudaErrorNotSupported;
   if (a.read_copy == nullptr) return run(k_refresh_heads<T, NoCopy, P, N, QM>);
   if constexpr (QM <= 16) {
     if (a.read_nvfp4) return run(k_refresh_heads<T, Nvfp4, P, N, QM>);

@@ -38,6 +38,7 @@ struct LaunchArgs {
   float* read_scale;
   uint8_t* read_bscale;   // NVFP4 block scales [nslots, H, P, N / 16]
   int anchor_f16;         // ReplaySSM anchor stored as fp16 (state points to __half), written by SR
+  int anchor_shared;      // ReplaySSM: the NVFP4 read copy is the only state (state unused), written by SR
   uint32_t sr_key0, sr_key1, sr_nonce;   // counter-based random words for the SR writes
   void* bx;
   float* bdt;

@@ -84,12 +84,14 @@ __device__ __noinline__ void stream_anchor_flush(AT* __restrict__ Hd, void* __re
                                                  const float (&c)[kDraftsMax][4], float* yo, int j, int hc,
                                                  const float* wx, float decay, const T* sB, SrCtr sr, uint32_t row0) {
   constexpr bool kF8 = std::is_same<CT, uint8_t>::value, kNv = std::is_same<CT, Nvfp4>::value;
+  constexpr bool kSh = std::is_same<AT, Nvfp4Shared>::value;   // the NVFP4 copy is the state
+  static_assert(!kSh || kNv, "a shared state is an NVFP4 copy");
 #pragma unroll 1
   for (int d0 = 0; d0 < P; d0 += 8) {
     float h[8][4], acc[8][4];
 #pragma unroll
     for (int r = 0; r < 8; ++r) {
-      Quad<float>::unpack(anchor_ld<AT>(Hd, (size_t)(d0 + r) * N + 4 * j), h[r]);
+      Quad<float>::unpack(anchor_row<AT, N>(Hd, R, Rb, Rs, d0 + r, j), h[r]);
 #pragma unroll
       for (int e = 0; e < 4; ++e) acc[r][e] = 0.f;
     }
@@ -117,7 +119,7 @@ __device__ __noinline__ void stream_anchor_flush(AT* __restrict__ Hd, void* __re
       float ls = 1.f;
       if constexpr (kNv) {
         float s;
-        nvfp4_store_row<N>(v, (uint8_t*)R, Rb, Rs, d0 + r, j, rv, &ls, &s);
+        nvfp4_store_row<N, kSh>(v, (uint8_t*)R, Rb, Rs, d0 + r, j, rv, &ls, &s, copy_words<AT>(sr, row0 + d0 + r, j));
         if ((j & 7) == r) srow = s;
       } else if constexpr (kF8) {
         float s;
@@ -277,7 +279,7 @@ __global__ void __launch_bounds__(kThreads, 2) k_verify_heads(LaunchArgs a) {
   __syncthreads();
   if (!active) return;
   if (flush)
-    stream_anchor_flush<T, HT, P, N, AT>((AT*)a.state + soff,
+    stream_anchor_flush<T, HT, P, N, AT>(anchor_ptr<AT>(a, soff),
                                      std::is_same<HT, Nvfp4>::value ? (void*)((uint8_t*)a.read_copy + soff / 2)
                                                                     : (void*)((HT*)a.read_copy + soff),
                                      a.read_bscale + soff / 16, a.read_scale + ((size_t)slot * a.H + h) * P, c, yo,
@@ -365,6 +367,10 @@ bool heads_verify_supported(int P, int N, int Q, int T, int H, int G) {
 }
 
 cudaError_t heads_verify(const LaunchArgs& a, cudaStream_t s) {
+  if (a.anchor_shared) {   // the shared NVFP4 state: bf16 io, an NVFP4 copy (checked by the API)
+    if (a.io != ERS_DTYPE_BF16 || !a.read_nvfp4) return cudaErrorNotSupported;
+    return launch_verify_heads<__nv_bfloat16, Nvfp4, 16, Nvfp4Shared>(a, s);
+  }
   if (a.anchor_f16) {   // fp16 anchors: bf16 io only (checked by the API)
     if (a.io != ERS_DTYPE_BF16) return cudaErrorNotSupported;
     if (a.read_nvfp4) return launch_verify_heads<__nv_bfloat16, Nvfp4, 16, __half>(a, s);

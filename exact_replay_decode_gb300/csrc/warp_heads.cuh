@@ -206,10 +206,34 @@ __device__ __forceinline__ uint32_t e2m1x2(float lo, float hi) {   // two codes,
   return r & 0xFFu;
 }
 
+// Stochastic rounding of x to the e2m1 grid with the random word r: with lo the largest e2m1
+// magnitude <= |x| and step the spacing above it (0.5 below 2, 1 below 4, 2 below 6), |x| goes up to
+// lo + step iff r < 2^32 (|x| - lo) / step, else down to lo; |x| >= 6 gives 6; the sign is kept.
+// From the fp32 fields of |x| (m its bits without the sign): at or above 1 the step is the top
+// mantissa bit, so frac * 2^32 = (m & 0x3FFFFF) * 2^10 and r < that iff (r >> 10) < (m & 0x3FFFFF);
+// in [0.5, 1) lo = 0.5 and frac * 2^32 = (m & 0x7FFFFF) * 2^9; below 0.5 lo = 0 and frac * 2^32 =
+// |x| * 2^33 (exact, below 2^32), which r must be below the ceiling of.
+__device__ __forceinline__ float sr_e2m1(float x, uint32_t r) {
+  const uint32_t b = __float_as_uint(x), sign = b & 0x80000000u, m = b & 0x7FFFFFFFu;
+  uint32_t q;
+  if (m >= 0x40C00000u) {                 // |x| >= 6 (and NaN): 6
+    q = 0x40C00000u;
+  } else if (m >= 0x3F800000u) {          // [1, 6): lo has the top mantissa bit; the sum is a grid value
+    q = (m & ~0x3FFFFFu) + ((r >> 10) < (m & 0x3FFFFFu) ? 0x400000u : 0u);
+  } else if (m >= 0x3F000000u) {          // [0.5, 1): 0.5 or 1
+    q = (r >> 9) < (m & 0x7FFFFFu) ? 0x3F800000u : 0x3F000000u;
+  } else {                                // [0, 0.5): 0 or 0.5
+    q = r < __float2uint_ru(__fmul_rn(__uint_as_float(m), 8589934592.f)) ? 0x3F000000u : 0u;
+  }
+  return __uint_as_float(sign | q);
+}
+
 // Quantises the warp's row (lane quad v): returns lane j's 16 code bits; the block scale byte, its
-// value and the row scale in *bs, *beta, *scale.
+// value and the row scale in *bs, *beta, *scale.  kSR: the codes round stochastically (sr_e2m1 with
+// the words of rw, word e for value 4j + e) instead of to nearest; the scales are the same.
+template <bool kSR = false>
 __device__ __forceinline__ uint32_t nvfp4_quant_row(const float (&v)[4], int j, uint32_t* bs, float* beta,
-                                                    float* scale) {
+                                                    float* scale, uint4 rw = make_uint4(0u, 0u, 0u, 0u)) {
   float m = fmaxf(fmaxf(fabsf(v[0]), fabsf(v[1])), fmaxf(fabsf(v[2]), fabsf(v[3])));
   float mb = m;
 #pragma unroll
@@ -234,16 +258,26 @@ __device__ __forceinline__ uint32_t nvfp4_quant_row(const float (&v)[4], int j, 
   *beta = bv;
   if (bv == 0.f) return 0u;
   const float rho = __frcp_rn(bv);
-  return e2m1x2(__fmul_rn(u[0], rho), __fmul_rn(u[1], rho)) | (e2m1x2(__fmul_rn(u[2], rho), __fmul_rn(u[3], rho)) << 8);
+  float x[4];
+#pragma unroll
+  for (int e = 0; e < 4; ++e) x[e] = __fmul_rn(u[e], rho);
+  if constexpr (kSR) {
+    x[0] = sr_e2m1(x[0], rw.x);
+    x[1] = sr_e2m1(x[1], rw.y);
+    x[2] = sr_e2m1(x[2], rw.z);
+    x[3] = sr_e2m1(x[3], rw.w);
+  }
+  return e2m1x2(x[0], x[1]) | (e2m1x2(x[2], x[3]) << 8);
 }
 
 // Writes row d (lane quad v) of an NVFP4 copy; returns the code values (rv) and the block scale
 // (*beta) that a dot product reads, and the row scale in *scale.
-template <int N>
+template <int N, bool kSR = false>
 __device__ __forceinline__ void nvfp4_store_row(const float (&v)[4], uint8_t* C4, uint8_t* Bs, float* Rs, int d,
-                                                int j, float (&rv)[4], float* beta, float* scale) {
+                                                int j, float (&rv)[4], float* beta, float* scale,
+                                                uint4 rw = make_uint4(0u, 0u, 0u, 0u)) {
   uint32_t bs;
-  const uint32_t c = nvfp4_quant_row(v, j, &bs, beta, scale);
+  const uint32_t c = nvfp4_quant_row<kSR>(v, j, &bs, beta, scale, rw);
   *reinterpret_cast<uint16_t*>(C4 + (size_t)d * (N / 2) + 2 * j) = (uint16_t)c;
   if ((j & 3) == 0) Bs[(size_t)d * (N / 16) + (j >> 2)] = (uint8_t)bs;
   if (j == 0) Rs[d] = *scale;
@@ -298,6 +332,22 @@ __device__ __forceinline__ uint16_t sr_fp16_bits(float v, uint32_t r) {
   return sign | __half_as_ushort(__float2half_rn(q));   // q is on the fp16 grid: the conversion is exact
 }
 
+// ---- a shared NVFP4 state (ReplaySSM "Paper-reported results": the shared-FP4 recurrence mode) ------
+// The NVFP4 read copy is the only state: a refresh folds from its values (code * (beta * s) in fp32)
+// and writes it back with the NVFP4 cast, its codes rounded by sr_e2m1 with the words of counter
+// (nonce, slot, h * P + d, j).  The rows are read with coherent loads: the same launch rewrites them.
+struct Nvfp4Shared {};   // anchor tag: the anchor is the NVFP4 read copy itself
+
+template <int N>
+__device__ __forceinline__ float4 nvfp4_shared_ld(const uint8_t* C4, const uint8_t* Bs, const float* Rs, int d, int j) {
+  const uint32_t c = *reinterpret_cast<const uint16_t*>(C4 + (size_t)d * (N / 2) + 2 * j);
+  const uint32_t b = Bs[(size_t)d * (N / 16) + (j >> 2)];
+  float q[4], beta;
+  nvfp4_codes(c | (b << 16), q, &beta);
+  const float bs = __fmul_rn(beta, Rs[d]);
+  return make_float4(__fmul_rn(q[0], bs), __fmul_rn(q[1], bs), __fmul_rn(q[2], bs), __fmul_rn(q[3], bs));
+}
+
 // One lane's 4 anchor values of row d (offset o = d * N + 4j): fp32, or fp16 read exactly.
 template <typename AT>
 __device__ __forceinline__ float4 anchor_ld(const AT* H, size_t o) {
@@ -313,7 +363,9 @@ __device__ __forceinline__ float4 anchor_ld(const AT* H, size_t o) {
 // Stores them: fp32 as is, fp16 by stochastic rounding with the words of counter (row, j).
 template <typename AT>
 __device__ __forceinline__ void anchor_st(AT* H, size_t o, const float (&v)[4], const SrCtr& sr, uint32_t row, int j) {
-  if constexpr (std::is_same<AT, __half>::value) {
+  if constexpr (std::is_same<AT, Nvfp4Shared>::value) {
+    // nothing: the state is written by the copy's cast
+  } else if constexpr (std::is_same<AT, __half>::value) {
     const uint4 r = philox4x32_10(make_uint4(sr.nonce, sr.slot, row, (uint32_t)j), sr.k0, sr.k1);
     uint2 u;
     u.x = (uint32_t)sr_fp16_bits(v[0], r.x) | ((uint32_t)sr_fp16_bits(v[1], r.y) << 16);
@@ -321,6 +373,37 @@ __device__ __forceinline__ void anchor_st(AT* H, size_t o, const float (&v)[4], 
     *reinterpret_cast<uint2*>(H + o) = u;
   } else {
     *reinterpret_cast<float4*>(H + o) = make_float4(v[0], v[1], v[2], v[3]);
+  }
+}
+
+// Row d of the anchor as the fold reads it: fp32, fp16, or the shared NVFP4 state (R, Rb, Rs).
+template <typename AT, int N>
+__device__ __forceinline__ float4 anchor_row(const AT* Hd, const void* R, const uint8_t* Rb, const float* Rs, int d,
+                                             int j) {
+  if constexpr (std::is_same<AT, Nvfp4Shared>::value) {
+    return nvfp4_shared_ld<N>((const uint8_t*)R, Rb, Rs, d, j);
+  } else {
+    return anchor_ld<AT>(Hd, (size_t)d * N + 4 * j);
+  }
+}
+
+// The random words of a shared NVFP4 row write (zeros for the other anchors, which do not use them).
+template <typename AT>
+__device__ __forceinline__ uint4 copy_words(const SrCtr& sr, uint32_t row, int j) {
+  if constexpr (std::is_same<AT, Nvfp4Shared>::value) {
+    return philox4x32_10(make_uint4(sr.nonce, sr.slot, row, (uint32_t)j), sr.k0, sr.k1);
+  } else {
+    return make_uint4(0u, 0u, 0u, 0u);
+  }
+}
+
+// A head's anchor rows at element offset soff of the state (none for the shared NVFP4 state).
+template <typename AT>
+__device__ __forceinline__ AT* anchor_ptr(const LaunchArgs& a, size_t soff) {
+  if constexpr (std::is_same<AT, Nvfp4Shared>::value) {
+    return nullptr;
+  } else {
+    return reinterpret_cast<AT*>(a.state) + soff;
   }
 }
 

@@ -194,7 +194,10 @@ class ReplayCache:
 
     anchor "fp32": state [S,H,P,N] fp32.  anchor "fp16_sr" (ReplaySSM only): state [S,H,P,N] fp16,
     written by stochastic rounding with random words keyed by sr_key and the attribute sr_nonce,
-    which the caller sets to a fresh value before every call that may refresh anchors.
+    which the caller sets to a fresh value before every call that may refresh anchors.  anchor
+    "nvfp4_sr_shared" (ReplaySSM only, with an NVFP4 read copy): the read copy is the only state
+    (state is None), rewritten at refresh with stochastically rounded codes; seed() casts an fp32
+    state into it.
 
     paged=(page_rows, npages): the partial-chunk buffers are [npages, page_rows, ...] and
     buf_pages [S, chunk / page_rows] int32 maps each slot's logical pages to physical ones
@@ -207,8 +210,10 @@ class ReplayCache:
         if read_dtype not in ("bf16", "fp8", "nvfp4"):
             raise ValueError(f"read_dtype must be 'bf16', 'fp8' or 'nvfp4', got {read_dtype!r}")
         self.nslots, self.H, self.G, self.P, self.N, self.Q = nslots, nheads, ngroups, headdim, dstate, chunk
-        if anchor not in ("fp32", "fp16_sr"):
-            raise ValueError(f"anchor must be 'fp32' or 'fp16_sr', got {anchor!r}")
+        if anchor not in ("fp32", "fp16_sr", "nvfp4_sr_shared"):
+            raise ValueError(f"anchor must be 'fp32', 'fp16_sr' or 'nvfp4_sr_shared', got {anchor!r}")
+        if anchor == "nvfp4_sr_shared" and not (read_copy and read_dtype == "nvfp4"):
+            raise ValueError("anchor 'nvfp4_sr_shared' needs read_copy=True and read_dtype='nvfp4'")
         self.io = io_dtype
         self.read_dtype = read_dtype
         self.anchor = anchor
@@ -216,7 +221,8 @@ class ReplayCache:
         self.sr_nonce = 0
         z = dict(device=device)
         shp = (nslots, nheads, headdim, dstate)
-        self.state = torch.zeros(*shp, dtype=torch.float16 if anchor == "fp16_sr" else torch.float32, **z)
+        self.state = None if anchor == "nvfp4_sr_shared" else \
+            torch.zeros(*shp, dtype=torch.float16 if anchor == "fp16_sr" else torch.float32, **z)
         self.read_copy = None
         self.read_scale = None
         self.read_block_scale = None
@@ -256,11 +262,15 @@ class ReplayCache:
         return _dims(self.H, self.G, self.P, self.N, self.Q, self.io)
 
     def _c(self) -> _abi.Cache:
+        anc = {"fp32": _abi.ANCHOR_F32, "fp16_sr": _abi.ANCHOR_F16_SR,
+               "nvfp4_sr_shared": _abi.ANCHOR_NVFP4_SHARED_SR}[self.anchor]
+        return self._c_with(_ptr(self.state), anc)
+
+    def _c_with(self, state_ptr, anchor_code) -> _abi.Cache:
         rd = {"bf16": _abi.READ_BF16, "fp8": _abi.READ_FP8_E4M3, "nvfp4": _abi.READ_NVFP4}[self.read_dtype]
-        return _abi.Cache(self.state.data_ptr(), _ptr(self.read_copy), self.buf_x.data_ptr(), self.buf_dt.data_ptr(),
+        return _abi.Cache(state_ptr, _ptr(self.read_copy), self.buf_x.data_ptr(), self.buf_dt.data_ptr(),
                           self.buf_B.data_ptr(), self.buf_C.data_ptr(), self.pos.data_ptr(), self.nslots, rd,
-                          _ptr(self.read_scale), _ptr(self.read_block_scale),
-                          _abi.ANCHOR_F16_SR if self.anchor == "fp16_sr" else _abi.ANCHOR_F32,
+                          _ptr(self.read_scale), _ptr(self.read_block_scale), anchor_code,
                           (ctypes.c_uint32 * 2)(*self.sr_key), int(self.sr_nonce) & 0xFFFFFFFF,
                           _ptr(self.buf_pages), self.page_rows, self.npages)
 
@@ -279,9 +289,27 @@ class ReplayCache:
         beta = self.read_block_scale.view(torch.float8_e4m3fn).float().repeat_interleave(16, dim=-1)
         return q * beta * self.read_scale.unsqueeze(-1)
 
+    def seed(self, state: torch.Tensor, params: "LayerParams", nseq: Optional[int] = None,
+             slot: Optional[torch.Tensor] = None, stream=None) -> None:
+        """Casts an fp32 state [nslots,H,P,N] into the shared NVFP4 state of the listed slots (all by
+        default), rounding to nearest: the cast an fp32-anchor ReplaySSM refresh with an empty history
+        writes into its NVFP4 copy (ers_refresh with that state and anchor code ERS_ANCHOR_F32).  The
+        slots must have pos = 0."""
+        if self.anchor != "nvfp4_sr_shared":
+            raise ValueError("seed() is for the 'nvfp4_sr_shared' anchor")
+        _need(state, torch.float32, "state", (self.nslots, self.H, self.P, self.N))
+        S = self.nslots if nseq is None else nseq
+        st = Status(self.pos.device)
+        c = self._c_with(state.data_ptr(), _abi.ANCHOR_F32)
+        code = _abi.lib().ers_refresh(ctypes.byref(self.dims), ctypes.byref(params._c()), ctypes.byref(c), S,
+                                      _slot_arg(slot, S), _abi.FLAG_REPLAYSSM, self.Q + 1, _stream(stream),
+                                      _ptr(st.t))
+        _finish(code, "ers_refresh (seed)", st, True)
+
     def nbytes(self) -> int:
-        ts = [self.state, self.buf_x, self.buf_dt, self.buf_B, self.buf_C, self.pos]
-        ts += [t for t in (self.read_copy, self.read_scale, self.read_block_scale, self.buf_pages) if t is not None]
+        ts = [self.buf_x, self.buf_dt, self.buf_B, self.buf_C, self.pos]
+        ts += [t for t in (self.state, self.read_copy, self.read_scale, self.read_block_scale, self.buf_pages)
+               if t is not None]
         return sum(t.numel() * t.element_size() for t in ts)
 
 
@@ -349,7 +377,7 @@ def refresh(cache: ReplayCache, params: LayerParams, nseq: Optional[int] = None,
             stream=None) -> None:
     """Checkpoint refresh (ers_refresh): exact mode folds full chunks; ReplaySSM mode applies h + T > L."""
     S = cache.nslots if nseq is None else nseq
-    st = status if status is not None else (Status(cache.state.device) if check else None)
+    st = status if status is not None else (Status(cache.pos.device) if check else None)
     code = _abi.lib().ers_refresh(ctypes.byref(cache.dims), ctypes.byref(params._c()), ctypes.byref(cache._c()), S,
                                   _slot_arg(slot, S), _abi.FLAG_REPLAYSSM if replayssm else 0, int(drafts_T),
                                   _stream(stream), _ptr(st.t) if st else None)

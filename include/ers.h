@@ -100,8 +100,8 @@ typedef struct ers_params {
 } ers_params;
 
 /* Per-slot replay cache (exact-replay RFC section 3; ReplaySSM "Motivation and method").
- *   state     [nslots, H, P, N] fp32 (or fp16, see anchor_dtype): the boundary checkpoint (exact
- *             mode) or recurrence anchor (ReplaySSM)
+ *   state     [nslots, H, P, N] fp32 (or fp16, or unused, see anchor_dtype): the boundary checkpoint
+ *             (exact mode) or recurrence anchor (ReplaySSM)
  *   read_copy [nslots, H, P, N] or NULL: low-precision copy cast from the same fp32 values as `state`,
  *             bf16 (read_dtype ERS_READ_BF16) or FP8 e4m3 bytes (ERS_READ_FP8_E4M3)
  *   buf_x     [nslots, Q, H, P] io dtype;  buf_dt [nslots, Q, H] fp32 raw dt
@@ -149,8 +149,21 @@ typedef struct ers_params {
  * r = word n % 4 of Philox4x32-10(counter = (sr_nonce, s, h * P + d, n / 4), key = sr_key).  The
  * caller gives every call that may write anchors a fresh sr_nonce.  ReplaySSM mode only, bf16 io,
  * with a read copy, where the warp-per-head kernels run (headdim 64, dstate 128, chunk <= 16). */
+/* ERS_ANCHOR_NVFP4_SHARED_SR (ReplaySSM "Paper-reported results", the shared-FP4 recurrence mode; the
+ * rounding is this library's reading): the NVFP4 read copy is the only state and `state` is unused
+ * (may be NULL).  A refresh folds from the copy's values (code * (beta * s), fp32), then writes the
+ * copy with the NVFP4 cast above except that each code rounds stochastically: with x = u * (1 / beta)
+ * (as above), lo the largest e2m1 magnitude <= |x| and step the spacing above it (0.5 below 2, 1
+ * below 4, 2 below 6), |x| goes up to lo + step iff r < 2^32 (|x| - lo) / step, else down to lo;
+ * |x| >= 6 gives 6; the sign is kept; r as for fp16 anchors (word n % 4 of Philox4x32-10 at counter
+ * (sr_nonce, s, h * P + d, n / 4), key sr_key).  The scales are those of the round-to-nearest cast.
+ * A slot with pos == 0 is never rewritten (an empty history leaves the state as it is).  To start
+ * from an fp32 state, cast it with ers_refresh (ReplaySSM, pos = 0) on a cache with ERS_ANCHOR_F32,
+ * that state and the same NVFP4 copy, then use the copy with this mode.  ReplaySSM mode only, bf16
+ * io, an NVFP4 read copy, the warp-per-head shapes. */
 #define ERS_ANCHOR_F32 0
 #define ERS_ANCHOR_F16_SR 1
+#define ERS_ANCHOR_NVFP4_SHARED_SR 2
 
 typedef struct ers_cache {
   void* state;

@@ -197,15 +197,31 @@ def nvfp4_row_scale_exponent(amax: np.ndarray) -> np.ndarray:
     return np.where(a < 2.0 ** -126, -127, np.maximum(k, -127))
 
 
-def nvfp4_rows_round(a: np.ndarray, parts: bool = False):
+def sr_e2m1(v: np.ndarray, r: np.ndarray) -> np.ndarray:
+    """Stochastic rounding of fp32 values to the e2m1 grid with one random 32-bit word r per value:
+    with lo the largest e2m1 magnitude <= |v| and step the spacing above it (0.5 in [0, 2), 1 in
+    [2, 4), 2 in [4, 6)), |v| rounds up to lo + step iff r < 2^32 (|v| - lo) / step, else down to lo;
+    magnitudes at or above 6 give 6; the sign is kept.  Returned as fp32 values."""
+    f = np.asarray(v, dtype=np.float32).astype(np.float64)
+    a = np.abs(f)
+    step = np.where(a < 2.0, 0.5, np.where(a < 4.0, 1.0, 2.0))
+    lo = np.floor(a / step) * step
+    frac = (a - lo) / step                                    # exact, in [0, 1)
+    up = np.asarray(r, dtype=np.float64) < np.ldexp(frac, 32)
+    out = np.where(a >= E2M1_MAX, E2M1_MAX, lo + up * step)
+    return np.copysign(out, f).astype(np.float32)
+
+
+def nvfp4_rows_round(a: np.ndarray, parts: bool = False, words: Optional[np.ndarray] = None):
     """NVFP4 read copy of an fp32 state (the last axis is dstate, a multiple of 16): FP4 e2m1 codes
     in blocks of 16 consecutive values, each block with an e4m3 scale beta, each row with a
     power-of-two scale s = 2**k (k from nvfp4_row_scale_exponent):
         beta = e4m3(t / 6) with t = amax(|block|) / s (exact) and an fp32 division,
         q    = e2m1((v / s) * rho), rho = 1 / beta (fp32 reciprocal, fp32 product); q = 0 if beta = 0,
         value = q * beta * s (exact).
-    Input values are taken through fp32 as the GPU anchor is stored in fp32; returns fp64 values
-    (and, with parts=True, also q, beta and k)."""
+    With words (uint32, the shape of a), q rounds stochastically instead (sr_e2m1 with one word per
+    value); the scales are the same.  Input values are taken through fp32 as the GPU anchor is
+    stored in fp32; returns fp64 values (and, with parts=True, also q, beta and k)."""
     f = np.ascontiguousarray(a, dtype=np.float32).astype(np.float64)
     N = f.shape[-1]
     k = nvfp4_row_scale_exponent(np.max(np.abs(f), axis=-1, keepdims=True))
@@ -217,7 +233,11 @@ def nvfp4_rows_round(a: np.ndarray, parts: bool = False):
     with np.errstate(divide="ignore"):
         rho = np.where(beta > 0, np.float32(1.0) / np.where(beta > 0, beta, np.float32(1.0)), np.float32(0.0))
     y = (fb32 * rho.astype(np.float32)).astype(np.float32)
-    q = np.where(beta > 0, e2m1_round(y), np.float32(0.0))
+    if words is None:
+        q = np.where(beta > 0, e2m1_round(y), np.float32(0.0))
+    else:
+        wb = np.asarray(words).reshape(y.shape)
+        q = np.where(beta > 0, sr_e2m1(y, wb), np.float32(0.0))
     val = (q.astype(np.float64) * beta.astype(np.float64)).reshape(f.shape) * s
     if parts:
         return val, q.reshape(f.shape), beta[..., 0], k[..., 0]
@@ -287,6 +307,15 @@ def sr_fp16_anchor(fin: np.ndarray, key: Tuple[int, int], nonce: int, slot: int)
     through fp32, as the GPU folds in fp32) with the slot's random words for this nonce."""
     H, P, N = fin.shape
     return sr_fp16(np.asarray(fin, dtype=np.float64).astype(np.float32), sr_words(key, nonce, slot, H, P, N))
+
+
+def nvfp4_sr_state(fin: np.ndarray, key: Tuple[int, int], nonce: int, slot: int) -> np.ndarray:
+    """A shared NVFP4 state written by a refresh: the NVFP4 cast of the refreshed state fin [H, P, N]
+    (taken through fp32, as the GPU folds in fp32) with stochastically rounded codes, one word per
+    value from the slot's random words for this nonce (the counter layout of the fp16 anchors)."""
+    H, P, N = fin.shape
+    return nvfp4_rows_round(np.asarray(fin, dtype=np.float64).astype(np.float32),
+                            words=sr_words(key, nonce, slot, H, P, N))
 
 
 # ---- causal depthwise conv1d with a conv state (exact-replay RFC, Evidence item 6) -------------------
@@ -427,13 +456,16 @@ class ReplaySSMModel:
     """
 
     def __init__(self, params, anchor: np.ndarray, L: int, nthreads: Optional[int] = None, read_cast=None,
-                 anchor_round=None):
+                 anchor_round=None, shared: bool = False):
         self.A, self.D, self.dt_bias = (_f64(params.A), _f64(params.D), _f64(params.dt_bias))
         self.anchor = np.array(anchor, dtype=np.float64, copy=True)  # [S,H,P,N]
         self.read_cast = read_cast if read_cast is not None else bf16_round
         # anchor_round(i, fin) -> the stored anchor of sequence i after a refresh (default: fin itself)
         self.anchor_round = anchor_round
-        self.read = self.read_cast(self.anchor)
+        # shared: the stored anchor is also the read copy (one low-precision state; anchor_round
+        # gives it, and the initial anchor must already be in that format)
+        self.shared = shared
+        self.read = self.anchor.copy() if shared else self.read_cast(self.anchor)
         self.L = L
         self.nthreads = nthreads
         S = anchor.shape[0]
@@ -459,7 +491,7 @@ class ReplaySSMModel:
         _, fin = recurrence(x, dt, self.A, B, C, self.D, self.dt_bias, cu, self.anchor[which], self.nthreads)
         for k, i in enumerate(which):
             self.anchor[i] = fin[k] if self.anchor_round is None else self.anchor_round(i, fin[k])
-            self.read[i] = self.read_cast(fin[k])
+            self.read[i] = self.anchor[i] if self.shared else self.read_cast(fin[k])
             self.committed[i] = []
         self.flushes += len(which)
 

@@ -164,12 +164,38 @@ def test_validation_of_fp16_sr_anchors(lib):
         return lib.ers_replay_decode(ctypes.byref(d), ctypes.byref(p), ctypes.byref(c), 4, None, FAKE, FAKE, FAKE,
                                      FAKE, flags, FAKE, None, None)
 
-    assert dec(_dims(), cache(anchor=2)) == 3                                  # ERS_EDTYPE
+    assert dec(_dims(), cache(anchor=3)) == 3                                  # ERS_EDTYPE
     assert dec(_dims(), cache(), flags=0) == 12                                # exact mode
     assert dec(_dims(io_dtype=_abi.DTYPE_F32), cache()) == 12                  # fp32 io
     assert dec(_dims(chunk=32), cache()) == 12                                 # outside the warp-per-head shapes
     assert lib.ers_refresh(ctypes.byref(_dims()), ctypes.byref(p), ctypes.byref(cache(copy=0)), 4, None,
                            _abi.FLAG_REPLAYSSM, 1, None, None) == 12            # no read copy
+    assert lib.ers_chunked_prefill(ctypes.byref(_dims()), ctypes.byref(p), ctypes.byref(cache()), 1, 16, 16, FAKE,
+                                   None, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 1 << 40, None, None) == 12
+
+
+@needs_no_gpu
+def test_validation_of_shared_nvfp4_state(lib):
+    """The shared NVFP4 state (anchor code 2): state may be NULL; it needs an NVFP4 read copy, bf16 io,
+    ReplaySSM mode and the warp-per-head shapes, else ERS_EUNSUPPORTED before any launch; a NULL state
+    is still an error for the other anchors."""
+    from exact_replay_decode_gb300 import _abi
+    p = _prm()
+
+    def cache(anchor=_abi.ANCHOR_NVFP4_SHARED_SR, read_dtype=_abi.READ_NVFP4, state=0):
+        return _abi.Cache(state, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 4, read_dtype, FAKE, FAKE, anchor)
+
+    def dec(d, c, flags=_abi.FLAG_REPLAYSSM):
+        return lib.ers_replay_decode(ctypes.byref(d), ctypes.byref(p), ctypes.byref(c), 4, None, FAKE, FAKE, FAKE,
+                                     FAKE, flags, FAKE, None, None)
+
+    assert dec(_dims(), cache(), flags=0) == 12                                # exact mode: no fp32 state
+    assert dec(_dims(), cache(read_dtype=_abi.READ_BF16)) == 12                # the state is an NVFP4 copy
+    assert dec(_dims(), cache(read_dtype=_abi.READ_FP8_E4M3)) == 12
+    assert dec(_dims(io_dtype=_abi.DTYPE_F32), cache()) == 12                  # bf16 io only
+    assert dec(_dims(chunk=32), cache()) == 12
+    assert dec(_dims(), cache(anchor=_abi.ANCHOR_F32)) == 1                    # NULL state elsewhere
+    assert dec(_dims(), cache(anchor=_abi.ANCHOR_F16_SR)) == 1
     assert lib.ers_chunked_prefill(ctypes.byref(_dims()), ctypes.byref(p), ctypes.byref(cache()), 1, 16, 16, FAKE,
                                    None, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 1 << 40, None, None) == 12
 

@@ -536,6 +536,94 @@ def test_sr_fp16_is_unbiased():
     assert abs(mean - float(v)) <= 2.0 ** -10 / 4096
 
 
+def test_sr_e2m1_decisions():
+    """Stochastic rounding onto the e2m1 grid, worked by hand: the spacing above lo is 0.5 below 2,
+    1 below 4 and 2 below 6; |v| goes up iff r < 2^32 (|v| - lo) / step."""
+    sr = lambda v, r: float(oracle.sr_e2m1(np.float32(v), np.uint32(r)))
+    assert sr(0.75, 2 ** 31 - 1) == 1.0 and sr(0.75, 2 ** 31) == 0.5          # half-way in [0.5, 1]
+    assert sr(5.0, 2 ** 31 - 1) == 6.0 and sr(5.0, 2 ** 31) == 4.0            # half-way in [4, 6]
+    assert sr(-2.5, 0) == -3.0 and sr(-2.5, 2 ** 32 - 1) == -2.0               # sign kept
+    # fp32(0.1) = 13421773 * 2^-27: (|v| - 0) / 0.5 * 2^32 = 13421773 * 64 = 858993472 exactly
+    assert sr(0.1, 858993471) == 0.5 and sr(0.1, 858993472) == 0.0
+    # 3.25 in [3, 4): a quarter of the way; 1.75 in [1.5, 2): half-way
+    assert sr(3.25, 2 ** 30 - 1) == 4.0 and sr(3.25, 2 ** 30) == 3.0
+    assert sr(1.75, 2 ** 31 - 1) == 2.0 and sr(1.75, 2 ** 31) == 1.5
+    # saturation at 6 for any word
+    for r in (0, 2 ** 31, 2 ** 32 - 1):
+        assert sr(6.5, r) == 6.0 and sr(-100.0, r) == -6.0 and sr(5.99, 0) == 6.0
+    # every grid value stays where it is for any word
+    grid = np.array([0, 0.5, 1, 1.5, 2, 3, 4, 6], np.float32)
+    grid = np.concatenate([grid, -grid[1:]])
+    for r in (0, 1, 2 ** 31, 2 ** 32 - 1):
+        assert np.array_equal(oracle.sr_e2m1(grid, np.full(grid.shape, r, np.uint32)), grid)
+
+
+def test_sr_e2m1_is_round_to_nearest_at_mid_word_and_unbiased():
+    rng = np.random.Generator(np.random.PCG64(13))
+    v = rng.uniform(-6.5, 6.5, 20000).astype(np.float32)
+    a = np.abs(v.astype(np.float64))
+    step = np.where(a < 2, 0.5, np.where(a < 4, 1.0, 2.0))
+    frac = (a - np.floor(a / step) * step) / step
+    away = (np.abs(frac - 0.5) > 2.0 ** -20) | (a >= 6)
+    # with r = 2^31 - 1 the rule goes up exactly when frac > 1/2 - 2^-32: round to nearest off ties
+    got = oracle.sr_e2m1(v, np.full(v.shape, 2 ** 31 - 1, np.uint32))
+    assert np.array_equal(got[away], oracle.e2m1_round(v)[away])
+    # averaged over the 2^16 evenly spaced words k * 2^16, values on a step / 2^16 lattice come back
+    # exactly (the count of words below frac * 2^32 is frac * 2^16)
+    rs = (np.arange(2 ** 16, dtype=np.uint64) << np.uint64(16)).astype(np.uint32)
+    for x in (0.3 - 0.3 % 2.0 ** -17, 2.0 + 0.7 - 0.7 % 2.0 ** -16, -(4.0 + 1.3 - 1.3 % 2.0 ** -15), 0.0):
+        m = oracle.sr_e2m1(np.full(rs.shape, x, np.float32), rs).astype(np.float64).mean()
+        assert m == x, (x, m)
+
+
+def test_nvfp4_sr_cast_keeps_the_scales_and_brackets_each_value():
+    """The stochastic NVFP4 cast has the round-to-nearest cast's row and block scales; each code is
+    one of the two e2m1 neighbours of the scaled value; with every word 2^31 - 1 it is the
+    round-to-nearest cast (ties aside); the words follow the anchor counter layout."""
+    rng = np.random.Generator(np.random.PCG64(14))
+    a = rng.standard_normal((2, 3, 8, 64)) * np.exp(rng.uniform(-6, 6, (2, 3, 8, 1)))
+    words = rng.integers(0, 2 ** 32, a.shape, dtype=np.uint64).astype(np.uint32)
+    r0, q0, b0, k0 = oracle.nvfp4_rows_round(a, parts=True)
+    r1, q1, b1, k1 = oracle.nvfp4_rows_round(a, parts=True, words=words)
+    assert np.array_equal(b0, b1) and np.array_equal(k0, k1)
+    assert np.array_equal(oracle.e2m1_round(q1), q1)
+    lo = oracle.nvfp4_rows_round(a, parts=True, words=np.full(a.shape, 2 ** 32 - 1, np.uint32))[1]
+    hi = oracle.nvfp4_rows_round(a, parts=True, words=np.zeros(a.shape, np.uint32))[1]
+    assert np.all((q1 == lo) | (q1 == hi)) and np.all(np.abs(hi) >= np.abs(lo))
+    assert np.mean(q1 != q0) > 0.2                                                  # rounding did vary
+    mid = oracle.nvfp4_rows_round(a, words=np.full(a.shape, 2 ** 31 - 1, np.uint32))
+    assert np.mean(mid != r0) < 1e-3
+    st = rng.standard_normal((2, 4, 32))
+    got = oracle.nvfp4_sr_state(st, (3, 4), 11, 6)
+    assert np.array_equal(got, oracle.nvfp4_rows_round(st, words=oracle.sr_words((3, 4), 11, 6, 2, 4, 32)))
+
+
+def test_protocol_shared_state_model():
+    """A shared state: the read copy is the stored anchor itself after every refresh; an empty history
+    (zero acceptance) never changes it; with an exact (identity) rounding the model is the fp32-anchor
+    model with an fp64 read copy."""
+    params, anchor, drafts, acc, L = _protocol_case(18, steps=12, N=32)
+    key = (5, 6)
+    nonce = {"v": 0}
+    a0 = oracle.nvfp4_rows_round(anchor)
+    m = oracle.ReplaySSMModel(params, a0, L, shared=True,
+                              anchor_round=lambda i, fin: oracle.nvfp4_sr_state(fin, key, nonce["v"], i))
+    m0 = oracle.ReplaySSMModel(params, a0, L, shared=True,
+                               anchor_round=lambda i, fin: oracle.nvfp4_sr_state(fin, key, nonce["v"], i))
+    for k in range(len(drafts)):
+        nonce["v"] = 100 + k
+        m.verify(drafts[k]); m.commit(acc[k])
+        m0.verify(drafts[k]); m0.commit([0] * len(acc[k]))
+        assert np.array_equal(m.read, m.anchor)
+    assert m.flushes > 0 and m0.flushes == 0 and np.array_equal(m0.anchor, a0)
+    ident = oracle.ReplaySSMModel(params, anchor, L, shared=True, anchor_round=lambda i, fin: fin)
+    ref = oracle.ReplaySSMModel(params, anchor, L, read_cast=lambda x: np.asarray(x, dtype=np.float64))
+    for k in range(len(drafts)):
+        assert np.array_equal(ident.verify(drafts[k]), ref.verify(drafts[k]))
+        ident.commit(acc[k]); ref.commit(acc[k])
+    assert np.array_equal(ident.anchor, ref.anchor)
+
+
 def test_protocol_anchor_independent_of_fp8_read_copy():
     """The fp32 anchor is the same whether outputs read a bf16, an FP8 or an NVFP4 copy."""
     params, anchor, drafts, acc, L = _protocol_case(17, steps=12, N=32)   # two 16-value blocks per row
