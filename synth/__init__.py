@@ -196,9 +196,10 @@ def exact_fold_inputs(seed: int, S: int, K: int, dims: Dims):
     """Inputs whose refresh folds are exact in fp32 (and fp64): A = 0 and dt_bias = 0, raw dt = 40
     (softplus passes large arguments through, so every step's weight is 40 and every decay 1), x in
     {k / 8 : |k| <= 16}, B in {k / 4 : |k| <= 8}, C and D ~ N(0, 1).  Every weighted product is then a
-    multiple of 1/4 below 2^8, and a fold over at most 16 records stays exact (24 bits) for states
-    whose values are multiples of 2^-12 below 2^12.  Returns (params, stream [K*S rows], initial fp32 state
-    [S, H, P, N] ~ N(0, 1))."""
+    multiple of 1/4 below 2^8, so a fold over at most 16 records adds less than 2^12 and the state
+    stays exact in fp32 (24 bits) while its values are multiples of 2^-8 below 2^15: the initial state
+    is N(0, 1) rounded to multiples of 2^-8.  Returns (params, stream [K*S rows], initial fp32 state
+    [S, H, P, N])."""
     rng = np.random.Generator(np.random.PCG64(seed))
     H, G, P, N = dims.nheads, dims.ngroups, dims.headdim, dims.dstate
     params = Params(np.zeros(H, np.float32), rng.standard_normal(H).astype(np.float32), np.zeros(H, np.float32))
@@ -207,7 +208,7 @@ def exact_fold_inputs(seed: int, S: int, K: int, dims: Dims):
     dt = np.full((T, H), 40.0, np.float32)
     B = (rng.integers(-8, 9, (T, G, N)) / 4.0).astype(np.float32)
     C = round_bf16(rng.standard_normal((T, G, N)).astype(np.float32))
-    state = rng.standard_normal((S, H, P, N)).astype(np.float32)
+    state = (np.round(rng.standard_normal((S, H, P, N)) * 256.0) / 256.0).astype(np.float32)
     return params, Tokens(x, dt, B, C, True), state
 
 

@@ -61,46 +61,46 @@ def test_fp8_cast_untouched_without_flush():
     assert int((cache.read_copy != 0x5A).sum()) == 0 and bool((cache.read_scale == 2.0).all())
 
 
-def _exact_mode_cache(w, S, K, seed, read_dtype):
+def _exact_mode_cache(S, K, seed, read_dtype, dims=synth.Dims(64, 8, 64, 128, 16)):
+    """An exact-mode cache at position 0 holding an fp32 checkpoint, with exact-fold tokens (A = 0,
+    dt far above softplus's pass-through, dyadic x and B): every refresh rounds one exact sum to fp32,
+    as the oracle's fold taken through fp32 does."""
     ers = _ers()
-    d = w.dims
-    params, hist, _, stream = synth.decode_inputs(w, seed=seed, batch=S, steps=K)
+    params, stream, st0 = synth.exact_fold_inputs(seed, S, K, dims)
     prm = layer(params)
-    cache = ers.ReplayCache(S, d.nheads, d.ngroups, d.headdim, d.dstate, d.chunk, torch.bfloat16, read_copy=True,
-                            read_dtype=read_dtype)
-    htoks = synth.Tokens.concat(hist)
-    cu = torch.tensor(np.concatenate([[0], np.cumsum([h.ntokens for h in hist])]), dtype=torch.int32, device=dev())
-    hx, hdt, hB, hC = torch_io.tokens_to(htoks, dev())
-    ers.chunked_prefill(cache, prm, hx, hdt, hB, hC, cu)
-    return prm, cache, torch_io.tokens_to(stream, dev(), lead=(K, S))
+    cache = ers.ReplayCache(S, dims.nheads, dims.ngroups, dims.headdim, dims.dstate, dims.chunk, torch.bfloat16,
+                            read_copy=True, read_dtype=read_dtype)
+    cache.state.copy_(torch.from_numpy(st0))
+    return params, prm, cache, stream, st0, torch_io.tokens_to(stream, dev(), lead=(K, S))
 
 
 def test_fp8_exact_mode_fused_refresh_casts_and_matches_separate():
-    """Exact-mode decode keeps an FP8 copy: after every step the slots that filled a chunk hold
-    the FP8 rounding of their new checkpoint; fused and separate refresh agree bit for bit; the
-    outputs (which read the fp32 checkpoint) equal those of a run with a bf16 copy."""
+    """Exact-mode decode keeps an FP8 copy: every checkpoint a filled chunk writes equals the oracle's
+    fold (value for value) and the copy its FP8 rounding; fused and separate refresh agree bit for
+    bit; the outputs (which read the fp32 checkpoint) equal those of a run with a bf16 copy."""
     ers = _ers()
-    w = synth.workload("decode_b256_h64")
-    S, K = 24, 40
-    prm, c1, (sx, sdt, sB, sC) = _exact_mode_cache(w, S, K, 3, "fp8")
-    _, c2, _ = _exact_mode_cache(w, S, K, 3, "fp8")
-    _, c3, _ = _exact_mode_cache(w, S, K, 3, "bf16")
+    S, K, Q = 24, 40, 16
+    params, prm, c1, stream, st0, (sx, sdt, sB, sC) = _exact_mode_cache(S, K, 3, "fp8")
+    c2 = _exact_mode_cache(S, K, 3, "fp8")[2]
+    c3 = _exact_mode_cache(S, K, 3, "bf16")[2]
+    ck = st0.astype(np.float64)
     casts = 0
     for k in range(K):
-        before = c1.pos.clone()
         y1 = ers.replay_decode(c1, prm, sx[k], sdt[k], sB[k], sC[k], fuse_refresh=True)
         y2 = ers.replay_decode(c2, prm, sx[k], sdt[k], sB[k], sC[k], fuse_refresh=False)
         ers.refresh(c2, prm)
         y3 = ers.replay_decode(c3, prm, sx[k], sdt[k], sB[k], sC[k], fuse_refresh=True)
         assert same_bits(y1, y2) and same_bits(y1, y3), k
         assert torch.equal(c1.read_copy, c2.read_copy) and same_bits(c1.read_scale, c2.read_scale), k
-        filled = (before == w.dims.chunk - 1).nonzero().flatten().tolist()
-        if filled:
-            st = c1.state[filled].cpu().numpy()
-            want = oracle.fp8_rows_round(st).astype(np.float32)
-            got = c1.read_values()[filled].cpu().numpy()
-            assert np.array_equal(got.view(np.uint32), want.view(np.uint32)), k
-            casts += len(filled)
+        if (k + 1) % Q == 0:                            # every slot filled its chunk at this step
+            r = (np.arange(k + 1 - Q, k + 1)[None, :] * S + np.arange(S)[:, None]).ravel()   # slot-major rows
+            _, ck = oracle.recurrence(stream.x[r], stream.dt[r], params.A, stream.B[r], stream.C[r], params.D,
+                                      params.dt_bias, np.arange(0, S * Q + 1, Q), ck)
+            want = ck.astype(np.float32)
+            assert np.array_equal(c1.state.cpu().numpy().view(np.uint32), want.view(np.uint32)), k
+            got = c1.read_values().cpu().numpy()
+            assert np.array_equal(got.view(np.uint32), oracle.fp8_rows_round(ck).astype(np.float32).view(np.uint32))
+            casts += S
     assert casts > 0
     assert same_bits(c1.state, c3.state) and torch.equal(c1.pos, c3.pos)
 
@@ -127,8 +127,8 @@ def _verify_run(w, S, K, seed, read_dtype):
 @pytest.mark.parametrize("read_dtype", ["fp8", "nvfp4"])
 def test_verify_equals_nonspec_decode_and_oracle(read_dtype):
     """Verify + commit with an FP8 / NVFP4 copy: accepted drafts equal non-speculative ReplaySSM
-    decode over the same committed stream bit for bit, flushes recast the copy exactly as the oracle
-    rounds the anchor, and outputs match the oracle's protocol model run with the same read cast."""
+    decode over the same committed stream bit for bit, and outputs match the oracle's protocol model
+    run with the same read cast."""
     ers = _ers()
     w = synth.workload("verify_b512_t4")
     S, K, T, L = 64, 24, w.drafts, w.dims.chunk
@@ -145,11 +145,7 @@ def test_verify_equals_nonspec_decode_and_oracle(read_dtype):
     for k in range(K):
         flushing = ((cache.pos + T) > L).nonzero().flatten().tolist()
         y = ers.spec_verify(cache, prm, dx[k], ddt[k], dB[k], dC[k])
-        if flushing:
-            want = _CAST[read_dtype](cache.state[flushing].cpu().numpy()).astype(np.float32)
-            got = cache.read_values()[flushing].cpu().numpy()
-            assert np.array_equal(got.view(np.uint32), want.view(np.uint32)), k
-            flushes += len(flushing)
+        flushes += len(flushing)
         ers.commit(cache, acc_t[k], T)
         ers.refresh(ref, prm, replayssm=True, drafts_T=T)
         a = acc[k]
@@ -174,6 +170,37 @@ def test_verify_equals_nonspec_decode_and_oracle(read_dtype):
     assert torch.equal(cache.read_copy, ref.read_copy) and same_bits(cache.read_scale, ref.read_scale)
     if read_dtype == "nvfp4":
         assert torch.equal(cache.read_block_scale, ref.read_block_scale)
+
+
+@pytest.mark.parametrize("read_dtype", ["fp8", "nvfp4"])
+def test_verify_flush_casts_equal_the_oracle_under_exact_folds(read_dtype):
+    """Verify + commit with exact-fold drafts: after every step the anchors equal the oracle model's
+    and the copies its FP8 / NVFP4 rounding of them, value for value."""
+    ers = _ers()
+    d = synth.Dims(64, 8, 64, 128, 16)
+    S, K, T, L = 16, 14, 4, d.chunk
+    params, stream, st0 = synth.exact_fold_inputs(21, S, K * T, d)
+    prm = layer(params)
+    acc = np.random.Generator(np.random.PCG64(22)).integers(0, T + 1, (K, S)).astype(np.int32)
+    cache = ers.ReplayCache(S, d.nheads, d.ngroups, d.headdim, d.dstate, L, torch.bfloat16, read_copy=True,
+                            read_dtype=read_dtype)
+    cache.state.copy_(torch.from_numpy(st0))
+    ers.refresh(cache, prm, replayssm=True, drafts_T=L + 1)
+    model = oracle.ReplaySSMModel(params, st0.astype(np.float64), L, read_cast=_CAST[read_dtype])
+    sh = lambda a: a.reshape(K, S, T, *a.shape[1:])
+    dx, ddt, dB, dC = (torch.from_numpy(sh(a)).to(dev()) for a in (stream.x, stream.dt, stream.B, stream.C))
+    dx, dB, dC = dx.to(torch.bfloat16), dB.to(torch.bfloat16), dC.to(torch.bfloat16)
+    acc_t = torch.from_numpy(acc).to(dev())
+    flushes = 0
+    for k in range(K):
+        ers.spec_verify(cache, prm, dx[k], ddt[k], dB[k], dC[k])
+        ers.commit(cache, acc_t[k], T)
+        model.verify([tuple(sh(a)[k, i] for a in (stream.x, stream.dt, stream.B, stream.C)) for i in range(S)])
+        model.commit(acc[k])
+        assert np.array_equal(cache.state.cpu().numpy().view(np.uint32),
+                              model.anchor.astype(np.float32).view(np.uint32)), k
+        assert np.array_equal(cache.read_values().cpu().numpy().astype(np.float64), model.read), k
+    assert model.flushes > 0
 
 
 def test_anchor_independent_of_read_precision():

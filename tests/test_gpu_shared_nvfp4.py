@@ -83,11 +83,11 @@ def test_fused_flush_equals_refresh_and_decode_and_matches_the_model():
     params, hist, _, stream = synth.decode_inputs(w, seed=82, batch=S, steps=K)
     prm = layer(params)
     ht = synth.Tokens.concat(hist)
-    cu = torch.tensor(np.concatenate([[0], np.cumsum([h.ntokens for h in hist])]), dtype=torch.int32, device=dev())
-    hx, hdt, hB, hC = torch_io.tokens_to(ht, dev())
-    _, fin = ers.ssd_scan_fwd(hx, hdt, prm, hB, hC, chunk=L, cu_seqlens=cu)
-    c1, c2 = _shared(ers, S, DIMS, prm, fin), _shared(ers, S, DIMS, prm, fin)
-    a0 = oracle.nvfp4_rows_round(fin.cpu().numpy()[samples])
+    cu = np.concatenate([[0], np.cumsum([h.ntokens for h in hist])])
+    _, fin = oracle.recurrence(ht.x, ht.dt, params.A, ht.B, ht.C, params.D, params.dt_bias, cu)
+    fin32 = fin.astype(np.float32)                     # the oracle's state after the history starts both
+    c1, c2 = (_shared(ers, S, DIMS, prm, torch.from_numpy(fin32).to(dev())) for _ in range(2))
+    a0 = oracle.nvfp4_rows_round(fin32[samples])
     assert np.array_equal(c1.read_values()[samples].cpu().numpy().astype(np.float64), a0)
     nonce = {"v": 0}
     model = oracle.ReplaySSMModel(params, a0, L, shared=True,

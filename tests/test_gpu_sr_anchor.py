@@ -2,9 +2,10 @@
 "NVFP4 read / FP16+SR recurrence"; the rounding rule and the random words are this library's
 reading: Philox4x32-10 at counter (nonce, slot, h * P + d, n / 4)).
 
-* An anchor write equals the oracle's stochastic rounding of the fp32 refresh result, bit for bit:
-  the same refresh on an fp32-anchor cache holding the same (fp16) values yields that fp32 result,
-  and both caches cast the same read copy from it.
+* Anchor writes equal the oracle's, value for value, under exact folds (A = 0, dt far above
+  softplus's pass-through, dyadic x and B, so both sides round the same exact sum once to fp32),
+  across the fp16 range (subnormals, smallest normals, saturation); the read copy cast from the
+  same values equals the oracle's too.
 * Fused flush in decode == ers_refresh + decode, verify == non-speculative decode, bit for bit, with
   fp16 anchors and an NVFP4 copy (the paper's tp4_hi16_sr configuration).
 * Parity with the oracle's protocol model run with the same rounding (anchors within a few fp16
@@ -42,49 +43,84 @@ def _anchor_err(got: torch.Tensor, ref: np.ndarray) -> float:
     return float((d / np.maximum(r, 1e-30)).max())
 
 
+def _oracle_start(params, hist) -> np.ndarray:
+    """The oracle's state after each sequence's history (fp64 [S, H, P, N]): the starting anchor of
+    both the oracle model and the caches (which get its fp16 cast)."""
+    ht = synth.Tokens.concat(hist)
+    cu = np.concatenate([[0], np.cumsum([h.ntokens for h in hist])])
+    _, fin = oracle.recurrence(ht.x, ht.dt, params.A, ht.B, ht.C, params.D, params.dt_bias, cu)
+    return fin
+
+
 def _setup(S, K, seed, read_dtype, anchor, dims=synth.Dims(64, 8, 64, 128, 16)):
     ers = _ers()
     w = dataclasses.replace(synth.workload("decode_b256_h64"), dims=dims)
     d, L = w.dims, w.dims.chunk
     params, hist, h0, stream = synth.decode_inputs(w, seed=seed, batch=S, steps=K)
     prm = layer(params)
-    ht = synth.Tokens.concat(hist)
-    lens = [h.ntokens for h in hist]
-    cu = torch.tensor(np.concatenate([[0], np.cumsum(lens)]), dtype=torch.int32, device=dev())
-    _, fin = ers.ssd_scan_fwd(*torch_io.tokens_to(ht, dev())[:2], prm, *torch_io.tokens_to(ht, dev())[2:], chunk=L,
-                              cu_seqlens=cu)
-    fin16 = fin.half()                                          # the anchor starts on the fp16 grid
+    st16 = _oracle_start(params, hist).astype(np.float32).astype(np.float16)   # on the fp16 grid
 
     def fresh(anc=anchor):
         c = ers.ReplayCache(S, d.nheads, d.ngroups, d.headdim, d.dstate, L, torch.bfloat16, read_copy=True,
                             read_dtype=read_dtype, anchor=anc, sr_key=KEY)
-        c.state.copy_(fin16 if anc == "fp16_sr" else fin16.float())
+        c.state.copy_(torch.from_numpy(st16 if anc == "fp16_sr" else st16.astype(np.float32)))
         ers.refresh(c, prm, replayssm=True, drafts_T=L + 1)    # h = 0: the anchor keeps its bits
         return c
-    starts = np.concatenate([[0], np.cumsum(lens)])
-    return params, prm, ht, starts, stream, torch_io.tokens_to(stream, dev(), lead=(K, S)), fin16, fresh
+    return params, prm, stream, torch_io.tokens_to(stream, dev(), lead=(K, S)), st16, fresh
+
+
+def _exact_model(params, anchor0, L, read_dtype, nonce):
+    cast = oracle.nvfp4_rows_round if read_dtype == "nvfp4" else oracle.bf16_round
+    return oracle.ReplaySSMModel(params, anchor0, L, read_cast=cast,
+                                 anchor_round=lambda i, fin: oracle.sr_fp16_anchor(fin, KEY, nonce, i))
+
+
+def _run_exact(ers, params, stream, st16, S, K, read_dtype, nonce):
+    """K decodes of every slot from the fp16 anchor st16, then a refresh of every slot; returns the
+    cache and the oracle model run over the same records (the fold is exact on both sides, so the
+    stochastic rounding sees the same fp32 values)."""
+    d, L = DIMS, DIMS.chunk
+    prm = layer(params)
+    c = ers.ReplayCache(S, d.nheads, d.ngroups, d.headdim, d.dstate, L, torch.bfloat16, read_copy=True,
+                        read_dtype=read_dtype, anchor="fp16_sr", sr_key=KEY)
+    c.state.copy_(st16)
+    ers.refresh(c, prm, replayssm=True, drafts_T=L + 1)        # h = 0: the anchor keeps its bits
+    model = _exact_model(params, st16.float().cpu().numpy().astype(np.float64), L, read_dtype, nonce)
+    tok = torch_io.tokens_to(stream, dev(), lead=(K, S))
+    for k in range(K):
+        ers.replay_decode(c, prm, *(t[k] for t in tok), replayssm=True, fuse_refresh=False)
+        model.verify([(stream.x[r:r + 1], stream.dt[r:r + 1], stream.B[r:r + 1], stream.C[r:r + 1])
+                      for r in range(k * S, (k + 1) * S)])
+        model.commit([1] * S)
+    c.sr_nonce = nonce
+    ers.refresh(c, prm, replayssm=True, drafts_T=L)            # h + L > L: every slot folds
+    model.refresh(list(range(S)))
+    return c, model
+
+
+DIMS = synth.Dims(64, 8, 64, 128, 16)
 
 
 @pytest.mark.parametrize("read_dtype", ["bf16", "nvfp4"])
 def test_sr_anchor_write_matches_oracle(read_dtype):
+    """Exact folds (A = 0, dt far above softplus's pass-through, dyadic x and B): the fp32 value each
+    rounding sees is the single rounding of an exact sum on both sides, so the fp16 anchor and the
+    read copy equal the oracle's, value for value."""
     ers = _ers()
-    S, K = 12, 9
-    params, prm, _, _, _, tok, fin16, fresh = _setup(S, K, 31, read_dtype, "fp16_sr")
-    c16, c32 = fresh("fp16_sr"), fresh("fp32")
-    assert same_bits(c16.state, fin16)
-    assert torch.equal(c16.read_copy.view(torch.uint8), c32.read_copy.view(torch.uint8))
-    for k in range(K):                                          # K < L committed records, no flush
-        y16 = ers.replay_decode(c16, prm, *(t[k] for t in tok), replayssm=True, fuse_refresh=False)
-        y32 = ers.replay_decode(c32, prm, *(t[k] for t in tok), replayssm=True, fuse_refresh=False)
-        assert same_bits(y16, y32)
-    for c in (c16, c32):
-        c.sr_nonce = 77
-        ers.refresh(c, prm, replayssm=True, drafts_T=16)        # K + 16 > L: every slot flushes
-    want = np.stack([oracle.sr_fp16_anchor(c32.state[i].cpu().numpy(), KEY, 77, i) for i in range(S)])
-    got = c16.state.float().cpu().numpy().astype(np.float64)
-    assert np.array_equal(got, want)
-    assert torch.equal(c16.read_copy.view(torch.uint8), c32.read_copy.view(torch.uint8))
-    moved = np.abs(got - c32.state.cpu().numpy().astype(np.float64)) > 0
+    S, K = 6, 9
+    params, stream, st0 = synth.exact_fold_inputs(31, S, K, DIMS)
+    st16 = torch.from_numpy(st0.astype(np.float16)).to(dev())
+    c, model = _run_exact(ers, params, stream, st16, S, K, read_dtype, 77)
+    got = c.state.float().cpu().numpy().astype(np.float64)
+    assert np.array_equal(got, model.anchor)
+    assert np.array_equal(c.read_values().cpu().numpy().astype(np.float64), model.read)
+    plain = oracle.ReplaySSMModel(params, st16.float().cpu().numpy().astype(np.float64), DIMS.chunk)
+    for k in range(K):
+        plain.verify([(stream.x[r:r + 1], stream.dt[r:r + 1], stream.B[r:r + 1], stream.C[r:r + 1])
+                      for r in range(k * S, (k + 1) * S)])
+        plain.commit([1] * S)
+    plain.refresh(list(range(S)))
+    moved = got != plain.anchor.astype(np.float32).astype(np.float64)
     assert moved.mean() > 0.5                                   # rounding did happen
 
 
@@ -94,9 +130,9 @@ def test_fused_flush_and_verify_with_sr_anchors():
     ers = _ers()
     S, K, L = 32, 40, 16
     samples = [0, 9, 31]
-    params, prm, ht, starts, stream, tok, fin16, fresh = _setup(S, K, 32, "nvfp4", "fp16_sr")
+    params, prm, stream, tok, st16, fresh = _setup(S, K, 32, "nvfp4", "fp16_sr")
     c1, c2 = fresh(), fresh()
-    anchor0 = fin16.float().cpu().numpy().astype(np.float64)[samples]
+    anchor0 = st16.astype(np.float64)[samples]
     nonce = {"v": 0}
     model = oracle.ReplaySSMModel(params, anchor0, L, read_cast=oracle.nvfp4_rows_round,
                                   anchor_round=lambda i, fin: oracle.sr_fp16_anchor(fin, KEY, nonce["v"],
@@ -179,37 +215,24 @@ def test_sr_anchor_unsupported_calls_raise():
 
 
 def test_sr_anchor_write_edge_values():
-    """Anchors spanning the fp16 range (subnormals, the smallest normals, values near 65504): with
-    x = 0 the refresh result is decay * S, so the rounding sees values across every range; the fp16
-    write equals the oracle's rounding of the fp32-anchor cache's result bit for bit."""
+    """Anchors spanning the fp16 range (subnormals, the smallest normals, values near 65504) under
+    exact folds whose increments are scaled per head to the anchor's own spacing (x times 2^-27 on
+    the subnormal head, 2^-17 on the smallest normals): the fp16 writes equal the oracle's rounding,
+    value for value, on every path (subnormal, normal, saturation)."""
     ers = _ers()
-    S, K, L, H, G, P, N = 6, 5, 16, 64, 8, 64, 128
-    w = synth.workload("decode_b256_h64")
-    params, _, _, stream = synth.decode_inputs(w, seed=34, batch=S, steps=K)
-    prm = layer(params)
-    stream.x[:] = 0
-    tok = torch_io.tokens_to(stream, dev(), lead=(K, S))
+    S, K, H, P, N = 6, 5, 64, 64, 128
+    params, stream, _ = synth.exact_fold_inputs(34, S, K, DIMS)
+    stream.x[:, 1] *= np.float32(2.0 ** -27)
+    stream.x[:, 2] *= np.float32(2.0 ** -17)
     st = synth.quant_probe_state(35, (S, H, P, N))
     st = np.clip(st, -60000.0, 60000.0)
     st[0, 1] = np.float32(2.0 ** -20) * np.sign(st[0, 1])                 # a head of fp16 subnormals
     st[0, 2] = np.float32(2.0 ** -14) * (1 + (np.arange(N) % 7) / 8.0)     # the smallest normals
-    st16 = torch.from_numpy(st).half()
-
-    def fresh(anc):
-        c = ers.ReplayCache(S, H, G, P, N, L, torch.bfloat16, read_copy=True, read_dtype="nvfp4", anchor=anc,
-                            sr_key=KEY)
-        c.state.copy_(st16 if anc == "fp16_sr" else st16.float())
-        ers.refresh(c, prm, replayssm=True, drafts_T=L + 1)
-        return c
-    c16, c32 = fresh("fp16_sr"), fresh("fp32")
-    for k in range(K):
-        ers.replay_decode(c16, prm, *(t[k] for t in tok), replayssm=True, fuse_refresh=False)
-        ers.replay_decode(c32, prm, *(t[k] for t in tok), replayssm=True, fuse_refresh=False)
-    for c in (c16, c32):
-        c.sr_nonce = 91
-        ers.refresh(c, prm, replayssm=True, drafts_T=16)
-    want = np.stack([oracle.sr_fp16_anchor(c32.state[i].cpu().numpy(), KEY, 91, i) for i in range(S)])
-    got = c16.state.float().cpu().numpy().astype(np.float64)
-    assert np.array_equal(got, want)
+    st[1, 3] = np.float32(65472.0) * np.where(st[1, 3] < 0, -1, 1)          # next to the fp16 maximum
+    st16 = torch.from_numpy(st.astype(np.float16)).to(dev())
+    c, model = _run_exact(ers, params, stream, st16, S, K, "nvfp4", 91)
+    got = c.state.float().cpu().numpy().astype(np.float64)
+    assert np.array_equal(got, model.anchor)
     sub = np.abs(got[0, 1]) < 2.0 ** -14
     assert sub.mean() > 0.9 and np.any(got[0, 1] != 0)                   # the subnormal path ran
+    assert np.any(np.abs(got) == 65504.0)                                 # and the saturation
