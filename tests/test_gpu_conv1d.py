@@ -19,7 +19,7 @@ def _ers():
 
 def _inputs(seed, T, C, W, S_state, io):
     rng = np.random.Generator(np.random.PCG64(seed))
-    cast = (lambda a: torch.from_numpy(a.astype(np.float32)).to(dev()).to(io))
+    cast = (lambda a: torch.from_numpy(a.astype(np.float32)).to(io).to(dev()))   # rounded on the host
     x = cast(rng.standard_normal((T, C)))
     w = cast(rng.standard_normal((C, W)) * 0.5)
     b = cast(rng.standard_normal(C) * 0.1)
