@@ -604,7 +604,7 @@ def bench_conv(dev, hbm: float, reps: int = 50):
             "l2": "flushed before each call"}
 
 
-def bench_gdn_verify(dev, steps: int, hbm: float):
+def bench_gdn_verify(dev, steps: int, hbm: float, batch: Optional[int] = None):
     """Output-only verify of a gated-delta-rule layer: 512 sequences x 4 drafts, 32 value heads / 16
     key groups, dk = dv = 128, window 16, bf16 io, 3 warm-up steps (then the cache goes back to its
     start), 32 timed verify + commit steps; the 512 MiB read copy exceeds L2.  Bytes from the run's own
@@ -615,7 +615,7 @@ def bench_gdn_verify(dev, steps: int, hbm: float):
     import torch
     import exact_replay_decode_gb300 as ers
     d = synth.GDN_VERIFY["dims"]
-    S, T = synth.GDN_VERIFY["batch"], synth.GDN_VERIFY["drafts"]
+    S, T = batch or synth.GDN_VERIFY["batch"], synth.GDN_VERIFY["drafts"]
     anchor, toks, acc = synth.gdn_verify_inputs(0, S, steps, d, T)
     cache = ers.GdnCache(S, d.nheads, d.ngroups, d.dk, d.dv, d.window, torch.bfloat16)
     cache.anchor.copy_(torch.from_numpy(anchor))
@@ -783,7 +783,8 @@ def main(argv=None):
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--decode-only", action="store_true", help="only the headline decode measurement")
-    ap.add_argument("--batch", type=int, default=None, help="decode sequences per GPU (profiling runs only)")
+    ap.add_argument("--batch", type=int, default=None,
+                    help="decode (or, with --section gdn, GDN) sequences per GPU (profiling runs only)")
     ap.add_argument("--section", choices=["prefill", "verify", "rssm", "ssu", "conv", "gdn"], default=None,
                     help="run only this secondary workload and print its JSON (profiling aid, no headline)")
     args = ap.parse_args(argv)
@@ -806,7 +807,7 @@ def main(argv=None):
         elif args.section == "conv":
             out = bench_conv(dev, hbm)
         elif args.section == "gdn":
-            out = bench_gdn_verify(dev, 32, hbm)
+            out = bench_gdn_verify(dev, 32, hbm, args.batch)
         elif args.section == "rssm":
             out = {r: bench_rssm_decode(dev, 4, hbm, r) for r in ("bf16", "fp8", "nvfp4")}
             out["nvfp4_fp16sr"] = bench_rssm_decode(dev, 4, hbm, "nvfp4", "fp16_sr")

@@ -33,6 +33,8 @@ constexpr int kGWarps = kThreads / 32;         // 8
 constexpr int kGRows = kGD / kGWarps;          // state rows per warp
 constexpr int kGL = 32;                        // max window L
 constexpr int kGT = 8;                         // max drafts T
+constexpr int kYS = kGD + 8;                   // padded row of the y / z tables (8 banks apart)
+constexpr int kZ0 = kGT * kYS + 4;             // z table: 4 banks after y's
 
 struct GdnSmem {
   float k[kGL + kGT][kGD];   // committed rows 0..hc-1, drafts at kGL + s
@@ -40,8 +42,9 @@ struct GdnSmem {
   float v[kGT][kGD];         // drafts' v
   float vc[kGL][kGD];        // committed v (flush)
   float u[kGL + kGT][kGD];   // residuals: committed (cached), drafts at kGL + s
-  float y[kGT][kGD];         // S_read k_s
-  float z[kGT][kGD];         // S_read q_s
+  // S_read k_s (row s at s * kYS) and S_read q_s (row s at kZ0 + s * kYS): rows padded so that the
+  // 32 lanes of a reduce-scatter (4 rows x 4 drafts x {k, q}) store to 32 different banks
+  float yz[kZ0 + kGT * kYS];
   float gc[kGL + kGT];       // cumulative log-gates of the output rows
   float bt[kGL + kGT];       // beta of the output rows
   float gf[kGL];             // cumulative log-gates of the committed rows (flush)
@@ -93,9 +96,9 @@ __device__ __forceinline__ void draft_dots(GdnSmem& sm, const float (&rv)[32 / (
   const float v = reduce_scatter32(part, j);
   const int d = d0 + j / (2 * TM), idx = j % (2 * TM);
   if (idx < TM) {
-    if (idx < Td) sm.y[idx][d] = v;
+    if (idx < Td) sm.yz[idx * kYS + d] = v;
   } else if (idx - TM < Td) {
-    sm.z[idx - TM][d] = v;
+    sm.yz[kZ0 + (idx - TM) * kYS + d] = v;
   }
 }
 
@@ -187,24 +190,30 @@ __device__ __forceinline__ void load_committed_head(GdnSmem& sm, const GdnArgs& 
   }
 }
 
-// Gates of the committed records summed in row order, and their betas (thread 0).
+// Lane r of a warp gets v_0 + v_1 + ... + v_r (n <= 32 values, lane q holding v_q), added one at a
+// time from 0 in row order: the bits of a serial running sum.
+__device__ __forceinline__ float ordered_prefix(float v, int n, int r) {
+  float acc = 0.f;
+  for (int q = 0; q < n; ++q) {
+    const float vq = __shfl_sync(kFull, v, q);
+    if (q <= r) acc = __fadd_rn(acc, vq);
+  }
+  return acc;
+}
+
+// Gates of the committed records summed in row order, and their betas (warp 0).
 // (Warp 0: the lanes load one row each, then lane 0 sums in row order.)
 __device__ __forceinline__ void flush_scalars(GdnSmem& sm, const GdnArgs& a, int slot, int h, int hc) {
   if (threadIdx.x < 32) {
     const int r = threadIdx.x;
+    float gr = 0.f;
     if (r < hc) {
       const size_t row = (size_t)slot * a.L + r;
-      sm.gf[r] = a.bg[row * a.H + h];
+      gr = a.bg[row * a.H + h];
       sm.bf[r] = a.bbeta[row * a.H + h];
     }
-    __syncwarp();
-    if (r == 0) {
-      float acc = 0.f;
-      for (int q = 0; q < hc; ++q) {
-        acc = __fadd_rn(acc, sm.gf[q]);
-        sm.gf[q] = acc;
-      }
-    }
+    const float acc = ordered_prefix(gr, hc, r);
+    if (r < hc) sm.gf[r] = acc;
   }
 }
 
@@ -304,38 +313,36 @@ __global__ void __launch_bounds__(kThreads, TM == 4 ? 2 : 1) k_gdn_verify(GdnArg
   for (int hh = 0; hh < hpg; ++hh) {
     const int h = g * hpg + hh;
     const size_t soff = ((size_t)slot * a.H + h) * kGD * kGD;
+    uint2 raw[kGRows];   // without a flush: the warp's read-copy rows, in flight while the scalars load
+    if (!flush) {
+      const __nv_bfloat16* R = (const __nv_bfloat16*)a.copy + soff;
+#pragma unroll
+      for (int rr = 0; rr < kGRows; ++rr)
+        raw[rr] = Quad<__nv_bfloat16>::ld_stream(R + (size_t)(w * kGRows + rr) * kGD + 4 * j);
+    }
     load_committed_head<T>(sm, a, slot, h, hc, flush);
     for (int s = w; s < Td; s += kGWarps)
       load_vec<T>((const T*)a.v + (((size_t)i * Td + s) * a.H + h) * kGD, sm.v[s]);
     if (flush && hc > 0) flush_scalars(sm, a, slot, h, hc);
-    if (w == 1) {   // output rows: committed rows 0..h0-1, then the drafts; gates summed in row order
-      for (int r = j; r < h0 + Td; r += 32) {
+    if (w == 1) {   // output rows: committed rows 0..h0-1, then the drafts (h0 + Td <= 32); gates in row order
+      const int r = j, n = h0 + Td;
+      float gr = 0.f;
+      if (r < n) {
         const size_t br = ((size_t)slot * a.L + r) * a.H + h, tr = ((size_t)i * Td + (r - h0)) * a.H + h;
-        sm.gc[r] = r < h0 ? a.bg[br] : a.g[tr];
+        gr = r < h0 ? a.bg[br] : a.g[tr];
         sm.bt[r] = r < h0 ? a.bbeta[br] : a.beta[tr];
       }
-      __syncwarp();
-      if (j == 0) {
-        float acc = 0.f;
-        for (int r = 0; r < h0 + Td; ++r) {
-          acc = __fadd_rn(acc, sm.gc[r]);
-          sm.gc[r] = acc;
-        }
-      }
+      const float acc = ordered_prefix(gr, n, r);
+      if (r < n) sm.gc[r] = acc;
     }
     __syncthreads();
     if (flush && hc > 0) flush_coeffs(sm, hc);
     draft_coeffs(sm, h0, Td);
-    __syncthreads();
+    if (flush) __syncthreads();   // the fold reads the flush coefficients; the plain stream needs none
     if (flush && hc > 0) {
       gdn_fold_rows<TM>(sm, a.anchor + soff, (__nv_bfloat16*)a.copy + soff, hc, Td, w, j);
     } else {
-      // stream the read copy: S_read k_s and S_read q_s for every draft
-      const __nv_bfloat16* R = (const __nv_bfloat16*)a.copy + soff;
-      uint2 raw[kGRows];   // the warp's rows, all in flight before the math
-#pragma unroll
-      for (int rr = 0; rr < kGRows; ++rr)
-        raw[rr] = Quad<__nv_bfloat16>::ld_stream(R + (size_t)(w * kGRows + rr) * kGD + 4 * j);
+      // S_read k_s and S_read q_s for every draft from the rows loaded above
 #pragma unroll
       for (int rr = 0; rr < kGRows; rr += RPG) {
         float rvg[RPG][4];
@@ -345,27 +352,30 @@ __global__ void __launch_bounds__(kThreads, TM == 4 ? 2 : 1) k_gdn_verify(GdnArg
       }
     }
     __syncthreads();
-    // residuals and outputs, one state row d per thread, drafts in order
+    // residuals, one state row d per thread, drafts in order (draft s needs the residuals before it)
     if (tid < kGD) {
       const int d = tid;
       for (int s = 0; s < Td; ++s) {
         const int t = h0 + s;
-        const float gam = sm.gam[s];
-        float acc = __fmul_rn(sm.bt[t], __fmaf_rn(-gam, sm.y[s][d], sm.v[s][d]));
+        float acc = __fmul_rn(sm.bt[t], __fmaf_rn(-sm.gam[s], sm.yz[s * kYS + d], sm.v[s][d]));
         for (int r = 0; r < t; ++r) {
           const float ur = r < h0 ? sm.u[r][d] : sm.u[kGL + r - h0][d];
           acc = __fmaf_rn(-sm.cc[r][s], ur, acc);
         }
         sm.u[kGL + s][d] = acc;
-        float out = __fmul_rn(gam, sm.z[s][d]);
-        for (int r = 0; r <= t; ++r) {
-          const float ur = r < h0 ? sm.u[r][d] : sm.u[kGL + r - h0][d];
-          out = __fmaf_rn(sm.wq[r][s], ur, out);
-        }
-        ((T*)a.o)[(((size_t)i * Td + s) * a.H + h) * kGD + d] = from_f<T>(out);
       }
     }
     __syncthreads();
+    // outputs, (row d, draft s) over all threads, each sum in row order
+    for (int p = tid; p < Td * kGD; p += kThreads) {
+      const int d = p % kGD, s = p / kGD, t = h0 + s;
+      float out = __fmul_rn(sm.gam[s], sm.yz[kZ0 + s * kYS + d]);
+      for (int r = 0; r <= t; ++r) {
+        const float ur = r < h0 ? sm.u[r][d] : sm.u[kGL + r - h0][d];
+        out = __fmaf_rn(sm.wq[r][s], ur, out);
+      }
+      ((T*)a.o)[(((size_t)i * Td + s) * a.H + h) * kGD + d] = from_f<T>(out);
+    }
     // this head's draft rows (v, residual, gate, beta) go to buffer rows h0..h0+T-1
     for (int s = w; s < Td; s += kGWarps) {
       const size_t row = (size_t)slot * a.L + h0 + s, tok = (size_t)i * Td + s;
@@ -378,7 +388,7 @@ __global__ void __launch_bounds__(kThreads, TM == 4 ? 2 : 1) k_gdn_verify(GdnArg
         a.bbeta[row * a.H + h] = a.beta[tok * a.H + h];
       }
     }
-    __syncthreads();
+    __syncthreads();   // the next head's loads overwrite the committed residuals the outputs read
   }
   // the group's draft key rows, after every head has read the committed ones
   for (int s = w; s < Td; s += kGWarps) {
