@@ -103,28 +103,61 @@ __device__ __forceinline__ void draft_dots(GdnSmem& sm, const float (&rv)[32 / (
 }
 
 // The flush of warp w's anchor rows, in three passes:
-//  A. S k_i for the hc committed records, one reduce-scatter per row (lane i gets row d's S k_i);
+//  A. S k_i for the hc committed records, by reduce-scatter: with hc <= 16 two rows per reduce-scatter
+//     (lane i: row rr's S k_i, lane 16 + i: row rr + 1's), else one row (lane i: S k_i);
 //  B. the triangular solve, one row per lane (lanes 0..15), in row order, in place of S k_i;
 //  C. the fold S'[d][n] = gamma_{1..hc} S[d][n] + sum_i gamma_{i+1..hc} u_i[d] k_i[n] (fma chain in
-//     row order), stored to the anchor and cast to the bf16 read copy; with drafts, S' k_s and S' q_s
-//     from the cast values (draft_dots).
+//     row order), two rows per pass sharing the key loads, stored to the anchor and cast to the bf16
+//     read copy; with drafts, S' k_s and S' q_s from the cast values (draft_dots).
+// Passes A and C keep the next pair of anchor rows in flight.  Each S k_i is a Dot<128> reduction
+// whichever lane and row pairing carries it, so the bits do not depend on hc's branch.
 template <int TM>
 __device__ __forceinline__ void gdn_fold_rows(GdnSmem& sm, float* __restrict__ S, __nv_bfloat16* __restrict__ R,
                                               int hc, int ndraft, int w, int j) {
   constexpr int RPG = 32 / (2 * TM);
+  static_assert(kGRows % 2 == 0 && RPG % 2 == 0 || RPG == 2, "row pairs fill the draft groups");
   float (*YU)[kGL + 1] = sm.yu[w];   // [row of the warp][record]: S k_i, then u_i
-  for (int rr = 0; rr < kGRows; ++rr) {
-    const int d = w * kGRows + rr;
-    float hq[4];
-    Quad<float>::unpack(*reinterpret_cast<const float4*>(S + (size_t)d * kGD + 4 * j), hq);
-    float part[32];
+  const float* Sw = S + (size_t)(w * kGRows) * kGD + 4 * j;
+  auto ldrow = [&](int rr) { return *reinterpret_cast<const float4*>(Sw + (size_t)rr * kGD); };
+  if (hc <= 16) {
+    float4 c0 = ldrow(0), c1 = ldrow(1);
+    for (int rr = 0; rr < kGRows; rr += 2) {
+      float4 n0 = c0, n1 = c1;
+      if (rr + 2 < kGRows) {
+        n0 = ldrow(rr + 2);
+        n1 = ldrow(rr + 3);
+      }
+      float h0[4], h1[4];
+      Quad<float>::unpack(c0, h0);
+      Quad<float>::unpack(c1, h1);
+      float part[32];
 #pragma unroll
-    for (int r = 0; r < kGL; ++r) {
-      float kq4[4];
-      lds4(sm.k[r] + 4 * j, kq4);
-      part[r] = r < hc ? Dot<kGD>::partial(kq4, hq) : 0.f;
+      for (int r = 0; r < 16; ++r) {
+        float kq4[4];
+        lds4(sm.k[r] + 4 * j, kq4);
+        part[r] = r < hc ? Dot<kGD>::partial(kq4, h0) : 0.f;
+        part[16 + r] = r < hc ? Dot<kGD>::partial(kq4, h1) : 0.f;
+      }
+      YU[rr + (j >> 4)][j & 15] = reduce_scatter32(part, j);
+      c0 = n0;
+      c1 = n1;
     }
-    YU[rr][j] = reduce_scatter32(part, j);
+  } else {
+    float4 c0 = ldrow(0);
+    for (int rr = 0; rr < kGRows; ++rr) {
+      const float4 n0 = rr + 1 < kGRows ? ldrow(rr + 1) : c0;
+      float hq[4];
+      Quad<float>::unpack(c0, hq);
+      float part[32];
+#pragma unroll
+      for (int r = 0; r < kGL; ++r) {
+        float kq4[4];
+        lds4(sm.k[r] + 4 * j, kq4);
+        part[r] = r < hc ? Dot<kGD>::partial(kq4, hq) : 0.f;
+      }
+      YU[rr][j] = reduce_scatter32(part, j);
+      c0 = n0;
+    }
   }
   __syncwarp();
   if (j < kGRows) {
@@ -138,35 +171,55 @@ __device__ __forceinline__ void gdn_fold_rows(GdnSmem& sm, float* __restrict__ S
   __syncwarp();
   const float gall = sm.gamf[hc - 1];
   float rvg[RPG][4];
-  for (int rr = 0; rr < kGRows; ++rr) {
-    const int d = w * kGRows + rr;
-    float hq[4], nv[4];
-    Quad<float>::unpack(*reinterpret_cast<const float4*>(S + (size_t)d * kGD + 4 * j), hq);
+  float4 c0 = ldrow(0), c1 = ldrow(1);
+  for (int rr = 0; rr < kGRows; rr += 2) {
+    float4 n0 = c0, n1 = c1;
+    if (rr + 2 < kGRows) {
+      n0 = ldrow(rr + 2);
+      n1 = ldrow(rr + 3);
+    }
+    float h0[4], h1[4], v0[4], v1[4];
+    Quad<float>::unpack(c0, h0);
+    Quad<float>::unpack(c1, h1);
 #pragma unroll
-    for (int e = 0; e < 4; ++e) nv[e] = __fmul_rn(gall, hq[e]);
+    for (int e = 0; e < 4; ++e) {
+      v0[e] = __fmul_rn(gall, h0[e]);
+      v1[e] = __fmul_rn(gall, h1[e]);
+    }
     for (int r = 0; r < hc; ++r) {
       float kq4[4];
       lds4(sm.k[r] + 4 * j, kq4);
-      const float wu = __fmul_rn(sm.wf[r], YU[rr][r]);
+      const float wf = sm.wf[r];
+      const float wu0 = __fmul_rn(wf, YU[rr][r]), wu1 = __fmul_rn(wf, YU[rr + 1][r]);
 #pragma unroll
-      for (int e = 0; e < 4; ++e) nv[e] = __fmaf_rn(wu, kq4[e], nv[e]);
+      for (int e = 0; e < 4; ++e) {
+        v0[e] = __fmaf_rn(wu0, kq4[e], v0[e]);
+        v1[e] = __fmaf_rn(wu1, kq4[e], v1[e]);
+      }
     }
-    *reinterpret_cast<float4*>(S + (size_t)d * kGD + 4 * j) = make_float4(nv[0], nv[1], nv[2], nv[3]);
-    const __nv_bfloat162 lo2 = __floats2bfloat162_rn(nv[0], nv[1]), hi2 = __floats2bfloat162_rn(nv[2], nv[3]);
-    uint2 pk;
-    pk.x = *reinterpret_cast<const uint32_t*>(&lo2);
-    pk.y = *reinterpret_cast<const uint32_t*>(&hi2);
-    *reinterpret_cast<uint2*>(R + (size_t)d * kGD + 4 * j) = pk;
-    float rv[4];
-    Quad<__nv_bfloat16>::unpack(pk, rv);
-    if (ndraft > 0) {
 #pragma unroll
-      for (int g = 0; g < RPG; ++g)
-        if (rr % RPG == g)
+    for (int q = 0; q < 2; ++q) {
+      const float* v = q ? v1 : v0;
+      const int row = rr + q, d = w * kGRows + row;
+      *reinterpret_cast<float4*>(S + (size_t)d * kGD + 4 * j) = make_float4(v[0], v[1], v[2], v[3]);
+      const __nv_bfloat162 lo2 = __floats2bfloat162_rn(v[0], v[1]), hi2 = __floats2bfloat162_rn(v[2], v[3]);
+      uint2 pk;
+      pk.x = *reinterpret_cast<const uint32_t*>(&lo2);
+      pk.y = *reinterpret_cast<const uint32_t*>(&hi2);
+      *reinterpret_cast<uint2*>(R + (size_t)d * kGD + 4 * j) = pk;
+      if (ndraft > 0) {
+        float rv[4];
+        Quad<__nv_bfloat16>::unpack(pk, rv);
 #pragma unroll
-          for (int e = 0; e < 4; ++e) rvg[g][e] = rv[e];
-      if (rr % RPG == RPG - 1) draft_dots<TM>(sm, rvg, d - (RPG - 1), ndraft, j);
+        for (int g = 0; g < RPG; ++g)
+          if (row % RPG == g)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) rvg[g][e] = rv[e];
+        if (row % RPG == RPG - 1) draft_dots<TM>(sm, rvg, d - (RPG - 1), ndraft, j);
+      }
     }
+    c0 = n0;
+    c1 = n1;
   }
 }
 
