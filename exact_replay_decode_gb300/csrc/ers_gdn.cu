@@ -17,6 +17,7 @@
 // residual and output sums run in row order.  The same rows give the same bits whether they are
 // drafts of one verify or tokens of T = 1 verifies, and a refresh gives the bits of the flush that
 // a verify would run.
+#include <stddef.h>
 #include <stdint.h>
 
 #include "ers_common.cuh"
@@ -27,6 +28,11 @@ namespace ers {
 namespace {
 
 using namespace wh;
+using tc::bulk_g2s;
+using tc::fence_mbar_init;
+using tc::mbar_arrive_expect_tx;
+using tc::mbar_init;
+using tc::mbar_wait;
 
 constexpr int kGD = 128;                       // dk = dv
 constexpr int kGWarps = kThreads / 32;         // 8
@@ -36,11 +42,23 @@ constexpr int kGT = 8;                         // max drafts T
 constexpr int kYS = kGD + 8;                   // padded row of the y / z tables (8 banks apart)
 constexpr int kZ0 = kGT * kYS + 4;             // z table: 4 banks after y's
 
+// What only a flushing CTA uses; a CTA without a flush keeps a head's read copy in the same bytes.
+struct GdnFlush {
+  float vc[kGL][kGD];        // committed v
+  float kkf[kGL][kGL];       // k_i . k_r, committed rows
+  float cf[kGL][kGL];        // beta_r gamma_{i+1..r} (k_i . k_r), i < r
+  float yu[kGWarps][kGRows][kGL + 1];   // per warp and row, S k_i then the residual u_i (padded)
+};
+
+// Every row array starts on a 16-byte boundary (lane quads are read as 16-byte vectors).
 struct GdnSmem {
-  float k[kGL + kGT][kGD];   // committed rows 0..hc-1, drafts at kGL + s
+  union alignas(16) {
+    GdnFlush f;
+    __nv_bfloat16 cb[kGD * kGD];   // without a flush: the head's read copy (one bulk copy)
+  } x;
+  alignas(16) float k[kGL + kGT][kGD];   // committed rows 0..hc-1, drafts at kGL + s
   float q[kGT][kGD];
   float v[kGT][kGD];         // drafts' v
-  float vc[kGL][kGD];        // committed v (flush)
   float u[kGL + kGT][kGD];   // residuals: committed (cached), drafts at kGL + s
   // S_read k_s (row s at s * kYS) and S_read q_s (row s at kZ0 + s * kYS): rows padded so that the
   // 32 lanes of a reduce-scatter (4 rows x 4 drafts x {k, q}) store to 32 different banks
@@ -49,18 +67,20 @@ struct GdnSmem {
   float bt[kGL + kGT];       // beta of the output rows
   float gf[kGL];             // cumulative log-gates of the committed rows (flush)
   float bf[kGL];
-  float kkf[kGL][kGL];       // k_i . k_r, committed rows (flush)
   float kk[kGL + kGT][kGT];  // k_row . k_draft
   float kq[kGL + kGT][kGT];  // k_row . q_draft
   // per-head coefficients, computed once per head (same expressions, so the same bits, as inline)
-  float cf[kGL][kGL];        // flush: beta_r gamma_{i+1..r} (k_i . k_r), i < r
   float gamf[kGL];           // flush: gamma_{1..r}
   float wf[kGL];             // flush: gamma_{r+1..hc}
   float cc[kGL + kGT][kGT];  // drafts: beta_t gamma_{r+1..t} (k_r . k_s), r < t = h0 + s
   float wq[kGL + kGT][kGT];  // drafts: gamma_{r+1..t} (k_r . q_s), r <= t
   float gam[kGT];            // drafts: gamma_{1..t}
-  float yu[kGWarps][kGRows][kGL + 1];   // flush: per warp and row, S k_i then the residual u_i (padded)
+  uint64_t bar;              // completion of the read-copy bulk copies, one phase per head
 };
+static_assert(sizeof(GdnFlush) >= kGD * kGD * 2, "the read copy fits the flush arrays' bytes");
+static_assert(offsetof(GdnSmem, k) % 16 == 0 && offsetof(GdnSmem, q) % 16 == 0 && offsetof(GdnSmem, u) % 16 == 0 &&
+                  offsetof(GdnSmem, x) % 16 == 0 && offsetof(GdnSmem, bar) % 8 == 0,
+              "16-byte rows, an 8-byte mbarrier");
 
 template <typename T>
 __device__ __forceinline__ void load_vec(const T* __restrict__ p, float* dst) {
@@ -116,7 +136,7 @@ __device__ __forceinline__ void gdn_fold_rows(GdnSmem& sm, float* __restrict__ S
                                               int hc, int ndraft, int w, int j) {
   constexpr int RPG = 32 / (2 * TM);
   static_assert(kGRows % 2 == 0 && RPG % 2 == 0 || RPG == 2, "row pairs fill the draft groups");
-  float (*YU)[kGL + 1] = sm.yu[w];   // [row of the warp][record]: S k_i, then u_i
+  float (*YU)[kGL + 1] = sm.x.f.yu[w];   // [row of the warp][record]: S k_i, then u_i
   const float* Sw = S + (size_t)(w * kGRows) * kGD + 4 * j;
   auto ldrow = [&](int rr) { return *reinterpret_cast<const float4*>(Sw + (size_t)rr * kGD); };
   if (hc <= 16) {
@@ -163,8 +183,8 @@ __device__ __forceinline__ void gdn_fold_rows(GdnSmem& sm, float* __restrict__ S
   if (j < kGRows) {
     const int d = w * kGRows + j;
     for (int r = 0; r < hc; ++r) {
-      float acc = __fmul_rn(sm.bf[r], __fmaf_rn(-sm.gamf[r], YU[j][r], sm.vc[r][d]));
-      for (int i = 0; i < r; ++i) acc = __fmaf_rn(-sm.cf[i][r], YU[j][i], acc);
+      float acc = __fmul_rn(sm.bf[r], __fmaf_rn(-sm.gamf[r], YU[j][r], sm.x.f.vc[r][d]));
+      for (int i = 0; i < r; ++i) acc = __fmaf_rn(-sm.x.f.cf[i][r], YU[j][i], acc);
       YU[j][r] = acc;
     }
   }
@@ -197,10 +217,8 @@ __device__ __forceinline__ void gdn_fold_rows(GdnSmem& sm, float* __restrict__ S
         v1[e] = __fmaf_rn(wu1, kq4[e], v1[e]);
       }
     }
-#pragma unroll
-    for (int q = 0; q < 2; ++q) {
-      const float* v = q ? v1 : v0;
-      const int row = rr + q, d = w * kGRows + row;
+    auto emit = [&](const float (&v)[4], int row) {
+      const int d = w * kGRows + row;
       *reinterpret_cast<float4*>(S + (size_t)d * kGD + 4 * j) = make_float4(v[0], v[1], v[2], v[3]);
       const __nv_bfloat162 lo2 = __floats2bfloat162_rn(v[0], v[1]), hi2 = __floats2bfloat162_rn(v[2], v[3]);
       uint2 pk;
@@ -217,7 +235,9 @@ __device__ __forceinline__ void gdn_fold_rows(GdnSmem& sm, float* __restrict__ S
             for (int e = 0; e < 4; ++e) rvg[g][e] = rv[e];
         if (row % RPG == RPG - 1) draft_dots<TM>(sm, rvg, d - (RPG - 1), ndraft, j);
       }
-    }
+    };
+    emit(v0, rr);
+    emit(v1, rr + 1);
     c0 = n0;
     c1 = n1;
   }
@@ -237,7 +257,7 @@ __device__ __forceinline__ void load_committed_head(GdnSmem& sm, const GdnArgs& 
   for (int r = w; r < hc; r += kGWarps) {
     const size_t row = (size_t)slot * a.L + r;
     if (flush)
-      load_vec<T>((const T*)a.bv + (row * a.H + h) * kGD, sm.vc[r]);
+      load_vec<T>((const T*)a.bv + (row * a.H + h) * kGD, sm.x.f.vc[r]);
     else
       load_vec<float>(a.bu + (row * a.H + h) * kGD, sm.u[r]);
   }
@@ -276,7 +296,7 @@ __device__ __forceinline__ void flush_gram(GdnSmem& sm, int hc) {
     const int i = p / hc, r = p % hc;
     if (i < r) {
       const float v = sdot(sm.k[i], sm.k[r], j);
-      if (j == 0) sm.kkf[i][r] = v;
+      if (j == 0) sm.x.f.kkf[i][r] = v;
     }
   }
 }
@@ -285,7 +305,8 @@ __device__ __forceinline__ void flush_gram(GdnSmem& sm, int hc) {
 __device__ __forceinline__ void flush_coeffs(GdnSmem& sm, int hc) {
   for (int p = threadIdx.x; p < hc * hc; p += kThreads) {
     const int i = p / hc, r = p % hc;
-    if (i < r) sm.cf[i][r] = __fmul_rn(__fmul_rn(sm.bf[r], expf(__fsub_rn(sm.gf[r], sm.gf[i]))), sm.kkf[i][r]);
+    if (i < r)
+      sm.x.f.cf[i][r] = __fmul_rn(__fmul_rn(sm.bf[r], expf(__fsub_rn(sm.gf[r], sm.gf[i]))), sm.x.f.kkf[i][r]);
   }
   for (int r = threadIdx.x; r < hc; r += kThreads) {
     sm.gamf[r] = expf(sm.gf[r]);
@@ -342,6 +363,14 @@ __global__ void __launch_bounds__(kThreads, TM == 4 ? 2 : 1) k_gdn_verify(GdnArg
     return;
   }
   const int h0 = flush ? 0 : hc;   // committed rows that precede the drafts
+  constexpr uint32_t kCopyBytes = kGD * kGD * 2;
+  const __nv_bfloat16* Rg = (const __nv_bfloat16*)a.copy + (size_t)slot * a.H * kGD * kGD;   // the slot's copy
+  if (!flush && tid == 0) {   // the first head's read copy, in flight through the prologue
+    mbar_init(&sm.bar, 1);
+    fence_mbar_init();
+    mbar_arrive_expect_tx(&sm.bar, kCopyBytes);
+    bulk_g2s(sm.x.cb, Rg + (size_t)(g * hpg) * kGD * kGD, kCopyBytes, &sm.bar);
+  }
   load_committed_k<T>(sm, a, slot, g, hc);
   for (int s = w; s < Td; s += kGWarps) {
     const size_t tok = (size_t)i * Td + s;
@@ -366,13 +395,6 @@ __global__ void __launch_bounds__(kThreads, TM == 4 ? 2 : 1) k_gdn_verify(GdnArg
   for (int hh = 0; hh < hpg; ++hh) {
     const int h = g * hpg + hh;
     const size_t soff = ((size_t)slot * a.H + h) * kGD * kGD;
-    uint2 raw[kGRows];   // without a flush: the warp's read-copy rows, in flight while the scalars load
-    if (!flush) {
-      const __nv_bfloat16* R = (const __nv_bfloat16*)a.copy + soff;
-#pragma unroll
-      for (int rr = 0; rr < kGRows; ++rr)
-        raw[rr] = Quad<__nv_bfloat16>::ld_stream(R + (size_t)(w * kGRows + rr) * kGD + 4 * j);
-    }
     load_committed_head<T>(sm, a, slot, h, hc, flush);
     for (int s = w; s < Td; s += kGWarps)
       load_vec<T>((const T*)a.v + (((size_t)i * Td + s) * a.H + h) * kGD, sm.v[s]);
@@ -388,23 +410,35 @@ __global__ void __launch_bounds__(kThreads, TM == 4 ? 2 : 1) k_gdn_verify(GdnArg
       const float acc = ordered_prefix(gr, n, r);
       if (r < n) sm.gc[r] = acc;
     }
-    __syncthreads();
+    // the head's read copy has landed (without a flush); a wait that gave up ends the CTA
+    const bool late = !flush && !mbar_wait(&sm.bar, hh & 1, a.status);
+    if (__syncthreads_or(late)) {
+      if (tid == 0) mbar_wait(&sm.bar, hh & 1, nullptr);   // bounded: no copy left in flight on exit
+      return;
+    }
     if (flush && hc > 0) flush_coeffs(sm, hc);
     draft_coeffs(sm, h0, Td);
     if (flush) __syncthreads();   // the fold reads the flush coefficients; the plain stream needs none
     if (flush && hc > 0) {
       gdn_fold_rows<TM>(sm, a.anchor + soff, (__nv_bfloat16*)a.copy + soff, hc, Td, w, j);
     } else {
-      // S_read k_s and S_read q_s for every draft from the rows loaded above
+      // S_read k_s and S_read q_s for every draft from the head's copy in shared memory
 #pragma unroll
       for (int rr = 0; rr < kGRows; rr += RPG) {
         float rvg[RPG][4];
 #pragma unroll
-        for (int g = 0; g < RPG; ++g) Quad<__nv_bfloat16>::unpack(raw[rr + g], rvg[g]);
+        for (int g = 0; g < RPG; ++g) {
+          const uint2 raw = *reinterpret_cast<const uint2*>(sm.x.cb + (size_t)(w * kGRows + rr + g) * kGD + 4 * j);
+          Quad<__nv_bfloat16>::unpack(raw, rvg[g]);
+        }
         draft_dots<TM>(sm, rvg, w * kGRows + rr, Td, j);
       }
     }
     __syncthreads();
+    if (!flush && tid == 0 && hh + 1 < hpg) {   // every warp is done with this head's copy
+      mbar_arrive_expect_tx(&sm.bar, kCopyBytes);
+      bulk_g2s(sm.x.cb, Rg + (size_t)(h + 1) * kGD * kGD, kCopyBytes, &sm.bar);
+    }
     // residuals, one state row d per thread, drafts in order (draft s needs the residuals before it)
     if (tid < kGD) {
       const int d = tid;
