@@ -75,16 +75,31 @@ struct GdnSmem {
   float cc[kGL + kGT][kGT];  // drafts: beta_t gamma_{r+1..t} (k_r . k_s), r < t = h0 + s
   float wq[kGL + kGT][kGT];  // drafts: gamma_{r+1..t} (k_r . q_s), r <= t
   float gam[kGT];            // drafts: gamma_{1..t}
+  float gd[kGT];             // drafts' own log-gates (for the buffer)
   uint64_t bar;              // completion of the read-copy bulk copies, one phase per head
 };
 static_assert(sizeof(GdnFlush) >= kGD * kGD * 2, "the read copy fits the flush arrays' bytes");
 static_assert(offsetof(GdnSmem, k) % 16 == 0 && offsetof(GdnSmem, q) % 16 == 0 && offsetof(GdnSmem, u) % 16 == 0 &&
+                  offsetof(GdnSmem, v) % 16 == 0 &&
                   offsetof(GdnSmem, x) % 16 == 0 && offsetof(GdnSmem, bar) % 8 == 0,
               "16-byte rows, an 8-byte mbarrier");
 
 template <typename T>
-__device__ __forceinline__ void load_vec(const T* __restrict__ p, float* dst) {
-  for (int e = threadIdx.x & 31; e < kGD; e += 32) dst[e] = to_f(p[e]);
+__device__ __forceinline__ void load_vec(const T* __restrict__ p, float* dst) {   // one 128-vector per warp
+  const int l = threadIdx.x & 31;
+  float f[4];
+  Quad<T>::unpack(*reinterpret_cast<const typename Quad<T>::raw*>(p + 4 * l), f);
+  *reinterpret_cast<float4*>(dst + 4 * l) = make_float4(f[0], f[1], f[2], f[3]);
+}
+
+template <typename T>
+__device__ __forceinline__ void store_vec(const float* src, T* __restrict__ p) {   // exact: src holds T values
+  const int l = threadIdx.x & 31;
+  const float4 f = *reinterpret_cast<const float4*>(src + 4 * l);
+  p[4 * l] = from_f<T>(f.x);
+  p[4 * l + 1] = from_f<T>(f.y);
+  p[4 * l + 2] = from_f<T>(f.z);
+  p[4 * l + 3] = from_f<T>(f.w);
 }
 
 // Warp-per-dot products of two smem vectors (Dot<128> order); lane 0 stores.
@@ -406,6 +421,7 @@ __global__ void __launch_bounds__(kThreads, TM == 4 ? 2 : 1) k_gdn_verify(GdnArg
         const size_t br = ((size_t)slot * a.L + r) * a.H + h, tr = ((size_t)i * Td + (r - h0)) * a.H + h;
         gr = r < h0 ? a.bg[br] : a.g[tr];
         sm.bt[r] = r < h0 ? a.bbeta[br] : a.beta[tr];
+        if (r >= h0) sm.gd[r - h0] = gr;
       }
       const float acc = ordered_prefix(gr, n, r);
       if (r < n) sm.gc[r] = acc;
@@ -445,10 +461,9 @@ __global__ void __launch_bounds__(kThreads, TM == 4 ? 2 : 1) k_gdn_verify(GdnArg
       for (int s = 0; s < Td; ++s) {
         const int t = h0 + s;
         float acc = __fmul_rn(sm.bt[t], __fmaf_rn(-sm.gam[s], sm.yz[s * kYS + d], sm.v[s][d]));
-        for (int r = 0; r < t; ++r) {
-          const float ur = r < h0 ? sm.u[r][d] : sm.u[kGL + r - h0][d];
-          acc = __fmaf_rn(-sm.cc[r][s], ur, acc);
-        }
+#pragma unroll 4
+        for (int r = 0; r < h0; ++r) acc = __fmaf_rn(-sm.cc[r][s], sm.u[r][d], acc);
+        for (int r = h0; r < t; ++r) acc = __fmaf_rn(-sm.cc[r][s], sm.u[kGL + r - h0][d], acc);
         sm.u[kGL + s][d] = acc;
       }
     }
@@ -457,30 +472,27 @@ __global__ void __launch_bounds__(kThreads, TM == 4 ? 2 : 1) k_gdn_verify(GdnArg
     for (int p = tid; p < Td * kGD; p += kThreads) {
       const int d = p % kGD, s = p / kGD, t = h0 + s;
       float out = __fmul_rn(sm.gam[s], sm.yz[kZ0 + s * kYS + d]);
-      for (int r = 0; r <= t; ++r) {
-        const float ur = r < h0 ? sm.u[r][d] : sm.u[kGL + r - h0][d];
-        out = __fmaf_rn(sm.wq[r][s], ur, out);
-      }
+#pragma unroll 4
+      for (int r = 0; r < h0; ++r) out = __fmaf_rn(sm.wq[r][s], sm.u[r][d], out);
+      for (int r = h0; r <= t; ++r) out = __fmaf_rn(sm.wq[r][s], sm.u[kGL + r - h0][d], out);
       ((T*)a.o)[(((size_t)i * Td + s) * a.H + h) * kGD + d] = from_f<T>(out);
     }
     // this head's draft rows (v, residual, gate, beta) go to buffer rows h0..h0+T-1
     for (int s = w; s < Td; s += kGWarps) {
-      const size_t row = (size_t)slot * a.L + h0 + s, tok = (size_t)i * Td + s;
-      for (int e = j; e < kGD; e += 32) {
-        ((T*)a.bv)[(row * a.H + h) * kGD + e] = ((const T*)a.v)[(tok * a.H + h) * kGD + e];
-        a.bu[(row * a.H + h) * kGD + e] = sm.u[kGL + s][e];
-      }
+      const size_t row = (size_t)slot * a.L + h0 + s;
+      store_vec<T>(sm.v[s], (T*)a.bv + (row * a.H + h) * kGD);
+      store_vec<float>(sm.u[kGL + s], a.bu + (row * a.H + h) * kGD);
       if (j == 0) {
-        a.bg[row * a.H + h] = a.g[tok * a.H + h];
-        a.bbeta[row * a.H + h] = a.beta[tok * a.H + h];
+        a.bg[row * a.H + h] = sm.gd[s];
+        a.bbeta[row * a.H + h] = sm.bt[h0 + s];
       }
     }
     __syncthreads();   // the next head's loads overwrite the committed residuals the outputs read
   }
   // the group's draft key rows, after every head has read the committed ones
   for (int s = w; s < Td; s += kGWarps) {
-    const size_t row = (size_t)slot * a.L + h0 + s, tok = (size_t)i * Td + s;
-    for (int e = j; e < kGD; e += 32) ((T*)a.bk)[(row * a.G + g) * kGD + e] = ((const T*)a.k)[(tok * a.G + g) * kGD + e];
+    const size_t row = (size_t)slot * a.L + h0 + s;
+    store_vec<T>(sm.k[kGL + s], (T*)a.bk + (row * a.G + g) * kGD);
   }
 }
 
