@@ -74,6 +74,14 @@ def test_gdn_verify_equals_nonspec_and_oracle():
     _run(synth.GdnDims(32, 16, 128, 128, 16), 24, 20, 4, 71, [0, 11, 23])
 
 
+def test_gdn_verify_full_size_sampled():
+    """The bench's launch configuration (512 sequences x 4 drafts, 32 value heads / 16 key groups,
+    dk = dv = 128, window 16): bitwise equal to non-speculative verification for every sequence, and
+    within the tolerances of the oracle for sampled sequences."""
+    w = synth.GDN_VERIFY
+    _run(w["dims"], w["batch"], 8, w["drafts"], 75, [0, 257, 511])
+
+
 def test_gdn_verify_fp32_io_short_window_long_drafts():
     _run(synth.GdnDims(8, 2, 128, 128, 8), 6, 14, 6, 72, [0, 5], io=torch.float32)
 
