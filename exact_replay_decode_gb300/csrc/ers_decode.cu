@@ -287,7 +287,8 @@ __device__ __forceinline__ void advance_pos(int32_t* pos, int ncta, int32_t newp
 
 // HT: what the output stream reads (fp32 checkpoint, bf16 or FP8 read copy); W8: the read copy a
 // fused refresh writes is FP8 (else bf16, or none when read_copy is null).
-// AT: the ReplaySSM anchor's type (fp32, or fp16 written by stochastic rounding).
+// AT: the ReplaySSM anchor (fp32; fp16 written by stochastic rounding; or Nvfp4Shared: the NVFP4 read
+// copy is the state itself).
 template <typename T, typename HT, bool W8, int P, int N, int QM, typename AT = float>
 __global__ void __launch_bounds__(kThreads, 2) k_decode_heads(LaunchArgs a) {
   static_assert(N == 128 && P % 32 == 0, "lane split of Dot<128>; 32-row reduction blocks");
