@@ -703,12 +703,12 @@ class _OracleDecode:
     Tokens come from a small pre-generated ring (sequence-major, ready for the oracle's varlen
     call) so that only the recurrence itself is timed; the state is carried from call to call."""
 
-    def __init__(self, seed: int, S: int, K: int, ring: int = 4):
+    def __init__(self, seed: int, S: int, K: int, ring: int = 4, threads: Optional[int] = None):
         import oracle
         self.oracle = oracle
         w = synth.workload("decode_b256_h64")
         self.d = d = w.dims
-        self.threads = oracle.default_threads()
+        self.threads = threads or oracle.default_threads()
         rng = np.random.Generator(np.random.PCG64(seed))
         self.params = synth.make_params(rng, d.nheads)
         self.S, self.K = S, K
@@ -730,19 +730,75 @@ class _OracleDecode:
         return self.S * self.K
 
 
+def _timed(fn, budget_s: float):
+    """Calls fn() (returning units done) until budget_s has passed; returns (units, seconds)."""
+    done, t0 = 0, time.perf_counter()
+    while True:
+        done += fn()
+        el = time.perf_counter() - t0
+        if el >= budget_s:
+            return done, el
+
+
+def _oracle_prefill(threads: int, budget_s: float):
+    """The oracle's prefill of prefill_2048_h32 (one call = all 2048 tokens): tokens/s."""
+    import oracle
+    w = synth.workload("prefill_2048_h32")
+    params, toks, cu = synth.prefill_inputs(w, seed=0)
+    def run():
+        oracle.recurrence(toks.x, toks.dt, params.A, toks.B, toks.C, params.D, params.dt_bias, cu, nthreads=threads)
+        return toks.ntokens
+    done, el = _timed(run, budget_s)
+    return {"value": done / el, "unit": "tok/s", "cores": threads,
+            "sample": f"prefill_2048_h32 whole calls, {done // toks.ntokens} in {el:.1f} s"}
+
+
+def _oracle_verify(threads: int, budget_s: float):
+    """The oracle's ReplaySSM protocol model on 16 sequences of verify_b512_t4 (verify + commit per
+    step, flushes included): sequence-verify-steps/s."""
+    import oracle
+    w = synth.workload("verify_b512_t4")
+    S, K, T, L = 16, 8, w.drafts, w.dims.chunk
+    params, hist, drafts, acc = synth.verify_inputs(w, seed=0, batch=S, steps=K)
+    _, anchor = oracle.recurrence(hist.x, hist.dt, params.A, hist.B, hist.C, params.D, params.dt_bias,
+                                  np.arange(0, S * 32 + 1, 32), nthreads=threads)
+    sh = lambda a: a.reshape(K, S, T, *a.shape[1:])
+    dr = [[tuple(sh(a)[k, i] for a in (drafts.x, drafts.dt, drafts.B, drafts.C)) for i in range(S)] for k in range(K)]
+    state = {"m": None, "k": K}
+
+    def step():
+        if state["k"] == K:
+            state["m"], state["k"] = oracle.ReplaySSMModel(params, anchor, L, nthreads=threads), 0
+        k = state["k"]
+        state["m"].verify(dr[k])
+        state["m"].commit(acc[k])
+        state["k"] += 1
+        return S
+    done, el = _timed(step, budget_s)
+    return {"value": done / el, "unit": "seq-verify-steps/s", "cores": threads,
+            "sample": f"{S} of the 512 sequences x {done // S} verify + commit steps (bf16 read copy, L 16, "
+                      f"4 drafts), {el:.1f} s"}
+
+
 def cpu_baseline(seed: int, budget_s: float = 10.0):
     """fp64 oracle on this host's cores: decode seq-steps/s on a bounded sample of the B=256
-    workload (32 of the sequences advanced 16 steps per call, state carried, for ~budget_s)."""
+    workload (32 of the sequences advanced 16 steps per call, state carried, for ~budget_s), plus
+    the same on one core and, on all cores and on one, prefill_2048_h32 tokens/s and
+    verify_b512_t4 sequence-verify-steps/s (bounded samples of ~2 s each)."""
     o = _OracleDecode(seed, S=32, K=16)
     o.call()
-    done, t0 = 0, time.perf_counter()
-    while time.perf_counter() - t0 < budget_s:
-        done += o.call()
-    el = time.perf_counter() - t0
+    done, el = _timed(o.call, budget_s)
     d = o.d
-    return {"value": done / el, "unit": "seq-steps/s", "cores": o.threads, "kind": "oracle",
-            "sample": f"{o.S} of the 256 sequences x {done // o.S} decode steps, state carried (fp64 recurrence, "
-                      f"{d.nheads} heads, headdim {d.headdim}, dstate {d.dstate}), {el:.1f} s"}
+    out = {"value": done / el, "unit": "seq-steps/s", "cores": o.threads, "kind": "oracle",
+           "sample": f"{o.S} of the 256 sequences x {done // o.S} decode steps, state carried (fp64 recurrence, "
+                     f"{d.nheads} heads, headdim {d.headdim}, dstate {d.dstate}), {el:.1f} s"}
+    o1 = _OracleDecode(seed, S=8, K=4, threads=1)
+    done1, el1 = _timed(o1.call, 2.0)
+    out["decode_one_core"] = {"value": done1 / el1, "unit": "seq-steps/s", "cores": 1,
+                              "sample": f"8 sequences x {done1 // 8} decode steps, {el1:.1f} s"}
+    for name, fn in (("prefill_2048_h32", _oracle_prefill), ("verify_b512_t4", _oracle_verify)):
+        out[name] = {"all_cores": fn(o.threads, 2.0), "one_core": fn(1, 2.0)}
+    return out
 
 
 def reference_arm(args):
