@@ -859,7 +859,7 @@ def main(argv=None):
     hbm, tc, peak_kind = _peaks()
     if args.section is not None:
         if args.section == "prefill":
-            out = {n: bench_prefill(dev, n, 10, args.warmup, hbm, tc) for n in ("prefill_2048_h32", "varlen_4seq_h64")}
+            out = {n: bench_prefill(dev, n, 20, args.warmup, hbm, tc) for n in ("prefill_2048_h32", "varlen_4seq_h64")}
         elif args.section == "conv":
             out = bench_conv(dev, hbm)
         elif args.section == "gdn":
@@ -897,7 +897,7 @@ def main(argv=None):
 
     extra = {}
     if not args.decode_only:
-        extra["prefill"] = {n: bench_prefill(dev, n, 10, 3, hbm, tc) for n in ("prefill_2048_h32", "varlen_4seq_h64")}
+        extra["prefill"] = {n: bench_prefill(dev, n, 20, 3, hbm, tc) for n in ("prefill_2048_h32", "varlen_4seq_h64")}
         extra["verify"] = bench_verify(dev, 32, hbm)
         extra["verify_fp8"] = bench_verify(dev, 32, hbm, "fp8")
         extra["verify_nvfp4"] = bench_verify(dev, 32, hbm, "nvfp4")
