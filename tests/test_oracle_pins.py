@@ -283,6 +283,26 @@ def _protocol_case(seed, S=3, steps=9, T=4, L=16, N=4):
     return params, anchor, drafts, acc, L
 
 
+def test_protocol_flush_rule_hand_worked():
+    """The flush rule h + T > L (ReplaySSM "Core equations"; commit h = (flushed ? 0 : h) + accepted),
+    worked by hand for L = 5, T = 3 and acceptances 3, 0, 2, 3, 1, 3: the committed counts after
+    each commit are 3, 0, 2, 5, 1, 4 and flushes happen at steps 2 and 5 only (step 4 has h + T = L:
+    no flush).  Both protocol models (Mamba2 and GDN) follow it."""
+    L, T, acc = 5, 3, [3, 0, 2, 3, 1, 3]
+    want_h, want_flushes = [3, 0, 2, 5, 1, 4], [0, 1, 1, 1, 2, 2]
+    params, anchor, drafts, _, _ = _protocol_case(19, S=1, steps=len(acc), T=T, L=L)
+    m = oracle.ReplaySSMModel(params, anchor, L)
+    d = synth.GdnDims(2, 1, 4, 3, L)
+    rng = np.random.Generator(np.random.PCG64(20))
+    g = oracle.GdnReplayModel(rng.standard_normal((1, 2, 3, 4)), L)
+    for k, a in enumerate(acc):
+        m.verify(drafts[k]); m.commit([a])
+        t = synth.make_gdn_tokens(rng, T, d, False)
+        g.verify([(t.q, t.k, t.v, t.g, t.beta)]); g.commit([a])
+        assert int(m.h()[0]) == want_h[k] and m.flushes == want_flushes[k], k
+        assert int(g.h()[0]) == want_h[k] and g.flushes == want_flushes[k], k
+
+
 def test_protocol_zero_acceptance_keeps_anchor():
     params, anchor, drafts, _, L = _protocol_case(11)
     m = oracle.ReplaySSMModel(params, anchor, L)

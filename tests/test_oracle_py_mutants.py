@@ -1,0 +1,75 @@
+"""The pins must reject a broken oracle: the Python-side definitions (gated delta rule, its protocol
+model, stochastic rounding onto the e2m1 grid, the fp16 stochastic rounding).
+
+Each case plants one plausible mistake in a scratch copy of oracle/__init__.py (never in the
+committed file), lays out a scratch tree with that copy, the committed synth package and the pin
+suite, and runs the pins there in a subprocess (against the committed, already built C recurrence).
+Every mutant must fail at least one pin.
+"""
+import os
+import shutil
+import subprocess
+import sys
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+SRC = os.path.join(ROOT, "oracle", "__init__.py")
+
+MUTANTS = {
+    "gdn_delta_sign": ("u = beta[t][:, None] * (v[t] - a * Sk)", "u = beta[t][:, None] * (v[t] + a * Sk)"),
+    "gdn_missing_beta": ("u = beta[t][:, None] * (v[t] - a * Sk)", "u = v[t] - a * Sk"),
+    "gdn_state_not_decayed": ("S = a[:, :, None] * S + u[:, :, None] * kt[:, None, :]",
+                              "S = S + u[:, :, None] * kt[:, None, :]"),
+    "gdn_output_before_update": (
+        "        S = a[:, :, None] * S + u[:, :, None] * kt[:, None, :]\n"
+        "        out[t] = np.einsum(\"hdn,hn->hd\", S, qt)",
+        "        out[t] = np.einsum(\"hdn,hn->hd\", S, qt)\n"
+        "        S = a[:, :, None] * S + u[:, :, None] * kt[:, None, :]"),
+    "gdn_key_for_query": ("out[t] = np.einsum(\"hdn,hn->hd\", S, qt)", "out[t] = np.einsum(\"hdn,hn->hd\", S, kt)"),
+    "gdn_group_index_mod": ("hg = np.arange(H) // (H // G)", "hg = np.arange(H) % G"),
+    "gdn_flush_one_early": ("if len(self.committed[i]) + T > self.L and self.committed[i]:",
+                            "if len(self.committed[i]) + T >= self.L and self.committed[i]:"),
+    "mamba_flush_one_early": ("flush = [i for i in range(S) if len(self.committed[i]) + T > self.L]",
+                              "flush = [i for i in range(S) if len(self.committed[i]) + T >= self.L]"),
+    "sr_e2m1_inclusive_threshold": (
+        "frac = (a - lo) / step                                    # exact, in [0, 1)\n"
+        "    up = np.asarray(r, dtype=np.float64) < np.ldexp(frac, 32)",
+        "frac = (a - lo) / step                                    # exact, in [0, 1)\n"
+        "    up = np.asarray(r, dtype=np.float64) <= np.ldexp(frac, 32)"),
+    "sr_e2m1_step_of_one_below_two": ("step = np.where(a < 2.0, 0.5, np.where(a < 4.0, 1.0, 2.0))",
+                                      "step = np.where(a < 2.0, 1.0, np.where(a < 4.0, 1.0, 2.0))"),
+    "sr_fp16_spacing_off_by_one": ("ue = np.maximum(e - 1, -14) - 10", "ue = np.maximum(e - 1, -14) - 11"),
+}
+
+
+def _oracle_lib():
+    sys.path.insert(0, ROOT)
+    import oracle
+    return oracle._LIB_OVERRIDE or oracle._LIB_PATH
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_pins_reject_python_mutant(name, tmp_path):
+    before, after = MUTANTS[name]
+    src = open(SRC).read()
+    assert src.count(before) == 1, "mutation site no longer present (once) in oracle/__init__.py"
+    lib = _oracle_lib()
+    assert os.path.exists(lib), "the C oracle is built on import"
+    (tmp_path / "oracle").mkdir()
+    (tmp_path / "oracle" / "__init__.py").write_text(src.replace(before, after))
+    shutil.copy(os.path.join(ROOT, "oracle", "oracle.c"), tmp_path / "oracle" / "oracle.c")
+    shutil.copytree(os.path.join(ROOT, "synth"), tmp_path / "synth",
+                    ignore=shutil.ignore_patterns("__pycache__"))
+    (tmp_path / "tests").mkdir()
+    for f in ("conftest.py", "test_oracle_pins.py"):
+        shutil.copy(os.path.join(ROOT, "tests", f), tmp_path / "tests" / f)
+    golden = os.path.join(ROOT, "tests", "golden")
+    if os.path.isdir(golden):
+        shutil.copytree(golden, tmp_path / "tests" / "golden")
+    env = dict(os.environ, ERS_ORACLE_LIB=lib)
+    r = subprocess.run([sys.executable, "-m", "pytest", "-q", "-x", "-p", "no:cacheprovider",
+                        str(tmp_path / "tests" / "test_oracle_pins.py")],
+                       cwd=str(tmp_path), env=env, capture_output=True, text=True, timeout=300)
+    assert "passed" in r.stdout or "failed" in r.stdout, r.stdout[-2000:] + r.stderr[-2000:]
+    assert r.returncode != 0, f"mutant {name} passed every pin:\n{r.stdout[-2000:]}"
