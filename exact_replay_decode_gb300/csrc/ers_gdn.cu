@@ -2,7 +2,7 @@
 // notes, "Core equations": the GDN residuals u_j solve the triangular system
 //     u_j + sum_{i<j} beta_j gamma_{i+1:j} (k_i . k_j) u_i = beta_j (v_j - gamma_j S_ckpt k_j),
 // the state after h committed records is S_h = gamma_h S_ckpt + sum_j gamma_{j+1:h} u_j k_j^T, and a
-// draft's output is o_s = S_{h+s} q_s written in the same terms; "Data protocol": an empty
+// draft's output is o_s = S_{h+s} q_s written in the same terms; "Data protocol and entry point": an empty
 // committed history leaves the anchor unchanged and never runs an empty solve).
 //
 // Per (sequence, value head) the cache keeps an fp32 anchor S [dv, dk], a bf16 read copy cast from

@@ -316,7 +316,7 @@ ERS_API ers_status ers_ssu_update(const ers_dims* dims, const ers_params* prm, f
 /* ---------------------------------------------------------------------------------------------
  * Gated delta rule (GDN) layer: output-only speculative verify, refresh and commit (ReplaySSM notes,
  * "Core equations": GDN residuals solve u_j + sum_{i<j} beta_j gamma_{i+1:j} (k_i . k_j) u_i =
- * beta_j (v_j - gamma_j S_ckpt k_j); "Data protocol": an empty history leaves the anchor unchanged).
+ * beta_j (v_j - gamma_j S_ckpt k_j); "Data protocol and entry point": an empty history leaves the anchor unchanged).
  * Per value head h (key group h / (H/G)), token t: a_t = exp(g_t), u_t = beta_t (v_t - a_t S k_t),
  * S <- a_t S + u_t k_t^T, o_t = S q_t; S is [dv, dk] (maps keys to values).
  *

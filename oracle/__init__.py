@@ -379,8 +379,8 @@ def gdn_recurrence(q, k, v, g, beta, state: np.ndarray):
 
 class GdnReplayModel:
     """ReplaySSM-style speculative decoding for a GDN layer (ReplaySSM notes, "Core equations" and
-    "Data protocol"): per sequence an fp64 anchor, a read copy cast from it, and the committed
-    records since the last refresh.  verify() flushes when h + T > L (folds the committed records
+    "Data protocol and entry point"): per sequence an fp64 anchor, a read copy cast from it, and the
+    committed records since the last refresh.  verify() flushes when h + T > L (folds the committed records
     into the anchor with the recurrence, recasts the read copy), then runs the recurrence from the
     READ COPY over committed records + drafts and returns the drafts' outputs; commit() appends the
     accepted drafts.  An empty history leaves the anchor unchanged."""

@@ -1,6 +1,6 @@
 """Gated-delta-rule (GDN) output-only verify on the GPU (ReplaySSM notes, "Core equations": GDN
 residuals from the triangular system, outputs from the checkpoint and the residuals; "Data
-protocol": zero, partial and full acceptance, window refresh, no empty solve).  Verify outputs equal
+protocol and entry point": zero, partial and full acceptance, window refresh, no empty solve).  Verify outputs equal
 non-speculative (T = 1) verification over the same committed stream and refresh points bit for bit;
 the anchor never sees the read copy; parity with the oracle's stepwise recurrence."""
 import numpy as np
