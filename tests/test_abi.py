@@ -200,6 +200,19 @@ def test_validation_of_shared_nvfp4_state(lib):
                                    None, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 1 << 40, None, None) == 12
 
 
+def test_shared_state_cache_needs_an_nvfp4_copy():
+    import exact_replay_decode_gb300 as ers
+    with pytest.raises(ValueError):
+        ers.ReplayCache(2, 8, 2, 64, 128, 16, read_copy=True, read_dtype="bf16", anchor="nvfp4_sr_shared",
+                        device="cpu")
+    with pytest.raises(ValueError):
+        ers.ReplayCache(2, 8, 2, 64, 128, 16, read_copy=False, read_dtype="nvfp4", anchor="nvfp4_sr_shared",
+                        device="cpu")
+    c = ers.ReplayCache(2, 8, 2, 64, 128, 16, read_copy=True, read_dtype="nvfp4", anchor="nvfp4_sr_shared",
+                        device="cpu")
+    assert c.state is None and c.read_copy.shape == (2, 8, 64, 64) and c.read_block_scale.shape == (2, 8, 64, 8)
+
+
 @needs_no_gpu
 def test_validation_of_conv1d(lib):
     from exact_replay_decode_gb300 import _abi

@@ -119,3 +119,30 @@ def test_gdn_overflow_without_auto_flush():
     st = ers.Status(dev())
     ers.gdn_verify(c, q[1], k[1], v[1], g[1], beta[1], auto_flush=False, status=st, check=False)
     assert st.read() == 6                                          # ERS_EOVERFLOW
+
+
+def test_gdn_device_errors_are_reported_without_side_effects():
+    """Device-detected conditions go to the status word and leave the cache as it was: a slot index
+    out of range (ERS_ESLOT), a committed count out of [0, L] (ERS_EALIGN), an accepted count above
+    T (ERS_ECOMMIT)."""
+    ers = _ers()
+    d = synth.GdnDims(8, 4, 128, 128, 16)
+    S, T = 4, 4
+    anchor, toks, _ = synth.gdn_verify_inputs(76, S, 1, d, T)
+    q, k, v, g, beta = _drafts(toks, 1, S, T, torch.bfloat16)
+    c = _cache(ers, anchor, d)
+    before = (c.anchor.clone(), c.read_copy.clone(), c.pos.clone())
+    st = ers.Status(dev())
+    bad = torch.tensor([0, 1, 2, 99], dtype=torch.int32, device=dev())
+    ers.gdn_verify(c, q[0], k[0], v[0], g[0], beta[0], slot=bad, status=st, check=False)
+    assert st.read() == 8                                          # ERS_ESLOT
+    assert same_bits(c.anchor, before[0]) and same_bits(c.read_copy, before[1])
+    c.pos[1] = d.window + 3
+    st = ers.Status(dev())
+    ers.gdn_verify(c, q[0], k[0], v[0], g[0], beta[0], status=st, check=False)
+    assert st.read() == 5                                          # ERS_EALIGN
+    c.pos.copy_(before[2])
+    st = ers.Status(dev())
+    ers.gdn_commit(c, torch.tensor([0, T + 1, 1, 2], dtype=torch.int32, device=dev()), T, status=st, check=False)
+    assert st.read() == 7                                          # ERS_ECOMMIT
+    assert int(c.pos[1]) == 0
