@@ -29,6 +29,7 @@ namespace {
 
 using namespace wh;
 using tc::bulk_g2s;
+using tc::sw128;
 using tc::fence_mbar_init;
 using tc::mbar_arrive_expect_tx;
 using tc::mbar_init;
@@ -44,18 +45,22 @@ constexpr int kZ0 = kGT * kYS + 4;             // z table: 4 banks after y's
 
 // What only a flushing CTA uses; a CTA without a flush keeps a head's read copy in the same bytes.
 struct GdnFlush {
-  float vc[kGL][kGD];        // committed v
-  float kkf[kGL][kGL];       // k_i . k_r, committed rows
-  float cf[kGL][kGL];        // beta_r gamma_{i+1..r} (k_i . k_r), i < r
-  float yu[kGWarps][kGRows][kGL + 1];   // per warp and row, S k_i then the residual u_i (padded)
+  float vc[kGL][kGD];        // committed v (per head)
+  float cf[kGL][kGL];        // beta_r gamma_{i+1..r} (k_i . k_r), i < r (per head)
+  float yu[kGWarps][kGRows][kGL + 1];   // per warp and row, S k_i then the residual u_i (per head)
+  float kkf[kGL][kGL];       // k_i . k_r, committed rows (per group: past the read-copy tile's bytes)
 };
 
 // Every row array starts on a 16-byte boundary (lane quads are read as 16-byte vectors).
 struct GdnSmem {
-  union alignas(16) {
+  union alignas(1024) {
     GdnFlush f;
-    __nv_bfloat16 cb[kGD * kGD];   // without a flush: the head's read copy (one bulk copy)
+    // without a flush, or after a flush's fold: the head's read copy; fp32 io keeps it row-major
+    // (one bulk copy), bf16 io in the 128-byte-swizzled K-major operand layout of the tensor core
+    __nv_bfloat16 cb[kGD * kGD];
   } x;
+  // bf16 io: the drafts' key rows (operand rows 0..7) and query rows (8..15), swizzled, K = dk
+  alignas(1024) uint8_t bq[16 * kGD * 2];
   alignas(16) float k[kGL + kGT][kGD];   // committed rows 0..hc-1, drafts at kGL + s
   float q[kGT][kGD];
   float v[kGT][kGD];         // drafts' v
@@ -76,9 +81,13 @@ struct GdnSmem {
   float wq[kGL + kGT][kGT];  // drafts: gamma_{r+1..t} (k_r . q_s), r <= t
   float gam[kGT];            // drafts: gamma_{1..t}
   float gd[kGT];             // drafts' own log-gates (for the buffer)
-  uint64_t bar;              // completion of the read-copy bulk copies, one phase per head
+  uint64_t bar;
+  uint64_t mbar;             // bf16 io: completion of the drafts' MMAs, one phase per head
+  uint32_t tmem;             // bf16 io: the CTA's tensor-memory columns (32)              // completion of the read-copy bulk copies, one phase per head
 };
 static_assert(sizeof(GdnFlush) >= kGD * kGD * 2, "the read copy fits the flush arrays' bytes");
+static_assert(offsetof(GdnFlush, kkf) >= kGD * kGD * 2, "reloading a head's copy keeps the group's key products");
+static_assert(sizeof(GdnSmem) + 1024 + 1024 <= 228 * 1024 / 2, "two CTAs per SM (1 KB reserved per CTA)");
 static_assert(offsetof(GdnSmem, k) % 16 == 0 && offsetof(GdnSmem, q) % 16 == 0 && offsetof(GdnSmem, u) % 16 == 0 &&
                   offsetof(GdnSmem, v) % 16 == 0 &&
                   offsetof(GdnSmem, x) % 16 == 0 && offsetof(GdnSmem, bar) % 8 == 0,
@@ -108,6 +117,33 @@ __device__ __forceinline__ float sdot(const float* a, const float* b, int j) {
   lds4(a + 4 * j, qa);
   lds4(b + 4 * j, qb);
   return Dot<kGD>::reduce(Dot<kGD>::partial(qa, qb));
+}
+
+// bf16 io, the drafts' dot products on the tensor core: D[d][n] = sum_e S_read[d][e] Bq[n][e] for the
+// 16 operand rows n (k_s at n = s, q_s at n = 8 + s, zero rows for absent drafts): one
+// tcgen05.mma kind::f16 chain (M = 128 state rows, N = 16, K = dk in 8 steps of 16) into 16 TMEM
+// columns.  A column's result does not depend on the other columns, so a draft gets the same bits
+// whether it is one of several drafts or alone.
+constexpr int kBq = 16;   // operand rows of the drafts' tile
+
+__device__ __forceinline__ void copy_tile_async(uint8_t* tile, const __nv_bfloat16* __restrict__ src) {
+  for (int id = threadIdx.x; id < kGD * (kGD / 8); id += kThreads) {   // 16-byte chunks, swizzled
+    const int d = id >> 4, c = id & 15;
+    tc::cp_async16(tile + sw128(kGD, d, 8 * c), src + (size_t)d * kGD + 8 * c);
+  }
+}
+
+__device__ __forceinline__ void issue_draft_mma(uint32_t tmem_d, uint32_t aT, uint32_t bT) {
+  const uint32_t id = tc::idesc_bf16(128, kBq, false, false);
+#pragma unroll
+  for (int k = 0; k < kGD / 16; ++k) {
+    const uint32_t ao = (k >> 2) * (uint32_t)kGD * 128u + (k & 3) * 32u, bo = (k >> 2) * (uint32_t)kBq * 128u + (k & 3) * 32u;
+    tc::mma(tmem_d, tc::sdesc(aT + ao, 16, 1024), tc::sdesc(bT + bo, 16, 1024), id, k > 0);
+  }
+}
+
+__device__ __forceinline__ GdnSmem& gdn_smem(unsigned char* raw) {   // 1024-byte aligned (swizzled tiles)
+  return *reinterpret_cast<GdnSmem*>((reinterpret_cast<uintptr_t>(raw) + 1023) & ~uintptr_t(1023));
 }
 
 // S_src k_s and S_src q_s for the drafts (at most TM of them), RPG = 32 / (2 TM) rows per
@@ -360,8 +396,9 @@ __device__ __forceinline__ bool gdn_slot(const GdnArgs& a, int i, int* slot) {
 template <typename T, int TM>
 __global__ void __launch_bounds__(kThreads, TM == 4 ? 2 : 1) k_gdn_verify(GdnArgs a) {
   constexpr int RPG = 32 / (2 * TM);
+  constexpr bool kTc = std::is_same<T, __nv_bfloat16>::value;   // bf16 io: drafts' dots on the tensor core
   extern __shared__ __align__(16) unsigned char gsm_raw[];
-  GdnSmem& sm = *reinterpret_cast<GdnSmem*>(gsm_raw);
+  GdnSmem& sm = gdn_smem(gsm_raw);
   const int g = blockIdx.x, i = blockIdx.y, tid = threadIdx.x, w = tid >> 5, j = tid & 31;
   const int hpg = a.H / a.G;
   const int Td = a.T;
@@ -380,7 +417,14 @@ __global__ void __launch_bounds__(kThreads, TM == 4 ? 2 : 1) k_gdn_verify(GdnArg
   const int h0 = flush ? 0 : hc;   // committed rows that precede the drafts
   constexpr uint32_t kCopyBytes = kGD * kGD * 2;
   const __nv_bfloat16* Rg = (const __nv_bfloat16*)a.copy + (size_t)slot * a.H * kGD * kGD;   // the slot's copy
-  if (!flush && tid == 0) {   // the first head's read copy, in flight through the prologue
+  if constexpr (kTc) {
+    if (w == 0) tc::tmem_alloc(&sm.tmem, 32);
+    if (tid == 0) {
+      mbar_init(&sm.mbar, 1);
+      fence_mbar_init();
+    }
+    if (!flush) copy_tile_async((uint8_t*)sm.x.cb, Rg + (size_t)(g * hpg) * kGD * kGD);   // first head's copy
+  } else if (!flush && tid == 0) {   // the first head's read copy, in flight through the prologue
     mbar_init(&sm.bar, 1);
     fence_mbar_init();
     mbar_arrive_expect_tx(&sm.bar, kCopyBytes);
@@ -393,6 +437,19 @@ __global__ void __launch_bounds__(kThreads, TM == 4 ? 2 : 1) k_gdn_verify(GdnArg
     load_vec<T>((const T*)a.q + (tok * a.G + g) * kGD, sm.q[s]);
   }
   __syncthreads();
+  if constexpr (kTc) {   // the drafts' operand tile: row n = k_n (n < 8) or q_{n-8}; zeros past the drafts
+    const int n = tid >> 4, c = tid & 15, s = n & 7;
+    uint32_t pk[4] = {0u, 0u, 0u, 0u};
+    if (s < Td) {
+      const float* src = (n < 8 ? sm.k[kGL + s] : sm.q[s]) + 8 * c;
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const __nv_bfloat162 b2 = __floats2bfloat162_rn(src[2 * e], src[2 * e + 1]);   // bf16 values: exact
+        pk[e] = *reinterpret_cast<const uint32_t*>(&b2);
+      }
+    }
+    *reinterpret_cast<uint4*>(sm.bq + sw128(kBq, n, 8 * c)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+  }
   if (flush && hc > 0) flush_gram(sm, hc);
   // k_row . k_s (rows before draft s) and k_row . q_s (rows up to draft s), row r of the output rows
   for (int p = w; p < (h0 + Td) * Td; p += kGWarps) {
@@ -426,6 +483,38 @@ __global__ void __launch_bounds__(kThreads, TM == 4 ? 2 : 1) k_gdn_verify(GdnArg
       const float acc = ordered_prefix(gr, n, r);
       if (r < n) sm.gc[r] = acc;
     }
+    if constexpr (kTc) {
+      tc::publish();   // the head's copy (without a flush) and the drafts' tile, visible to the tensor core
+      if (flush && hc > 0) flush_coeffs(sm, hc);
+      draft_coeffs(sm, h0, Td);
+      if (flush) {
+        __syncthreads();
+        if (hc > 0) gdn_fold_rows<TM>(sm, a.anchor + soff, (__nv_bfloat16*)a.copy + soff, hc, 0, w, j);
+        __syncthreads();   // the new copy is written; the fold's arrays are free
+        copy_tile_async((uint8_t*)sm.x.cb, (const __nv_bfloat16*)a.copy + soff);
+        tc::publish();
+      }
+      if (tid == 0) {
+        issue_draft_mma(sm.tmem, tc::smem_u32(sm.x.cb), tc::smem_u32(sm.bq));
+        tc::commit(&sm.mbar);
+      }
+      mbar_wait(&sm.mbar, hh & 1, a.status);   // bounded; a wait that gave up has reported ERS_ETIMEOUT
+      tc::after_sync();
+      if (w < 4) {   // warp w reads TMEM lanes 32w..32w+31 = state rows d = tid
+        float dv[kBq];
+        tc::tmem_ld16(tc::taddr(sm.tmem, 32 * w, 0), dv);
+#pragma unroll
+        for (int s = 0; s < 8; ++s) {
+          if (s < Td) {
+            sm.yz[s * kYS + tid] = dv[s];
+            sm.yz[kZ0 + s * kYS + tid] = dv[8 + s];
+          }
+        }
+      }
+      tc::before_sync();
+      __syncthreads();   // y, z ready; the MMA has read the copy tile
+      if (!flush && hh + 1 < hpg) copy_tile_async((uint8_t*)sm.x.cb, Rg + (size_t)(h + 1) * kGD * kGD);
+    } else {
     // the head's read copy has landed (without a flush); a wait that gave up ends the CTA
     const bool late = !flush && !mbar_wait(&sm.bar, hh & 1, a.status);
     if (__syncthreads_or(late)) {
@@ -454,6 +543,7 @@ __global__ void __launch_bounds__(kThreads, TM == 4 ? 2 : 1) k_gdn_verify(GdnArg
     if (!flush && tid == 0 && hh + 1 < hpg) {   // every warp is done with this head's copy
       mbar_arrive_expect_tx(&sm.bar, kCopyBytes);
       bulk_g2s(sm.x.cb, Rg + (size_t)(h + 1) * kGD * kGD, kCopyBytes, &sm.bar);
+    }
     }
     // residuals, one state row d per thread, drafts in order (draft s needs the residuals before it)
     if (tid < kGD) {
@@ -494,6 +584,10 @@ __global__ void __launch_bounds__(kThreads, TM == 4 ? 2 : 1) k_gdn_verify(GdnArg
     const size_t row = (size_t)slot * a.L + h0 + s;
     store_vec<T>(sm.k[kGL + s], (T*)a.bk + (row * a.G + g) * kGD);
   }
+  if constexpr (kTc) {   // every TMEM read finished before the last head's barriers: free the columns
+    tc::after_sync();
+    if (w == 0) tc::tmem_dealloc(sm.tmem, 32);
+  }
 }
 
 // Standalone refresh: slots with h + T > L (T = drafts_T) and h > 0 fold their records exactly as a
@@ -501,7 +595,7 @@ __global__ void __launch_bounds__(kThreads, TM == 4 ? 2 : 1) k_gdn_verify(GdnArg
 template <typename T>
 __global__ void __launch_bounds__(kThreads, 2) k_gdn_refresh(GdnArgs a) {
   extern __shared__ __align__(16) unsigned char gsm_raw[];
-  GdnSmem& sm = *reinterpret_cast<GdnSmem*>(gsm_raw);
+  GdnSmem& sm = gdn_smem(gsm_raw);
   const int g = blockIdx.x, i = blockIdx.y, w = threadIdx.x >> 5, j = threadIdx.x & 31;
   const int hpg = a.H / a.G;
   int slot;
@@ -563,7 +657,7 @@ bool gdn_supported(int dk, int dv, int L, int T) {
 }
 
 cudaError_t gdn_launch(const GdnArgs& a, int kind, const int32_t* accepted, cudaStream_t s) {
-  const size_t sm = sizeof(GdnSmem);
+  const size_t sm = sizeof(GdnSmem) + 1024;   // + room to align the tiles to 1024 bytes
   cudaError_t e;
   if (kind == 2) {
     k_gdn_commit<<<(a.nseq + 255) / 256, 256, 0, s>>>(a, accepted);

@@ -82,6 +82,11 @@ def test_gdn_verify_full_size_sampled():
     _run(w["dims"], w["batch"], 8, w["drafts"], 75, [0, 257, 511])
 
 
+def test_gdn_verify_bf16_eight_drafts():
+    """Eight drafts with bf16 io: the 8-wide variant, its tensor-core dot products over 16 operand rows."""
+    _run(synth.GdnDims(8, 2, 128, 128, 16), 6, 10, 8, 77, [0, 5])
+
+
 def test_gdn_verify_fp32_io_short_window_long_drafts():
     _run(synth.GdnDims(8, 2, 128, 128, 8), 6, 14, 6, 72, [0, 5], io=torch.float32)
 
