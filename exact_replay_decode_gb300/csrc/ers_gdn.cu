@@ -9,7 +9,8 @@
 // it, and the committed records since the last refresh: k (per key group), v, the log-gate g and
 // beta, and the residual u_j that the verify that first saw the record computed from the read copy.
 // With those cached, a verify streams the read copy once, computing for each of its T drafts
-// S_read k_s and S_read q_s; the residuals and outputs then need only scalars per row.  A flush
+// S_read k_s and S_read q_s (bf16 io: one tensor-core MMA chain per head; fp32 io: CUDA-core
+// reduce-scatters); the residuals and outputs then need only scalars per row.  A flush
 // (h + T > L) folds the committed records into the anchor: one pass over the anchor rows computes
 // S k_i, solves the residuals and folds them, row by row, and casts the read copy from the same
 // fp32 values.  Fixed orders everywhere: gates are summed from the checkpoint in row order
@@ -391,7 +392,7 @@ __device__ __forceinline__ bool gdn_slot(const GdnArgs& a, int i, int* slot) {
 // One CTA per (sequence, key group); its value heads run one after another, so the group's key rows
 // are read once and the drafts' key rows are written after every head of the group has read the
 // committed ones (a flush reuses buffer rows from 0).
-// Two CTAs per SM (~102 KB of shared memory each) when the drafts' dots are 4 wide; the 8-wide
+// Two CTAs per SM (~113 KB of shared memory each) for up to 4 drafts; the 8-draft
 // variant needs more registers than two CTAs leave.
 template <typename T, int TM>
 __global__ void __launch_bounds__(kThreads, TM == 4 ? 2 : 1) k_gdn_verify(GdnArgs a) {
