@@ -87,6 +87,12 @@ def test_gdn_verify_bf16_eight_drafts():
     _run(synth.GdnDims(8, 2, 128, 128, 16), 6, 10, 8, 77, [0, 5])
 
 
+def test_gdn_verify_window_32():
+    """The widest window (L = 32): flushes fold up to 32 records, so the fold's first pass takes its
+    one-row-per-reduce-scatter branch (more than 16 records)."""
+    _run(synth.GdnDims(8, 2, 128, 128, 32), 8, 22, 4, 78, [0, 7])
+
+
 def test_gdn_verify_fp32_io_short_window_long_drafts():
     _run(synth.GdnDims(8, 2, 128, 128, 8), 6, 14, 6, 72, [0, 5], io=torch.float32)
 
