@@ -28,7 +28,7 @@ namespace {
 using namespace wh;
 
 constexpr int kDraftsMax = 4;
-constexpr int kVerifyRowsInFlight = 16;
+constexpr int kVerifyRowsInFlight = 8;
 
 template <typename T, int P, int N, int QM>
 constexpr size_t verify_smem_bytes() {
