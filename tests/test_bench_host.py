@@ -105,3 +105,20 @@ def test_profiled_traffic_is_null_once_the_kernel_changed(tmp_path):
     src.write_text("kernel v2")
     assert bench.profiled_traffic(str(prof), [str(src)]) is None
     assert bench.profiled_traffic(str(tmp_path / "missing.md"), [str(src)]) is None
+
+
+def test_copy_and_anchor_byte_counts():
+    """The per-sequence byte figures the secondary sections sum: the decode workload's 64 heads x 64
+    rows of 128 values; NVFP4 = half a byte per value + one e4m3 byte per 16 values + a 4-byte row
+    scale; FP8 = a byte per value + the row scale; the shared NVFP4 state has no separate anchor."""
+    sys.path.insert(0, ROOT)
+    import bench
+    import synth
+    d = synth.workload("decode_b256_h64").dims
+    rows = 64 * 64
+    assert bench._copy_bytes(d, "bf16") == rows * 128 * 2
+    assert bench._copy_bytes(d, "fp8") == rows * (128 + 4)
+    assert bench._copy_bytes(d, "nvfp4") == rows * (64 + 8 + 4) == 311296
+    assert bench._anchor_bytes(d, "fp32") == rows * 128 * 4 == 2 * 1024 * 1024
+    assert bench._anchor_bytes(d, "fp16_sr") == rows * 128 * 2
+    assert bench._anchor_bytes(d, "nvfp4_sr_shared") == 0
