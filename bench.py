@@ -388,6 +388,24 @@ def bench_prefill(dev, name: str, iters: int, warmup: int, hbm: float, tc: float
             "tflops": PREFILL_FLOPS[name] / (ms * 1e-3) / 1e12, "l2": "flushed before each call"}
 
 
+def flat_prefill(pf: dict, cpu: dict = None) -> dict:
+    """The SSD prefill figures as one flat object of scalars (the 2048-token workload's keys bare,
+    the varlen workload's prefixed), with the oracle's prefill tokens/s beside them when measured."""
+    a, v = pf["prefill_2048_h32"], pf["varlen_4seq_h64"]
+    out = {"workload": "prefill_2048_h32 (1 x 2048 tok, 32 heads / 1 group) and varlen_4seq_h64 "
+                       "({2048, 777, 513, 1}, 64 heads / 8 groups); headdim 64, dstate 128, chunk 256, bf16"}
+    for pre, r in (("", a), ("varlen_", v)):
+        for k in ("tok_per_s", "us_per_call", "achieved_gbs", "hbm_frac", "roofline_us", "tflops"):
+            out[pre + k] = r[k]
+        out[pre + "algorithmic_bytes"] = PREFILL_BYTES["prefill_2048_h32" if pre == "" else "varlen_4seq_h64"]
+    out["l2"] = a["l2"]
+    if cpu is not None:
+        out["cpu_tok_per_s"] = cpu.get("prefill_tok_per_s")
+        out["cpu_cores"] = cpu.get("cores")
+        out["cpu_tok_per_s_one_core"] = cpu.get("prefill_tok_per_s_one_core")
+    return out
+
+
 def _copy_bytes(d, read_dtype: str) -> int:
     """Bytes of one sequence's read copy: bf16 values; FP8 codes + an fp32 scale per row; NVFP4
     codes (half a byte per value) + an e4m3 scale per 16 values + an fp32 scale per row."""
@@ -794,10 +812,14 @@ def cpu_baseline(seed: int, budget_s: float = 10.0):
                      f"{d.nheads} heads, headdim {d.headdim}, dstate {d.dstate}), {el:.1f} s"}
     o1 = _OracleDecode(seed, S=8, K=4, threads=1)
     done1, el1 = _timed(o1.call, 2.0)
-    out["decode_one_core"] = {"value": done1 / el1, "unit": "seq-steps/s", "cores": 1,
-                              "sample": f"8 sequences x {done1 // 8} decode steps, {el1:.1f} s"}
-    for name, fn in (("prefill_2048_h32", _oracle_prefill), ("verify_b512_t4", _oracle_verify)):
-        out[name] = {"all_cores": fn(o.threads, 2.0), "one_core": fn(1, 2.0)}
+    # the other samples as flat scalars (value, then its sample text)
+    out["decode_one_core"] = done1 / el1
+    out["decode_one_core_sample"] = f"8 sequences x {done1 // 8} decode steps, 1 core, {el1:.1f} s"
+    for key, fn, unit in (("prefill", _oracle_prefill, "tok_per_s"), ("verify", _oracle_verify, "seq_verify_steps_per_s")):
+        for suffix, th in (("", o.threads), ("_one_core", 1)):
+            r = fn(th, 2.0)
+            out[f"{key}_{unit}{suffix}"] = r["value"]
+            out[f"{key}_sample{suffix}"] = f"{r['sample']}, {th} core(s)"
     return out
 
 
@@ -896,8 +918,10 @@ def main(argv=None):
     torch.cuda.empty_cache()
 
     extra = {}
+    pf = None
     if not args.decode_only:
-        extra["prefill"] = {n: bench_prefill(dev, n, 20, 3, hbm, tc) for n in ("prefill_2048_h32", "varlen_4seq_h64")}
+        pf = {n: bench_prefill(dev, n, 20, 3, hbm, tc) for n in ("prefill_2048_h32", "varlen_4seq_h64")}
+        extra["prefill"] = flat_prefill(pf)
         extra["verify"] = bench_verify(dev, 32, hbm)
         extra["verify_fp8"] = bench_verify(dev, 32, hbm, "fp8")
         extra["verify_nvfp4"] = bench_verify(dev, 32, hbm, "nvfp4")
@@ -936,8 +960,14 @@ def main(argv=None):
         "clocks": clocks,
     }
     line.update(extra)
+    if pf is not None:   # the SSD scan's own roofline fractions beside the decode kernel's
+        for pre, n in (("ssd_prefill_", "prefill_2048_h32"), ("ssd_prefill_varlen_", "varlen_4seq_h64")):
+            line["roofline"][pre + "us"] = pf[n]["us_per_call"]
+            line["roofline"][pre + "hbm_frac"] = pf[n]["hbm_frac"]
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(seed=7)
+        if pf is not None:
+            line["prefill"] = flat_prefill(pf, line["cpu_baseline"])
     if rank == 0:
         print(json.dumps(line))
     if ws > 1:

@@ -605,10 +605,46 @@ static __device__ __align__(256) unsigned char ers_scan_scratch[ERS_STATIC_SCRAT
 namespace {
 constexpr int kMaxScratchDevices = 64;
 std::mutex scratch_mu;
-void* scratch_addr[kMaxScratchDevices];
+struct ScratchEntry {
+  unsigned long long ctx_id;   // cuCtxGetId of the context the address belongs to (0: none yet)
+  void* addr;
+};
+ScratchEntry scratch_cache[kMaxScratchDevices];
 
-// Address of ers_scan_scratch on the current device, looked up once per device (with that device
-// current) and cached.
+typedef int (*CtxGetCurrentFn)(void**);
+typedef int (*CtxGetIdFn)(void*, unsigned long long*);
+
+// Process-unique id of the calling thread's current context (cuCtxGetCurrent + cuCtxGetId, reached
+// through the runtime's driver entry points so that the library needs no link against the driver),
+// or 0 when there is none or the driver cannot say.
+unsigned long long current_ctx_id() {
+  static CtxGetCurrentFn get_current = nullptr;
+  static CtxGetIdFn get_id = nullptr;
+  static bool looked_up = false;
+  if (!looked_up) {
+    looked_up = true;
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_current = reinterpret_cast<CtxGetCurrentFn>(f);
+    f = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &f, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_id = reinterpret_cast<CtxGetIdFn>(f);
+    cudaGetLastError();
+  }
+  if (get_current == nullptr || get_id == nullptr) return 0;
+  void* ctx = nullptr;
+  unsigned long long id = 0;
+  if (get_current(&ctx) != 0 || ctx == nullptr || get_id(ctx, &id) != 0) return 0;
+  return id;
+}
+
+// Address of ers_scan_scratch in the current device's current context.  The address is looked up
+// with that device current (cudaGetSymbolAddress) and cached together with the context's id; a
+// different context on the same device (after cudaDeviceReset, or a context the caller made
+// current) has its own copy of the array, so a changed id triggers a fresh lookup.
 ers_status static_scratch(void** out) {
   int dev = -1;
   if (cudaGetDevice(&dev) != cudaSuccess) {
@@ -617,15 +653,18 @@ ers_status static_scratch(void** out) {
   }
   if (dev < 0 || dev >= kMaxScratchDevices) return ERS_EUNSUPPORTED;
   std::lock_guard<std::mutex> lock(scratch_mu);
-  if (scratch_addr[dev] == nullptr) {
+  ScratchEntry& e = scratch_cache[dev];
+  const unsigned long long id = current_ctx_id();
+  if (e.addr == nullptr || id == 0 || e.ctx_id != id) {
     void* p = nullptr;
     if (cudaGetSymbolAddress(&p, ers_scan_scratch) != cudaSuccess || p == nullptr) {
       cudaGetLastError();
       return ERS_ECUDA;
     }
-    scratch_addr[dev] = p;
+    e.addr = p;
+    e.ctx_id = current_ctx_id();   // the lookup may have created the primary context
   }
-  *out = scratch_addr[dev];
+  *out = e.addr;
   return ERS_OK;
 }
 }  // namespace

@@ -280,9 +280,13 @@ __device__ __noinline__ void stream_flush_copy(AT* __restrict__ Hd, void* __rest
 constexpr int kPosBits = 16;
 constexpr int32_t kPosMask = (1 << kPosBits) - 1;
 
-__device__ __forceinline__ void advance_pos(int32_t* pos, int ncta, int32_t newp) {
+// Counts the calling CTA in the upper bits of a slot's position; the last of the slot's ncta CTAs
+// stores the new position and gets true.
+__device__ __forceinline__ bool advance_pos(int32_t* pos, int ncta, int32_t newp) {
   const int32_t old = atomicAdd(pos, 1 << kPosBits);
-  if ((old >> kPosBits) == ncta - 1) atomicExch(pos, newp);
+  if ((old >> kPosBits) != ncta - 1) return false;
+  atomicExch(pos, newp);
+  return true;
 }
 
 // HT: what the output stream reads (fp32 checkpoint, bf16 or FP8 read copy); W8: the read copy a
@@ -377,7 +381,18 @@ __global__ void __launch_bounds__(kThreads, 2) k_decode_heads(LaunchArgs a) {
   const df at = {__shfl_sync(kFull, v.hi, pn), __shfl_sync(kFull, v.lo, pn)};
   cp_async_wait_all();
   __syncthreads();
-  if (tid == 0) advance_pos(&a.pos[slot], ncta, refresh ? 0 : pn + 1);
+  // A fused flush stores the new token as buffer row 0, which is a committed record that every CTA
+  // of the slot folds.  With one CTA per group (nbl == 1) each group's rows are read and written by
+  // that CTA alone; with several, the group's B/C rows are written only by the slot's last CTA to
+  // count itself, after every CTA of the slot has finished reading its rows (fences on both sides
+  // of the count order those reads before the writes).
+  const bool shared_rows = flush && nbl > 1;
+  __shared__ int last_cta;
+  if (tid == 0) {
+    if (shared_rows) __threadfence();
+    last_cta = advance_pos(&a.pos[slot], ncta, refresh ? 0 : pn + 1);
+    if (shared_rows) __threadfence();
+  }
   for (int s = w; s <= pn; s += kHeadsPerCta) {
     float bs[4];
     lds4(sB + (o0 + s) * N + 4 * j, bs);
@@ -450,7 +465,14 @@ __global__ void __launch_bounds__(kThreads, 2) k_decode_heads(LaunchArgs a) {
   T* dx = (T*)a.bx + brow * HP + (size_t)h * P;
   for (int d = j; d < P; d += 32) dx[d] = sx[p * P + d];
   if (j == 0) a.bdt[brow * a.H + h] = a.dt[(size_t)i * a.H + h];
-  if (hl == 0) {
+  if (shared_rows) {
+    if (last_cta && w == 0) {   // every group's rows of the slot, from the new token's inputs
+      for (int e = j; e < a.G * N; e += 32) {
+        ((T*)a.bB)[brow * GN + e] = ((const T*)a.B)[(size_t)i * GN + e];
+        ((T*)a.bC)[brow * GN + e] = ((const T*)a.C)[(size_t)i * GN + e];
+      }
+    }
+  } else if (hl == 0) {
     const size_t dst = brow * GN + (size_t)g * N, src = (size_t)i * GN + (size_t)g * N;
     for (int n = j; n < N; n += 32) {
       ((T*)a.bB)[dst + n] = sB[p * N + n];

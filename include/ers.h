@@ -20,7 +20,9 @@
  *
  * Conventions shared by every entry point
  *  - All tensor pointers are DEVICE pointers to caller-owned, densely packed
- *    row-major memory with the shapes given below; the library keeps no pointer
+ *    row-major memory with the shapes given below.  The library takes no strides
+ *    (there are no stride descriptors and no stride status code): a caller holding
+ *    a strided view copies it to a dense buffer first.  The library keeps no pointer
  *    after a call returns and allocates no device or host memory.  Scratch
  *    memory, where needed, is a caller buffer sized by the matching
  *    *_workspace_size query.
@@ -415,11 +417,13 @@ ERS_API ers_status ers_conv1d_update(const ers_conv_dims* dims, int32_t nseq, co
  * call whose ers_ssd_scan_fwd_workspace_size exceeds it returns ERS_EWORKSPACE and launches
  * nothing (16 MiB holds, e.g., 2048 tokens x 32 heads x headdim 64 x dstate 128 at chunk 256,
  * which needs 8.4 MB).  Nothing in the scratch needs to start at zero: a call reads only bytes it
- * wrote earlier in the same call.  The first call on a device looks up the scratch address with
- * that device current (cudaGetSymbolAddress) and caches it; make one call on each device before
- * any stream capture.  Allocates nothing.  The scratch is shared: two calls on the same device
- * that can run at the same time (different streams, or different host threads) race on it and
- * must be serialised by the caller. */
+ * wrote earlier in the same call.  The first call in a context looks up the scratch address with
+ * that context current (cudaGetSymbolAddress) and caches it with the context's id; a call made
+ * in another context of the same device (after cudaDeviceReset, or with a context the caller
+ * created made current) has its own copy of the array and looks it up again.  Make one call in
+ * each context before any stream capture.  Allocates nothing.  The scratch is shared: two calls
+ * on the same device that can run at the same time (different streams, or different host
+ * threads) race on it and must be serialised by the caller. */
 #define ERS_STATIC_SCRATCH_BYTES ((size_t)16 << 20)
 ERS_API ers_status ers_ssd_scan_fwd_static(const ers_dims* dims, const ers_params* prm, int32_t nseq,
                                    int64_t ntokens, int32_t max_seqlen, const int32_t* cu_seqlens,

@@ -22,9 +22,57 @@ def layer(params):
     return ers.LayerParams(A, D, dtb)
 
 
+# Sanity bound on single elements: within a unit (one sequence and head), max|dy| may not exceed
+# this fraction of the unit's max|y|.  bf16 output rounding alone contributes at most 2^-8 of it
+# (half an ulp of the largest binade); read copies with 4- or 8-bit codes get a looser bound, since
+# one code the GPU's fp32 state and the oracle's fp64 state round to different sides moves an
+# output by a fraction of a block's largest value.
+MAX_REL_BF16 = 2.0 ** -6
+MAX_REL_NARROW = 2.0 ** -3
+
+
 def out_err(got: torch.Tensor, ref: np.ndarray) -> float:
     g = got.float().cpu().numpy().astype(np.float64)
     return float(np.abs(g - ref).mean() / np.abs(ref).mean())
+
+
+def unit_errs(got, ref: np.ndarray, keep, cu=None):
+    """Per-unit parity metrics.  A unit is one index of the `keep` axes (e.g. the head axis) within
+    one packed sequence (rows cu[i]:cu[i+1] of axis 0 when cu is given).  Returns the arrays
+    (mean|dy| / mean|y|, max|dy| / max|y|) over all units."""
+    g = got.float().cpu().numpy().astype(np.float64) if isinstance(got, torch.Tensor) else np.asarray(got, np.float64)
+    r = np.asarray(ref, np.float64)
+    assert g.shape == r.shape, (g.shape, r.shape)
+    keep = tuple(a % g.ndim for a in (keep if isinstance(keep, (tuple, list)) else (keep,)))
+    bounds = [(0, g.shape[0])] if cu is None else [(int(cu[i]), int(cu[i + 1])) for i in range(len(cu) - 1)]
+    means, maxes = [], []
+    for lo, hi in bounds:
+        if hi <= lo:
+            continue
+        gs, rs = g[lo:hi], r[lo:hi]
+        rest = [a for a in range(g.ndim) if a not in keep]
+        gu = np.transpose(gs, keep + tuple(rest)).reshape(-1, int(np.prod([gs.shape[a] for a in rest])))
+        ru = np.transpose(rs, keep + tuple(rest)).reshape(gu.shape)
+        d = np.abs(gu - ru)
+        means.append(d.mean(axis=1) / np.maximum(np.abs(ru).mean(axis=1), 1e-300))
+        maxes.append(d.max(axis=1) / np.maximum(np.abs(ru).max(axis=1), 1e-300))
+    return np.concatenate(means), np.concatenate(maxes)
+
+
+def check_out(got, ref: np.ndarray, tol: float, keep, cu=None, max_rel=MAX_REL_BF16, what: str = "") -> float:
+    """Asserts the output parity bar on the whole tensor AND on every unit (see unit_errs):
+    mean|dy| <= tol * mean|y| for both, and max|dy| <= max_rel * max|y| per unit (max_rel None skips
+    the element bound).  Returns the whole-tensor metric."""
+    whole = out_err(got, ref) if isinstance(got, torch.Tensor) else \
+        float(np.abs(np.asarray(got, np.float64) - ref).mean() / np.abs(ref).mean())
+    assert whole <= tol, f"{what} whole-tensor mean|dy|/mean|y| = {whole:.3e} > {tol:.1e}"
+    m, x = unit_errs(got, ref, keep, cu)
+    w = int(np.argmax(m))
+    assert m[w] <= tol, f"{what} unit {w}: mean|dy|/mean|y| = {m[w]:.3e} > {tol:.1e} (whole tensor {whole:.3e})"
+    if max_rel is not None:
+        w = int(np.argmax(x))
+        assert x[w] <= max_rel, f"{what} unit {w}: max|dy|/max|y| = {x[w]:.3e} > {max_rel:.3e}"
+    return whole
 
 
 def state_err(got: torch.Tensor, ref: np.ndarray) -> float:
@@ -46,3 +94,8 @@ def same_bits(a: torch.Tensor, b: torch.Tensor) -> bool:
 
 def out_tol(tokens) -> float:
     return OUT_TOL_BF16 if tokens.bf16 else OUT_TOL_F32
+
+
+def max_rel(tokens) -> float:
+    """Element bound of check_out: bf16 outputs as MAX_REL_BF16; fp32 outputs 1e-4 of the unit's max."""
+    return MAX_REL_BF16 if tokens.bf16 else 1e-4

@@ -9,7 +9,7 @@ import torch
 
 import oracle
 import synth
-from gpu_helpers import OUT_TOL_BF16, STATE_TOL, dev, out_err, same_bits, state_err
+from gpu_helpers import OUT_TOL_BF16, STATE_TOL, check_out, dev, same_bits, state_err
 
 pytestmark = pytest.mark.gpu
 
@@ -61,7 +61,7 @@ def _run(d, S, K, T, seed, samples, io=torch.bfloat16):
                     for f in ("q", "k", "v", "g", "beta")) for i in samples]
         o_ref = model.verify(dr)
         model.commit([int(acc[st, i]) for i in samples])
-        assert out_err(o[samples], o_ref) <= OUT_TOL_BF16, st
+        check_out(o[samples], o_ref, OUT_TOL_BF16, keep=(0, 2), what=f"GDN step {st}")   # per (sequence, head)
     assert flushes > 0
     assert torch.equal(cache.pos, ref.pos)
     assert same_bits(cache.anchor, ref.anchor) and same_bits(cache.read_copy, ref.read_copy)

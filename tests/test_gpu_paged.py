@@ -9,9 +9,10 @@ import numpy as np
 import pytest
 import torch
 
+import oracle
 import synth
 from synth import torch_io
-from gpu_helpers import dev, layer, same_bits
+from gpu_helpers import STATE_TOL, check_out, dev, layer, same_bits, state_err
 
 pytestmark = pytest.mark.gpu
 
@@ -55,11 +56,31 @@ def test_exact_decode_paged_equals_contiguous(chunk, page_rows):
     y1 = ers.chunked_prefill(c1, prm, hx, hdt, hB, hC, cu)
     assert same_bits(y0, y1)
     tok = torch_io.tokens_to(stream, dev(), lead=(K, S))
+    ys = []
     for k in range(K):
         a = ers.replay_decode(c0, prm, *(t[k] for t in tok))
         b = ers.replay_decode(c1, prm, *(t[k] for t in tok))
         assert same_bits(a, b), k
+        ys.append(b)
     assert same_bits(c0.state, c1.state) and torch.equal(c0.pos, c1.pos)
+    # the paged cache against the oracle: history outputs, decoded outputs per (sequence, head), and
+    # the boundary checkpoints
+    parts = [synth.Tokens.concat([hist[i]] + [stream.slice(k * S + i, k * S + i + 1) for k in range(K)])
+             for i in range(S)]
+    allt = synth.Tokens.concat(parts)
+    cu_o = np.concatenate([[0], np.cumsum([q.ntokens for q in parts])]).astype(np.int64)
+    y_o, _ = oracle.recurrence(allt.x, allt.dt, params.A, allt.B, allt.C, params.D, params.dt_bias, cu_o)
+    hl = [h.ntokens for h in hist]
+    y_hist = np.concatenate([y_o[cu_o[i]:cu_o[i] + hl[i]] for i in range(S)])
+    check_out(y1, y_hist, 2e-3, keep=1, cu=cu.cpu().numpy(), what="paged chunked prefill")
+    ref = np.stack([y_o[cu_o[i] + hl[i]:cu_o[i + 1]] for i in range(S)])                  # [S, K, H, P]
+    check_out(torch.stack(ys).transpose(0, 1), ref, 2e-3, keep=(0, 2), what="paged decode")
+    Q = d.chunk
+    nb = [(q.ntokens // Q) * Q for q in parts]
+    sel = np.concatenate([np.arange(cu_o[i], cu_o[i] + nb[i]) for i in range(S)]).astype(np.int64)
+    _, s_o = oracle.recurrence(allt.x[sel], allt.dt[sel], params.A, allt.B[sel], allt.C[sel], params.D,
+                               params.dt_bias, np.concatenate([[0], np.cumsum(nb)]))
+    assert state_err(c1.state, s_o) <= STATE_TOL
     for name in ("buf_x", "buf_dt", "buf_B", "buf_C"):
         for i in range(S):
             p = int(c0.pos[i])
@@ -83,12 +104,23 @@ def test_verify_paged_equals_contiguous():
         ers.refresh(c, prm, replayssm=True, drafts_T=L + 1)
     dx, ddt, dB, dC = torch_io.tokens_to(drafts, dev(), lead=(K, S, T))
     acc_t = torch.from_numpy(acc).to(dev())
+    # the oracle's protocol model (fp64 anchor, bf16 read copy) on every sequence of the paged cache
+    _, anchor = oracle.recurrence(hist.x, hist.dt, params.A, hist.B, hist.C, params.D, params.dt_bias,
+                                  np.arange(0, S * 32 + 1, 32))
+    model = oracle.ReplaySSMModel(params, anchor, L)
+    shp = {f: getattr(drafts, f).reshape(K, S, T, *getattr(drafts, f).shape[1:]) for f in ("x", "dt", "B", "C")}
     for k in range(K):
         a = ers.spec_verify(c0, prm, dx[k], ddt[k], dB[k], dC[k]); ers.commit(c0, acc_t[k], T)
         b = ers.spec_verify(c1, prm, dx[k], ddt[k], dB[k], dC[k]); ers.commit(c1, acc_t[k], T)
         assert same_bits(a, b), k
+        y_o = model.verify([tuple(np.ascontiguousarray(shp[f][k, i]) for f in ("x", "dt", "B", "C"))
+                            for i in range(S)])
+        model.commit([int(v) for v in acc[k]])
+        check_out(b, y_o, 2e-3, keep=(0, 2), what=f"paged verify step {k}")
     assert same_bits(c0.state, c1.state) and torch.equal(c0.pos, c1.pos)
     assert same_bits(c0.read_copy, c1.read_copy)
+    assert np.array_equal(c1.pos.cpu().numpy(), model.h())
+    assert state_err(c1.state, model.anchor) <= STATE_TOL
 
 
 def test_bad_page_index_is_reported_and_clamped():

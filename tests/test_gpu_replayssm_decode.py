@@ -13,7 +13,8 @@ import torch
 import oracle
 import synth
 from synth import torch_io
-from gpu_helpers import OUT_TOL_BF16, STATE_TOL, dev, layer, out_err, same_bits, state_err
+from gpu_helpers import (MAX_REL_BF16, MAX_REL_NARROW, OUT_TOL_BF16, STATE_TOL, check_out, dev, layer,
+                         same_bits, state_err)
 
 pytestmark = pytest.mark.gpu
 
@@ -65,7 +66,8 @@ def _run(dims, read_dtype, S, K, seed, samples):
         y_o = model.verify([(stream.x[r:r + 1], stream.dt[r:r + 1], stream.B[r:r + 1], stream.C[r:r + 1])
                             for r in rows])
         model.commit([1] * len(samples))
-        assert out_err(y1[samples], y_o[:, 0]) <= OUT_TOL_BF16, k
+        check_out(y1[samples], y_o[:, 0], OUT_TOL_BF16, keep=(0, 1),
+                  max_rel=MAX_REL_BF16 if read_dtype == "bf16" else MAX_REL_NARROW, what=f"step {k}")
     assert flushes > 0
     assert torch.equal(c1.pos, c2.pos) and same_bits(c1.state, c2.state)
     assert torch.equal(c1.read_copy.view(torch.uint8), c2.read_copy.view(torch.uint8))
@@ -88,3 +90,11 @@ def test_fused_flush_warp_per_head(read_dtype):
                          ids=["tensor-core-chunk64", "fma-p32n32"])
 def test_fused_flush_two_launch_engines(dims):
     _run(dims, "bf16", 12, 2 * dims.chunk + 5, 22, [0, 11])
+
+
+@pytest.mark.parametrize("read_dtype", ["bf16", "fp8", "nvfp4"])
+def test_fused_flush_group_spread_over_several_ctas(read_dtype):
+    """32 heads in one group: the group's heads span four CTAs of the decode kernel, all of which
+    fold the group's committed B rows while the flushing step stores the new token as buffer row 0.
+    Fused and separate refreshes still agree bit for bit, and outputs match the protocol model."""
+    _run(synth.Dims(32, 1, 64, 128, 16), read_dtype, 96, 40, 23, [0, 41, 95])

@@ -500,6 +500,61 @@ def test_nvfp4_values_are_codes_times_scales_within_bound():
     assert np.all(err <= 0.25 * np.abs(fb) + 0.25 * bs + 2.0 ** -4 * amax_b * 1.01)
 
 
+def _e2m1_nearest_even_f64(x):
+    """Brute-force e2m1 rounding of fp64 values (no intermediate fp32 rounding): nearest magnitude of
+    {0, 0.5, 1, 1.5, 2, 3, 4, 6}, ties to the even code, saturating at 6, sign kept."""
+    pv = np.array([0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0])
+    a = np.minimum(np.abs(np.asarray(x, np.float64)), 6.0)
+    d = np.abs(a[..., None] - pv)
+    dmin = d.min(axis=-1, keepdims=True)
+    near = d == dmin
+    # among equally near values take the one whose code is even (index parity = mantissa bit)
+    even = near & ((np.arange(8) % 2) == 0)
+    idx = np.where(even.any(axis=-1), np.argmax(even, axis=-1), np.argmax(near, axis=-1))
+    return np.sign(x) * pv[idx]
+
+
+def test_nvfp4_reciprocal_form_against_the_division_form():
+    """The oracle's NVFP4 codes are e2m1(u * RN(1/beta)) with fp32 reciprocal and product; the plain
+    definition of a block-scaled code is e2m1(u / beta).  RN(1/beta) and the fp32 product each add
+    at most 2^-24 relative error, so |u * rcp - u / beta| < 2^-22.9 |u / beta|: the two forms can only
+    differ where u / beta lies within that distance of a rounding midpoint (0.25, 0.75, 1.25, 1.75,
+    2.5, 3.5, 5), and there by one e2m1 step.  Exact ties are where they do differ."""
+    mids = np.array([0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5.0])
+    step = {0.25: 0.5, 0.75: 0.5, 1.25: 0.5, 1.75: 0.5, 2.5: 1.0, 3.5: 1.0, 5.0: 2.0}
+    # (1) exact ties: u = m * beta for every positive normal e4m3 beta in [2^-6, 448] and every midpoint
+    betas = np.unique(oracle.e4m3_round(np.exp2(np.linspace(-6, 8.8, 4000)).astype(np.float32)))
+    betas = betas[betas >= 2.0 ** -6]
+    n_diff = 0
+    for m in mids:
+        u = (m * betas).astype(np.float32)                                   # exact: <= 7 significant bits
+        assert np.array_equal(u.astype(np.float64), m * betas.astype(np.float64))
+        rcp = (np.float32(1.0) / betas.astype(np.float32)).astype(np.float32)
+        q_rcp = oracle.e2m1_round((u * rcp).astype(np.float32)).astype(np.float64)
+        q_div = _e2m1_nearest_even_f64(u.astype(np.float64) / betas.astype(np.float64))
+        diff = q_rcp != q_div
+        n_diff += int(diff.sum())
+        assert np.all(np.abs(q_rcp - q_div)[diff] == step[m])                # one step, never more
+        assert np.all(q_div == _e2m1_nearest_even_f64(np.full(len(betas), m)))   # division: ties to even
+    assert n_diff > 0                                                         # the readings do differ here
+    # (2) random states: codes of the oracle's cast against the division form with the oracle's scales
+    rng = np.random.Generator(np.random.PCG64(77))
+    a = rng.standard_normal((64, 64, 128)) * np.exp(rng.uniform(-6, 6, (64, 64, 1)))
+    r, q, beta, k = oracle.nvfp4_rows_round(a, parts=True)
+    u = (a.astype(np.float32).astype(np.float64) / np.exp2(k.astype(np.float64))[..., None])
+    ub = u.reshape(u.shape[:-1] + (8, 16))
+    bb = beta.astype(np.float64)[..., None]
+    with np.errstate(divide="ignore", invalid="ignore"):
+        ratio = np.where(bb > 0, ub / np.where(bb > 0, bb, 1.0), 0.0)
+    q_div = np.where(bb > 0, _e2m1_nearest_even_f64(ratio), 0.0)
+    qb = q.reshape(ub.shape).astype(np.float64)
+    diff = qb != q_div
+    near_mid = np.min(np.abs(np.abs(ratio)[..., None] - mids), axis=-1) <= 2.0 ** -22.9 * np.abs(ratio)
+    assert np.all(near_mid[diff])                                             # only next to a midpoint
+    assert np.all(np.abs(qb - q_div)[diff] <= 2.0)                            # by one step
+    assert diff.sum() <= 1e-4 * diff.size                                     # and rarely
+
+
 def test_philox4x32_10_known_answers():
     # the generator's published known-answer vectors (counter, key -> output)
     kat = [((0, 0, 0, 0), (0, 0), (0x6627E8D5, 0xE169C58D, 0xBC57AC4C, 0x9B00DBD8)),
