@@ -79,18 +79,62 @@ __device__ __forceinline__ uint64_t globaltimer() {
   return t;
 }
 
-// Waits for the phase with the given parity to complete.  Gives up after ~1 s (wall clock),
+// Default limit of every bounded wait in the library: 1 s of wall clock.
+constexpr uint64_t kWaitLimitNs = 1000000000ull;
+
+// Waits for the phase with the given parity to complete.  Gives up after limit_ns of wall clock,
 // reporting ERS_ETIMEOUT, so that no wait in this library can spin forever.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int32_t* status) {
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int32_t* status,
+                                          uint64_t limit_ns = kWaitLimitNs) {
   if (mbar_try(bar, parity)) return true;
   const uint64_t t0 = globaltimer();
   for (;;) {
     if (mbar_try(bar, parity)) return true;
-    if (globaltimer() - t0 > 1000000000ull) {
+    if (globaltimer() - t0 > limit_ns) {
       if (status != nullptr) atomicCAS(status, 0, ERS_ETIMEOUT);
       return false;
     }
   }
+}
+
+// ---- flags between CTAs of one launch (device scope) ----------------------------------------------
+__device__ __forceinline__ int32_t ld_acquire(const int32_t* p) {
+  int32_t v;
+  asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+__device__ __forceinline__ void st_release(int32_t* p, int32_t v) {
+  asm volatile("st.release.gpu.global.b32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+// Waits until *flag != 0 and returns its value (read with acquire semantics).  Gives up after
+// limit_ns of wall clock, reporting ERS_ETIMEOUT, and returns 0.
+__device__ __forceinline__ int32_t flag_wait(const int32_t* flag, int32_t* status, uint64_t limit_ns = kWaitLimitNs) {
+  int32_t v = ld_acquire(flag);
+  if (v != 0) return v;
+  const uint64_t t0 = globaltimer();
+  for (;;) {
+    __nanosleep(32);
+    v = ld_acquire(flag);
+    if (v != 0) return v;
+    if (globaltimer() - t0 > limit_ns) {
+      if (status != nullptr) atomicCAS(status, 0, ERS_ETIMEOUT);
+      return 0;
+    }
+  }
+}
+
+// ---- TMA (tensor-map bulk copies, this GPU's own memory, no multicast) -----------------------------
+// 3-D tiled load of the box at coordinates (x, y, z) (x innermost, in elements) into shared memory,
+// completion counted on `bar` in bytes.  x * element size must be a multiple of 16 bytes.
+__device__ __forceinline__ void tma_load_3d(void* dst, const void* map, int x, int y, int z, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], [%5];"
+      ::"r"(smem_u32(dst)), "l"(map), "r"(x), "r"(y), "r"(z), "r"(smem_u32(bar))
+      : "memory");
+}
+__device__ __forceinline__ void tma_prefetch_desc(const void* map) {
+  asm volatile("prefetch.tensormap [%0];" ::"l"(map) : "memory");
 }
 
 __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {

@@ -99,3 +99,26 @@ def out_tol(tokens) -> float:
 def max_rel(tokens) -> float:
     """Element bound of check_out: bf16 outputs as MAX_REL_BF16; fp32 outputs 1e-4 of the unit's max."""
     return MAX_REL_BF16 if tokens.bf16 else 1e-4
+
+
+class StepCheck:
+    """Parity over a run of steps: each step's whole output tensor is held to `tol` when it arrives,
+    and at the end every unit (the `keep` axes of one step's tensor, e.g. sequence and head) is held
+    to check_out's bars over all steps together, so that a unit holds as many outputs as the run
+    gives it rather than one noisy row."""
+
+    def __init__(self, tol: float, keep, max_rel=MAX_REL_BF16, what: str = ""):
+        self.tol, self.keep, self.max_rel, self.what = tol, tuple(keep), max_rel, what
+        self.got, self.ref = [], []
+
+    def step(self, got, ref, label=""):
+        g = got.float().cpu().numpy().astype(np.float64)
+        r = np.asarray(ref, np.float64)
+        e = float(np.abs(g - r).mean() / np.abs(r).mean())
+        assert e <= self.tol, f"{self.what} {label}: whole-step mean|dy|/mean|y| = {e:.3e} > {self.tol:.1e}"
+        self.got.append(g)
+        self.ref.append(r)
+
+    def finish(self):
+        return check_out(np.stack(self.got), np.stack(self.ref), self.tol, keep=tuple(k + 1 for k in self.keep),
+                         max_rel=self.max_rel, what=self.what + " (all steps)")

@@ -9,7 +9,7 @@ import torch
 
 import oracle
 import synth
-from gpu_helpers import OUT_TOL_BF16, STATE_TOL, check_out, dev, same_bits, state_err
+from gpu_helpers import OUT_TOL_BF16, STATE_TOL, StepCheck, dev, same_bits, state_err
 
 pytestmark = pytest.mark.gpu
 
@@ -41,6 +41,7 @@ def _run(d, S, K, T, seed, samples, io=torch.bfloat16):
     acc_t = torch.from_numpy(acc).to(dev())
     model = oracle.GdnReplayModel(anchor[samples].astype(np.float64), d.window)
     flushes = 0
+    chk = StepCheck(OUT_TOL_BF16, keep=(0, 2), what="GDN verify")   # per (sequence, head) over all steps
     for st in range(K):
         flushes += int(((cache.pos + T) > d.window).sum())
         o = ers.gdn_verify(cache, q[st], k[st], v[st], g[st], beta[st])
@@ -61,7 +62,8 @@ def _run(d, S, K, T, seed, samples, io=torch.bfloat16):
                     for f in ("q", "k", "v", "g", "beta")) for i in samples]
         o_ref = model.verify(dr)
         model.commit([int(acc[st, i]) for i in samples])
-        check_out(o[samples], o_ref, OUT_TOL_BF16, keep=(0, 2), what=f"GDN step {st}")   # per (sequence, head)
+        chk.step(o[samples], o_ref, f"step {st}")
+    chk.finish()
     assert flushes > 0
     assert torch.equal(cache.pos, ref.pos)
     assert same_bits(cache.anchor, ref.anchor) and same_bits(cache.read_copy, ref.read_copy)

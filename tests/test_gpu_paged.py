@@ -12,7 +12,7 @@ import torch
 import oracle
 import synth
 from synth import torch_io
-from gpu_helpers import STATE_TOL, check_out, dev, layer, same_bits, state_err
+from gpu_helpers import STATE_TOL, StepCheck, check_out, dev, layer, same_bits, state_err
 
 pytestmark = pytest.mark.gpu
 
@@ -108,6 +108,7 @@ def test_verify_paged_equals_contiguous():
     _, anchor = oracle.recurrence(hist.x, hist.dt, params.A, hist.B, hist.C, params.D, params.dt_bias,
                                   np.arange(0, S * 32 + 1, 32))
     model = oracle.ReplaySSMModel(params, anchor, L)
+    chk = StepCheck(2e-3, keep=(0, 2), what="paged verify")
     shp = {f: getattr(drafts, f).reshape(K, S, T, *getattr(drafts, f).shape[1:]) for f in ("x", "dt", "B", "C")}
     for k in range(K):
         a = ers.spec_verify(c0, prm, dx[k], ddt[k], dB[k], dC[k]); ers.commit(c0, acc_t[k], T)
@@ -116,7 +117,8 @@ def test_verify_paged_equals_contiguous():
         y_o = model.verify([tuple(np.ascontiguousarray(shp[f][k, i]) for f in ("x", "dt", "B", "C"))
                             for i in range(S)])
         model.commit([int(v) for v in acc[k]])
-        check_out(b, y_o, 2e-3, keep=(0, 2), what=f"paged verify step {k}")
+        chk.step(b, y_o, f"step {k}")
+    chk.finish()
     assert same_bits(c0.state, c1.state) and torch.equal(c0.pos, c1.pos)
     assert same_bits(c0.read_copy, c1.read_copy)
     assert np.array_equal(c1.pos.cpu().numpy(), model.h())

@@ -13,8 +13,8 @@ import torch
 import oracle
 import synth
 from synth import torch_io
-from gpu_helpers import (MAX_REL_BF16, MAX_REL_NARROW, OUT_TOL_BF16, STATE_TOL, check_out, dev, layer,
-                         same_bits, state_err)
+from gpu_helpers import (MAX_REL_BF16, MAX_REL_NARROW, OUT_TOL_BF16, STATE_TOL, StepCheck, dev, layer, same_bits,
+                         state_err)
 
 pytestmark = pytest.mark.gpu
 
@@ -55,6 +55,8 @@ def _run(dims, read_dtype, S, K, seed, samples):
     cast = {"fp8": oracle.fp8_rows_round, "nvfp4": oracle.nvfp4_rows_round}.get(read_dtype)
     model = oracle.ReplaySSMModel(params, anchor, L, read_cast=cast)
     flushes = 0
+    chk = StepCheck(OUT_TOL_BF16, keep=(0, 1), max_rel=MAX_REL_BF16 if read_dtype == "bf16" else MAX_REL_NARROW,
+                    what=f"ReplaySSM decode ({read_dtype} copy)")   # per (sequence, head)
     for k in range(K):
         x, dt, B, C = (t[k] for t in tok)
         flushes += int((c1.pos == L).sum())
@@ -66,8 +68,8 @@ def _run(dims, read_dtype, S, K, seed, samples):
         y_o = model.verify([(stream.x[r:r + 1], stream.dt[r:r + 1], stream.B[r:r + 1], stream.C[r:r + 1])
                             for r in rows])
         model.commit([1] * len(samples))
-        check_out(y1[samples], y_o[:, 0], OUT_TOL_BF16, keep=(0, 1),
-                  max_rel=MAX_REL_BF16 if read_dtype == "bf16" else MAX_REL_NARROW, what=f"step {k}")
+        chk.step(y1[samples], y_o[:, 0], f"step {k}")
+    chk.finish()
     assert flushes > 0
     assert torch.equal(c1.pos, c2.pos) and same_bits(c1.state, c2.state)
     assert torch.equal(c1.read_copy.view(torch.uint8), c2.read_copy.view(torch.uint8))

@@ -18,7 +18,7 @@ import torch
 import oracle
 import synth
 from synth import torch_io
-from gpu_helpers import MAX_REL_NARROW, OUT_TOL_BF16, check_out, dev, layer, same_bits
+from gpu_helpers import MAX_REL_NARROW, OUT_TOL_BF16, StepCheck, dev, layer, same_bits
 
 pytestmark = pytest.mark.gpu
 
@@ -93,6 +93,7 @@ def test_fused_flush_equals_refresh_and_decode_and_matches_the_model():
     model = oracle.ReplaySSMModel(params, a0, L, shared=True,
                                   anchor_round=lambda i, f: oracle.nvfp4_sr_state(f, KEY, nonce["v"], samples[i]))
     tok = torch_io.tokens_to(stream, dev(), lead=(K, S))
+    chk = StepCheck(OUT_TOL_BF16, keep=(0, 1), max_rel=MAX_REL_NARROW, what="ReplaySSM decode")
     flushes = 0
     for k in range(K):
         nonce["v"] = c1.sr_nonce = c2.sr_nonce = 3000 + k
@@ -105,7 +106,8 @@ def test_fused_flush_equals_refresh_and_decode_and_matches_the_model():
         y_o = model.verify([(stream.x[r:r + 1], stream.dt[r:r + 1], stream.B[r:r + 1], stream.C[r:r + 1])
                             for r in rows])
         model.commit([1] * len(samples))
-        check_out(y1[samples], y_o[:, 0], OUT_TOL_BF16, keep=(0, 1), max_rel=MAX_REL_NARROW, what=f"step {k}")
+        chk.step(y1[samples], y_o[:, 0], f"step {k}")
+    chk.finish()
     assert flushes > 0 and model.flushes > 0
     assert torch.equal(c1.pos, c2.pos) and _same_copy(_copy_bytes(c1), _copy_bytes(c2))
     # the GPU folds in fp32 and the model in fp64: a stochastic decision flips only where the two

@@ -19,7 +19,7 @@ import torch
 import oracle
 import synth
 from synth import torch_io
-from gpu_helpers import MAX_REL_NARROW, OUT_TOL_BF16, check_out, dev, layer, same_bits
+from gpu_helpers import MAX_REL_NARROW, OUT_TOL_BF16, StepCheck, dev, layer, same_bits
 
 pytestmark = pytest.mark.gpu
 
@@ -137,6 +137,7 @@ def test_fused_flush_and_verify_with_sr_anchors():
     model = oracle.ReplaySSMModel(params, anchor0, L, read_cast=oracle.nvfp4_rows_round,
                                   anchor_round=lambda i, fin: oracle.sr_fp16_anchor(fin, KEY, nonce["v"],
                                                                                     samples[i]))
+    chk = StepCheck(OUT_TOL_BF16, keep=(0, 1), max_rel=MAX_REL_NARROW, what="ReplaySSM decode")
     flushes = 0
     for k in range(K):
         nonce["v"] = 1000 + k
@@ -150,7 +151,8 @@ def test_fused_flush_and_verify_with_sr_anchors():
         y_o = model.verify([(stream.x[r:r + 1], stream.dt[r:r + 1], stream.B[r:r + 1], stream.C[r:r + 1])
                             for r in rows])
         model.commit([1] * len(samples))
-        check_out(y1[samples], y_o[:, 0], OUT_TOL_BF16, keep=(0, 1), max_rel=MAX_REL_NARROW, what=f"step {k}")
+        chk.step(y1[samples], y_o[:, 0], f"step {k}")
+    chk.finish()
     assert flushes > 0
     assert same_bits(c1.state, c2.state) and torch.equal(c1.pos, c2.pos)
     assert torch.equal(c1.read_copy, c2.read_copy) and torch.equal(c1.read_block_scale, c2.read_block_scale)

@@ -9,7 +9,7 @@ import torch
 import oracle
 import synth
 from synth import torch_io
-from gpu_helpers import STATE_TOL, check_out, dev, layer, same_bits, state_err
+from gpu_helpers import STATE_TOL, StepCheck, dev, layer, same_bits, state_err
 
 pytestmark = pytest.mark.gpu
 
@@ -43,6 +43,7 @@ def _verify_vs_nonspec(w, S, K, seed, samples):
     dx, ddt, dB, dC = torch_io.tokens_to(drafts, dev(), lead=(K, S, T))
     acc_t = torch.from_numpy(acc).to(dev())
     model = oracle.ReplaySSMModel(params, _oracle_anchor(params, hist, samples, 32), L)
+    chk = StepCheck(2e-3, keep=(0, 2), what="verify")   # per (sequence, head) over all steps and drafts
     for k in range(K):
         y = ers.spec_verify(cache, prm, dx[k], ddt[k], dB[k], dC[k])
         ers.commit(cache, acc_t[k], T)
@@ -63,7 +64,8 @@ def _verify_vs_nonspec(w, S, K, seed, samples):
                     for f in ("x", "dt", "B", "C")) for i in samples]
         y_o = model.verify(dr)
         model.commit([int(acc[k, i]) for i in samples])
-        check_out(y[samples], y_o, 2e-3, keep=(0, 2), what=f"verify step {k}")   # per (sequence, head)
+        chk.step(y[samples], y_o, f"step {k}")
+    chk.finish()
     assert torch.equal(cache.pos, ref.pos)
     assert same_bits(cache.state, ref.state) and same_bits(cache.read_copy, ref.read_copy)
     assert np.array_equal(cache.pos.cpu().numpy()[samples], model.h())
