@@ -37,7 +37,7 @@ EXPORTS = (
     "ers_status_str", "ers_version", "ers_ssd_scan_fwd_workspace_size", "ers_ssd_scan_fwd",
     "ers_chunked_prefill_workspace_size", "ers_chunked_prefill", "ers_replay_decode", "ers_refresh",
     "ers_spec_verify", "ers_commit", "ers_ssu_update", "ers_ssd_scan_fwd_static", "ers_conv1d_fwd",
-    "ers_conv1d_update", "ers_gdn_verify", "ers_gdn_commit", "ers_gdn_refresh",
+    "ers_conv1d_update", "ers_gdn_verify", "ers_gdn_commit", "ers_gdn_refresh", "ers_selftest_bounded_wait",
 )
 
 
@@ -99,6 +99,7 @@ _CACHE = ctypes.POINTER(Cache)
 _SIGS = {
     "ers_status_str": ([_I32], ctypes.c_char_p),
     "ers_version": ([], _I32),
+    "ers_selftest_bounded_wait": ([ctypes.c_uint64, _P, _P], _I32),
     "ers_ssd_scan_fwd_workspace_size": ([_DIMS, _I32, _I32], _SZ),
     "ers_chunked_prefill_workspace_size": ([_DIMS, _I32, _I32], _SZ),
     "ers_ssd_scan_fwd": ([_DIMS, _PRM, _I32, _I64, _I32, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _SZ, _P, _P], _I32),

@@ -133,20 +133,24 @@ void set_cache(LaunchArgs& a, const ers_cache* c) {
   a.nslots = c->nslots;
 }
 
-struct Workspace {
-  size_t states, tot, decay, total;
-};
-
-// Prefill scratch: per (sequence, chunk, head) the chunk state (later the state at the chunk's
-// start), the chunk's total log-decay, and its rows' delta and log-decay prefix.
-Workspace prefill_workspace(const ers_dims* d, int32_t nseq, int32_t max_chunks) {
-  Workspace w;
+// Prefill scratch.  CUDA-core engine: per (sequence, chunk, head) the chunk state (later the state
+// at the chunk's start) and the chunk's total log-decay.  Tensor-core engine: the single-pass scan's
+// chunk states, chunk end states, decay factors and look-back flags (tc_scan_workspace).
+size_t prefill_workspace(const ers_dims* d, int32_t nseq, int32_t max_chunks) {
+  if (ers::tc_supported(d->io_dtype, d->headdim, d->dstate, d->chunk))
+    return ers::tc_scan_workspace(nseq, max_chunks, d->nheads);
   const size_t units = (size_t)(nseq > 0 ? nseq : 0) * (size_t)(max_chunks > 0 ? max_chunks : 0) * d->nheads;
-  w.states = ers::align256(units * d->headdim * d->dstate * sizeof(float));
-  w.tot = ers::align256(units * sizeof(float));
-  w.decay = ers::align256(units * 3 * (size_t)d->chunk * sizeof(float));
-  w.total = w.states + w.tot + w.decay;
-  return w;
+  return ers::align256(units * d->headdim * d->dstate * sizeof(float)) + ers::align256(units * sizeof(float));
+}
+
+void carve_workspace(LaunchArgs& a, void* workspace) {
+  if (ers::tc_supported(a.io, a.P, a.N, a.Q)) {
+    ers::tc_scan_carve(a, workspace);
+    return;
+  }
+  const size_t units = (size_t)a.nseq * (size_t)a.max_chunks * a.H;
+  a.ws_states = (float*)workspace;
+  a.ws_tot = (float*)((char*)workspace + ers::align256(units * a.P * a.N * sizeof(float)));
 }
 
 int32_t scan_chunks(int32_t max_seqlen, int32_t Q) { return (max_seqlen + Q - 1) / Q; }
@@ -185,16 +189,22 @@ const char* ers_status_str(ers_status s) {
   }
 }
 
-int32_t ers_version(void) { return 100; }
+int32_t ers_version(void) { return 200; }
+
+ers_status ers_selftest_bounded_wait(uint64_t limit_ns, ers_stream_t stream, int32_t* dev_status) {
+  if (dev_status == nullptr || limit_ns == 0 || limit_ns > 10000000000ull) return ERS_EINVAL;
+  ERS_TRY(check_ptr(dev_status, true));
+  return finish(ers::wait_selftest(limit_ns, dev_status, (cudaStream_t)stream));
+}
 
 size_t ers_ssd_scan_fwd_workspace_size(const ers_dims* dims, int32_t nseq, int32_t max_seqlen) {
   if (check_dims(dims) != ERS_OK || nseq < 0 || max_seqlen < 0) return 0;
-  return prefill_workspace(dims, nseq, scan_chunks(max_seqlen, dims->chunk)).total;
+  return prefill_workspace(dims, nseq, scan_chunks(max_seqlen, dims->chunk));
 }
 
 size_t ers_chunked_prefill_workspace_size(const ers_dims* dims, int32_t nseq, int32_t max_seqlen) {
   if (check_dims(dims) != ERS_OK || nseq < 0 || max_seqlen < 0) return 0;
-  return prefill_workspace(dims, nseq, resume_chunks(max_seqlen, dims->chunk)).total;
+  return prefill_workspace(dims, nseq, resume_chunks(max_seqlen, dims->chunk));
 }
 
 ers_status ers_ssd_scan_fwd(const ers_dims* dims, const ers_params* prm, int32_t nseq, int64_t ntokens,
@@ -214,21 +224,20 @@ ers_status ers_ssd_scan_fwd(const ers_dims* dims, const ers_params* prm, int32_t
   ERS_TRY(check_ptr(chunk_states, false));
   ERS_TRY(check_ptr(dev_status, false));
   const int32_t mc = scan_chunks(max_seqlen, dims->chunk);
-  const Workspace w = prefill_workspace(dims, nseq, mc);
-  if (w.total > 0 && (workspace == nullptr || workspace_bytes < w.total)) return ERS_EWORKSPACE;
+  const size_t wsz = prefill_workspace(dims, nseq, mc);
+  if (wsz > 0 && (workspace == nullptr || workspace_bytes < wsz)) return ERS_EWORKSPACE;
   ERS_TRY(check_ptr(workspace, false));
   LaunchArgs a = base_args(dims, prm);
   a.x = x; a.dt = dt; a.B = B; a.C = C;
   a.cu = cu_seqlens;
   a.nseq = nseq;
+  a.ntokens = ntokens;
   a.max_chunks = mc;
   a.y = y;
   a.init_state = init_state;
   a.final_state = final_state;
   a.chunk_states = chunk_states;
-  a.ws_states = (float*)workspace;
-  a.ws_tot = (float*)((char*)workspace + w.states);
-  a.ws_decay = (float*)((char*)workspace + w.states + w.tot);
+  carve_workspace(a, workspace);
   a.status = dev_status;
   if (ers::tc_supported(a.io, a.P, a.N, a.Q)) return finish(ers::tc_prefill(a, ers::Op::kScan, (cudaStream_t)stream));
   return finish(ers::fma_prefill(a, ers::Op::kScan, (cudaStream_t)stream));
@@ -253,8 +262,8 @@ ers_status ers_chunked_prefill(const ers_dims* dims, const ers_params* prm, cons
   ERS_TRY(check_ptr(y, ntokens > 0));
   ERS_TRY(check_ptr(dev_status, false));
   const int32_t mc = resume_chunks(max_seqlen, dims->chunk);
-  const Workspace w = prefill_workspace(dims, nseq, mc);
-  if (w.total > 0 && (workspace == nullptr || workspace_bytes < w.total)) return ERS_EWORKSPACE;
+  const size_t wsz = prefill_workspace(dims, nseq, mc);
+  if (wsz > 0 && (workspace == nullptr || workspace_bytes < wsz)) return ERS_EWORKSPACE;
   ERS_TRY(check_ptr(workspace, false));
   LaunchArgs a = base_args(dims, prm);
   set_cache(a, cache);
@@ -262,11 +271,10 @@ ers_status ers_chunked_prefill(const ers_dims* dims, const ers_params* prm, cons
   a.cu = cu_seqlens;
   a.slot = slot;
   a.nseq = nseq;
+  a.ntokens = ntokens;
   a.max_chunks = mc;
   a.y = y;
-  a.ws_states = (float*)workspace;
-  a.ws_tot = (float*)((char*)workspace + w.states);
-  a.ws_decay = (float*)((char*)workspace + w.states + w.tot);
+  carve_workspace(a, workspace);
   a.status = dev_status;
   if (ers::tc_supported(a.io, a.P, a.N, a.Q))
     return finish(ers::tc_prefill(a, ers::Op::kChunkedPrefill, (cudaStream_t)stream));

@@ -16,7 +16,6 @@
 
 #include "ers_common.cuh"
 #include "ers_internal.h"
-#include "tc_engine.cuh"
 
 namespace ers {
 namespace {
@@ -229,17 +228,7 @@ __global__ void __launch_bounds__(kThreads) k_prefill_chain(LaunchArgs a, bool c
     for (int k = 0; k < kChainBatch; ++k) {
       if (c0 + k < sg.nch) {
         const size_t base = ((size_t)i * a.max_chunks + c0 + k) * a.H + h;
-        if (a.ws_split) {   // tile-aligned fp32 layout (tensor-core engine)
-          if constexpr (P == tc::P && N == tc::N) {
-            const uint8_t* slot = reinterpret_cast<const uint8_t*>(a.ws_states + base * hs);
-            const int d = idx / N, n = idx % N;
-            const float2 lo2 = *reinterpret_cast<const float2*>(slot + tc::tile_aligned_f32(d, n));
-            const float2 hi2 = *reinterpret_cast<const float2*>(slot + tc::tile_aligned_f32(d, n + 2));
-            sv[k] = make_float4(lo2.x, lo2.y, hi2.x, hi2.y);
-          }
-        } else {
-          sv[k] = *reinterpret_cast<const float4*>(a.ws_states + base * hs + idx);
-        }
+        sv[k] = *reinterpret_cast<const float4*>(a.ws_states + base * hs + idx);
         tot[k] = a.ws_tot[base];
       }
     }
@@ -254,21 +243,9 @@ __global__ void __launch_bounds__(kThreads) k_prefill_chain(LaunchArgs a, bool c
         for (int e = 0; e < kChainElems; ++e) keep[e] = Hr[e];
       }
       const float sc[kChainElems] = {sv[k].x, sv[k].y, sv[k].z, sv[k].w};
-      // the state at the start of chunk c, read by the output kernel: fp32, or already split into
-      // the tensor-core engine's [H_hi; H_lo] operand tile (the slot has the same size; each thread
-      // overwrites only the 16 bytes it read above)
-      if (a.ws_split) {
-        if constexpr (P == tc::P && N == tc::N) {
-          uint2 hi, lo;
-          tc::split4(Hr, hi, lo);
-          uint8_t* tile = reinterpret_cast<uint8_t*>(a.ws_states + base * hs);
-          const int d = idx / N, n = idx % N;
-          *reinterpret_cast<uint2*>(tile + tc::sw128(128, d, n)) = hi;
-          *reinterpret_cast<uint2*>(tile + tc::sw128(128, P + d, n)) = lo;
-        }
-      } else {
-        *reinterpret_cast<float4*>(a.ws_states + base * hs + idx) = make_float4(Hr[0], Hr[1], Hr[2], Hr[3]);
-      }
+      // the state at the start of chunk c, read by the output kernel (each thread overwrites the
+      // 16 bytes it read above)
+      *reinterpret_cast<float4*>(a.ws_states + base * hs + idx) = make_float4(Hr[0], Hr[1], Hr[2], Hr[3]);
 #pragma unroll
       for (int e = 0; e < kChainElems; ++e) Hr[e] = __fmaf_rn(decay, Hr[e], sc[e]);
       if (a.chunk_states != nullptr)
@@ -654,18 +631,6 @@ cudaError_t launch_setpos(const LaunchArgs& a, int kind, cudaStream_t s) {
 cudaError_t launch_commit(const LaunchArgs& a, cudaStream_t s) {
   if (a.nseq > 0) k_commit<<<(a.nseq + 255) / 256, 256, 0, s>>>(a);
   return cudaGetLastError();
-}
-
-cudaError_t launch_chain(const LaunchArgs& a, bool chunked, cudaStream_t s) {
-  if (a.nseq <= 0 || a.max_chunks <= 0) return cudaSuccess;
-#define ERS_CH(p_, n_)                                                                                  \
-  if (a.P == p_ && a.N == n_) {                                                                        \
-    k_prefill_chain<p_, n_><<<dim3(a.nseq, a.H, chain_slices(p_, n_)), kThreads, 0, s>>>(a, chunked); \
-    return cudaGetLastError();                                                                         \
-  }
-  ERS_FMA_SHAPES(ERS_CH)
-#undef ERS_CH
-  return cudaErrorInvalidValue;
 }
 
 cudaError_t launch_tail(const LaunchArgs& a, cudaStream_t s) {

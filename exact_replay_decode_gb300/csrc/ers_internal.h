@@ -56,11 +56,13 @@ struct LaunchArgs {
   const float* init_state;
   float* final_state;
   float* chunk_states;
+  long long ntokens;  // prefill: rows of the packed token tensors
   // workspace
-  float* ws_states;  // [nseq, max_chunks, H, P, N]
-  float* ws_tot;     // [nseq, max_chunks, H]
-  float* ws_decay;   // [nseq, max_chunks, H, 3, Q]: delta, Acum (hi), Acum (lo) of each chunk row
-  int ws_split;      // chain output: 0 = fp32 start states, 1 = [H_hi; H_lo] bf16 operand tiles
+  float* ws_states;  // [nseq, max_chunks, H, P, N]: chunk states (CUDA cores: the start states after the chain)
+  float* ws_tot;     // [nseq, max_chunks, H]: chunk log-decay (CUDA cores) or decay factor (tensor cores)
+  float* ws_incl;    // tensor cores: [nseq, max_chunks, H, P, N] end state of each chunk, for the look-back
+  int32_t* ws_flags; // tensor cores: [nseq, max_chunks, H] 0 / 1 (chunk state published) / 2 (end state too)
+  unsigned long long wait_ns;   // limit of every bounded device wait (0: the default, 1 s)
   const int32_t* accepted;
   int32_t* status;
 };
@@ -88,7 +90,6 @@ cudaError_t heads_verify(const LaunchArgs& a, cudaStream_t s);
 cudaError_t launch_setpos(const LaunchArgs& a, int kind, cudaStream_t s);  // kind: 0 decode, 1 refresh
 cudaError_t launch_commit(const LaunchArgs& a, cudaStream_t s);
 cudaError_t launch_tail(const LaunchArgs& a, cudaStream_t s);
-cudaError_t launch_chain(const LaunchArgs& a, bool chunked, cudaStream_t s);
 
 // tensor-core engine (bf16 io, P = 64, N = 128, Q % 16 == 0, Q >= kTcMinChunk), ers_tc.cu.  Each
 // configuration runs every path on ONE engine (bitwise identity needs identical arithmetic):
@@ -97,7 +98,11 @@ cudaError_t launch_chain(const LaunchArgs& a, bool chunked, cudaStream_t s);
 // engine defines the arithmetic.
 constexpr int kTcMinChunk = 64;
 bool tc_supported(int io, int P, int N, int Q);
-cudaError_t tc_prefill(const LaunchArgs& a, Op op, cudaStream_t s);
+cudaError_t tc_prefill(const LaunchArgs& a, Op op, cudaStream_t s);   // single-pass scan, ers_tc_scan.cu
+size_t tc_scan_workspace(int nseq, int max_chunks, int H);               // its workspace bytes
+void tc_scan_carve(LaunchArgs& a, void* workspace);                      // and layout
+// a 2-CTA launch whose bounded waits (an mbarrier, a flag) are never satisfied, ers_tc_scan.cu
+cudaError_t wait_selftest(unsigned long long limit_ns, int32_t* status, cudaStream_t s);
 cudaError_t tc_decode(const LaunchArgs& a, cudaStream_t s);
 cudaError_t tc_refresh(const LaunchArgs& a, cudaStream_t s);
 cudaError_t tc_verify(const LaunchArgs& a, cudaStream_t s);

@@ -1,6 +1,7 @@
-// Tensor-core (tcgen05) kernels for bf16 io, P = 64, N = 128: chunked SSD prefill, exact-replay
-// decode with fused refresh, refresh, and output-only speculative verify.  Every output row and
-// chunk state goes through tc_outputs() / tc_state() below, so all paths agree bit for bit
+// Tensor-core (tcgen05) kernels for bf16 io, P = 64, N = 128: exact-replay decode with fused
+// refresh, refresh, and output-only speculative verify (the SSD prefill is ers_tc_scan.cu).  Every
+// output row and chunk state goes through tc_outputs() / tc_state() below, which issue the same MMA
+// sequences and build the same operand values as the prefill, so all paths agree bit for bit
 // (exact-replay RFC, vLLM issue 55524, section 3; ReplaySSM notes, "Core equations").
 #include "ers_common.cuh"
 #include "ers_internal.h"
@@ -254,155 +255,6 @@ __device__ __forceinline__ void fold_from_tmem(float* Hd, bf16* Rd, float decay)
   }
 }
 
-// X and B rows [s0, s0 + 128) into 128-row block tiles (zeros from row nrows on); asynchronous.
-__device__ __forceinline__ void load_xb_block(const Rows<bf16>& rows, int nrows, int s0, uint8_t* Bt, uint8_t* Xt) {
-  for (int id = threadIdx.x; id < 128 * 24; id += blockDim.x) {
-    const int r = id / 24, c = id % 24, s = s0 + r;
-    if (c < 8) {
-      if (s < nrows) row_to_tile(rows.x(s), Xt, 1, r, c);
-      else zero_tile_chunk(Xt, 1, r, c);
-    } else {
-      if (s < nrows) row_to_tile(rows.B(s), Bt, 128, r, c - 8);
-      else zero_tile_chunk(Bt, 128, r, c - 8);
-    }
-  }
-}
-
-// tc_state with the B and X rows loaded one 128-row K block at a time (block 0 already issued by
-// the caller).  Same weights, U tiles and MMA sequence, so the same chunk state.
-__device__ bool tc_state_blocked(const Rows<bf16>& rows, int nrows, int K, uint8_t* Bt, uint8_t* Xt, uint8_t* u,
-                                 int32_t* status, uint32_t* phase) {
-  TcHdr& hd = hdr();
-  if (threadIdx.x < nrows) {
-    const df last = {hd.ahi[nrows - 1], hd.alo[nrows - 1]};
-    hd.w[threadIdx.x] =
-        __fmul_rn(hd.delta[threadIdx.x], expf(df_diff(last, df{hd.ahi[threadIdx.x], hd.alo[threadIdx.x]})));
-  }
-  uint8_t* u0 = u;
-  uint8_t* u1 = u + 128 * 128;
-  uint8_t* u2 = u + 2 * 128 * 128;
-  bool ok = true;
-  for (int s0 = 0; s0 < K && ok; s0 += 128) {
-    const int nr = K - s0 < 128 ? K - s0 : 128;
-    if (s0 > 0) load_xb_block(rows, nrows, s0, Bt, Xt);
-    cp_async_wait_all();
-    __syncthreads();
-    build_u_tiles(Xt - (size_t)s0 * 128, hd.w, nrows, s0, nr, u0, u1, u2);   // X rows addressed by s
-    publish();
-    if (threadIdx.x == 0) {
-      issue_state_block_rel(hd.tmem, smem_u32(Bt), smem_u32(u0), smem_u32(u1), smem_u32(u2), nr / 16, s0 > 0);
-      commit(&hd.bar);
-    }
-    ok = __syncthreads_and(mbar_wait(&hd.bar, *phase, status));
-    *phase ^= 1;
-    after_sync();
-  }
-  return ok;
-}
-
-// ---- prefill: chunk states ------------------------------------------------------------------------
-constexpr int kStateWarps = 16;   // U-tile build and loads are latency-bound: 16 warps
-
-template <bool CHUNKED>
-__global__ void __launch_bounds__(kStateWarps * 32, 2) k_tc_prefill_state(LaunchArgs a) {
-  const int c = blockIdx.x, i = blockIdx.y, h = blockIdx.z;
-  SeqGrid sg;
-  if (!seq_grid(a, CHUNKED, i, &sg) || c >= sg.nch) return;
-  const int nrows = min(a.Q, sg.total - c * a.Q);
-  const int nbuf = max(0, sg.p - c * a.Q);
-  const Rows<bf16> rows = make_rows<bf16>(a, sg.slot, h, nbuf, (long long)a.cu[i] + (long long)c * a.Q - sg.p);
-  const int K = round16(nrows);
-  setup_tmem(64);
-  // arena: B block (128 x 256) | X block (128 x 128) | U (3 x 128 x 128): one 128-row K block at a
-  // time, so that two CTAs fit on an SM
-  uint8_t* Bt = tiles();
-  uint8_t* Xt = Bt + 128 * 256;
-  uint8_t* u = Xt + 128 * 128;
-  load_xb_block(rows, nrows, 0, Bt, Xt);   // asynchronous: lands while the decays are scanned
-  load_decays(rows, nrows, a.A[h], a.dt_bias[h]);
-  {  // the chunk's decays, for the output kernel
-    TcHdr& hd = hdr();
-    float* wd = a.ws_decay + (((size_t)i * a.max_chunks + c) * a.H + h) * 3 * a.Q;
-    for (int t = threadIdx.x; t < a.Q; t += blockDim.x) {
-      wd[t] = hd.delta[t];
-      wd[a.Q + t] = hd.ahi[t];
-      wd[2 * a.Q + t] = hd.alo[t];
-    }
-  }
-  uint32_t phase = 0;
-  if (tc_state_blocked(rows, nrows, K, Bt, Xt, u, a.status, &phase)) {
-    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-    constexpr int DC = P / (kStateWarps / 4);   // state columns (d) per warp
-    const int q = warp & 3, sl = warp >> 2;
-    const int n = 32 * q + lane;
-    const size_t base = ((size_t)i * a.max_chunks + c) * a.H + h;
-    uint8_t* out = reinterpret_cast<uint8_t*>(a.ws_states + base * P * N);   // tile-aligned layout
-    float s[DC];
-    tmem_ld16(taddr(hdr().tmem, 32 * q, DC * sl), s);
-#pragma unroll
-    for (int j = 0; j < DC; ++j) *reinterpret_cast<float*>(out + tile_aligned_f32(DC * sl + j, n)) = s[j];
-    if (threadIdx.x == 0) a.ws_tot[base] = hdr().ahi[nrows - 1];
-  }
-  teardown_tmem(64);
-}
-
-// ---- prefill: outputs, one CTA per (chunk, sequence, head), all t-tiles of the chunk ----------------
-constexpr int kOutWarps = 16;   // the output kernel's M tiles and epilogue are latency-bound: 16 warps
-
-// The token X and B tiles (all rows the chunk's last t-tile needs) and the decays are loaded once;
-// each t-tile then loads its query tile C and the start-state tile (its M tiles overwrite both) and
-// runs tc_outputs.  The B operand of every tile is read from the same full-height B tile, which
-// gives the MMAs the same operand values as a tile-sized one.
-template <bool CHUNKED>
-__global__ void __launch_bounds__(kOutWarps * 32, 1) k_tc_prefill_out(LaunchArgs a, int ntiles, uint32_t tcols) {
-  const int c = blockIdx.x, i = blockIdx.y, h = blockIdx.z;
-  SeqGrid sg;
-  if (!seq_grid(a, CHUNKED, i, &sg) || c >= sg.nch) return;
-  const int nrows = min(a.Q, sg.total - c * a.Q);
-  const int nbuf = max(0, sg.p - c * a.Q);
-  if (nbuf >= nrows) return;   // no new token in this chunk
-  const long long tok0 = (long long)a.cu[i] + (long long)c * a.Q - sg.p;
-  const Rows<bf16> rows = make_rows<bf16>(a, sg.slot, h, nbuf, tok0);
-  setup_tmem(tcols);
-  const int S_max = geom(a.Q, ntiles - 1).S_ext;
-  const Arena ar = arena(S_max);
-  const size_t unit = ((size_t)i * a.max_chunks + c) * a.H + h;
-  const uint8_t* htile = reinterpret_cast<const uint8_t*>(a.ws_states + unit * P * N);
-  {  // the chunk's decays, written by the chunk-state kernel
-    TcHdr& hd = hdr();
-    const float* wd = a.ws_decay + unit * 3 * a.Q;
-    const int q4 = a.Q / 4;
-    for (int k = threadIdx.x; k < 3 * q4; k += blockDim.x) {
-      const int part = k / q4, e = k % q4;
-      float* dst = part == 0 ? hd.delta : (part == 1 ? hd.ahi : hd.alo);
-      cp_async16(dst + 4 * e, wd + part * a.Q + 4 * e);
-    }
-  }
-  load_xb(rows, min(nrows, S_max), ar);
-  bool first = true;
-  for (int tau = 0; tau < ntiles; ++tau) {
-    const Geom ge = geom(a.Q, tau);
-    const int out_lo = max(nbuf, ge.t0), out_hi = min(nrows, ge.t0 + ge.TT);
-    if (out_lo >= out_hi) continue;
-    if (!first) {   // fresh barrier phases for this tile's MMAs
-      __syncthreads();
-      if (threadIdx.x == 0) {
-        mbar_init(&hdr().bar, 1);
-        fence_mbar_init();
-      }
-    }
-    first = false;
-    // the start state, already split into the [H_hi; H_lo] operand tile by the inter-chunk chain
-    for (int k = threadIdx.x; k < (int)(kHTile / 16); k += blockDim.x) cp_async16(ar.Hs + 16 * k, htile + 16 * k);
-    load_c(rows, ge.t0, ge.t0, min(nrows, ge.t0 + ge.TT), ar);
-    publish();
-    bf16* ybase = (bf16*)a.y + ((tok0 + out_lo) * a.H + h) * P;
-    if (!tc_outputs<kOutWarps>(ar, a.Q, tau, nrows, out_lo, out_hi, a.D[h], ybase, (long long)a.H * P, a.status))
-      break;
-  }
-  teardown_tmem(tcols);
-}
-
 // ---- replay decode (one CTA per sequence and head) ---------------------------------------------------
 __global__ void __launch_bounds__(kThreads, 1) k_tc_decode(LaunchArgs a, uint32_t tcols) {
   const int i = blockIdx.x, h = blockIdx.y;
@@ -564,39 +416,11 @@ cudaError_t set_smem(K kernel, size_t bytes) {
 
 size_t out_smem(int BR) { return kHdrBytes + arena_bytes(BR) + 1024; }
 size_t state_smem(int K) { return kHdrBytes + (size_t)K * (256 + 128) + kUBytes + 1024; }
-size_t state_blocked_smem() { return kHdrBytes + 128 * (256 + 128) + kUBytes + 1024; }
 
 }  // namespace
 
 bool tc_supported(int io, int P_, int N_, int Q) {
   return io == ERS_DTYPE_BF16 && P_ == P && N_ == N && Q % 16 == 0 && Q >= kTcMinChunk && Q <= kQMax;
-}
-
-cudaError_t tc_prefill(const LaunchArgs& a, Op op, cudaStream_t s) {
-  const bool chunked = op == Op::kChunkedPrefill;
-  cudaError_t e;
-  LaunchArgs b = a;
-  b.ws_split = 1;   // the chain hands the output kernel ready [H_hi; H_lo] tiles
-  if (a.max_chunks > 0 && a.nseq > 0) {
-    const int ntiles = (a.Q + 127) / 128;
-    const size_t ss = state_blocked_smem(), so = out_smem(a.Q);
-    const uint32_t tcols = tmem_cols(a.Q);
-    if (chunked) {
-      if ((e = set_smem(k_tc_prefill_state<true>, ss)) != cudaSuccess) return e;
-      if ((e = set_smem(k_tc_prefill_out<true>, so)) != cudaSuccess) return e;
-      k_tc_prefill_state<true><<<dim3(a.max_chunks, a.nseq, a.H), kStateWarps * 32, ss, s>>>(a);
-      if ((e = launch_chain(b, true, s)) != cudaSuccess) return e;
-      k_tc_prefill_out<true><<<dim3(a.max_chunks, a.nseq, a.H), kOutWarps * 32, so, s>>>(a, ntiles, tcols);
-    } else {
-      if ((e = set_smem(k_tc_prefill_state<false>, ss)) != cudaSuccess) return e;
-      if ((e = set_smem(k_tc_prefill_out<false>, so)) != cudaSuccess) return e;
-      k_tc_prefill_state<false><<<dim3(a.max_chunks, a.nseq, a.H), kStateWarps * 32, ss, s>>>(a);
-      if ((e = launch_chain(b, false, s)) != cudaSuccess) return e;
-      k_tc_prefill_out<false><<<dim3(a.max_chunks, a.nseq, a.H), kOutWarps * 32, so, s>>>(a, ntiles, tcols);
-    }
-  }
-  if (chunked) return launch_tail(a, s);
-  return cudaGetLastError();
 }
 
 cudaError_t tc_decode(const LaunchArgs& a, cudaStream_t s) {

@@ -116,19 +116,6 @@ __device__ __forceinline__ void issue_state_block(uint32_t tS, uint32_t bT, uint
   }
 }
 
-// The same MMAs for one 128-row K block held in its own tile (rows relative to the block):
-// accumulate = acc_in || term > 0 || k > 0 reproduces the sequence above for s0 = 128 * blk.
-__device__ __forceinline__ void issue_state_block_rel(uint32_t tS, uint32_t bT, uint32_t u0, uint32_t u1,
-                                                      uint32_t u2, int nk, bool acc_in) {
-  const uint32_t id = idesc_bf16(128, P, true, true);
-  for (int term = 0; term < 3; ++term) {
-    const uint32_t uT = term == 0 ? u0 : (term == 1 ? u1 : u2);
-    for (int k = 0; k < nk; ++k)
-      mma(tS, sdesc(bT + (uint32_t)(16 * k) * 128u, 128u * 128u, 1024), sdesc(uT + (uint32_t)k * 2048u, 1024, 1024),
-          id, (acc_in || term > 0 || k > 0) ? 1u : 0u);
-  }
-}
-
 // ---- operand builders (generic proxy writes; the caller fences before issuing) ---------------------
 __device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
   const __nv_bfloat162 v = __floats2bfloat162_rn(a, b);
@@ -145,16 +132,6 @@ __device__ __forceinline__ void split8(const float (&v)[8], uint4& hi, uint4& lo
   }
   hi = make_uint4(pack_bf16x2(h[0], h[1]), pack_bf16x2(h[2], h[3]), pack_bf16x2(h[4], h[5]), pack_bf16x2(h[6], h[7]));
   lo = make_uint4(pack_bf16x2(l[0], l[1]), pack_bf16x2(l[2], l[3]), pack_bf16x2(l[4], l[5]), pack_bf16x2(l[6], l[7]));
-}
-
-// Byte offset, inside a [H_hi; H_lo] tile slot (32 KB), of fp32 state element (d, n) in the
-// "tile-aligned" layout the prefill workspace uses: elements n4 = n & ~3 .. n4 + 1 of row d sit in
-// the 8 bytes that will hold their hi halves (tile row d), elements n4 + 2, n4 + 3 in the 8 bytes
-// of their lo halves (tile row P + d).  A thread that owns (d, n4 .. n4 + 3) reads exactly the 16
-// bytes it later overwrites with the split values.
-__host__ __device__ __forceinline__ uint32_t tile_aligned_f32(uint32_t d, uint32_t n) {
-  const uint32_t n4 = n & ~3u, e = n & 3u;
-  return e < 2 ? sw128(128, d, n4) + 4 * e : sw128(128, P + d, n4) + 4 * (e - 2);
 }
 
 // 4 fp32 values -> hi and lo bf16 (8 bytes each), the same operations as split8

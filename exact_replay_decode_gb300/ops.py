@@ -178,7 +178,14 @@ def ssd_scan_fwd_static(x: torch.Tensor, dt: torch.Tensor, params: LayerParams, 
     return y, fin
 
 
-STATIC_SCRATCH_BYTES = 16 << 20
+STATIC_SCRATCH_BYTES = 32 << 20
+
+
+def selftest_bounded_wait(limit_ns: int, status: Status, stream=None) -> None:
+    """ers_selftest_bounded_wait: two blocks whose waits (an mbarrier, a device flag) are never
+    satisfied give up after limit_ns and report ERS_ETIMEOUT through `status`."""
+    code = _abi.lib().ers_selftest_bounded_wait(int(limit_ns), _stream(stream), status.ptr())
+    _finish(code, "ers_selftest_bounded_wait", None, False)
 
 
 # ------------------------------------------------------------------------------------------------

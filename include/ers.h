@@ -193,6 +193,15 @@ ERS_API const char* ers_status_str(ers_status s);
 /* Library version as major*10000 + minor*100 + patch. */
 ERS_API int32_t ers_version(void);
 
+/* Check of the library's bounded device waits (no counterpart on the pages; every wait in the
+ * library gives up after a limit instead of spinning forever, and reports ERS_ETIMEOUT).  Launches
+ * two blocks on `stream`: one waits on an mbarrier phase that nothing completes, the other on a
+ * device flag that nothing sets, each with the library's own wait routine and the given limit
+ * (1 ns .. 10 s).  Both give up after limit_ns, write ERS_ETIMEOUT to *dev_status (device int32,
+ * required, zeroed by the caller) and return; the context stays usable.  ERS_EINVAL for a NULL
+ * status or a limit outside that range. */
+ERS_API ers_status ers_selftest_bounded_wait(uint64_t limit_ns, ers_stream_t stream, int32_t* dev_status);
+
 /* ---------------------------------------------------------------------------------------------
  * Chunked SSD scan (prefill).  RFC section 1 (the chunked scan used for prefill), Evidence 3
  * (prefix- and packing-invariant outputs) and Evidence 4 (fp32 inter-chunk state passing inside
@@ -415,16 +424,17 @@ ERS_API ers_status ers_conv1d_update(const ers_conv_dims* dims, int32_t nseq, co
  * Same arguments, semantics and outputs as ers_ssd_scan_fwd minus the workspace.  The scratch is a
  * fixed device array of ERS_STATIC_SCRATCH_BYTES inside this library (one per device context); a
  * call whose ers_ssd_scan_fwd_workspace_size exceeds it returns ERS_EWORKSPACE and launches
- * nothing (16 MiB holds, e.g., 2048 tokens x 32 heads x headdim 64 x dstate 128 at chunk 256,
- * which needs 8.4 MB).  Nothing in the scratch needs to start at zero: a call reads only bytes it
- * wrote earlier in the same call.  The first call in a context looks up the scratch address with
+ * nothing (32 MiB holds, e.g., 2048 tokens x 32 heads x headdim 64 x dstate 128 at chunk 256,
+ * which needs 16.8 MB).  Nothing in the scratch needs to start at zero: a call clears what it
+ * reads before writing it (the look-back flags, by an asynchronous memset on `stream`) or reads
+ * only bytes it wrote earlier in the same call.  The first call in a context looks up the scratch address with
  * that context current (cudaGetSymbolAddress) and caches it with the context's id; a call made
  * in another context of the same device (after cudaDeviceReset, or with a context the caller
  * created made current) has its own copy of the array and looks it up again.  Make one call in
  * each context before any stream capture.  Allocates nothing.  The scratch is shared: two calls
  * on the same device that can run at the same time (different streams, or different host
  * threads) race on it and must be serialised by the caller. */
-#define ERS_STATIC_SCRATCH_BYTES ((size_t)16 << 20)
+#define ERS_STATIC_SCRATCH_BYTES ((size_t)32 << 20)
 ERS_API ers_status ers_ssd_scan_fwd_static(const ers_dims* dims, const ers_params* prm, int32_t nseq,
                                    int64_t ntokens, int32_t max_seqlen, const int32_t* cu_seqlens,
                                    const void* x, const float* dt, const void* B, const void* C,

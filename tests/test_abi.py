@@ -261,3 +261,10 @@ def test_validation_of_gdn_calls(lib):
 
     assert ver(dk=64) == 2 and ver(L=33) == 2 and ver(T=9) == 2 and ver(H=6, G=4) == 2   # ERS_ESHAPE
     assert ver(io=5) == 3 and ver(T=0) == 1 and ver(L=2, T=3) == 1 and ver(flags=1) == 1
+
+
+def test_bounded_wait_selftest_validation(lib):
+    # host validation only: NULL status, zero and over-long limits are rejected before any launch
+    assert lib.ers_selftest_bounded_wait(1000, None, None) == 1
+    assert lib.ers_selftest_bounded_wait(0, None, ctypes.c_void_p(16)) == 1
+    assert lib.ers_selftest_bounded_wait(20_000_000_000, None, ctypes.c_void_p(16)) == 1

@@ -40,7 +40,7 @@ def test_static_scratch_scan_matches_workspace_scan_twice(name):
 def test_static_scratch_rejects_calls_beyond_its_size():
     import exact_replay_decode_gb300 as ers
     from exact_replay_decode_gb300 import _abi
-    w, prm, (x, dt, B, C), cu = _inputs("varlen_4seq_h64", 0)   # needs 64 MiB of chunk-state scratch
+    w, prm, (x, dt, B, C), cu = _inputs("varlen_4seq_h64", 0)   # needs 128 MiB of chunk-state scratch
     y = torch.full_like(x, 7.0)
     with pytest.raises(ers.ErsError) as e:
         ers.ssd_scan_fwd_static(x, dt, prm, B, C, chunk=w.dims.chunk, cu_seqlens=cu, out=(y, torch.empty(
@@ -48,5 +48,5 @@ def test_static_scratch_rejects_calls_beyond_its_size():
     assert e.value.code == 10   # ERS_EWORKSPACE
     torch.cuda.synchronize()
     assert bool((y == 7.0).all())                                # nothing was launched
-    assert np.isclose(ers.STATIC_SCRATCH_BYTES, 16 << 20)
+    assert np.isclose(ers.STATIC_SCRATCH_BYTES, 32 << 20)
     assert _abi.STATUS_NAMES[10] == "ERS_EWORKSPACE"
