@@ -341,12 +341,23 @@ def _l2_flush(fb):
     fb.sum()
 
 
-def time_per_iter(fn, iters: int, warmup: int, dev, flush: bool = True):
-    """Mean device time of fn() over iters, L2 flushed before each timed call (events per call)."""
+def time_per_iter(fn, iters: int, warmup: int, dev, flush: bool = True, graph: bool = False):
+    """Median device time of fn() over iters, L2 flushed before each timed call (events per call).
+    With graph=True, fn is captured once in a CUDA graph and each timed call replays it, so that the
+    host-side work of a call (argument checks, marshalling, launch) cannot leave the device idle
+    between the events: the replay is enqueued while the preceding flush still runs."""
     import torch
     fb = _flush_buf(dev) if flush else None
     for _ in range(warmup):
         fn()
+    run = fn
+    if graph:
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            fn()
+        g.replay()
+        run = g.replay
     s = torch.cuda.current_stream()
     evs = []
     for _ in range(iters):
@@ -354,7 +365,7 @@ def time_per_iter(fn, iters: int, warmup: int, dev, flush: bool = True):
             _l2_flush(fb)
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record(s)
-        fn()
+        run()
         e1.record(s)
         evs.append((e0, e1))
     torch.cuda.synchronize()
@@ -379,13 +390,14 @@ def bench_prefill(dev, name: str, iters: int, warmup: int, hbm: float, tc: float
     st = ers.Status(dev)
     fn = lambda: ers.ssd_scan_fwd(x, dt, prm, B, C, chunk=w.dims.chunk, cu_seqlens=cu_t, max_seqlen=ms_len,
                                   status=st, check=False, out=(y, fin), workspace=ws)
-    ms = time_per_iter(fn, iters, warmup, dev)
+    ms = time_per_iter(fn, iters, warmup, dev, graph=True)
     st.raise_if_error("bench prefill")
     T = toks.ntokens
     ach = PREFILL_BYTES[name] / (ms * 1e-3) / 1e9
     return {"tok_per_s": T / (ms * 1e-3), "us_per_call": ms * 1e3, "achieved_gbs": ach,
             "hbm_frac": ach / hbm, "roofline_us": PREFILL_BYTES[name] / (hbm * 1e9) * 1e6,
-            "tflops": PREFILL_FLOPS[name] / (ms * 1e-3) / 1e12, "l2": "flushed before each call"}
+            "tflops": PREFILL_FLOPS[name] / (ms * 1e-3) / 1e12,
+            "l2": "flushed before each call (one CUDA-graph replay of the call per timed iteration)"}
 
 
 def flat_prefill(pf: dict, cpu: dict = None) -> dict:

@@ -18,10 +18,10 @@ struct TcHdr {
   uint64_t bar;          // MMA completion
   uint32_t tmem;         // TMEM base written by tcgen05.alloc
   uint32_t pad;
-  float delta[kQMax];
-  float ahi[kQMax];      // Acum (double-float); dA before the scan
-  float alo[kQMax];
-  float w[kQMax];        // chunk-state weights
+  alignas(16) float delta[kQMax];
+  alignas(16) float ahi[kQMax];      // Acum (double-float); dA before the scan
+  alignas(16) float alo[kQMax];
+  alignas(16) float w[kQMax];        // chunk-state weights
   float ydiag_row[P];    // decode: Ydiag of the output row
 };
 

@@ -22,13 +22,15 @@
 #include <cuda.h>
 #include <string.h>
 
+#include <mutex>
+
 #include "ers_common.cuh"
 #include "ers_internal.h"
 #include "tc_engine.cuh"
 
 namespace ers {
 
-struct alignas(64) ScanMaps {
+struct ScanMaps {
   CUtensorMap x;   // [T, H, P] bf16 as a 3-D map {P, H, T}, box {64, 1, Q}, 128-byte swizzle
   CUtensorMap B;   // [T, G, N] bf16 as {N, G, T}, box {64, 1, Q}
   CUtensorMap C;
@@ -43,19 +45,19 @@ constexpr int kScanWarps = 16;
 constexpr int kScanThreads = kScanWarps * 32;
 constexpr uint32_t kScanTmemCols = 512;
 // TMEM columns: [0, 128) Gram of t-tile 0, then its diagonal sums (hi [0, 64), lo [64, 128));
-// [128, 384) Gram of t-tile 1, then its diagonal sums in [128, 256); [384, 448) the chunk state S^T,
-// then [384, 512) the off-diagonal sums of the current t-tile (hi, lo).
-constexpr uint32_t kColG1 = 128, kColState = 384, kColOff = 384;
+// [128, 384) Gram of t-tile 1, then its diagonal sums in [128, 256) and its off-diagonal sums in
+// [256, 384); [384, 448) the chunk state S^T, then [384, 512) t-tile 0's off-diagonal sums.
+constexpr uint32_t kColG1 = 128, kColState = 384, kColOff = 384, kColOff1 = 256;
 
 struct ScanHdr {
   uint64_t bar_tma, bar_gram, bar_state, bar_diag, bar_off;
   uint32_t tmem;
-  int32_t lb_stop;   // look-back: chunk whose end state starts the chain (-1: none, i.e. H_0)
+  int32_t lb_stop;   // look-back: the chunk whose published end state starts the chain
   int32_t lb_ok;
-  float delta[kQMax];
-  float ahi[kQMax];
-  float alo[kQMax];
-  float w[kQMax];
+  alignas(16) float delta[kQMax];
+  alignas(16) float ahi[kQMax];
+  alignas(16) float alo[kQMax];
+  alignas(16) float w[kQMax];
 };
 
 extern __shared__ __align__(1024) unsigned char scan_smem[];
@@ -148,16 +150,16 @@ __device__ __forceinline__ void build_m(const ScanArena& ar, uint32_t tb, uint32
 
 // Outputs of t-tile tau, rows [out_lo, out_hi): y = fma(D, x, exp(Acum_t) (Yoff_hi + Yoff_lo) +
 // (Ydiag_hi + Ydiag_lo)), 16 consecutive d per thread.
-__device__ __forceinline__ void epilogue(const ScanArena& ar, uint32_t tb, uint32_t dcol, int Q, int tau, int out_lo,
-                                         int out_hi, float Dh, bf16* y, long long tok0, int H, int h) {
+__device__ __forceinline__ void epilogue(const ScanArena& ar, uint32_t tb, uint32_t dcol, uint32_t ocol, int Q, int tau,
+                                         int out_lo, int out_hi, float Dh, bf16* y, long long tok0, int H, int h) {
   const Geom ge = geom(Q, tau);
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   const int q = warp & 3, sl = warp >> 2;
   const int row = 32 * q + lane;
   const int t = ge.t0 + row;
   float oh[16], ol[16], dh[16], dl[16];
-  tmem_ld16(taddr(tb, 32 * q, kColOff + 16 * sl), oh);
-  tmem_ld16(taddr(tb, 32 * q, kColOff + 64 + 16 * sl), ol);
+  tmem_ld16(taddr(tb, 32 * q, ocol + 16 * sl), oh);
+  tmem_ld16(taddr(tb, 32 * q, ocol + 64 + 16 * sl), ol);
   tmem_ld16(taddr(tb, 32 * q, dcol + 16 * sl), dh);
   tmem_ld16(taddr(tb, 32 * q, dcol + 64 + 16 * sl), dl);
   if (t < out_lo || t >= out_hi || row >= ge.TT) return;
@@ -294,29 +296,39 @@ __global__ void __launch_bounds__(kScanThreads, 1)
   float S[16];
   const float e_c = expf(hd.ahi[nrows - 1]);
   if (ok) tmem_ld16(taddr(tb, 32 * q, kColState + d0), S);
-  // ---- 3. publish S_c for the later chunks of (i, h) -----------------------------------------------------
+  // ---- 3. publish S_c (and e_c) for the later chunks of (i, h) ----------------------------------------
+  // Published states are laid out [n][d] (each thread's 16 values contiguous); the public outputs
+  // (chunk states, final state, checkpoint) keep the [d][n] layout.
   const bool has_next = c + 1 < sg.nch;
   if (ok && c > 0 && has_next) {
-    float* ws = a.ws_states + unit * hs;
+    float4* ws = reinterpret_cast<float4*>(a.ws_states + unit * hs + (size_t)n * P + d0);
 #pragma unroll
-    for (int j = 0; j < 16; ++j) ws[(d0 + j) * N + n] = S[j];
+    for (int j = 0; j < 4; ++j) ws[j] = make_float4(S[4 * j], S[4 * j + 1], S[4 * j + 2], S[4 * j + 3]);
     if (tid == 0) a.ws_tot[unit] = e_c;
     __threadfence();
   }
   __syncthreads();
   if (ok && c > 0 && has_next && tid == 0) st_release(a.ws_flags + unit, 1);
-  // ---- 4. diagonal block 0 of t-tile 0 (needs no start state) --------------------------------------------
-  uint32_t ph_diag = 0, ph_off = 0;
+  // ---- 4. every diagonal block (needs no start state) ------------------------------------------------
+  // Accumulators: t-tile 0 in [0, 128), t-tile 1 in [128, 256) over the Gram block each consumes.
+  uint32_t ph_diag = 0;
   bool diag_pending = false;
-  if (ok) {
-    ok = mma_done(&hd.bar_gram, 0, a);
-    if (ok) {
-      build_m(ar, tb, 0, Q, 0, 0, nrows);
+  if (ok) ok = mma_done(&hd.bar_gram, 0, a);
+  for (int tau = 0; tau < ntiles && ok; ++tau) {
+    const Geom ge = geom(Q, tau);
+    const uint32_t dcol = tau == 0 ? 0u : kColG1;
+    for (int blk = 0; blk < ge.nblk && ok; ++blk) {
+      if (diag_pending) {   // the previous diagonal MMAs still read the M tile
+        ok = mma_done(&hd.bar_diag, ph_diag, a);
+        ph_diag ^= 1;
+        diag_pending = false;
+        if (!ok) break;
+      }
+      build_m(ar, tb, dcol + 128 * blk, Q, tau, blk, nrows);
       publish();
       if (tid == 0) {
-        const int se = geom(Q, 0).S_ext;
-        issue_ydiag(tb, smem_u32(ar.B), 128, 1024, smem_u32(ar.X), 0, se);
-        issue_ydiag(tb + 64, smem_u32(ar.B + 32768), 128, 1024, smem_u32(ar.X), 0, se);
+        issue_ydiag(tb + dcol, smem_u32(ar.B), 128, 1024, smem_u32(ar.X), blk, ge.S_ext);
+        issue_ydiag(tb + dcol + 64, smem_u32(ar.B + 32768), 128, 1024, smem_u32(ar.X), blk, ge.S_ext);
         commit(&hd.bar_diag);
       }
       diag_pending = true;
@@ -331,36 +343,64 @@ __global__ void __launch_bounds__(kScanThreads, 1)
 #pragma unroll
       for (int j = 0; j < 16; ++j) Hc[j] = init ? init[(d0 + j) * N + n] : 0.f;
     } else {
-      if (tid == 0) {
-        int k = c - 1, good = 1;
-        for (;;) {   // chunk 0 always publishes its end state, so the walk stops at k >= 0
-          const int32_t f = flag_wait(a.ws_flags + unit_index(a, i, k, h), a.status, a.wait_ns);
-          if (f == 2) break;
-          if (f != 1 || k == 0) {
+      // warp 0: lane l watches chunk top - l, 32 chunks per window, from c - 1 down; the chain
+      // starts at the nearest chunk that has published its end state, once every chunk above it has
+      // published its chunk state (chunk 0 publishes only its end state)
+      if (warp == 0) {
+        int top = c - 1, k0 = -1, good = 1;
+        while (good && k0 < 0) {
+          const int k = top - lane;
+          int32_t f = 2;
+          if (k >= 0) f = flag_wait(a.ws_flags + unit_index(a, i, k, h), a.status, a.wait_ns);
+          if (!__all_sync(kFull, f != 0)) {
             good = 0;
             break;
           }
-          --k;
+          const unsigned inc = __ballot_sync(kFull, k >= 0 && f == 2);
+          if (inc != 0) k0 = top - (__ffs(inc) - 1);
+          else if (top < 32) good = 0;   // no end state at all: cannot happen (chunk 0 publishes one)
+          top -= 32;
         }
-        hd.lb_stop = k;
-        hd.lb_ok = good;
+        if (lane == 0) {
+          hd.lb_stop = k0;
+          hd.lb_ok = good;
+        }
       }
       __syncthreads();
       ok = hd.lb_ok != 0;
       if (ok) {
         const int k0 = hd.lb_stop;
-        const float* Hk = a.ws_incl + unit_index(a, i, k0, h) * hs;   // H_{k0+1}
+        const float4* Hk = reinterpret_cast<const float4*>(a.ws_incl + unit_index(a, i, k0, h) * hs + (size_t)n * P + d0);
 #pragma unroll
-        for (int j = 0; j < 16; ++j) Hc[j] = __ldcg(Hk + (d0 + j) * N + n);
-        for (int kk = k0 + 1; kk < c; ++kk) {
-          const size_t uk = unit_index(a, i, kk, h);
-          const float e = __ldcg(a.ws_tot + uk);
-          const float* Sk = a.ws_states + uk * hs;
-          float sv[16];
+        for (int j = 0; j < 4; ++j) {
+          const float4 v = __ldcg(Hk + j);
+          Hc[4 * j] = v.x; Hc[4 * j + 1] = v.y; Hc[4 * j + 2] = v.z; Hc[4 * j + 3] = v.w;
+        }
+        for (int kk = k0 + 1; kk < c; kk += 2) {   // two chunks' loads in flight
+          float4 sv[2][4];
+          float ev[2] = {0.f, 0.f};
 #pragma unroll
-          for (int j = 0; j < 16; ++j) sv[j] = __ldcg(Sk + (d0 + j) * N + n);
+          for (int u = 0; u < 2; ++u) {
+            if (kk + u < c) {
+              const size_t uk = unit_index(a, i, kk + u, h);
+              ev[u] = __ldcg(a.ws_tot + uk);
+              const float4* Sk = reinterpret_cast<const float4*>(a.ws_states + uk * hs + (size_t)n * P + d0);
 #pragma unroll
-          for (int j = 0; j < 16; ++j) Hc[j] = __fmaf_rn(e, Hc[j], sv[j]);
+              for (int j = 0; j < 4; ++j) sv[u][j] = __ldcg(Sk + j);
+            }
+          }
+#pragma unroll
+          for (int u = 0; u < 2; ++u) {
+            if (kk + u < c) {
+#pragma unroll
+              for (int j = 0; j < 4; ++j) {
+                Hc[4 * j] = __fmaf_rn(ev[u], Hc[4 * j], sv[u][j].x);
+                Hc[4 * j + 1] = __fmaf_rn(ev[u], Hc[4 * j + 1], sv[u][j].y);
+                Hc[4 * j + 2] = __fmaf_rn(ev[u], Hc[4 * j + 2], sv[u][j].z);
+                Hc[4 * j + 3] = __fmaf_rn(ev[u], Hc[4 * j + 3], sv[u][j].w);
+              }
+            }
+          }
         }
       }
     }
@@ -370,9 +410,9 @@ __global__ void __launch_bounds__(kScanThreads, 1)
 #pragma unroll
     for (int j = 0; j < 16; ++j) Hn[j] = __fmaf_rn(e_c, Hc[j], S[j]);
     if (has_next) {
-      float* wi = a.ws_incl + unit * hs;
+      float4* wi = reinterpret_cast<float4*>(a.ws_incl + unit * hs + (size_t)n * P + d0);
 #pragma unroll
-      for (int j = 0; j < 16; ++j) wi[(d0 + j) * N + n] = Hn[j];
+      for (int j = 0; j < 4; ++j) wi[j] = make_float4(Hn[4 * j], Hn[4 * j + 1], Hn[4 * j + 2], Hn[4 * j + 3]);
       __threadfence();
     }
     float* out = nullptr;
@@ -398,47 +438,25 @@ __global__ void __launch_bounds__(kScanThreads, 1)
   }
   publish();
   if (ok && has_next && tid == 0) st_release(a.ws_flags + unit, 2);
-  // ---- 6. off-diagonal sums and the remaining diagonal blocks, tile by tile ------------------------------
+  // ---- 6. off-diagonal sums of every t-tile, then the epilogues ----------------------------------------
+  // t-tile 0 into [384, 512) (the chunk state's columns, read above), t-tile 1 into [256, 384) (its
+  // second Gram block, consumed by its M tile).
+  if (ok && tid == 0) {
+    for (int tau = 0; tau < ntiles; ++tau)
+      issue_yoff(tb + (tau == 0 ? kColOff : kColOff1), smem_u32(ar.C + 128 * 128 * tau), Q, 1024, smem_u32(ar.U), 128);
+    commit(&hd.bar_off);
+  }
+  if (ok && diag_pending) {
+    ok = mma_done(&hd.bar_diag, ph_diag, a);
+    ph_diag ^= 1;
+    diag_pending = false;
+  }
+  if (ok) ok = mma_done(&hd.bar_off, 0, a);
   const float Dh = a.D[h];
-  bf16* y = (bf16*)a.y;
   for (int tau = 0; tau < ntiles && ok; ++tau) {
     const Geom ge = geom(Q, tau);
-    const uint32_t dcol = tau == 0 ? 0u : kColG1;
-    if (tid == 0) {
-      issue_yoff(tb + kColOff, smem_u32(ar.C + 128 * 128 * tau), Q, 1024, smem_u32(ar.U), 128);
-      commit(&hd.bar_off);
-    }
-    if (tau > 0) {   // diagonal blocks of this tile (tile 0's only block is already issued)
-      for (int blk = 0; blk < ge.nblk && ok; ++blk) {
-        if (diag_pending) {   // the previous diagonal MMAs still read the M tile
-          ok = mma_done(&hd.bar_diag, ph_diag, a);
-          ph_diag ^= 1;
-          diag_pending = false;
-          if (!ok) break;
-        }
-        build_m(ar, tb, kColG1 + 128 * blk, Q, tau, blk, nrows);
-        publish();
-        if (tid == 0) {
-          issue_ydiag(tb + dcol, smem_u32(ar.B), 128, 1024, smem_u32(ar.X), blk, ge.S_ext);
-          issue_ydiag(tb + dcol + 64, smem_u32(ar.B + 32768), 128, 1024, smem_u32(ar.X), blk, ge.S_ext);
-          commit(&hd.bar_diag);
-        }
-        diag_pending = true;
-      }
-    }
-    if (!ok) break;
-    if (diag_pending) {
-      ok = mma_done(&hd.bar_diag, ph_diag, a);
-      ph_diag ^= 1;
-      diag_pending = false;
-    }
-    ok = ok && mma_done(&hd.bar_off, ph_off, a);
-    ph_off ^= 1;
-    if (!ok) break;
-    epilogue(ar, tb, dcol, Q, tau, max(nbuf, ge.t0), min(nrows, ge.t0 + ge.TT), Dh, y, tok0, a.H, h);
-    before_sync();
-    __syncthreads();   // the off-diagonal columns are read before the next tile's MMAs overwrite them
-    after_sync();
+    epilogue(ar, tb, tau == 0 ? 0u : kColG1, tau == 0 ? kColOff : kColOff1, Q, tau, max(nbuf, ge.t0),
+             min(nrows, ge.t0 + ge.TT), Dh, (bf16*)a.y, tok0, a.H, h);
   }
   if (diag_pending) mma_done(&hd.bar_diag, ph_diag, a);   // no MMA may outlive the TMEM allocation
   before_sync();
@@ -480,6 +498,25 @@ bool encode_rows(CUtensorMap* m, const void* base, long long T, int R, int W, in
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// The kernels' dynamic shared-memory limit, raised to the largest size once per device (a call made
+// under stream capture after the first one on its device sets nothing).
+cudaError_t smem_attr(bool chunked, size_t bytes) {
+  static std::mutex mu;
+  static bool done[2][64];
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(mu);
+  if (done[chunked][dev]) return cudaSuccess;
+  (void)bytes;
+  const int most = (int)scan_smem_bytes(kQMaxHost);
+  e = chunked ? cudaFuncSetAttribute(k_tc_scan<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, most)
+              : cudaFuncSetAttribute(k_tc_scan<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, most);
+  if (e == cudaSuccess) done[chunked][dev] = true;
+  return e;
+}
+
 }  // namespace
 
 size_t tc_scan_workspace(int nseq, int max_chunks, int H) {
@@ -513,15 +550,11 @@ cudaError_t tc_prefill(const LaunchArgs& a0, Op op, cudaStream_t s) {
     int use_tma = encode_rows(&maps.x, a.x, a.ntokens, a.H, P, a.Q) && encode_rows(&maps.B, a.B, a.ntokens, a.G, N, a.Q) &&
                   encode_rows(&maps.C, a.C, a.ntokens, a.G, N, a.Q);
     const size_t sm = scan_smem_bytes(a.Q);
-    if (chunked) {
-      if ((e = cudaFuncSetAttribute(k_tc_scan<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm)) != cudaSuccess)
-        return e;
+    if ((e = smem_attr(chunked, sm)) != cudaSuccess) return e;
+    if (chunked)
       k_tc_scan<true><<<(unsigned)units, kScanThreads, sm, s>>>(a, maps, use_tma);
-    } else {
-      if ((e = cudaFuncSetAttribute(k_tc_scan<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm)) != cudaSuccess)
-        return e;
+    else
       k_tc_scan<false><<<(unsigned)units, kScanThreads, sm, s>>>(a, maps, use_tma);
-    }
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
   if (chunked) return launch_tail(a0, s);

@@ -227,33 +227,43 @@ __device__ __forceinline__ void build_u_tiles(const uint8_t* xT, const float* w,
   }
 }
 
-// Row `row` (chunk row t = t0 + row) of the masked decayed Gram for block blk, 64 columns
+// Row `row` (chunk row t = t0 + row) of the masked decayed Gram for block blk, NC columns
 // [col0, col0 + NC) of the block, from NC Gram values g[] (TMEM columns of the same range).
 // The segment decay uses the hardware exponential (__expf): its relative error (a few 1e-7 for the
 // O(1) segment sums that matter, growing with |Acum_t - Acum_s| only where the decay is already
 // negligible) is far below the 2^-16 resolution of the hi + lo bf16 split it feeds.
 // Writes hi and lo bf16 to the M tiles at tile row `trow` (atoms mR rows apart).  Entries with
-// s > t, s >= S_ext or t >= tmax are zero.
+// s > t, s >= S_ext or t >= tmax are zero.  Called by every lane of a warp together (the warp's
+// lanes agree on blk, col0 and S_ext): an 8-column group that is zero on every lane is stored
+// without arithmetic, and one that is live on every lane skips the per-entry mask; the value of
+// every entry is the same in all three cases.  delta / ahi / alo are 16-byte aligned.
 template <int NC>
 __device__ __forceinline__ void m_row(const float (&g)[NC], int t, int tmax, int blk, int col0, int S_ext,
                                       const float* delta, const float* ahi, const float* alo, uint8_t* mhi,
                                       uint8_t* mlo, uint32_t mR, uint32_t trow) {
   static_assert(NC % 8 == 0, "whole 16-byte chunks");
   const df at = {ahi[t], alo[t]};
+  const bool row_ok = t < tmax;
 #pragma unroll
   for (int c = 0; c < NC / 8; ++c) {
-    float v[8];
+    const int s0 = 128 * blk + col0 + 8 * c;   // first s of the group, a multiple of 8
+    uint4 hi = make_uint4(0, 0, 0, 0), lo = hi;
+    if (!__all_sync(0xffffffffu, !row_ok || s0 > t || s0 >= S_ext)) {
+      const bool full = __all_sync(0xffffffffu, row_ok && s0 + 7 <= t && s0 + 7 < S_ext);
+      const float4 d0 = *reinterpret_cast<const float4*>(delta + s0), d1 = *reinterpret_cast<const float4*>(delta + s0 + 4);
+      const float4 h0 = *reinterpret_cast<const float4*>(ahi + s0), h1 = *reinterpret_cast<const float4*>(ahi + s0 + 4);
+      const float4 l0 = *reinterpret_cast<const float4*>(alo + s0), l1 = *reinterpret_cast<const float4*>(alo + s0 + 4);
+      const float dv[8] = {d0.x, d0.y, d0.z, d0.w, d1.x, d1.y, d1.z, d1.w};
+      const float hv[8] = {h0.x, h0.y, h0.z, h0.w, h1.x, h1.y, h1.z, h1.w};
+      const float lv[8] = {l0.x, l0.y, l0.z, l0.w, l1.x, l1.y, l1.z, l1.w};
+      float v[8];
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      const int sl = col0 + 8 * c + i;  // s within the block
-      const int s = 128 * blk + sl;
-      float m = 0.f;
-      if (s <= t && s < S_ext && t < tmax)
-        m = __fmul_rn(__fmul_rn(g[8 * c + i], delta[s]), __expf(df_diff(at, df{ahi[s], alo[s]})));
-      v[i] = m;
+      for (int i = 0; i < 8; ++i) {
+        const float m = __fmul_rn(__fmul_rn(g[8 * c + i], dv[i]), __expf(df_diff(at, df{hv[i], lv[i]})));
+        v[i] = (full || (row_ok && s0 + i <= t && s0 + i < S_ext)) ? m : 0.f;
+      }
+      split8(v, hi, lo);
     }
-    uint4 hi, lo;
-    split8(v, hi, lo);
     const uint32_t off = sw128(mR, trow, col0 + 8 * c);
     *reinterpret_cast<uint4*>(mhi + off) = hi;
     *reinterpret_cast<uint4*>(mlo + off) = lo;
