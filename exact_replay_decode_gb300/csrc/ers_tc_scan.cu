@@ -41,8 +41,11 @@ namespace {
 using bf16 = __nv_bfloat16;
 using namespace tc;
 
-constexpr int kScanWarps = 16;
+constexpr int kScanWarps = 32;
 constexpr int kScanThreads = kScanWarps * 32;
+constexpr int kSlices = kScanWarps / 4;   // column slices per TMEM lane quarter
+constexpr int kMC = 128 / kSlices;        // M-tile columns per warp
+constexpr int kOC = 64 / kSlices;         // output columns / state rows per thread
 constexpr uint32_t kScanTmemCols = 512;
 // TMEM columns: [0, 128) Gram of t-tile 0, then its diagonal sums (hi [0, 64), lo [64, 128));
 // [128, 384) Gram of t-tile 1, then its diagonal sums in [128, 256) and its off-diagonal sums in
@@ -50,7 +53,7 @@ constexpr uint32_t kScanTmemCols = 512;
 constexpr uint32_t kColG1 = 128, kColState = 384, kColOff = 384, kColOff1 = 256;
 
 struct ScanHdr {
-  uint64_t bar_tma, bar_gram, bar_state, bar_diag, bar_off;
+  uint64_t bar_tma, bar_c, bar_gram, bar_state, bar_diag[2], bar_off;
   uint32_t tmem;
   int32_t lb_stop;   // look-back: the chunk whose published end state starts the chain
   int32_t lb_ok;
@@ -65,9 +68,10 @@ extern __shared__ __align__(1024) unsigned char scan_smem[];
 constexpr size_t kScanHdrBytes = (sizeof(ScanHdr) + 1023) & ~size_t(1023);
 constexpr uint32_t kUTile = 128u * 128u;   // one bf16 U term: 128 rows x 64 d
 
-// Shared-memory arena: header | X [Q x 64] | B region max(Q x 128, M tile) | C [Q x 128] | U (3 terms).
-// The M tile (hi, lo: 2 x 128 x 128 bf16) reuses the B region once the Gram and state MMAs are
-// done; the [H_hi; H_lo] tile reuses the U region once the state MMAs are done.
+// Shared-memory arena: header | X [Q x 64] | B region max(Q x 128, M tile) | C region max(Q x 128,
+// M tile) | U (3 terms).  Once the Gram MMAs are done the C region holds the second K block's state
+// operand, then M tiles (hi, lo: 2 x 128 x 128 bf16) alternate between the B and C regions, and the
+// C tile is reloaded for the off-diagonal MMAs; the [H_hi; H_lo] tile reuses the U region.
 struct ScanArena {
   ScanHdr* hd;
   uint8_t* X;
@@ -80,7 +84,7 @@ __host__ __device__ __forceinline__ size_t scan_b_bytes(int Q) {
   return b > 65536 ? b : 65536;
 }
 __host__ __device__ __forceinline__ size_t scan_smem_bytes(int Q) {
-  return 1024 + kScanHdrBytes + (size_t)Q * 128 + scan_b_bytes(Q) + (size_t)Q * 256 + 3 * kUTile;
+  return 1024 + kScanHdrBytes + (size_t)Q * 128 + 2 * scan_b_bytes(Q) + 3 * kUTile;
 }
 __device__ __forceinline__ ScanArena scan_arena(int Q) {
   unsigned char* base =
@@ -90,7 +94,7 @@ __device__ __forceinline__ ScanArena scan_arena(int Q) {
   ar.X = base + kScanHdrBytes;
   ar.B = ar.X + (size_t)Q * 128;
   ar.C = ar.B + scan_b_bytes(Q);
-  ar.U = ar.C + (size_t)Q * 256;
+  ar.U = ar.C + scan_b_bytes(Q);
   return ar;
 }
 
@@ -130,26 +134,27 @@ __device__ __forceinline__ void load_rows_async(const ScanArena& ar, const Rows<
   }
 }
 
-// Masked decayed Gram block `blk` of t-tile tau into the M tile (hi, lo), from Gram columns
-// [gcol, gcol + 128): every warp handles one TMEM lane quarter (rows) and a 32-column slice.
-__device__ __forceinline__ void build_m(const ScanArena& ar, uint32_t tb, uint32_t gcol, int Q, int tau, int blk,
-                                       int nrows) {
+// Masked decayed Gram block `blk` of t-tile tau into the M tile at `mt` (hi, then lo 32 KB on),
+// from Gram columns [gcol, gcol + 128): every warp handles one TMEM lane quarter (rows) and a
+// kMC-column slice.
+__device__ __forceinline__ void build_m(const ScanArena& ar, uint8_t* mt, uint32_t tb, uint32_t gcol, int Q, int tau,
+                                       int blk, int nrows) {
   const Geom ge = geom(Q, tau);
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   const int q = warp & 3, sl = warp >> 2;
   const int row = 32 * q + lane;
   const int width = ge.S_ext - 128 * blk < 128 ? ge.S_ext - 128 * blk : 128;
   const int tlim = nrows < ge.t0 + ge.TT ? nrows : ge.t0 + ge.TT;
-  if (32 * sl < width) {
-    float g[32];
-    tmem_ld32(taddr(tb, 32 * q, gcol + 32 * sl), g);
-    m_row<32>(g, ge.t0 + row, tlim, blk, 32 * sl, ge.S_ext, ar.hd->delta, ar.hd->ahi, ar.hd->alo, ar.B,
-              ar.B + 32768, 128, row);
+  if (kMC * sl < width) {
+    float g[kMC];
+    tmem_ld16(taddr(tb, 32 * q, gcol + kMC * sl), g);
+    m_row<kMC>(g, ge.t0 + row, tlim, blk, kMC * sl, ge.S_ext, ar.hd->delta, ar.hd->ahi, ar.hd->alo, mt, mt + 32768,
+               128, row);
   }
 }
 
 // Outputs of t-tile tau, rows [out_lo, out_hi): y = fma(D, x, exp(Acum_t) (Yoff_hi + Yoff_lo) +
-// (Ydiag_hi + Ydiag_lo)), 16 consecutive d per thread.
+// (Ydiag_hi + Ydiag_lo)), kOC consecutive d per thread.
 __device__ __forceinline__ void epilogue(const ScanArena& ar, uint32_t tb, uint32_t dcol, uint32_t ocol, int Q, int tau,
                                          int out_lo, int out_hi, float Dh, bf16* y, long long tok0, int H, int h) {
   const Geom ge = geom(Q, tau);
@@ -157,32 +162,52 @@ __device__ __forceinline__ void epilogue(const ScanArena& ar, uint32_t tb, uint3
   const int q = warp & 3, sl = warp >> 2;
   const int row = 32 * q + lane;
   const int t = ge.t0 + row;
-  float oh[16], ol[16], dh[16], dl[16];
-  tmem_ld16(taddr(tb, 32 * q, ocol + 16 * sl), oh);
-  tmem_ld16(taddr(tb, 32 * q, ocol + 64 + 16 * sl), ol);
-  tmem_ld16(taddr(tb, 32 * q, dcol + 16 * sl), dh);
-  tmem_ld16(taddr(tb, 32 * q, dcol + 64 + 16 * sl), dl);
+  float oh[kOC], ol[kOC], dh[kOC], dl[kOC];
+  tmem_ld8(taddr(tb, 32 * q, ocol + kOC * sl), oh);
+  tmem_ld8(taddr(tb, 32 * q, ocol + 64 + kOC * sl), ol);
+  tmem_ld8(taddr(tb, 32 * q, dcol + kOC * sl), dh);
+  tmem_ld8(taddr(tb, 32 * q, dcol + 64 + kOC * sl), dl);
   if (t < out_lo || t >= out_hi || row >= ge.TT) return;
   const float et = expf(ar.hd->ahi[t]);
-  const uint4 x0 = *reinterpret_cast<const uint4*>(ar.X + sw128(1, t, 16 * sl));
-  const uint4 x1 = *reinterpret_cast<const uint4*>(ar.X + sw128(1, t, 16 * sl + 8));
-  const bf16* xa = reinterpret_cast<const bf16*>(&x0);
-  const bf16* xb = reinterpret_cast<const bf16*>(&x1);
-  uint32_t packed[8];
+  const uint4 xr = *reinterpret_cast<const uint4*>(ar.X + sw128(1, t, kOC * sl));
+  const bf16* xv = reinterpret_cast<const bf16*>(&xr);
+  uint32_t packed[kOC / 2];
 #pragma unroll
-  for (int j = 0; j < 16; j += 2) {
-    float o[2];
-#pragma unroll
-    for (int u = 0; u < 2; ++u) {
-      const int e = j + u;
-      const float xv = __bfloat162float(e < 8 ? xa[e] : xb[e - 8]);
-      o[u] = combine_out(et, __fadd_rn(oh[e], ol[e]), __fadd_rn(dh[e], dl[e]), Dh, xv);
-    }
-    packed[j / 2] = pack_bf16x2(o[0], o[1]);
+  for (int e = 0; e < kOC; e += 2) {
+    const float o0 = combine_out(et, __fadd_rn(oh[e], ol[e]), __fadd_rn(dh[e], dl[e]), Dh, __bfloat162float(xv[e]));
+    const float o1 =
+        combine_out(et, __fadd_rn(oh[e + 1], ol[e + 1]), __fadd_rn(dh[e + 1], dl[e + 1]), Dh, __bfloat162float(xv[e + 1]));
+    packed[e / 2] = pack_bf16x2(o0, o1);
   }
-  uint4* dst = reinterpret_cast<uint4*>(y + ((tok0 + t) * H + h) * P + 16 * sl);
-  dst[0] = make_uint4(packed[0], packed[1], packed[2], packed[3]);
-  dst[1] = make_uint4(packed[4], packed[5], packed[6], packed[7]);
+  *reinterpret_cast<uint4*>(y + ((tok0 + t) * H + h) * P + kOC * sl) = make_uint4(packed[0], packed[1], packed[2], packed[3]);
+}
+
+// Publishes `value` in a unit's flag after every thread's stores before this call (one fence).
+__device__ __forceinline__ void publish_flag(int32_t* flag, int32_t value) {
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    __threadfence();
+    st_release(flag, value);
+  }
+}
+
+// The C tile again (its region held operands in between): TMA, or cp.async from `rows`.
+__device__ __forceinline__ void reload_c(const ScanArena& ar, const ScanMaps& maps, const Rows<bf16>& rows, bool tma,
+                                         int Q, int nrows, int g, int z, uint64_t* bar) {
+  if (tma) {
+    if (threadIdx.x == 0) {
+      mbar_arrive_expect_tx(bar, (uint32_t)Q * 256u);
+      tma_load_3d(ar.C, &maps.C, 0, g, z, bar);
+      tma_load_3d(ar.C + Q * 128, &maps.C, 64, g, z, bar);
+    }
+  } else {
+    for (int id = threadIdx.x; id < Q * 16; id += kScanThreads) {
+      const int r = id / 16, k = id % 16;
+      uint8_t* dst = ar.C + sw128(Q, r, 8 * k);
+      if (r < nrows) cp_async16(dst, rows.C(r) + 8 * k);
+      else *reinterpret_cast<uint4*>(dst) = make_uint4(0, 0, 0, 0);
+    }
+  }
 }
 
 template <bool CHUNKED>
@@ -199,7 +224,7 @@ __global__ void __launch_bounds__(kScanThreads, 1)
   const int warp = tid / 32, lane = tid % 32;
   const int q = warp & 3, sl = warp >> 2;
   const int n = 32 * q + lane;   // state column owned by this thread
-  const int d0 = 16 * sl;        // and its 16 state rows d0 .. d0 + 15
+  const int d0 = kOC * sl;       // and its kOC state rows d0 ..
   if (sg.nch == 0) {             // empty sequence: the final state is the initial one
     if (!CHUNKED && c == 0) {
       const float* init = a.init_state ? a.init_state + ((size_t)i * a.H + h) * hs : nullptr;
@@ -214,17 +239,21 @@ __global__ void __launch_bounds__(kScanThreads, 1)
   const int nbuf = max(0, sg.p - c * Q);
   if (nbuf >= nrows) return;   // a resumed slot's partial chunk with no new token: nothing changes
   const long long tok0 = (long long)a.cu[i] + (long long)c * Q - sg.p;
-  const Rows<bf16> rows = make_rows<bf16>(a, sg.slot, h, nbuf, tok0);
   const int g = h / (a.H / a.G);
   const size_t unit = unit_index(a, i, c, h);
   const ScanArena ar = scan_arena(Q);
   ScanHdr& hd = *ar.hd;
   const bool tma = use_tma != 0 && nbuf == 0;
+  const int ntiles = (Q + 127) / 128;
+  const int K = (nrows + 15) & ~15;
+  const bool two_state_blocks = K > 128;
   if (tid == 0) {
     mbar_init(&hd.bar_tma, 1);
+    mbar_init(&hd.bar_c, 1);
     mbar_init(&hd.bar_gram, 1);
     mbar_init(&hd.bar_state, 1);
-    mbar_init(&hd.bar_diag, 1);
+    mbar_init(&hd.bar_diag[0], 1);
+    mbar_init(&hd.bar_diag[1], 1);
     mbar_init(&hd.bar_off, 1);
     fence_mbar_init();
   }
@@ -245,12 +274,12 @@ __global__ void __launch_bounds__(kScanThreads, 1)
       tma_load_3d(ar.C + Q * 128, &maps.C, 64, g, z, &hd.bar_tma);
     }
   } else {
-    load_rows_async(ar, rows, Q, nrows);
+    load_rows_async(ar, make_rows<bf16>(a, sg.slot, h, nbuf, tok0), Q, nrows);
   }
   if (tid < kQMax) {
     float dl = 0.f, da = 0.f;
     if (tid < nrows) {
-      dl = delta_of(rows.dt(tid), a.dt_bias[h]);
+      dl = delta_of(make_rows<bf16>(a, sg.slot, h, nbuf, tok0).dt(tid), a.dt_bias[h]);
       da = __fmul_rn(dl, a.A[h]);
     }
     hd.delta[tid] = dl;
@@ -270,175 +299,203 @@ __global__ void __launch_bounds__(kScanThreads, 1)
   }
   publish();
   ok = __syncthreads_and(ok);
-  const int ntiles = (Q + 127) / 128;
-  // ---- 2. Gram MMAs of every t-tile, then the chunk state --------------------------------------------
+  // ---- 2. Gram MMAs of every t-tile; chunk state (its second K block's operand in the C region) ------
   if (ok && tid == 0) {
     issue_gram(tb, smem_u32(ar.C), Q, 1024, smem_u32(ar.B), Q, geom(Q, 0).S_ext);
     if (ntiles > 1) issue_gram(tb + kColG1, smem_u32(ar.C + 128 * 128), Q, 1024, smem_u32(ar.B), Q, geom(Q, 1).S_ext);
     commit(&hd.bar_gram);
   }
-  uint8_t* u0 = ar.U;
-  uint8_t* u1 = ar.U + kUTile;
-  uint8_t* u2 = ar.U + 2 * kUTile;
-  const int K = (nrows + 15) & ~15;
-  uint32_t ph_state = 0;
-  for (int s0 = 0; s0 < K && ok; s0 += 128) {
-    const int nr = K - s0 < 128 ? K - s0 : 128;
-    build_u_tiles(ar.X, hd.w, nrows, s0, nr, u0, u1, u2);
+  if (ok) {
+    build_u_tiles(ar.X, hd.w, nrows, 0, K < 128 ? K : 128, ar.U, ar.U + kUTile, ar.U + 2 * kUTile);
     publish();
-    if (tid == 0) {
-      issue_state_block(tb + kColState, smem_u32(ar.B), Q, smem_u32(u0), smem_u32(u1), smem_u32(u2), s0, nr / 16);
-      commit(&hd.bar_state);
-    }
-    ok = mma_done(&hd.bar_state, ph_state, a);
-    ph_state ^= 1;
+    if (tid == 0)
+      issue_state_block(tb + kColState, smem_u32(ar.B), Q, smem_u32(ar.U), smem_u32(ar.U + kUTile),
+                        smem_u32(ar.U + 2 * kUTile), 0, (K < 128 ? K : 128) / 16);
+    ok = mma_done(&hd.bar_gram, 0, a);   // the C tile is free from here until it is reloaded
   }
-  float S[16];
-  const float e_c = expf(hd.ahi[nrows - 1]);
-  if (ok) tmem_ld16(taddr(tb, 32 * q, kColState + d0), S);
-  // ---- 3. publish S_c (and e_c) for the later chunks of (i, h) ----------------------------------------
-  // Published states are laid out [n][d] (each thread's 16 values contiguous); the public outputs
-  // (chunk states, final state, checkpoint) keep the [d][n] layout.
+  if (ok && two_state_blocks) {
+    build_u_tiles(ar.X, hd.w, nrows, 128, K - 128, ar.C, ar.C + kUTile, ar.C + 2 * kUTile);
+    publish();
+    if (tid == 0)
+      issue_state_block(tb + kColState, smem_u32(ar.B), Q, smem_u32(ar.C), smem_u32(ar.C + kUTile),
+                        smem_u32(ar.C + 2 * kUTile), 128, (K - 128) / 16);
+  }
+  if (ok && tid == 0) commit(&hd.bar_state);
+  if (ok) ok = mma_done(&hd.bar_state, 0, a);
+  // ---- 3. publish: chunk 0 its end state H_1 at once (H_0 is known), later chunks their S_c and e_c --
+  // Published states are laid out [n][d] (each thread's kOC values contiguous); the public outputs
+  // (chunk states, final state, checkpoint) keep the [d][n] layout.  S_c stays in TMEM until the
+  // off-diagonal MMAs, so no register holds it across the diagonal work.
   const bool has_next = c + 1 < sg.nch;
-  if (ok && c > 0 && has_next) {
-    float4* ws = reinterpret_cast<float4*>(a.ws_states + unit * hs + (size_t)n * P + d0);
-#pragma unroll
-    for (int j = 0; j < 4; ++j) ws[j] = make_float4(S[4 * j], S[4 * j + 1], S[4 * j + 2], S[4 * j + 3]);
-    if (tid == 0) a.ws_tot[unit] = e_c;
-    __threadfence();
-  }
-  __syncthreads();
-  if (ok && c > 0 && has_next && tid == 0) st_release(a.ws_flags + unit, 1);
-  // ---- 4. every diagonal block (needs no start state) ------------------------------------------------
-  // Accumulators: t-tile 0 in [0, 128), t-tile 1 in [128, 256) over the Gram block each consumes.
-  uint32_t ph_diag = 0;
-  bool diag_pending = false;
-  if (ok) ok = mma_done(&hd.bar_gram, 0, a);
-  for (int tau = 0; tau < ntiles && ok; ++tau) {
-    const Geom ge = geom(Q, tau);
-    const uint32_t dcol = tau == 0 ? 0u : kColG1;
-    for (int blk = 0; blk < ge.nblk && ok; ++blk) {
-      if (diag_pending) {   // the previous diagonal MMAs still read the M tile
-        ok = mma_done(&hd.bar_diag, ph_diag, a);
-        ph_diag ^= 1;
-        diag_pending = false;
-        if (!ok) break;
-      }
-      build_m(ar, tb, dcol + 128 * blk, Q, tau, blk, nrows);
-      publish();
-      if (tid == 0) {
-        issue_ydiag(tb + dcol, smem_u32(ar.B), 128, 1024, smem_u32(ar.X), blk, ge.S_ext);
-        issue_ydiag(tb + dcol + 64, smem_u32(ar.B + 32768), 128, 1024, smem_u32(ar.X), blk, ge.S_ext);
-        commit(&hd.bar_diag);
-      }
-      diag_pending = true;
-    }
-  }
-  // ---- 5. start state H_c: look back over the earlier chunks, then publish H_{c+1} -----------------------
-  float Hc[16];
-  if (ok) {
-    if (c == 0) {
-      const float* init = CHUNKED ? a.state + ((size_t)sg.slot * a.H + h) * hs
-                                  : (a.init_state ? a.init_state + ((size_t)i * a.H + h) * hs : nullptr);
-#pragma unroll
-      for (int j = 0; j < 16; ++j) Hc[j] = init ? init[(d0 + j) * N + n] : 0.f;
-    } else {
-      // warp 0: lane l watches chunk top - l, 32 chunks per window, from c - 1 down; the chain
-      // starts at the nearest chunk that has published its end state, once every chunk above it has
-      // published its chunk state (chunk 0 publishes only its end state)
-      if (warp == 0) {
-        int top = c - 1, k0 = -1, good = 1;
-        while (good && k0 < 0) {
-          const int k = top - lane;
-          int32_t f = 2;
-          if (k >= 0) f = flag_wait(a.ws_flags + unit_index(a, i, k, h), a.status, a.wait_ns);
-          if (!__all_sync(kFull, f != 0)) {
-            good = 0;
-            break;
-          }
-          const unsigned inc = __ballot_sync(kFull, k >= 0 && f == 2);
-          if (inc != 0) k0 = top - (__ffs(inc) - 1);
-          else if (top < 32) good = 0;   // no end state at all: cannot happen (chunk 0 publishes one)
-          top -= 32;
-        }
-        if (lane == 0) {
-          hd.lb_stop = k0;
-          hd.lb_ok = good;
-        }
-      }
-      __syncthreads();
-      ok = hd.lb_ok != 0;
-      if (ok) {
-        const int k0 = hd.lb_stop;
-        const float4* Hk = reinterpret_cast<const float4*>(a.ws_incl + unit_index(a, i, k0, h) * hs + (size_t)n * P + d0);
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const float4 v = __ldcg(Hk + j);
-          Hc[4 * j] = v.x; Hc[4 * j + 1] = v.y; Hc[4 * j + 2] = v.z; Hc[4 * j + 3] = v.w;
-        }
-        for (int kk = k0 + 1; kk < c; kk += 2) {   // two chunks' loads in flight
-          float4 sv[2][4];
-          float ev[2] = {0.f, 0.f};
-#pragma unroll
-          for (int u = 0; u < 2; ++u) {
-            if (kk + u < c) {
-              const size_t uk = unit_index(a, i, kk + u, h);
-              ev[u] = __ldcg(a.ws_tot + uk);
-              const float4* Sk = reinterpret_cast<const float4*>(a.ws_states + uk * hs + (size_t)n * P + d0);
-#pragma unroll
-              for (int j = 0; j < 4; ++j) sv[u][j] = __ldcg(Sk + j);
-            }
-          }
-#pragma unroll
-          for (int u = 0; u < 2; ++u) {
-            if (kk + u < c) {
-#pragma unroll
-              for (int j = 0; j < 4; ++j) {
-                Hc[4 * j] = __fmaf_rn(ev[u], Hc[4 * j], sv[u][j].x);
-                Hc[4 * j + 1] = __fmaf_rn(ev[u], Hc[4 * j + 1], sv[u][j].y);
-                Hc[4 * j + 2] = __fmaf_rn(ev[u], Hc[4 * j + 2], sv[u][j].z);
-                Hc[4 * j + 3] = __fmaf_rn(ev[u], Hc[4 * j + 3], sv[u][j].w);
-              }
-            }
-          }
-        }
-      }
-    }
-  }
-  if (ok) {
-    float Hn[16];
-#pragma unroll
-    for (int j = 0; j < 16; ++j) Hn[j] = __fmaf_rn(e_c, Hc[j], S[j]);
+  auto store_end_state = [&](const float (&Hn)[kOC]) {
     if (has_next) {
       float4* wi = reinterpret_cast<float4*>(a.ws_incl + unit * hs + (size_t)n * P + d0);
-#pragma unroll
-      for (int j = 0; j < 4; ++j) wi[j] = make_float4(Hn[4 * j], Hn[4 * j + 1], Hn[4 * j + 2], Hn[4 * j + 3]);
-      __threadfence();
+      wi[0] = make_float4(Hn[0], Hn[1], Hn[2], Hn[3]);
+      wi[1] = make_float4(Hn[4], Hn[5], Hn[6], Hn[7]);
     }
     float* out = nullptr;
     if (!CHUNKED && a.chunk_states != nullptr) out = a.chunk_states + unit * hs;
     if (!CHUNKED && c == sg.nch - 1) {
       float* fs = a.final_state + ((size_t)i * a.H + h) * hs;
 #pragma unroll
-      for (int j = 0; j < 16; ++j) fs[(d0 + j) * N + n] = Hn[j];
+      for (int j = 0; j < kOC; ++j) fs[(d0 + j) * N + n] = Hn[j];
     }
     if (CHUNKED && c + 1 == sg.total / Q) out = a.state + ((size_t)sg.slot * a.H + h) * hs;   // new checkpoint
     if (out != nullptr) {
 #pragma unroll
-      for (int j = 0; j < 16; ++j) out[(d0 + j) * N + n] = Hn[j];
+      for (int j = 0; j < kOC; ++j) out[(d0 + j) * N + n] = Hn[j];
     }
-    // the [H_hi; H_lo] operand tile (U region: the state MMAs are done)
+  };
+  // the [H_hi; H_lo] operand tile of the start state (U region: the state MMAs are done)
+  auto store_h_tile = [&](const float (&Hc)[kOC]) {
 #pragma unroll
-    for (int j = 0; j < 16; ++j) {
+    for (int j = 0; j < kOC; ++j) {
       const bf16 hi = __float2bfloat16_rn(Hc[j]);
       const bf16 lo = __float2bfloat16_rn(__fsub_rn(Hc[j], __bfloat162float(hi)));
       *reinterpret_cast<bf16*>(ar.U + sw128(128, d0 + j, n)) = hi;
       *reinterpret_cast<bf16*>(ar.U + sw128(128, P + d0 + j, n)) = lo;
     }
+  };
+  if (ok && c == 0) {
+    float S[kOC], Hc[kOC], Hn[kOC];
+    tmem_ld8(taddr(tb, 32 * q, kColState + d0), S);
+    const float e_c = expf(hd.ahi[nrows - 1]);
+    const float* init = CHUNKED ? a.state + ((size_t)sg.slot * a.H + h) * hs
+                                : (a.init_state ? a.init_state + ((size_t)i * a.H + h) * hs : nullptr);
+#pragma unroll
+    for (int j = 0; j < kOC; ++j) Hc[j] = init ? init[(d0 + j) * N + n] : 0.f;
+#pragma unroll
+    for (int j = 0; j < kOC; ++j) Hn[j] = __fmaf_rn(e_c, Hc[j], S[j]);
+    store_end_state(Hn);
+    store_h_tile(Hc);
+    if (has_next) publish_flag(a.ws_flags + unit, 2);
   }
-  publish();
-  if (ok && has_next && tid == 0) st_release(a.ws_flags + unit, 2);
-  // ---- 6. off-diagonal sums of every t-tile, then the epilogues ----------------------------------------
+  if (ok && c > 0 && has_next) {
+    float S[kOC];
+    tmem_ld8(taddr(tb, 32 * q, kColState + d0), S);
+    const float e_c = expf(hd.ahi[nrows - 1]);
+    float4* ws = reinterpret_cast<float4*>(a.ws_states + unit * hs + (size_t)n * P + d0);
+    ws[0] = make_float4(S[0], S[1], S[2], S[3]);
+    ws[1] = make_float4(S[4], S[5], S[6], S[7]);
+    if (tid == 0) a.ws_tot[unit] = e_c;
+    publish_flag(a.ws_flags + unit, 1);
+  }
+  // ---- 4. every diagonal block (needs no start state), M tiles alternating between the B and C ------
+  // regions; accumulators: t-tile 0 in [0, 128), t-tile 1 in [128, 256) over the Gram block each uses.
+  uint32_t ph_diag[2] = {0, 0};
+  bool pend[2] = {false, false};
+  int jb = 0;
+  for (int tau = 0; tau < ntiles && ok; ++tau) {
+    const Geom ge = geom(Q, tau);
+    const uint32_t dcol = tau == 0 ? 0u : kColG1;
+    for (int blk = 0; blk < ge.nblk && ok; ++blk, ++jb) {
+      const int bi = jb & 1;
+      uint8_t* mt = bi == 0 ? ar.B : ar.C;
+      if (pend[bi]) {   // the diagonal MMAs two blocks back still read this M tile
+        ok = mma_done(&hd.bar_diag[bi], ph_diag[bi], a);
+        ph_diag[bi] ^= 1;
+        pend[bi] = false;
+        if (!ok) break;
+      }
+      build_m(ar, mt, tb, dcol + 128 * blk, Q, tau, blk, nrows);
+      publish();
+      if (tid == 0) {
+        issue_ydiag(tb + dcol, smem_u32(mt), 128, 1024, smem_u32(ar.X), blk, ge.S_ext);
+        issue_ydiag(tb + dcol + 64, smem_u32(mt + 32768), 128, 1024, smem_u32(ar.X), blk, ge.S_ext);
+        commit(&hd.bar_diag[bi]);
+      }
+      pend[bi] = true;
+    }
+  }
+  // the C tile comes back once nothing reads its region (state operand, M tile)
+  const bool c_used = two_state_blocks || jb > 1;
+  bool c_pending = false;   // a TMA reload of the C tile is in flight
+  if (ok && c_used) {
+    if (pend[1]) {
+      ok = mma_done(&hd.bar_diag[1], ph_diag[1], a);
+      ph_diag[1] ^= 1;
+      pend[1] = false;
+    }
+    if (ok) {
+      reload_c(ar, maps, make_rows<bf16>(a, sg.slot, h, nbuf, tok0), tma, Q, nrows, g, (int)tok0, &hd.bar_c);
+      c_pending = tma;
+    }
+  }
+  // ---- 5. start state H_c of a later chunk: look back over the earlier chunks, publish H_{c+1} --------
+  if (ok && c > 0) {
+    // warp 0: lane l watches chunk top - l, 32 chunks per window, from c - 1 down; the chain starts
+    // at the nearest chunk that has published its end state, once every chunk above it has
+    // published its chunk state (chunk 0 publishes its end state, never its chunk state)
+    if (warp == 0) {
+      int top = c - 1, k0 = -1, good = 1;
+      while (good && k0 < 0) {
+        const int k = top - lane;
+        int32_t f = 2;
+        if (k >= 0) f = flag_wait(a.ws_flags + unit_index(a, i, k, h), a.status, a.wait_ns);
+        if (!__all_sync(kFull, f != 0)) {
+          good = 0;
+          break;
+        }
+        const unsigned inc = __ballot_sync(kFull, k >= 0 && f == 2);
+        if (inc != 0) k0 = top - (__ffs(inc) - 1);
+        else if (top < 32) good = 0;
+        top -= 32;
+      }
+      if (lane == 0) {
+        hd.lb_stop = k0;
+        hd.lb_ok = good;
+      }
+    }
+    __syncthreads();
+    ok = hd.lb_ok != 0;
+    if (ok) {
+      float Hc[kOC];
+      const int k0 = hd.lb_stop;
+      const float4* Hk = reinterpret_cast<const float4*>(a.ws_incl + unit_index(a, i, k0, h) * hs + (size_t)n * P + d0);
+      const float4 v0 = __ldcg(Hk), v1 = __ldcg(Hk + 1);
+      Hc[0] = v0.x; Hc[1] = v0.y; Hc[2] = v0.z; Hc[3] = v0.w;
+      Hc[4] = v1.x; Hc[5] = v1.y; Hc[6] = v1.z; Hc[7] = v1.w;
+      for (int kk = k0 + 1; kk < c; kk += 2) {   // two chunks' loads in flight
+        float4 sv[2][2];
+        float ev[2];
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+          ev[u] = 0.f;
+          if (kk + u < c) {
+            const size_t uk = unit_index(a, i, kk + u, h);
+            ev[u] = __ldcg(a.ws_tot + uk);
+            const float4* Sk = reinterpret_cast<const float4*>(a.ws_states + uk * hs + (size_t)n * P + d0);
+            sv[u][0] = __ldcg(Sk);
+            sv[u][1] = __ldcg(Sk + 1);
+          }
+        }
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+          if (kk + u < c) {
+            const float sx[kOC] = {sv[u][0].x, sv[u][0].y, sv[u][0].z, sv[u][0].w,
+                                   sv[u][1].x, sv[u][1].y, sv[u][1].z, sv[u][1].w};
+#pragma unroll
+            for (int j = 0; j < kOC; ++j) Hc[j] = __fmaf_rn(ev[u], Hc[j], sx[j]);
+          }
+        }
+      }
+      float S[kOC], Hn[kOC];
+      tmem_ld8(taddr(tb, 32 * q, kColState + d0), S);
+      const float e_c = expf(hd.ahi[nrows - 1]);
+#pragma unroll
+      for (int j = 0; j < kOC; ++j) Hn[j] = __fmaf_rn(e_c, Hc[j], S[j]);
+      store_end_state(Hn);
+      store_h_tile(Hc);
+      if (has_next) publish_flag(a.ws_flags + unit, 2);
+    }
+  }
+  // ---- 6. off-diagonal MMAs ------------------------------------------------------------------------------
+  if (c_pending) {   // waited for even after an error: no copy may land in a finished CTA's memory
+    ok = mbar_wait(&hd.bar_c, 0, a.status, a.wait_ns) && ok;
+    c_pending = false;
+  }
+  publish();   // also completes a cp.async reload of the C tile
+  ok = __syncthreads_and(ok);
   // t-tile 0 into [384, 512) (the chunk state's columns, read above), t-tile 1 into [256, 384) (its
   // second Gram block, consumed by its M tile).
   if (ok && tid == 0) {
@@ -446,19 +503,23 @@ __global__ void __launch_bounds__(kScanThreads, 1)
       issue_yoff(tb + (tau == 0 ? kColOff : kColOff1), smem_u32(ar.C + 128 * 128 * tau), Q, 1024, smem_u32(ar.U), 128);
     commit(&hd.bar_off);
   }
-  if (ok && diag_pending) {
-    ok = mma_done(&hd.bar_diag, ph_diag, a);
-    ph_diag ^= 1;
-    diag_pending = false;
+  for (int bi = 0; bi < 2 && ok; ++bi) {
+    if (pend[bi]) {
+      ok = mma_done(&hd.bar_diag[bi], ph_diag[bi], a);
+      ph_diag[bi] ^= 1;
+      pend[bi] = false;
+    }
   }
   if (ok) ok = mma_done(&hd.bar_off, 0, a);
+  // ---- 7. epilogues ---------------------------------------------------------------------------------
   const float Dh = a.D[h];
   for (int tau = 0; tau < ntiles && ok; ++tau) {
     const Geom ge = geom(Q, tau);
     epilogue(ar, tb, tau == 0 ? 0u : kColG1, tau == 0 ? kColOff : kColOff1, Q, tau, max(nbuf, ge.t0),
              min(nrows, ge.t0 + ge.TT), Dh, (bf16*)a.y, tok0, a.H, h);
   }
-  if (diag_pending) mma_done(&hd.bar_diag, ph_diag, a);   // no MMA may outlive the TMEM allocation
+  for (int bi = 0; bi < 2; ++bi)   // no MMA may outlive the TMEM allocation
+    if (pend[bi]) mma_done(&hd.bar_diag[bi], ph_diag[bi], a);
   before_sync();
   __syncthreads();
   if (warp == 0) tmem_dealloc(tb, kScanTmemCols);
