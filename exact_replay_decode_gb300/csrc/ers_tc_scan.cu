@@ -425,11 +425,11 @@ __global__ void __launch_bounds__(kScanThreads, 1)
     }
     hand_off(hd);   // token tiles (and the weights, for every math thread)
     // ---- chunk state: U operands (the second K block's in the C region, once the Gram MMAs are done) ----
-    build_u_tiles(ar.X, hd.w, nrows, 0, K < 128 ? K : 128, ar.U, ar.U + kUTile, ar.U + 2 * kUTile);
+    build_u_tiles(ar.X, hd.w, nrows, 0, K < 128 ? K : 128, ar.U, ar.U + kUTile, ar.U + 2 * kUTile, kMath);
     hand_off(hd);
     mma_wait(&hd.bar_gram, 0, a);
     if (two_state_blocks) {
-      build_u_tiles(ar.X, hd.w, nrows, 128, K - 128, ar.C, ar.C + kUTile, ar.C + 2 * kUTile);
+      build_u_tiles(ar.X, hd.w, nrows, 128, K - 128, ar.C, ar.C + kUTile, ar.C + 2 * kUTile, kMath);
       hand_off(hd);
     }
     mma_wait(&hd.bar_state, 0, a);

@@ -193,10 +193,11 @@ __device__ __forceinline__ void zero_tile_chunk(uint8_t* tile, uint32_t R, uint3
 
 // U_term rows [0, nk16) for chunk rows s = s0 + r: u = w_s x_s[d]; hi = bf16(u),
 // mid = bf16(u - hi), lo = bf16(u - hi - mid).  xT holds rows s (MN-major, 64 wide); rows with
-// s >= nrows are written as zeros.  All kThreads threads.
+// s >= nrows are written as zeros.  Threads [0, nthreads) of the block take part (default: all).
 __device__ __forceinline__ void build_u_tiles(const uint8_t* xT, const float* w, int nrows, int s0, int nr,
-                                              uint8_t* u0, uint8_t* u1, uint8_t* u2) {
-  for (int id = threadIdx.x; id < nr * (P / 8); id += blockDim.x) {
+                                              uint8_t* u0, uint8_t* u1, uint8_t* u2, int nthreads = 0) {
+  const int stride = nthreads > 0 ? nthreads : (int)blockDim.x;
+  for (int id = threadIdx.x; id < nr * (P / 8); id += stride) {
     const int r = id / (P / 8), c = id % (P / 8);
     const int s = s0 + r;
     uint4 h4 = make_uint4(0, 0, 0, 0), m4 = h4, l4 = h4;
