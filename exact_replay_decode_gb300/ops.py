@@ -281,21 +281,6 @@ class ReplayCache:
                           (ctypes.c_uint32 * 2)(*self.sr_key), int(self.sr_nonce) & 0xFFFFFFFF,
                           _ptr(self.buf_pages), self.page_rows, self.npages)
 
-    def read_values(self) -> Optional[torch.Tensor]:
-        """The read copy's values as fp32 (FP8: code * row scale), or None without a read copy."""
-        if self.read_copy is None:
-            return None
-        if self.read_scale is None:
-            return self.read_copy.float()
-        if self.read_block_scale is None:
-            return self.read_copy.view(torch.float8_e4m3fn).float() * self.read_scale.unsqueeze(-1)
-        e2m1 = torch.tensor([0, 0.5, 1, 1.5, 2, 3, 4, 6, -0.0, -0.5, -1, -1.5, -2, -3, -4, -6],
-                            dtype=torch.float32, device=self.read_copy.device)
-        c = self.read_copy.long()
-        q = torch.stack([e2m1[c & 15], e2m1[c >> 4]], dim=-1).flatten(-2)
-        beta = self.read_block_scale.view(torch.float8_e4m3fn).float().repeat_interleave(16, dim=-1)
-        return q * beta * self.read_scale.unsqueeze(-1)
-
     def seed(self, state: torch.Tensor, params: "LayerParams", nseq: Optional[int] = None,
              slot: Optional[torch.Tensor] = None, stream=None) -> None:
         """Casts an fp32 state [nslots,H,P,N] into the shared NVFP4 state of the listed slots (all by

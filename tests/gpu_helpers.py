@@ -92,6 +92,24 @@ def same_bits(a: torch.Tensor, b: torch.Tensor) -> bool:
     return a.shape == b.shape and torch.equal(bits(a), bits(b))
 
 
+def read_values(cache):
+    """Inspection of a cache's read copy in the tests: its values as fp32 tensors (bf16 as is; FP8
+    e4m3 code times the row scale; NVFP4 e2m1 code times block scale times row scale), or None
+    without a read copy.  Decodes the stored bytes per the layouts include/ers.h documents."""
+    if cache.read_copy is None:
+        return None
+    if cache.read_scale is None:
+        return cache.read_copy.float()
+    if cache.read_block_scale is None:
+        return cache.read_copy.view(torch.float8_e4m3fn).float() * cache.read_scale.unsqueeze(-1)
+    e2m1 = torch.tensor([0, 0.5, 1, 1.5, 2, 3, 4, 6, -0.0, -0.5, -1, -1.5, -2, -3, -4, -6],
+                        dtype=torch.float32, device=cache.read_copy.device)
+    c = cache.read_copy.long()
+    q = torch.stack([e2m1[c & 15], e2m1[c >> 4]], dim=-1).flatten(-2)
+    beta = cache.read_block_scale.view(torch.float8_e4m3fn).float().repeat_interleave(16, dim=-1)
+    return q * beta * cache.read_scale.unsqueeze(-1)
+
+
 def out_tol(tokens) -> float:
     return OUT_TOL_BF16 if tokens.bf16 else OUT_TOL_F32
 

@@ -14,7 +14,7 @@ import torch
 import oracle
 import synth
 from synth import torch_io
-from gpu_helpers import OUT_TOL_BF16, dev, layer, same_bits
+from gpu_helpers import OUT_TOL_BF16, dev, layer, same_bits, read_values
 
 pytestmark = pytest.mark.gpu
 
@@ -43,7 +43,7 @@ def test_refresh_cast_matches_oracle(read_dtype):
     cache.state.copy_(torch.from_numpy(st))
     prm = layer(_params(H))
     ers.refresh(cache, prm, replayssm=True, drafts_T=L + 1)   # h = 0 + T > L everywhere
-    got = cache.read_values().cpu().numpy()
+    got = read_values(cache).cpu().numpy()
     want = _CAST[read_dtype](st).astype(np.float32)
     assert np.array_equal(got.view(np.uint32), want.view(np.uint32))
     assert same_bits(cache.state, torch.from_numpy(st).to(dev()))     # the anchor is untouched
@@ -98,7 +98,7 @@ def test_fp8_exact_mode_fused_refresh_casts_and_matches_separate():
                                       params.dt_bias, np.arange(0, S * Q + 1, Q), ck)
             want = ck.astype(np.float32)
             assert np.array_equal(c1.state.cpu().numpy().view(np.uint32), want.view(np.uint32)), k
-            got = c1.read_values().cpu().numpy()
+            got = read_values(c1).cpu().numpy()
             assert np.array_equal(got.view(np.uint32), oracle.fp8_rows_round(ck).astype(np.float32).view(np.uint32))
             casts += S
     assert casts > 0
@@ -199,7 +199,7 @@ def test_verify_flush_casts_equal_the_oracle_under_exact_folds(read_dtype):
         model.commit(acc[k])
         assert np.array_equal(cache.state.cpu().numpy().view(np.uint32),
                               model.anchor.astype(np.float32).view(np.uint32)), k
-        assert np.array_equal(cache.read_values().cpu().numpy().astype(np.float64), model.read), k
+        assert np.array_equal(read_values(cache).cpu().numpy().astype(np.float64), model.read), k
     assert model.flushes > 0
 
 

@@ -18,7 +18,7 @@ import torch
 import oracle
 import synth
 from synth import torch_io
-from gpu_helpers import MAX_REL_NARROW, OUT_TOL_BF16, StepCheck, dev, layer, same_bits
+from gpu_helpers import MAX_REL_NARROW, OUT_TOL_BF16, StepCheck, dev, layer, same_bits, read_values
 
 pytestmark = pytest.mark.gpu
 
@@ -54,7 +54,7 @@ def test_shared_state_refreshes_equal_the_oracle_exactly():
     prm = layer(params)
     c = _shared(ers, S, DIMS, prm, torch.from_numpy(st0).to(dev()))
     a0 = oracle.nvfp4_rows_round(st0)                                   # the seed: round-to-nearest cast
-    assert np.array_equal(c.read_values().cpu().numpy().astype(np.float64), a0)
+    assert np.array_equal(read_values(c).cpu().numpy().astype(np.float64), a0)
     nonce = {"v": 0}
     model = oracle.ReplaySSMModel(params, a0, L, shared=True,
                                   anchor_round=lambda i, fin: oracle.nvfp4_sr_state(fin, KEY, nonce["v"], i))
@@ -70,7 +70,7 @@ def test_shared_state_refreshes_equal_the_oracle_exactly():
             c.sr_nonce = 500 + k
             ers.refresh(c, prm, replayssm=True, drafts_T=L)
             model.refresh(list(range(S)))
-            got = c.read_values().cpu().numpy().astype(np.float64)
+            got = read_values(c).cpu().numpy().astype(np.float64)
             assert np.array_equal(got, model.anchor), k
     assert model.flushes == 2 * S
 
@@ -88,7 +88,7 @@ def test_fused_flush_equals_refresh_and_decode_and_matches_the_model():
     fin32 = fin.astype(np.float32)                     # the oracle's state after the history starts both
     c1, c2 = (_shared(ers, S, DIMS, prm, torch.from_numpy(fin32).to(dev())) for _ in range(2))
     a0 = oracle.nvfp4_rows_round(fin32[samples])
-    assert np.array_equal(c1.read_values()[samples].cpu().numpy().astype(np.float64), a0)
+    assert np.array_equal(read_values(c1)[samples].cpu().numpy().astype(np.float64), a0)
     nonce = {"v": 0}
     model = oracle.ReplaySSMModel(params, a0, L, shared=True,
                                   anchor_round=lambda i, f: oracle.nvfp4_sr_state(f, KEY, nonce["v"], samples[i]))
@@ -113,7 +113,7 @@ def test_fused_flush_equals_refresh_and_decode_and_matches_the_model():
     # the GPU folds in fp32 and the model in fp64: a stochastic decision flips only where the two
     # fp32 values straddle the threshold of a word (about 2^-23 relative per value and flush), so
     # almost every value is the model's and none is more than a few code steps away
-    got = c1.read_values()[samples].cpu().numpy().astype(np.float64)
+    got = read_values(c1)[samples].cpu().numpy().astype(np.float64)
     assert np.mean(got != model.anchor) < 1e-3
 
 

@@ -19,7 +19,7 @@ import torch
 import oracle
 import synth
 from synth import torch_io
-from gpu_helpers import MAX_REL_NARROW, OUT_TOL_BF16, StepCheck, dev, layer, same_bits
+from gpu_helpers import MAX_REL_NARROW, OUT_TOL_BF16, StepCheck, dev, layer, same_bits, read_values
 
 pytestmark = pytest.mark.gpu
 
@@ -113,7 +113,7 @@ def test_sr_anchor_write_matches_oracle(read_dtype):
     c, model = _run_exact(ers, params, stream, st16, S, K, read_dtype, 77)
     got = c.state.float().cpu().numpy().astype(np.float64)
     assert np.array_equal(got, model.anchor)
-    assert np.array_equal(c.read_values().cpu().numpy().astype(np.float64), model.read)
+    assert np.array_equal(read_values(c).cpu().numpy().astype(np.float64), model.read)
     plain = oracle.ReplaySSMModel(params, st16.float().cpu().numpy().astype(np.float64), DIMS.chunk)
     for k in range(K):
         plain.verify([(stream.x[r:r + 1], stream.dt[r:r + 1], stream.B[r:r + 1], stream.C[r:r + 1])
