@@ -53,6 +53,10 @@ constexpr int kSlices = kMathWarps / 4;              // column slices per TMEM l
 constexpr int kMC = 128 / kSlices;                   // M-tile columns per math warp
 constexpr int kOC = 64 / kSlices;                    // output columns / state rows per math thread
 constexpr uint32_t kBarMath = 1;
+// Operand hand-offs per unit: token tiles, up to two state operands, up to three M tiles, the
+// start-state tile.  Each has its own single-use mbarrier, so that the math warps may run any
+// number of hand-offs ahead of the issuer.
+constexpr int kMaxHandoffs = 8;
 constexpr uint32_t kScanTmemCols = 512;
 // TMEM columns: [0, 128) Gram of t-tile 0, then its diagonal sums (hi [0, 64), lo [64, 128));
 // [128, 384) Gram of t-tile 1, then its diagonal sums in [128, 256) and its off-diagonal sums in
@@ -61,7 +65,7 @@ constexpr uint32_t kColG1 = 128, kColState = 384, kColOff = 384, kColOff1 = 256;
 
 struct ScanHdr {
   uint64_t bar_tma, bar_c, bar_gram, bar_state, bar_diag[2], bar_off;
-  uint64_t bar_ready;   // math -> issuer: an operand is in shared memory (one arrival per hand-off)
+  uint64_t bar_ready[kMaxHandoffs];   // math -> issuer: hand-off k's operand is in shared memory
   uint64_t bar_sdone;   // math -> publisher: S_c and e_c are stored
   uint64_t bar_hdone;   // math -> publisher: H_{c+1} is stored
   uint64_t bar_lb;      // publisher -> math: the look-back result is in lb_stop / lb_ok
@@ -119,13 +123,14 @@ __device__ __forceinline__ void math_sync() { named_sync(kBarMath, kMath); }
 
 // Math threads: their shared-memory writes (generic proxy, cp.async) are complete and visible to
 // the tensor core and their TMEM loads are done; after a barrier among them, one arrival on the
-// issuer's operand barrier (so that consecutive hand-offs can never share a phase).
-__device__ __forceinline__ void hand_off(ScanHdr& hd) {
+// hand-off's own barrier.
+__device__ __forceinline__ void hand_off(ScanHdr& hd, int& k) {
   cp_async_wait_all();
   fence_async_smem();
   before_sync();
   math_sync();
-  if (threadIdx.x == 0) mbar_arrive(&hd.bar_ready);
+  if (threadIdx.x == 0) mbar_arrive(&hd.bar_ready[k]);
+  ++k;
 }
 
 // Math threads: wait for an MMA group; true unless the wait gave up (reported).
@@ -288,7 +293,7 @@ __global__ void __launch_bounds__(kScanThreads, 1)
     mbar_init(&hd.bar_diag[0], 1);
     mbar_init(&hd.bar_diag[1], 1);
     mbar_init(&hd.bar_off, 1);
-    mbar_init(&hd.bar_ready, 1);
+    for (int k = 0; k < kMaxHandoffs; ++k) mbar_init(&hd.bar_ready[k], 1);
     mbar_init(&hd.bar_sdone, kMath);
     mbar_init(&hd.bar_hdone, kMath);
     mbar_init(&hd.bar_lb, 1);
@@ -312,10 +317,9 @@ __global__ void __launch_bounds__(kScanThreads, 1)
         tma_load_3d(ar.C, &maps.C, 0, g, z, &hd.bar_tma);
         tma_load_3d(ar.C + Q * 128, &maps.C, 64, g, z, &hd.bar_tma);
       }
-      uint32_t ph = 0;
+      int hk = 0;
       auto ready = [&]() {   // the next operand hand-off of the math threads
-        mbar_wait(&hd.bar_ready, ph, a.status, a.wait_ns);
-        ph ^= 1;
+        mbar_wait(&hd.bar_ready[hk++], 0, a.status, a.wait_ns);
         after_sync();
       };
       ready();   // token tiles in place (tail rows zeroed)
@@ -402,6 +406,7 @@ __global__ void __launch_bounds__(kScanThreads, 1)
     const int q = warp & 3, sl = warp >> 2;
     const int n = 32 * q + lane;   // state column owned by this thread
     const int d0 = kOC * sl;       // and its kOC state rows d0 ..
+    int hk = 0;                    // hand-offs so far
     if (!tma) load_rows_async(ar, make_rows<bf16>(a, sg.slot, h, nbuf, tok0), Q, nrows, false);
     if (tid < kQMax) {
       float dl = 0.f, da = 0.f;
@@ -423,14 +428,14 @@ __global__ void __launch_bounds__(kScanThreads, 1)
       const df last = {hd.ahi[nrows - 1], hd.alo[nrows - 1]};
       hd.w[tid] = __fmul_rn(hd.delta[tid], expf(df_diff(last, df{hd.ahi[tid], hd.alo[tid]})));
     }
-    hand_off(hd);   // token tiles (and the weights, for every math thread)
+    hand_off(hd, hk);   // token tiles (and the weights, for every math thread)
     // ---- chunk state: U operands (the second K block's in the C region, once the Gram MMAs are done) ----
     build_u_tiles(ar.X, hd.w, nrows, 0, K < 128 ? K : 128, ar.U, ar.U + kUTile, ar.U + 2 * kUTile, kMath);
-    hand_off(hd);
+    hand_off(hd, hk);
     mma_wait(&hd.bar_gram, 0, a);
     if (two_state_blocks) {
       build_u_tiles(ar.X, hd.w, nrows, 128, K - 128, ar.C, ar.C + kUTile, ar.C + 2 * kUTile, kMath);
-      hand_off(hd);
+      hand_off(hd, hk);
     }
     mma_wait(&hd.bar_state, 0, a);
     // ---- publish: chunk 0 its end state H_1 (H_0 is known), later chunks S_c and e_c ------------------
@@ -506,7 +511,7 @@ __global__ void __launch_bounds__(kScanThreads, 1)
           math_sync();   // ... for every math thread before any overwrites it
         }
         build_m(ar, mt, tb, dcol + 128 * blk, Q, tau, blk, nrows);
-        hand_off(hd);
+        hand_off(hd, hk);
         pend[bi] = true;
       }
     }
@@ -566,7 +571,7 @@ __global__ void __launch_bounds__(kScanThreads, 1)
       store_end_state(Hn);
       store_h_tile(Hc);
     }
-    hand_off(hd);   // start-state tile (the off-diagonal MMAs overwrite the state's TMEM columns)
+    hand_off(hd, hk);   // start-state tile (the off-diagonal MMAs overwrite the state's TMEM columns)
     for (int bi = 0; bi < 2; ++bi)
       if (pend[bi]) {
         mma_wait(&hd.bar_diag[bi], ph_diag[bi], a);
