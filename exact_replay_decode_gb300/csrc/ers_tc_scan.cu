@@ -466,10 +466,10 @@ __global__ void __launch_bounds__(kScanThreads, 1)
     auto store_h_tile = [&](const float (&Hc)[kOC]) {
 #pragma unroll
       for (int j = 0; j < kOC; ++j) {
-        uint32_t hb, lb;
-        split1(Hc[j], hb, lb);
-        *reinterpret_cast<uint16_t*>(ar.U + sw128(128, d0 + j, n)) = (uint16_t)hb;
-        *reinterpret_cast<uint16_t*>(ar.U + sw128(128, P + d0 + j, n)) = (uint16_t)lb;
+        const bf16 hi = __float2bfloat16_rn(Hc[j]);
+        const bf16 lo = __float2bfloat16_rn(__fsub_rn(Hc[j], __bfloat162float(hi)));
+        *reinterpret_cast<bf16*>(ar.U + sw128(128, d0 + j, n)) = hi;
+        *reinterpret_cast<bf16*>(ar.U + sw128(128, P + d0 + j, n)) = lo;
       }
     };
     if (c == 0) {

@@ -117,45 +117,33 @@ __device__ __forceinline__ void issue_state_block(uint32_t tS, uint32_t bT, uint
 }
 
 // ---- operand builders (generic proxy writes; the caller fences before issuing) ---------------------
-// fp32 -> bf16 round-to-nearest-even on the bit pattern (integer operations only): add half an ulp
-// of the bf16 grid, minus one when the kept part is even, and drop the low 16 bits; exact for every
-// finite value (values rounding past the largest bf16 become infinities, as RNE requires).  A NaN
-// becomes the quiet NaN 0x7FFF.  Every operand split and packed output of the engine goes through
-// this one routine, so all paths round identically.
-__device__ __forceinline__ uint32_t bf16_rne_bits(float v) {
-  const uint32_t u = __float_as_uint(v);
-  if ((u & 0x7FFFFFFFu) > 0x7F800000u) return 0x7FFFu;
-  return (u + 0x7FFFu + ((u >> 16) & 1u)) >> 16;
-}
-// the bf16 value of those bits as fp32 (exact)
-__device__ __forceinline__ float bf16_bits_to_f(uint32_t b) { return __uint_as_float(b << 16); }
-
 __device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
-  return bf16_rne_bits(a) | (bf16_rne_bits(b) << 16);
-}
-
-// one fp32 value -> bf16 bits of hi = RNE(v) and lo = RNE(v - hi)
-__device__ __forceinline__ void split1(float v, uint32_t& hb, uint32_t& lb) {
-  hb = bf16_rne_bits(v);
-  lb = bf16_rne_bits(__fsub_rn(v, bf16_bits_to_f(hb)));
+  const __nv_bfloat162 v = __floats2bfloat162_rn(a, b);
+  return *reinterpret_cast<const uint32_t*>(&v);
 }
 
 // 8 fp32 values -> hi and lo bf16 chunks
 __device__ __forceinline__ void split8(const float (&v)[8], uint4& hi, uint4& lo) {
-  uint32_t h[8], l[8];
+  float h[8], l[8];
 #pragma unroll
-  for (int i = 0; i < 8; ++i) split1(v[i], h[i], l[i]);
-  hi = make_uint4(h[0] | (h[1] << 16), h[2] | (h[3] << 16), h[4] | (h[5] << 16), h[6] | (h[7] << 16));
-  lo = make_uint4(l[0] | (l[1] << 16), l[2] | (l[3] << 16), l[4] | (l[5] << 16), l[6] | (l[7] << 16));
+  for (int i = 0; i < 8; ++i) {
+    h[i] = __bfloat162float(__float2bfloat16_rn(v[i]));
+    l[i] = __fsub_rn(v[i], h[i]);
+  }
+  hi = make_uint4(pack_bf16x2(h[0], h[1]), pack_bf16x2(h[2], h[3]), pack_bf16x2(h[4], h[5]), pack_bf16x2(h[6], h[7]));
+  lo = make_uint4(pack_bf16x2(l[0], l[1]), pack_bf16x2(l[2], l[3]), pack_bf16x2(l[4], l[5]), pack_bf16x2(l[6], l[7]));
 }
 
 // 4 fp32 values -> hi and lo bf16 (8 bytes each), the same operations as split8
 __device__ __forceinline__ void split4(const float (&v)[4], uint2& hi, uint2& lo) {
-  uint32_t h[4], l[4];
+  float h[4], l[4];
 #pragma unroll
-  for (int i = 0; i < 4; ++i) split1(v[i], h[i], l[i]);
-  hi = make_uint2(h[0] | (h[1] << 16), h[2] | (h[3] << 16));
-  lo = make_uint2(l[0] | (l[1] << 16), l[2] | (l[3] << 16));
+  for (int i = 0; i < 4; ++i) {
+    h[i] = __bfloat162float(__float2bfloat16_rn(v[i]));
+    l[i] = __fsub_rn(v[i], h[i]);
+  }
+  hi = make_uint2(pack_bf16x2(h[0], h[1]), pack_bf16x2(h[2], h[3]));
+  lo = make_uint2(pack_bf16x2(l[0], l[1]), pack_bf16x2(l[2], l[3]));
 }
 
 // fp32 state [64][128] -> [H_hi; H_lo] tile.  Called by all kThreads threads (blockDim.x ==
@@ -215,21 +203,23 @@ __device__ __forceinline__ void build_u_tiles(const uint8_t* xT, const float* w,
     uint4 h4 = make_uint4(0, 0, 0, 0), m4 = h4, l4 = h4;
     if (s < nrows) {
       const uint4 xv = *reinterpret_cast<const uint4*>(xT + sw128(1, s, 8 * c));
-      const uint32_t xw[4] = {xv.x, xv.y, xv.z, xv.w};
+      const __nv_bfloat16* xb = reinterpret_cast<const __nv_bfloat16*>(&xv);
       const float ws = w[s];
-      uint32_t hh[8], mm[8], ll[8];
+      float hh[8], mm[8], ll[8];
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
-        const float xf = bf16_bits_to_f((xw[i / 2] >> (16 * (i % 2))) & 0xFFFFu);
-        const float u = __fmul_rn(ws, xf);
-        hh[i] = bf16_rne_bits(u);
-        const float r1 = __fsub_rn(u, bf16_bits_to_f(hh[i]));
-        mm[i] = bf16_rne_bits(r1);
-        ll[i] = bf16_rne_bits(__fsub_rn(r1, bf16_bits_to_f(mm[i])));
+        const float u = __fmul_rn(ws, __bfloat162float(xb[i]));
+        hh[i] = __bfloat162float(__float2bfloat16_rn(u));
+        const float r1 = __fsub_rn(u, hh[i]);
+        mm[i] = __bfloat162float(__float2bfloat16_rn(r1));
+        ll[i] = __fsub_rn(r1, mm[i]);
       }
-      h4 = make_uint4(hh[0] | (hh[1] << 16), hh[2] | (hh[3] << 16), hh[4] | (hh[5] << 16), hh[6] | (hh[7] << 16));
-      m4 = make_uint4(mm[0] | (mm[1] << 16), mm[2] | (mm[3] << 16), mm[4] | (mm[5] << 16), mm[6] | (mm[7] << 16));
-      l4 = make_uint4(ll[0] | (ll[1] << 16), ll[2] | (ll[3] << 16), ll[4] | (ll[5] << 16), ll[6] | (ll[7] << 16));
+      h4 = make_uint4(pack_bf16x2(hh[0], hh[1]), pack_bf16x2(hh[2], hh[3]), pack_bf16x2(hh[4], hh[5]),
+                      pack_bf16x2(hh[6], hh[7]));
+      m4 = make_uint4(pack_bf16x2(mm[0], mm[1]), pack_bf16x2(mm[2], mm[3]), pack_bf16x2(mm[4], mm[5]),
+                      pack_bf16x2(mm[6], mm[7]));
+      l4 = make_uint4(pack_bf16x2(ll[0], ll[1]), pack_bf16x2(ll[2], ll[3]), pack_bf16x2(ll[4], ll[5]),
+                      pack_bf16x2(ll[6], ll[7]));
     }
     const uint32_t off = sw128(1, r, 8 * c);
     *reinterpret_cast<uint4*>(u0 + off) = h4;
@@ -252,24 +242,15 @@ template <int NC>
 __device__ __forceinline__ void m_row(const float (&g)[NC], int t, int tmax, int blk, int col0, int S_ext,
                                       const float* delta, const float* ahi, const float* alo, uint8_t* mhi,
                                       uint8_t* mlo, uint32_t mR, uint32_t trow) {
-  static_assert(NC % 8 == 0 && NC / 8 <= 32, "whole 16-byte chunks");
+  static_assert(NC % 8 == 0, "whole 16-byte chunks");
   const df at = {ahi[t], alo[t]};
   const bool row_ok = t < tmax;
-  // warp-uniform classification of every 8-column group first, so that the arithmetic below is one
-  // straight run: `live` groups hold at least one entry of some lane, `full` ones none masked
-  uint32_t live = 0, full = 0;
-#pragma unroll
-  for (int c = 0; c < NC / 8; ++c) {
-    const int s0 = 128 * blk + col0 + 8 * c;
-    if (!__all_sync(0xffffffffu, !row_ok || s0 > t || s0 >= S_ext)) live |= 1u << c;
-    if (__all_sync(0xffffffffu, row_ok && s0 + 7 <= t && s0 + 7 < S_ext)) full |= 1u << c;
-  }
 #pragma unroll
   for (int c = 0; c < NC / 8; ++c) {
     const int s0 = 128 * blk + col0 + 8 * c;   // first s of the group, a multiple of 8
     uint4 hi = make_uint4(0, 0, 0, 0), lo = hi;
-    if (live & (1u << c)) {
-      const bool fl = (full >> c) & 1u;
+    if (!__all_sync(0xffffffffu, !row_ok || s0 > t || s0 >= S_ext)) {
+      const bool full = __all_sync(0xffffffffu, row_ok && s0 + 7 <= t && s0 + 7 < S_ext);
       const float4 d0 = *reinterpret_cast<const float4*>(delta + s0), d1 = *reinterpret_cast<const float4*>(delta + s0 + 4);
       const float4 h0 = *reinterpret_cast<const float4*>(ahi + s0), h1 = *reinterpret_cast<const float4*>(ahi + s0 + 4);
       const float4 l0 = *reinterpret_cast<const float4*>(alo + s0), l1 = *reinterpret_cast<const float4*>(alo + s0 + 4);
@@ -280,7 +261,7 @@ __device__ __forceinline__ void m_row(const float (&g)[NC], int t, int tmax, int
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
         const float m = __fmul_rn(__fmul_rn(g[8 * c + i], dv[i]), __expf(df_diff(at, df{hv[i], lv[i]})));
-        v[i] = (fl || (row_ok && s0 + i <= t && s0 + i < S_ext)) ? m : 0.f;
+        v[i] = (full || (row_ok && s0 + i <= t && s0 + i < S_ext)) ? m : 0.f;
       }
       split8(v, hi, lo);
     }
