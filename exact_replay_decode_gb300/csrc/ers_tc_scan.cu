@@ -204,11 +204,15 @@ __device__ __forceinline__ void build_m(const ScanArena& ar, uint8_t* mt, uint32
   const int row = 32 * q + lane;
   const int width = ge.S_ext - 128 * blk < 128 ? ge.S_ext - 128 * blk : 128;
   const int tlim = nrows < ge.t0 + ge.TT ? nrows : ge.t0 + ge.TT;
-  if (kMC * sl < width) {
-    float g[kMC];
-    tmem_ld32(taddr(tb, 32 * q, gcol + kMC * sl), g);
-    m_row<kMC>(g, ge.t0 + row, tlim, blk, kMC * sl, ge.S_ext, ar.hd->delta, ar.hd->ahi, ar.hd->alo, mt, mt + 32768,
-               128, row);
+#pragma unroll 1
+  for (int half = 0; half < kMC / 16; ++half) {   // 16 columns at a time
+    const int col0 = kMC * sl + 16 * half;
+    if (col0 < width) {
+      float g[16];
+      tmem_ld16(taddr(tb, 32 * q, gcol + col0), g);
+      m_row<16>(g, ge.t0 + row, tlim, blk, col0, ge.S_ext, ar.hd->delta, ar.hd->ahi, ar.hd->alo, mt, mt + 32768, 128,
+                row);
+    }
   }
 }
 

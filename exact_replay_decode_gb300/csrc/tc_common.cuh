@@ -107,21 +107,29 @@ __device__ __forceinline__ void st_release(int32_t* p, int32_t v) {
   asm volatile("st.release.gpu.global.b32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
 
-// Waits until *flag != 0 and returns its value (read with acquire semantics).  Gives up after
+__device__ __forceinline__ int32_t ld_relaxed(const int32_t* p) {
+  int32_t v;
+  asm volatile("ld.relaxed.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+// Waits until *flag != 0 and returns its value, with acquire semantics for what the flag's writer
+// released: the flag is polled with relaxed loads and acquired once it is seen set (polling with
+// acquire loads would order every poll against the SM's other memory traffic).  Gives up after
 // limit_ns of wall clock, reporting ERS_ETIMEOUT, and returns 0.
 __device__ __forceinline__ int32_t flag_wait(const int32_t* flag, int32_t* status, uint64_t limit_ns = kWaitLimitNs) {
-  int32_t v = ld_acquire(flag);
-  if (v != 0) return v;
-  const uint64_t t0 = globaltimer();
-  for (;;) {
-    __nanosleep(32);
-    v = ld_acquire(flag);
-    if (v != 0) return v;
-    if (globaltimer() - t0 > limit_ns) {
-      if (status != nullptr) atomicCAS(status, 0, ERS_ETIMEOUT);
-      return 0;
+  if (ld_relaxed(flag) == 0) {
+    const uint64_t t0 = globaltimer();
+    for (;;) {
+      __nanosleep(100);
+      if (ld_relaxed(flag) != 0) break;
+      if (globaltimer() - t0 > limit_ns) {
+        if (status != nullptr) atomicCAS(status, 0, ERS_ETIMEOUT);
+        return 0;
+      }
     }
   }
+  return ld_acquire(flag);
 }
 
 // ---- TMA (tensor-map bulk copies, this GPU's own memory, no multicast) -----------------------------
