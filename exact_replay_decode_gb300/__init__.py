@@ -11,7 +11,7 @@ __version__ = "0.1.0"
 _OPS = ("LayerParams", "ReplayCache", "Status", "ssd_scan_fwd", "ssd_scan_fwd_static", "STATIC_SCRATCH_BYTES",
         "chunked_prefill", "replay_decode", "refresh",
         "spec_verify", "commit", "ssu_update", "conv1d_fwd", "conv1d_update", "GdnCache", "gdn_verify",
-        "gdn_commit", "gdn_refresh", "selftest_bounded_wait")
+        "gdn_commit", "gdn_refresh", "selftest_bounded_wait", "spec_verify_exact", "commit_exact")
 
 
 def __getattr__(name):

@@ -38,6 +38,7 @@ EXPORTS = (
     "ers_chunked_prefill_workspace_size", "ers_chunked_prefill", "ers_replay_decode", "ers_refresh",
     "ers_spec_verify", "ers_commit", "ers_ssu_update", "ers_ssd_scan_fwd_static", "ers_conv1d_fwd",
     "ers_conv1d_update", "ers_gdn_verify", "ers_gdn_commit", "ers_gdn_refresh", "ers_selftest_bounded_wait",
+    "ers_spec_verify_exact_workspace_size", "ers_spec_verify_exact", "ers_commit_exact",
 )
 
 
@@ -110,6 +111,9 @@ _SIGS = {
     "ers_refresh": ([_DIMS, _PRM, _CACHE, _I32, _P, _U32, _I32, _P, _P], _I32),
     "ers_spec_verify": ([_DIMS, _PRM, _CACHE, _I32, _P, _I32, _P, _P, _P, _P, _U32, _P, _P, _P], _I32),
     "ers_commit": ([_DIMS, _CACHE, _I32, _P, _P, _I32, _U32, _P, _P], _I32),
+    "ers_spec_verify_exact_workspace_size": ([_DIMS, _I32], _SZ),
+    "ers_spec_verify_exact": ([_DIMS, _PRM, _CACHE, _I32, _P, _I32, _P, _P, _P, _P, _P, _P, _SZ, _P, _P], _I32),
+    "ers_commit_exact": ([_DIMS, _PRM, _CACHE, _I32, _P, _P, _I32, _P, _P, _P, _P, _P, _SZ, _P, _P], _I32),
     "ers_ssu_update": ([_DIMS, _PRM, _P, _I32, _I32, _P, _P, _P, _P, _P, _P, _P, _P], _I32),
     "ers_conv1d_fwd": ([ctypes.POINTER(ConvDims), _I32, _I64, _I32, _P, _P, _P, _P, _P, _I32, _P, _I32, _P, _P, _P],
                        _I32),

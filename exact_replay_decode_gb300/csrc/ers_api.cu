@@ -408,6 +408,150 @@ ers_status ers_commit(const ers_dims* dims, const ers_cache* cache, int32_t nseq
   return finish(ers::launch_commit(a, (cudaStream_t)stream));
 }
 
+}  // extern "C"
+
+// ---- exact-mode speculative decode -----------------------------------------------------------
+namespace {
+struct ExactSpecWs {
+  size_t st, bx, bdt, bB, bC, pos, x1, dt1, B1, C1, y1, total;
+};
+ExactSpecWs exact_spec_ws(const ers_dims* d, int32_t nseq) {
+  ExactSpecWs w;
+  const size_t S = (size_t)(nseq > 0 ? nseq : 0), es = d->io_dtype == ERS_DTYPE_BF16 ? 2 : 4;
+  const size_t HP = (size_t)d->nheads * d->headdim, GN = (size_t)d->ngroups * d->dstate, Q = (size_t)d->chunk;
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    const size_t o = off;
+    off += ers::align256(bytes);
+    return o;
+  };
+  w.st = take(S * HP * d->dstate * sizeof(float));
+  w.bx = take(S * Q * HP * es);
+  w.bdt = take(S * Q * d->nheads * sizeof(float));
+  w.bB = take(S * Q * GN * es);
+  w.bC = take(S * Q * GN * es);
+  w.pos = take(S * sizeof(int32_t));
+  w.x1 = take(S * HP * es);
+  w.dt1 = take(S * d->nheads * sizeof(float));
+  w.B1 = take(S * GN * es);
+  w.C1 = take(S * GN * es);
+  w.y1 = take(S * HP * es);
+  w.total = off;
+  return w;
+}
+
+ers_status check_exact_spec(const ers_dims* dims, const ers_params* prm, const ers_cache* cache, int32_t nseq,
+                            const int32_t* slot, int32_t T, const void* x, const float* dt, const void* B,
+                            const void* C, int32_t* dev_status) {
+  ERS_TRY(check_dims(dims));
+  ERS_TRY(check_params(prm));
+  ERS_TRY(check_cache(cache, false));
+  ERS_TRY(check_pages(dims, cache));
+  if (cache->anchor_dtype != ERS_ANCHOR_F32 || cache->state == nullptr) return ERS_EUNSUPPORTED;
+  if (has_nvfp4_copy(cache)) return ERS_EUNSUPPORTED;   // NVFP4 copies are kept in ReplaySSM mode only
+  if (has_narrow_copy(cache) && !narrow_read_shape(dims)) return ERS_EUNSUPPORTED;
+  if (nseq < 0 || T < 1 || T > dims->chunk) return ERS_EINVAL;
+  if (nseq > 0 && slot == nullptr && nseq > cache->nslots) return ERS_EINVAL;
+  ERS_TRY(check_ptr(slot, false));
+  ERS_TRY(check_tokens(x, dt, B, C, nseq > 0));
+  ERS_TRY(check_ptr(dev_status, false));
+  return ERS_OK;
+}
+}  // namespace
+
+extern "C" {
+
+size_t ers_spec_verify_exact_workspace_size(const ers_dims* dims, int32_t nseq) {
+  if (check_dims(dims) != ERS_OK || nseq < 0) return 0;
+  return exact_spec_ws(dims, nseq).total;
+}
+
+ers_status ers_spec_verify_exact(const ers_dims* dims, const ers_params* prm, const ers_cache* cache, int32_t nseq,
+                                 const int32_t* slot, int32_t T, const void* x, const float* dt, const void* B,
+                                 const void* C, void* y, void* workspace, size_t workspace_bytes, ers_stream_t stream,
+                                 int32_t* dev_status) {
+  ERS_TRY(check_exact_spec(dims, prm, cache, nseq, slot, T, x, dt, B, C, dev_status));
+  if (nseq == 0) return ERS_OK;
+  ERS_TRY(check_ptr(y, true));
+  const ExactSpecWs w = exact_spec_ws(dims, nseq);
+  if (workspace == nullptr || workspace_bytes < w.total) return ERS_EWORKSPACE;
+  ERS_TRY(check_ptr(workspace, true));
+  const cudaStream_t s = (cudaStream_t)stream;
+  char* ws = (char*)workspace;
+  LaunchArgs a = base_args(dims, prm);
+  set_cache(a, cache);
+  a.slot = slot;
+  a.nseq = nseq;
+  a.T = T;
+  a.status = dev_status;
+  cudaError_t e = ers::launch_spec_snapshot(a, (float*)(ws + w.st), ws + w.bx, (float*)(ws + w.bdt), ws + w.bB,
+                                            ws + w.bC, (int32_t*)(ws + w.pos), s);
+  if (e != cudaSuccess) return finish(e);
+  // the shadow cache: slot i of the workspace, contiguous buffers, exact-mode decode with refresh
+  LaunchArgs d = base_args(dims, prm);
+  d.state = (float*)(ws + w.st);
+  d.bx = ws + w.bx;
+  d.bdt = (float*)(ws + w.bdt);
+  d.bB = ws + w.bB;
+  d.bC = ws + w.bC;
+  d.pos = (int32_t*)(ws + w.pos);
+  d.nslots = nseq;
+  d.page_rows = 1;
+  d.nseq = nseq;
+  d.flags = ERS_FLAG_FUSE_REFRESH;
+  d.x = ws + w.x1;
+  d.dt = (float*)(ws + w.dt1);
+  d.B = ws + w.B1;
+  d.C = ws + w.C1;
+  d.y = ws + w.y1;
+  d.status = dev_status;
+  const bool tc = ers::tc_supported(d.io, d.P, d.N, d.Q);
+  for (int j = 0; j < T; ++j) {
+    if ((e = ers::launch_spec_rows(a, j, 0, x, dt, B, C, (void*)d.x, (float*)d.dt, (void*)d.B, (void*)d.C, nullptr,
+                                   nullptr, s)) != cudaSuccess)
+      return finish(e);
+    if ((e = tc ? ers::tc_decode(d, s) : ers::fma_decode(d, s)) != cudaSuccess) return finish(e);
+    if ((e = ers::launch_spec_rows(a, j, 1, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, y,
+                                   d.y, s)) != cudaSuccess)
+      return finish(e);
+  }
+  return ERS_OK;
+}
+
+ers_status ers_commit_exact(const ers_dims* dims, const ers_params* prm, const ers_cache* cache, int32_t nseq,
+                            const int32_t* slot, const int32_t* accepted, int32_t T, const void* x, const float* dt,
+                            const void* B, const void* C, void* workspace, size_t workspace_bytes, ers_stream_t stream,
+                            int32_t* dev_status) {
+  ERS_TRY(check_exact_spec(dims, prm, cache, nseq, slot, T, x, dt, B, C, dev_status));
+  if (nseq == 0) return ERS_OK;
+  ERS_TRY(check_ptr(accepted, true));
+  if (workspace == nullptr || workspace_bytes < ers::align256((size_t)nseq * sizeof(int32_t))) return ERS_EWORKSPACE;
+  ERS_TRY(check_ptr(workspace, true));
+  const cudaStream_t s = (cudaStream_t)stream;
+  LaunchArgs a = base_args(dims, prm);
+  set_cache(a, cache);
+  a.slot = slot;
+  a.nseq = nseq;
+  a.T = T;
+  a.accepted = accepted;
+  a.x = x; a.dt = dt; a.B = B; a.C = C;
+  a.status = dev_status;
+  int32_t* old_pos = (int32_t*)workspace;
+  cudaError_t e = ers::launch_commit_exact(a, 0, old_pos, s);
+  if (e != cudaSuccess) return finish(e);
+  LaunchArgs r = a;   // the chunks the accepted drafts filled: the exact-mode refresh (pos == Q)
+  r.flags = 0;
+  r.x = r.dt = nullptr;
+  r.B = r.C = nullptr;
+  if ((e = ers::tc_supported(r.io, r.P, r.N, r.Q) ? ers::tc_refresh(r, s) : ers::fma_refresh(r, s)) != cudaSuccess)
+    return finish(e);
+  return finish(ers::launch_commit_exact(a, 1, old_pos, s));
+}
+
+}  // extern "C"
+
+extern "C" {
+
 ers_status ers_ssu_update(const ers_dims* dims, const ers_params* prm, float* state, int32_t nslots,
                           int32_t nseq, const int32_t* slot, const void* x, const float* dt, const void* B,
                           const void* C, void* y, ers_stream_t stream, int32_t* dev_status) {

@@ -623,6 +623,157 @@ cudaError_t fma_verify(const LaunchArgs& a, cudaStream_t s) {
 #undef ERS_ARGS
 }
 
+// ---- exact-mode speculative decode: shadow copies and draft rows ------------------------------
+// Copies a row of `n` io elements; bf16 and fp32 rows are moved as 16-bit / 32-bit words.
+__device__ __forceinline__ void copy_elems(void* dst, const void* src, int n, int es, int lane, int nl) {
+  if (es == 2) {
+    for (int k = lane; k < n; k += nl) ((uint16_t*)dst)[k] = ((const uint16_t*)src)[k];
+  } else {
+    for (int k = lane; k < n; k += nl) ((uint32_t*)dst)[k] = ((const uint32_t*)src)[k];
+  }
+}
+
+// Shadow of sequence i's slot (blockIdx.y = i, blockIdx.x = head): its fp32 checkpoint head, its
+// buffered rows [0, pos) (x, dt of the head; B, C of group h when h < G) in the contiguous layout,
+// its position.  `a` describes the real cache; sh_* the shadow (slot i, Q rows per slot).
+__global__ void k_spec_snapshot(LaunchArgs a, float* sh_state, void* sh_bx, float* sh_bdt, void* sh_bB, void* sh_bC,
+                                int32_t* sh_pos) {
+  const int i = blockIdx.y, h = blockIdx.x;
+  const int slot = a.slot != nullptr ? a.slot[i] : i;
+  if (slot < 0 || slot >= a.nslots) {
+    if (threadIdx.x == 0 && h == 0) {
+      report(a.status, ERS_ESLOT);
+      sh_pos[i] = -1;   // the shadow decode reports it again and touches nothing
+    }
+    return;
+  }
+  const int p = a.pos[slot];
+  if (p < 0 || p >= a.Q) {
+    if (threadIdx.x == 0 && h == 0) {
+      report(a.status, ERS_EALIGN);
+      sh_pos[i] = -1;
+    }
+    return;
+  }
+  const size_t hs = (size_t)a.P * a.N;
+  const float4* src = reinterpret_cast<const float4*>(a.state + ((size_t)slot * a.H + h) * hs);
+  float4* dst = reinterpret_cast<float4*>(sh_state + ((size_t)i * a.H + h) * hs);
+  for (size_t k = threadIdx.x; k < hs / 4; k += blockDim.x) dst[k] = src[k];
+  const int es = a.io == ERS_DTYPE_BF16 ? 2 : 4;
+  const long long HP = (long long)a.H * a.P, GN = (long long)a.G * a.N;
+  for (int r = 0; r < p; ++r) {
+    const long long br = buf_row(a, slot, r), sr = (long long)i * a.Q + r;
+    copy_elems((char*)sh_bx + (sr * HP + (long long)h * a.P) * es, (const char*)a.bx + (br * HP + (long long)h * a.P) * es,
+               a.P, es, threadIdx.x, blockDim.x);
+    if (threadIdx.x == 0) sh_bdt[sr * a.H + h] = a.bdt[br * a.H + h];
+    if (h < a.G) {
+      copy_elems((char*)sh_bB + (sr * GN + (long long)h * a.N) * es, (const char*)a.bB + (br * GN + (long long)h * a.N) * es,
+                 a.N, es, threadIdx.x, blockDim.x);
+      copy_elems((char*)sh_bC + (sr * GN + (long long)h * a.N) * es, (const char*)a.bC + (br * GN + (long long)h * a.N) * es,
+                 a.N, es, threadIdx.x, blockDim.x);
+    }
+  }
+  if (threadIdx.x == 0 && h == 0) sh_pos[i] = p;
+}
+
+// Draft j of every sequence into contiguous one-token inputs (dir = 0), or a one-token output back
+// into draft j's output row (dir = 1).  blockIdx.x = sequence.
+__global__ void k_spec_draft_rows(LaunchArgs a, int j, int dir, const void* x, const float* dt, const void* B,
+                                  const void* C, void* x1, float* dt1, void* B1, void* C1, void* y, const void* y1) {
+  const int i = blockIdx.x;
+  const int es = a.io == ERS_DTYPE_BF16 ? 2 : 4;
+  const long long HP = (long long)a.H * a.P, GN = (long long)a.G * a.N;
+  const long long row = (long long)i * a.T + j;
+  if (dir == 0) {
+    copy_elems((char*)x1 + i * HP * es, (const char*)x + row * HP * es, (int)HP, es, threadIdx.x, blockDim.x);
+    for (int k = threadIdx.x; k < a.H; k += blockDim.x) dt1[(long long)i * a.H + k] = dt[row * a.H + k];
+    copy_elems((char*)B1 + i * GN * es, (const char*)B + row * GN * es, (int)GN, es, threadIdx.x, blockDim.x);
+    copy_elems((char*)C1 + i * GN * es, (const char*)C + row * GN * es, (int)GN, es, threadIdx.x, blockDim.x);
+  } else {
+    copy_elems((char*)y + row * HP * es, (const char*)y1 + i * HP * es, (int)HP, es, threadIdx.x, blockDim.x);
+  }
+}
+
+// Commit, part 1: sequence i (blockIdx.x) appends its accepted drafts [0, a) that fit the chunk
+// to buffer rows [p, min(Q, p + a)) and keeps p in `old_pos`; a chunk that fills is marked for the
+// refresh with pos = Q, otherwise pos = p + a.
+__global__ void k_commit_exact_fill(LaunchArgs a, int32_t* old_pos) {
+  const int i = blockIdx.x;
+  const int slot = a.slot != nullptr ? a.slot[i] : i;
+  old_pos[i] = -1;
+  if (slot < 0 || slot >= a.nslots) {
+    if (threadIdx.x == 0) report(a.status, ERS_ESLOT);
+    return;
+  }
+  const int p = a.pos[slot], acc = a.accepted[i];
+  if (p < 0 || p >= a.Q) {
+    if (threadIdx.x == 0) report(a.status, ERS_EALIGN);
+    return;
+  }
+  if (acc < 0 || acc > a.T) {
+    if (threadIdx.x == 0) report(a.status, ERS_ECOMMIT);
+    return;
+  }
+  const int es = a.io == ERS_DTYPE_BF16 ? 2 : 4;
+  const long long HP = (long long)a.H * a.P, GN = (long long)a.G * a.N;
+  const int end = p + acc < a.Q ? p + acc : a.Q;
+  for (int r = p; r < end; ++r) {
+    const long long br = buf_row(a, slot, r), row = (long long)i * a.T + (r - p);
+    copy_elems((char*)a.bx + br * HP * es, (const char*)a.x + row * HP * es, (int)HP, es, threadIdx.x, blockDim.x);
+    for (int k = threadIdx.x; k < a.H; k += blockDim.x) a.bdt[br * a.H + k] = a.dt[row * a.H + k];
+    copy_elems((char*)a.bB + br * GN * es, (const char*)a.B + row * GN * es, (int)GN, es, threadIdx.x, blockDim.x);
+    copy_elems((char*)a.bC + br * GN * es, (const char*)a.C + row * GN * es, (int)GN, es, threadIdx.x, blockDim.x);
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    old_pos[i] = p;
+    a.pos[slot] = p + acc >= a.Q ? a.Q : p + acc;
+  }
+}
+
+// Commit, part 3 (after the refresh of the filled chunks): the accepted drafts past the chunk
+// boundary become buffer rows [0, p + a - Q) and pos = p + a - Q.
+__global__ void k_commit_exact_tail(LaunchArgs a, const int32_t* old_pos) {
+  const int i = blockIdx.x;
+  const int p = old_pos[i];
+  if (p < 0) return;
+  const int slot = a.slot != nullptr ? a.slot[i] : i;
+  const int acc = a.accepted[i];
+  if (p + acc < a.Q) return;
+  const int es = a.io == ERS_DTYPE_BF16 ? 2 : 4;
+  const long long HP = (long long)a.H * a.P, GN = (long long)a.G * a.N;
+  const int n2 = p + acc - a.Q;
+  for (int r = 0; r < n2; ++r) {
+    const long long br = buf_row(a, slot, r), row = (long long)i * a.T + (a.Q - p + r);
+    copy_elems((char*)a.bx + br * HP * es, (const char*)a.x + row * HP * es, (int)HP, es, threadIdx.x, blockDim.x);
+    for (int k = threadIdx.x; k < a.H; k += blockDim.x) a.bdt[br * a.H + k] = a.dt[row * a.H + k];
+    copy_elems((char*)a.bB + br * GN * es, (const char*)a.B + row * GN * es, (int)GN, es, threadIdx.x, blockDim.x);
+    copy_elems((char*)a.bC + br * GN * es, (const char*)a.C + row * GN * es, (int)GN, es, threadIdx.x, blockDim.x);
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) a.pos[slot] = n2;
+}
+
+cudaError_t launch_spec_snapshot(const LaunchArgs& a, float* st, void* bx, float* bdt, void* bB, void* bC, int32_t* pos,
+                                 cudaStream_t s) {
+  if (a.nseq > 0) k_spec_snapshot<<<dim3(a.H, a.nseq), kThreads, 0, s>>>(a, st, bx, bdt, bB, bC, pos);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_spec_rows(const LaunchArgs& a, int j, int dir, const void* x, const float* dt, const void* B,
+                             const void* C, void* x1, float* dt1, void* B1, void* C1, void* y, const void* y1,
+                             cudaStream_t s) {
+  if (a.nseq > 0) k_spec_draft_rows<<<a.nseq, kThreads, 0, s>>>(a, j, dir, x, dt, B, C, x1, dt1, B1, C1, y, y1);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_commit_exact(const LaunchArgs& a, int part, int32_t* old_pos, cudaStream_t s) {
+  if (a.nseq <= 0) return cudaSuccess;
+  if (part == 0) k_commit_exact_fill<<<a.nseq, kThreads, 0, s>>>(a, old_pos);
+  else k_commit_exact_tail<<<a.nseq, kThreads, 0, s>>>(a, old_pos);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_setpos(const LaunchArgs& a, int kind, cudaStream_t s) {
   if (a.nseq > 0) k_setpos<<<(a.nseq + 255) / 256, 256, 0, s>>>(a, kind);
   return cudaGetLastError();

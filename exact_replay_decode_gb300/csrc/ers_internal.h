@@ -90,6 +90,13 @@ cudaError_t heads_verify(const LaunchArgs& a, cudaStream_t s);
 cudaError_t launch_setpos(const LaunchArgs& a, int kind, cudaStream_t s);  // kind: 0 decode, 1 refresh
 cudaError_t launch_commit(const LaunchArgs& a, cudaStream_t s);
 cudaError_t launch_tail(const LaunchArgs& a, cudaStream_t s);
+// exact-mode speculative decode: shadow snapshot of slots, draft rows in / outputs out, commit parts
+cudaError_t launch_spec_snapshot(const LaunchArgs& a, float* st, void* bx, float* bdt, void* bB, void* bC, int32_t* pos,
+                                 cudaStream_t s);
+cudaError_t launch_spec_rows(const LaunchArgs& a, int j, int dir, const void* x, const float* dt, const void* B,
+                             const void* C, void* x1, float* dt1, void* B1, void* C1, void* y, const void* y1,
+                             cudaStream_t s);
+cudaError_t launch_commit_exact(const LaunchArgs& a, int part, int32_t* old_pos, cudaStream_t s);
 
 // tensor-core engine (bf16 io, P = 64, N = 128, Q % 16 == 0, Q >= kTcMinChunk), ers_tc.cu.  Each
 // configuration runs every path on ONE engine (bitwise identity needs identical arithmetic):

@@ -404,6 +404,48 @@ def commit(cache: ReplayCache, accepted: torch.Tensor, T: int, slot: Optional[to
     _finish(code, "ers_commit", st, check)
 
 
+def _exact_ws(cache: ReplayCache, S: int, workspace: Optional[torch.Tensor], device) -> torch.Tensor:
+    need = _abi.lib().ers_spec_verify_exact_workspace_size(ctypes.byref(cache.dims), S)
+    if workspace is None or workspace.numel() < need:
+        workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=device)
+    return workspace
+
+
+def spec_verify_exact(cache: ReplayCache, params: LayerParams, x, dt, B, C, slot: Optional[torch.Tensor] = None,
+                      status: Optional[Status] = None, check: bool = True, stream=None,
+                      out: Optional[torch.Tensor] = None, workspace: Optional[torch.Tensor] = None) -> torch.Tensor:
+    """Exact-mode speculative verify of T drafts per sequence that keeps the chunk grid
+    (ers_spec_verify_exact): x [S,T,H,P], dt [S,T,H], B/C [S,T,G,N] -> y [S,T,H,P]; the cache is
+    not changed."""
+    S, T = x.shape[0], x.shape[1]
+    _tok_checks(cache, x, dt, B, C, (S, T))
+    y = torch.empty_like(x) if out is None else out
+    ws = _exact_ws(cache, S, workspace, x.device)
+    st = status if status is not None else (Status(x.device) if check else None)
+    code = _abi.lib().ers_spec_verify_exact(ctypes.byref(cache.dims), ctypes.byref(params._c()),
+                                            ctypes.byref(cache._c()), S, _slot_arg(slot, S), T, x.data_ptr(),
+                                            dt.data_ptr(), B.data_ptr(), C.data_ptr(), y.data_ptr(), ws.data_ptr(),
+                                            ws.numel(), _stream(stream), _ptr(st.t) if st else None)
+    _finish(code, "ers_spec_verify_exact", st, check)
+    return y
+
+
+def commit_exact(cache: ReplayCache, params: LayerParams, accepted: torch.Tensor, x, dt, B, C,
+                 slot: Optional[torch.Tensor] = None, status: Optional[Status] = None, check: bool = True,
+                 stream=None, workspace: Optional[torch.Tensor] = None) -> None:
+    """Commit the accepted drafts of an exact-mode verify (ers_commit_exact): the same x, dt, B, C."""
+    S, T = x.shape[0], x.shape[1]
+    _tok_checks(cache, x, dt, B, C, (S, T))
+    _need(accepted, torch.int32, "accepted", (S,))
+    ws = workspace if workspace is not None else torch.empty(max(256, 4 * S), dtype=torch.uint8, device=x.device)
+    st = status if status is not None else (Status(x.device) if check else None)
+    code = _abi.lib().ers_commit_exact(ctypes.byref(cache.dims), ctypes.byref(params._c()), ctypes.byref(cache._c()),
+                                       S, _slot_arg(slot, S), accepted.data_ptr(), T, x.data_ptr(), dt.data_ptr(),
+                                       B.data_ptr(), C.data_ptr(), ws.data_ptr(), ws.numel(), _stream(stream),
+                                       _ptr(st.t) if st else None)
+    _finish(code, "ers_commit_exact", st, check)
+
+
 def ssu_update(state: torch.Tensor, params: LayerParams, x, dt, B, C, slot: Optional[torch.Tensor] = None,
                status: Optional[Status] = None, check: bool = True, stream=None,
                out: Optional[torch.Tensor] = None) -> torch.Tensor:

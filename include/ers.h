@@ -315,6 +315,41 @@ ERS_API ers_status ers_commit(const ers_dims* dims, const ers_cache* cache, int3
                       int32_t* dev_status);
 
 /* ---------------------------------------------------------------------------------------------
+ * Exact-mode speculative verify and commit: speculation that keeps the chunk grid.  RFC section 6
+ * (the phase-1 prototype's speculative decoding on the exact-replay path) with ReplaySSM "Motivation
+ * and method" (outputs of drafts from the checkpoint and the buffered inputs; rejected drafts never
+ * enter the state).  In exact mode the checkpoint sits on the chunk grid, so a draft past the end of
+ * the current chunk gets the output exact-replay decode would give it: from the boundary state that
+ * the full chunk (buffered rows, then the drafts before the boundary) folds into.
+ *
+ * ers_spec_verify_exact: T drafts per sequence, 1 <= T <= Q: x [nseq, T, H, P], dt [nseq, T, H] raw,
+ *   B/C [nseq, T, G, N]; y [nseq, T, H, P] (out).  Draft j's output is, bit for bit, the output
+ *   ers_replay_decode (exact mode, ERS_FLAG_FUSE_REFRESH) gives draft j after drafts 0 .. j-1 were
+ *   decoded, crossing the chunk boundary where they reach it.  The cache is not changed: the call
+ *   copies the slots' checkpoints, buffered rows and positions into `workspace`
+ *   (ers_spec_verify_exact_workspace_size(dims, nseq) bytes, about an fp32 state and a buffer per
+ *   sequence) and decodes the drafts there one at a time (T decode launches and their row copies).
+ *   Requires an fp32 checkpoint (ERS_ANCHOR_F32; read copies, if any, are neither read nor written)
+ *   and 0 <= pos < Q.
+ * ers_commit_exact: after a verify, the first accepted[i] (0 <= accepted[i] <= T, device int32 [nseq])
+ *   drafts of sequence i, passed again as the same x, dt, B, C, enter the cache: those that fit the
+ *   current chunk are appended to the buffer; if they fill it, the chunk folds into the checkpoint by
+ *   the exact-mode refresh (the arithmetic of decode's fused refresh; a read copy is recast with it)
+ *   and the drafts past the boundary become the new buffer; pos = (pos + accepted) mod Q.  The state
+ *   afterwards is bit for bit the one decoding the accepted drafts would leave.  workspace: at least
+ *   nseq * 4 bytes rounded up to 256 (the verify's workspace serves).
+ * Device errors: ERS_EALIGN (pos outside [0, Q)), ERS_ECOMMIT, ERS_ESLOT. */
+ERS_API size_t ers_spec_verify_exact_workspace_size(const ers_dims* dims, int32_t nseq);
+ERS_API ers_status ers_spec_verify_exact(const ers_dims* dims, const ers_params* prm, const ers_cache* cache,
+                                         int32_t nseq, const int32_t* slot, int32_t T, const void* x, const float* dt,
+                                         const void* B, const void* C, void* y, void* workspace,
+                                         size_t workspace_bytes, ers_stream_t stream, int32_t* dev_status);
+ERS_API ers_status ers_commit_exact(const ers_dims* dims, const ers_params* prm, const ers_cache* cache, int32_t nseq,
+                                    const int32_t* slot, const int32_t* accepted, int32_t T, const void* x,
+                                    const float* dt, const void* B, const void* C, void* workspace,
+                                    size_t workspace_bytes, ers_stream_t stream, int32_t* dev_status);
+
+/* ---------------------------------------------------------------------------------------------
  * Per-token state-writeback update (the recurrent "selective state update" the RFC's section 1
  * contrasts with the chunked scan; the comparison point for replay decode).
  *   state [nslots, H, P, N] fp32, updated in place for slot[i] (slot NULL = identity)

@@ -268,3 +268,27 @@ def test_bounded_wait_selftest_validation(lib):
     assert lib.ers_selftest_bounded_wait(1000, None, None) == 1
     assert lib.ers_selftest_bounded_wait(0, None, ctypes.c_void_p(16)) == 1
     assert lib.ers_selftest_bounded_wait(20_000_000_000, None, ctypes.c_void_p(16)) == 1
+
+
+def test_exact_speculation_validation(lib):
+    from exact_replay_decode_gb300 import _abi
+    d = _abi.Dims(8, 2, 64, 128, 16, _abi.DTYPE_BF16)
+    assert lib.ers_spec_verify_exact_workspace_size(ctypes.byref(d), 4) > 4 * 8 * 64 * 128 * 4
+    p16 = ctypes.c_void_p(16)
+    prm = _abi.Params(p16, p16, p16)
+    cache = _abi.Cache()
+    cache.state = cache.buf_x = cache.buf_B = cache.buf_C = cache.buf_dt = cache.pos = 16
+    cache.nslots = 4
+    args = (4, None, 4, p16, p16, p16, p16)
+    # T outside [1, Q], a missing workspace, a workspace too small: rejected before any launch
+    assert lib.ers_spec_verify_exact(ctypes.byref(d), ctypes.byref(prm), ctypes.byref(cache), 4, None, 0, p16, p16,
+                                     p16, p16, p16, p16, 1 << 30, None, None) == 1
+    assert lib.ers_spec_verify_exact(ctypes.byref(d), ctypes.byref(prm), ctypes.byref(cache), *args, p16, None, 0,
+                                     None, None) == 10
+    assert lib.ers_spec_verify_exact(ctypes.byref(d), ctypes.byref(prm), ctypes.byref(cache), *args, p16, p16, 256,
+                                     None, None) == 10
+    assert lib.ers_commit_exact(ctypes.byref(d), ctypes.byref(prm), ctypes.byref(cache), 4, None, p16, 4, p16, p16,
+                                p16, p16, p16, 8, None, None) == 10
+    cache.anchor_dtype = 1   # fp16 anchors: exact mode keeps an fp32 checkpoint
+    assert lib.ers_spec_verify_exact(ctypes.byref(d), ctypes.byref(prm), ctypes.byref(cache), *args, p16, p16,
+                                     1 << 30, None, None) == 12
