@@ -308,6 +308,8 @@ ers_status ers_replay_decode(const ers_dims* dims, const ers_params* prm, const 
   a.flags = flags;
   a.y = y;
   a.status = dev_status;
+  if (rssm && ers::rssm_tc_supported(a.io, a.P, a.N, a.Q, a.H, a.G))   // decode with the fused flush
+    return finish(ers::rssm_tc(a, 1, true, (cudaStream_t)stream));
   const bool tc = ers::tc_supported(a.io, a.P, a.N, a.Q);
   if (rssm && (flags & ERS_FLAG_FUSE_REFRESH) && (tc || !ers::heads_decode_supported(a.P, a.N, a.Q))) {
     // engines without the fused flush: the flush rule for one token (ers_refresh with T = 1), then
@@ -365,7 +367,9 @@ ers_status ers_spec_verify(const ers_dims* dims, const ers_params* prm, const er
   ERS_TRY(check_tokens(x, dt, B, C, true));
   ERS_TRY(check_ptr(y, true));
   ERS_TRY(check_ptr(dev_status, false));
-  if ((has_narrow_copy(cache) || f16_anchor(cache)) &&
+  const bool rssm_tc = ers::rssm_tc_supported(dims->io_dtype, dims->headdim, dims->dstate, dims->chunk, dims->nheads,
+                                              dims->ngroups);
+  if ((has_narrow_copy(cache) || f16_anchor(cache)) && !rssm_tc &&
       !(narrow_read_shape(dims) && ers::heads_verify_supported(dims->headdim, dims->dstate, dims->chunk, T,
                                                                dims->nheads, dims->ngroups)))
     return ERS_EUNSUPPORTED;
@@ -379,6 +383,7 @@ ers_status ers_spec_verify(const ers_dims* dims, const ers_params* prm, const er
   a.flags = flags;
   a.y = y;
   a.status = dev_status;
+  if (rssm_tc) return finish(ers::rssm_tc(a, T, false, (cudaStream_t)stream));
   if (ers::tc_supported(a.io, a.P, a.N, a.Q)) return finish(ers::tc_verify(a, (cudaStream_t)stream));
   return finish(ers::fma_verify(a, (cudaStream_t)stream));
 }

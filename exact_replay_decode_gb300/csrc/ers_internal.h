@@ -86,6 +86,12 @@ cudaError_t heads_refresh(const LaunchArgs& a, cudaStream_t s);
 bool heads_verify_supported(int P, int N, int Q, int T, int H, int G);
 cudaError_t heads_verify(const LaunchArgs& a, cudaStream_t s);
 
+// ReplaySSM decode (T = 1, position advance, fused flush) and verify of T <= L drafts with the read
+// copy's products on the tensor core (bf16 io, P = 64, N = 128, L <= 16, H/G <= 8), ers_rssm_tc.cu.
+// Both calls run the same kernel, so verify outputs keep decode's bits.
+bool rssm_tc_supported(int io, int P, int N, int Q, int H, int G);
+cudaError_t rssm_tc(const LaunchArgs& a, int T, bool decode, cudaStream_t s);
+
 // pointer-only kernels, ers_fma.cu
 cudaError_t launch_setpos(const LaunchArgs& a, int kind, cudaStream_t s);  // kind: 0 decode, 1 refresh
 cudaError_t launch_commit(const LaunchArgs& a, cudaStream_t s);

@@ -30,6 +30,7 @@
 #include "ers_common.cuh"
 #include "ers_internal.h"
 #include "tc_engine.cuh"
+#include "tma_host.h"
 
 namespace ers {
 
@@ -597,29 +598,9 @@ __global__ void __launch_bounds__(kScanThreads, 1)
 }
 
 // ---- host side ---------------------------------------------------------------------------------------
-typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
-                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
-                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-EncodeTiledFn encode_fn() {
-  static EncodeTiledFn fn = nullptr;
-  static bool looked = false;
-  if (!looked) {
-    looked = true;
-    void* f = nullptr;
-    cudaDriverEntryPointQueryResult qr;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &qr) ==
-            cudaSuccess &&
-        qr == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<EncodeTiledFn>(f);
-    cudaGetLastError();
-  }
-  return fn;
-}
-
 // 3-D map over a token-major bf16 tensor [T, R, W] (W contiguous): dims {W, R, T}, box {64, 1, Q}.
 bool encode_rows(CUtensorMap* m, const void* base, long long T, int R, int W, int Q) {
-  EncodeTiledFn fn = encode_fn();
+  EncodeTiledFn fn = tma_encode_fn();
   if (fn == nullptr || T <= 0) return false;
   const cuuint64_t dims[3] = {(cuuint64_t)W, (cuuint64_t)R, (cuuint64_t)T};
   const cuuint64_t strides[2] = {(cuuint64_t)W * 2, (cuuint64_t)W * R * 2};
@@ -650,6 +631,21 @@ cudaError_t smem_attr(bool chunked, size_t bytes) {
 }
 
 }  // namespace
+
+EncodeTiledFn tma_encode_fn() {
+  static const EncodeTiledFn fn = [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult qr;
+    EncodeTiledFn r = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &qr) ==
+            cudaSuccess &&
+        qr == cudaDriverEntryPointSuccess)
+      r = reinterpret_cast<EncodeTiledFn>(f);
+    cudaGetLastError();
+    return r;
+  }();
+  return fn;
+}
 
 size_t tc_scan_workspace(int nseq, int max_chunks, int H) {
   const size_t units = (size_t)(nseq > 0 ? nseq : 0) * (size_t)(max_chunks > 1 ? max_chunks : 1) * (size_t)H;
