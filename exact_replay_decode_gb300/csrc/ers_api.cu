@@ -308,7 +308,7 @@ ers_status ers_replay_decode(const ers_dims* dims, const ers_params* prm, const 
   a.flags = flags;
   a.y = y;
   a.status = dev_status;
-  if (rssm && ers::rssm_tc_supported(a.io, a.P, a.N, a.Q, a.H, a.G))   // decode with the fused flush
+  if (rssm && ers::rssm_tc_supported(a.io, a.P, a.N, a.Q, a.H, a.G, cache->read_dtype, cache->anchor_dtype))
     return finish(ers::rssm_tc(a, 1, true, (cudaStream_t)stream));
   const bool tc = ers::tc_supported(a.io, a.P, a.N, a.Q);
   if (rssm && (flags & ERS_FLAG_FUSE_REFRESH) && (tc || !ers::heads_decode_supported(a.P, a.N, a.Q))) {
@@ -368,7 +368,7 @@ ers_status ers_spec_verify(const ers_dims* dims, const ers_params* prm, const er
   ERS_TRY(check_ptr(y, true));
   ERS_TRY(check_ptr(dev_status, false));
   const bool rssm_tc = ers::rssm_tc_supported(dims->io_dtype, dims->headdim, dims->dstate, dims->chunk, dims->nheads,
-                                              dims->ngroups);
+                                              dims->ngroups, cache->read_dtype, cache->anchor_dtype);
   if ((has_narrow_copy(cache) || f16_anchor(cache)) && !rssm_tc &&
       !(narrow_read_shape(dims) && ers::heads_verify_supported(dims->headdim, dims->dstate, dims->chunk, T,
                                                                dims->nheads, dims->ngroups)))

@@ -87,9 +87,10 @@ bool heads_verify_supported(int P, int N, int Q, int T, int H, int G);
 cudaError_t heads_verify(const LaunchArgs& a, cudaStream_t s);
 
 // ReplaySSM decode (T = 1, position advance, fused flush) and verify of T <= L drafts with the read
-// copy's products on the tensor core (bf16 io, P = 64, N = 128, L <= 16, H/G <= 8), ers_rssm_tc.cu.
-// Both calls run the same kernel, so verify outputs keep decode's bits.
-bool rssm_tc_supported(int io, int P, int N, int Q, int H, int G);
+// copy's products on the tensor core (bf16 io and read copy, fp32 or fp16 anchors, P = 64, N = 128,
+// L <= 16, H/G <= 8), ers_rssm_tc.cu.  Both calls run the same kernel, so verify outputs keep
+// decode's bits; every other configuration runs decode and verify on the CUDA-core kernels.
+bool rssm_tc_supported(int io, int P, int N, int Q, int H, int G, int read_dtype, int anchor_dtype);
 cudaError_t rssm_tc(const LaunchArgs& a, int T, bool decode, cudaStream_t s);
 
 // pointer-only kernels, ers_fma.cu

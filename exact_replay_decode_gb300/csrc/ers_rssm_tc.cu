@@ -1,5 +1,6 @@
-// ReplaySSM decode and speculative verify for small refresh periods (L <= 16) with bf16 io, P = 64,
-// N = 128 and at most 8 heads per B/C group: the read copy's products on the tensor core.
+// ReplaySSM decode and speculative verify for small refresh periods (L <= 16) with bf16 io, a bf16
+// read copy, P = 64, N = 128 and at most 8 heads per B/C group: the read copy's products on the
+// tensor core.
 //
 // ReplaySSM notes ("Motivation and method", "Core equations"): the output of a token at buffer row t
 // is the off-diagonal term (S_read C_t), decayed by exp(Acum_t), plus the replay of the committed
@@ -10,19 +11,19 @@
 // decode bit for bit.
 //
 // The drafts' products S_read C_k (M = state rows, N = drafts, K = dstate) are one dense contraction
-// per head: tcgen05.mma kind::f16 with the copy as the A operand (bf16 values; FP8 codes, or NVFP4
-// codes times their block scale, both exact in bf16, with the row scale applied to the fp32 result)
-// and the drafts' C rows as the B operand (row k = draft k, zero rows past the drafts), fp32
-// accumulators in tensor memory.  A column's result depends only on its own B row, so a draft gets
+// per head: tcgen05.mma kind::f16 with the bf16 copy as the A operand and the drafts' C rows as the
+// B operand (row k = draft k, zero rows past the drafts), fp32 accumulators in tensor memory.  A column's result depends only on its own B row, so a draft gets
 // the same bits in column k of a verify as in column 0 of a decode step.
 //
 // Layout: one CTA per (sequence, group), one warp per head (8 warps).  The A operand is a ring of two
 // 32 KB chain buffers of 128 rows x K 128; round r in {0, 1} holds state rows [32r, 32r + 32) of
 // heads 4c..4c+3 in buffer c, so warp w reads its head's results from the TMEM lane quarter w % 4 of
-// chain (r, w / 4): lane j gets row 32r + j, the lane layout of the outputs.  A plain step (bf16
-// copy) loads each round with one TMA box {64, 32, 1, 4} per K half (a 4-D map over the copy, this
-// GPU's memory only); FP8 / NVFP4 copies are converted by the warps; a flushing slot's warps fold
-// their anchor rows and store the freshly cast values into the ring.  Every wait is bounded.
+// chain (r, w / 4): lane j gets row 32r + j, the lane layout of the outputs.  A plain step streams
+// the copy through the ring as TMA boxes {64, 32, 1, 4} (a 4-D map over the copy, this GPU's memory
+// only); a flushing slot's warps fold their anchor rows and store the freshly cast values into the
+// ring.  Every wait is bounded.  FP8 and NVFP4 copies keep the CUDA-core kernels for decode and
+// verify alike: their tiles would have to be converted by the warps between the rounds, which cost
+// more than the products it saves.
 #include <cuda.h>
 #include <string.h>
 
@@ -76,15 +77,6 @@ __device__ __forceinline__ RsmSmem& rsm_smem(unsigned char* raw) {
 // A operand address of state row d (round d / 32) of head w, K element 4j (lane j's 4 values).
 __device__ __forceinline__ uint8_t* ring_at(RsmSmem& sm, int w, int d, int j) {
   return sm.ring[w >> 2] + sw128(128, (uint32_t)((w & 3) * 32 + (d & 31)), (uint32_t)(4 * j));
-}
-
-__device__ __forceinline__ void st_ring(RsmSmem& sm, int w, int d, int j, const float (&v)[4]) {
-  // the values are bf16 values (exact conversions)
-  const __nv_bfloat162 lo = __floats2bfloat162_rn(v[0], v[1]), hi = __floats2bfloat162_rn(v[2], v[3]);
-  uint2 u;
-  u.x = *reinterpret_cast<const uint32_t*>(&lo);
-  u.y = *reinterpret_cast<const uint32_t*>(&hi);
-  *reinterpret_cast<uint2*>(ring_at(sm, w, d, j)) = u;
 }
 
 // K steps [k0, k1) of chain (r, c): D[row][n] (+)= sum over the step's 16 values of A[row][.] Ct[n][.],
@@ -157,51 +149,46 @@ __device__ __forceinline__ void fma2(uint64_t& acc, uint64_t a, uint64_t b) {
 
 // Flush, rows [32r, 32r + 32) of head w: each anchor row is folded with the hc committed records in
 // chunk_state / fold_state order (acc = fma(w_s x_s[d], B_s[n], acc) over s < hc, w_s x_s[d] one fp32
-// product, then fma(decay, H, acc)), written back, cast into the read copy (bf16, FP8 or NVFP4), and
-// the cast values as the product reads them (bf16 values; FP8 codes; NVFP4 codes times their block
-// scale) stored into the ring.  Lane s holds w_s in wl.  Returns the row scale of row 32r + j (FP8,
-// NVFP4).  Every value gets the operations of the standalone refresh, so anchors and copies get its
-// bits; 8 rows share each record's loads, and the products and sums run as paired instructions.
-template <typename HT, typename AT>
-__device__ __forceinline__ float flush_round(RsmSmem& sm, AT* __restrict__ Hd, void* __restrict__ R,
-                                             uint8_t* __restrict__ Rb, float* __restrict__ Rs, int w, int j, int r,
-                                             int hc, float wl, float decay, SrCtr sr, uint32_t row0) {
-  constexpr bool kF8 = std::is_same<HT, uint8_t>::value, kNv = std::is_same<HT, Nvfp4>::value;
-  constexpr bool kSh = std::is_same<AT, Nvfp4Shared>::value;   // the NVFP4 copy is the state
-  static_assert(!kSh || kNv, "a shared state is an NVFP4 copy");
+// product, then fma(decay, H, acc)), written back (fp32, or fp16 by stochastic rounding), cast into
+// the bf16 read copy, and the cast values stored into the ring.  Lane s holds w_s in wl.  Every value
+// gets the operations of the standalone refresh, so anchors and copies get its bits; 4 rows share each
+// record's loads, and the products and sums run as paired instructions.
+template <typename AT>
+__device__ __forceinline__ void flush_round(RsmSmem& sm, AT* __restrict__ Hd, __nv_bfloat16* __restrict__ R, int w,
+                                            int j, int r, int hc, float wl, float decay, SrCtr sr, uint32_t row0) {
   const __nv_bfloat16* sx = sm.x[w];
-  float keep = 1.f;
 #pragma unroll 1
-  for (int blk = 0; blk < 4; ++blk) {
-    const int d0 = 32 * r + 8 * blk;
-    float4 cur[8];   // the block's anchor rows (in L2 by then), landing while the records are summed
+  for (int blk = 0; blk < 8; ++blk) {
+    const int d0 = 32 * r + 4 * blk;
+    float4 cur[4];   // the block's anchor rows (in L2 by then), landing while the records are summed
 #pragma unroll
-    for (int q = 0; q < 8; ++q) cur[q] = anchor_row<AT, kRN>(Hd, R, Rb, Rs, d0 + q, j);
-    uint64_t acc[4][4];   // acc[p][e] = rows (d0 + 2p, d0 + 2p + 1), column 4j + e
+    for (int q = 0; q < 4; ++q) cur[q] = anchor_ld<AT>(Hd, (size_t)(d0 + q) * kRN + 4 * j);
+    uint64_t acc[2][4];   // acc[p][e] = rows (d0 + 2p, d0 + 2p + 1), column 4j + e
 #pragma unroll
-    for (int p = 0; p < 4; ++p)
+    for (int p = 0; p < 2; ++p)
 #pragma unroll
       for (int e = 0; e < 4; ++e) acc[p][e] = 0ull;
+#pragma unroll 4
     for (int s = 0; s < hc; ++s) {
       float bs[4];
       lds4(sm.b + s * kRN + 4 * j, bs);
-      const uint4 xw = *reinterpret_cast<const uint4*>(sx + s * kRP + d0);   // x_s[d0 .. d0 + 8), bf16
+      const uint2 xw = *reinterpret_cast<const uint2*>(sx + s * kRP + d0);   // x_s[d0 .. d0 + 4), bf16
       const float ws = __shfl_sync(kFull, wl, s);
       const uint64_t w2 = pk2(ws, ws);
-      const uint32_t xv[4] = {xw.x, xw.y, xw.z, xw.w};
-      uint64_t wx[4];   // (w_s x_s[d0 + 2p], w_s x_s[d0 + 2p + 1])
+      const uint32_t xv[2] = {xw.x, xw.y};
+      uint64_t wx[2];
 #pragma unroll
-      for (int p = 0; p < 4; ++p)
+      for (int p = 0; p < 2; ++p)
         wx[p] = mul2(w2, pk2(__uint_as_float(xv[p] << 16), __uint_as_float(xv[p] & 0xFFFF0000u)));
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
         const uint64_t b2 = pk2(bs[e], bs[e]);
 #pragma unroll
-        for (int p = 0; p < 4; ++p) fma2(acc[p][e], wx[p], b2);
+        for (int p = 0; p < 2; ++p) fma2(acc[p][e], wx[p], b2);
       }
     }
 #pragma unroll
-    for (int q = 0; q < 8; ++q) {
+    for (int q = 0; q < 4; ++q) {
       const int d = d0 + q;
       float h[4], v[4];
       Quad<float>::unpack(cur[q], h);
@@ -213,57 +200,19 @@ __device__ __forceinline__ float flush_round(RsmSmem& sm, AT* __restrict__ Hd, v
       }
       const size_t o = (size_t)d * kRN + 4 * j;
       if (hc > 0) anchor_st<AT>(Hd, o, v, sr, row0 + d, j);
-      if constexpr (kNv) {
-        float rv[4], beta, rsc;
-        nvfp4_store_row<kRN, kSh>(v, (uint8_t*)R, Rb, Rs, d, j, rv, &beta, &rsc, copy_words<AT>(sr, row0 + d, j));
-#pragma unroll
-        for (int e = 0; e < 4; ++e) rv[e] = __fmul_rn(rv[e], beta);   // exact: at most 6 significant bits
-        st_ring(sm, w, d, j, rv);
-        if (j == 8 * blk + q) keep = rsc;
-      } else if constexpr (kF8) {
-        float sc, rv[4];
-        const uint32_t wq = fp8_quant_row(v, &sc);
-        *reinterpret_cast<uint32_t*>((uint8_t*)R + o) = wq;
-        if (j == 0) Rs[d] = sc;
-        fp8_codes(wq, rv);
-        st_ring(sm, w, d, j, rv);
-        if (j == 8 * blk + q) keep = sc;
-      } else {
-        const __nv_bfloat162 lo2 = __floats2bfloat162_rn(v[0], v[1]), hi2 = __floats2bfloat162_rn(v[2], v[3]);
-        uint2 u;
-        u.x = *reinterpret_cast<const uint32_t*>(&lo2);
-        u.y = *reinterpret_cast<const uint32_t*>(&hi2);
-        *reinterpret_cast<uint2*>((__nv_bfloat16*)R + o) = u;
-        st_ring_raw(sm, w, d, j, u);
-      }
+      const __nv_bfloat162 lo2 = __floats2bfloat162_rn(v[0], v[1]), hi2 = __floats2bfloat162_rn(v[2], v[3]);
+      uint2 u;
+      u.x = *reinterpret_cast<const uint32_t*>(&lo2);
+      u.y = *reinterpret_cast<const uint32_t*>(&hi2);
+      *reinterpret_cast<uint2*>(R + o) = u;
+      st_ring_raw(sm, w, d, j, u);
     }
-  }
-  return keep;
-}
-
-// Round r of a plain step with an FP8 / NVFP4 copy: rows [32r, 32r + 32) of head w from the words in
-// q (row 32r + t in q[t]) into the ring as bf16 (codes; NVFP4 codes times their block scale); in
-// round 0 the words of round 1 are loaded into q as each one is consumed.
-template <typename HT>
-__device__ __forceinline__ void convert_round(RsmSmem& sm, const RowSrc<HT, kRN>& src, uint32_t (&q)[32], int w,
-                                              int j, int r) {
-#pragma unroll
-  for (int t = 0; t < 32; ++t) {
-    float v[4], ls;
-    row_values<HT>(q[t], v, &ls);
-    if constexpr (kLaneScale<HT>) {
-#pragma unroll
-      for (int e = 0; e < 4; ++e) v[e] = __fmul_rn(v[e], ls);
-    }
-    st_ring(sm, w, 32 * r + t, j, v);
-    if (r == 0) q[t] = src.ld(32 + t, j);
   }
 }
 
-// Outputs of every draft for state row d = 32r + j of head w (lane j): the product from TMEM
-// (times the row scale sc for FP8 / NVFP4 copies), the replay over output rows s <= t = h0 + k in
-// order, and combine_out.  Lane s holds output row s's decay term dl and log-decay prefix v.
-__device__ __forceinline__ void out_round(const RsmSmem& sm, const float (&dv)[kRTM], float sc, int w, int j, int r,
+// Outputs of every draft for state row d = 32r + j of head w (lane j): the product from TMEM, the
+// replay over output rows s <= t = h0 + k in order, and combine_out.  Lane s holds output row s's decay term dl and log-decay prefix v.
+__device__ __forceinline__ void out_round(const RsmSmem& sm, const float (&dv)[kRTM], int w, int j, int r,
                                           int h0, int Td, float dl, df v, float Dh, __nv_bfloat16* __restrict__ y,
                                           size_t ystride) {
   const __nv_bfloat16* sx = sm.x[w];
@@ -277,8 +226,7 @@ __device__ __forceinline__ void out_round(const RsmSmem& sm, const float (&dv)[k
     float acc = 0.f;
     for (int s = 0; s <= t; ++s)
       acc = __fmaf_rn(__shfl_sync(kFull, M, s), to_f(sx[(s < h0 ? s : kRQM + s - h0) * kRP + d]), acc);
-    const float yo = __fmul_rn(dv[k], sc);
-    y[(size_t)k * ystride + d] = from_f<__nv_bfloat16>(combine_out(expf(at.hi), yo, acc, Dh, to_f(sx[(kRQM + k) * kRP + d])));
+    y[(size_t)k * ystride + d] = from_f<__nv_bfloat16>(combine_out(expf(at.hi), dv[k], acc, Dh, to_f(sx[(kRQM + k) * kRP + d])));
   }
 }
 
@@ -328,11 +276,18 @@ __device__ __forceinline__ void rows_ready(RsmSmem& sm, int r, int j) {
 // decode != 0: one token per sequence (Td = 1) with the position advance (and, with
 // ERS_FLAG_FUSE_REFRESH, the flush of a full buffer); else a verify of Td drafts (pointers unchanged;
 // ERS_FLAG_AUTO_FLUSH allows flushes).
-template <typename HT, typename AT>
+// part: kAll, or a call split in two launches so that the long flushing CTAs run alongside the plain
+// ones instead of after them: kFlushes (the flushing slots; reads the positions, lets the dependent
+// launch start, writes no position) then kPlain (launched as its programmatic dependent: the plain
+// slots, and every position advance; its last CTA waits for the first launch, so the pair completes
+// together).
+enum RsmPart : int { kAll = 0, kFlushes = 1, kPlain = 2 };
+
+template <typename AT>
 __global__ void __maxnreg__(96)
-    k_rssm_tc(const __grid_constant__ LaunchArgs a, const __grid_constant__ CUtensorMap map, int Td, int decode) {
+    k_rssm_tc(const __grid_constant__ LaunchArgs a, const __grid_constant__ CUtensorMap map, int Td, int decode,
+              int part) {
   using T = __nv_bfloat16;
-  constexpr bool kBf = std::is_same<HT, __nv_bfloat16>::value;
   extern __shared__ __align__(16) unsigned char rsm_raw[];
   RsmSmem& sm = rsm_smem(rsm_raw);
   const int tid = threadIdx.x, w = tid >> 5, j = tid & 31;
@@ -362,9 +317,21 @@ __global__ void __maxnreg__(96)
       return;
     }
   }
+  if (part == kFlushes) {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");   // this CTA has read its position
+    if (!flush) return;
+  } else if (part == kPlain) {
+    if (blockIdx.x == gridDim.x - 1 && blockIdx.y == gridDim.y - 1)
+      asm volatile("griddepcontrol.wait;" ::: "memory");   // completes only after the flushing launch
+    if (flush) {   // done by the first launch; a decode still counts the slot's CTAs here
+      __syncthreads();   // every thread of the CTA has read the position
+      if (decode && tid == 0) count_and_advance(&a.pos[slot], a.G, 1);
+      return;
+    }
+  }
   const int h0 = flush ? 0 : hc;   // committed rows that precede the drafts
   const int nchains = hpg > 4 ? 2 : 1;
-  const bool tma = kBf && !flush;
+  const bool tma = !flush;
   const int head0 = slot * a.H + g * hpg;   // the CTA's first head in the copy's head index
   const uint64_t lim = a.wait_ns ? a.wait_ns : tc::kWaitLimitNs;
   const size_t HP = (size_t)a.H * kRP, GN = (size_t)a.G * kRN;
@@ -385,32 +352,8 @@ __global__ void __maxnreg__(96)
     tc::tmem_alloc(&sm.tmem, kRTmemCols);
   }
   const size_t soff = ((size_t)slot * a.H + h) * kRP * kRN;
-  if (flush && active && j == 0) {   // the head's anchor rows stream into L2 while the prologue runs
-    if constexpr (std::is_same<AT, Nvfp4Shared>::value) {
-      l2_prefetch((const uint8_t*)a.read_copy + soff / 2, kRP * kRN / 2);
-    } else {
-      l2_prefetch(reinterpret_cast<const AT*>(a.state) + soff, kRP * kRN * sizeof(AT));
-    }
-  }
-  // FP8 / NVFP4 copy of a plain step: the first 32 rows' words in flight, the row scales of rows j, 32 + j
-  RowSrc<HT, kRN> src;
-  uint32_t q[kBf ? 1 : 32];
-  float sc[2] = {1.f, 1.f};
-  if constexpr (!kBf) {
-    if constexpr (std::is_same<HT, Nvfp4>::value) {
-      src.c4 = (const uint8_t*)a.read_copy + soff / 2;
-      src.bs = a.read_bscale + soff / 16;
-    } else {
-      src.p = (const HT*)a.read_copy + soff;
-    }
-    if (!flush && active) {
-#pragma unroll
-      for (int t = 0; t < 32; ++t) q[t] = src.ld(t, j);
-      const float* Rs = a.read_scale + ((size_t)slot * a.H + h) * kRP;
-      sc[0] = Rs[j];
-      sc[1] = Rs[32 + j];
-    }
-  }
+  if (flush && active && j == 0)   // the head's anchor rows stream into L2 while the prologue runs
+    l2_prefetch(reinterpret_cast<const AT*>(a.state) + soff, kRP * kRN * sizeof(AT));
   // committed rows 0..hc-1 at smem rows 0..hc-1, drafts at rows kRQM..kRQM+Td-1
   const T* bB = (const T*)a.bB + (size_t)g * kRN;
   constexpr int kBChunks = kRN * 2 / 16, kXChunks = kRP * 2 / 16;
@@ -447,7 +390,7 @@ __global__ void __maxnreg__(96)
     if (j == 0) issuer(sm, &map, tma, nchains, head0, a.status, lim);
     __syncwarp();
   } else {
-    if (decode && tid == 0) count_and_advance(&a.pos[slot], a.G, h0 + 1);   // every thread has read pos
+    if (decode && part != kFlushes && tid == 0) count_and_advance(&a.pos[slot], a.G, h0 + 1);   // pos read by all
     // output rows s < h0 + Td: committed rows, then the drafts; lane s holds row s
     const int nout = h0 + Td;
     const float dt_o_d = __shfl_sync(kFull, dt_d, max(j - h0, 0) & 31);
@@ -471,19 +414,19 @@ __global__ void __maxnreg__(96)
     }
     tc::named_sync(1, kRMath);   // Gram rows complete (math warps only)
     T* y = (T*)a.y + (size_t)i * Td * HP + (size_t)h * kRP;
-    auto out = [&](int r, float scr) {
+    auto out = [&](int r) {
       mbar_wait(&sm.done[r], 0, a.status, lim);   // bounded; a wait that gave up has reported ERS_ETIMEOUT
       tc::after_sync();
       if (active) {
         float dv[kRTM];
         tc::tmem_ld16(tc::taddr(sm.tmem, 32 * (w & 3), 16 * (2 * r + (w >> 2))), dv);
-        out_round(sm, dv, scr, w, j, r, h0, Td, dl, v, Dh, y, HP);
+        out_round(sm, dv, w, j, r, h0, Td, dl, v, Dh, y, HP);
       }
     };
     if (tma) {
-      out(0, 1.f);
-      out(1, 1.f);
-    } else if (flush) {   // fold, write back and recast each round's anchor rows into the ring
+      out(0);
+      out(1);
+    } else {   // a flushing slot: fold, write back and recast each round's anchor rows into the ring
       float dc = 0.f;
       df vc = {0.f, 0.f};
       if (j < hc) {
@@ -494,29 +437,16 @@ __global__ void __maxnreg__(96)
       const df last = {__shfl_sync(kFull, vc.hi, hc - 1), __shfl_sync(kFull, vc.lo, hc - 1)};
       const float wl = j < hc ? __fmul_rn(dc, expf(df_diff(last, vc))) : 0.f;   // state_weights
       const float decay = expf(last.hi);
-      AT* Hd = anchor_ptr<AT>(a, soff);
-      void* R = std::is_same<HT, Nvfp4>::value ? (void*)((uint8_t*)a.read_copy + soff / 2)
-                                               : (void*)((HT*)a.read_copy + soff);
-      uint8_t* Rb = a.read_bscale + soff / 16;
-      float* Rsw = a.read_scale + ((size_t)slot * a.H + h) * kRP;
+      AT* Hd = reinterpret_cast<AT*>(a.state) + soff;
+      T* R = (T*)a.read_copy + soff;
       const SrCtr sr{a.sr_key0, a.sr_key1, a.sr_nonce, (uint32_t)slot};
-      if (active) sc[0] = flush_round<HT, AT>(sm, Hd, R, Rb, Rsw, w, j, 0, hc, wl, decay, sr, (uint32_t)(h * kRP));
+      if (active) flush_round<AT>(sm, Hd, R, w, j, 0, hc, wl, decay, sr, (uint32_t)(h * kRP));
       rows_ready(sm, 0, j);
       mbar_wait(&sm.done[0], 0, a.status, lim);   // round 0's MMAs have read the ring
-      if (active) sc[1] = flush_round<HT, AT>(sm, Hd, R, Rb, Rsw, w, j, 1, hc, wl, decay, sr, (uint32_t)(h * kRP));
+      if (active) flush_round<AT>(sm, Hd, R, w, j, 1, hc, wl, decay, sr, (uint32_t)(h * kRP));
       rows_ready(sm, 1, j);
-      out(0, sc[0]);
-      out(1, sc[1]);
-    } else {
-      if constexpr (!kBf) {   // a narrow copy's codes, converted into the ring
-        if (active) convert_round<HT>(sm, src, q, w, j, 0);
-        rows_ready(sm, 0, j);
-        mbar_wait(&sm.done[0], 0, a.status, lim);
-        if (active) convert_round<HT>(sm, src, q, w, j, 1);
-        rows_ready(sm, 1, j);
-        out(0, sc[0]);
-        out(1, sc[1]);
-      }
+      out(0);
+      out(1);
     }
     if (active) {   // the drafts go to buffer rows h0..h0+Td-1 (B/C once per group)
       for (int k = 0; k < Td; ++k) {
@@ -554,46 +484,55 @@ bool encode_copy_map(CUtensorMap* m, const void* base, long long heads) {
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <typename HT, typename AT>
-cudaError_t launch_rssm(const LaunchArgs& a, const CUtensorMap& map, int T, bool decode, cudaStream_t s) {
+// split: the call may flush (a fused decode flush, or a verify with ERS_FLAG_AUTO_FLUSH): two launches.
+template <typename AT>
+cudaError_t launch_rssm(const LaunchArgs& a, const CUtensorMap& map, int T, bool decode, bool split, cudaStream_t s) {
   constexpr size_t sm = rsm_smem_bytes();
-  cudaError_t e = prep(k_rssm_tc<HT, AT>, sm);
+  auto k = k_rssm_tc<AT>;
+  cudaError_t e = prep(k, sm);
   if (e != cudaSuccess) return e;
   // the largest shared-memory carveout: two CTAs per SM (the default follows the occupancy rule for
   // kernels that allocate tensor memory, one CTA per SM, and leaves room for one)
-  e = cudaFuncSetAttribute(k_rssm_tc<HT, AT>, cudaFuncAttributePreferredSharedMemoryCarveout,
-                           cudaSharedmemCarveoutMaxShared);
+  e = cudaFuncSetAttribute(k, cudaFuncAttributePreferredSharedMemoryCarveout, cudaSharedmemCarveoutMaxShared);
   if (e != cudaSuccess) return e;
-  k_rssm_tc<HT, AT><<<dim3(a.G, a.nseq), kRThreads, sm, s>>>(a, map, T, decode ? 1 : 0);
-  return cudaGetLastError();
+  const dim3 grid(a.G, a.nseq);
+  const int dec = decode ? 1 : 0;
+  if (!split) {
+    k<<<grid, kRThreads, sm, s>>>(a, map, T, dec, (int)kAll);
+    return cudaGetLastError();
+  }
+  k<<<grid, kRThreads, sm, s>>>(a, map, T, dec, (int)kFlushes);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = dim3(kRThreads);
+  cfg.dynamicSmemBytes = sm;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, k, a, map, T, dec, (int)kPlain);
 }
 
 }  // namespace
 
-bool rssm_tc_supported(int io, int P, int N, int Q, int H, int G) {
-  return io == ERS_DTYPE_BF16 && P == kRP && N == kRN && Q >= 1 && Q <= kRQM && G > 0 && H % G == 0 &&
-         H / G <= kRWarps;
+bool rssm_tc_supported(int io, int P, int N, int Q, int H, int G, int read_dtype, int anchor_dtype) {
+  return io == ERS_DTYPE_BF16 && read_dtype == ERS_READ_BF16 && anchor_dtype != ERS_ANCHOR_NVFP4_SHARED_SR &&
+         P == kRP && N == kRN && Q >= 1 && Q <= kRQM && G > 0 && H % G == 0 && H / G <= kRWarps;
 }
 
 cudaError_t rssm_tc(const LaunchArgs& a, int T, bool decode, cudaStream_t s) {
   if (a.read_copy == nullptr || T < 1 || T > a.Q || (decode && T != 1)) return cudaErrorInvalidValue;
   if (a.nseq == 0) return cudaSuccess;
+  const bool split = decode ? (a.flags & ERS_FLAG_FUSE_REFRESH) != 0 : (a.flags & ERS_FLAG_AUTO_FLUSH) != 0;
   CUtensorMap map;
   memset(&map, 0, sizeof(map));
-  if (!a.read_fp8 && !a.read_nvfp4 && !encode_copy_map(&map, a.read_copy, (long long)a.nslots * a.H))
-    return cudaErrorNotSupported;
-  if (a.anchor_shared) {
-    if (!a.read_nvfp4) return cudaErrorNotSupported;
-    return launch_rssm<Nvfp4, Nvfp4Shared>(a, map, T, decode, s);
-  }
-  if (a.anchor_f16) {
-    if (a.read_nvfp4) return launch_rssm<Nvfp4, __half>(a, map, T, decode, s);
-    if (a.read_fp8) return launch_rssm<uint8_t, __half>(a, map, T, decode, s);
-    return launch_rssm<__nv_bfloat16, __half>(a, map, T, decode, s);
-  }
-  if (a.read_nvfp4) return launch_rssm<Nvfp4, float>(a, map, T, decode, s);
-  if (a.read_fp8) return launch_rssm<uint8_t, float>(a, map, T, decode, s);
-  return launch_rssm<__nv_bfloat16, float>(a, map, T, decode, s);
+  if (!encode_copy_map(&map, a.read_copy, (long long)a.nslots * a.H)) return cudaErrorNotSupported;
+  if (a.read_fp8 || a.read_nvfp4 || a.anchor_shared) return cudaErrorNotSupported;
+  if (a.anchor_f16) return launch_rssm<__half>(a, map, T, decode, split, s);
+  return launch_rssm<float>(a, map, T, decode, split, s);
 }
 
 }  // namespace ers
