@@ -334,7 +334,7 @@ __global__ void __launch_bounds__(kThreads, 2) k_decode_heads(LaunchArgs a) {
   float c[4];
   load_k<T, 4>((const T*)a.C + (size_t)i * GN + (size_t)g * N + 4 * j, c);
   typename RawOf<HT>::type q[rows_in_flight<HT>()];
-  if (active) {
+  if (active && a.part != kPartFlushes) {   // the first launch of a split call streams anchors only
 #pragma unroll
     for (int r = 0; r < rows_in_flight<HT>(); ++r) q[r] = src.ld(r, j);
   }
@@ -345,6 +345,17 @@ __global__ void __launch_bounds__(kThreads, 2) k_decode_heads(LaunchArgs a) {
   if (p > a.Q || (p == a.Q && !flush)) {   // the same for every CTA of the slot: none counts, pos stays
     if (tid == 0) report(a.status, ERS_EALIGN);
     return;
+  }
+  if (a.part == kPartFlushes) {   // a split call (one CTA per group): the flushing slots only
+    allow_dependents();
+    if (!flush) return;
+  } else if (a.part == kPartPlain) {
+    if (last_cta_of_grid()) wait_primary();
+    if (flush) {   // done by the first launch; its position advances here
+      __syncthreads();   // every thread of the CTA has read the position
+      if (tid == 0) advance_pos(&a.pos[slot], ncta, 1);
+      return;
+    }
   }
   // exact mode (which streams the fp32 checkpoint) refreshes when the new token fills the chunk
   const bool refresh = std::is_same<HT, float>::value && !rssm && fuse && p + 1 == a.Q;
@@ -390,7 +401,7 @@ __global__ void __launch_bounds__(kThreads, 2) k_decode_heads(LaunchArgs a) {
   __shared__ int last_cta;
   if (tid == 0) {
     if (shared_rows) __threadfence();
-    last_cta = advance_pos(&a.pos[slot], ncta, refresh ? 0 : pn + 1);
+    last_cta = a.part == kPartFlushes ? 0 : advance_pos(&a.pos[slot], ncta, refresh ? 0 : pn + 1);
     if (shared_rows) __threadfence();
   }
   for (int s = w; s <= pn; s += kHeadsPerCta) {
@@ -487,9 +498,12 @@ cudaError_t launch_decode_heads(const LaunchArgs& a, cudaStream_t s) {
   const dim3 grid(a.G * nbl, a.nseq);
   constexpr size_t sm = heads_smem_bytes<T, P, N, QM>();
   const bool rssm = (a.flags & ERS_FLAG_REPLAYSSM) != 0;
+  // a fused ReplaySSM flush with one CTA per group: two launches (launch_parts)
+  const bool split = rssm && (a.flags & ERS_FLAG_FUSE_REFRESH) && nbl == 1;
   auto run = [&](auto kernel) {
     cudaError_t e = prep(kernel, sm);
     if (e != cudaSuccess) return e;
+    if (split) return launch_parts(kernel, grid, kThreads, sm, s, a);
     kernel<<<grid, kThreads, sm, s>>>(a);
     return cudaGetLastError();   // the kernel advances the positions itself
   };

@@ -63,11 +63,19 @@ struct LaunchArgs {
   float* ws_incl;    // tensor cores: [nseq, max_chunks, H, P, N] end state of each chunk, for the look-back
   int32_t* ws_flags; // tensor cores: [nseq, max_chunks, H] 0 / 1 (chunk state published) / 2 (end state too)
   unsigned long long wait_ns;   // limit of every bounded device wait (0: the default, 1 s)
+  int part;                     // a ReplaySSM call that may flush, split in two launches: kPart*
   const int32_t* accepted;
   int32_t* status;
 };
 
 enum class Op { kScan, kChunkedPrefill };
+
+// A ReplaySSM decode or verify that may flush runs as two launches so that the long flushing CTAs
+// overlap the others instead of trailing them: kPartFlushes (the flushing slots; every CTA reads its
+// position, then lets the dependent launch start; no position is written) and kPartPlain (launched as
+// its programmatic dependent: the other slots and every position advance; its last CTA waits for the
+// first launch, so the pair completes together).  kPartAll: one launch does everything.
+enum : int { kPartAll = 0, kPartFlushes = 1, kPartPlain = 2 };
 
 // FMA (CUDA-core) engine, ers_fma.cu
 cudaError_t fma_prefill(const LaunchArgs& a, Op op, cudaStream_t s);

@@ -177,6 +177,13 @@ __global__ void __launch_bounds__(kThreads, 2) k_verify_heads(LaunchArgs a) {
     if (tid == 0) report(a.status, ERS_EOVERFLOW);
     return;
   }
+  if (a.part == kPartFlushes) {   // a split call: the flushing slots only
+    allow_dependents();
+    if (!flush) return;
+  } else if (a.part == kPartPlain) {
+    if (last_cta_of_grid()) wait_primary();
+    if (flush) return;   // done by the first launch
+  }
   const int h0 = flush ? 0 : hc;   // committed rows that precede the drafts
   const size_t HP = (size_t)a.H * P, GN = (size_t)a.G * N;
   const size_t soff = ((size_t)slot * a.H + h) * P * N;
@@ -355,6 +362,7 @@ cudaError_t launch_verify_heads(const LaunchArgs& a, cudaStream_t s) {
   constexpr size_t sm = verify_smem_bytes<T, P, N, QM>();
   cudaError_t e = prep(k_verify_heads<T, HT, P, N, QM, AT>, sm);
   if (e != cudaSuccess) return e;
+  if (a.flags & ERS_FLAG_AUTO_FLUSH) return launch_parts(k_verify_heads<T, HT, P, N, QM, AT>, dim3(a.G, a.nseq), kThreads, sm, s, a);
   k_verify_heads<T, HT, P, N, QM, AT><<<dim3(a.G, a.nseq), kThreads, sm, s>>>(a);
   return cudaGetLastError();
 }

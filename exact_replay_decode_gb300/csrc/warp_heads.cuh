@@ -448,5 +448,34 @@ cudaError_t prep(K kernel, size_t smem) {
   return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
 }
 
+// Programmatic dependent launch, device side: the first launch of a split call lets its dependent
+// start once every CTA has read its position; the dependent's last CTA waits for the first launch.
+__device__ __forceinline__ void allow_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void wait_primary() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ bool last_cta_of_grid() {
+  return blockIdx.x == gridDim.x - 1 && blockIdx.y == gridDim.y - 1 && blockIdx.z == gridDim.z - 1;
+}
+
+// A split call (kPartFlushes, then kPartPlain as its programmatic dependent) of kernel(LaunchArgs).
+template <typename K>
+cudaError_t launch_parts(K kernel, dim3 grid, int threads, size_t smem, cudaStream_t s, LaunchArgs a) {
+  a.part = kPartFlushes;
+  kernel<<<grid, threads, smem, s>>>(a);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  a.part = kPartPlain;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = dim3(threads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, a);
+}
+
 }  // namespace wh
 }  // namespace ers
