@@ -110,20 +110,12 @@ __device__ __noinline__ void stream_state_refresh(float* __restrict__ Hd, __nv_b
     float pb[8];
 #pragma unroll
     for (int hf = 0; hf < 2; ++hf) {
-      float acc[4][4];
-#pragma unroll
-      for (int r = 0; r < 4; ++r)
-#pragma unroll
-        for (int e = 0; e < 4; ++e) acc[r][e] = 0.f;
+      Fold4 acc;
+      acc.zero();
       for (int s = 0; s <= p; ++s) {
         float bs[4];
         lds4(sB + s * N + 4 * j, bs);
-        const float4 wv = *reinterpret_cast<const float4*>(wx + s * P + blk * 8 + 4 * hf);
-        const float wr[4] = {wv.x, wv.y, wv.z, wv.w};
-#pragma unroll
-        for (int r = 0; r < 4; ++r)
-#pragma unroll
-          for (int e = 0; e < 4; ++e) acc[r][e] = __fmaf_rn(wr[r], bs[e], acc[r][e]);
+        acc.add(*reinterpret_cast<const float4*>(wx + s * P + blk * 8 + 4 * hf), bs);
       }
 #pragma unroll
       for (int r4 = 0; r4 < 4; ++r4) {
@@ -133,7 +125,7 @@ __device__ __noinline__ void stream_state_refresh(float* __restrict__ Hd, __nv_b
         pb[r] = Dot<N>::partial(c, h);
         float v[4];
 #pragma unroll
-        for (int e = 0; e < 4; ++e) v[e] = __fmaf_rn(decay, h[e], acc[r4][e]);
+        for (int e = 0; e < 4; ++e) v[e] = __fmaf_rn(decay, h[e], acc.get(r4, e));
         const size_t o = (size_t)(blk * 8 + r) * N + 4 * j;
         *reinterpret_cast<float4*>(Hd + o) = make_float4(v[0], v[1], v[2], v[3]);
         if (Rd != nullptr) {
@@ -202,20 +194,12 @@ __device__ __noinline__ void stream_flush_copy(AT* __restrict__ Hd, void* __rest
     float pb[8];
 #pragma unroll
     for (int hf = 0; hf < 2; ++hf) {
-      float acc[4][4];
-#pragma unroll
-      for (int r = 0; r < 4; ++r)
-#pragma unroll
-        for (int e = 0; e < 4; ++e) acc[r][e] = 0.f;
+      Fold4 acc;
+      acc.zero();
       for (int s = 0; s < hc; ++s) {
         float bs[4];
         lds4(sB + s * N + 4 * j, bs);
-        const float4 wv = *reinterpret_cast<const float4*>(wx + s * P + blk * 8 + 4 * hf);
-        const float wr[4] = {wv.x, wv.y, wv.z, wv.w};
-#pragma unroll
-        for (int r = 0; r < 4; ++r)
-#pragma unroll
-          for (int e = 0; e < 4; ++e) acc[r][e] = __fmaf_rn(wr[r], bs[e], acc[r][e]);
+        acc.add(*reinterpret_cast<const float4*>(wx + s * P + blk * 8 + 4 * hf), bs);
       }
 #pragma unroll
       for (int r4 = 0; r4 < 4; ++r4) {
@@ -223,7 +207,7 @@ __device__ __noinline__ void stream_flush_copy(AT* __restrict__ Hd, void* __rest
         float h[4], v[4], rv[4];
         Quad<float>::unpack(cur[r], h);
 #pragma unroll
-        for (int e = 0; e < 4; ++e) v[e] = hc > 0 ? __fmaf_rn(decay, h[e], acc[r4][e]) : h[e];
+        for (int e = 0; e < 4; ++e) v[e] = hc > 0 ? __fmaf_rn(decay, h[e], acc.get(r4, e)) : h[e];
         const size_t o = (size_t)(blk * 8 + r) * N + 4 * j;
         if (hc > 0) anchor_st<AT>(Hd, o, v, sr, row0 + blk * 8 + r, j);
         float ls = 1.f;

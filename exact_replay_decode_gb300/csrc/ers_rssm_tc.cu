@@ -128,25 +128,6 @@ __device__ __forceinline__ void count_and_advance(int32_t* pos, int ncta, int32_
   if ((old >> 16) == ncta - 1) atomicExch(pos, newp);
 }
 
-// Paired fp32 arithmetic (one instruction for two IEEE round-to-nearest operations; per element the
-// result is that of the scalar operation).
-__device__ __forceinline__ uint64_t pk2(float lo, float hi) {
-  uint64_t r;
-  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
-  return r;
-}
-__device__ __forceinline__ void up2(uint64_t v, float& lo, float& hi) {
-  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
-}
-__device__ __forceinline__ uint64_t mul2(uint64_t a, uint64_t b) {
-  uint64_t r;
-  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
-  return r;
-}
-__device__ __forceinline__ void fma2(uint64_t& acc, uint64_t a, uint64_t b) {
-  asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(acc) : "l"(a), "l"(b));
-}
-
 // Flush, rows [32r, 32r + 32) of head w: each anchor row is folded with the hc committed records in
 // chunk_state / fold_state order (acc = fma(w_s x_s[d], B_s[n], acc) over s < hc, w_s x_s[d] one fp32
 // product, then fma(decay, H, acc)), written back (fp32, or fp16 by stochastic rounding), cast into

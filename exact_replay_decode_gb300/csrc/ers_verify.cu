@@ -88,23 +88,17 @@ __device__ __noinline__ void stream_anchor_flush(AT* __restrict__ Hd, void* __re
   static_assert(!kSh || kNv, "a shared state is an NVFP4 copy");
 #pragma unroll 1
   for (int d0 = 0; d0 < P; d0 += 8) {
-    float h[8][4], acc[8][4];
+    float h[8][4];
+    Fold4 acc[2];   // rows d0..d0+3, d0+4..d0+7
 #pragma unroll
-    for (int r = 0; r < 8; ++r) {
-      Quad<float>::unpack(anchor_row<AT, N>(Hd, R, Rb, Rs, d0 + r, j), h[r]);
-#pragma unroll
-      for (int e = 0; e < 4; ++e) acc[r][e] = 0.f;
-    }
+    for (int r = 0; r < 8; ++r) Quad<float>::unpack(anchor_row<AT, N>(Hd, R, Rb, Rs, d0 + r, j), h[r]);
+    acc[0].zero();
+    acc[1].zero();
     for (int s = 0; s < hc; ++s) {
       float bs[4];
       lds4(sB + s * N + 4 * j, bs);
-      const float4 w0 = *reinterpret_cast<const float4*>(wx + s * P + d0);
-      const float4 w1 = *reinterpret_cast<const float4*>(wx + s * P + d0 + 4);
-      const float wr[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
-#pragma unroll
-      for (int r = 0; r < 8; ++r)
-#pragma unroll
-        for (int e = 0; e < 4; ++e) acc[r][e] = __fmaf_rn(wr[r], bs[e], acc[r][e]);
+      acc[0].add(*reinterpret_cast<const float4*>(wx + s * P + d0), bs);
+      acc[1].add(*reinterpret_cast<const float4*>(wx + s * P + d0 + 4), bs);
     }
     float part[32];
     float srow = 0.f;   // FP8: scale of row d0 + j % 8
@@ -112,7 +106,7 @@ __device__ __noinline__ void stream_anchor_flush(AT* __restrict__ Hd, void* __re
     for (int r = 0; r < 8; ++r) {
       float v[4];
 #pragma unroll
-      for (int e = 0; e < 4; ++e) v[e] = __fmaf_rn(decay, h[r][e], acc[r][e]);
+      for (int e = 0; e < 4; ++e) v[e] = __fmaf_rn(decay, h[r][e], acc[r >> 2].get(r & 3, e));
       const size_t o = (size_t)(d0 + r) * N + 4 * j;
       anchor_st<AT>(Hd, o, v, sr, row0 + d0 + r, j);
       float rv[4];   // what the read copy now holds (FP8 / NVFP4: the codes, scaled as they are read)

@@ -67,6 +67,51 @@ __device__ __forceinline__ void lds4(const __nv_bfloat16* p, float (&v)[4]) {
   Quad<__nv_bfloat16>::unpack(*reinterpret_cast<const uint2*>(p), v);
 }
 
+// Paired fp32 arithmetic (one instruction for two IEEE round-to-nearest operations; per element the
+// result is that of the scalar operation).
+__device__ __forceinline__ uint64_t pk2(float lo, float hi) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ void up2(uint64_t v, float& lo, float& hi) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ uint64_t mul2(uint64_t a, uint64_t b) {
+  uint64_t r;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+__device__ __forceinline__ void fma2(uint64_t& acc, uint64_t a, uint64_t b) {
+  asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(acc) : "l"(a), "l"(b));
+}
+
+// A 4-row x 4-column block of fold accumulators (lane j: columns 4j..4j+3), rows paired:
+// add(w, b) is acc[r][e] = fma(w[r], b[e], acc[r][e]) for every r, e, as 8 paired fmas.
+struct Fold4 {
+  uint64_t a[2][4];   // a[p][e] = (acc[2p][e], acc[2p + 1][e])
+  __device__ __forceinline__ void zero() {
+#pragma unroll
+    for (int p = 0; p < 2; ++p)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) a[p][e] = 0ull;
+  }
+  __device__ __forceinline__ void add(float4 w, const float (&b)[4]) {
+    const uint64_t w01 = pk2(w.x, w.y), w23 = pk2(w.z, w.w);
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const uint64_t b2 = pk2(b[e], b[e]);
+      fma2(a[0][e], w01, b2);
+      fma2(a[1][e], w23, b2);
+    }
+  }
+  __device__ __forceinline__ float get(int r, int e) const {
+    float lo, hi;
+    up2(a[r >> 1][e], lo, hi);
+    return (r & 1) ? hi : lo;
+  }
+};
+
 // Reduce-scatter of 32 partials v[0..31] (row r of the 32 in v[r]) with the pairings of
 // Dot<128>'s butterfly: each stage keeps the half of the rows whose index bit matches the lane's,
 // so lane j returns row j's reduction, bit-identical to Dot<128>::reduce of that row (same tree;
