@@ -217,7 +217,9 @@ class DecodeBench:
         self.tok = torch_io.tokens_to(stream, dev, lead=(TOKEN_RING, self.S))
         self.y = torch.empty(self.S, d.nheads, d.headdim, dtype=torch.bfloat16, device=dev)
         self.status = ers.Status(dev)
-        self.launches_per_step = 1   # k_decode_heads (advances the positions itself)
+        # k_decode_heads twice: the slots whose step fills the chunk, then the others as its
+        # programmatic dependent (the kernel advances the positions itself)
+        self.launches_per_step = 2
 
     def step(self, k: int):
         x, dt, B, C = (t[k % TOKEN_RING] for t in self.tok)

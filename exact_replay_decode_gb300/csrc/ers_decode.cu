@@ -330,19 +330,22 @@ __global__ void __launch_bounds__(kThreads, 2) k_decode_heads(LaunchArgs a) {
     if (tid == 0) report(a.status, ERS_EALIGN);
     return;
   }
-  if (a.part == kPartFlushes) {   // a split call (one CTA per group): the flushing slots only
+  // exact mode (which streams the fp32 checkpoint) refreshes when the new token fills the chunk
+  const bool refresh = std::is_same<HT, float>::value && !rssm && fuse && p + 1 == a.Q;
+  // a split call (a fused refresh or flush, one CTA per group): the first launch does the slots
+  // whose step fills the chunk (exact mode) or flushes (ReplaySSM), the second the others
+  const bool heavy = flush || refresh;
+  if (a.part == kPartFlushes) {
     allow_dependents();
-    if (!flush) return;
+    if (!heavy) return;
   } else if (a.part == kPartPlain) {
     if (last_cta_of_grid()) wait_primary();
-    if (flush) {   // done by the first launch; its position advances here
+    if (heavy) {   // done by the first launch; its position advances here
       __syncthreads();   // every thread of the CTA has read the position
-      if (tid == 0) advance_pos(&a.pos[slot], ncta, 1);
+      if (tid == 0) advance_pos(&a.pos[slot], ncta, refresh ? 0 : 1);
       return;
     }
   }
-  // exact mode (which streams the fp32 checkpoint) refreshes when the new token fills the chunk
-  const bool refresh = std::is_same<HT, float>::value && !rssm && fuse && p + 1 == a.Q;
   const int o0 = flush ? p : 0, pn = p - o0;   // output rows s = 0..pn are smem rows o0 + s
   // buffer rows 0..p-1 and the new token as row p: the group's B rows, this head's x rows
   const T* bB = (const T*)a.bB + (size_t)g * N;   // buffer row r at buf_row(a, slot, r)
@@ -482,8 +485,9 @@ cudaError_t launch_decode_heads(const LaunchArgs& a, cudaStream_t s) {
   const dim3 grid(a.G * nbl, a.nseq);
   constexpr size_t sm = heads_smem_bytes<T, P, N, QM>();
   const bool rssm = (a.flags & ERS_FLAG_REPLAYSSM) != 0;
-  // a fused ReplaySSM flush with one CTA per group: two launches (launch_parts)
-  const bool split = rssm && (a.flags & ERS_FLAG_FUSE_REFRESH) && nbl == 1;
+  // a fused refresh (exact mode) or flush (ReplaySSM) with one CTA per group: two launches
+  // (launch_parts), the slots whose step refreshes or flushes first
+  const bool split = (a.flags & ERS_FLAG_FUSE_REFRESH) && nbl == 1;
   auto run = [&](auto kernel) {
     cudaError_t e = prep(kernel, sm);
     if (e != cudaSuccess) return e;
