@@ -50,8 +50,8 @@ DECODE_SOURCES = [os.path.join(ROOT, "exact_replay_decode_gb300", "csrc", f)
 
 
 def profiled_traffic(profile: str = DECODE_PROFILE, sources=None):
-    """DRAM bytes per launch (dram__bytes_read.sum + dram__bytes_write.sum) from the committed ncu
-    summary, or None when the kernel's sources have changed since the capture (sha256 over the
+    """DRAM bytes per step (dram__bytes_read.sum + dram__bytes_write.sum of the step's launches) from the
+    committed ncu summary, or None when the kernel's sources have changed since the capture (sha256 over the
     concatenated files) or no record exists."""
     import hashlib
     import re
@@ -59,7 +59,7 @@ def profiled_traffic(profile: str = DECODE_PROFILE, sources=None):
     try:
         text = open(profile).read()
         want = re.search(r"kernel_source_sha256 = ([0-9a-f]{64})", text).group(1)
-        traffic = int(re.search(r"traffic_per_launch_bytes = (\d+)", text).group(1))
+        traffic = int(re.search(r"traffic_per_step_bytes = (\d+)", text).group(1))
         hsh = hashlib.sha256()
         for f in sources:
             hsh.update(open(f, "rb").read())

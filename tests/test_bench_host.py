@@ -100,7 +100,7 @@ def test_profiled_traffic_is_null_once_the_kernel_changed(tmp_path):
     src.write_text("kernel v1")
     prof = tmp_path / "p.md"
     h = hashlib.sha256(b"kernel v1").hexdigest()
-    prof.write_text(f"kernel_source_sha256 = {h}\ntraffic_per_launch_bytes = 1234\n")
+    prof.write_text(f"kernel_source_sha256 = {h}\ntraffic_per_step_bytes = 1234\n")
     assert bench.profiled_traffic(str(prof), [str(src)]) == 1234
     src.write_text("kernel v2")
     assert bench.profiled_traffic(str(prof), [str(src)]) is None
