@@ -36,11 +36,38 @@ using namespace wh;
 template <int QM>
 constexpr int heads_rows() { return QM + 1; }
 
+// The last region serves a step that fills or flushes the chunk as the per-warp w_s x_s[d] table and a
+// plain step with an NVFP4 copy as the heads' staged copy (P N / 2 code bytes + P N / 16 block-scale
+// bytes per warp), so it takes the larger of the two.
+template <int P, int N>
+constexpr size_t staged_bytes() { return (size_t)P * N / 2 + (size_t)P * N / 16; }
+template <int P, int N, int QM>
+constexpr size_t heads_table_bytes() {
+  return (size_t)kHeadsPerCta * ((size_t)QM * P * sizeof(float) > staged_bytes<P, N>() ? (size_t)QM * P * sizeof(float)
+                                                                                       : staged_bytes<P, N>());
+}
+
 template <typename T, int P, int N, int QM>
 constexpr size_t heads_smem_bytes() {
   return (size_t)heads_rows<QM>() * N * sizeof(T) + (size_t)kHeadsPerCta * heads_rows<QM>() * P * sizeof(T) +
-         QM * sizeof(float) + (size_t)kHeadsPerCta * (P + QM * P) * sizeof(float);
+         QM * sizeof(float) + (size_t)kHeadsPerCta * P * sizeof(float) + heads_table_bytes<P, N, QM>();
 }
+
+// A plain ReplaySSM step with an NVFP4 copy stages each head's whole copy (4 KB of codes + 512 B of
+// block scales) in shared memory with one burst of 16-byte copies, so that every byte of the CTA is
+// in flight at once (32 rows of 3 bytes per lane in registers kept too few bytes in flight), and
+// streams the rows from there.  (Staging the 8 KB FP8 copies measured slower: 83 against 72 us.)
+template <typename HT> constexpr bool kStaged = std::is_same<HT, Nvfp4>::value;
+
+template <typename HT, int N> struct RowSmem;
+template <int N> struct RowSmem<Nvfp4, N> {     // e2m1 codes (row d at c4 + d N / 2), block scales after them
+  const uint8_t* c4;
+  const uint8_t* bs;
+  __device__ __forceinline__ uint32_t ld(int d, int j) const {
+    const uint32_t c = *reinterpret_cast<const uint16_t*>(c4 + (size_t)d * (N / 2) + 2 * j);
+    return c | ((uint32_t)bs[(size_t)d * (N / 16) + (j >> 2)] << 16);
+  }
+};
 
 // Streams one head's state: lane j of row d reads elements [4j, 4j+4), 8 rows per block, with
 // rows_in_flight rows in flight (q holds the first of them on entry).  yo[d] ends with the
@@ -53,8 +80,8 @@ constexpr size_t heads_smem_bytes() {
 template <typename HT>
 constexpr int rows_in_flight() { return sizeof(typename RawOf<HT>::type) == 16 ? 16 : 32; }
 
-template <typename HT, int P, int N>
-__device__ __forceinline__ void stream_state(const RowSrc<HT, N>& src,
+template <typename HT, int P, int N, typename Src>
+__device__ __forceinline__ void stream_state(const Src& src,
                                              typename RawOf<HT>::type (&q)[rows_in_flight<HT>()],
                                              const float (&c)[4], float* yo, int j, const float (&sc)[2]) {
   constexpr int NBLK = P / 8, RIF = rows_in_flight<HT>();
@@ -318,7 +345,7 @@ __global__ void __launch_bounds__(kThreads, 2) k_decode_heads(LaunchArgs a) {
   float c[4];
   load_k<T, 4>((const T*)a.C + (size_t)i * GN + (size_t)g * N + 4 * j, c);
   typename RawOf<HT>::type q[rows_in_flight<HT>()];
-  if (active && a.part != kPartFlushes) {   // the first launch of a split call streams anchors only
+  if (!kStaged<HT> && active && a.part != kPartFlushes) {   // the first launch of a split call streams anchors only
 #pragma unroll
     for (int r = 0; r < rows_in_flight<HT>(); ++r) q[r] = src.ld(r, j);
   }
@@ -344,6 +371,15 @@ __global__ void __launch_bounds__(kThreads, 2) k_decode_heads(LaunchArgs a) {
       __syncthreads();   // every thread of the CTA has read the position
       if (tid == 0) advance_pos(&a.pos[slot], ncta, refresh ? 0 : 1);
       return;
+    }
+  }
+  uint8_t* stage = reinterpret_cast<uint8_t*>(swa) + (size_t)w * (heads_table_bytes<P, N, QM>() / kHeadsPerCta);
+  if constexpr (kStaged<HT>) {   // a plain step: the head's copy into shared memory, all at once
+    if (!flush && active) {
+      constexpr int kCodeBytes = P * N / 2;
+      const uint8_t* cg = (const uint8_t*)a.read_copy + soff / 2;
+      for (int k = j; k < kCodeBytes / 16; k += 32) cp_async16(stage + 16 * k, cg + 16 * k);
+      for (int k = j; k < P * N / 16 / 16; k += 32) cp_async16(stage + kCodeBytes + 16 * k, a.read_bscale + soff / 16 + 16 * k);
     }
   }
   const int o0 = flush ? p : 0, pn = p - o0;   // output rows s = 0..pn are smem rows o0 + s
@@ -445,6 +481,13 @@ __global__ void __launch_bounds__(kThreads, 2) k_decode_heads(LaunchArgs a) {
                                      a.read_bscale + soff / 16, a.read_scale + ((size_t)slot * a.H + h) * P, c[0],
                                      c[1], c[2], c[3], yo, j, p, wx, expf(last.hi), sB,
                                      SrCtr{a.sr_key0, a.sr_key1, a.sr_nonce, (uint32_t)slot}, (uint32_t)(h * P));
+  } else if constexpr (kStaged<HT>) {   // rows from the staged copy (landed before the last barrier)
+    RowSmem<HT, N> ss;
+    ss.c4 = stage;
+    ss.bs = stage + P * N / 2;
+#pragma unroll
+    for (int r = 0; r < rows_in_flight<HT>(); ++r) q[r] = ss.ld(r, j);
+    stream_state<HT, P, N>(ss, q, c, yo, j, sc);
   } else {
     stream_state<HT, P, N>(src, q, c, yo, j, sc);
   }
