@@ -498,6 +498,75 @@ def bench_verify(dev, steps: int, hbm: float, read_dtype: str = "bf16", anchor: 
             "warmup_steps": warm}
 
 
+def bench_verify_exact(dev, steps: int, hbm: float, T: int = 4):
+    """Exact-mode speculative verify + commit that keep the chunk grid (ers_spec_verify_exact /
+    ers_commit_exact) on the decode workload: 256 sequences with fp32 checkpoints, chunk 16, T
+    drafts per step, accepted ~ U{0..T}; 3 untimed steps, then `steps` timed ones.  Bytes: the
+    single-pass minimum of the method (each sequence's checkpoint read once, its buffered rows, the
+    drafts in and their outputs, the accepted drafts appended, a chunk fold's checkpoint write);
+    the kernels make about T + 1 passes (a shadow snapshot, T decode steps), so the fraction is low
+    by construction."""
+    import ctypes
+    import torch
+    import exact_replay_decode_gb300 as ers
+    from exact_replay_decode_gb300 import _abi
+    from synth import torch_io
+    w = synth.workload("decode_b256_h64")
+    d = w.dims
+    S, Q = w.batch, d.chunk
+    warm = VERIFY_WARMUP
+    K = steps + warm
+    params, hist, p0, stream = synth.decode_inputs(w, seed=5, batch=S, steps=K * T)
+    A, D, dtb = torch_io.params_to(params, dev)
+    prm = ers.LayerParams(A, D, dtb)
+    cu = torch.tensor(np.concatenate([[0], np.cumsum([h.ntokens for h in hist])]), dtype=torch.int32, device=dev)
+    hx, hdt, hB, hC = torch_io.tokens_to(synth.Tokens.concat(hist), dev)
+    cache = ers.ReplayCache(S, d.nheads, d.ngroups, d.headdim, d.dstate, Q, torch.bfloat16)
+    ers.chunked_prefill(cache, prm, hx, hdt, hB, hC, cu)
+    del hx, hdt, hB, hC
+    drafts = [t.transpose(1, 2).contiguous() for t in torch_io.tokens_to(stream, dev, lead=(K, T, S))]
+    acc = np.random.Generator(np.random.PCG64(6)).integers(0, T + 1, size=(K, S)).astype(np.int32)
+    acc_t = torch.from_numpy(acc).to(dev)
+    ws = torch.empty(_abi.lib().ers_spec_verify_exact_workspace_size(ctypes.byref(cache.dims), S), dtype=torch.uint8,
+                     device=dev)
+    y = torch.empty(S, T, d.nheads, d.headdim, dtype=torch.bfloat16, device=dev)
+    st = ers.Status(dev)
+    state_bytes = d.nheads * d.headdim * d.dstate * 4
+    hs = p0.astype(np.int64)
+    total = 0
+    for k in range(K):
+        b = S * (state_bytes + T * (12_544 + 8_192)) + int(hs.sum()) * 10_496 + int(acc[k].sum()) * 12_544
+        b += int(((hs + acc[k]) >= Q).sum()) * state_bytes          # a filled chunk's checkpoint write
+        if k >= warm:
+            total += b
+        hs = (hs + acc[k]) % Q
+
+    def step(k):
+        dx, ddt, dB, dC = (t[k] for t in drafts)
+        ers.spec_verify_exact(cache, prm, dx, ddt, dB, dC, status=st, check=False, out=y, workspace=ws)
+        ers.commit_exact(cache, prm, acc_t[k], dx, ddt, dB, dC, status=st, check=False, workspace=ws)
+
+    for k in range(warm):
+        step(k)
+    torch.cuda.synchronize()
+    s = torch.cuda.current_stream()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(s)
+    for k in range(warm, K):
+        step(k)
+    e1.record(s)
+    torch.cuda.synchronize()
+    st.raise_if_error("bench exact verify")
+    if not np.array_equal(cache.pos.cpu().numpy(), hs.astype(np.int32)):
+        raise AssertionError("exact verify bench: positions differ from the byte model")
+    ms = e0.elapsed_time(e1)
+    ach = total / (ms * 1e-3) / 1e9
+    return {"drafts": T, "seq_verify_steps_per_s": S * steps / (ms * 1e-3),
+            "committed_tok_per_s": float(acc[warm:].sum()) / (ms * 1e-3), "us_per_step": ms * 1e3 / steps,
+            "achieved_gbs": ach, "hbm_frac": ach / hbm, "single_pass_bytes": total, "steps": steps,
+            "warmup_steps": warm}
+
+
 def _anchor_bytes(d, anchor: str) -> int:
     """Bytes of one sequence's separate anchor: fp32 or fp16 (none for the shared NVFP4 state)."""
     if anchor == "nvfp4_sr_shared":
@@ -893,7 +962,7 @@ def main(argv=None):
     ap.add_argument("--decode-only", action="store_true", help="only the headline decode measurement")
     ap.add_argument("--batch", type=int, default=None,
                     help="decode (or, with --section gdn, GDN) sequences per GPU (profiling runs only)")
-    ap.add_argument("--section", choices=["prefill", "verify", "rssm", "ssu", "conv", "gdn"], default=None,
+    ap.add_argument("--section", choices=["prefill", "verify", "rssm", "ssu", "conv", "gdn", "exact"], default=None,
                     help="run only this secondary workload and print its JSON (profiling aid, no headline)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
@@ -916,6 +985,8 @@ def main(argv=None):
             out = bench_conv(dev, hbm)
         elif args.section == "gdn":
             out = bench_gdn_verify(dev, 32, hbm, args.batch)
+        elif args.section == "exact":
+            out = bench_verify_exact(dev, 32, hbm)
         elif args.section == "rssm":
             out = {r: bench_rssm_decode(dev, 4, hbm, r) for r in ("bf16", "fp8", "nvfp4")}
             out["nvfp4_fp16sr"] = bench_rssm_decode(dev, 4, hbm, "nvfp4", "fp16_sr")
@@ -963,6 +1034,7 @@ def main(argv=None):
         extra["ssu"] = bench_ssu(dev, 16, hbm)
         extra["conv1d"] = bench_conv(dev, hbm)
         extra["gdn_verify"] = bench_gdn_verify(dev, 32, hbm)
+        extra["verify_exact"] = bench_verify_exact(dev, 32, hbm)
     line = {
         "metric": "replay-decode seq-steps/s per layer @B=256",
         "value": value,
