@@ -489,6 +489,12 @@ ers_status ers_spec_verify_exact(const ers_dims* dims, const ers_params* prm, co
   a.nseq = nseq;
   a.T = T;
   a.status = dev_status;
+  if (ers::exact_verify_supported(a.io, a.P, a.N, a.Q, T, a.H, a.G) && !ers::tc_supported(a.io, a.P, a.N, a.Q)) {
+    // one pass over the checkpoints (the workspace is not used)
+    a.x = x; a.dt = dt; a.B = B; a.C = C;
+    a.y = y;
+    return finish(ers::exact_verify(a, s));
+  }
   cudaError_t e = ers::launch_spec_snapshot(a, (float*)(ws + w.st), ws + w.bx, (float*)(ws + w.bdt), ws + w.bB,
                                             ws + w.bC, (int32_t*)(ws + w.pos), s);
   if (e != cudaSuccess) return finish(e);

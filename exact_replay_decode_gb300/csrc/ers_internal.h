@@ -92,6 +92,10 @@ cudaError_t heads_decode(const LaunchArgs& a, cudaStream_t s);
 cudaError_t heads_refresh(const LaunchArgs& a, cudaStream_t s);
 // warp-per-head speculative verify (chunk <= 16, P = 64, N = 128, T <= 4, H/G <= 8), ers_verify.cu
 bool heads_verify_supported(int P, int N, int Q, int T, int H, int G);
+// exact-mode speculative verify in one pass over the checkpoints (chunk <= 16, P = 64, N = 128,
+// T <= 4, H/G <= 8; the chunk fold of drafts past the boundary formed row by row), ers_verify.cu
+bool exact_verify_supported(int io, int P, int N, int Q, int T, int H, int G);
+cudaError_t exact_verify(const LaunchArgs& a, cudaStream_t s);
 cudaError_t heads_verify(const LaunchArgs& a, cudaStream_t s);
 
 // ReplaySSM decode (T = 1, position advance, fused flush) and verify of T <= L drafts with the read

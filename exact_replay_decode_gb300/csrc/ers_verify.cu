@@ -361,11 +361,227 @@ cudaError_t launch_verify_heads(const LaunchArgs& a, cudaStream_t s) {
   return cudaGetLastError();
 }
 
+// ---- exact-mode speculative verify in one pass (exact-replay RFC, sections 3 and 6) ----------------
+// Drafts at chunk positions hc + k.  A draft before the chunk end takes its output from the fp32
+// checkpoint H and the replay of the chunk's rows up to it, exactly as an exact-mode decode step at
+// that position does.  When the drafts run past the chunk end (hc + T > Q), the first kb = Q - hc of
+// them complete the chunk, and a later draft takes its output from the checkpoint H' that the chunk
+// fold of exact decode would write (fold_state over the Q rows: the committed records and the
+// completing drafts), with the replay restarting at the new chunk.  H' is formed row by row from H as
+// the rows stream and feeds the later drafts' dot products; nothing is written, so the cache keeps
+// its state.  Every operation is exact decode's (scans, Gram rows, the Dot<128> pairings, the fold
+// order, combine_out), so each output has the bits of the decode step it stands for.
+
+// The fold stream: H rows and, per 8 rows, the chunk fold H' = fma(decay, H, sum_s w_s x_s[d] B_s) over
+// the Q rows; draft k < kb dots H, draft k >= kb dots H' (yo as in stream_read_copy).
+// The chunk's row s (committed rows s < hc, then the completing drafts) is smem row s or QM + s - hc.
+template <typename T, int P, int N, int QM>
+__device__ __noinline__ void stream_exact_fold(const float* __restrict__ Hd, const float (&c)[kDraftsMax][4],
+                                               float* yo, int j, int hc, int kb, const float* wx, float decay,
+                                               const T* sB) {
+  const int q = hc + kb;
+#pragma unroll 1
+  for (int d0 = 0; d0 < P; d0 += 8) {
+    float h[8][4];
+    Fold4 acc[2];   // rows d0..d0+3, d0+4..d0+7
+#pragma unroll
+    for (int r = 0; r < 8; ++r) Quad<float>::unpack(Quad<float>::ld_stream(Hd + (size_t)(d0 + r) * N + 4 * j), h[r]);
+    acc[0].zero();
+    acc[1].zero();
+    for (int s = 0; s < q; ++s) {
+      float bs[4];
+      lds4(sB + (s < hc ? s : QM + s - hc) * N + 4 * j, bs);
+      acc[0].add(*reinterpret_cast<const float4*>(wx + s * P + d0), bs);
+      acc[1].add(*reinterpret_cast<const float4*>(wx + s * P + d0 + 4), bs);
+    }
+    float part[32];
+#pragma unroll
+    for (int r = 0; r < 8; ++r) {
+      float v[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) v[e] = __fmaf_rn(decay, h[r][e], acc[r >> 2].get(r & 3, e));
+#pragma unroll
+      for (int k = 0; k < kDraftsMax; ++k) part[k * 8 + r] = Dot<N>::partial(c[k], k < kb ? h[r] : v);
+    }
+    yo[(j >> 3) * P + d0 + (j & 7)] = reduce_scatter32(part, j);
+  }
+  __syncwarp();
+}
+
+template <typename T, int P, int N, int QM>
+__global__ void __launch_bounds__(kThreads, 2) k_verify_exact_heads(LaunchArgs a) {
+  static_assert(N == 128 && P % 8 == 0 && QM <= 32 - kDraftsMax, "lane split of Dot<128>; one warp scans");
+  constexpr int QR = QM + kDraftsMax;
+  extern __shared__ __align__(16) unsigned char vsm[];
+  T* sB = reinterpret_cast<T*>(vsm);                                   // [QR] rows: committed, then drafts at QM
+  T* sxa = sB + QR * N;                                                // [warp][QR][P]
+  float* sg = reinterpret_cast<float*>(sxa + kHeadsPerCta * QR * P);   // [draft][QR] Gram rows
+  float* syo = sg + kDraftsMax * QR;                                   // [warp][draft][P]
+  float* swa = syo + kHeadsPerCta * kDraftsMax * P;                    // [warp][QM][P] w_s x_s[d]
+  const int tid = threadIdx.x, w = tid >> 5, j = tid & 31;
+  const int i = blockIdx.y, g = blockIdx.x;
+  const int hpg = a.H / a.G;
+  const bool active = w < hpg;
+  const int h = g * hpg + (active ? w : 0);
+  const int Td = a.T;
+  int slot;
+  if (!resolve_slot(a, i, &slot)) return;
+  const int hc = a.pos[slot];
+  if (hc < 0 || hc >= a.Q) {   // an exact-mode position is in [0, Q)
+    if (tid == 0) report(a.status, ERS_EALIGN);
+    return;
+  }
+  const int kb = min(Td, a.Q - hc);   // drafts up to the chunk end
+  const bool cross = kb < Td;         // later drafts see the folded checkpoint
+  const size_t HP = (size_t)a.H * P, GN = (size_t)a.G * N;
+  const size_t soff = ((size_t)slot * a.H + h) * P * N;
+  RowSrc<float, N> src;
+  src.p = a.state + soff;
+  float c[kDraftsMax][4];
+#pragma unroll
+  for (int k = 0; k < kDraftsMax; ++k) {
+    if (k < Td) {
+      load_k<T, 4>((const T*)a.C + ((size_t)i * Td + k) * GN + (size_t)g * N + 4 * j, c[k]);
+    } else {
+#pragma unroll
+      for (int e = 0; e < 4; ++e) c[k][e] = 0.f;
+    }
+  }
+  typename RawOf<float>::type qr[kVerifyRowsInFlight];
+  if (!cross && active) {
+#pragma unroll
+    for (int r = 0; r < kVerifyRowsInFlight; ++r) qr[r] = src.ld(r, j);
+  }
+  // committed rows 0..hc-1 at smem rows 0..hc-1, drafts at rows QM..QM+T-1
+  const T* bB = (const T*)a.bB + (size_t)g * N;
+  constexpr int kBChunks = N * sizeof(T) / 16, kXChunks = P * sizeof(T) / 16;
+  for (int k = tid; k < (hc + Td) * kBChunks; k += kThreads) {
+    const int r = k / kBChunks, e = k % kBChunks;
+    const T* s = r < hc ? bB + buf_row(a, slot, r) * GN : (const T*)a.B + ((size_t)i * Td + (r - hc)) * GN + (size_t)g * N;
+    cp_async16(reinterpret_cast<char*>(sB + (r < hc ? r : QM + r - hc) * N) + 16 * e, reinterpret_cast<const char*>(s) + 16 * e);
+  }
+  T* sx = sxa + w * QR * P;
+  if (active) {
+    const T* bx = (const T*)a.bx + (size_t)h * P;
+    for (int k = j; k < (hc + Td) * kXChunks; k += 32) {
+      const int r = k / kXChunks, e = k % kXChunks;
+      const T* s = r < hc ? bx + buf_row(a, slot, r) * HP : (const T*)a.x + ((size_t)i * Td + (r - hc)) * HP + (size_t)h * P;
+      cp_async16(reinterpret_cast<char*>(sx + (r < hc ? r : QM + r - hc) * P) + 16 * e, reinterpret_cast<const char*>(s) + 16 * e);
+    }
+  }
+  const float dt_c = j < hc ? a.bdt[buf_row(a, slot, j) * a.H + h] : 0.f;
+  const float dt_d = j < Td ? a.dt[((size_t)i * Td + j) * a.H + h] : 0.f;
+  const float Ah = a.A[h], bias = a.dt_bias[h];
+  // the old chunk's rows (lane s: committed s < hc, then the completing drafts) and the new chunk's
+  // (lane s: draft kb + s); their decay terms and prefix scans, as exact decode builds them
+  const float dt_sh = __shfl_sync(kFull, dt_d, max(j - hc, 0) & 31);   // every lane shuffles
+  const float dt_new = __shfl_sync(kFull, dt_d, (kb + j) & 31);
+  const float dt_old = j < hc ? dt_c : dt_sh;
+  float dlo = 0.f, dln = 0.f;
+  df vo = {0.f, 0.f}, vn = {0.f, 0.f};
+  if (j < hc + kb) {
+    dlo = delta_of(dt_old, bias);
+    vo.hi = __fmul_rn(dlo, Ah);
+  }
+  if (j < Td - kb) {
+    dln = delta_of(dt_new, bias);
+    vn.hi = __fmul_rn(dln, Ah);
+  }
+  vo = warp_scan_df(vo, j);
+  vn = warp_scan_df(vn, j);
+  cp_async_wait_all();
+  __syncthreads();
+  // Gram rows: a draft before the chunk end against the old chunk's rows s <= hc + k, a later one
+  // against the new chunk's rows s <= k - kb (smem row of new-chunk row s: QM + kb + s)
+  for (int k = 0; k < Td; ++k) {
+    const int last = k < kb ? hc + k : k - kb;
+    for (int s = w; s <= last; s += kHeadsPerCta) {
+      const int row = k < kb ? (s < hc ? s : QM + s - hc) : QM + kb + s;
+      float bs[4];
+      lds4(sB + row * N + 4 * j, bs);
+      const float gv = Dot<N>::reduce(Dot<N>::partial(c[k], bs));
+      if (j == 0) sg[k * QR + s] = gv;
+    }
+  }
+  // the chunk fold's w_s x_s[d] over the Q rows (state_weights with the old chunk's last prefix)
+  float* sw = swa + w * QM * P;
+  float decay = 0.f;
+  if (cross) {
+    const int q = hc + kb;   // = Q
+    const df last = {__shfl_sync(kFull, vo.hi, q - 1), __shfl_sync(kFull, vo.lo, q - 1)};
+    const float wl = j < q ? __fmul_rn(dlo, expf(df_diff(last, vo))) : 0.f;
+    decay = expf(last.hi);
+    for (int s = 0; s < q; ++s) {
+      const float ws = __shfl_sync(kFull, wl, s);
+      const T* xr = sx + (s < hc ? s : QM + s - hc) * P;
+#pragma unroll
+      for (int m = 0; m < P / 32; ++m) sw[s * P + 32 * m + j] = __fmul_rn(ws, to_f(xr[32 * m + j]));
+    }
+    __syncwarp();
+  }
+  __syncthreads();
+  if (!active) return;
+  float* yo = syo + w * kDraftsMax * P;
+  if (cross) {
+    stream_exact_fold<T, P, N, QM>(a.state + soff, c, yo, j, hc, kb, sw, decay, sB);
+  } else {
+    const float sc[2] = {1.f, 1.f};
+    stream_read_copy<float, P, N>(src, qr, c, yo, j, sc);
+  }
+  // outputs of draft k at d = j + 32 m
+  const float Dh = a.D[h];
+  constexpr int DPL = P / 32;
+  for (int k = 0; k < Td; ++k) {
+    const bool pre = k < kb;
+    const int t = pre ? hc + k : k - kb;
+    const df vv = pre ? vo : vn;
+    const float dl = pre ? dlo : dln;
+    const df at = {__shfl_sync(kFull, vv.hi, t), __shfl_sync(kFull, vv.lo, t)};
+    const float M = j <= t ? __fmul_rn(__fmul_rn(sg[k * QR + j], dl), expf(df_diff(at, vv))) : 0.f;
+    float acc[DPL];
+#pragma unroll
+    for (int m = 0; m < DPL; ++m) acc[m] = 0.f;
+    for (int s = 0; s <= t; ++s) {
+      const float Ms = __shfl_sync(kFull, M, s);
+      const T* xr = sx + (pre ? (s < hc ? s : QM + s - hc) : QM + kb + s) * P;
+#pragma unroll
+      for (int m = 0; m < DPL; ++m) acc[m] = __fmaf_rn(Ms, to_f(xr[32 * m + j]), acc[m]);
+    }
+    const float et = expf(at.hi);
+    T* y = (T*)a.y + ((size_t)i * Td + k) * HP + (size_t)h * P;
+#pragma unroll
+    for (int m = 0; m < DPL; ++m) {
+      const int d = 32 * m + j;
+      y[d] = from_f<T>(combine_out(et, yo[k * P + d], acc[m], Dh, to_f(sx[(QM + k) * P + d])));
+    }
+  }
+}
+
+template <typename T, int QM>
+cudaError_t launch_verify_exact_heads(const LaunchArgs& a, cudaStream_t s) {
+  constexpr int P = 64, N = 128;
+  constexpr size_t sm = verify_smem_bytes<T, P, N, QM>();
+  cudaError_t e = prep(k_verify_exact_heads<T, P, N, QM>, sm);
+  if (e != cudaSuccess) return e;
+  k_verify_exact_heads<T, P, N, QM><<<dim3(a.G, a.nseq), kThreads, sm, s>>>(a);
+  return cudaGetLastError();
+}
+
 }  // namespace
 
 bool heads_verify_supported(int P, int N, int Q, int T, int H, int G) {
   return P == 64 && N == 128 && Q >= 1 && Q <= 16 && T >= 1 && T <= kDraftsMax && G > 0 && H % G == 0 &&
          H / G <= kHeadsPerCta;
+}
+
+bool exact_verify_supported(int io, int P, int N, int Q, int T, int H, int G) {
+  return (io == ERS_DTYPE_BF16 || io == ERS_DTYPE_F32) && P == 64 && N == 128 && Q >= 1 && Q <= 16 && T >= 1 &&
+         T <= kDraftsMax && G > 0 && H % G == 0 && H / G <= kHeadsPerCta;
+}
+
+cudaError_t exact_verify(const LaunchArgs& a, cudaStream_t s) {
+  if (a.io == ERS_DTYPE_BF16) return launch_verify_exact_heads<__nv_bfloat16, 16>(a, s);
+  return launch_verify_exact_heads<float, 16>(a, s);
 }
 
 cudaError_t heads_verify(const LaunchArgs& a, cudaStream_t s) {

@@ -325,10 +325,13 @@ ERS_API ers_status ers_commit(const ers_dims* dims, const ers_cache* cache, int3
  * ers_spec_verify_exact: T drafts per sequence, 1 <= T <= Q: x [nseq, T, H, P], dt [nseq, T, H] raw,
  *   B/C [nseq, T, G, N]; y [nseq, T, H, P] (out).  Draft j's output is, bit for bit, the output
  *   ers_replay_decode (exact mode, ERS_FLAG_FUSE_REFRESH) gives draft j after drafts 0 .. j-1 were
- *   decoded, crossing the chunk boundary where they reach it.  The cache is not changed: the call
- *   copies the slots' checkpoints, buffered rows and positions into `workspace`
- *   (ers_spec_verify_exact_workspace_size(dims, nseq) bytes, about an fp32 state and a buffer per
- *   sequence) and decodes the drafts there one at a time (T decode launches and their row copies).
+ *   decoded, crossing the chunk boundary where they reach it.  The cache is not changed.  With
+ *   Q <= 16, T <= 4, P = 64, N = 128 and at most 8 heads per group the call is one launch that
+ *   streams each checkpoint once and forms the folded boundary state row by row for the drafts past
+ *   it (`workspace` is not touched); otherwise it copies the slots' checkpoints, buffered rows and
+ *   positions into `workspace` (ers_spec_verify_exact_workspace_size(dims, nseq) bytes, about an
+ *   fp32 state and a buffer per sequence) and decodes the drafts there one at a time (T decode
+ *   launches and their row copies).  The workspace is required in both cases.
  *   Requires an fp32 checkpoint (ERS_ANCHOR_F32; read copies, if any, are neither read nor written)
  *   and 0 <= pos < Q.
  * ers_commit_exact: after a verify, the first accepted[i] (0 <= accepted[i] <= T, device int32 [nseq])
