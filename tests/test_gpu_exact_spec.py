@@ -34,7 +34,8 @@ def _caches(w, S, KT, seed, n):
     hx, hdt, hB, hC = torch_io.tokens_to(synth.Tokens.concat(hist), dev())
     caches = []
     for _ in range(n):
-        c = ers.ReplayCache(S, d.nheads, d.ngroups, d.headdim, d.dstate, d.chunk, torch.bfloat16)
+        c = ers.ReplayCache(S, d.nheads, d.ngroups, d.headdim, d.dstate, d.chunk,
+                            torch.bfloat16 if w.bf16 else torch.float32)
         ers.chunked_prefill(c, prm, hx, hdt, hB, hC, cu)
         caches.append(c)
     return params, prm, hist, p0, stream, caches
@@ -73,12 +74,13 @@ def _decode_accepted(ers, c, prm, dr, acc, T):
     return outs
 
 
-@pytest.mark.parametrize("dims,T", [(synth.Dims(64, 8, 64, 128, 16), 4), (synth.Dims(64, 8, 64, 128, 16), 16),
-                                    (synth.Dims(16, 2, 64, 128, 64), 4)],
-                         ids=["chunk16-T4", "chunk16-T16", "tensor-core-chunk64-T4"])
-def test_verify_equals_decode_and_commit_equals_decode(dims, T):
+@pytest.mark.parametrize("dims,T,bf16", [(synth.Dims(64, 8, 64, 128, 16), 4, True), (synth.Dims(64, 8, 64, 128, 16), 16, True),
+                                         (synth.Dims(16, 2, 64, 128, 64), 4, True), (synth.Dims(12, 3, 64, 128, 16), 3, True),
+                                         (synth.Dims(16, 2, 64, 128, 16), 4, False)],
+                         ids=["chunk16-T4", "chunk16-T16", "tensor-core-chunk64-T4", "chunk16-T3-4heads", "chunk16-T4-fp32"])
+def test_verify_equals_decode_and_commit_equals_decode(dims, T, bf16):
     ers = _ers()
-    w = dataclasses.replace(synth.workload("decode_b256_h64"), dims=dims)
+    w = dataclasses.replace(synth.workload("decode_b256_h64"), dims=dims, bf16=bf16)
     Q = dims.chunk
     S = 40
     params, prm, hist, p0, stream, (c_spec, c_dec, c_ref) = _caches(w, S, T, 61, 3)

@@ -135,3 +135,15 @@ def test_verify_fp32_io_wide_groups_and_long_drafts(heads, groups, bf16, drafts)
     base = synth.workload("verify_b512_t4")
     w = dataclasses.replace(base, dims=synth.Dims(heads, groups, 64, 128, 16), bf16=bf16, drafts=drafts)
     _verify_vs_nonspec(w, 8, 24, 4, [0, 7])
+
+
+@pytest.mark.parametrize("heads,groups", [(8, 2), (12, 2), (3, 3)])
+def test_verify_tensor_core_partial_head_blocks(heads, groups):
+    """ReplaySSM verify and decode on the tensor-core kernel with fewer than 8 heads per group: one
+    operand chain of 4 heads, a second chain whose box reaches past the group (6 heads), one head per
+    group; bitwise against non-speculative decode and within tolerance of the protocol model."""
+    import dataclasses
+    base = synth.workload("verify_b512_t4")
+    w = dataclasses.replace(base, dims=synth.Dims(heads, groups, 64, 128, 16))
+    _verify_vs_nonspec(w, 8, 24, 5, [0, 7])
+
