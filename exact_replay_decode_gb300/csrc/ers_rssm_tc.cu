@@ -257,12 +257,9 @@ __device__ __forceinline__ void rows_ready(RsmSmem& sm, int r, int j) {
 // decode != 0: one token per sequence (Td = 1) with the position advance (and, with
 // ERS_FLAG_FUSE_REFRESH, the flush of a full buffer); else a verify of Td drafts (pointers unchanged;
 // ERS_FLAG_AUTO_FLUSH allows flushes).
-// part: kAll, or a call split in two launches so that the long flushing CTAs run alongside the plain
-// ones instead of after them: kFlushes (the flushing slots; reads the positions, lets the dependent
-// launch start, writes no position) then kPlain (launched as its programmatic dependent: the plain
-// slots, and every position advance; its last CTA waits for the first launch, so the pair completes
-// together).
-enum RsmPart : int { kAll = 0, kFlushes = 1, kPlain = 2 };
+// part: kPartAll, or one of the two launches of a call that may flush (kPartFlushes, then kPartPlain
+// as its programmatic dependent; ers_internal.h), so that the long flushing CTAs run alongside the
+// plain ones instead of after them.
 
 template <typename AT>
 __global__ void __maxnreg__(96)
@@ -298,12 +295,11 @@ __global__ void __maxnreg__(96)
       return;
     }
   }
-  if (part == kFlushes) {
-    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");   // this CTA has read its position
+  if (part == kPartFlushes) {
+    allow_dependents();   // this CTA has read its position
     if (!flush) return;
-  } else if (part == kPlain) {
-    if (blockIdx.x == gridDim.x - 1 && blockIdx.y == gridDim.y - 1)
-      asm volatile("griddepcontrol.wait;" ::: "memory");   // completes only after the flushing launch
+  } else if (part == kPartPlain) {
+    if (last_cta_of_grid()) wait_primary();   // completes only after the flushing launch
     if (flush) {   // done by the first launch; a decode still counts the slot's CTAs here
       __syncthreads();   // every thread of the CTA has read the position
       if (decode && tid == 0) count_and_advance(&a.pos[slot], a.G, 1);
@@ -371,7 +367,7 @@ __global__ void __maxnreg__(96)
     if (j == 0) issuer(sm, &map, tma, nchains, head0, a.status, lim);
     __syncwarp();
   } else {
-    if (decode && part != kFlushes && tid == 0) count_and_advance(&a.pos[slot], a.G, h0 + 1);   // pos read by all
+    if (decode && part != kPartFlushes && tid == 0) count_and_advance(&a.pos[slot], a.G, h0 + 1);   // pos read by all
     // output rows s < h0 + Td: committed rows, then the drafts; lane s holds row s
     const int nout = h0 + Td;
     const float dt_o_d = __shfl_sync(kFull, dt_d, max(j - h0, 0) & 31);
@@ -479,10 +475,10 @@ cudaError_t launch_rssm(const LaunchArgs& a, const CUtensorMap& map, int T, bool
   const dim3 grid(a.G, a.nseq);
   const int dec = decode ? 1 : 0;
   if (!split) {
-    k<<<grid, kRThreads, sm, s>>>(a, map, T, dec, (int)kAll);
+    k<<<grid, kRThreads, sm, s>>>(a, map, T, dec, (int)kPartAll);
     return cudaGetLastError();
   }
-  k<<<grid, kRThreads, sm, s>>>(a, map, T, dec, (int)kFlushes);
+  k<<<grid, kRThreads, sm, s>>>(a, map, T, dec, (int)kPartFlushes);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = grid;
@@ -494,7 +490,7 @@ cudaError_t launch_rssm(const LaunchArgs& a, const CUtensorMap& map, int T, bool
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, k, a, map, T, dec, (int)kPlain);
+  return cudaLaunchKernelEx(&cfg, k, a, map, T, dec, (int)kPartPlain);
 }
 
 }  // namespace
