@@ -541,30 +541,36 @@ def bench_verify_exact(dev, steps: int, hbm: float, T: int = 4):
             total += b
         hs = (hs + acc[k]) % Q
 
-    def step(k):
+    def step(k, mid=None):
         dx, ddt, dB, dC = (t[k] for t in drafts)
         ers.spec_verify_exact(cache, prm, dx, ddt, dB, dC, status=st, check=False, out=y, workspace=ws)
+        if mid is not None:
+            mid.record(torch.cuda.current_stream())
         ers.commit_exact(cache, prm, acc_t[k], dx, ddt, dB, dC, status=st, check=False, workspace=ws)
 
     for k in range(warm):
         step(k)
     torch.cuda.synchronize()
     s = torch.cuda.current_stream()
+    # events at every step's start and after its verify: the step and its verify share
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(s)
-    for k in range(warm, K):
-        step(k)
+    for n, k in enumerate(range(warm, K)):
+        ev[n][0].record(s)
+        step(k, ev[n][1])
     e1.record(s)
     torch.cuda.synchronize()
     st.raise_if_error("bench exact verify")
+    verify_ms = sum(a.elapsed_time(b) for a, b in ev)
     if not np.array_equal(cache.pos.cpu().numpy(), hs.astype(np.int32)):
         raise AssertionError("exact verify bench: positions differ from the byte model")
     ms = e0.elapsed_time(e1)
     ach = total / (ms * 1e-3) / 1e9
     return {"drafts": T, "seq_verify_steps_per_s": S * steps / (ms * 1e-3),
             "committed_tok_per_s": float(acc[warm:].sum()) / (ms * 1e-3), "us_per_step": ms * 1e3 / steps,
-            "achieved_gbs": ach, "hbm_frac": ach / hbm, "single_pass_bytes": total, "steps": steps,
-            "warmup_steps": warm}
+            "verify_us_per_step": verify_ms * 1e3 / steps, "achieved_gbs": ach, "hbm_frac": ach / hbm,
+            "single_pass_bytes": total, "steps": steps, "warmup_steps": warm}
 
 
 def _anchor_bytes(d, anchor: str) -> int:

@@ -633,6 +633,50 @@ __device__ __forceinline__ void copy_elems(void* dst, const void* src, int n, in
   }
 }
 
+// Draft rows j0 .. j0+n-1 of sequence i (token rows i T + j of x, B, C; dt as floats) into buffer rows
+// r0 .. r0+n-1 of its slot.  The x, B and C rows move as 16-byte words (their sizes are multiples of
+// 16 bytes: P = 64 or N = 128 io elements per head or group), each thread loading all of its words
+// before storing any, so that a CTA's copies overlap instead of waiting one round trip each; dt
+// (H floats a row) moves as floats.
+__device__ __forceinline__ void copy_draft_rows(const LaunchArgs& a, int i, int slot, int j0, int n, int r0) {
+  const int es = a.io == ERS_DTYPE_BF16 ? 2 : 4;
+  const long long HP = (long long)a.H * a.P, GN = (long long)a.G * a.N;
+  const int xw = (int)(HP * es / 16), gw = (int)(GN * es / 16), per = xw + 2 * gw, W = n * per;
+  constexpr int kBatch = 8;
+  for (int base = threadIdx.x; base < W; base += kBatch * blockDim.x) {
+    uint4 v[kBatch];
+    uint4* dst[kBatch];
+#pragma unroll
+    for (int u = 0; u < kBatch; ++u) {
+      const int wi = base + u * blockDim.x;
+      dst[u] = nullptr;
+      if (wi < W) {
+        const int r = wi / per, o = wi % per;
+        const long long tok = (long long)i * a.T + j0 + r, br = buf_row(a, slot, r0 + r);
+        const uint4* src;
+        if (o < xw) {
+          src = (const uint4*)((const char*)a.x + tok * HP * es) + o;
+          dst[u] = (uint4*)((char*)a.bx + br * HP * es) + o;
+        } else if (o < xw + gw) {
+          src = (const uint4*)((const char*)a.B + tok * GN * es) + (o - xw);
+          dst[u] = (uint4*)((char*)a.bB + br * GN * es) + (o - xw);
+        } else {
+          src = (const uint4*)((const char*)a.C + tok * GN * es) + (o - xw - gw);
+          dst[u] = (uint4*)((char*)a.bC + br * GN * es) + (o - xw - gw);
+        }
+        v[u] = __ldg(src);
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < kBatch; ++u)
+      if (dst[u] != nullptr) *dst[u] = v[u];
+  }
+  for (int e = threadIdx.x; e < n * a.H; e += blockDim.x) {
+    const int r = e / a.H, k = e % a.H;
+    a.bdt[buf_row(a, slot, r0 + r) * a.H + k] = a.dt[((long long)i * a.T + j0 + r) * a.H + k];
+  }
+}
+
 // Shadow of sequence i's slot (blockIdx.y = i, blockIdx.x = head): its fp32 checkpoint head, its
 // buffered rows [0, pos) (x, dt of the head; B, C of group h when h < G) in the contiguous layout,
 // its position.  `a` describes the real cache; sh_* the shadow (slot i, Q rows per slot).
@@ -714,16 +758,8 @@ __global__ void k_commit_exact_fill(LaunchArgs a, int32_t* old_pos) {
     if (threadIdx.x == 0) report(a.status, ERS_ECOMMIT);
     return;
   }
-  const int es = a.io == ERS_DTYPE_BF16 ? 2 : 4;
-  const long long HP = (long long)a.H * a.P, GN = (long long)a.G * a.N;
   const int end = p + acc < a.Q ? p + acc : a.Q;
-  for (int r = p; r < end; ++r) {
-    const long long br = buf_row(a, slot, r), row = (long long)i * a.T + (r - p);
-    copy_elems((char*)a.bx + br * HP * es, (const char*)a.x + row * HP * es, (int)HP, es, threadIdx.x, blockDim.x);
-    for (int k = threadIdx.x; k < a.H; k += blockDim.x) a.bdt[br * a.H + k] = a.dt[row * a.H + k];
-    copy_elems((char*)a.bB + br * GN * es, (const char*)a.B + row * GN * es, (int)GN, es, threadIdx.x, blockDim.x);
-    copy_elems((char*)a.bC + br * GN * es, (const char*)a.C + row * GN * es, (int)GN, es, threadIdx.x, blockDim.x);
-  }
+  copy_draft_rows(a, i, slot, 0, end - p, p);   // drafts 0 .. end-p-1 into rows p .. end-1
   __syncthreads();
   if (threadIdx.x == 0) {
     old_pos[i] = p;
@@ -740,16 +776,8 @@ __global__ void k_commit_exact_tail(LaunchArgs a, const int32_t* old_pos) {
   const int slot = a.slot != nullptr ? a.slot[i] : i;
   const int acc = a.accepted[i];
   if (p + acc < a.Q) return;
-  const int es = a.io == ERS_DTYPE_BF16 ? 2 : 4;
-  const long long HP = (long long)a.H * a.P, GN = (long long)a.G * a.N;
   const int n2 = p + acc - a.Q;
-  for (int r = 0; r < n2; ++r) {
-    const long long br = buf_row(a, slot, r), row = (long long)i * a.T + (a.Q - p + r);
-    copy_elems((char*)a.bx + br * HP * es, (const char*)a.x + row * HP * es, (int)HP, es, threadIdx.x, blockDim.x);
-    for (int k = threadIdx.x; k < a.H; k += blockDim.x) a.bdt[br * a.H + k] = a.dt[row * a.H + k];
-    copy_elems((char*)a.bB + br * GN * es, (const char*)a.B + row * GN * es, (int)GN, es, threadIdx.x, blockDim.x);
-    copy_elems((char*)a.bC + br * GN * es, (const char*)a.C + row * GN * es, (int)GN, es, threadIdx.x, blockDim.x);
-  }
+  copy_draft_rows(a, i, slot, a.Q - p, n2, 0);   // drafts Q-p .. into rows 0 .. n2-1
   __syncthreads();
   if (threadIdx.x == 0) a.pos[slot] = n2;
 }
