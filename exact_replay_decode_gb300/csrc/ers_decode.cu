@@ -513,11 +513,12 @@ __global__ void __launch_bounds__(kThreads, 2) k_decode_heads(LaunchArgs a) {
         ((T*)a.bC)[brow * GN + e] = ((const T*)a.C)[(size_t)i * GN + e];
       }
     }
-  } else if (hl == 0) {
-    const size_t dst = brow * GN + (size_t)g * N, src = (size_t)i * GN + (size_t)g * N;
-    for (int n = j; n < N; n += 32) {
-      ((T*)a.bB)[dst + n] = sB[p * N + n];
-      ((T*)a.bC)[dst + n] = ((const T*)a.C)[src + n];
+  } else if (hl == 0) {   // lane j's 4 values of the group's rows: B from shared memory, C from its registers
+    const size_t dst = brow * GN + (size_t)g * N + 4 * j;
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      ((T*)a.bB)[dst + e] = sB[p * N + 4 * j + e];
+      ((T*)a.bC)[dst + e] = from_f<T>(c[e]);   // exact: c holds io values
     }
   }
 }

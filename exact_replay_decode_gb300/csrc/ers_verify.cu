@@ -338,13 +338,16 @@ __global__ void __launch_bounds__(kThreads, 2) k_verify_heads(LaunchArgs a) {
     for (int d = j; d < P; d += 32) dx[d] = sx[(QM + k) * P + d];
   }
   if (j < Td) a.bdt[buf_row(a, slot, h0 + j) * a.H + h] = dt_d;
-  if (w == 0) {
-    for (int k = 0; k < Td; ++k) {
-      const size_t dst = buf_row(a, slot, h0 + k) * GN + (size_t)g * N;
-      const size_t src = ((size_t)i * Td + k) * GN + (size_t)g * N;
-      for (int n = j; n < N; n += 32) {
-        ((T*)a.bB)[dst + n] = sB[(QM + k) * N + n];
-        ((T*)a.bC)[dst + n] = ((const T*)a.C)[src + n];
+  if (w == 0) {   // lane j's 4 values of each draft's group rows: B from shared memory, C from registers
+#pragma unroll
+    for (int k = 0; k < kDraftsMax; ++k) {
+      if (k < Td) {
+        const size_t dst = buf_row(a, slot, h0 + k) * GN + (size_t)g * N + 4 * j;
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          ((T*)a.bB)[dst + e] = sB[(QM + k) * N + 4 * j + e];
+          ((T*)a.bC)[dst + e] = from_f<T>(c[k][e]);   // exact: c holds io values
+        }
       }
     }
   }
