@@ -78,7 +78,7 @@ typedef int32_t ers_status;
 #define ERS_DTYPE_BF16 1
 
 /* Flags */
-#define ERS_FLAG_FUSE_REFRESH 1u /* replay_decode (exact mode): refresh in the same launch when a chunk fills */
+#define ERS_FLAG_FUSE_REFRESH 1u /* replay_decode: refresh (exact mode) or flush (ReplaySSM) in the same call */
 #define ERS_FLAG_REPLAYSSM 2u    /* replay_decode / refresh: ReplaySSM mode (read copy, flush rule) */
 #define ERS_FLAG_AUTO_FLUSH 4u   /* spec_verify / commit: flush when h + T > L instead of failing */
 
@@ -264,6 +264,12 @@ ERS_API ers_status ers_chunked_prefill(const ers_dims* dims, const ers_params* p
  * pos advances by one per call (or returns to 0, or 1 after a ReplaySSM flush); while the call runs, the
  * upper 16 bits of a slot's pos entry may hold a count of the kernel's own, cleared before it ends,
  * so no other work may read or write pos concurrently with the call.
+ * Launches (all on `stream`): with ERS_FLAG_FUSE_REFRESH and at most 8 heads per group (chunk <= 32)
+ * the call is two launches, the slots whose step refreshes or flushes first and the others as its
+ * programmatic dependent, which completes after it.  ReplaySSM with bf16 io and a bf16 read copy
+ * (chunk <= 16, P = 64, N = 128, at most 8 heads per group) computes the read copy's products on the
+ * tensor core, in the kernel ers_spec_verify runs for the same cache, so the two keep each other's
+ * bits; FP8 and NVFP4 copies use the CUDA-core kernels for both calls.
  * Device errors: ERS_EALIGN (pos out of range), ERS_ESLOT. */
 ERS_API ers_status ers_replay_decode(const ers_dims* dims, const ers_params* prm, const ers_cache* cache, int32_t nseq,
                              const int32_t* slot, const void* x, const float* dt, const void* B, const void* C,
@@ -297,7 +303,11 @@ ERS_API ers_status ers_refresh(const ers_dims* dims, const ers_params* prm, cons
  * pos is NOT changed: ers_commit must follow before the next verify on the same slots.
  * With ERS_FLAG_AUTO_FLUSH a slot with h + T > L first refreshes its h committed records (as
  * ers_refresh in ReplaySSM mode); without it such a slot reports ERS_EOVERFLOW.
- * Requires 1 <= T <= L. */
+ * Requires 1 <= T <= L.  Supported read copies: bf16 for any T (bf16 io, L <= 16, P = 64, N = 128,
+ * at most 8 heads per group: the drafts' products on the tensor core, the kernel ReplaySSM decode of
+ * the same cache runs); FP8, NVFP4 and fp16 / shared anchors otherwise need T <= 4, L <= 16, P = 64,
+ * N = 128 and at most 8 heads per group (ERS_EUNSUPPORTED).  With ERS_FLAG_AUTO_FLUSH the call is two
+ * launches on `stream` (the flushing slots first, the others as its programmatic dependent). */
 ERS_API ers_status ers_spec_verify(const ers_dims* dims, const ers_params* prm, const ers_cache* cache, int32_t nseq,
                            const int32_t* slot, int32_t T, const void* x, const float* dt, const void* B,
                            const void* C, uint32_t flags, void* y, ers_stream_t stream, int32_t* dev_status);
