@@ -94,12 +94,26 @@ static_assert(offsetof(GdnSmem, k) % 16 == 0 && offsetof(GdnSmem, q) % 16 == 0 &
                   offsetof(GdnSmem, x) % 16 == 0 && offsetof(GdnSmem, bar) % 8 == 0,
               "16-byte rows, an 8-byte mbarrier");
 
-template <typename T>
-__device__ __forceinline__ void load_vec(const T* __restrict__ p, float* dst) {   // one 128-vector per warp
-  const int l = threadIdx.x & 31;
-  float f[4];
-  Quad<T>::unpack(*reinterpret_cast<const typename Quad<T>::raw*>(p + 4 * l), f);
-  *reinterpret_cast<float4*>(dst + 4 * l) = make_float4(f[0], f[1], f[2], f[3]);
+// Rows r = w, w + kGWarps, ... < n of warp w: 128-vectors src(r) -> dst(r), every load issued before
+// any store, so that a warp's rows cost one round trip rather than one each (kMax rows per warp).
+template <typename T, int kMax, typename Src, typename Dst>
+__device__ __forceinline__ void load_rows(int n, Src src, Dst dst) {
+  const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
+  typename Quad<T>::raw v[kMax];
+#pragma unroll
+  for (int q = 0; q < kMax; ++q) {
+    const int r = w + q * kGWarps;
+    if (r < n) v[q] = *reinterpret_cast<const typename Quad<T>::raw*>(src(r) + 4 * l);
+  }
+#pragma unroll
+  for (int q = 0; q < kMax; ++q) {
+    const int r = w + q * kGWarps;
+    if (r < n) {
+      float f[4];
+      Quad<T>::unpack(v[q], f);
+      *reinterpret_cast<float4*>(dst(r) + 4 * l) = make_float4(f[0], f[1], f[2], f[3]);
+    }
+  }
 }
 
 template <typename T>
@@ -298,21 +312,21 @@ __device__ __forceinline__ void gdn_fold_rows(GdnSmem& sm, float* __restrict__ S
 // Committed records' key rows (the group's; shared by its heads) and per-head rows.
 template <typename T>
 __device__ __forceinline__ void load_committed_k(GdnSmem& sm, const GdnArgs& a, int slot, int g, int hc) {
-  const int w = threadIdx.x >> 5;
-  for (int r = w; r < hc; r += kGWarps)
-    load_vec<T>((const T*)a.bk + (((size_t)slot * a.L + r) * a.G + g) * kGD, sm.k[r]);
+  load_rows<T, (kGL + kGWarps - 1) / kGWarps>(
+      hc, [&](int r) { return (const T*)a.bk + (((size_t)slot * a.L + r) * a.G + g) * kGD; },
+      [&](int r) { return sm.k[r]; });
 }
 
 template <typename T>
 __device__ __forceinline__ void load_committed_head(GdnSmem& sm, const GdnArgs& a, int slot, int h, int hc, bool flush) {
-  const int w = threadIdx.x >> 5;
-  for (int r = w; r < hc; r += kGWarps) {
-    const size_t row = (size_t)slot * a.L + r;
-    if (flush)
-      load_vec<T>((const T*)a.bv + (row * a.H + h) * kGD, sm.x.f.vc[r]);
-    else
-      load_vec<float>(a.bu + (row * a.H + h) * kGD, sm.u[r]);
-  }
+  constexpr int kMax = (kGL + kGWarps - 1) / kGWarps;
+  if (flush)
+    load_rows<T, kMax>(
+        hc, [&](int r) { return (const T*)a.bv + (((size_t)slot * a.L + r) * a.H + h) * kGD; },
+        [&](int r) { return sm.x.f.vc[r]; });
+  else
+    load_rows<float, kMax>(
+        hc, [&](int r) { return a.bu + (((size_t)slot * a.L + r) * a.H + h) * kGD; }, [&](int r) { return sm.u[r]; });
 }
 
 // Lane r of a warp gets v_0 + v_1 + ... + v_r (n <= 32 values, lane q holding v_q), added one at a
@@ -432,11 +446,11 @@ __global__ void __launch_bounds__(kThreads, TM == 4 ? 2 : 1) k_gdn_verify(GdnArg
     bulk_g2s(sm.x.cb, Rg + (size_t)(g * hpg) * kGD * kGD, kCopyBytes, &sm.bar);
   }
   load_committed_k<T>(sm, a, slot, g, hc);
-  for (int s = w; s < Td; s += kGWarps) {
-    const size_t tok = (size_t)i * Td + s;
-    load_vec<T>((const T*)a.k + (tok * a.G + g) * kGD, sm.k[kGL + s]);
-    load_vec<T>((const T*)a.q + (tok * a.G + g) * kGD, sm.q[s]);
-  }
+  // the drafts' k rows (r < Td) and q rows (r >= Td), one batch
+  load_rows<T, (2 * kGT + kGWarps - 1) / kGWarps>(
+      2 * Td,
+      [&](int r) { return (const T*)(r < Td ? a.k : a.q) + (((size_t)i * Td + (r < Td ? r : r - Td)) * a.G + g) * kGD; },
+      [&](int r) { return r < Td ? sm.k[kGL + r] : sm.q[r - Td]; });
   __syncthreads();
   if constexpr (kTc) {   // the drafts' operand tile: row n = k_n (n < 8) or q_{n-8}; zeros past the drafts
     const int n = tid >> 4, c = tid & 15, s = n & 7;
@@ -469,8 +483,8 @@ __global__ void __launch_bounds__(kThreads, TM == 4 ? 2 : 1) k_gdn_verify(GdnArg
     const int h = g * hpg + hh;
     const size_t soff = ((size_t)slot * a.H + h) * kGD * kGD;
     load_committed_head<T>(sm, a, slot, h, hc, flush);
-    for (int s = w; s < Td; s += kGWarps)
-      load_vec<T>((const T*)a.v + (((size_t)i * Td + s) * a.H + h) * kGD, sm.v[s]);
+    load_rows<T, (kGT + kGWarps - 1) / kGWarps>(
+        Td, [&](int s) { return (const T*)a.v + (((size_t)i * Td + s) * a.H + h) * kGD; }, [&](int s) { return sm.v[s]; });
     if (flush && hc > 0) flush_scalars(sm, a, slot, h, hc);
     if (w == 1) {   // output rows: committed rows 0..h0-1, then the drafts (h0 + Td <= 32); gates in row order
       const int r = j, n = h0 + Td;
