@@ -39,8 +39,6 @@ constexpr int heads_rows() { return QM + 1; }
 // The last region serves a step that fills or flushes the chunk as the per-warp w_s x_s[d] table and a
 // plain step with an NVFP4 copy as the heads' staged copy (P N / 2 code bytes + P N / 16 block-scale
 // bytes per warp), so it takes the larger of the two.
-template <int P, int N>
-constexpr size_t staged_bytes() { return (size_t)P * N / 2 + (size_t)P * N / 16; }
 template <int P, int N, int QM>
 constexpr size_t heads_table_bytes() {
   return (size_t)kHeadsPerCta * ((size_t)QM * P * sizeof(float) > staged_bytes<P, N>() ? (size_t)QM * P * sizeof(float)
@@ -59,15 +57,6 @@ constexpr size_t heads_smem_bytes() {
 // streams the rows from there.  (Staging the 8 KB FP8 copies measured slower: 83 against 72 us.)
 template <typename HT> constexpr bool kStaged = std::is_same<HT, Nvfp4>::value;
 
-template <typename HT, int N> struct RowSmem;
-template <int N> struct RowSmem<Nvfp4, N> {     // e2m1 codes (row d at c4 + d N / 2), block scales after them
-  const uint8_t* c4;
-  const uint8_t* bs;
-  __device__ __forceinline__ uint32_t ld(int d, int j) const {
-    const uint32_t c = *reinterpret_cast<const uint16_t*>(c4 + (size_t)d * (N / 2) + 2 * j);
-    return c | ((uint32_t)bs[(size_t)d * (N / 16) + (j >> 2)] << 16);
-  }
-};
 
 // Streams one head's state: lane j of row d reads elements [4j, 4j+4), 8 rows per block, with
 // rows_in_flight rows in flight (q holds the first of them on entry).  yo[d] ends with the

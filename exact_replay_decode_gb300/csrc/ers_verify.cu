@@ -37,15 +37,18 @@ constexpr size_t verify_smem_bytes() {
          + (size_t)kHeadsPerCta * QR * P * sizeof(T)                 // x rows, per warp
          + (size_t)kDraftsMax * QR * sizeof(float)                   // Gram rows, per draft
          + (size_t)kHeadsPerCta * kDraftsMax * P * sizeof(float)     // off-diagonal terms, per warp
-         + (size_t)kHeadsPerCta * QM * P * sizeof(float);            // flush w_s x_s[d], per warp
+         + (size_t)kHeadsPerCta *                                    // flush w_s x_s[d], or a plain
+               ((size_t)QM * P * sizeof(float) > staged_bytes<P, N>()     // step's staged NVFP4 copy, per warp
+                    ? (size_t)QM * P * sizeof(float)
+                    : staged_bytes<P, N>());
 }
 
 // Read-copy stream: yo[k * P + d] = Dot<128>(C of draft k, R[d]) for all rows d.  q holds rows
 // [0, kVerifyRowsInFlight) on entry.  FP8 and NVFP4 copies are read as codes: NVFP4 lane partials
 // are scaled by their block scale and each row's dot products by the row scale (lane d % 32 holds
 // it in sc[d / 32]), as in the decode stream.
-template <typename HT, int P, int N>
-__device__ __forceinline__ void stream_read_copy(const RowSrc<HT, N>& src,
+template <typename HT, int P, int N, typename Src>
+__device__ __forceinline__ void stream_read_copy(const Src& src,
                                                  typename RawOf<HT>::type (&q)[kVerifyRowsInFlight],
                                                  const float (&c)[kDraftsMax][4], float* yo, int j,
                                                  const float (&sc)[2]) {
@@ -207,10 +210,22 @@ __global__ void __launch_bounds__(kThreads, 2) k_verify_heads(LaunchArgs a) {
       for (int e = 0; e < 4; ++e) c[k][e] = 0.f;
     }
   }
+  // a plain step with an NVFP4 copy stages the head's copy in shared memory in one burst (3 bytes a
+  // row per lane, 8 rows in flight, kept too few bytes in flight) and streams it from there
+  constexpr bool kStaged = std::is_same<HT, Nvfp4>::value;
+  constexpr int kCodeBytes = P * N / 2;
+  uint8_t* stage = reinterpret_cast<uint8_t*>(swa) + (size_t)w * staged_bytes<P, N>();
   typename RawOf<HT>::type q[kVerifyRowsInFlight];
-  if (!flush && active) {
+  if (!kStaged && !flush && active) {
 #pragma unroll
     for (int r = 0; r < kVerifyRowsInFlight; ++r) q[r] = src.ld(r, j);
+  }
+  if constexpr (kStaged) {
+    if (!flush && active) {
+      const uint8_t* cg = (const uint8_t*)a.read_copy + soff / 2;
+      for (int k = j; k < kCodeBytes / 16; k += 32) cp_async16(stage + 16 * k, cg + 16 * k);
+      for (int k = j; k < P * N / 16 / 16; k += 32) cp_async16(stage + kCodeBytes + 16 * k, a.read_bscale + soff / 16 + 16 * k);
+    }
   }
   // committed rows 0..hc-1 at smem rows 0..hc-1, drafts at rows QM..QM+T-1
   const T* bB = (const T*)a.bB + (size_t)g * N;   // buffer row r at buf_row(a, slot, r)
@@ -235,7 +250,7 @@ __global__ void __launch_bounds__(kThreads, 2) k_verify_heads(LaunchArgs a) {
   const float dt_d = j < Td ? a.dt[((size_t)i * Td + j) * a.H + h] : 0.f;
   const float Ah = a.A[h], bias = a.dt_bias[h];
   float* yo = syo + w * kDraftsMax * P;
-  if (!flush && active) stream_read_copy<HT, P, N>(src, q, c, yo, j, sc);
+  if (!kStaged && !flush && active) stream_read_copy<HT, P, N>(src, q, c, yo, j, sc);
   // output rows s < h0 + T: committed rows then drafts
   const int nout = h0 + Td;
   const float dt_o_d = __shfl_sync(kFull, dt_d, max(j - h0, 0) & 31);
@@ -248,6 +263,14 @@ __global__ void __launch_bounds__(kThreads, 2) k_verify_heads(LaunchArgs a) {
   v = warp_scan_df(v, j);
   cp_async_wait_all();
   __syncthreads();
+  if constexpr (kStaged) {
+    if (!flush && active) {
+      const RowSmem<Nvfp4, N> ss{stage, stage + kCodeBytes};
+#pragma unroll
+      for (int r = 0; r < kVerifyRowsInFlight; ++r) q[r] = ss.ld(r, j);
+      stream_read_copy<HT, P, N>(ss, q, c, yo, j, sc);
+    }
+  }
   // Gram rows of the drafts: G[k][s] = C_{h0+k} . B_s for s <= h0 + k
   for (int k = 0; k < Td; ++k)
     for (int s = w; s <= h0 + k; s += kHeadsPerCta) {

@@ -488,6 +488,21 @@ __device__ __forceinline__ void row_values(typename RawOf<HT>::type r, float (&h
   }
 }
 
+// A head's NVFP4 copy staged in shared memory (P N / 2 code bytes, then P N / 16 block-scale bytes),
+// read row by row with the global reader's word layout (RowSrc<Nvfp4, N>::ld).
+template <int P, int N>
+constexpr size_t staged_bytes() { return (size_t)P * N / 2 + (size_t)P * N / 16; }
+
+template <typename HT, int N> struct RowSmem;
+template <int N> struct RowSmem<Nvfp4, N> {     // e2m1 codes (row d at c4 + d N / 2), block scales after them
+  const uint8_t* c4;
+  const uint8_t* bs;
+  __device__ __forceinline__ uint32_t ld(int d, int j) const {
+    const uint32_t c = *reinterpret_cast<const uint16_t*>(c4 + (size_t)d * (N / 2) + 2 * j);
+    return c | ((uint32_t)bs[(size_t)d * (N / 16) + (j >> 2)] << 16);
+  }
+};
+
 template <typename K>
 cudaError_t prep(K kernel, size_t smem) {
   return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
