@@ -42,57 +42,73 @@ constexpr int kGRows = kGD / kGWarps;          // state rows per warp
 constexpr int kGL = 32;                        // max window L
 constexpr int kGT = 8;                         // max drafts T
 constexpr int kYS = kGD + 8;                   // padded row of the y / z tables (8 banks apart)
-constexpr int kZ0 = kGT * kYS + 4;             // z table: 4 banks after y's
 
 // What only a flushing CTA uses; a CTA without a flush keeps a head's read copy in the same bytes.
-struct GdnFlush {
-  float vc[kGL][kGD];        // committed v (per head)
-  float cf[kGL][kGL];        // beta_r gamma_{i+1..r} (k_i . k_r), i < r (per head)
-  float yu[kGWarps][kGRows][kGL + 1];   // per warp and row, S k_i then the residual u_i (per head)
-  float kkf[kGL][kGL];       // k_i . k_r, committed rows (per group: past the read-copy tile's bytes)
+// LM is the largest window the layout holds.
+template <int LM>
+struct GdnFlushT {
+  static constexpr int kHead = LM * kGD + LM * LM + kGWarps * kGRows * (LM + 1);
+  static constexpr int kPad = kGD * kGD / 2 - kHead;   // floats up to the read copy's bytes
+  float vc[LM][kGD];         // committed v (per head)
+  float cf[LM][LM];          // beta_r gamma_{i+1..r} (k_i . k_r), i < r (per head)
+  float yu[kGWarps][kGRows][LM + 1];   // per warp and row, S k_i then the residual u_i (per head)
+  float pad[kPad > 0 ? kPad : 4];
+  float kkf[LM][LM];         // k_i . k_r, committed rows (per group: past the read-copy tile's bytes)
 };
 
-// Every row array starts on a 16-byte boundary (lane quads are read as 16-byte vectors).
-struct GdnSmem {
+// Every row array starts on a 16-byte boundary (lane quads are read as 16-byte vectors).  LM and TM
+// are the largest window and draft count the layout holds: 32 and 8 in general, 16 and 4 in a
+// layout small enough for three CTAs per SM.
+template <int LM, int TM>
+struct GdnSmemT {
+  static constexpr int kL = LM;
+  static constexpr int kZ0 = TM * kYS + 4;   // z table: 4 banks after y's
   union alignas(1024) {
-    GdnFlush f;
+    GdnFlushT<LM> f;
     // without a flush, or after a flush's fold: the head's read copy; fp32 io keeps it row-major
     // (one bulk copy), bf16 io in the 128-byte-swizzled K-major operand layout of the tensor core
     __nv_bfloat16 cb[kGD * kGD];
   } x;
   // bf16 io: the drafts' key rows (operand rows 0..7) and query rows (8..15), swizzled, K = dk
   alignas(1024) uint8_t bq[16 * kGD * 2];
-  alignas(16) float k[kGL + kGT][kGD];   // committed rows 0..hc-1, drafts at kGL + s
-  float q[kGT][kGD];
-  float v[kGT][kGD];         // drafts' v
-  float u[kGL + kGT][kGD];   // residuals: committed (cached), drafts at kGL + s
+  alignas(16) float k[LM + TM][kGD];   // committed rows 0..hc-1, drafts at LM + s
+  float q[TM][kGD];
+  float v[TM][kGD];          // drafts' v
+  float u[LM + TM][kGD];     // residuals: committed (cached), drafts at LM + s
   // S_read k_s (row s at s * kYS) and S_read q_s (row s at kZ0 + s * kYS): rows padded so that the
   // 32 lanes of a reduce-scatter (4 rows x 4 drafts x {k, q}) store to 32 different banks
-  float yz[kZ0 + kGT * kYS];
-  float gc[kGL + kGT];       // cumulative log-gates of the output rows
-  float bt[kGL + kGT];       // beta of the output rows
-  float gf[kGL];             // cumulative log-gates of the committed rows (flush)
-  float bf[kGL];
-  float kk[kGL + kGT][kGT];  // k_row . k_draft
-  float kq[kGL + kGT][kGT];  // k_row . q_draft
+  float yz[kZ0 + TM * kYS];
+  float gc[LM + TM];         // cumulative log-gates of the output rows
+  float bt[LM + TM];         // beta of the output rows
+  float gf[LM];              // cumulative log-gates of the committed rows (flush)
+  float bf[LM];
+  float kk[LM + TM][TM];     // k_row . k_draft
+  float kq[LM + TM][TM];     // k_row . q_draft
   // per-head coefficients, computed once per head (same expressions, so the same bits, as inline)
-  float gamf[kGL];           // flush: gamma_{1..r}
-  float wf[kGL];             // flush: gamma_{r+1..hc}
-  float cc[kGL + kGT][kGT];  // drafts: beta_t gamma_{r+1..t} (k_r . k_s), r < t = h0 + s
-  float wq[kGL + kGT][kGT];  // drafts: gamma_{r+1..t} (k_r . q_s), r <= t
-  float gam[kGT];            // drafts: gamma_{1..t}
-  float gd[kGT];             // drafts' own log-gates (for the buffer)
+  float gamf[LM];            // flush: gamma_{1..r}
+  float wf[LM];              // flush: gamma_{r+1..hc}
+  float cc[LM + TM][TM];     // drafts: beta_t gamma_{r+1..t} (k_r . k_s), r < t = h0 + s
+  float wq[LM + TM][TM];     // drafts: gamma_{r+1..t} (k_r . q_s), r <= t
+  float gam[TM];             // drafts: gamma_{1..t}
+  float gd[TM];              // drafts' own log-gates (for the buffer)
   uint64_t bar;
   uint64_t mbar;             // bf16 io: completion of the drafts' MMAs, one phase per head
-  uint32_t tmem;             // bf16 io: the CTA's tensor-memory columns (32)              // completion of the read-copy bulk copies, one phase per head
+  uint32_t tmem;             // bf16 io: the CTA's tensor-memory columns (32)
 };
-static_assert(sizeof(GdnFlush) >= kGD * kGD * 2, "the read copy fits the flush arrays' bytes");
-static_assert(offsetof(GdnFlush, kkf) >= kGD * kGD * 2, "reloading a head's copy keeps the group's key products");
-static_assert(sizeof(GdnSmem) + 1024 + 1024 <= 228 * 1024 / 2, "two CTAs per SM (1 KB reserved per CTA)");
-static_assert(offsetof(GdnSmem, k) % 16 == 0 && offsetof(GdnSmem, q) % 16 == 0 && offsetof(GdnSmem, u) % 16 == 0 &&
-                  offsetof(GdnSmem, v) % 16 == 0 &&
-                  offsetof(GdnSmem, x) % 16 == 0 && offsetof(GdnSmem, bar) % 8 == 0,
-              "16-byte rows, an 8-byte mbarrier");
+using GdnSmemWide = GdnSmemT<kGL, kGT>;   // any window and draft count (two CTAs per SM)
+using GdnSmemSmall = GdnSmemT<16, 4>;     // L <= 16, T <= 4 (three CTAs per SM)
+
+template <class SM, int kCtas>
+constexpr bool gdn_layout_ok() {
+  using F = decltype(SM::x.f);
+  return sizeof(F) >= kGD * kGD * 2 && offsetof(F, kkf) >= kGD * kGD * 2 && offsetof(F, kkf) % 16 == 0 &&
+         sizeof(SM) + 1024 + 1024 <= 228 * 1024 / kCtas && offsetof(SM, k) % 16 == 0 && offsetof(SM, q) % 16 == 0 &&
+         offsetof(SM, u) % 16 == 0 && offsetof(SM, v) % 16 == 0 && offsetof(SM, x) % 16 == 0 &&
+         offsetof(SM, bar) % 8 == 0;
+}
+// the read copy fits the flush arrays' bytes; reloading a head's copy keeps the group's key products;
+// the CTAs per SM fit (1 KB reserved per CTA); 16-byte rows, an 8-byte mbarrier
+static_assert(gdn_layout_ok<GdnSmemWide, 2>() && gdn_layout_ok<GdnSmemSmall, 3>(), "shared-memory layout");
 
 // Rows r = w, w + kGWarps, ... < n of warp w: 128-vectors src(r) -> dst(r), every load issued before
 // any store, so that a warp's rows cost one round trip rather than one each (kMax rows per warp).
@@ -157,21 +173,22 @@ __device__ __forceinline__ void issue_draft_mma(uint32_t tmem_d, uint32_t aT, ui
   }
 }
 
-__device__ __forceinline__ GdnSmem& gdn_smem(unsigned char* raw) {   // 1024-byte aligned (swizzled tiles)
-  return *reinterpret_cast<GdnSmem*>((reinterpret_cast<uintptr_t>(raw) + 1023) & ~uintptr_t(1023));
+template <class SM>
+__device__ __forceinline__ SM& gdn_smem(unsigned char* raw) {   // 1024-byte aligned (swizzled tiles)
+  return *reinterpret_cast<SM*>((reinterpret_cast<uintptr_t>(raw) + 1023) & ~uintptr_t(1023));
 }
 
 // S_src k_s and S_src q_s for the drafts (at most TM of them), RPG = 32 / (2 TM) rows per
 // reduce-scatter: lane l gets the sum of partial l = 2 TM * (row of the group) + (s for k, TM + s
 // for q); the pairings are Dot<128>'s, so each value has the bits of a Dot<128> reduction.
-template <int TM>
-__device__ __forceinline__ void draft_dots(GdnSmem& sm, const float (&rv)[32 / (2 * TM)][4], int d0, int Td, int j) {
+template <int TM, class SM>
+__device__ __forceinline__ void draft_dots(SM& sm, const float (&rv)[32 / (2 * TM)][4], int d0, int Td, int j) {
   constexpr int RPG = 32 / (2 * TM);
   float part[32];
 #pragma unroll
   for (int s = 0; s < TM; ++s) {
     float ka[4], qb[4];
-    lds4(sm.k[kGL + s] + 4 * j, ka);
+    lds4(sm.k[SM::kL + s] + 4 * j, ka);
     lds4(sm.q[s] + 4 * j, qb);
 #pragma unroll
     for (int g = 0; g < RPG; ++g) {
@@ -184,7 +201,7 @@ __device__ __forceinline__ void draft_dots(GdnSmem& sm, const float (&rv)[32 / (
   if (idx < TM) {
     if (idx < Td) sm.yz[idx * kYS + d] = v;
   } else if (idx - TM < Td) {
-    sm.yz[kZ0 + (idx - TM) * kYS + d] = v;
+    sm.yz[SM::kZ0 + (idx - TM) * kYS + d] = v;
   }
 }
 
@@ -197,15 +214,15 @@ __device__ __forceinline__ void draft_dots(GdnSmem& sm, const float (&rv)[32 / (
 //     read copy; with drafts, S' k_s and S' q_s from the cast values (draft_dots).
 // Passes A and C keep the next pair of anchor rows in flight.  Each S k_i is a Dot<128> reduction
 // whichever lane and row pairing carries it, so the bits do not depend on hc's branch.
-template <int TM>
-__device__ __forceinline__ void gdn_fold_rows(GdnSmem& sm, float* __restrict__ S, __nv_bfloat16* __restrict__ R,
+template <int TM, class SM>
+__device__ __forceinline__ void gdn_fold_rows(SM& sm, float* __restrict__ S, __nv_bfloat16* __restrict__ R,
                                               int hc, int ndraft, int w, int j) {
   constexpr int RPG = 32 / (2 * TM);
   static_assert(kGRows % 2 == 0 && RPG % 2 == 0 || RPG == 2, "row pairs fill the draft groups");
-  float (*YU)[kGL + 1] = sm.x.f.yu[w];   // [row of the warp][record]: S k_i, then u_i
+  float (*YU)[SM::kL + 1] = sm.x.f.yu[w];   // [row of the warp][record]: S k_i, then u_i
   const float* Sw = S + (size_t)(w * kGRows) * kGD + 4 * j;
   auto ldrow = [&](int rr) { return *reinterpret_cast<const float4*>(Sw + (size_t)rr * kGD); };
-  if (hc <= 16) {
+  if (SM::kL <= 16 || hc <= 16) {
     float4 c0 = ldrow(0), c1 = ldrow(1);
     for (int rr = 0; rr < kGRows; rr += 2) {
       float4 n0 = c0, n1 = c1;
@@ -228,7 +245,7 @@ __device__ __forceinline__ void gdn_fold_rows(GdnSmem& sm, float* __restrict__ S
       c0 = n0;
       c1 = n1;
     }
-  } else {
+  } else if constexpr (SM::kL > 16) {
     float4 c0 = ldrow(0);
     for (int rr = 0; rr < kGRows; ++rr) {
       const float4 n0 = rr + 1 < kGRows ? ldrow(rr + 1) : c0;
@@ -236,7 +253,7 @@ __device__ __forceinline__ void gdn_fold_rows(GdnSmem& sm, float* __restrict__ S
       Quad<float>::unpack(c0, hq);
       float part[32];
 #pragma unroll
-      for (int r = 0; r < kGL; ++r) {
+      for (int r = 0; r < SM::kL; ++r) {
         float kq4[4];
         lds4(sm.k[r] + 4 * j, kq4);
         part[r] = r < hc ? Dot<kGD>::partial(kq4, hq) : 0.f;
@@ -310,16 +327,16 @@ __device__ __forceinline__ void gdn_fold_rows(GdnSmem& sm, float* __restrict__ S
 }
 
 // Committed records' key rows (the group's; shared by its heads) and per-head rows.
-template <typename T>
-__device__ __forceinline__ void load_committed_k(GdnSmem& sm, const GdnArgs& a, int slot, int g, int hc) {
-  load_rows<T, (kGL + kGWarps - 1) / kGWarps>(
+template <typename T, class SM>
+__device__ __forceinline__ void load_committed_k(SM& sm, const GdnArgs& a, int slot, int g, int hc) {
+  load_rows<T, (SM::kL + kGWarps - 1) / kGWarps>(
       hc, [&](int r) { return (const T*)a.bk + (((size_t)slot * a.L + r) * a.G + g) * kGD; },
       [&](int r) { return sm.k[r]; });
 }
 
-template <typename T>
-__device__ __forceinline__ void load_committed_head(GdnSmem& sm, const GdnArgs& a, int slot, int h, int hc, bool flush) {
-  constexpr int kMax = (kGL + kGWarps - 1) / kGWarps;
+template <typename T, class SM>
+__device__ __forceinline__ void load_committed_head(SM& sm, const GdnArgs& a, int slot, int h, int hc, bool flush) {
+  constexpr int kMax = (SM::kL + kGWarps - 1) / kGWarps;
   if (flush)
     load_rows<T, kMax>(
         hc, [&](int r) { return (const T*)a.bv + (((size_t)slot * a.L + r) * a.H + h) * kGD; },
@@ -342,7 +359,8 @@ __device__ __forceinline__ float ordered_prefix(float v, int n, int r) {
 
 // Gates of the committed records summed in row order, and their betas (warp 0).
 // (Warp 0: the lanes load one row each, then lane 0 sums in row order.)
-__device__ __forceinline__ void flush_scalars(GdnSmem& sm, const GdnArgs& a, int slot, int h, int hc) {
+template <class SM>
+__device__ __forceinline__ void flush_scalars(SM& sm, const GdnArgs& a, int slot, int h, int hc) {
   if (threadIdx.x < 32) {
     const int r = threadIdx.x;
     float gr = 0.f;
@@ -356,7 +374,8 @@ __device__ __forceinline__ void flush_scalars(GdnSmem& sm, const GdnArgs& a, int
   }
 }
 
-__device__ __forceinline__ void flush_gram(GdnSmem& sm, int hc) {
+template <class SM>
+__device__ __forceinline__ void flush_gram(SM& sm, int hc) {
   const int w = threadIdx.x >> 5, j = threadIdx.x & 31;
   for (int p = w; p < hc * hc; p += kGWarps) {
     const int i = p / hc, r = p % hc;
@@ -368,7 +387,8 @@ __device__ __forceinline__ void flush_gram(GdnSmem& sm, int hc) {
 }
 
 // Per-head flush coefficients from gf, bf and kkf (all threads; call after both are in smem).
-__device__ __forceinline__ void flush_coeffs(GdnSmem& sm, int hc) {
+template <class SM>
+__device__ __forceinline__ void flush_coeffs(SM& sm, int hc) {
   for (int p = threadIdx.x; p < hc * hc; p += kThreads) {
     const int i = p / hc, r = p % hc;
     if (i < r)
@@ -381,7 +401,8 @@ __device__ __forceinline__ void flush_coeffs(GdnSmem& sm, int hc) {
 }
 
 // Per-head draft coefficients from gc, bt, kk and kq.
-__device__ __forceinline__ void draft_coeffs(GdnSmem& sm, int h0, int Td) {
+template <class SM>
+__device__ __forceinline__ void draft_coeffs(SM& sm, int h0, int Td) {
   for (int p = threadIdx.x; p < (h0 + Td) * Td; p += kThreads) {
     const int r = p / Td, s = p % Td, t = h0 + s;
     if (r <= t) {
@@ -406,14 +427,17 @@ __device__ __forceinline__ bool gdn_slot(const GdnArgs& a, int i, int* slot) {
 // One CTA per (sequence, key group); its value heads run one after another, so the group's key rows
 // are read once and the drafts' key rows are written after every head of the group has read the
 // committed ones (a flush reuses buffer rows from 0).
-// Two CTAs per SM (~113 KB of shared memory each) for up to 4 drafts; the 8-draft
-// variant needs more registers than two CTAs leave.
-template <typename T, int TM>
-__global__ void __launch_bounds__(kThreads, TM == 4 ? 2 : 1) k_gdn_verify(GdnArgs a) {
+// LM and TM bound the window and the drafts the shared-memory layout holds.  With L <= 16 and up to
+// 4 drafts the layout takes 69.6 KB and three CTAs fit on an SM (80 registers); other windows with up
+// to 4 drafts run two per SM (111.6 KB, 128 registers); the 8-draft variant needs more registers
+// than two CTAs leave.
+template <typename T, int TM, int LM>
+__global__ void __launch_bounds__(kThreads, TM == 8 ? 1 : (LM == 16 ? 3 : 2)) k_gdn_verify(GdnArgs a) {
+  using SM = GdnSmemT<LM, TM>;
   constexpr int RPG = 32 / (2 * TM);
   constexpr bool kTc = std::is_same<T, __nv_bfloat16>::value;   // bf16 io: drafts' dots on the tensor core
   extern __shared__ __align__(16) unsigned char gsm_raw[];
-  GdnSmem& sm = gdn_smem(gsm_raw);
+  SM& sm = gdn_smem<SM>(gsm_raw);
   const int g = blockIdx.x, i = blockIdx.y, tid = threadIdx.x, w = tid >> 5, j = tid & 31;
   const int hpg = a.H / a.G;
   const int Td = a.T;
@@ -447,16 +471,16 @@ __global__ void __launch_bounds__(kThreads, TM == 4 ? 2 : 1) k_gdn_verify(GdnArg
   }
   load_committed_k<T>(sm, a, slot, g, hc);
   // the drafts' k rows (r < Td) and q rows (r >= Td), one batch
-  load_rows<T, (2 * kGT + kGWarps - 1) / kGWarps>(
+  load_rows<T, (2 * TM + kGWarps - 1) / kGWarps>(
       2 * Td,
       [&](int r) { return (const T*)(r < Td ? a.k : a.q) + (((size_t)i * Td + (r < Td ? r : r - Td)) * a.G + g) * kGD; },
-      [&](int r) { return r < Td ? sm.k[kGL + r] : sm.q[r - Td]; });
+      [&](int r) { return r < Td ? sm.k[LM + r] : sm.q[r - Td]; });
   __syncthreads();
   if constexpr (kTc) {   // the drafts' operand tile: row n = k_n (n < 8) or q_{n-8}; zeros past the drafts
     const int n = tid >> 4, c = tid & 15, s = n & 7;
     uint32_t pk[4] = {0u, 0u, 0u, 0u};
     if (s < Td) {
-      const float* src = (n < 8 ? sm.k[kGL + s] : sm.q[s]) + 8 * c;
+      const float* src = (n < 8 ? sm.k[LM + s] : sm.q[s]) + 8 * c;
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
         const __nv_bfloat162 b2 = __floats2bfloat162_rn(src[2 * e], src[2 * e + 1]);   // bf16 values: exact
@@ -469,10 +493,10 @@ __global__ void __launch_bounds__(kThreads, TM == 4 ? 2 : 1) k_gdn_verify(GdnArg
   // k_row . k_s (rows before draft s) and k_row . q_s (rows up to draft s), row r of the output rows
   for (int p = w; p < (h0 + Td) * Td; p += kGWarps) {
     const int r = p / Td, s = p % Td;
-    const float* kr = r < h0 ? sm.k[r] : sm.k[kGL + r - h0];
+    const float* kr = r < h0 ? sm.k[r] : sm.k[LM + r - h0];
     if (r <= h0 + s) {
       const float vq = sdot(kr, sm.q[s], j);
-      const float vk = r < h0 + s ? sdot(kr, sm.k[kGL + s], j) : 0.f;
+      const float vk = r < h0 + s ? sdot(kr, sm.k[LM + s], j) : 0.f;
       if (j == 0) {
         sm.kq[r][s] = vq;
         sm.kk[r][s] = vk;
@@ -483,7 +507,7 @@ __global__ void __launch_bounds__(kThreads, TM == 4 ? 2 : 1) k_gdn_verify(GdnArg
     const int h = g * hpg + hh;
     const size_t soff = ((size_t)slot * a.H + h) * kGD * kGD;
     load_committed_head<T>(sm, a, slot, h, hc, flush);
-    load_rows<T, (kGT + kGWarps - 1) / kGWarps>(
+    load_rows<T, (TM + kGWarps - 1) / kGWarps>(
         Td, [&](int s) { return (const T*)a.v + (((size_t)i * Td + s) * a.H + h) * kGD; }, [&](int s) { return sm.v[s]; });
     if (flush && hc > 0) flush_scalars(sm, a, slot, h, hc);
     if (w == 1) {   // output rows: committed rows 0..h0-1, then the drafts (h0 + Td <= 32); gates in row order
@@ -522,7 +546,7 @@ __global__ void __launch_bounds__(kThreads, TM == 4 ? 2 : 1) k_gdn_verify(GdnArg
         for (int s = 0; s < 8; ++s) {
           if (s < Td) {
             sm.yz[s * kYS + tid] = dv[s];
-            sm.yz[kZ0 + s * kYS + tid] = dv[8 + s];
+            sm.yz[SM::kZ0 + s * kYS + tid] = dv[8 + s];
           }
         }
       }
@@ -568,25 +592,25 @@ __global__ void __launch_bounds__(kThreads, TM == 4 ? 2 : 1) k_gdn_verify(GdnArg
         float acc = __fmul_rn(sm.bt[t], __fmaf_rn(-sm.gam[s], sm.yz[s * kYS + d], sm.v[s][d]));
 #pragma unroll 4
         for (int r = 0; r < h0; ++r) acc = __fmaf_rn(-sm.cc[r][s], sm.u[r][d], acc);
-        for (int r = h0; r < t; ++r) acc = __fmaf_rn(-sm.cc[r][s], sm.u[kGL + r - h0][d], acc);
-        sm.u[kGL + s][d] = acc;
+        for (int r = h0; r < t; ++r) acc = __fmaf_rn(-sm.cc[r][s], sm.u[LM + r - h0][d], acc);
+        sm.u[LM + s][d] = acc;
       }
     }
     __syncthreads();
     // outputs, (row d, draft s) over all threads, each sum in row order
     for (int p = tid; p < Td * kGD; p += kThreads) {
       const int d = p % kGD, s = p / kGD, t = h0 + s;
-      float out = __fmul_rn(sm.gam[s], sm.yz[kZ0 + s * kYS + d]);
+      float out = __fmul_rn(sm.gam[s], sm.yz[SM::kZ0 + s * kYS + d]);
 #pragma unroll 4
       for (int r = 0; r < h0; ++r) out = __fmaf_rn(sm.wq[r][s], sm.u[r][d], out);
-      for (int r = h0; r <= t; ++r) out = __fmaf_rn(sm.wq[r][s], sm.u[kGL + r - h0][d], out);
+      for (int r = h0; r <= t; ++r) out = __fmaf_rn(sm.wq[r][s], sm.u[LM + r - h0][d], out);
       ((T*)a.o)[(((size_t)i * Td + s) * a.H + h) * kGD + d] = from_f<T>(out);
     }
     // this head's draft rows (v, residual, gate, beta) go to buffer rows h0..h0+T-1
     for (int s = w; s < Td; s += kGWarps) {
       const size_t row = (size_t)slot * a.L + h0 + s;
       store_vec<T>(sm.v[s], (T*)a.bv + (row * a.H + h) * kGD);
-      store_vec<float>(sm.u[kGL + s], a.bu + (row * a.H + h) * kGD);
+      store_vec<float>(sm.u[LM + s], a.bu + (row * a.H + h) * kGD);
       if (j == 0) {
         a.bg[row * a.H + h] = sm.gd[s];
         a.bbeta[row * a.H + h] = sm.bt[h0 + s];
@@ -597,7 +621,7 @@ __global__ void __launch_bounds__(kThreads, TM == 4 ? 2 : 1) k_gdn_verify(GdnArg
   // the group's draft key rows, after every head has read the committed ones
   for (int s = w; s < Td; s += kGWarps) {
     const size_t row = (size_t)slot * a.L + h0 + s;
-    store_vec<T>(sm.k[kGL + s], (T*)a.bk + (row * a.G + g) * kGD);
+    store_vec<T>(sm.k[LM + s], (T*)a.bk + (row * a.G + g) * kGD);
   }
   if constexpr (kTc) {   // every TMEM read finished before the last head's barriers: free the columns
     tc::after_sync();
@@ -610,7 +634,7 @@ __global__ void __launch_bounds__(kThreads, TM == 4 ? 2 : 1) k_gdn_verify(GdnArg
 template <typename T>
 __global__ void __launch_bounds__(kThreads, 2) k_gdn_refresh(GdnArgs a) {
   extern __shared__ __align__(16) unsigned char gsm_raw[];
-  GdnSmem& sm = gdn_smem(gsm_raw);
+  GdnSmemWide& sm = gdn_smem<GdnSmemWide>(gsm_raw);
   const int g = blockIdx.x, i = blockIdx.y, w = threadIdx.x >> 5, j = threadIdx.x & 31;
   const int hpg = a.H / a.G;
   int slot;
@@ -672,25 +696,35 @@ bool gdn_supported(int dk, int dv, int L, int T) {
 }
 
 cudaError_t gdn_launch(const GdnArgs& a, int kind, const int32_t* accepted, cudaStream_t s) {
-  const size_t sm = sizeof(GdnSmem) + 1024;   // + room to align the tiles to 1024 bytes
   cudaError_t e;
   if (kind == 2) {
     k_gdn_commit<<<(a.nseq + 255) / 256, 256, 0, s>>>(a, accepted);
     return cudaGetLastError();
   }
   const dim3 grid(a.G, a.nseq);
-  auto run = [&](auto kernel) {
+  // + room to align the tiles to 1024 bytes; the shared-memory carveout at its maximum, so that the
+  // small layout's three CTAs fit on an SM
+  auto run = [&](auto kernel, size_t sm) {
     cudaError_t err = prep(kernel, sm);
+    if (err == cudaSuccess)
+      err = cudaFuncSetAttribute(kernel, cudaFuncAttributePreferredSharedMemoryCarveout, cudaSharedmemCarveoutMaxShared);
     if (err != cudaSuccess) return err;
     kernel<<<grid, kThreads, sm, s>>>(a);
     return cudaGetLastError();
   };
+  const size_t wide = sizeof(GdnSmemWide) + 1024, narrow = sizeof(GdnSmemSmall) + 1024;
   const bool small = a.T <= 4;   // drafts' dot products 4 wide (4 rows per reduce-scatter), else 8
+  const bool short_window = small && a.L <= 16;   // the small layout, three CTAs per SM
   if (a.io == ERS_DTYPE_BF16) {
-    e = kind == 1 ? run(k_gdn_refresh<__nv_bfloat16>)
-                  : (small ? run(k_gdn_verify<__nv_bfloat16, 4>) : run(k_gdn_verify<__nv_bfloat16, 8>));
+    e = kind == 1        ? run(k_gdn_refresh<__nv_bfloat16>, wide)
+        : short_window ? run(k_gdn_verify<__nv_bfloat16, 4, 16>, narrow)
+        : small        ? run(k_gdn_verify<__nv_bfloat16, 4, kGL>, wide)
+                       : run(k_gdn_verify<__nv_bfloat16, 8, kGL>, wide);
   } else {
-    e = kind == 1 ? run(k_gdn_refresh<float>) : (small ? run(k_gdn_verify<float, 4>) : run(k_gdn_verify<float, 8>));
+    e = kind == 1        ? run(k_gdn_refresh<float>, wide)
+        : short_window ? run(k_gdn_verify<float, 4, 16>, narrow)
+        : small        ? run(k_gdn_verify<float, 4, kGL>, wide)
+                       : run(k_gdn_verify<float, 8, kGL>, wide);
   }
   if (e != cudaSuccess) return e;
   if (kind == 1) {
