@@ -674,9 +674,9 @@ def bench_rssm_decode(dev, cycles: int, hbm: float, read_dtype: str, anchor: str
     ach = total / nsteps / (ms * 1e-3) / 1e9
     return {"read_copy": read_dtype, "anchor": anchor, "seq_steps_per_s": S / (ms * 1e-3), "us_per_step": ms * 1e3,
             "achieved_gbs": ach, "hbm_frac": ach / hbm, "bytes_per_step": total / nsteps, "steps": nsteps,
-            # a bf16 copy: the tensor-core kernel as two launches (flushing slots, then the others);
-            # FP8 / NVFP4 copies: one warp-per-head launch
-            "launches_per_step": 2 if read_dtype == "bf16" else 1}
+            # two launches per fused call whatever the copy (the tensor-core kernel for bf16, the
+            # warp-per-head kernel otherwise): the flushing slots, then the others as its dependent
+            "launches_per_step": 2}
 
 
 def bench_conv(dev, hbm: float, reps: int = 50):
