@@ -356,6 +356,23 @@ def test_bf16_round_matches_synth_rounding():
     assert oracle.bf16_round(np.array([1.0 + 3 * 2.0 ** -8], np.float32))[0] == 1.0 + 2.0 ** -6
 
 
+def test_bf16_round_matches_a_library_cast_over_the_whole_range():
+    """The library's fp32 -> bf16 cast (PyTorch on the CPU, round-to-nearest-even) on magnitudes from
+    the subnormals to past the largest finite bf16, exact ties and both signs."""
+    torch = pytest.importorskip("torch")
+    rng = np.random.default_rng(15)
+    mant = rng.uniform(1.0, 2.0, 20000)
+    expo = rng.integers(-133, 128, 20000)
+    v = (mant * np.exp2(expo.astype(np.float64)) * rng.choice([-1.0, 1.0], 20000)).astype(np.float32)
+    ties = (np.arange(1, 257, dtype=np.float64) * 2.0 ** -7 + 2.0 ** -8).astype(np.float32)   # halfway cases
+    edge = np.array([0.0, -0.0, 3.3895314e38, 3.3961776e38, np.finfo(np.float32).max, 2.0 ** -133, 2.0 ** -126],
+                    np.float32)
+    for a in (v, ties, -ties, edge):
+        want = torch.from_numpy(a).to(torch.bfloat16).to(torch.float32).numpy()
+        got = oracle.bf16_round(a).astype(np.float32)
+        assert np.array_equal(got.view(np.uint32), want.view(np.uint32))
+
+
 def _e4m3_table():
     """Every finite e4m3 value, decoded from the bit fields by the format's definition."""
     vals = []
