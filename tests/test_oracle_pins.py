@@ -364,7 +364,8 @@ def test_bf16_round_matches_a_library_cast_over_the_whole_range():
     mant = rng.uniform(1.0, 2.0, 20000)
     expo = rng.integers(-133, 128, 20000)
     v = (mant * np.exp2(expo.astype(np.float64)) * rng.choice([-1.0, 1.0], 20000)).astype(np.float32)
-    ties = (np.arange(1, 257, dtype=np.float64) * 2.0 ** -7 + 2.0 ** -8).astype(np.float32)   # halfway cases
+    k = np.arange(128, dtype=np.float64)   # every halfway case of [1, 2) (spacing 2^-7) and [2, 4) (2^-6)
+    ties = np.concatenate([1.0 + k * 2.0 ** -7 + 2.0 ** -8, 2.0 + k * 2.0 ** -6 + 2.0 ** -7]).astype(np.float32)
     edge = np.array([0.0, -0.0, 3.3895314e38, 3.3961776e38, np.finfo(np.float32).max, 2.0 ** -133, 2.0 ** -126],
                     np.float32)
     for a in (v, ties, -ties, edge):
