@@ -116,6 +116,43 @@ def test_zero_sequences_is_a_noop(lib):
 
 
 @needs_no_gpu
+def test_empty_batches_are_noops_at_every_entry_point(lib):
+    """Zero sequences: every per-sequence call checks its descriptors, returns ERS_OK and launches
+    nothing (so the per-call pointers may be NULL); a negative count is ERS_EINVAL."""
+    from exact_replay_decode_gb300 import _abi
+    d, p = _dims(), _prm()
+    c = _abi.Cache()
+    c.state = c.read_copy = c.buf_x = c.buf_dt = c.buf_B = c.buf_C = c.pos = FAKE
+    c.nslots = 4
+    D, P, C = ctypes.byref(d), ctypes.byref(p), ctypes.byref(c)
+    for n, want in ((0, 0), (-1, 1)):
+        assert lib.ers_chunked_prefill(D, P, C, n, 0, 0, None, None, None, None, None, None, None, None, 0, None,
+                                       None) == want
+        for flags in (0, _abi.FLAG_FUSE_REFRESH, _abi.FLAG_REPLAYSSM | _abi.FLAG_FUSE_REFRESH):
+            assert lib.ers_replay_decode(D, P, C, n, None, None, None, None, None, flags, None, None, None) == want
+        assert lib.ers_refresh(D, P, C, n, None, _abi.FLAG_REPLAYSSM, 4, None, None) == want
+        assert lib.ers_spec_verify(D, P, C, n, None, 4, None, None, None, None, _abi.FLAG_AUTO_FLUSH, None, None,
+                                   None) == want
+        assert lib.ers_commit(D, C, n, None, None, 4, _abi.FLAG_AUTO_FLUSH, None, None) == want
+        assert lib.ers_spec_verify_exact(D, P, C, n, None, 4, None, None, None, None, None, None, 0, None,
+                                         None) == want
+        assert lib.ers_commit_exact(D, P, C, n, None, None, 4, None, None, None, None, None, 0, None, None) == want
+        gd = _abi.GdnDims(8, 4, 128, 128, 16, _abi.DTYPE_BF16)
+        gc = _abi.GdnCache(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 4)
+        GD, GC = ctypes.byref(gd), ctypes.byref(gc)
+        assert lib.ers_gdn_verify(GD, GC, n, None, 4, None, None, None, None, None, _abi.FLAG_AUTO_FLUSH, None, None,
+                                  None) == want
+        assert lib.ers_gdn_commit(GD, GC, n, None, None, 4, _abi.FLAG_AUTO_FLUSH, None, None) == want
+        assert lib.ers_gdn_refresh(GD, GC, n, None, 4, None, None) == want
+        cd = _abi.ConvDims(64, 4, _abi.DTYPE_BF16, 1)
+        assert lib.ers_conv1d_fwd(ctypes.byref(cd), n, 0, 0, None, None, None, None, None, 0, None, 0, None, None,
+                                  None) == want
+        assert lib.ers_conv1d_update(ctypes.byref(cd), n, None, None, None, None, 0, None, None, None, None) == want
+    assert lib.ers_ssd_scan_fwd(D, P, -1, 0, 0, None, None, None, None, None, None, None, None, None, None, 0, None,
+                                None) == 1
+
+
+@needs_no_gpu
 def test_validation_of_fp8_read_copies(lib):
     """FP8 / NVFP4 read copies: the dtype code is checked, the scales are required and aligned, and
     shapes the warp-per-head kernels do not cover (and NVFP4 outside ReplaySSM mode) return
