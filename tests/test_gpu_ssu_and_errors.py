@@ -98,6 +98,35 @@ def test_device_errors_are_reported_not_trapped():
     assert torch.isfinite(y.float()).all()
 
 
+def test_empty_batches_through_the_binding():
+    """Zero sequences through the Python binding: empty outputs of the right shape, no error, and no
+    cache byte changes (decode, verify, commit and refresh of a ReplaySSM cache; GDN verify and
+    commit; the conv1d update)."""
+    ers = _ers()
+    prm = _prm()
+    c = _cache()
+    c.pos.copy_(torch.tensor([3, 15, 0, 9], dtype=torch.int32, device=dev()))
+    snap = [t.clone() for t in (c.state, c.read_copy, c.pos, c.buf_x, c.buf_B)]
+    assert ers.replay_decode(c, prm, *_tok(0), replayssm=True).shape == (0, 8, 64)
+    assert ers.spec_verify(c, prm, *_tok(0, (4,))).shape == (0, 4, 8, 64)
+    ers.commit(c, torch.zeros(0, dtype=torch.int32, device=dev()), 4)
+    ers.refresh(c, prm, nseq=0, replayssm=True, drafts_T=4)
+    gc = ers.GdnCache(4, 8, 4, window=16)
+    q = torch.zeros(0, 4, 4, 128, dtype=torch.bfloat16, device=dev())
+    v = torch.zeros(0, 4, 8, 128, dtype=torch.bfloat16, device=dev())
+    gb = torch.zeros(0, 4, 8, dtype=torch.float32, device=dev())
+    assert ers.gdn_verify(gc, q, q, v, gb, gb).shape == (0, 4, 8, 128)
+    ers.gdn_commit(gc, torch.zeros(0, dtype=torch.int32, device=dev()), 4)
+    w = torch.randn(64, 4, device=dev()).to(torch.bfloat16)
+    cs = torch.randn(4, 3, 64, device=dev()).to(torch.bfloat16)
+    cs0 = cs.clone()
+    assert ers.conv1d_update(torch.zeros(0, 64, dtype=torch.bfloat16, device=dev()), w, None, cs).shape == (0, 64)
+    torch.cuda.synchronize()
+    for a, b in zip((c.state, c.read_copy, c.pos, c.buf_x, c.buf_B), snap):
+        assert same_bits(a, b)
+    assert same_bits(cs, cs0) and int(gc.pos.abs().sum()) == 0
+
+
 def test_host_validation_errors_launch_nothing():
     ers = _ers()
     prm = _prm()
