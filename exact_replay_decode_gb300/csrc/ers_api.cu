@@ -840,7 +840,7 @@ ers_status ers_ssd_scan_fwd_static(const ers_dims* dims, const ers_params* prm, 
                                    float* final_state, float* chunk_states, ers_stream_t stream,
                                    int32_t* dev_status) {
   void* scratch = nullptr;
-  ERS_TRY(static_scratch(&scratch));
+  if (nseq > 0) ERS_TRY(static_scratch(&scratch));   // an empty or invalid count needs no scratch
   return ers_ssd_scan_fwd(dims, prm, nseq, ntokens, max_seqlen, cu_seqlens, x, dt, B, C, init_state, y,
                           final_state, chunk_states, scratch, ERS_STATIC_SCRATCH_BYTES, stream, dev_status);
 }

@@ -39,6 +39,10 @@
  *    first error wins.  It may be NULL, in which case such errors are dropped
  *    (the affected sequence's outputs are left unwritten).  No kernel traps.
  *  - Within one call, distinct sequences must name distinct slots.
+ *  - An empty batch (nseq == 0) is valid everywhere: after the descriptor
+ *    checks (dims, params, cache) the call returns ERS_OK, launches nothing and
+ *    reads none of its per-call pointers, which may then be NULL.  A negative
+ *    nseq is ERS_EINVAL.
  */
 #ifndef ERS_H
 #define ERS_H

@@ -148,6 +148,8 @@ def test_empty_batches_are_noops_at_every_entry_point(lib):
         assert lib.ers_conv1d_fwd(ctypes.byref(cd), n, 0, 0, None, None, None, None, None, 0, None, 0, None, None,
                                   None) == want
         assert lib.ers_conv1d_update(ctypes.byref(cd), n, None, None, None, None, 0, None, None, None, None) == want
+        assert lib.ers_ssd_scan_fwd_static(D, P, n, 0, 0, None, None, None, None, None, None, None, None, None, None,
+                                           None) == want   # no scratch lookup for an empty batch
     assert lib.ers_ssd_scan_fwd(D, P, -1, 0, 0, None, None, None, None, None, None, None, None, None, None, 0, None,
                                 None) == 1
 
