@@ -210,8 +210,8 @@ __global__ void __launch_bounds__(kThreads, 2) k_verify_heads(LaunchArgs a) {
       for (int e = 0; e < 4; ++e) c[k][e] = 0.f;
     }
   }
-  // a plain step with an NVFP4 copy stages the head's copy in shared memory in one burst (3 bytes a
-  // row per lane, 8 rows in flight, kept too few bytes in flight) and streams it from there
+  // a plain step with an NVFP4 copy stages the head's copy in shared memory in one burst and streams
+  // the rows from there: read from global memory, 8 rows of 3 bytes per lane in flight are too few
   constexpr bool kStaged = std::is_same<HT, Nvfp4>::value;
   constexpr int kCodeBytes = P * N / 2;
   uint8_t* stage = reinterpret_cast<uint8_t*>(swa) + (size_t)w * staged_bytes<P, N>();
