@@ -111,17 +111,18 @@ def test_verify_equals_decode_and_commit_equals_decode(dims, T, bf16):
     assert np.array_equal(c_spec.pos.cpu().numpy(), (p0 + acc) % Q)
 
 
-def test_speculative_loop_matches_decode_and_oracle():
-    """32 steps of verify + commit at 4 drafts with accepted ~ U{0..4}: every accepted draft's
-    output equals non-speculative exact decode of the committed stream bit for bit, the caches end
-    identical, and outputs and checkpoints match the fp64 oracle per (sequence, head)."""
+def _spec_loop(S, K, seeds, sample=None):
+    """K steps of verify + commit at 4 drafts with accepted ~ U{0..4} on S sequences of the decode
+    workload: every accepted draft's output equals non-speculative exact decode of the committed
+    stream bit for bit, the caches end identical, and outputs and checkpoints of the sampled
+    sequences (all when sample is None) match the fp64 oracle per (sequence, head)."""
     ers = _ers()
     w = synth.workload("decode_b256_h64")
     d = w.dims
-    Q, T, K, S = d.chunk, 4, 32, 24
-    params, prm, hist, p0, stream, (c_spec, c_ref) = _caches(w, S, K * T, 63, 2)
+    Q, T = d.chunk, 4
+    params, prm, hist, p0, stream, (c_spec, c_ref) = _caches(w, S, K * T, seeds[0], 2)
     drafts = _drafts(stream, K, T, S)
-    acc_all = np.random.Generator(np.random.PCG64(64)).integers(0, T + 1, size=(K, S)).astype(np.int32)
+    acc_all = np.random.Generator(np.random.PCG64(seeds[1])).integers(0, T + 1, size=(K, S)).astype(np.int32)
     from exact_replay_decode_gb300 import _abi
     ws = torch.empty(_abi.lib().ers_spec_verify_exact_workspace_size(ctypes.byref(c_spec.dims), S),
                      dtype=torch.uint8, device=dev())
@@ -141,24 +142,37 @@ def test_speculative_loop_matches_decode_and_oracle():
                 ys[i].append(y[i, j])
     torch.cuda.synchronize()
     _same_cache(c_spec, _cache_state(c_ref), S, Q)
-    # the oracle over history + committed drafts, per (sequence, head)
+    assert np.array_equal(c_spec.pos.cpu().numpy(), np.array([(hist[i].ntokens + len(committed[i])) % Q
+                                                              for i in range(S)]))
+    # the oracle over history + committed drafts, per (sequence, head) of the sampled sequences
+    idx = list(range(S)) if sample is None else list(sample)
     parts = [synth.Tokens.concat([hist[i], synth.Tokens(stream.x[committed[i]], stream.dt[committed[i]],
                                                          stream.B[committed[i]], stream.C[committed[i]], True)])
-             for i in range(S)]
+             for i in idx]
     allt = synth.Tokens.concat(parts)
     cu = np.concatenate([[0], np.cumsum([p.ntokens for p in parts])]).astype(np.int64)
     y_o, _ = oracle.recurrence(allt.x, allt.dt, params.A, allt.B, allt.C, params.D, params.dt_bias, cu)
-    # per (sequence, head) over each sequence's committed drafts
-    got = torch.stack([yy for i in range(S) for yy in ys[i]])
-    ref = np.concatenate([y_o[cu[i] + hist[i].ntokens:cu[i + 1]] for i in range(S)])
-    cu_c = np.concatenate([[0], np.cumsum([len(ys[i]) for i in range(S)])])
+    got = torch.stack([yy for i in idx for yy in ys[i]])
+    ref = np.concatenate([y_o[cu[n] + hist[i].ntokens:cu[n + 1]] for n, i in enumerate(idx)])
+    cu_c = np.concatenate([[0], np.cumsum([len(ys[i]) for i in idx])])
     check_out(got, ref, 2e-3, keep=1, cu=cu_c, what="exact speculative outputs")
     nb = [(p.ntokens // Q) * Q for p in parts]
-    sel = np.concatenate([np.arange(cu[i], cu[i] + nb[i]) for i in range(S)]).astype(np.int64)
+    sel = np.concatenate([np.arange(cu[n], cu[n] + nb[n]) for n in range(len(idx))]).astype(np.int64)
     _, s_o = oracle.recurrence(allt.x[sel], allt.dt[sel], params.A, allt.B[sel], allt.C[sel], params.D,
                                params.dt_bias, np.concatenate([[0], np.cumsum(nb)]))
-    assert state_err(c_spec.state, s_o) <= STATE_TOL
-    assert np.array_equal(c_spec.pos.cpu().numpy(), np.array([p.ntokens % Q for p in parts]))
+    assert state_err(c_spec.state[torch.tensor(idx, device=dev())], s_o) <= STATE_TOL
+
+
+def test_speculative_loop_matches_decode_and_oracle():
+    """32 steps on 24 sequences, the oracle on every one."""
+    _spec_loop(24, 32, (63, 64))
+
+
+def test_speculative_loop_full_size_sampled():
+    """The bench's launch configuration (256 sequences x 4 drafts, 64 heads / 8 groups, headdim 64,
+    dstate 128, chunk 16) for 8 steps: every accepted draft bitwise against exact decode, the oracle
+    on sampled sequences."""
+    _spec_loop(256, 8, (65, 66), sample=[0, 101, 255])
 
 
 def test_commit_exact_rejects_bad_counts_and_positions():

@@ -100,3 +100,11 @@ def test_fused_flush_group_spread_over_several_ctas(read_dtype):
     fold the group's committed B rows while the flushing step stores the new token as buffer row 0.
     Fused and separate refreshes still agree bit for bit, and outputs match the protocol model."""
     _run(synth.Dims(32, 1, 64, 128, 16), read_dtype, 96, 40, 23, [0, 41, 95])
+
+
+@pytest.mark.parametrize("read_dtype", ["bf16", "fp8", "nvfp4"])
+def test_fused_flush_full_size_sampled(read_dtype):
+    """The bench's launch configuration (256 sequences, 64 heads / 8 groups, headdim 64, dstate 128,
+    L 16) for 20 steps, so that every slot passes a fused flush: fused and separate refreshes agree
+    bit for bit over every sequence, and sampled sequences match the protocol model."""
+    _run(synth.Dims(64, 8, 64, 128, 16), read_dtype, 256, 20, 24, [0, 128, 255])
