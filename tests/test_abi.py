@@ -331,3 +331,19 @@ def test_exact_speculation_validation(lib):
     cache.anchor_dtype = 1   # fp16 anchors: exact mode keeps an fp32 checkpoint
     assert lib.ers_spec_verify_exact(ctypes.byref(d), ctypes.byref(prm), ctypes.byref(cache), *args, p16, p16,
                                      1 << 30, None, None) == 12
+
+
+def test_missing_library_fails_loudly_and_the_package_has_no_fallback(monkeypatch):
+    """Without the built library the binding raises instead of computing anything; no module of the
+    package imports the oracle (the only CPU implementation of the method in the repository)."""
+    from exact_replay_decode_gb300 import _abi
+    monkeypatch.setattr(_abi, "LIB_PATH", os.path.join(ROOT, "_no_such_dir", "libers.so"))
+    monkeypatch.setattr(_abi, "_lib", None)
+    with pytest.raises(RuntimeError, match="is missing"):
+        _abi.lib()
+    pkg = os.path.join(ROOT, "exact_replay_decode_gb300")
+    for dirpath, _, files in os.walk(pkg):
+        for f in files:
+            if f.endswith(".py"):
+                src = open(os.path.join(dirpath, f)).read()
+                assert not re.search(r"^\s*(import|from)\s+oracle\b", src, flags=re.M), f
