@@ -1,5 +1,6 @@
 """The pins must reject a broken oracle: the Python-side definitions (gated delta rule, its protocol
-model, stochastic rounding onto the e2m1 grid, the fp16 stochastic rounding).
+model, stochastic rounding onto the e2m1 grid, the fp16 stochastic rounding, the bf16, e4m3 and e2m1
+roundings and the FP8 / NVFP4 row scales).
 
 Each case plants one plausible mistake in a scratch copy of oracle/__init__.py (never in the
 committed file), lays out a scratch tree with that copy, the committed synth package and the pin
@@ -40,6 +41,13 @@ MUTANTS = {
     "sr_e2m1_step_of_one_below_two": ("step = np.where(a < 2.0, 0.5, np.where(a < 4.0, 1.0, 2.0))",
                                       "step = np.where(a < 2.0, 1.0, np.where(a < 4.0, 1.0, 2.0))"),
     "sr_fp16_spacing_off_by_one": ("ue = np.maximum(e - 1, -14) - 10", "ue = np.maximum(e - 1, -14) - 11"),
+    "bf16_truncates": ('r = (((u + 0x7FFF + ((u >> 16) & 1)) >> 16) << 16).astype(np.uint32)', 'r = ((u >> 16) << 16).astype(np.uint32)'),
+    "bf16_ties_away_from_zero": ('r = (((u + 0x7FFF + ((u >> 16) & 1)) >> 16) << 16).astype(np.uint32)', 'r = (((u + 0x8000) >> 16) << 16).astype(np.uint32)'),
+    "e4m3_subnormal_quantum": ('ex = np.maximum(e - 1, -6)', 'ex = np.maximum(e - 1, -7)'),
+    "e4m3_no_saturation": ('r = np.minimum(r, E4M3_MAX)', 'r = np.minimum(r, 480.0)'),
+    "fp8_scale_boundary": ('k = e.astype(np.int64) - 9 + (m > 0.875)', 'k = e.astype(np.int64) - 9 + (m >= 0.875)'),
+    "e2m1_subnormal_quantum": ('ex = np.maximum(e - 1, 0)', 'ex = np.maximum(e - 1, -1)'),
+    "nvfp4_scale_boundary": ('k = e.astype(np.int64) - 12 + (m > 0.65625)', 'k = e.astype(np.int64) - 12 + (m >= 0.65625)'),
 }
 
 
