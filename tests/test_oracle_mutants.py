@@ -24,6 +24,14 @@ MUTANTS = {
     "output_before_update": ("        Sd[n] = decay * Sd[n] + v * Bt[n];\n        acc += Sd[n] * Ct[n];",
                              "        acc += Sd[n] * Ct[n];\n        Sd[n] = decay * Sd[n] + v * Bt[n];"),
     "missing_dt_bias": ("softplus64(j->dt[t * H + h] + j->dt_bias[h])", "softplus64(j->dt[t * H + h])"),
+    "initial_state_ignored": ("  double* S = j->state + ((int64_t)s * H + h) * (int64_t)P * N;\n",
+                              "  double* S = j->state + ((int64_t)s * H + h) * (int64_t)P * N;\n"
+                              "  memset(S, 0, sizeof(double) * (size_t)P * N);\n"),
+    "state_of_sequence_zero": ("double* S = j->state + ((int64_t)s * H + h) * (int64_t)P * N;",
+                               "double* S = j->state + ((int64_t)0 * H + h) * (int64_t)P * N;"),
+    "first_token_skipped": ("for (int64_t t = j->cu[s]; t < j->cu[s + 1]; ++t) {",
+                            "for (int64_t t = j->cu[s] + 1; t < j->cu[s + 1]; ++t) {"),
+    "skip_term_head_zero": ("yt[d] = acc + j->D[h] * xt[d];", "yt[d] = acc + j->D[0] * xt[d];"),
 }
 
 
