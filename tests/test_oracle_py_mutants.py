@@ -1,6 +1,6 @@
 """The pins must reject a broken oracle: the Python-side definitions (gated delta rule, its protocol
 model, stochastic rounding onto the e2m1 grid, the fp16 stochastic rounding, the bf16, e4m3 and e2m1
-roundings and the FP8 / NVFP4 row scales).
+roundings and the FP8 / NVFP4 row scales, the causal conv1d and SiLU).
 
 Each case plants one plausible mistake in a scratch copy of oracle/__init__.py (never in the
 committed file), lays out a scratch tree with that copy, the committed synth package and the pin
@@ -41,13 +41,26 @@ MUTANTS = {
     "sr_e2m1_step_of_one_below_two": ("step = np.where(a < 2.0, 0.5, np.where(a < 4.0, 1.0, 2.0))",
                                       "step = np.where(a < 2.0, 1.0, np.where(a < 4.0, 1.0, 2.0))"),
     "sr_fp16_spacing_off_by_one": ("ue = np.maximum(e - 1, -14) - 10", "ue = np.maximum(e - 1, -14) - 11"),
-    "bf16_truncates": ('r = (((u + 0x7FFF + ((u >> 16) & 1)) >> 16) << 16).astype(np.uint32)', 'r = ((u >> 16) << 16).astype(np.uint32)'),
-    "bf16_ties_away_from_zero": ('r = (((u + 0x7FFF + ((u >> 16) & 1)) >> 16) << 16).astype(np.uint32)', 'r = (((u + 0x8000) >> 16) << 16).astype(np.uint32)'),
-    "e4m3_subnormal_quantum": ('ex = np.maximum(e - 1, -6)', 'ex = np.maximum(e - 1, -7)'),
-    "e4m3_no_saturation": ('r = np.minimum(r, E4M3_MAX)', 'r = np.minimum(r, 480.0)'),
-    "fp8_scale_boundary": ('k = e.astype(np.int64) - 9 + (m > 0.875)', 'k = e.astype(np.int64) - 9 + (m >= 0.875)'),
-    "e2m1_subnormal_quantum": ('ex = np.maximum(e - 1, 0)', 'ex = np.maximum(e - 1, -1)'),
-    "nvfp4_scale_boundary": ('k = e.astype(np.int64) - 12 + (m > 0.65625)', 'k = e.astype(np.int64) - 12 + (m >= 0.65625)'),
+    "bf16_truncates": ("r = (((u + 0x7FFF + ((u >> 16) & 1)) >> 16) << 16).astype(np.uint32)",
+                       "r = ((u >> 16) << 16).astype(np.uint32)"),
+    "bf16_ties_away_from_zero": ("r = (((u + 0x7FFF + ((u >> 16) & 1)) >> 16) << 16).astype(np.uint32)",
+                                 "r = (((u + 0x8000) >> 16) << 16).astype(np.uint32)"),
+    "e4m3_subnormal_quantum": ("ex = np.maximum(e - 1, -6)", "ex = np.maximum(e - 1, -7)"),
+    "e4m3_no_saturation": ("r = np.minimum(r, E4M3_MAX)", "r = np.minimum(r, 480.0)"),
+    "fp8_scale_boundary": ("k = e.astype(np.int64) - 9 + (m > 0.875)", "k = e.astype(np.int64) - 9 + (m >= 0.875)"),
+    "e2m1_subnormal_quantum": ("ex = np.maximum(e - 1, 0)", "ex = np.maximum(e - 1, -1)"),
+    "nvfp4_scale_boundary": ("k = e.astype(np.int64) - 12 + (m > 0.65625)",
+                             "k = e.astype(np.int64) - 12 + (m >= 0.65625)"),
+    "conv_taps_reversed": ("acc = acc + w[:, k] * u[t + k]",
+                          "acc = acc + w[:, W - 1 - k] * u[t + k]"),
+    "conv_bias_dropped": ("            acc = b.copy()\n",
+                         "            acc = np.zeros_like(b)\n"),
+    "conv_state_not_prepended": ("pre = np.zeros((W - 1, C)) if init_state is None else _f64(init_state[i])",
+                                "pre = np.zeros((W - 1, C))"),
+    "conv_final_state_off_by_one": ("fin[i] = u[len(u) - (W - 1):]",
+                                   "fin[i] = u[len(u) - W:len(u) - 1]"),
+    "silu_sign": ("return a / (1.0 + np.exp(-a))",
+                 "return a / (1.0 + np.exp(a))"),
 }
 
 
