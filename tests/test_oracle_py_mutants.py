@@ -1,6 +1,6 @@
 """The pins must reject a broken oracle: the Python-side definitions (gated delta rule, its protocol
 model, stochastic rounding onto the e2m1 grid, the fp16 stochastic rounding, the bf16, e4m3 and e2m1
-roundings and the FP8 / NVFP4 row scales, the causal conv1d and SiLU).
+roundings and the FP8 / NVFP4 row scales, the causal conv1d and SiLU, the Philox generator and the counter layout of the random words).
 
 Each case plants one plausible mistake in a scratch copy of oracle/__init__.py (never in the
 committed file), lays out a scratch tree with that copy, the committed synth package and the pin
@@ -61,6 +61,14 @@ MUTANTS = {
                                    "fin[i] = u[len(u) - W:len(u) - 1]"),
     "silu_sign": ("return a / (1.0 + np.exp(-a))",
                  "return a / (1.0 + np.exp(a))"),
+    "philox_nine_rounds": ("    for rnd in range(10):\n        if rnd:\n            k0 = (k0 + np.uint64(PHILOX_W0)) & m32",
+                          "    for rnd in range(9):\n        if rnd:\n            k0 = (k0 + np.uint64(PHILOX_W0)) & m32"),
+    "philox_key_not_bumped": ("            k1 = (k1 + np.uint64(PHILOX_W1)) & m32\n",
+                             "            k1 = k1\n"),
+    "sr_words_nonce_and_slot_swapped": ("np.uint64(nonce & 0xFFFFFFFF), np.uint64(slot & 0xFFFFFFFF), hd, jj)",
+                                       "np.uint64(slot & 0xFFFFFFFF), np.uint64(nonce & 0xFFFFFFFF), hd, jj)"),
+    "sr_fp16_no_saturation": ("out = np.where(a >= FP16_MAX, FP16_MAX, out)",
+                             "out = out"),
 }
 
 
