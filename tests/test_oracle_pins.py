@@ -333,6 +333,26 @@ def test_protocol_committed_stream_matches_plain_recurrence():
         assert _relerr(m.anchor[i], fin[0]) < 1e-12
 
 
+def test_protocol_outputs_read_the_recast_copy():
+    """After a refresh the outputs read a copy recast from the refreshed anchor: with no committed
+    records left, the drafts' outputs are the recurrence over the drafts alone started from the bf16
+    cast of the new anchor (both pieces pinned on their own above)."""
+    params, anchor, drafts, acc, L = _protocol_case(14, steps=12)
+    m = oracle.ReplaySSMModel(params, anchor, L)
+    for k in range(len(drafts) - 1):
+        m.verify(drafts[k])
+        m.commit(acc[k])
+    assert m.flushes > 0
+    m.refresh(range(len(anchor)))
+    nxt = drafts[-1]
+    y = m.verify(nxt)
+    for i in range(len(anchor)):
+        x, dt, B, C = nxt[i]
+        want, _ = oracle.recurrence(x, dt, params.A, B, C, params.D, params.dt_bias,
+                                    init_state=oracle.bf16_round(m.anchor[i:i + 1]))
+        assert _relerr(y[i], want) < 1e-12
+
+
 def test_protocol_anchor_independent_of_read_precision():
     """Read-copy rounding never feeds the anchor (dual precision)."""
     params, anchor, drafts, acc, L = _protocol_case(13, steps=12)

@@ -1,6 +1,7 @@
 """The pins must reject a broken oracle: the Python-side definitions (gated delta rule, its protocol
 model, stochastic rounding onto the e2m1 grid, the fp16 stochastic rounding, the bf16, e4m3 and e2m1
-roundings and the FP8 / NVFP4 row scales, the causal conv1d and SiLU, the Philox generator and the counter layout of the random words).
+roundings and the FP8 / NVFP4 row scales, the causal conv1d and SiLU, the Philox generator and the counter layout of the random words, and the ReplaySSM protocol model's
+outputs, commit and recast).
 
 Each case plants one plausible mistake in a scratch copy of oracle/__init__.py (never in the
 committed file), lays out a scratch tree with that copy, the committed synth package and the pin
@@ -69,6 +70,15 @@ MUTANTS = {
                                        "np.uint64(slot & 0xFFFFFFFF), np.uint64(nonce & 0xFFFFFFFF), hd, jj)"),
     "sr_fp16_no_saturation": ("out = np.where(a >= FP16_MAX, FP16_MAX, out)",
                              "out = out"),
+    "replayssm_outputs_from_anchor": (
+        "y, _ = recurrence(x, dt, self.A, B, C, self.D, self.dt_bias, cu, self.read, self.nthreads)",
+        "y, _ = recurrence(x, dt, self.A, B, C, self.D, self.dt_bias, cu, self.anchor, self.nthreads)"),
+    "replayssm_commit_keeps_rejected": (
+        "            for j in range(int(a)):\n                self.committed[i].append(tuple(self._pending[i][k][j] for k in range(4)))",
+        "            for j in range(self._pending[i][0].shape[0]):\n                self.committed[i].append(tuple(self._pending[i][k][j] for k in range(4)))"),
+    "replayssm_refresh_keeps_stale_copy": (
+        "            self.read[i] = self.anchor[i] if self.shared else self.read_cast(fin[k])\n",
+        "            self.read[i] = self.anchor[i] if self.shared else self.read[i]\n"),
 }
 
 
