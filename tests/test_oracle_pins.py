@@ -890,3 +890,32 @@ def test_gdn_protocol_pins():
         if rest:
             _, got = oracle.gdn_recurrence(*(np.stack([r[f] for r in rest]) for f in range(5)), got)
         assert np.allclose(got, want, rtol=1e-12, atol=1e-12)
+
+
+def test_gdn_protocol_drafts_and_recast_copy():
+    """The drafts of one verify give the outputs of one-draft verifies with each committed in turn
+    (the same rows, the same outputs); and a flushing verify's outputs read the copy recast from the
+    folded anchor: the recurrence over the draft alone from the bf16 cast of the new anchor."""
+    d = synth.GdnDims(4, 2, 8, 6, 5)
+    rng = np.random.Generator(np.random.PCG64(65))
+    S, T = 3, 3
+    tok = lambda n: tuple(getattr(synth.make_gdn_tokens(rng, n, d, False), f) for f in ("q", "k", "v", "g", "beta"))
+    anchor = rng.standard_normal((S, d.nheads, d.dv, d.dk))
+    hist = [tok(2) for _ in range(S)]                       # two committed records per sequence
+    drafts = [tok(T) for _ in range(S)]
+    ma = oracle.GdnReplayModel(anchor, d.window)
+    mb = oracle.GdnReplayModel(anchor, d.window)
+    for m in (ma, mb):
+        m.verify(hist); m.commit([2] * S)
+    ya = ma.verify(drafts)
+    for s in range(T):
+        yb = mb.verify([tuple(f[s:s + 1] for f in dr) for dr in drafts]); mb.commit([1] * S)
+        assert np.allclose(yb[:, 0], ya[:, s], rtol=1e-12, atol=1e-12)
+    assert ma.flushes == 0 and mb.flushes == 0
+    # mb now holds 5 = L records: the next one-draft verify flushes first
+    nxt = [tok(1) for _ in range(S)]
+    y = mb.verify(nxt)
+    assert mb.flushes == S
+    for i in range(S):
+        want, _ = oracle.gdn_recurrence(*nxt[i], oracle.bf16_round(mb.anchor[i]))
+        assert np.allclose(y[i], want, rtol=1e-12, atol=1e-12)

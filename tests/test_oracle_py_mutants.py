@@ -79,6 +79,18 @@ MUTANTS = {
     "replayssm_refresh_keeps_stale_copy": (
         "            self.read[i] = self.anchor[i] if self.shared else self.read_cast(fin[k])\n",
         "            self.read[i] = self.anchor[i] if self.shared else self.read[i]\n"),
+    "gdn_outputs_from_anchor": (
+        "o, _ = gdn_recurrence(*seq, self.read[i])",
+        "o, _ = gdn_recurrence(*seq, self.anchor[i])"),
+    "gdn_refresh_keeps_stale_copy": (
+        "                self.read[i] = self.read_cast(fin)\n",
+        ""),
+    "gdn_commit_keeps_rejected": (
+        "            for j in range(int(a)):\n                self.committed[i].append(tuple(self._pending[i][f][j] for f in range(5)))",
+        "            for j in range(self._pending[i][0].shape[0]):\n                self.committed[i].append(tuple(self._pending[i][f][j] for f in range(5)))"),
+    "gdn_outputs_of_committed_rows": (
+        "outs.append(o[len(recs):])",
+        "outs.append(o[:o.shape[0] - len(recs)])"),
 }
 
 
