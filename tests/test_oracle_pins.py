@@ -333,6 +333,22 @@ def test_protocol_committed_stream_matches_plain_recurrence():
         assert _relerr(m.anchor[i], fin[0]) < 1e-12
 
 
+def test_protocol_drafts_equal_one_draft_verifies():
+    """With committed records in place, the drafts of one verify give the outputs of one-draft
+    verifies with each draft committed in turn (the same rows, the same outputs; no flush)."""
+    params, anchor, drafts, _, L = _protocol_case(15, steps=2)
+    S, T = len(anchor), drafts[0][0][0].shape[0]
+    ma = oracle.ReplaySSMModel(params, anchor, L)
+    mb = oracle.ReplaySSMModel(params, anchor, L)
+    for m in (ma, mb):
+        m.verify(drafts[0]); m.commit([3] * S)
+    ya = ma.verify(drafts[1])
+    for s in range(T):
+        yb = mb.verify([tuple(f[s:s + 1] for f in dr) for dr in drafts[1]]); mb.commit([1] * S)
+        assert _relerr(yb[:, 0], ya[:, s]) < 1e-12
+    assert ma.flushes == 0 and mb.flushes == 0
+
+
 def test_protocol_outputs_read_the_recast_copy():
     """After a refresh the outputs read a copy recast from the refreshed anchor: with no committed
     records left, the drafts' outputs are the recurrence over the drafts alone started from the bf16

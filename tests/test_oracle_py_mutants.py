@@ -91,6 +91,12 @@ MUTANTS = {
     "gdn_outputs_of_committed_rows": (
         "outs.append(o[len(recs):])",
         "outs.append(o[:o.shape[0] - len(recs)])"),
+    "replayssm_outputs_of_committed_rows": (
+        "            out[i] = y[cu[i + 1] - T:cu[i + 1]]",
+        "            out[i] = y[cu[i]:cu[i] + T]"),
+    "replayssm_flush_on_h_plus_T_only_when_full": (
+        "flush = [i for i in range(S) if len(self.committed[i]) + T > self.L]",
+        "flush = [i for i in range(S) if len(self.committed[i]) >= self.L]"),
 }
 
 
