@@ -727,6 +727,27 @@ def test_nvfp4_sr_cast_keeps_the_scales_and_brackets_each_value():
     assert np.array_equal(got, oracle.nvfp4_rows_round(st, words=oracle.sr_words((3, 4), 11, 6, 2, 4, 32)))
 
 
+def test_protocol_refresh_stores_the_rounded_anchor():
+    """A model whose stored anchor is a rounding of the refreshed state (fp16 stochastic rounding,
+    the shared NVFP4 state) stores rounding(refreshed state): with a rounding onto the grid of
+    quarters, a refresh leaves the quarter rounding of the recurrence over the committed records from
+    the previous stored anchor, every value a multiple of 1/4."""
+    params, anchor, drafts, acc, L = _protocol_case(16, steps=6)
+    q4 = lambda i, fin: np.round(np.asarray(fin, dtype=np.float64) * 4.0) / 4.0
+    m = oracle.ReplaySSMModel(params, anchor, L, anchor_round=q4)
+    for k in range(len(drafts)):
+        m.verify(drafts[k]); m.commit(acc[k])
+    which = [i for i in range(len(anchor)) if m.committed[i]]
+    assert which
+    before = {i: (m.anchor[i].copy(), [np.stack([r[f] for r in m.committed[i]]) for f in range(4)]) for i in which}
+    m.refresh(which)
+    for i in which:
+        prev, (x, dt, B, C) = before[i]
+        _, fin = oracle.recurrence(x, dt, params.A, B, C, params.D, params.dt_bias, init_state=prev[None])
+        assert np.array_equal(m.anchor[i], q4(i, fin[0]))
+        assert np.array_equal(m.anchor[i] * 4.0, np.round(m.anchor[i] * 4.0))
+
+
 def test_protocol_shared_state_model():
     """A shared state: the read copy is the stored anchor itself after every refresh; an empty history
     (zero acceptance) never changes it; with an exact (identity) rounding the model is the fp32-anchor

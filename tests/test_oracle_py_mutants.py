@@ -97,6 +97,21 @@ MUTANTS = {
     "replayssm_flush_on_h_plus_T_only_when_full": (
         "flush = [i for i in range(S) if len(self.committed[i]) + T > self.L]",
         "flush = [i for i in range(S) if len(self.committed[i]) >= self.L]"),
+    "nvfp4_block_scale_over_four": (
+        "beta = e4m3_round(t / np.float32(6.0))",
+        "beta = e4m3_round(t / np.float32(4.0))"),
+    "nvfp4_block_of_eight": (
+        "fb = (f / s).reshape(f.shape[:-1] + (N // NVFP4_BLOCK, NVFP4_BLOCK))",
+        "fb = (f / s).reshape(f.shape[:-1] + (N // 8, 8))"),
+    "nvfp4_row_scale_not_applied": (
+        "val = (q.astype(np.float64) * beta.astype(np.float64)).reshape(f.shape) * s",
+        "val = (q.astype(np.float64) * beta.astype(np.float64)).reshape(f.shape)"),
+    "replayssm_anchor_round_ignored": (
+        "            self.anchor[i] = fin[k] if self.anchor_round is None else self.anchor_round(i, fin[k])\n",
+        "            self.anchor[i] = fin[k]\n"),
+    "replayssm_shared_copy_recast": (
+        "            self.read[i] = self.anchor[i] if self.shared else self.read_cast(fin[k])\n",
+        "            self.read[i] = self.read_cast(fin[k])\n"),
 }
 
 
