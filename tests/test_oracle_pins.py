@@ -657,6 +657,19 @@ def test_sr_words_counter_layout():
     assert not np.array_equal(oracle.sr_words((7, 9), 4, 5, 2, 4, 8), w)   # a new nonce, new words
 
 
+def test_sr_anchor_writes_take_their_own_slots_words():
+    """A slot's stochastically rounded write (fp16 anchor or shared NVFP4 state) uses the words of its
+    own counter: the same state written for two slots, or under two nonces, rounds differently,
+    and the same (nonce, slot) reproduces its bits."""
+    rng = np.random.Generator(np.random.PCG64(31))
+    fin = rng.standard_normal((2, 4, 16)) * 3.0
+    for write in (oracle.sr_fp16_anchor, oracle.nvfp4_sr_state):
+        a = write(fin, (7, 9), 3, 5)
+        assert np.array_equal(a, write(fin, (7, 9), 3, 5))
+        assert not np.array_equal(a, write(fin, (7, 9), 3, 6))       # another slot
+        assert not np.array_equal(a, write(fin, (7, 9), 4, 5))       # another nonce
+
+
 def test_sr_fp16_is_unbiased():
     # averaged over an even grid of r, the rounded value equals the input to within the grid step
     v = np.float32(1 + 0.3 * 2.0 ** -10)

@@ -112,6 +112,22 @@ MUTANTS = {
     "replayssm_shared_copy_recast": (
         "            self.read[i] = self.anchor[i] if self.shared else self.read_cast(fin[k])\n",
         "            self.read[i] = self.read_cast(fin[k])\n"),
+    "sr_e2m1_sign_dropped": (
+        "    return np.copysign(out, f).astype(np.float32)\n",
+        "    return out.astype(np.float32)\n"),
+    "sr_e2m1_no_saturation": (
+        "out = np.where(a >= E2M1_MAX, E2M1_MAX, lo + up * step)",
+        "out = lo + up * step"),
+    "sr_fp16_sign_dropped": (
+        "    return np.copysign(out, f)\n",
+        "    return out\n"),
+    "fp8_rows_scale_not_applied": (
+        "    q = e4m3_round(f / s).astype(np.float64)\n    return q * s\n",
+        "    q = e4m3_round(f / s).astype(np.float64)\n    return q\n"),
+    "sr_fp16_words_from_other_slot": (
+        "return sr_fp16(np.asarray(fin, dtype=np.float64).astype(np.float32), sr_words(key, nonce, slot, H, P, N))",
+        "return sr_fp16(np.asarray(fin, dtype=np.float64).astype(np.float32), sr_words(key, nonce, 0, H, P, N))"),
+    "nvfp4_sr_words_from_other_slot": ("words=sr_words(key, nonce, slot, H, P, N))", "words=sr_words(key, nonce, 0, H, P, N))"),
 }
 
 
