@@ -128,6 +128,9 @@ MUTANTS = {
         "return sr_fp16(np.asarray(fin, dtype=np.float64).astype(np.float32), sr_words(key, nonce, slot, H, P, N))",
         "return sr_fp16(np.asarray(fin, dtype=np.float64).astype(np.float32), sr_words(key, nonce, 0, H, P, N))"),
     "nvfp4_sr_words_from_other_slot": ("words=sr_words(key, nonce, slot, H, P, N))", "words=sr_words(key, nonce, 0, H, P, N))"),
+    "conv_window_crosses_sequences": (
+        "pre = np.zeros((W - 1, C)) if init_state is None else _f64(init_state[i])",
+        "pre = (np.zeros((W - 1, C)) if cu[i] < W - 1 else x[cu[i] - (W - 1):cu[i]]) if init_state is None else _f64(init_state[i])"),
 }
 
 
