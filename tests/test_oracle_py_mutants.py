@@ -12,6 +12,7 @@ import os
 import shutil
 import subprocess
 import sys
+from concurrent.futures import ThreadPoolExecutor
 
 import pytest
 
@@ -140,27 +141,43 @@ def _oracle_lib():
     return oracle._LIB_OVERRIDE or oracle._LIB_PATH
 
 
-@pytest.mark.parametrize("name", sorted(MUTANTS))
-def test_pins_reject_python_mutant(name, tmp_path):
+def _run_mutant(name, root):
+    """Runs the pin suite against the oracle with mutant `name` planted, in a scratch tree under root;
+    returns (exit code, output)."""
     before, after = MUTANTS[name]
     src = open(SRC).read()
-    assert src.count(before) == 1, "mutation site no longer present (once) in oracle/__init__.py"
-    lib = _oracle_lib()
-    assert os.path.exists(lib), "the C oracle is built on import"
-    (tmp_path / "oracle").mkdir()
-    (tmp_path / "oracle" / "__init__.py").write_text(src.replace(before, after))
-    shutil.copy(os.path.join(ROOT, "oracle", "oracle.c"), tmp_path / "oracle" / "oracle.c")
-    shutil.copytree(os.path.join(ROOT, "synth"), tmp_path / "synth",
-                    ignore=shutil.ignore_patterns("__pycache__"))
-    (tmp_path / "tests").mkdir()
+    if src.count(before) != 1:
+        return None, "mutation site no longer present (once) in oracle/__init__.py"
+    (root / "oracle").mkdir()
+    (root / "oracle" / "__init__.py").write_text(src.replace(before, after))
+    shutil.copy(os.path.join(ROOT, "oracle", "oracle.c"), root / "oracle" / "oracle.c")
+    shutil.copytree(os.path.join(ROOT, "synth"), root / "synth", ignore=shutil.ignore_patterns("__pycache__"))
+    (root / "tests").mkdir()
     for f in ("conftest.py", "test_oracle_pins.py"):
-        shutil.copy(os.path.join(ROOT, "tests", f), tmp_path / "tests" / f)
+        shutil.copy(os.path.join(ROOT, "tests", f), root / "tests" / f)
     golden = os.path.join(ROOT, "tests", "golden")
     if os.path.isdir(golden):
-        shutil.copytree(golden, tmp_path / "tests" / "golden")
-    env = dict(os.environ, ERS_ORACLE_LIB=lib)
+        shutil.copytree(golden, root / "tests" / "golden")
+    env = dict(os.environ, ERS_ORACLE_LIB=_oracle_lib())
     r = subprocess.run([sys.executable, "-m", "pytest", "-q", "-x", "-p", "no:cacheprovider",
-                        str(tmp_path / "tests" / "test_oracle_pins.py")],
-                       cwd=str(tmp_path), env=env, capture_output=True, text=True, timeout=300)
-    assert "passed" in r.stdout or "failed" in r.stdout, r.stdout[-2000:] + r.stderr[-2000:]
-    assert r.returncode != 0, f"mutant {name} passed every pin:\n{r.stdout[-2000:]}"
+                        str(root / "tests" / "test_oracle_pins.py")],
+                       cwd=str(root), env=env, capture_output=True, text=True, timeout=600)
+    return r.returncode, r.stdout[-2000:] + r.stderr[-2000:]
+
+
+@pytest.fixture(scope="module")
+def mutant_runs(tmp_path_factory):
+    """Every mutant's pin run, run side by side (each is a separate process on a scratch tree)."""
+    assert os.path.exists(_oracle_lib()), "the C oracle is built on import"
+    names = sorted(MUTANTS)
+    with ThreadPoolExecutor(max_workers=max(1, min(16, os.cpu_count() or 1))) as ex:
+        runs = ex.map(lambda n: _run_mutant(n, tmp_path_factory.mktemp(n)), names)
+        return dict(zip(names, runs))
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_pins_reject_python_mutant(name, mutant_runs):
+    code, out = mutant_runs[name]
+    assert code is not None, out
+    assert "passed" in out or "failed" in out, out
+    assert code != 0, f"mutant {name} passed every pin:\n{out}"
