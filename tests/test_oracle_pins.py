@@ -859,6 +859,20 @@ def _gdn_case(seed, T=7, d=None, bf16=False):
     return d, toks, S0
 
 
+def test_golden_gdn_scalar_two_token():
+    with open(os.path.join(HERE, "golden", "gdn_scalar_two_token.json")) as f:
+        g = json.load(f)
+    env = {"log": math.log, "exp": math.exp}
+    inp = g["inputs"]
+    T = len(inp["v"])
+    col = lambda v: np.full((T, 1, 1), v, dtype=np.float64)
+    o, S = oracle.gdn_recurrence(col(inp["q"]), col(inp["k"]), np.array(inp["v"]).reshape(T, 1, 1),
+                                 np.full((T, 1), eval(inp["g"], env)), np.full((T, 1), inp["beta"]),
+                                 np.full((1, 1, 1), inp["init_state"]))
+    assert o[:, 0, 0] == pytest.approx([eval(e, env) for e in g["expected_o"]], rel=1e-14)
+    assert S[0, 0, 0] == pytest.approx(eval(g["expected_final_state"], env), rel=1e-14)
+
+
 def test_gdn_beta_zero_is_pure_decay():
     d, t, S0 = _gdn_case(61)
     o, S = oracle.gdn_recurrence(t.q, t.k, t.v, t.g, np.zeros_like(t.beta), S0)
