@@ -132,6 +132,18 @@ MUTANTS = {
     "conv_window_crosses_sequences": (
         "pre = np.zeros((W - 1, C)) if init_state is None else _f64(init_state[i])",
         "pre = (np.zeros((W - 1, C)) if cu[i] < W - 1 else x[cu[i] - (W - 1):cu[i]]) if init_state is None else _f64(init_state[i])"),
+    "e4m3_sign_dropped": (
+        "    return (np.sign(f) * r).astype(np.float32)\n\n\ndef fp8_row_scale_exponent",
+        "    return r.astype(np.float32)\n\n\ndef fp8_row_scale_exponent"),
+    "e2m1_sign_dropped": (
+        "    return (np.sign(f) * r).astype(np.float32)\n\n\nNVFP4_BLOCK",
+        "    return r.astype(np.float32)\n\n\nNVFP4_BLOCK"),
+    "fp8_tiny_rows_not_floored": (
+        "    return np.where(tiny, -127, np.maximum(k, -127))",
+        "    return np.maximum(k, -127)"),
+    "replayssm_verify_skips_flush": (
+        "        flush = [i for i in range(S) if len(self.committed[i]) + T > self.L]\n        self.refresh(flush)\n",
+        "        flush = [i for i in range(S) if len(self.committed[i]) + T > self.L]\n"),
 }
 
 
