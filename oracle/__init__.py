@@ -16,6 +16,12 @@ commit) only decide WHICH tokens the recurrence runs over and from WHICH
 starting state, following the exact-replay RFC (vLLM issue 55524, section 3
 "Proposal") and the ReplaySSM reproduction notes ("Motivation and method",
 "Core equations").
+
+Every function is pinned to something other than itself in tests/test_oracle_pins.py: hand-worked
+fixtures (tests/golden), closed forms, library routines (scipy's IIR filter, numpy's convolution,
+PyTorch's bf16 cast), brute force over every code of a format, published known-answer vectors and
+protocol invariants; tests/test_oracle_mutants.py and tests/test_oracle_py_mutants.py plant
+plausible mistakes here and in oracle.c, each of which must fail a pin.
 """
 from __future__ import annotations
 
