@@ -148,14 +148,16 @@ MUTANTS = {
 
 
 def _oracle_lib():
-    sys.path.insert(0, ROOT)
+    """The committed C oracle, built if it is missing or stale."""
+    if ROOT not in sys.path:
+        sys.path.insert(0, ROOT)
     import oracle
-    return oracle._LIB_OVERRIDE or oracle._LIB_PATH
+    return oracle._LIB_OVERRIDE or oracle.build()
 
 
-def _run_mutant(name, root):
-    """Runs the pin suite against the oracle with mutant `name` planted, in a scratch tree under root;
-    returns (exit code, output)."""
+def _run_mutant(name, root, lib):
+    """Runs the pin suite against the oracle with mutant `name` planted, in a scratch tree under root
+    (lib: the built C oracle); returns (exit code, output)."""
     before, after = MUTANTS[name]
     src = open(SRC).read()
     if src.count(before) != 1:
@@ -170,7 +172,7 @@ def _run_mutant(name, root):
     golden = os.path.join(ROOT, "tests", "golden")
     if os.path.isdir(golden):
         shutil.copytree(golden, root / "tests" / "golden")
-    env = dict(os.environ, ERS_ORACLE_LIB=_oracle_lib())
+    env = dict(os.environ, ERS_ORACLE_LIB=lib)
     r = subprocess.run([sys.executable, "-m", "pytest", "-q", "-x", "-p", "no:cacheprovider",
                         str(root / "tests" / "test_oracle_pins.py")],
                        cwd=str(root), env=env, capture_output=True, text=True, timeout=600)
@@ -180,10 +182,12 @@ def _run_mutant(name, root):
 @pytest.fixture(scope="module")
 def mutant_runs(tmp_path_factory):
     """Every mutant's pin run, run side by side (each is a separate process on a scratch tree)."""
-    assert os.path.exists(_oracle_lib()), "the C oracle is built on import"
+    lib = _oracle_lib()
+    assert os.path.exists(lib), "the C oracle is built on import"
     names = sorted(MUTANTS)
+    roots = {n: tmp_path_factory.mktemp(n) for n in names}   # made here: the threads only run processes
     with ThreadPoolExecutor(max_workers=max(1, min(16, os.cpu_count() or 1))) as ex:
-        runs = ex.map(lambda n: _run_mutant(n, tmp_path_factory.mktemp(n)), names)
+        runs = ex.map(lambda n: _run_mutant(n, roots[n], lib), names)
         return dict(zip(names, runs))
 
 
